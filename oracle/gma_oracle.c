@@ -1,0 +1,298 @@
+/*
+ * fp64 CPU oracle for Gaussian Mixture Attention (GMA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  The CUDA library
+ * shares no code, header, table or helper with it.
+ *
+ * It states the method in its plain form, in double precision, one token at
+ * a time, with no blocking, chunking or reordering.  Source: the GMA explainer
+ * page "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing", technical summary, sections
+ * "핵심 메커니즘" (core mechanism) and "변형 및 학습" (variants and training):
+ *
+ *   S0  sigma^2 = softplus(raw variance), pi = softmax(mixture logits)
+ *       ("변형 및 학습": reparameterisation, softplus for variances, softmax
+ *       for priors).
+ *   S1  gamma_{i,k} = p(z = k | x_i), the standard posterior of a GMM with
+ *       means mu_k, diagonal covariances Sigma_k and priors pi_k
+ *       ("핵심 메커니즘", probabilistic latent routing).  Q_X and K_X are routed
+ *       through the same K components (the shared latent space).
+ *   S2  write:  Vt = Gamma_K^T V,  Z = Gamma_K^T 1_N   ("핵심 메커니즘", write phase)
+ *   S3  read:   O  = (Gamma_Q Vt) / (Gamma_Q Z + eps)  ("핵심 메커니즘", read phase)
+ *   S4  causal: Vt and Z are prefix sums, O_i uses only j <= i
+ *       ("변형 및 학습", bidirectional and causal variants)
+ *   S5  decode: the causal recurrence advanced by one token (state updated
+ *       with the token, then read).
+ *
+ * Readings where the page is silent (each is listed in the design notes):
+ *   - one GMM per head, shared by Q_X and K_X and by every batch element;
+ *   - the full Gaussian log-density, including the log(2 pi sigma^2) terms
+ *     (the 2 pi term cancels in the posterior; it is kept here because this
+ *     is the definition written out);
+ *   - eps is added once to each row's scalar denominator Gamma_Q Z;
+ *   - the causal prefix is inclusive (j <= i); a decode step writes the new
+ *     token into the state before reading.
+ *
+ * Parity pins (tests that do not use this code): a library GMM posterior
+ * (scikit-learn), the two-component logistic closed form, equal-component and
+ * permutation identities, brute-force N x N affinity, rank(Gamma_Q Gamma_K^T)
+ * <= K, causality under perturbation, K = 1 means, and sequence splitting.
+ *
+ * Layouts (row-major, double): per slice s the routing rows are x[s][n][d],
+ * values v[s][n][dv], outputs out[s][n][dv]; a slice uses the parameters of
+ * head head[s]: mu[h][k][d], var_raw[h][k][d], logit_pi[h][k].  A recurrent
+ * state is state[s][K*dv + K]: the latent memory Vt[k][c] followed by Z[k].
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static const double kLog2Pi = 1.8378770664093454835606594728112; /* log(2 pi) */
+
+int gma_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void gma_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* softplus(r) = log(1 + e^r), evaluated without overflow. */
+static double softplus(double r)
+{
+    return fmax(r, 0.0) + log1p(exp(-fabs(r)));
+}
+
+/* S0: variances of every head and log mixture priors (log-softmax of logits). */
+void gma_oracle_params(int H, int K, int d, const double *var_raw, const double *logit_pi,
+                       double *var, double *log_pi)
+{
+    for (long i = 0; i < (long)H * K * d; ++i)
+        var[i] = softplus(var_raw[i]);
+    for (int h = 0; h < H; ++h) {
+        const double *l = logit_pi + (long)h * K;
+        double m = l[0];
+        for (int k = 1; k < K; ++k) m = fmax(m, l[k]);
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) s += exp(l[k] - m);
+        double lse = m + log(s);
+        for (int k = 0; k < K; ++k) log_pi[(long)h * K + k] = l[k] - lse;
+    }
+}
+
+/* S1 for one routing vector x[d]: gamma[k] = pi_k N(x; mu_k, diag var_k) / sum_j (...).
+ * Evaluated in the log domain; ll[K] is scratch. */
+static void posterior(int d, int K, const double *mu, const double *var, const double *log_pi,
+                      const double *x, double *gamma, double *ll)
+{
+    double m = -INFINITY;
+    for (int k = 0; k < K; ++k) {
+        const double *mk = mu + (long)k * d, *vk = var + (long)k * d;
+        double q = 0.0;
+        for (int j = 0; j < d; ++j) {
+            double t = x[j] - mk[j];
+            q += t * t / vk[j] + log(vk[j]) + kLog2Pi;
+        }
+        ll[k] = log_pi[k] - 0.5 * q; /* log pi_k + log N(x; mu_k, Sigma_k) */
+        m = fmax(m, ll[k]);
+    }
+    double den = 0.0;
+    for (int k = 0; k < K; ++k) {
+        gamma[k] = exp(ll[k] - m);
+        den += gamma[k];
+    }
+    for (int k = 0; k < K; ++k) gamma[k] /= den;
+}
+
+typedef struct {
+    double *var, *log_pi;
+} prepared;
+
+static prepared prepare(int H, int K, int d, const double *var_raw, const double *logit_pi)
+{
+    prepared p;
+    p.var = (double *)malloc(sizeof(double) * (size_t)H * K * d);
+    p.log_pi = (double *)malloc(sizeof(double) * (size_t)H * K);
+    gma_oracle_params(H, K, d, var_raw, logit_pi, p.var, p.log_pi);
+    return p;
+}
+
+static void release(prepared p)
+{
+    free(p.var);
+    free(p.log_pi);
+}
+
+/* S1: responsibilities of S slices, gamma[s][n][K]. */
+void gma_oracle_responsibilities(int S, const int *head, int H, int N, int d, int K,
+                                 const double *mu, const double *var_raw, const double *logit_pi,
+                                 const double *x, double *gamma)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+#pragma omp parallel
+    {
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(dynamic) collapse(2)
+        for (int s = 0; s < S; ++s)
+            for (int i = 0; i < N; ++i) {
+                int h = head[s];
+                posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
+                          x + ((long)s * N + i) * d, gamma + ((long)s * N + i) * K, ll);
+            }
+        free(ll);
+    }
+    release(p);
+}
+
+/* S3 for one query row: out[c] = (gq . Vt[:, c]) / (gq . Z + eps). */
+static void read_row(int K, int dv, const double *gq, const double *Vt, const double *Z, double eps,
+                     double *out)
+{
+    double den = 0.0;
+    for (int k = 0; k < K; ++k) den += gq[k] * Z[k];
+    den += eps;
+    for (int c = 0; c < dv; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += gq[k] * Vt[(long)k * dv + c];
+        out[c] = num / den;
+    }
+}
+
+/* S2 for one key row: Vt += gk v^T, Z += gk. */
+static void write_row(int K, int dv, const double *gk, const double *v, double *Vt, double *Z)
+{
+    for (int k = 0; k < K; ++k) {
+        for (int c = 0; c < dv; ++c) Vt[(long)k * dv + c] += gk[k] * v[c];
+        Z[k] += gk[k];
+    }
+}
+
+/* S2 alone: state[s] += [Gamma_K^T V, Gamma_K^T 1] over the slice's n key/value rows. */
+void gma_oracle_write(int S, const int *head, int H, int N, int d, int dv, int K,
+                      const double *mu, const double *var_raw, const double *logit_pi,
+                      const double *kx, const double *v, double *state)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+    const long sz = (long)K * dv + K;
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int j = 0; j < N; ++j) {
+            posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
+                      kx + ((long)s * N + j) * d, g, ll);
+            write_row(K, dv, g, v + ((long)s * N + j) * dv, state + s * sz, state + s * sz + (long)K * dv);
+        }
+        free(g); free(ll);
+    }
+    release(p);
+}
+
+/* S3 alone: every query row of the slice reads the fixed memory state[s]. */
+void gma_oracle_read(int S, const int *head, int H, int N, int d, int dv, int K,
+                     const double *mu, const double *var_raw, const double *logit_pi,
+                     const double *qx, const double *state, double eps, double *out)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+    const long sz = (long)K * dv + K;
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int i = 0; i < N; ++i) {
+            posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
+                      qx + ((long)s * N + i) * d, g, ll);
+            read_row(K, dv, g, state + s * sz, state + s * sz + (long)K * dv, eps,
+                     out + ((long)s * N + i) * dv);
+        }
+        free(g); free(ll);
+    }
+    release(p);
+}
+
+/* S2 + S3, bidirectional: every query reads the memory written by all N keys. */
+void gma_oracle_bidir(int S, const int *head, int H, int N, int d, int dv, int K,
+                      const double *mu, const double *var_raw, const double *logit_pi,
+                      const double *qx, const double *kx, const double *v, double eps, double *out)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        const double *mu_h = mu + (long)h * K * d, *var_h = p.var + (long)h * K * d;
+        const double *lp_h = p.log_pi + (long)h * K;
+        double *Vt = (double *)calloc((size_t)K * dv, sizeof(double));
+        double *Z = (double *)calloc((size_t)K, sizeof(double));
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int j = 0; j < N; ++j) {
+            posterior(d, K, mu_h, var_h, lp_h, kx + ((long)s * N + j) * d, g, ll);
+            write_row(K, dv, g, v + ((long)s * N + j) * dv, Vt, Z);
+        }
+        for (int i = 0; i < N; ++i) {
+            posterior(d, K, mu_h, var_h, lp_h, qx + ((long)s * N + i) * d, g, ll);
+            read_row(K, dv, g, Vt, Z, eps, out + ((long)s * N + i) * dv);
+        }
+        free(Vt); free(Z); free(g); free(ll);
+    }
+    release(p);
+}
+
+/* S4, causal: token i writes its key into the running memory, then its query
+ * reads it, so O_i depends on tokens j <= i only.  state_in (nullable) is the
+ * memory left by earlier tokens; state_out (nullable) receives the final one. */
+void gma_oracle_causal(int S, const int *head, int H, int N, int d, int dv, int K,
+                       const double *mu, const double *var_raw, const double *logit_pi,
+                       const double *qx, const double *kx, const double *v, double eps,
+                       const double *state_in, double *state_out, double *out)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+    const long sz = (long)K * dv + K;
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        const double *mu_h = mu + (long)h * K * d, *var_h = p.var + (long)h * K * d;
+        const double *lp_h = p.log_pi + (long)h * K;
+        double *st = (double *)calloc((size_t)sz, sizeof(double));
+        if (state_in) memcpy(st, state_in + s * sz, sizeof(double) * (size_t)sz);
+        double *Vt = st, *Z = st + (long)K * dv;
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int i = 0; i < N; ++i) {
+            posterior(d, K, mu_h, var_h, lp_h, kx + ((long)s * N + i) * d, g, ll);
+            write_row(K, dv, g, v + ((long)s * N + i) * dv, Vt, Z);
+            posterior(d, K, mu_h, var_h, lp_h, qx + ((long)s * N + i) * d, g, ll);
+            read_row(K, dv, g, Vt, Z, eps, out + ((long)s * N + i) * dv);
+        }
+        if (state_out) memcpy(state_out + s * sz, st, sizeof(double) * (size_t)sz);
+        free(st); free(g); free(ll);
+    }
+    release(p);
+}
+
+/* S5: one decode step per slice; state[s] is advanced in place. */
+void gma_oracle_decode_step(int S, const int *head, int H, int d, int dv, int K,
+                            const double *mu, const double *var_raw, const double *logit_pi,
+                            const double *qx, const double *kx, const double *v, double eps,
+                            double *state, double *out)
+{
+    gma_oracle_causal(S, head, H, 1, d, dv, K, mu, var_raw, logit_pi, qx, kx, v, eps,
+                      state, state, out);
+}

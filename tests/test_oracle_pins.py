@@ -1,0 +1,307 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each test checks the oracle against what the GMA explainer page ("Gaussian
+Mixture Attention: Linear-Time Sequence Mixing via Probabilistic Latent
+Routing", technical summary, "핵심 메커니즘" and "변형 및 학습") or mathematics
+fixes: a library GMM posterior (scikit-learn), the two-component logistic
+closed form, brute-force N x N affinity, rank(Gamma_Q Gamma_K^T) <= K, the
+causal prefix property, K = 1 means, equal-component identities and sequence
+splitting.  None of them retypes the oracle's own code.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import softmax
+
+from gaussian_mixture_sequence_gb300 import workloads as wlmod
+
+TINY = wlmod.WORKLOADS["tiny"]
+
+
+def _tiny(seed=None, K=None, N=None, d=None, dv=None):
+    wl = TINY.with_(**{k: v for k, v in dict(K=K, N=N, d=d, dv=dv).items() if v is not None})
+    mu, vr, lp = wlmod.params(wl, seed)
+    qx, kx, v = wlmod.slice_inputs(wl, 0, 0, seed, mu)
+    return wl, mu, vr, lp, qx[None], kx[None], v[None]
+
+
+def _sklearn_posterior(mu, var_raw, logit_pi, x):
+    """GMM posterior from scikit-learn's GaussianMixture (diagonal covariances).
+
+    The parameters are reparameterised with library routines (numpy logaddexp
+    for softplus, scipy softmax for the priors)."""
+    sk = pytest.importorskip("sklearn.mixture")
+    K, d = mu.shape
+    g = sk.GaussianMixture(n_components=K, covariance_type="diag")
+    cov = np.logaddexp(0.0, var_raw.astype(np.float64))
+    g.weights_ = softmax(logit_pi.astype(np.float64))
+    g.means_ = mu.astype(np.float64)
+    g.covariances_ = cov
+    g.precisions_cholesky_ = 1.0 / np.sqrt(cov)
+    g.precisions_ = 1.0 / cov
+    return g.predict_proba(x.astype(np.float64))
+
+
+# ---------------------------------------------------------------- S0 -------
+
+def test_s0_softplus_closed_forms(orc):
+    r = np.array([0.0, math.log(math.e - 1.0), 50.0, -50.0, 1e-3, -1e-3])
+    var, _ = orc.params(r.reshape(1, 1, -1), np.zeros((1, 1)))
+    var = var.ravel()
+    assert var[0] == pytest.approx(math.log(2.0), rel=1e-15)
+    assert var[1] == pytest.approx(1.0, rel=1e-15)
+    assert var[2] == pytest.approx(50.0 + math.exp(-50.0), rel=1e-15)
+    assert var[3] == pytest.approx(math.exp(-50.0), rel=1e-14)
+    # softplus(r) - softplus(-r) = r
+    rr = np.random.default_rng(0).normal(0, 3, size=64)
+    a, _ = orc.params(rr.reshape(1, 1, -1), np.zeros((1, 1)))
+    b, _ = orc.params(-rr.reshape(1, 1, -1), np.zeros((1, 1)))
+    np.testing.assert_allclose((a - b).ravel(), rr, rtol=0, atol=1e-13)
+
+
+def test_s0_log_priors(orc):
+    rng = np.random.default_rng(1)
+    l = rng.normal(0, 2, size=(3, 11))
+    _, log_pi = orc.params(np.zeros((3, 11, 2)), l)
+    np.testing.assert_allclose(np.exp(log_pi).sum(1), 1.0, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(log_pi - log_pi[:, :1], l - l[:, :1], rtol=0, atol=1e-13)
+    _, u = orc.params(np.zeros((1, 5, 1)), np.full((1, 5), 3.7))
+    np.testing.assert_allclose(u, -math.log(5.0), rtol=1e-15)
+
+
+# ---------------------------------------------------------------- S1 -------
+
+@pytest.mark.parametrize("K,d,dist", [(8, 16, "normal"), (128, 64, "normal"), (32, 64, "peaked"),
+                                      (3, 5, "normal")])
+def test_s1_matches_library_gmm_posterior(orc, K, d, dist):
+    wl = TINY.with_(K=K, d=d, N=300, dist=dist)
+    mu, vr, lp = wlmod.params(wl)
+    x = wlmod.slice_inputs(wl, 0, 0, mu=mu)[0]
+    g = orc.responsibilities(mu, vr, lp, x[None])[0]
+    ref = _sklearn_posterior(mu[0], vr[0], lp[0], x)
+    np.testing.assert_allclose(g, ref, rtol=0, atol=1e-10)
+
+
+def test_s1_two_component_logistic(orc):
+    """d = 1, K = 2, equal variances: the posterior is the logistic function of a
+    linear discriminant (the textbook Gaussian discriminant closed form)."""
+    rng = np.random.default_rng(2)
+    mu = np.array([[[0.7], [-1.3]]])
+    r = 0.4
+    var = math.log1p(math.exp(r))
+    l = np.array([[0.25, -0.6]])
+    x = rng.normal(0, 2, size=(1, 50, 1))
+    g = orc.responsibilities(mu, np.full((1, 2, 1), r), l, x)[0]
+    m1, m2 = 0.7, -1.3
+    a = (m1 - m2) * x[0, :, 0] / var - (m1 * m1 - m2 * m2) / (2 * var) + (0.25 - (-0.6))
+    expect = 1.0 / (1.0 + np.exp(-a))
+    np.testing.assert_allclose(g[:, 0], expect, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(g[:, 1], 1.0 - expect, rtol=1e-12, atol=1e-15)
+
+
+def test_s1_equal_components_give_priors(orc):
+    rng = np.random.default_rng(3)
+    K, d = 6, 4
+    mu = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    vr = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    l = rng.normal(size=(1, K))
+    g = orc.responsibilities(mu, vr, l, rng.normal(size=(1, 40, d)))[0]
+    np.testing.assert_allclose(g, np.tile(softmax(l[0]), (40, 1)), rtol=1e-13)
+
+
+def test_s1_component_permutation(orc):
+    wl, mu, vr, lp, qx, _, _ = _tiny()
+    perm = np.random.default_rng(4).permutation(wl.K)
+    g = orc.responsibilities(mu, vr, lp, qx)[0]
+    gp = orc.responsibilities(mu[:, perm], vr[:, perm], lp[:, perm], qx)[0]
+    np.testing.assert_allclose(gp, g[:, perm], rtol=0, atol=1e-13)
+
+
+def test_s1_rows_are_distributions_even_far_away(orc):
+    wl, mu, vr, lp, qx, _, _ = _tiny()
+    x = np.concatenate([qx[0], np.full((2, wl.d), 1e3), np.full((2, wl.d), -1e3)])
+    g = orc.responsibilities(mu, vr, lp, x[None])[0]
+    assert np.isfinite(g).all() and (g >= 0).all()
+    np.testing.assert_allclose(g.sum(1), 1.0, rtol=0, atol=1e-12)
+    # a token sitting on a component with a tiny variance belongs to it
+    mu2, vr2 = mu.copy(), vr.copy()
+    vr2[0, 3] = -30.0
+    g2 = orc.responsibilities(mu2, vr2, lp, mu2[:, 3:4].astype(np.float64))[0]
+    assert g2[0, 3] > 1 - 1e-12
+
+
+# ------------------------------------------------------------- S2 + S3 -----
+
+def _bruteforce(gq, gk, v, eps, causal):
+    A = gq @ gk.T                        # the N x N affinity Gamma_Q Gamma_K^T
+    if causal:
+        A = np.tril(A)                   # j <= i
+    return (A @ v) / (A.sum(1, keepdims=True) + eps)
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.37])
+@pytest.mark.parametrize("causal", [False, True])
+def test_s2_s4_match_bruteforce_affinity(orc, eps, causal):
+    """The latent-memory form equals materialising the N x N affinity, with
+    responsibilities from the library GMM posterior."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    gq = _sklearn_posterior(mu[0], vr[0], lp[0], qx[0])
+    gk = _sklearn_posterior(mu[0], vr[0], lp[0], kx[0])
+    ref = _bruteforce(gq, gk, v[0].astype(np.float64), eps, causal)
+    fn = orc.causal if causal else orc.bidir
+    out = fn(mu, vr, lp, qx, kx, v, eps)[0]
+    np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12)
+
+
+def test_affinity_rank_at_most_K(orc):
+    wl, mu, vr, lp, qx, kx, _ = _tiny()
+    gq = orc.responsibilities(mu, vr, lp, qx)[0]
+    gk = orc.responsibilities(mu, vr, lp, kx)[0]
+    s = np.linalg.svd(gq @ gk.T, compute_uv=False)
+    assert wl.N > wl.K
+    assert s[wl.K:].max() < 1e-12 * s[0]
+    assert s[wl.K - 1] > 1e-12 * s[0]
+
+
+def test_bidir_K1_is_the_mean(orc):
+    wl, mu, vr, lp, qx, kx, v = _tiny(K=1)
+    eps = 0.25
+    out = orc.bidir(mu, vr, lp, qx, kx, v, eps)[0]
+    expect = v[0].astype(np.float64).sum(0) / (wl.N + eps)
+    np.testing.assert_allclose(out, np.tile(expect, (wl.N, 1)), rtol=1e-12, atol=1e-15)
+
+
+def test_bidir_equal_components_give_scaled_mean(orc):
+    rng = np.random.default_rng(5)
+    K, d, dv, N = 5, 3, 4, 64
+    mu = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    vr = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    l = rng.normal(size=(1, K))
+    v = rng.normal(size=(1, N, dv))
+    eps = 0.1
+    out = orc.bidir(mu, vr, l, rng.normal(size=(1, N, d)), rng.normal(size=(1, N, d)), v, eps)[0]
+    pp = float((softmax(l[0]) ** 2).sum())
+    expect = v[0].sum(0) * pp / (N * pp + eps)
+    np.testing.assert_allclose(out, np.tile(expect, (N, 1)), rtol=1e-12)
+
+
+def test_bidir_convexity_permutation_linearity(orc):
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    out = orc.bidir(mu, vr, lp, qx, kx, v, 1e-6)[0]
+    assert (np.abs(out) <= np.abs(v[0]).max(0) + 1e-12).all()
+    perm = np.random.default_rng(6).permutation(wl.N)
+    outp = orc.bidir(mu, vr, lp, qx, kx[:, perm], v[:, perm], 1e-6)[0]
+    np.testing.assert_allclose(outp, out, rtol=1e-11, atol=1e-14)
+    v2 = np.random.default_rng(7).normal(size=v.shape)
+    o2 = orc.bidir(mu, vr, lp, qx, kx, v2, 1e-6)[0]
+    o12 = orc.bidir(mu, vr, lp, qx, kx, 2.0 * v - 3.0 * v2, 1e-6)[0]
+    np.testing.assert_allclose(o12, 2.0 * out - 3.0 * o2, rtol=1e-10, atol=1e-12)
+    ones = orc.bidir(mu, vr, lp, qx, kx, np.ones_like(v), 1e-6)[0]
+    assert (ones < 1).all() and (ones > 1 - 1e-4).all()
+
+
+# ---------------------------------------------------------------- S4 -------
+
+def test_s4_causal_prefix_property(orc):
+    """O_i depends on tokens j <= i only: perturbing later tokens leaves it bit-identical."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    out = orc.causal(mu, vr, lp, qx, kx, v, 1e-6)[0]
+    rng = np.random.default_rng(8)
+    for i in (0, 1, 63, 64, 200, wl.N - 2):
+        q2, k2, v2 = qx.copy(), kx.copy(), v.copy()
+        q2[0, i + 1:] += rng.normal(size=q2[0, i + 1:].shape).astype(np.float32)
+        k2[0, i + 1:] += rng.normal(size=k2[0, i + 1:].shape).astype(np.float32)
+        v2[0, i + 1:] += rng.normal(size=v2[0, i + 1:].shape).astype(np.float32)
+        o2 = orc.causal(mu, vr, lp, q2, k2, v2, 1e-6)[0]
+        assert np.array_equal(o2[: i + 1], out[: i + 1])
+        assert not np.array_equal(o2[i + 1:], out[i + 1:])
+
+
+def test_s4_K1_is_the_prefix_mean(orc):
+    wl, mu, vr, lp, qx, kx, v = _tiny(K=1)
+    eps = 0.5
+    out = orc.causal(mu, vr, lp, qx, kx, v, eps)[0]
+    cs = np.cumsum(v[0].astype(np.float64), 0)
+    n = np.arange(1, wl.N + 1, dtype=np.float64)[:, None]
+    np.testing.assert_allclose(out, cs / (n + eps), rtol=1e-12, atol=1e-15)
+
+
+def test_s4_last_row_equals_bidir(orc):
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    c = orc.causal(mu, vr, lp, qx, kx, v, 1e-6)[0]
+    b = orc.bidir(mu, vr, lp, qx, kx, v, 1e-6)[0]
+    np.testing.assert_allclose(c[-1], b[-1], rtol=1e-12, atol=1e-15)
+    assert not np.allclose(c[0], b[0])
+
+
+def test_s4_state_carry_and_split(orc):
+    """Splitting the sequence and carrying the state is exact, and the final
+    state is the bidirectional write [Gamma_K^T V, Gamma_K^T 1]."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    full, st = orc.causal(mu, vr, lp, qx, kx, v, 1e-6, return_state=True)
+    gk = _sklearn_posterior(mu[0], vr[0], lp[0], kx[0])
+    expect = np.concatenate([(gk.T @ v[0].astype(np.float64)).ravel(), gk.sum(0)])
+    np.testing.assert_allclose(st[0], expect, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(orc.write(mu, vr, lp, kx, v)[0], expect, rtol=1e-10, atol=1e-12)
+    for m in (1, 100, 128):
+        a, sa = orc.causal(mu, vr, lp, qx[:, :m], kx[:, :m], v[:, :m], 1e-6, return_state=True)
+        b, sb = orc.causal(mu, vr, lp, qx[:, m:], kx[:, m:], v[:, m:], 1e-6, state_in=sa,
+                           return_state=True)
+        np.testing.assert_allclose(np.concatenate([a, b], 1), full, rtol=1e-11, atol=1e-14)
+        np.testing.assert_allclose(sb, st, rtol=1e-12, atol=1e-12)
+
+
+def test_bidir_is_write_then_read_and_splits(orc):
+    """The bidirectional memory of a split sequence is the sum of the parts'
+    memories (the exchange a sequence-split run would all-reduce)."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    b = orc.bidir(mu, vr, lp, qx, kx, v, 1e-6)
+    s1 = orc.write(mu, vr, lp, kx[:, :77], v[:, :77])
+    s2 = orc.write(mu, vr, lp, kx[:, 77:], v[:, 77:])
+    np.testing.assert_allclose(orc.read(mu, vr, lp, qx, s1 + s2, 1e-6), b, rtol=1e-11, atol=1e-14)
+
+
+# ---------------------------------------------------------------- S5 -------
+
+def test_s5_decode_continues_prefill(orc):
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    m = 200
+    full = orc.causal(mu, vr, lp, qx, kx, v, 1e-6)[0]
+    _, st = orc.causal(mu, vr, lp, qx[:, :m], kx[:, :m], v[:, :m], 1e-6, return_state=True)
+    for t in range(m, wl.N):
+        o, st = orc.decode_step(mu, vr, lp, qx[:, t], kx[:, t], v[:, t], 1e-6, st)
+        np.testing.assert_allclose(o[0], full[t], rtol=1e-11, atol=1e-14)
+
+
+def test_oracle_heads_and_slices(orc):
+    """Slices use their own head's parameters; a sampled subset equals the full run."""
+    wl = wlmod.WORKLOADS["tiny"].with_(B=2, H=3, N=40)
+    mu, vr, lp = wlmod.params(wl)
+    qx, kx, v = wlmod.full_inputs(wl)
+    S = wl.B * wl.H
+    full = orc.causal(mu, vr, lp, qx.reshape(S, wl.N, -1), kx.reshape(S, wl.N, -1),
+                      v.reshape(S, wl.N, -1), wl.eps)
+    pick = [1, 5]
+    sub = orc.causal(mu, vr, lp, qx.reshape(S, wl.N, -1)[pick], kx.reshape(S, wl.N, -1)[pick],
+                     v.reshape(S, wl.N, -1)[pick], wl.eps, heads=[p % wl.H for p in pick])
+    np.testing.assert_array_equal(sub, full[pick])
+    one = orc.causal(mu[1:2], vr[1:2], lp[1:2], qx[1, 1][None], kx[1, 1][None], v[1, 1][None], wl.eps)
+    np.testing.assert_array_equal(one[0], full[4])
+
+
+def test_oracle_matches_its_recorded_values(orc):
+    """Guards against drift: sampled values recorded by tests/golden/make_golden.py."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "tiny_oracle.json")) as f:
+        rec = json.load(f)
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    rows = rec["rows"]
+    g = orc.responsibilities(mu, vr, lp, qx)[0]
+    c, st = orc.causal(mu, vr, lp, qx, kx, v, wl.eps, return_state=True)
+    b = orc.bidir(mu, vr, lp, qx, kx, v, wl.eps)
+    np.testing.assert_allclose(g[rows], rec["gamma_q"], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(c[0, rows], rec["causal"], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(b[0, rows], rec["bidir"], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(st[0], rec["state_final"], rtol=1e-12, atol=1e-13)
