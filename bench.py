@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Causal GMA forward throughput on GB300 (tokens/s at N=16384, K=128).
+
+One step = one full causal forward (parameter preparation, responsibilities
+of Q_X and K_X, chunkwise write/read with the carried memory) over one batch
+of seeded synthetic inputs already resident in HBM, through the library's C
+ABI.  Prints one JSON line (rank 0).  See --help for options.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+For N > 1 it is launched by torch.distributed.run, one rank per GPU; every
+rank runs its own replica of the workload (weak scaling, no collective on the
+data path) and the slowest rank's time sets the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GMA causal fwd tokens/sec at N=16K,K=128 (1 GB300); % of roofline"
+SM_COUNT, FP32_LANES_PER_SM = 152, 128
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gma", "reference"], default="gma")
+    p.add_argument("--workload", default="causal_16k_peaked")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--min-warmup-s", type=float, default=1.0,
+                   help="keep warming up (at least --warmup steps) until this many seconds passed")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------- work model --
+
+def stage_work(stage, wl):
+    """Algorithmic work of one launch of a stage: (bound, amount, unit-of-amount).
+
+    Per head-token (ht), with d = d_route, K components, d_v values, chunk C:
+      resp_q / resp_k : 4*K*d flop (one fp32x2 FMA for (x-mu)/sigma, one for the
+                        square-accumulate, per component and feature pair)
+      block_state     : 2*K*(d_v+1) flop  (Gamma_K^T [V | 1])
+      chunk_out       : 4*K*(d_v+1) + 2*C*K + C*(d_v+1) flop (read of the carried
+                        memory, its update, P = Gq Gk^T, lower half of P [V | 1])
+      state_scan      : 2 * 4 * (K*d_v + K) bytes per block (read + write)
+      prep_params     : negligible
+    """
+    ht = wl.B * wl.H * wl.N
+    K, d, dv, C = wl.K, wl.d, wl.dv, wl.chunk
+    if stage in ("resp_q", "resp_k"):
+        return "alu", 4.0 * K * d * ht, "flop"
+    if stage == "block_state":
+        return "alu", 2.0 * K * (dv + 1) * ht, "flop"
+    if stage == "chunk_out":
+        return "alu", (4.0 * K * (dv + 1) + 2.0 * C * K + C * (dv + 1)) * ht, "flop"
+    if stage == "state_scan":
+        nblk = -(-wl.N // 256)
+        return "hbm", 2.0 * 4 * (K * dv + K) * nblk * wl.B * wl.H, "byte"
+    return None, 0.0, None
+
+
+def path_roofline_s(wl, pk):
+    """Roofline time of the whole step: max(FP32 time of the routing, HBM time of
+    the minimum traffic, tensor time of the chunk products at the tf32 rate)."""
+    ht = wl.B * wl.H * wl.N
+    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
+    t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    vb = 2 if wl.v_dtype == "bf16" else 4
+    t_hbm = ((2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * ht) / (pk["hbm_gbs"] * 1e9)
+    mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * wl.chunk * wl.K + wl.chunk * (wl.dv + 1)) * ht
+    tf32 = pk["bf16_tflops"] * 1e12 * (1.1 / 2.25)
+    t_mma = mma / tf32
+    return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)
+
+
+# ----------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 <= t <= t1]
+        if len(win) < 3:
+            win = [p for _, p in self.samples]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower().startswith("active")})
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------- helpers ----
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def traffic_record(stage):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = source_hash()
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == stage and f[1] == h:
+            return float(f[3])
+    return None
+
+
+def source_hash():
+    d = os.path.join(ROOT, "gaussian_mixture_sequence_gb300", "csrc")
+    m = hashlib.sha256()
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh")):
+            m.update(open(os.path.join(d, fn), "rb").read())
+    return m.hexdigest()[:16]
+
+
+def cpu_baseline(wl, inputs_np, threads=None):
+    """The fp64 oracle as it stands, on a bounded sample of the same workload."""
+    import oracle
+    q, k, v, mu, vr, lp = inputs_np
+    nthr = oracle.max_threads() if threads is None else threads
+    S = min(wl.B * wl.H, max(8, nthr))
+    sl = list(range(S))
+    qs = q.reshape(wl.B * wl.H, wl.N, -1)[sl]
+    ks = k.reshape(wl.B * wl.H, wl.N, -1)[sl]
+    vs = v.reshape(wl.B * wl.H, wl.N, -1)[sl]
+    t0 = time.perf_counter()
+    oracle.causal(mu, vr, lp, qs, ks, vs, wl.eps, heads=[s % wl.H for s in sl])
+    dt = time.perf_counter() - t0
+    tokens = S * wl.N / wl.H
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": min(nthr, S), "kind": "oracle",
+            "sample": f"{S} of {wl.B * wl.H} (batch, head) sequences of workload {wl.name}, full length "
+                      f"N={wl.N} (= {tokens:.0f} tokens of H={wl.H} heads), fp64, {dt:.2f} s wall"}
+
+
+# ----------------------------------------------------------------- reference --
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from gaussian_mixture_sequence_gb300 import workloads
+    mu, vr, lp = workloads.params(wl)
+    nthr = oracle.max_threads()
+    S = min(wl.B * wl.H, max(1, nthr))
+    slices = [workloads.slice_inputs(wl, s // wl.H, s % wl.H, mu=mu) for s in range(S)]
+    q = np.stack([x[0] for x in slices]); k = np.stack([x[1] for x in slices]); v = np.stack([x[2] for x in slices])
+    heads = [s % wl.H for s in range(S)]
+    # size one step (a prefix of n tokens of S sequences) so that the whole run stays near 2 minutes
+    n = 256
+    t0 = time.perf_counter()
+    oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
+    per_tok = (time.perf_counter() - t0) / n
+    total = args.steps + args.warmup
+    n = int(max(64, min(wl.N, 120.0 / total / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    tokens = S * n / wl.H
+    val = tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d, "d_v": wl.dv,
+                   "K": wl.K, "chunk": wl.chunk},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": min(nthr, S), "kind": "oracle",
+                         "sample": f"each step: first {n} tokens of {S} (batch, head) sequences of {wl.name}"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- main -------
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    from gaussian_mixture_sequence_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    if wl.mode != "causal":
+        raise SystemExit("bench.py times the causal forward; pick a causal workload")
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+
+    import numpy as np
+    import torch
+    from gaussian_mixture_sequence_gb300 import gma
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    gma.load()
+
+    seed = wl.seed + rank
+    mu, vr, lp = workloads.params(wl, seed)
+    q, k, v = workloads.full_inputs(wl, seed)
+    tdt = lambda s: torch.bfloat16 if s == "bf16" else torch.float32
+    h_q = torch.from_numpy(q).to(tdt(wl.x_dtype)).pin_memory()
+    h_k = torch.from_numpy(k).to(tdt(wl.x_dtype)).pin_memory()
+    h_v = torch.from_numpy(v).to(tdt(wl.v_dtype)).pin_memory()
+    d_q, d_k, d_v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
+    prm = tuple(torch.from_numpy(a).to(dev) for a in (mu, vr, lp))
+    shape = gma.Shape.make(wl.B, wl.H, wl.N, wl.d, wl.dv, wl.K, chunk=wl.chunk, eps=wl.eps,
+                           x_dtype=wl.x_dtype, v_dtype=wl.v_dtype, gemm_dtype=wl.gemm_dtype)
+    ws = torch.empty(gma.gma_workspace_size(shape, gma.OP_CAUSAL), dtype=torch.uint8, device=dev)
+    out = torch.empty(wl.B, wl.H, wl.N, wl.dv, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    NE = gma.PROFILE_MAX_STAGES + 1
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(NE)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    step_events = [new_events() for _ in range(args.steps)]
+    warm_events = new_events()
+    torch.cuda.synchronize(dev)
+
+    def step(evs):
+        return gma.gma_forward_causal_profiled(shape, *prm, d_q, d_k, d_v, out, evs, ws=ws)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
+    # warm-up: at least --warmup steps and --min-warmup-s seconds (keeps the clock sampler fed)
+    t_w = time.time()
+    nw = 0
+    while nw < args.warmup or time.time() - t_w < args.min_warmup_s:
+        step(warm_events)
+        nw += 1
+        if nw % 20 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    start.record(stream)
+    names = None
+    for i in range(args.steps):
+        names = step(step_events[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if pg:
+        pg.barrier()
+    total_ms = start.elapsed_time(end)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks_summary = clocks.summary(t_host0, t_host1)
+
+    ms = total_ms / args.steps
+    tokens = wl.B * wl.N
+    value = world * tokens / (ms * 1e-3)
+    stage_ms = {}
+    for i, nm in enumerate(names):
+        stage_ms[nm] = statistics.mean(step_events[s][i].elapsed_time(step_events[s][i + 1])
+                                       for s in range(args.steps))
+    dom = max(stage_ms, key=stage_ms.get)
+    pk, pk_kind = peaks()
+    bound, amount, unit = stage_work(dom, wl)
+    if bound == "alu":
+        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        achieved = amount / (stage_ms[dom] * 1e-3) / 1e12
+        r_unit = "TFLOP/s"
+    elif bound == "tensor":
+        peak = pk["bf16_tflops"] * (1.1 / 2.25)
+        achieved = amount / (stage_ms[dom] * 1e-3) / 1e12
+        r_unit = "TFLOP/s"
+    else:
+        peak = pk["hbm_gbs"]
+        achieved = amount / (stage_ms[dom] * 1e-3) / 1e9
+        r_unit = "GB/s"
+    roof_s, roof_parts = path_roofline_s(wl, pk)
+
+    # end to end through the same public API: pinned host inputs in, result out, every step
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ne = max(1, min(args.e2e_steps, args.steps))
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e_start.record(stream)
+    for _ in range(ne):
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        gma.gma_forward_causal(shape, *prm, d_q, d_k, d_v, out, ws=ws)
+        h_out.copy_(out, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e_start.elapsed_time(e_end) / ne
+    if pg:
+        t = torch.tensor([e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e_ms = float(t.item())
+    clocks.stop()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    d2h = h_out.numel() * h_out.element_size()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, (q, k, v, mu, vr, lp))
+
+    if rank == 0:
+        tr = traffic_record(dom)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": nw, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if wl.gemm_dtype == "f32" else "f32+bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d, "d_v": wl.dv,
+                       "K": wl.K, "chunk": wl.chunk, "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
+                       "inputs": "peaked mixture around the K centres" if wl.dist == "peaked" else "N(0,1)",
+                       "l2": "inputs (%.0f MB) larger than L2 (129 MB), no flush" %
+                             ((h2d) / 1e6)},
+            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": r_unit,
+                         "frac": achieved / peak, "traffic": tr,
+                         "peak_source": ("FP32 lanes x 2 x max SM clock (%s clock)" % pk_kind)
+                         if bound == "alu" else pk_kind},
+            "path_roofline": {"tokens_per_s": tokens / roof_s, "frac": value / world / (tokens / roof_s),
+                              **{k2: v2 * 1e3 for k2, v2 in roof_parts.items()}, "unit_ms": True},
+            "stages_ms": stage_ms,
+            "gpu_launches": len(names) * args.steps,
+            "clocks": clocks_summary,
+            "e2e": {"value": world * tokens / (e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,291 @@
+// C ABI of libgma: host-side validation, workspace layout and launch order.
+// The operations are those of the GMA explainer "Gaussian Mixture Attention:
+// Linear-Time Sequence Mixing via Probabilistic Latent Routing" (technical
+// summary, "핵심 메커니즘" and "변형 및 학습"); see include/gma.h.
+#include "gma_internal.cuh"
+
+#include <math.h>
+
+using namespace gma;
+
+namespace {
+
+struct WsPlan {
+    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, bytes = 0;
+};
+
+bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }
+
+gma_status make_dims(const gma_shape *s, Dims *dm)
+{
+    if (!s) return GMA_ERR_INVALID_ARG;
+    if (s->B < 1 || s->H < 1 || s->N < 0 || s->K < 1 || s->d_route < 1 || s->d_v < 1 || s->chunk < 0)
+        return GMA_ERR_INVALID_ARG;
+    if (!(s->eps >= 0.f) || !isfinite(s->eps)) return GMA_ERR_INVALID_ARG;
+    if ((unsigned)s->x_dtype > 1u || (unsigned)s->v_dtype > 1u || (unsigned)s->gemm_dtype > 1u)
+        return GMA_ERR_INVALID_ARG;
+    if (!valid_width(s->d_route) || !valid_width(s->d_v) || s->K > 512) return GMA_ERR_UNSUPPORTED;
+    const int C = s->chunk == 0 ? 64 : s->chunk;
+    if (C != 16 && C != 32 && C != 64) return GMA_ERR_UNSUPPORTED;
+    const long long BH = (long long)s->B * s->H;
+    if (BH > 65535) return GMA_ERR_UNSUPPORTED;
+    const long long w = s->K > s->d_v ? (s->K > s->d_route ? s->K : s->d_route)
+                                      : (s->d_v > s->d_route ? s->d_v : s->d_route);
+    if (BH * (long long)s->N * w >= (1LL << 40)) return GMA_ERR_UNSUPPORTED;
+    dm->B = s->B; dm->H = s->H; dm->N = s->N; dm->D = s->d_route; dm->DV = s->d_v; dm->K = s->K;
+    dm->KP = (int)round_up(s->K, 8);
+    dm->C = C;
+    dm->eps = s->eps;
+    dm->x_bf16 = s->x_dtype == GMA_BF16;
+    dm->v_bf16 = s->v_dtype == GMA_BF16;
+    dm->g_bf16 = s->gemm_dtype == GMA_BF16;
+    return GMA_OK;
+}
+
+WsPlan plan(const Dims &dm, gma_op op)
+{
+    WsPlan p;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off = (size_t)round_up((long long)(off + n), 256);
+        return o;
+    };
+    p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
+    p.cst = take((size_t)dm.H * dm.K * 4);
+    if (op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL) {
+        const size_t gb = dm.g_bf16 ? 2 : 4;
+        p.gq = take((size_t)dm.BH() * dm.N * dm.KP * gb);
+        p.gk = take((size_t)dm.BH() * dm.N * dm.KP * gb);
+        p.partial = take((size_t)dm.BH() * dm.nblk() * dm.state_size() * 4);
+        if (op == GMA_OP_BIDIR) p.total = take((size_t)dm.BH() * dm.state_size() * 4);
+    }
+    p.bytes = off;
+    return p;
+}
+
+bool aligned(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+gma_status check_ptr(const void *p, bool required = true)
+{
+    if (!p) return required ? GMA_ERR_INVALID_ARG : GMA_OK;
+    return aligned(p) ? GMA_OK : GMA_ERR_ALIGNMENT;
+}
+
+gma_status check_params(const gma_params &p)
+{
+    gma_status s;
+    if ((s = check_ptr(p.mu)) != GMA_OK) return s;
+    if ((s = check_ptr(p.var_raw)) != GMA_OK) return s;
+    return check_ptr(p.logit_pi);
+}
+
+gma_status check_ws(void *ws, size_t ws_bytes, const WsPlan &wp)
+{
+    if (!ws || ws_bytes < wp.bytes) return GMA_ERR_WORKSPACE;
+    return aligned(ws) ? GMA_OK : GMA_ERR_ALIGNMENT;
+}
+
+#define GMA_TRY(expr)                                                                                      \
+    do {                                                                                                   \
+        gma_status _s = (expr);                                                                            \
+        if (_s != GMA_OK) return _s;                                                                       \
+    } while (0)
+#define GMA_CUDA(expr)                                                                                     \
+    do {                                                                                                   \
+        if ((expr) != cudaSuccess) return GMA_ERR_CUDA;                                                    \
+    } while (0)
+
+template <typename T>
+T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+} // namespace
+
+extern "C" {
+
+size_t gma_workspace_size(const gma_shape *shape, gma_op op)
+{
+    Dims dm;
+    if (make_dims(shape, &dm) != GMA_OK || (unsigned)op > 3u) return 0;
+    return plan(dm, op).bytes;
+}
+
+const char *gma_status_string(gma_status status)
+{
+    switch (status) {
+    case GMA_OK: return "ok";
+    case GMA_ERR_INVALID_ARG: return "invalid argument";
+    case GMA_ERR_UNSUPPORTED: return "unsupported size";
+    case GMA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case GMA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GMA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const void *x, float *gamma,
+                                void *ws, size_t ws_bytes, gma_stream_t stream)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(x, dm.N > 0));
+    GMA_TRY(check_ptr(gamma, dm.N > 0));
+    const WsPlan wp = plan(dm, GMA_OP_RESPONSIBILITIES);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    if (dm.N == 0) return GMA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, x, gamma, dm.K, false, st));
+    return GMA_OK;
+}
+
+gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                             const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx, dm.N > 0));
+    GMA_TRY(check_ptr(kx, dm.N > 0));
+    GMA_TRY(check_ptr(v, dm.N > 0));
+    GMA_TRY(check_ptr(out, dm.N > 0));
+    const WsPlan wp = plan(dm, GMA_OP_BIDIR);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    if (dm.N == 0) return GMA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
+    float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+    GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st));
+    GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
+    return GMA_OK;
+}
+
+} // extern "C"
+
+namespace {
+
+// Records the profiling event of the next launch (no-op without a profile).
+struct Marks {
+    gma_profile *prof;
+    int n = 0;
+    cudaStream_t st;
+    cudaError_t mark(const char *name)
+    {
+        if (!prof) return cudaSuccess;
+        if (n >= GMA_PROFILE_MAX_STAGES) return cudaErrorInvalidValue;
+        prof->stage_name[n] = name;
+        return cudaEventRecord(static_cast<cudaEvent_t>(prof->events[n++]), st);
+    }
+    cudaError_t finish()
+    {
+        if (!prof) return cudaSuccess;
+        prof->n_stages = n;
+        return cudaEventRecord(static_cast<cudaEvent_t>(prof->events[n]), st);
+    }
+};
+
+gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                      const void *v, const float *state_in, float *state_out, float *out, void *ws,
+                      size_t ws_bytes, gma_stream_t stream, gma_profile *prof)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx, dm.N > 0));
+    GMA_TRY(check_ptr(kx, dm.N > 0));
+    GMA_TRY(check_ptr(v, dm.N > 0));
+    GMA_TRY(check_ptr(out, dm.N > 0));
+    GMA_TRY(check_ptr(state_in, false));
+    GMA_TRY(check_ptr(state_out, false));
+    const WsPlan wp = plan(dm, GMA_OP_CAUSAL);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    if (prof) {
+        for (int i = 0; i <= GMA_PROFILE_MAX_STAGES; ++i)
+            if (!prof->events[i]) return GMA_ERR_INVALID_ARG;
+        prof->n_stages = 0;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Marks mk{prof, 0, st};
+    if (dm.N == 0) {
+        if (state_out && state_out != state_in) {
+            const size_t bytes = (size_t)dm.BH() * dm.state_size() * 4;
+            if (state_in)
+                GMA_CUDA(cudaMemcpyAsync(state_out, state_in, bytes, cudaMemcpyDeviceToDevice, st));
+            else
+                GMA_CUDA(cudaMemsetAsync(state_out, 0, bytes, st));
+        }
+        GMA_CUDA(mk.finish());
+        return GMA_OK;
+    }
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
+    float *partial = at<float>(ws, wp.partial);
+    GMA_CUDA(mk.mark("prep_params"));
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(mk.mark("resp_q"));
+    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(mk.mark("resp_k"));
+    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(mk.mark("block_state"));
+    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+    GMA_CUDA(mk.mark("state_scan"));
+    GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
+    GMA_CUDA(mk.mark("chunk_out"));
+    GMA_CUDA(launch_chunk_out(dm, true, gq, gk, v, partial, out, st));
+    GMA_CUDA(mk.finish());
+    return GMA_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+gma_status gma_forward_causal(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                              const void *v, const float *state_in, float *state_out, float *out, void *ws,
+                              size_t ws_bytes, gma_stream_t stream)
+{
+    return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, nullptr);
+}
+
+gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params, const void *qx,
+                                       const void *kx, const void *v, const float *state_in,
+                                       float *state_out, float *out, void *ws, size_t ws_bytes,
+                                       gma_stream_t stream, gma_profile *prof)
+{
+    if (!prof) return GMA_ERR_INVALID_ARG;
+    return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, prof);
+}
+
+gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                           const void *v, float *state, float *out, void *ws, size_t ws_bytes,
+                           gma_stream_t stream)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx));
+    GMA_TRY(check_ptr(kx));
+    GMA_TRY(check_ptr(v));
+    GMA_TRY(check_ptr(state));
+    GMA_TRY(check_ptr(out));
+    const WsPlan wp = plan(dm, GMA_OP_DECODE);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
+    return GMA_OK;
+}
+
+} // extern "C"

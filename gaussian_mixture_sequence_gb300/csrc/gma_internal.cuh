@@ -1,0 +1,84 @@
+// Internal declarations shared by the translation units of libgma.
+//
+// Data layout in device memory (all row-major):
+//   routing rows     x[bh][n][d_route]      (fp32 or bf16)
+//   values           v[bh][n][d_v]          (fp32 or bf16)
+//   responsibilities g[bh][n][KP]           (workspace; fp32 or bf16, KP = K rounded up to 8,
+//                                            the padding columns hold zeros)
+//   memory state     s[bh][K*d_v + K]       (Vt as K rows of d_v, then Z)
+//   packed params    prm[h][k][d_route/2]   float4 {s_d, s_d+1, -mu_d s_d, -mu_d+1 s_d+1},
+//                                            s = 1/sigma;  cst[h][k] = log pi_k - 1/2 sum_d log sigma^2
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gma.h"
+
+namespace gma {
+
+constexpr int kThreads = 256;     // threads per CTA of every generic kernel
+constexpr int kBlockRows = 256;   // rows per block of the block-state / causal-output kernels
+
+struct Dims {
+    int B, H, N, D, DV, K, KP, C;
+    float eps;
+    bool x_bf16, v_bf16, g_bf16;
+    long long BH() const { return (long long)B * H; }
+    long long state_size() const { return (long long)K * DV + K; }
+    int nblk() const { return (N + kBlockRows - 1) / kBlockRows; }
+};
+
+__host__ __device__ constexpr inline long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+
+// Element load from an fp32 or bf16 array (uniform runtime switch).
+__device__ __forceinline__ float load_elem(const void *base, long long i, bool bf16)
+{
+    return bf16 ? bf16_bits_to_f32(static_cast<const uint16_t *>(base)[i])
+                : static_cast<const float *>(base)[i];
+}
+
+// Four consecutive elements starting at i (i % 4 == 0, base 16-byte aligned).
+__device__ __forceinline__ float4 load4(const void *base, long long i, bool bf16)
+{
+    if (bf16) {
+        uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + i);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    return *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + i);
+}
+
+__device__ __forceinline__ void store_elem(void *base, long long i, float v, bool bf16)
+{
+    if (bf16)
+        static_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(base)[i] = v;
+}
+
+// ---- launchers (each returns the launch's cudaError_t) ----
+cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st);
+cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
+                        int ldg, bool gamma_bf16, cudaStream_t st);
+cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, float *partial,
+                               cudaStream_t st);
+cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total,
+                        bool exclusive, cudaStream_t st);
+cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
+                             float *states, float *out, cudaStream_t st);
+cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
+                          const void *kx, const void *v, float *state, float *out, cudaStream_t st);
+
+// Sets the dynamic shared-memory limit of a kernel once per process.
+template <typename Kern>
+inline cudaError_t allow_smem(Kern k, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+} // namespace gma

@@ -1,0 +1,237 @@
+// Parameter preparation (S0) and the responsibility kernel (S1).
+//
+// S0 follows the reparameterisation of the GMA explainer ("변형 및 학습"):
+// sigma^2 = softplus(var_raw), pi = softmax(logit_pi).  S1 evaluates the
+// diagonal-GMM posterior of "핵심 메커니즘":
+//   l_ik  = log pi_k - 1/2 sum_d [ (x_id - mu_kd)^2 / sigma_kd^2 + log sigma_kd^2 ]
+//   gamma = softmax_k(l)              (the -d/2 log 2pi term cancels)
+// The quadratic form is evaluated directly as ((x - mu) / sigma)^2 — never by
+// expanding it into x^2 and x terms, which cancel catastrophically — using one
+// packed fp32x2 FMA for (x * s - mu * s) and one for the square-accumulate.
+#include "gma_internal.cuh"
+
+#include <float.h>
+
+namespace gma {
+namespace {
+
+__device__ __forceinline__ float softplus(float r) { return fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))); }
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One CTA per head.
+__global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__restrict__ mu,
+                                                   const float *__restrict__ var_raw,
+                                                   const float *__restrict__ logit_pi,
+                                                   float4 *__restrict__ prm, float *__restrict__ cst)
+{
+    __shared__ float red[kThreads / 32];
+    __shared__ float bcast;
+    const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *l = logit_pi + (long long)h * K;
+
+    float m = -FLT_MAX;
+    for (int k = tid; k < K; k += kThreads) m = fmaxf(m, l[k]);
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < kThreads / 32 ? red[lane] : -FLT_MAX;
+        t = warp_max(t);
+        if (lane == 0) bcast = t;
+    }
+    __syncthreads();
+    const float lmax = bcast;
+    float s = 0.f;
+    for (int k = tid; k < K; k += kThreads) s += expf(l[k] - lmax);
+    s = warp_sum(s);
+    __syncthreads();
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < kThreads / 32 ? red[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) bcast = lmax + logf(t);
+    }
+    __syncthreads();
+    const float lse = bcast;
+
+    const float *vr = var_raw + (long long)h * K * D;
+    const float *mh = mu + (long long)h * K * D;
+    for (int k = tid; k < K; k += kThreads) {
+        float acc = 0.f;
+        for (int d = 0; d < D; ++d) acc += logf(softplus(vr[(long long)k * D + d]));
+        cst[(long long)h * K + k] = (l[k] - lse) - 0.5f * acc;
+    }
+    const int DP = D / 2;
+    for (int i = tid; i < K * DP; i += kThreads) {
+        const long long e = 2LL * i; // k * D + 2 * dp
+        float s0 = 1.0f / sqrtf(softplus(vr[e])), s1 = 1.0f / sqrtf(softplus(vr[e + 1]));
+        prm[(long long)h * K * DP + i] = make_float4(s0, s1, -mh[e] * s0, -mh[e + 1] * s1);
+    }
+}
+
+// Responsibilities of a range of rows of one (b, h) slice.
+//   RPT rows per thread (lane, lane + 32, ...): ROWS = 32 * RPT rows per tile.
+//   Each warp owns components k = warp, warp + 8, ... of the current component
+//   tile (parameters broadcast from shared memory); the log-joint l_ik goes to
+//   a shared [ROWS][K|1] tile and a warp per row then normalises it.
+template <int D>
+struct RespCfg {
+    static constexpr int RPT = D <= 64 ? 2 : 1;
+    static constexpr int ROWS = 32 * RPT;
+    static constexpr int KT = D == 128 ? 64 : 128; // components per parameter tile
+    static constexpr int ROWS_PER_CTA = 256;
+    static size_t smem(int K) { return (size_t)KT * (D / 2) * 16 + KT * 4 + (size_t)ROWS * (K | 1) * 4; }
+};
+
+template <int D>
+__device__ __forceinline__ void load_row(const void *x, bool bf16, long long row_off, bool valid,
+                                         float2 (&r)[D / 2])
+{
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) r[i] = make_float2(0.f, 0.f);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) {
+        float4 t = load4(x, row_off + 4 * i, bf16);
+        r[2 * i] = make_float2(t.x, t.y);
+        r[2 * i + 1] = make_float2(t.z, t.w);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_resp(int N, int K, int H, const void *__restrict__ x, bool x_bf16, const float4 *__restrict__ prm,
+           const float *__restrict__ cst, void *__restrict__ gamma, int ldg, bool g_bf16)
+{
+    using Cfg = RespCfg<D>;
+    constexpr int DP = D / 2, RPT = Cfg::RPT, ROWS = Cfg::ROWS, KT = Cfg::KT;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float4 *prm_s = reinterpret_cast<float4 *>(smem);
+    float *cst_s = reinterpret_cast<float *>(prm_s + KT * DP);
+    float *ell = cst_s + KT;
+    const int LDE = K | 1;
+
+    const long long bh = blockIdx.y;
+    const int h = (int)(bh % H);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row_begin = blockIdx.x * Cfg::ROWS_PER_CTA;
+    const int row_end = min(N, row_begin + Cfg::ROWS_PER_CTA);
+    const int ntiles = (K + KT - 1) / KT;
+    const float4 *prm_h = prm + (long long)h * K * DP;
+    const float *cst_h = cst + (long long)h * K;
+
+    auto load_tile = [&](int t) {
+        const int k0 = t * KT, kn = min(KT, K - k0);
+        for (int i = tid; i < kn * DP; i += kThreads) prm_s[i] = prm_h[(long long)k0 * DP + i];
+        for (int i = tid; i < kn; i += kThreads) cst_s[i] = cst_h[k0 + i];
+    };
+    if (ntiles == 1) load_tile(0);
+
+    for (int r0 = row_begin; r0 < row_end; r0 += ROWS) {
+        float2 xr[RPT][DP];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int row = r0 + lane + 32 * j;
+            load_row<D>(x, x_bf16, (bh * N + row) * D, row < row_end, xr[j]);
+        }
+        for (int t = 0; t < ntiles; ++t) {
+            if (ntiles > 1) {
+                __syncthreads();
+                load_tile(t);
+            }
+            __syncthreads();
+            const int k0 = t * KT, kn = min(KT, K - k0);
+            for (int kk = warp; kk < kn; kk += kThreads / 32) {
+                const float4 *pk = prm_s + kk * DP;
+                float2 acc[RPT][2];
+#pragma unroll
+                for (int j = 0; j < RPT; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int dp = 0; dp < DP; ++dp) {
+                    const float4 p = pk[dp];
+                    const float2 s = make_float2(p.x, p.y), nm = make_float2(p.z, p.w);
+#pragma unroll
+                    for (int j = 0; j < RPT; ++j) {
+                        const float2 y = __ffma2_rn(xr[j][dp], s, nm); // (x - mu) / sigma
+                        acc[j][dp & 1] = __ffma2_rn(y, y, acc[j][dp & 1]);
+                    }
+                }
+                const float c = cst_s[kk];
+#pragma unroll
+                for (int j = 0; j < RPT; ++j) {
+                    const float q = (acc[j][0].x + acc[j][0].y) + (acc[j][1].x + acc[j][1].y);
+                    ell[(lane + 32 * j) * LDE + k0 + kk] = fmaf(-0.5f, q, c);
+                }
+            }
+        }
+        __syncthreads();
+        for (int r = warp; r < ROWS; r += kThreads / 32) {
+            const int row = r0 + r;
+            if (row >= row_end) break;
+            float *er = ell + r * LDE;
+            float m = -FLT_MAX;
+            for (int k = lane; k < K; k += 32) m = fmaxf(m, er[k]);
+            m = warp_max(m);
+            float s = 0.f;
+            for (int k = lane; k < K; k += 32) {
+                const float e = expf(er[k] - m);
+                er[k] = e;
+                s += e;
+            }
+            const float inv = 1.0f / warp_sum(s);
+            const long long go = (bh * N + row) * (long long)ldg;
+            for (int k = lane; k < ldg; k += 32) store_elem(gamma, go + k, k < K ? er[k] * inv : 0.f, g_bf16);
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+cudaError_t launch_resp_d(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
+                          int ldg, bool gamma_bf16, cudaStream_t st)
+{
+    using Cfg = RespCfg<D>;
+    const size_t smem = Cfg::smem(dm.K);
+    static cudaError_t attr = allow_smem(k_resp<D>, Cfg::smem(512));
+    if (attr != cudaSuccess) return attr;
+    dim3 grid((dm.N + Cfg::ROWS_PER_CTA - 1) / Cfg::ROWS_PER_CTA, (unsigned)dm.BH());
+    k_resp<D><<<grid, kThreads, smem, st>>>(dm.N, dm.K, dm.H, x, dm.x_bf16, prm, cst, gamma, ldg, gamma_bf16);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st)
+{
+    k_prep<<<dm.H, kThreads, 0, st>>>(dm.K, dm.D, p.mu, p.var_raw, p.logit_pi, prm, cst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
+                        int ldg, bool gamma_bf16, cudaStream_t st)
+{
+    switch (dm.D) {
+    case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    case 32: return launch_resp_d<32>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    case 64: return launch_resp_d<64>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    case 128: return launch_resp_d<128>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+} // namespace gma

@@ -1,0 +1,164 @@
+/*
+ * libgma — Gaussian Mixture Attention (GMA) forward hot path for one GB300
+ * (sm_103a).  C ABI over caller-owned memory and a CUDA stream.
+ *
+ * The method is the one described by the explainer page "Gaussian Mixture
+ * Attention: Linear-Time Sequence Mixing via Probabilistic Latent Routing"
+ * (technical summary, sections "핵심 메커니즘" and "변형 및 학습"):
+ *
+ *   routing      gamma_{i,k} = p(z = k | x_i) under a K-component GMM with
+ *                means mu_k, diagonal variances sigma_k^2 = softplus(var_raw_k)
+ *                and priors pi = softmax(logit_pi); Q_X and K_X rows share the
+ *                same components (one GMM per head).
+ *   write        Vt = Gamma_K^T V  (K x d_v),  Z = Gamma_K^T 1  (K)
+ *   read         O  = Gamma_Q Vt / (Gamma_Q Z + eps)   (eps added once per row)
+ *   causal       Vt, Z are inclusive prefix sums over positions j <= i; the
+ *                library evaluates them in the chunkwise-parallel form of the
+ *                linear-attention page ("선형 어텐션 원리 정리", section
+ *                "쉽게 이해하기": dense products inside a chunk, a carried state
+ *                between chunks), which is exact, not an approximation.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous, 16-byte aligned (else GMA_ERR_ALIGNMENT).  The library
+ *     never allocates, frees or retains them.
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and is
+ *     asynchronous: the call returns before the GPU finishes.  Launch
+ *     failures are reported as GMA_ERR_CUDA; faults inside a kernel surface
+ *     at the caller's next synchronisation.
+ *   - Arguments are validated on the host before anything is launched; on
+ *     any error nothing is enqueued.  Unsupported sizes return
+ *     GMA_ERR_UNSUPPORTED; nothing falls back to another implementation.
+ *   - `ws` is caller-owned device scratch of at least
+ *     gma_workspace_size(shape, op) bytes (GMA_ERR_WORKSPACE otherwise).  Its
+ *     contents on entry are ignored and on return are unspecified.  Calls
+ *     that run concurrently must use different workspaces.
+ *   - The library keeps no global state; calls are reentrant.
+ *
+ * Supported sizes: d_route in {16, 32, 64, 128}; d_v in {16, 32, 64, 128};
+ * 1 <= K <= 512; B, H, N >= 1 with B*H*N*max(d_route, d_v, K) < 2^40;
+ * causal chunk in {16, 32, 64} (0 selects 64); B*H <= 65535.  N = 0 is
+ * accepted, the sequence pointers may then be NULL, and the call does nothing
+ * (a causal call copies state_in to state_out, or zeroes it).
+ */
+#ifndef GMA_H
+#define GMA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gma_stream_t; /* binary-compatible with cudaStream_t */
+
+typedef enum {
+    GMA_OK = 0,
+    GMA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum value */
+    GMA_ERR_UNSUPPORTED = 2, /* valid but not implemented: d_route, d_v, K or chunk */
+    GMA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
+    GMA_ERR_WORKSPACE = 4,   /* ws is null or smaller than gma_workspace_size() */
+    GMA_ERR_CUDA = 5         /* a CUDA launch or runtime call failed */
+} gma_status;
+
+typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype;
+
+typedef enum {
+    GMA_OP_RESPONSIBILITIES = 0,
+    GMA_OP_BIDIR = 1,
+    GMA_OP_CAUSAL = 2,
+    GMA_OP_DECODE = 3
+} gma_op;
+
+typedef struct {
+    int B, H, N;        /* batch, heads, tokens per sequence (ignored by decode) */
+    int d_route;        /* width of the Q_X / K_X routing rows */
+    int d_v;            /* width of the value rows and of the output */
+    int K;              /* number of Gaussian components per head */
+    int chunk;          /* causal chunk length C; 0 selects 64 */
+    float eps;          /* read-phase stabiliser, added to Gamma_Q Z (>= 0) */
+    gma_dtype x_dtype;  /* storage type of Q_X and K_X */
+    gma_dtype v_dtype;  /* storage type of V */
+    gma_dtype gemm_dtype; /* GMA_F32: chunk products carry fp32 operands (the
+                             1e-4 path); GMA_BF16: Gamma, V and P are rounded to
+                             bf16 as product operands, accumulation stays fp32 */
+} gma_shape;
+
+/* Per-head GMM parameters, fp32 device pointers (one GMM per head, shared by
+ * Q_X and K_X and by every batch element):
+ *   mu       [H, K, d_route]  component means
+ *   var_raw  [H, K, d_route]  raw variances; sigma^2 = softplus(var_raw)
+ *   logit_pi [H, K]           mixture logits;  pi = softmax over K          */
+typedef struct {
+    const float *mu;
+    const float *var_raw;
+    const float *logit_pi;
+} gma_params;
+
+/* Bytes of device scratch that `op` needs for `shape` (0 on invalid input). */
+size_t gma_workspace_size(const gma_shape *shape, gma_op op);
+
+/* Routing step alone (the "probabilistic latent routing" of "핵심 메커니즘"):
+ *   x      [B, H, N, d_route]  routing rows (x_dtype)
+ *   gamma  [B, H, N, K]        fp32 output, each row a probability vector.   */
+gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const void *x,
+                                float *gamma, void *ws, size_t ws_bytes, gma_stream_t stream);
+
+/* Bidirectional forward (write phase then read phase of "핵심 메커니즘"):
+ *   qx, kx [B, H, N, d_route] (x_dtype);  v [B, H, N, d_v] (v_dtype)
+ *   out    [B, H, N, d_v] fp32:  O = Gamma_Q Vt / (Gamma_Q Z + eps).        */
+gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx,
+                             const void *kx, const void *v, float *out, void *ws,
+                             size_t ws_bytes, gma_stream_t stream);
+
+/* Causal forward (prefix-sum variant of "변형 및 학습"): O_i reads the memory
+ * written by positions j <= i.
+ *   qx, kx, v, out  as gma_forward_bidir
+ *   state_in   nullable [B, H, K*d_v + K] fp32: memory left by earlier tokens
+ *              (Vt as K rows of d_v, then Z); NULL means empty.
+ *   state_out  nullable [B, H, K*d_v + K] fp32: memory after the N tokens
+ *              (state_in included).  May alias state_in.                     */
+gma_status gma_forward_causal(const gma_shape *shape, gma_params params, const void *qx,
+                              const void *kx, const void *v, const float *state_in,
+                              float *state_out, float *out, void *ws, size_t ws_bytes,
+                              gma_stream_t stream);
+
+/* One recurrent decode step (the causal form advanced by one token; constant
+ * memory per head as in "선형 어텐션 원리 정리"): the token is written into the
+ * memory first, then its query reads it.
+ *   qx, kx [B, H, d_route] (x_dtype); v [B, H, d_v] (v_dtype)
+ *   state  [B, H, K*d_v + K] fp32, updated in place
+ *   out    [B, H, d_v] fp32.  shape->N is ignored.                          */
+gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void *qx,
+                           const void *kx, const void *v, float *state, float *out, void *ws,
+                           size_t ws_bytes, gma_stream_t stream);
+
+/* Profiling variant of gma_forward_causal, for benchmarks.  It runs exactly
+ * the same launches on `stream`, and records events[i] just before launch i
+ * and events[n_stages] after the last one, so that the caller can time every
+ * kernel of the step with cudaEventElapsedTime.
+ *   prof->events     in:  GMA_PROFILE_MAX_STAGES + 1 cudaEvent_t handles
+ *                         (created by the caller, timing enabled)
+ *   prof->n_stages   out: number of launches of this call
+ *   prof->stage_name out: static, NUL-terminated kernel names (not owned)   */
+#define GMA_PROFILE_MAX_STAGES 8
+typedef struct {
+    void *events[GMA_PROFILE_MAX_STAGES + 1];
+    int n_stages;
+    const char *stage_name[GMA_PROFILE_MAX_STAGES];
+} gma_profile;
+
+gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params, const void *qx,
+                                       const void *kx, const void *v, const float *state_in,
+                                       float *state_out, float *out, void *ws, size_t ws_bytes,
+                                       gma_stream_t stream, gma_profile *prof);
+
+/* Static description of a status code (never NULL). */
+const char *gma_status_string(gma_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_H */

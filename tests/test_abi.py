@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gaussian_mixture_sequence_gb300 import build as gbuild
+from gaussian_mixture_sequence_gb300 import gma
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gma.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gma_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
+            "gma_workspace_size", "gma_status_string"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"libgma.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert gma.gma_status_string(code)
+    assert gma.gma_status_string(99) == "unknown status"
+
+
+def _shape(**kw):
+    base = dict(B=2, H=3, N=100, d_route=64, d_v=64, K=128)
+    base.update(kw)
+    return gma.Shape.make(**base)
+
+
+def test_workspace_size(lib):
+    s = _shape()
+    for op in range(4):
+        assert gma.gma_workspace_size(s, op) > 0
+    assert gma.gma_workspace_size(_shape(d_route=48), gma.OP_CAUSAL) == 0
+    assert gma.gma_workspace_size(_shape(K=513), gma.OP_CAUSAL) == 0
+    assert gma.gma_workspace_size(s, 7) == 0
+    # bf16 product operands halve the responsibility scratch
+    f = gma.gma_workspace_size(_shape(N=4096), gma.OP_CAUSAL)
+    b = gma.gma_workspace_size(_shape(N=4096, gemm_dtype="bf16"), gma.OP_CAUSAL)
+    assert b < f
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails before any launch
+
+
+def _call_causal(lib, shape, ptrs=None, ws_bytes=1 << 40):
+    p = dict(mu=FAKE, var=FAKE, lp=FAKE, q=FAKE, k=FAKE, v=FAKE, si=None, so=None, o=FAKE, ws=FAKE)
+    p.update(ptrs or {})
+    prm = gma._Params(p["mu"], p["var"], p["lp"])
+    sp = ctypes.byref(shape) if shape is not None else None
+    return lib.gma_forward_causal(sp, prm, p["q"], p["k"], p["v"], p["si"], p["so"], p["o"], p["ws"],
+                                  ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d_route=48), 2), (dict(d_v=8), 2), (dict(K=600), 2), (dict(chunk=48), 2),
+    (dict(B=0), 1), (dict(N=-1), 1), (dict(K=0), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
+    (dict(B=300, H=300), 2),
+])
+def test_rejects_bad_shapes(lib, kw, status):
+    assert _call_causal(lib, _shape(**kw)) == status
+
+
+def test_rejects_bad_pointers_and_workspace(lib):
+    s = _shape()
+    assert _call_causal(lib, None) == 1
+    assert _call_causal(lib, s, dict(q=None)) == 1
+    assert _call_causal(lib, s, dict(mu=None)) == 1
+    assert _call_causal(lib, s, dict(q=FAKE + 4)) == 3
+    assert _call_causal(lib, s, dict(si=FAKE + 8)) == 3
+    assert _call_causal(lib, s, dict(ws=None)) == 4
+    need = gma.gma_workspace_size(s, gma.OP_CAUSAL)
+    assert _call_causal(lib, s, ws_bytes=need - 1) == 4
+    bad = gma.Shape.make(2, 3, 100, 64, 64, 128)
+    bad.x_dtype = 5
+    assert _call_causal(lib, bad) == 1
+
+
+def test_empty_sequence_is_a_no_op(lib):
+    # N = 0: nothing to launch for the bidirectional form
+    s = _shape(N=0)
+    prm = gma._Params(FAKE, FAKE, FAKE)
+    assert lib.gma_forward_bidir(ctypes.byref(s), prm, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 0
+    assert lib.gma_responsibilities(ctypes.byref(s), prm, FAKE, FAKE, FAKE, 1 << 30, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gma, "_lib", None)
+    monkeypatch.setattr(gma, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        gma.load()

@@ -1,0 +1,194 @@
+"""GPU parity: the CUDA library, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Tolerance (normwise per (b, h) slice: max|O - O_ref| / max|O_ref|):
+1e-4 when the chunk products carry fp32 operands, 2e-2 when they are bf16
+(accumulation in fp32 either way).  Large workloads are checked on a fixed
+sample of slices at their full sizes, in the launch configuration the
+benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gaussian_mixture_sequence_gb300 import workloads
+from gpu_cases import TOL, Case, normwise
+
+pytestmark = pytest.mark.gpu
+W = workloads.WORKLOADS
+
+
+def _report(name, err, tol):
+    print(f"{name}: normwise error {err:.3e} (tolerance {tol:.0e})")
+    assert err <= tol, f"{name}: {err:.3e} > {tol:.0e}"
+
+
+# ------------------------------------------------------------ S1 --------------
+
+@pytest.mark.parametrize("wl,sample", [
+    (W["tiny"], None),
+    (W["tiny"].with_(K=1, B=2, H=2), None),
+    (W["tiny"].with_(K=3, d=32, N=77), None),
+    (W["tiny"].with_(K=200, d=128, N=300, H=2), None),
+    (W["causal_4k"], 4),
+    (W["bidir_16k_peaked"], 3),
+    (W["causal_8k_K512"], 2),
+    (W["causal_64k_bf16"], 2),
+])
+def test_responsibilities(wl, sample):
+    c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
+    for which in ("q", "k"):
+        g = c.pick(c.gamma(which))
+        ref = c.ref_gamma(which)
+        assert np.abs(g.reshape(ref.shape).sum(-1) - 1).max() < 1e-5
+        _report(f"gamma_{which} {wl.name} K={wl.K}", normwise(g, ref), TOL["f32"])
+
+
+# --------------------------------------------------------- S2 + S3 -------------
+
+@pytest.mark.parametrize("wl,sample", [
+    (W["tiny"].with_(mode="bidir"), None),
+    (W["tiny"].with_(mode="bidir", B=2, H=3, N=1000, d=32, dv=128, K=40), None),
+    (W["tiny"].with_(mode="bidir", N=1, K=16), None),
+    (W["bidir_16k_peaked"], 3),
+    (W["causal_4k"].with_(mode="bidir", gemm_dtype="bf16"), 2),
+])
+def test_bidir(wl, sample):
+    c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
+    out = c.pick(c.bidir())
+    _report(f"bidir {wl.name} N={wl.N} K={wl.K} dv={wl.dv}", normwise(out, c.ref_bidir()),
+            TOL[wl.gemm_dtype])
+
+
+# ------------------------------------------------------------ S4 --------------
+
+CAUSAL = [
+    (W["tiny"], None, 0),
+    (W["tiny"], None, 16),
+    (W["tiny"], None, 32),
+    (W["tiny"].with_(K=1, N=300), None, 0),
+    (W["tiny"].with_(N=1), None, 0),
+    (W["tiny"].with_(B=2, H=3, N=1000, d=32, dv=128, K=40), None, 0),
+    (W["tiny"].with_(N=257, K=24, dv=32), None, 16),
+    (W["causal_4k"], 4, 0),
+    (W["causal_4k_bf16"], 4, 0),
+    (W["causal_16k_peaked"], 3, 0),
+    (W["causal_64k_bf16"], 2, 0),
+    (W["causal_8k_K32"], 2, 0),
+    (W["causal_8k_K64"], 2, 0),
+    (W["causal_8k_K256"], 2, 0),
+    (W["causal_8k_K512"], 2, 0),
+]
+
+
+@pytest.mark.parametrize("wl,sample,chunk", CAUSAL, ids=[f"{w.name}-N{w.N}-K{w.K}-C{c}" for w, _, c in CAUSAL])
+def test_causal(wl, sample, chunk):
+    c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
+    out, st = c.causal(chunk=chunk, want_state=True)
+    ref, ref_st = c.ref_causal(return_state=True)
+    tol = TOL[wl.gemm_dtype]
+    _report(f"causal {wl.name} N={wl.N} K={wl.K} C={chunk}", normwise(c.pick(out), ref), tol)
+    _report(f"causal state {wl.name}", normwise(c.pick(st), ref_st), tol)
+
+
+def test_causal_state_carry():
+    """Two calls chained through state_out -> state_in equal one call on the whole sequence."""
+    wl = W["tiny"].with_(B=2, H=2, N=600, K=32)
+    c = Case(wl)
+    q, k, v = c.dev["seq"]
+    from gaussian_mixture_sequence_gb300 import gma
+    from gpu_cases import shape_of
+    m = 333
+    o1 = torch.empty(wl.B, wl.H, m, wl.dv, device="cuda:0")
+    o2 = torch.empty(wl.B, wl.H, wl.N - m, wl.dv, device="cuda:0")
+    s1 = torch.empty(wl.B, wl.H, wl.K * wl.dv + wl.K, device="cuda:0")
+    s2 = torch.empty_like(s1)
+    gma.gma_forward_causal(shape_of(wl, N=m), *c.prm, q[:, :, :m].contiguous(), k[:, :, :m].contiguous(),
+                           v[:, :, :m].contiguous(), o1, state_out=s1)
+    gma.gma_forward_causal(shape_of(wl, N=wl.N - m), *c.prm, q[:, :, m:].contiguous(),
+                           k[:, :, m:].contiguous(), v[:, :, m:].contiguous(), o2, state_in=s1, state_out=s2)
+    ref, ref_st = c.ref_causal(return_state=True)
+    out = torch.cat([o1, o2], 2)
+    _report("causal split at 333", normwise(c.pick(out), ref), TOL["f32"])
+    _report("causal split state", normwise(c.pick(s2), ref_st), TOL["f32"])
+    # state_out may alias state_in
+    gma.gma_forward_causal(shape_of(wl, N=wl.N - m), *c.prm, q[:, :, m:].contiguous(),
+                           k[:, :, m:].contiguous(), v[:, :, m:].contiguous(), o2, state_in=s1, state_out=s1)
+    assert torch.equal(s1, s2)
+    # an empty sequence passes the state through
+    s3 = torch.full_like(s1, 7.0)
+    e = torch.empty(wl.B, wl.H, 0, wl.dv, device="cuda:0")
+    z = torch.empty(wl.B, wl.H, 0, wl.d, device="cuda:0")
+    gma.gma_forward_causal(shape_of(wl, N=0), *c.prm, z, z, e, e, state_in=s2, state_out=s3)
+    assert torch.equal(s3, s2)
+
+
+def test_causal_prefix_property_bitwise():
+    """Perturbing tokens after position i leaves outputs 0..i bit-identical."""
+    wl = W["tiny"].with_(B=1, H=2, N=700, K=64, d=64, dv=64)
+    c = Case(wl)
+    base = c.causal()
+    q, k, v = c.dev["seq"]
+    for i in (0, 63, 64, 255, 256, 400):
+        c.dev["seq"] = (q.clone(), k.clone(), v.clone())
+        for t in c.dev["seq"]:
+            t[:, :, i + 1:] += 0.5
+        out = c.causal()
+        assert torch.equal(out[:, :, : i + 1], base[:, :, : i + 1]), i
+        assert not torch.equal(out[:, :, i + 1:], base[:, :, i + 1:])
+    c.dev["seq"] = (q, k, v)
+
+
+def test_chunk_size_invariance():
+    wl = W["tiny"].with_(B=1, H=2, N=1000, K=64, d=64, dv=64)
+    c = Case(wl)
+    outs = [c.causal(chunk=ch) for ch in (16, 32, 64)]
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 1e-5 * outs[0].abs().max().item()
+
+
+def test_repeatable_bitwise():
+    wl = W["causal_4k"].with_(B=1, H=2, N=2000)
+    c = Case(wl)
+    a, b = c.causal(), c.causal()
+    assert torch.equal(a, b)
+    x, y = c.bidir(), c.bidir()
+    assert torch.equal(x, y)
+
+
+# ------------------------------------------------------------ S5 --------------
+
+def _decode_run(c, prefill_state):
+    from gaussian_mixture_sequence_gb300 import gma
+    from gpu_cases import shape_of
+    wl = c.wl
+    q, k, v = c.dev["dec"]
+    state = prefill_state.clone()
+    outs = torch.empty(wl.B, wl.H, wl.decode_steps, wl.dv, device="cuda:0")
+    ws = torch.empty(gma.gma_workspace_size(shape_of(wl), gma.OP_DECODE), dtype=torch.uint8,
+                     device="cuda:0")
+    o = torch.empty(wl.B, wl.H, wl.dv, device="cuda:0")
+    qs, ks, vs = (t.permute(2, 0, 1, 3).contiguous() for t in (q, k, v))
+    for t in range(wl.decode_steps):
+        gma.gma_decode_step(shape_of(wl), *c.prm, qs[t], ks[t], vs[t], state, o, ws=ws)
+        outs[:, :, t] = o
+    return outs, state
+
+
+@pytest.mark.parametrize("wl,sample", [
+    (W["decode_b256"].with_(B=2, H=2, N=300, decode_steps=40, K=24, d=16, dv=32), None),
+    (W["decode_b256"], 3),
+])
+def test_decode_after_prefill(wl, sample):
+    c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample), decode=True)
+    _, st = c.causal(want_state=True)
+    outs, final = _decode_run(c, st)
+    _, ref_st = c.ref_causal(return_state=True)
+    q, k, v = c.host["dec"]
+    ref = np.empty((len(c.slices), wl.decode_steps, wl.dv))
+    import oracle
+    for t in range(wl.decode_steps):
+        ref[:, t], ref_st = oracle.decode_step(c.mu, c.vr, c.lp, q[:, t], k[:, t], v[:, t], wl.eps, ref_st,
+                                               heads=c.heads)
+    _report(f"decode {wl.name} B={wl.B}", normwise(c.pick(outs), ref), TOL["f32"])
+    _report(f"decode state {wl.name}", normwise(c.pick(final), ref_st), TOL["f32"])
