@@ -58,30 +58,59 @@ def peaks():
 
 # ----------------------------------------------------------------- work model --
 
-def stage_work(stage, wl):
-    """Algorithmic work of one launch of a stage: (bound, amount, unit-of-amount).
+def eff_chunk(wl):
+    """Chunk length the library uses for this workload (its default when 0)."""
+    if wl.chunk:
+        return wl.chunk
+    tc = wl.K == 128 and (wl.dv == 64 or (wl.dv == 128 and wl.gemm_dtype == "bf16"))
+    return 128 if tc else 64
 
-    Per head-token (ht), with d = d_route, K components, d_v values, chunk C:
-      resp_q / resp_k : 4*K*d flop (one fp32x2 FMA for (x-mu)/sigma, one for the
-                        square-accumulate, per component and feature pair)
-      block_state     : 2*K*(d_v+1) flop  (Gamma_K^T [V | 1])
-      chunk_out       : 4*K*(d_v+1) + 2*C*K + C*(d_v+1) flop (read of the carried
-                        memory, its update, P = Gq Gk^T, lower half of P [V | 1])
-      state_scan      : 2 * 4 * (K*d_v + K) bytes per block (read + write)
-      prep_params     : negligible
+
+def stage_work(stage, wl):
+    """Algorithmic work of one launch of a stage: (flop, pipe, bytes).
+
+    Per head-token (ht), with d = d_route, K components, d_v values, chunk C
+    (flop):
+      resp_q / resp_k     4*K*d on the FP32 pipe (one fp32x2 FMA for (x-mu)/sigma
+                          and one for the square-accumulate, per component and
+                          feature pair)
+      block_state /
+      chunk_state_tc      2*K*(d_v+1)           (Gamma_K^T [V | 1])
+      chunk_out(_tc)      2*C*K + C*(d_v+1) + 2*K*(d_v+1)   (P = Gq Gk^T, lower half
+                          of P [V | 1], read of the carried memory); the CUDA-core
+                          kernel also advances the memory: + 2*K*(d_v+1)
+    Bytes are the minimum each launch must move: its inputs once and its
+    outputs once (fp32 state of K*(d_v+1) per block of the scan).
     """
     ht = wl.B * wl.H * wl.N
-    K, d, dv, C = wl.K, wl.d, wl.dv, wl.chunk
+    K, d, dv = wl.K, wl.d, wl.dv
+    C = eff_chunk(wl)
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    vb = 2 if wl.v_dtype == "bf16" else 4
+    gb = 2 if wl.gemm_dtype == "bf16" else 4
+    st = 4.0 * K * (dv + 1)
+    tc = stage.endswith("_tc")
+    blk = C if tc else 256
+    nblk = wl.B * wl.H * -(-wl.N // blk)
     if stage in ("resp_q", "resp_k"):
-        return "alu", 4.0 * K * d * ht, "flop"
-    if stage == "block_state":
-        return "alu", 2.0 * K * (dv + 1) * ht, "flop"
-    if stage == "chunk_out":
-        return "alu", (4.0 * K * (dv + 1) + 2.0 * C * K + C * (dv + 1)) * ht, "flop"
+        return 4.0 * K * d * ht, "alu", (d * xb + K * gb) * ht
+    if stage in ("block_state", "chunk_state_tc"):
+        return 2.0 * K * (dv + 1) * ht, ("tensor" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
+    if stage in ("chunk_out", "chunk_out_tc"):
+        fl = 2.0 * C * K + C * (dv + 1) + 2.0 * K * (dv + 1) + (0 if tc else 2.0 * K * (dv + 1))
+        return fl * ht, ("tensor" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
     if stage == "state_scan":
-        nblk = -(-wl.N // 256)
-        return "hbm", 2.0 * 4 * (K * dv + K) * nblk * wl.B * wl.H, "byte"
-    return None, 0.0, None
+        return 0.0, "alu", 2.0 * st * nblk
+    return 0.0, "alu", 0.0
+
+
+def pipe_peak(pipe, wl, pk):
+    """Peak of a pipe in flop/s: FP32 lanes x 2 x max SM clock, or the tensor
+    rate of the product operands (tf32 = measured bf16 x 1.1/2.25 nominal ratio)."""
+    if pipe == "alu":
+        return SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
+    bf16 = pk["bf16_tflops"] * 1e12
+    return bf16 if wl.gemm_dtype == "bf16" else bf16 * (1.1 / 2.25)
 
 
 def path_roofline_s(wl, pk):
@@ -93,7 +122,8 @@ def path_roofline_s(wl, pk):
     xb = 2 if wl.x_dtype == "bf16" else 4
     vb = 2 if wl.v_dtype == "bf16" else 4
     t_hbm = ((2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * ht) / (pk["hbm_gbs"] * 1e9)
-    mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * wl.chunk * wl.K + wl.chunk * (wl.dv + 1)) * ht
+    C = eff_chunk(wl)
+    mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * C * wl.K + C * (wl.dv + 1)) * ht
     tf32 = pk["bf16_tflops"] * 1e12 * (1.1 / 2.25)
     t_mma = mma / tf32
     return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)
@@ -346,19 +376,16 @@ def main():
                                        for s in range(args.steps))
     dom = max(stage_ms, key=stage_ms.get)
     pk, pk_kind = peaks()
-    bound, amount, unit = stage_work(dom, wl)
-    if bound == "alu":
-        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
-        achieved = amount / (stage_ms[dom] * 1e-3) / 1e12
-        r_unit = "TFLOP/s"
-    elif bound == "tensor":
-        peak = pk["bf16_tflops"] * (1.1 / 2.25)
-        achieved = amount / (stage_ms[dom] * 1e-3) / 1e12
-        r_unit = "TFLOP/s"
+    flop, pipe, nbytes = stage_work(dom, wl)
+    t_dom = stage_ms[dom] * 1e-3
+    t_flop = flop / pipe_peak(pipe, wl, pk)
+    t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_flop >= t_mem:
+        bound = "alu" if pipe == "alu" else "tensor"
+        achieved, peak, r_unit = flop / t_dom / 1e12, pipe_peak(pipe, wl, pk) / 1e12, "TFLOP/s"
     else:
-        peak = pk["hbm_gbs"]
-        achieved = amount / (stage_ms[dom] * 1e-3) / 1e9
-        r_unit = "GB/s"
+        bound = "hbm"
+        achieved, peak, r_unit = nbytes / t_dom / 1e9, pk["hbm_gbs"], "GB/s"
     roof_s, roof_parts = path_roofline_s(wl, pk)
 
     # end to end through the same public API: pinned host inputs in, result out, every step
@@ -398,13 +425,13 @@ def main():
             "vs_baseline": None, "dtype": "f32" if wl.gemm_dtype == "f32" else "f32+bf16",
             "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d, "d_v": wl.dv,
-                       "K": wl.K, "chunk": wl.chunk, "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
+                       "K": wl.K, "chunk": eff_chunk(wl), "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
                        "inputs": "peaked mixture around the K centres" if wl.dist == "peaked" else "N(0,1)",
                        "l2": "inputs (%.0f MB) larger than L2 (129 MB), no flush" %
                              ((h2d) / 1e6)},
             "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": r_unit,
                          "frac": achieved / peak, "traffic": tr,
-                         "peak_source": ("FP32 lanes x 2 x max SM clock (%s clock)" % pk_kind)
+                         "peak_source": ("152 SMs x 128 FP32 lanes x 2 x max SM clock (%s)" % pk_kind)
                          if bound == "alu" else pk_kind},
             "path_roofline": {"tokens_per_s": tokens / roof_s, "frac": value / world / (tokens / roof_s),
                               **{k2: v2 * 1e3 for k2, v2 in roof_parts.items()}, "unit_ms": True},

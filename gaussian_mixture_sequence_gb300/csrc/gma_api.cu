@@ -16,7 +16,20 @@ struct WsPlan {
 
 bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }
 
-gma_status make_dims(const gma_shape *s, Dims *dm)
+gma_status make_dims_raw(const gma_shape *s, Dims *dm);
+
+// Dims of one operation: only the causal form uses the tensor-core chunking.
+gma_status make_dims(const gma_shape *s, Dims *dm, gma_op op = GMA_OP_CAUSAL)
+{
+    const gma_status st = make_dims_raw(s, dm);
+    if (st == GMA_OK && op != GMA_OP_CAUSAL && dm->C == 128) {
+        dm->C = 64;
+        dm->blk = kBlockRows;
+    }
+    return st;
+}
+
+gma_status make_dims_raw(const gma_shape *s, Dims *dm)
 {
     if (!s) return GMA_ERR_INVALID_ARG;
     if (s->B < 1 || s->H < 1 || s->N < 0 || s->K < 1 || s->d_route < 1 || s->d_v < 1 || s->chunk < 0)
@@ -25,8 +38,9 @@ gma_status make_dims(const gma_shape *s, Dims *dm)
     if ((unsigned)s->x_dtype > 1u || (unsigned)s->v_dtype > 1u || (unsigned)s->gemm_dtype > 1u)
         return GMA_ERR_INVALID_ARG;
     if (!valid_width(s->d_route) || !valid_width(s->d_v) || s->K > 512) return GMA_ERR_UNSUPPORTED;
-    const int C = s->chunk == 0 ? 64 : s->chunk;
-    if (C != 16 && C != 32 && C != 64) return GMA_ERR_UNSUPPORTED;
+    const bool tc = tc_path_eligible(s->K, s->d_v, s->gemm_dtype == GMA_BF16);
+    const int C = s->chunk == 0 ? (tc ? 128 : 64) : s->chunk;
+    if (C != 16 && C != 32 && C != 64 && !(C == 128 && tc)) return GMA_ERR_UNSUPPORTED;
     const long long BH = (long long)s->B * s->H;
     if (BH > 65535) return GMA_ERR_UNSUPPORTED;
     const long long w = s->K > s->d_v ? (s->K > s->d_route ? s->K : s->d_route)
@@ -35,6 +49,7 @@ gma_status make_dims(const gma_shape *s, Dims *dm)
     dm->B = s->B; dm->H = s->H; dm->N = s->N; dm->D = s->d_route; dm->DV = s->d_v; dm->K = s->K;
     dm->KP = (int)round_up(s->K, 8);
     dm->C = C;
+    dm->blk = C == 128 ? 128 : kBlockRows;
     dm->eps = s->eps;
     dm->x_bf16 = s->x_dtype == GMA_BF16;
     dm->v_bf16 = s->v_dtype == GMA_BF16;
@@ -106,7 +121,7 @@ extern "C" {
 size_t gma_workspace_size(const gma_shape *shape, gma_op op)
 {
     Dims dm;
-    if (make_dims(shape, &dm) != GMA_OK || (unsigned)op > 3u) return 0;
+    if ((unsigned)op > 3u || make_dims(shape, &dm, op) != GMA_OK) return 0;
     return plan(dm, op).bytes;
 }
 
@@ -127,7 +142,7 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
                                 void *ws, size_t ws_bytes, gma_stream_t stream)
 {
     Dims dm;
-    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_RESPONSIBILITIES));
     GMA_TRY(check_params(params));
     GMA_TRY(check_ptr(x, dm.N > 0));
     GMA_TRY(check_ptr(gamma, dm.N > 0));
@@ -146,7 +161,7 @@ gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const vo
                              const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
 {
     Dims dm;
-    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_BIDIR));
     GMA_TRY(check_params(params));
     GMA_TRY(check_ptr(qx, dm.N > 0));
     GMA_TRY(check_ptr(kx, dm.N > 0));
@@ -236,12 +251,21 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
     GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
     GMA_CUDA(mk.mark("resp_k"));
     GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
-    GMA_CUDA(mk.mark("block_state"));
-    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
-    GMA_CUDA(mk.mark("state_scan"));
-    GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
-    GMA_CUDA(mk.mark("chunk_out"));
-    GMA_CUDA(launch_chunk_out(dm, true, gq, gk, v, partial, out, st));
+    if (tc_path_applies(dm)) {
+        GMA_CUDA(mk.mark("chunk_state_tc"));
+        GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
+        GMA_CUDA(mk.mark("state_scan"));
+        GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
+        GMA_CUDA(mk.mark("chunk_out_tc"));
+        GMA_CUDA(launch_chunk_out_tc(dm, gq, gk, v, partial, out, st));
+    } else {
+        GMA_CUDA(mk.mark("block_state"));
+        GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+        GMA_CUDA(mk.mark("state_scan"));
+        GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
+        GMA_CUDA(mk.mark("chunk_out"));
+        GMA_CUDA(launch_chunk_out(dm, true, gq, gk, v, partial, out, st));
+    }
     GMA_CUDA(mk.finish());
     return GMA_OK;
 }
@@ -271,7 +295,7 @@ gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void
                            gma_stream_t stream)
 {
     Dims dm;
-    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_DECODE));
     GMA_TRY(check_params(params));
     GMA_TRY(check_ptr(qx));
     GMA_TRY(check_ptr(kx));

@@ -23,11 +23,12 @@ constexpr int kBlockRows = 256;   // rows per block of the block-state / causal-
 
 struct Dims {
     int B, H, N, D, DV, K, KP, C;
+    int blk;   // rows per block of the memory scan (kBlockRows, or C on the tensor-core path)
     float eps;
     bool x_bf16, v_bf16, g_bf16;
     long long BH() const { return (long long)B * H; }
     long long state_size() const { return (long long)K * DV + K; }
-    int nblk() const { return (N + kBlockRows - 1) / kBlockRows; }
+    int nblk() const { return (N + blk - 1) / blk; }
 };
 
 __host__ __device__ constexpr inline long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
@@ -72,6 +73,13 @@ cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const 
                              float *states, float *out, cudaStream_t st);
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
                           const void *kx, const void *v, float *state, float *out, cudaStream_t st);
+
+// Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
+bool tc_path_eligible(int K, int DV, bool g_bf16);
+bool tc_path_applies(const Dims &dm);
+cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v, float *partial, cudaStream_t st);
+cudaError_t launch_chunk_out_tc(const Dims &dm, const void *gq, const void *gk, const void *v, const float *states,
+                                float *out, cudaStream_t st);
 
 // Sets the dynamic shared-memory limit of a kernel once per process.
 template <typename Kern>

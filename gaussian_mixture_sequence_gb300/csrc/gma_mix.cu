@@ -87,8 +87,20 @@ __global__ void __launch_bounds__(kThreads) k_scan(long long SZ, int nblk, float
     if (e >= SZ) return;
     const long long bh = blockIdx.y;
     float run = state_in ? state_in[bh * SZ + e] : 0.f;
-    float *p = partial + bh * nblk * SZ + e;
-    for (int b = 0; b < nblk; ++b) {
+    float *__restrict__ p = partial + bh * nblk * SZ + e;
+    constexpr int U = 8; // loads in flight per thread
+    int b = 0;
+    for (; b + U <= nblk; b += U) {
+        float t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) t[u] = p[(long long)(b + u) * SZ];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (exclusive) p[(long long)(b + u) * SZ] = run;
+            run += t[u];
+        }
+    }
+    for (; b < nblk; ++b) {
         const float t = p[(long long)b * SZ];
         if (exclusive) p[(long long)b * SZ] = run;
         run += t;

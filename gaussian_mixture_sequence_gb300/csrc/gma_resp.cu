@@ -83,43 +83,35 @@ __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__
 }
 
 // Responsibilities of a range of rows of one (b, h) slice.
-//   RPT rows per thread (lane, lane + 32, ...): ROWS = 32 * RPT rows per tile.
-//   Each warp owns components k = warp, warp + 8, ... of the current component
+//   Lanes: HALVES lanes share a routing row, each holding DH = D / HALVES of
+//   its features (interleaved in pairs, so that the lanes of a row read
+//   neighbouring 16-byte parameter words: no bank conflicts); a thread holds
+//   RPT = 2 rows.  The partial quadratic forms of a row are combined with
+//   shuffles.  Each warp owns a set of components of the current parameter
 //   tile (parameters broadcast from shared memory); the log-joint l_ik goes to
 //   a shared [ROWS][K|1] tile and a warp per row then normalises it.
 template <int D>
 struct RespCfg {
-    static constexpr int RPT = D <= 64 ? 2 : 1;
-    static constexpr int ROWS = 32 * RPT;
-    static constexpr int KT = D == 128 ? 64 : 128; // components per parameter tile
+    static constexpr int HALVES = D >= 64 ? D / 32 : 1;        // lanes per row
+    static constexpr int DH = D / HALVES;                      // features per lane
+    static constexpr int RPT = 2;                              // rows per thread
+    static constexpr int WROWS = 32 / HALVES * RPT;            // rows per warp
+    static constexpr int ROWS = 64;                            // rows per tile
+    static constexpr int GROUPS = ROWS / WROWS;                // warp groups per tile
+    static constexpr int WPG = (kThreads / 32) / GROUPS;       // warps per group
+    static constexpr int KT = D == 128 ? 64 : 128;             // components per parameter tile
     static constexpr int ROWS_PER_CTA = 256;
     static size_t smem(int K) { return (size_t)KT * (D / 2) * 16 + KT * 4 + (size_t)ROWS * (K | 1) * 4; }
 };
 
 template <int D>
-__device__ __forceinline__ void load_row(const void *x, bool bf16, long long row_off, bool valid,
-                                         float2 (&r)[D / 2])
-{
-    if (!valid) {
-#pragma unroll
-        for (int i = 0; i < D / 2; ++i) r[i] = make_float2(0.f, 0.f);
-        return;
-    }
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-        float4 t = load4(x, row_off + 4 * i, bf16);
-        r[2 * i] = make_float2(t.x, t.y);
-        r[2 * i + 1] = make_float2(t.z, t.w);
-    }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_resp(int N, int K, int H, const void *__restrict__ x, bool x_bf16, const float4 *__restrict__ prm,
            const float *__restrict__ cst, void *__restrict__ gamma, int ldg, bool g_bf16)
 {
     using Cfg = RespCfg<D>;
-    constexpr int DP = D / 2, RPT = Cfg::RPT, ROWS = Cfg::ROWS, KT = Cfg::KT;
+    constexpr int DP = D / 2, HALVES = Cfg::HALVES, DH = Cfg::DH, RPT = Cfg::RPT, ROWS = Cfg::ROWS,
+                  KT = Cfg::KT, WPG = Cfg::WPG;
     extern __shared__ __align__(16) unsigned char smem[];
     float4 *prm_s = reinterpret_cast<float4 *>(smem);
     float *cst_s = reinterpret_cast<float *>(prm_s + KT * DP);
@@ -129,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long bh = blockIdx.y;
     const int h = (int)(bh % H);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int half = lane % HALVES, slot = lane / HALVES;
+    const int group = warp / WPG, wig = warp % WPG;
     const int row_begin = blockIdx.x * Cfg::ROWS_PER_CTA;
     const int row_end = min(N, row_begin + Cfg::ROWS_PER_CTA);
     const int ntiles = (K + KT - 1) / KT;
@@ -143,11 +137,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ntiles == 1) load_tile(0);
 
     for (int r0 = row_begin; r0 < row_end; r0 += ROWS) {
-        float2 xr[RPT][DP];
+        // this thread's rows (tile-local) and its feature pairs 2 * (dp * HALVES + half) + {0, 1}
+        int lrow[RPT];
+        float2 xr[RPT][DH / 2];
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
-            const int row = r0 + lane + 32 * j;
-            load_row<D>(x, x_bf16, (bh * N + row) * D, row < row_end, xr[j]);
+            lrow[j] = group * Cfg::WROWS + slot + j * (32 / HALVES);
+            const int row = r0 + lrow[j];
+            const long long off = (bh * N + row) * D;
+#pragma unroll
+            for (int dp = 0; dp < DH / 2; ++dp) {
+                const int f = 2 * (dp * HALVES + half);
+                if (row < row_end) {
+                    if (x_bf16) {
+                        const uint32_t u =
+                            *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(x) + off + f);
+                        xr[j][dp] = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+                    } else {
+                        xr[j][dp] = *reinterpret_cast<const float2 *>(static_cast<const float *>(x) + off + f);
+                    }
+                } else {
+                    xr[j][dp] = make_float2(0.f, 0.f);
+                }
+            }
         }
         for (int t = 0; t < ntiles; ++t) {
             if (ntiles > 1) {
@@ -156,26 +168,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncthreads();
             const int k0 = t * KT, kn = min(KT, K - k0);
-            for (int kk = warp; kk < kn; kk += kThreads / 32) {
-                const float4 *pk = prm_s + kk * DP;
+            for (int kk = wig; kk < kn; kk += WPG) {
+                const float4 *pk = prm_s + kk * DP + half;
                 float2 acc[RPT][2];
 #pragma unroll
                 for (int j = 0; j < RPT; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int dp = 0; dp < DP; ++dp) {
-                    const float4 p = pk[dp];
-                    const float2 s = make_float2(p.x, p.y), nm = make_float2(p.z, p.w);
+                for (int dp = 0; dp < DH / 2; ++dp) {
+                    const float4 p = pk[dp * HALVES];
+                    const float2 sc = make_float2(p.x, p.y), nm = make_float2(p.z, p.w);
 #pragma unroll
                     for (int j = 0; j < RPT; ++j) {
-                        const float2 y = __ffma2_rn(xr[j][dp], s, nm); // (x - mu) / sigma
+                        const float2 y = __ffma2_rn(xr[j][dp], sc, nm); // (x - mu) / sigma
                         acc[j][dp & 1] = __ffma2_rn(y, y, acc[j][dp & 1]);
                     }
                 }
                 const float c = cst_s[kk];
 #pragma unroll
                 for (int j = 0; j < RPT; ++j) {
-                    const float q = (acc[j][0].x + acc[j][0].y) + (acc[j][1].x + acc[j][1].y);
-                    ell[(lane + 32 * j) * LDE + k0 + kk] = fmaf(-0.5f, q, c);
+                    float q = (acc[j][0].x + acc[j][0].y) + (acc[j][1].x + acc[j][1].y);
+#pragma unroll
+                    for (int o = 1; o < HALVES; o <<= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                    if (half == 0) ell[lrow[j] * LDE + k0 + kk] = fmaf(-0.5f, q, c);
                 }
             }
         }

@@ -53,7 +53,7 @@ class Workload:
     v_dtype: str = "f32"      # storage of V
     gemm_dtype: str = "f32"   # chunk-product operand precision: "f32" or "bf16"
     dist: str = "normal"      # "normal" or "peaked"
-    chunk: int = 64
+    chunk: int = 0            # causal chunk length; 0 = the library's default
     decode_steps: int = 0     # decode workloads: steps after an N-token prefill
     seed: int = 1000
 

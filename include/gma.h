@@ -37,7 +37,7 @@
  *
  * Supported sizes: d_route in {16, 32, 64, 128}; d_v in {16, 32, 64, 128};
  * 1 <= K <= 512; B, H, N >= 1 with B*H*N*max(d_route, d_v, K) < 2^40;
- * causal chunk in {16, 32, 64} (0 selects 64); B*H <= 65535.  N = 0 is
+ * causal chunk as described in gma_shape; B*H <= 65535.  N = 0 is
  * accepted, the sequence pointers may then be NULL, and the call does nothing
  * (a causal call copies state_in to state_out, or zeroes it).
  */
@@ -76,7 +76,10 @@ typedef struct {
     int d_route;        /* width of the Q_X / K_X routing rows */
     int d_v;            /* width of the value rows and of the output */
     int K;              /* number of Gaussian components per head */
-    int chunk;          /* causal chunk length C; 0 selects 64 */
+    int chunk;          /* causal chunk length C in {16, 32, 64, 128}; 0 selects
+                           128 where the tensor-core path applies (K = 128 and
+                           d_v = 64, or d_v = 128 with bf16 products), else 64;
+                           128 is accepted only there */
     float eps;          /* read-phase stabiliser, added to Gamma_Q Z (>= 0) */
     gma_dtype x_dtype;  /* storage type of Q_X and K_X */
     gma_dtype v_dtype;  /* storage type of V */

@@ -71,7 +71,13 @@ CAUSAL = [
     (W["tiny"].with_(B=2, H=3, N=1000, d=32, dv=128, K=40), None, 0),
     (W["tiny"].with_(N=257, K=24, dv=32), None, 16),
     (W["causal_4k"], 4, 0),
+    (W["causal_4k"], 2, 64),
     (W["causal_4k_bf16"], 4, 0),
+    (W["causal_4k_bf16"], 2, 64),
+    (W["tiny"].with_(B=2, H=2, N=1000, d=64, dv=64, K=128), None, 0),
+    (W["tiny"].with_(B=1, H=2, N=129, d=16, dv=64, K=128), None, 0),
+    (W["tiny"].with_(B=1, H=1, N=1, d=64, dv=64, K=128), None, 0),
+    (W["tiny"].with_(B=1, H=2, N=700, d=32, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     (W["causal_16k_peaked"], 3, 0),
     (W["causal_64k_bf16"], 2, 0),
     (W["causal_8k_K32"], 2, 0),
@@ -123,13 +129,14 @@ def test_causal_state_carry():
     assert torch.equal(s3, s2)
 
 
-def test_causal_prefix_property_bitwise():
+@pytest.mark.parametrize("K", [64, 128])
+def test_causal_prefix_property_bitwise(K):
     """Perturbing tokens after position i leaves outputs 0..i bit-identical."""
-    wl = W["tiny"].with_(B=1, H=2, N=700, K=64, d=64, dv=64)
+    wl = W["tiny"].with_(B=1, H=2, N=700, K=K, d=64, dv=64)
     c = Case(wl)
     base = c.causal()
     q, k, v = c.dev["seq"]
-    for i in (0, 63, 64, 255, 256, 400):
+    for i in (0, 63, 64, 127, 128, 255, 256, 400):
         c.dev["seq"] = (q.clone(), k.clone(), v.clone())
         for t in c.dev["seq"]:
             t[:, :, i + 1:] += 0.5
@@ -139,10 +146,13 @@ def test_causal_prefix_property_bitwise():
     c.dev["seq"] = (q, k, v)
 
 
-def test_chunk_size_invariance():
-    wl = W["tiny"].with_(B=1, H=2, N=1000, K=64, d=64, dv=64)
+@pytest.mark.parametrize("K,chunks", [(64, (16, 32, 64)), (128, (16, 64, 128))])
+def test_chunk_size_invariance(K, chunks):
+    """The chunkwise form is exact: chunk lengths (and the tensor-core path at
+    chunk 128 against the CUDA-core path at 16/64) agree to rounding."""
+    wl = W["tiny"].with_(B=1, H=2, N=1000, K=K, d=64, dv=64)
     c = Case(wl)
-    outs = [c.causal(chunk=ch) for ch in (16, 32, 64)]
+    outs = [c.causal(chunk=ch) for ch in chunks]
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() <= 1e-5 * outs[0].abs().max().item()
 
@@ -151,6 +161,8 @@ def test_repeatable_bitwise():
     wl = W["causal_4k"].with_(B=1, H=2, N=2000)
     c = Case(wl)
     a, b = c.causal(), c.causal()
+    assert torch.equal(a, b)
+    a, b = c.causal(chunk=64), c.causal(chunk=64)
     assert torch.equal(a, b)
     x, y = c.bidir(), c.bidir()
     assert torch.equal(x, y)
