@@ -6,6 +6,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 using namespace gma;
 
 namespace {
@@ -313,3 +315,57 @@ gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void
 }
 
 } // extern "C"
+
+// ---- decode step whose scratch is a file-scope device array ----------------
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[GMA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_noalloc_once[kMaxDevices];
+void *g_noalloc_addr[kMaxDevices];
+cudaError_t g_noalloc_err[kMaxDevices];
+
+// Device address of the array on the current device.  In host code the
+// array's name only stands in for it, so the address is looked up once per
+// device, with that device current.
+gma_status noalloc_scratch(void **addr)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GMA_ERR_UNSUPPORTED;
+    std::call_once(g_noalloc_once[dev], [dev] {
+        void *p = nullptr;
+        g_noalloc_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        g_noalloc_addr[dev] = p;
+    });
+    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_addr[dev]) return GMA_ERR_CUDA;
+    *addr = g_noalloc_addr[dev];
+    return GMA_OK;
+}
+
+} // namespace
+
+extern "C" gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params params, const void *qx,
+                                              const void *kx, const void *v, float *state, float *out,
+                                              gma_stream_t stream)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_DECODE));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx));
+    GMA_TRY(check_ptr(kx));
+    GMA_TRY(check_ptr(v));
+    GMA_TRY(check_ptr(state));
+    GMA_TRY(check_ptr(out));
+    const WsPlan wp = plan(dm, GMA_OP_DECODE);
+    if (wp.bytes > GMA_NOALLOC_SCRATCH_BYTES) return GMA_ERR_WORKSPACE;
+    void *ws = nullptr;
+    GMA_TRY(noalloc_scratch(&ws));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
+    return GMA_OK;
+}

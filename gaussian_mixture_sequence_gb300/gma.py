@@ -81,10 +81,11 @@ def load():
         lib.gma_forward_bidir.argtypes = [S, _Params, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_forward_causal.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_decode_step.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.gma_decode_step_noalloc.argtypes = [S, _Params, P, P, P, P, P, P]
         lib.gma_forward_causal_profiled.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P,
                                                     ctypes.POINTER(Profile)]
         for fn in ("gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
-                   "gma_forward_causal_profiled"):
+                   "gma_forward_causal_profiled", "gma_decode_step_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -230,4 +231,26 @@ def gma_decode_step(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, state, out, 
     wp, wn = _ws(s, OP_DECODE, ws, dev)
     _check("gma_decode_step",
            load().gma_decode_step(ctypes.byref(s), prm, q, k, vv, st, o, wp, wn, _stream(dev, stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def gma_decode_step_noalloc(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, state, out, stream=None):
+    """gma_decode_step without a workspace: for callers that cannot allocate
+    device memory.  The library keeps the step's scratch in a fixed device
+    array of NOALLOC_SCRATCH_BYTES on every GPU that loads it; shapes that
+    need more raise GMAError (status 4).  Calls must not overlap on the GPU."""
+    dev = qx.device
+    s = shape
+    xdt, vdt = _TORCH_DT[s.x_dtype], _TORCH_DT[s.v_dtype]
+    q = _ptr(qx, "qx", (s.B, s.H, s.d_route), xdt, dev)
+    k = _ptr(kx, "kx", (s.B, s.H, s.d_route), xdt, dev)
+    vv = _ptr(v, "v", (s.B, s.H, s.d_v), vdt, dev)
+    st = _ptr(state, "state", (s.B, s.H, s.K * s.d_v + s.K), torch.float32, dev)
+    o = _ptr(out, "out", (s.B, s.H, s.d_v), torch.float32, dev)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    _check("gma_decode_step_noalloc",
+           load().gma_decode_step_noalloc(ctypes.byref(s), prm, q, k, vv, st, o, _stream(dev, stream)))
     return out

@@ -157,6 +157,34 @@ gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params
                                        float *state_out, float *out, void *ws, size_t ws_bytes,
                                        gma_stream_t stream, gma_profile *prof);
 
+/* Decode step for callers that cannot allocate device memory.
+ *
+ * No counterpart in the paper: this is a deployment convenience.  Some hosts
+ * cannot call cudaMalloc at the point where they run a decode step: plugins
+ * whose host application owns every device allocation, code held to a fixed
+ * memory budget, or loops that must not take the allocator's latency or
+ * failure modes.  This entry point computes exactly what gma_decode_step
+ * computes, with the same arguments minus the workspace, and allocates
+ * nothing: its scratch (the per-head parameters prepared for the step) lives
+ * in a file-scope device array of GMA_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU which loads the library holds until the process exits.
+ *   - The scratch of the calling thread's current device is used.  The
+ *     first call on a device looks up the array's device address (once per
+ *     device); make that first call before any stream capture.
+ *   - Shapes whose scratch would exceed GMA_NOALLOC_SCRATCH_BYTES, i.e.
+ *     256-byte-rounded H*K*d_route*8 plus 256-byte-rounded H*K*4, are
+ *     rejected with GMA_ERR_WORKSPACE and nothing is launched.
+ *   - Every call shares the one array.  Calls whose work overlaps on the GPU
+ *     (for example on two streams without ordering between them) race on it
+ *     and give undefined results; order them.  Each call rewrites the whole
+ *     part of the array it reads, so no clearing is needed between calls.
+ * All other arguments, layouts and errors are those of gma_decode_step.     */
+#define GMA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params params, const void *qx,
+                                   const void *kx, const void *v, float *state, float *out,
+                                   gma_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *gma_status_string(gma_status status);
 
