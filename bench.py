@@ -79,16 +79,24 @@ def stage_work(stage, wl):
       chunk_out(_tc)      2*C*K + C*(d_v+1) + 2*K*(d_v+1)   (P = Gq Gk^T, lower half
                           of P [V | 1], read of the carried memory); the CUDA-core
                           kernel also advances the memory: + 2*K*(d_v+1)
+      bidir_read          2*K*(d_v+1)           (Gq [Vt | Z])
+      decode (per (b,h))  8*K*d + 4*K*(d_v+1)   (two routings, update and read)
     Bytes are the minimum each launch must move: its inputs once and its
-    outputs once (fp32 state of K*(d_v+1) per block of the scan).
+    outputs once (fp32 state of K*(d_v+1) per block of the scan; for the
+    decode step the whole state in and out).
     """
-    ht = wl.B * wl.H * wl.N
     K, d, dv = wl.K, wl.d, wl.dv
-    C = eff_chunk(wl)
     xb = 2 if wl.x_dtype == "bf16" else 4
     vb = 2 if wl.v_dtype == "bf16" else 4
     gb = 2 if wl.gemm_dtype == "bf16" else 4
     st = 4.0 * K * (dv + 1)
+    if wl.mode == "decode":
+        bh = wl.B * wl.H
+        if stage == "decode":
+            return (8.0 * K * d + 4.0 * K * (dv + 1)) * bh, "alu", (2 * st + 2 * d * xb + dv * vb + 4 * dv) * bh
+        return 0.0, "alu", 0.0
+    ht = wl.B * wl.H * wl.N
+    C = eff_chunk(wl)
     tc = stage.endswith("_tc")
     blk = C if tc else 256
     nblk = wl.B * wl.H * -(-wl.N // blk)
@@ -99,7 +107,9 @@ def stage_work(stage, wl):
     if stage in ("chunk_out", "chunk_out_tc"):
         fl = 2.0 * C * K + C * (dv + 1) + 2.0 * K * (dv + 1) + (0 if tc else 2.0 * K * (dv + 1))
         return fl * ht, ("tensor" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
-    if stage == "state_scan":
+    if stage == "bidir_read":
+        return 2.0 * K * (dv + 1) * ht, "alu", (K * gb + 4 * dv) * ht + st * nblk
+    if stage in ("state_scan", "state_reduce"):
         return 0.0, "alu", 2.0 * st * nblk
     return 0.0, "alu", 0.0
 
@@ -114,19 +124,32 @@ def pipe_peak(pipe, wl, pk):
 
 
 def path_roofline_s(wl, pk):
-    """Roofline time of the whole step: max(FP32 time of the routing, HBM time of
-    the minimum traffic, tensor time of the chunk products at the tf32 rate)."""
-    ht = wl.B * wl.H * wl.N
+    """Roofline time of one step: max(FP32 time of the routing, HBM time of the
+    minimum traffic, tensor time of the memory products)."""
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
-    t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     xb = 2 if wl.x_dtype == "bf16" else 4
     vb = 2 if wl.v_dtype == "bf16" else 4
+    if wl.mode == "decode":
+        bh = wl.B * wl.H
+        t_alu = (8.0 * wl.K * wl.d + 4.0 * wl.K * (wl.dv + 1)) * bh / fp32_peak
+        t_hbm = (8.0 * wl.K * (wl.dv + 1) + 2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * bh / (pk["hbm_gbs"] * 1e9)
+        return max(t_alu, t_hbm), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=0.0)
+    ht = wl.B * wl.H * wl.N
+    t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     t_hbm = ((2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * ht) / (pk["hbm_gbs"] * 1e9)
     C = eff_chunk(wl)
-    mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * C * wl.K + C * (wl.dv + 1)) * ht
-    tf32 = pk["bf16_tflops"] * 1e12 * (1.1 / 2.25)
-    t_mma = mma / tf32
+    if wl.mode == "bidir":
+        mma = 4.0 * wl.K * (wl.dv + 1) * ht
+    else:
+        mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * C * wl.K + C * (wl.dv + 1)) * ht
+    tens = pk["bf16_tflops"] * 1e12 * (1.0 if wl.gemm_dtype == "bf16" else 1.1 / 2.25)
+    t_mma = mma / tens
     return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)
+
+
+def tokens_per_step(wl):
+    """Tokens (all H heads of a position) one step processes."""
+    return wl.B if wl.mode == "decode" else wl.B * wl.N
 
 
 # ----------------------------------------------------------------- clocks -----
@@ -216,23 +239,55 @@ def source_hash():
     return m.hexdigest()[:16]
 
 
-def cpu_baseline(wl, inputs_np, threads=None):
+def _oracle_call(wl, mu, vr, lp, q, k, v, heads):
+    """The oracle's form of the workload on [S, n, .] slices (decode: one step per slice)."""
+    import numpy as np
+    import oracle
+    if wl.mode == "bidir":
+        return oracle.bidir(mu, vr, lp, q, k, v, wl.eps, heads=heads)
+    if wl.mode == "decode":
+        S = q.shape[0]
+        state = np.ones((S, wl.K * wl.dv + wl.K))
+        return oracle.decode_step(mu, vr, lp, q[:, 0], k[:, 0], v[:, 0], wl.eps, state, heads=heads)
+    return oracle.causal(mu, vr, lp, q, k, v, wl.eps, heads=heads)
+
+
+def _host_slices(wl, S, n):
+    """Seeded inputs of the first S (b, h) slices, first n tokens, as [S, n, .] arrays."""
+    import numpy as np
+    from gaussian_mixture_sequence_gb300 import workloads
+    mu, vr, lp = workloads.params(wl)
+    qs, ks, vs = [], [], []
+    for s_ in range(S):
+        b, h = divmod(s_, wl.H)
+        q, k, v = workloads.slice_inputs(wl.with_(N=n), b, h, mu=mu)
+        qs.append(q); ks.append(k); vs.append(v)
+    return mu, vr, lp, np.stack(qs), np.stack(ks), np.stack(vs)
+
+
+def cpu_baseline(wl):
     """The fp64 oracle as it stands, on a bounded sample of the same workload."""
     import oracle
-    q, k, v, mu, vr, lp = inputs_np
-    nthr = oracle.max_threads() if threads is None else threads
-    S = min(wl.B * wl.H, max(8, nthr))
-    sl = list(range(S))
-    qs = q.reshape(wl.B * wl.H, wl.N, -1)[sl]
-    ks = k.reshape(wl.B * wl.H, wl.N, -1)[sl]
-    vs = v.reshape(wl.B * wl.H, wl.N, -1)[sl]
+    nthr = oracle.max_threads()
+    if wl.mode == "decode":
+        S, n = min(wl.B * wl.H, 1024 * max(1, nthr)), 1
+    else:
+        S, n = min(wl.B * wl.H, max(8, nthr)), wl.N
+    mu, vr, lp, q, k, v = _host_slices(wl, S, n)
+    heads = [s_ % wl.H for s_ in range(S)]
     t0 = time.perf_counter()
-    oracle.causal(mu, vr, lp, qs, ks, vs, wl.eps, heads=[s % wl.H for s in sl])
-    dt = time.perf_counter() - t0
-    tokens = S * wl.N / wl.H
+    reps = 0
+    while True:
+        _oracle_call(wl, mu, vr, lp, q, k, v, heads)
+        reps += 1
+        if wl.mode != "decode" or time.perf_counter() - t0 > 2.0:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    tokens = S * n / wl.H
+    what = "one decode step of" if wl.mode == "decode" else f"the full length N={wl.N} of"
     return {"value": tokens / dt, "unit": "tokens/s", "cores": min(nthr, S), "kind": "oracle",
-            "sample": f"{S} of {wl.B * wl.H} (batch, head) sequences of workload {wl.name}, full length "
-                      f"N={wl.N} (= {tokens:.0f} tokens of H={wl.H} heads), fp64, {dt:.2f} s wall"}
+            "sample": f"{what} {S} of {wl.B * wl.H} (batch, head) sequences of workload {wl.name} "
+                      f"(= {tokens:.0f} tokens of H={wl.H} heads), fp64, {dt:.3f} s wall per pass"}
 
 
 # ----------------------------------------------------------------- reference --
@@ -240,41 +295,120 @@ def cpu_baseline(wl, inputs_np, threads=None):
 def run_reference(args, wl, world, rank):
     if rank != 0:
         return
-    import numpy as np
     import oracle
-    from gaussian_mixture_sequence_gb300 import workloads
-    mu, vr, lp = workloads.params(wl)
     nthr = oracle.max_threads()
-    S = min(wl.B * wl.H, max(1, nthr))
-    slices = [workloads.slice_inputs(wl, s // wl.H, s % wl.H, mu=mu) for s in range(S)]
-    q = np.stack([x[0] for x in slices]); k = np.stack([x[1] for x in slices]); v = np.stack([x[2] for x in slices])
-    heads = [s % wl.H for s in range(S)]
-    # size one step (a prefix of n tokens of S sequences) so that the whole run stays near 2 minutes
-    n = 256
-    t0 = time.perf_counter()
-    oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
-    per_tok = (time.perf_counter() - t0) / n
-    total = args.steps + args.warmup
-    n = int(max(64, min(wl.N, 120.0 / total / max(per_tok, 1e-9))))
+    S = min(wl.B * wl.H, max(1, nthr) * (256 if wl.mode == "decode" else 1))
+    heads = [s_ % wl.H for s_ in range(S)]
+    if wl.mode == "decode":
+        n = 1
+    else:
+        # size one step (a prefix of n tokens of S sequences) so that the whole run stays near 2 minutes
+        mu, vr, lp, q, k, v = _host_slices(wl, S, 256)
+        t0 = time.perf_counter()
+        _oracle_call(wl, mu, vr, lp, q, k, v, heads)
+        per_tok = (time.perf_counter() - t0) / 256
+        n = int(max(64, min(wl.N, 120.0 / (args.steps + args.warmup) / max(per_tok, 1e-9))))
+    mu, vr, lp, q, k, v = _host_slices(wl, S, n)
     for _ in range(args.warmup):
-        oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
+        _oracle_call(wl, mu, vr, lp, q, k, v, heads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.causal(mu, vr, lp, q[:, :n], k[:, :n], v[:, :n], wl.eps, heads=heads)
+        _oracle_call(wl, mu, vr, lp, q, k, v, heads)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     tokens = S * n / wl.H
     val = tokens / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC if wl.mode == "causal" else f"GMA {wl.mode} tokens/sec",
+        "value": val, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d, "d_v": wl.dv,
-                   "K": wl.K, "chunk": wl.chunk},
+                   "K": wl.K, "chunk": eff_chunk(wl)},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": min(nthr, S), "kind": "oracle",
                          "sample": f"each step: first {n} tokens of {S} (batch, head) sequences of {wl.name}"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- runners ----
+
+class Runner:
+    """Device inputs of one workload and its profiled / plain step.
+
+    Causal and bidirectional workloads use the seeded host generator (the same
+    inputs the oracle sees); the decode workload draws its prefill and tokens
+    on the device with a seeded torch generator (4 GB per tensor at batch 256
+    would take minutes on the host) and builds the state with one causal
+    prefill through the library."""
+
+    def __init__(self, wl, dev, seed):
+        import torch
+        from gaussian_mixture_sequence_gb300 import gma, workloads
+        self.wl, self.dev, self.gma = wl, dev, gma
+        tdt = lambda s_: torch.bfloat16 if s_ == "bf16" else torch.float32
+        mu, vr, lp = workloads.params(wl, seed)
+        self.prm = tuple(torch.from_numpy(a).to(dev) for a in (mu, vr, lp))
+        self.shape = gma.Shape.make(wl.B, wl.H, wl.N, wl.d, wl.dv, wl.K, chunk=wl.chunk, eps=wl.eps,
+                                    x_dtype=wl.x_dtype, v_dtype=wl.v_dtype, gemm_dtype=wl.gemm_dtype)
+        if wl.mode == "decode":
+            g = torch.Generator(device=dev).manual_seed(seed)
+            shp = lambda w: (wl.B, wl.H, wl.N, w)
+            q, k, v = (torch.randn(*shp(w), device=dev, generator=g).to(tdt(t))
+                       for w, t in ((wl.d, wl.x_dtype), (wl.d, wl.x_dtype), (wl.dv, wl.v_dtype)))
+            self.state0 = torch.empty(wl.B, wl.H, wl.K * wl.dv + wl.K, device=dev)
+            gma.gma_forward_causal(self.shape, *self.prm, q, k, v, torch.empty(shp(wl.dv), device=dev),
+                                   state_out=self.state0)
+            del q, k, v
+            self.state = self.state0.clone()
+            nt = 16   # a ring of decode tokens
+            tok = lambda w, t: torch.randn(nt, wl.B, wl.H, w, device=dev, generator=g).to(tdt(t))
+            self.tq, self.tk, self.tv = tok(wl.d, wl.x_dtype), tok(wl.d, wl.x_dtype), tok(wl.dv, wl.v_dtype)
+            self.h_in = [t[0].cpu().pin_memory() for t in (self.tq, self.tk, self.tv)]
+            self.d_in = [t[0].clone() for t in (self.tq, self.tk, self.tv)]
+            self.out = torch.empty(wl.B, wl.H, wl.dv, device=dev)
+            op = gma.OP_DECODE
+        else:
+            q, k, v = workloads.full_inputs(wl, seed)
+            self.h_in = [torch.from_numpy(q).to(tdt(wl.x_dtype)).pin_memory(),
+                         torch.from_numpy(k).to(tdt(wl.x_dtype)).pin_memory(),
+                         torch.from_numpy(v).to(tdt(wl.v_dtype)).pin_memory()]
+            self.d_in = [t.to(dev) for t in self.h_in]
+            self.out = torch.empty(wl.B, wl.H, wl.N, wl.dv, device=dev)
+            op = gma.OP_BIDIR if wl.mode == "bidir" else gma.OP_CAUSAL
+        self.ws = torch.empty(gma.gma_workspace_size(self.shape, op), dtype=torch.uint8, device=dev)
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.i = 0
+
+    def profiled(self, evs):
+        g, wl = self.gma, self.wl
+        if wl.mode == "decode":
+            t = self.i % self.tq.shape[0]
+            self.i += 1
+            return g.gma_decode_step_profiled(self.shape, *self.prm, self.tq[t], self.tk[t], self.tv[t],
+                                              self.state, self.out, evs, ws=self.ws)
+        q, k, v = self.d_in
+        if wl.mode == "bidir":
+            return g.gma_forward_bidir_profiled(self.shape, *self.prm, q, k, v, self.out, evs, ws=self.ws)
+        return g.gma_forward_causal_profiled(self.shape, *self.prm, q, k, v, self.out, evs, ws=self.ws)
+
+    def e2e_step(self):
+        """One step through the plain entry point, host inputs in and the result out."""
+        g, wl = self.gma, self.wl
+        for d, h in zip(self.d_in, self.h_in):
+            d.copy_(h, non_blocking=True)
+        q, k, v = self.d_in
+        if wl.mode == "decode":
+            g.gma_decode_step(self.shape, *self.prm, q, k, v, self.state, self.out, ws=self.ws)
+        elif wl.mode == "bidir":
+            g.gma_forward_bidir(self.shape, *self.prm, q, k, v, self.out, ws=self.ws)
+        else:
+            g.gma_forward_causal(self.shape, *self.prm, q, k, v, self.out, ws=self.ws)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def io_bytes(self):
+        return (sum(t.numel() * t.element_size() for t in self.h_in),
+                self.h_out.numel() * self.h_out.element_size())
 
 
 # ----------------------------------------------------------------- main -------
@@ -284,12 +418,9 @@ def main():
     world, rank, local = dist_env()
     from gaussian_mixture_sequence_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
-    if wl.mode != "causal":
-        raise SystemExit("bench.py times the causal forward; pick a causal workload")
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
 
-    import numpy as np
     import torch
     from gaussian_mixture_sequence_gb300 import gma
 
@@ -303,20 +434,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     gma.load()
-
-    seed = wl.seed + rank
-    mu, vr, lp = workloads.params(wl, seed)
-    q, k, v = workloads.full_inputs(wl, seed)
-    tdt = lambda s: torch.bfloat16 if s == "bf16" else torch.float32
-    h_q = torch.from_numpy(q).to(tdt(wl.x_dtype)).pin_memory()
-    h_k = torch.from_numpy(k).to(tdt(wl.x_dtype)).pin_memory()
-    h_v = torch.from_numpy(v).to(tdt(wl.v_dtype)).pin_memory()
-    d_q, d_k, d_v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
-    prm = tuple(torch.from_numpy(a).to(dev) for a in (mu, vr, lp))
-    shape = gma.Shape.make(wl.B, wl.H, wl.N, wl.d, wl.dv, wl.K, chunk=wl.chunk, eps=wl.eps,
-                           x_dtype=wl.x_dtype, v_dtype=wl.v_dtype, gemm_dtype=wl.gemm_dtype)
-    ws = torch.empty(gma.gma_workspace_size(shape, gma.OP_CAUSAL), dtype=torch.uint8, device=dev)
-    out = torch.empty(wl.B, wl.H, wl.N, wl.dv, device=dev)
+    run = Runner(wl, dev, wl.seed + rank)
     stream = torch.cuda.current_stream(dev)
     NE = gma.PROFILE_MAX_STAGES + 1
 
@@ -330,9 +448,6 @@ def main():
     warm_events = new_events()
     torch.cuda.synchronize(dev)
 
-    def step(evs):
-        return gma.gma_forward_causal_profiled(shape, *prm, d_q, d_k, d_v, out, evs, ws=ws)
-
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", ""))
     clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
@@ -340,7 +455,7 @@ def main():
     t_w = time.time()
     nw = 0
     while nw < args.warmup or time.time() - t_w < args.min_warmup_s:
-        step(warm_events)
+        run.profiled(warm_events)
         nw += 1
         if nw % 20 == 0:
             torch.cuda.synchronize(dev)
@@ -354,7 +469,7 @@ def main():
     start.record(stream)
     names = None
     for i in range(args.steps):
-        names = step(step_events[i])
+        names = run.profiled(step_events[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
@@ -368,12 +483,12 @@ def main():
     clocks_summary = clocks.summary(t_host0, t_host1)
 
     ms = total_ms / args.steps
-    tokens = wl.B * wl.N
+    tokens = tokens_per_step(wl)
     value = world * tokens / (ms * 1e-3)
     stage_ms = {}
     for i, nm in enumerate(names):
-        stage_ms[nm] = statistics.mean(step_events[s][i].elapsed_time(step_events[s][i + 1])
-                                       for s in range(args.steps))
+        stage_ms[nm] = statistics.mean(step_events[s_][i].elapsed_time(step_events[s_][i + 1])
+                                       for s_ in range(args.steps))
     dom = max(stage_ms, key=stage_ms.get)
     pk, pk_kind = peaks()
     flop, pipe, nbytes = stage_work(dom, wl)
@@ -388,8 +503,7 @@ def main():
         achieved, peak, r_unit = nbytes / t_dom / 1e9, pk["hbm_gbs"], "GB/s"
     roof_s, roof_parts = path_roofline_s(wl, pk)
 
-    # end to end through the same public API: pinned host inputs in, result out, every step
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # end to end through the plain public entry point: pinned host inputs in, result out, every step
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ne = max(1, min(args.e2e_steps, args.steps))
     torch.cuda.synchronize(dev)
@@ -397,11 +511,7 @@ def main():
         pg.barrier()
     e_start.record(stream)
     for _ in range(ne):
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        gma.gma_forward_causal(shape, *prm, d_q, d_k, d_v, out, ws=ws)
-        h_out.copy_(out, non_blocking=True)
+        run.e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = e_start.elapsed_time(e_end) / ne
@@ -410,25 +520,30 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e_ms = float(t.item())
     clocks.stop()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
-    d2h = h_out.numel() * h_out.element_size()
+    h2d, d2h = run.io_bytes()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, (q, k, v, mu, vr, lp))
+        cpu = cpu_baseline(wl)
 
     if rank == 0:
         tr = traffic_record(dom)
+        cfg = {"workload": wl.name, "mode": wl.mode, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d,
+               "d_v": wl.dv, "K": wl.K, "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
+               "inputs": "peaked mixture around the K centres" if wl.dist == "peaked" else "N(0,1)"}
+        if wl.mode == "decode":
+            cfg["prefill"] = f"{wl.N} tokens (causal, on device)"
+            cfg["l2"] = "state %.0f MB per step, larger than L2 (129 MB), no flush" % (
+                wl.B * wl.H * (wl.K * wl.dv + wl.K) * 4 / 1e6)
+        else:
+            cfg["chunk"] = eff_chunk(wl)
+            cfg["l2"] = "inputs (%.0f MB) larger than L2 (129 MB), no flush" % (h2d / 1e6)
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC if wl.mode == "causal" else f"GMA {wl.mode} tokens/sec ({wl.name})",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": nw, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if wl.gemm_dtype == "f32" else "f32+bf16",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d, "d_v": wl.dv,
-                       "K": wl.K, "chunk": eff_chunk(wl), "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
-                       "inputs": "peaked mixture around the K centres" if wl.dist == "peaked" else "N(0,1)",
-                       "l2": "inputs (%.0f MB) larger than L2 (129 MB), no flush" %
-                             ((h2d) / 1e6)},
+            "data": "synthetic", "config": cfg,
             "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": r_unit,
                          "frac": achieved / peak, "traffic": tr,
                          "peak_source": ("152 SMs x 128 FP32 lanes x 2 x max SM clock (%s)" % pk_kind)

@@ -159,32 +159,6 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     return GMA_OK;
 }
 
-gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
-                             const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
-{
-    Dims dm;
-    GMA_TRY(make_dims(shape, &dm, GMA_OP_BIDIR));
-    GMA_TRY(check_params(params));
-    GMA_TRY(check_ptr(qx, dm.N > 0));
-    GMA_TRY(check_ptr(kx, dm.N > 0));
-    GMA_TRY(check_ptr(v, dm.N > 0));
-    GMA_TRY(check_ptr(out, dm.N > 0));
-    const WsPlan wp = plan(dm, GMA_OP_BIDIR);
-    GMA_TRY(check_ws(ws, ws_bytes, wp));
-    if (dm.N == 0) return GMA_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float4 *prm = at<float4>(ws, wp.prm);
-    float *cst = at<float>(ws, wp.cst);
-    void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
-    float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
-    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
-    GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st));
-    GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
-    return GMA_OK;
-}
 
 } // extern "C"
 
@@ -210,6 +184,80 @@ struct Marks {
     }
 };
 
+gma_status check_prof(gma_profile *prof)
+{
+    if (!prof) return GMA_OK;
+    for (int i = 0; i <= GMA_PROFILE_MAX_STAGES; ++i)
+        if (!prof->events[i]) return GMA_ERR_INVALID_ARG;
+    prof->n_stages = 0;
+    return GMA_OK;
+}
+
+gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, const void *kx, const void *v,
+                     float *out, void *ws, size_t ws_bytes, gma_stream_t stream, gma_profile *prof)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_BIDIR));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx, dm.N > 0));
+    GMA_TRY(check_ptr(kx, dm.N > 0));
+    GMA_TRY(check_ptr(v, dm.N > 0));
+    GMA_TRY(check_ptr(out, dm.N > 0));
+    const WsPlan wp = plan(dm, GMA_OP_BIDIR);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    GMA_TRY(check_prof(prof));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Marks mk{prof, 0, st};
+    if (dm.N == 0) {
+        GMA_CUDA(mk.finish());
+        return GMA_OK;
+    }
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
+    float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
+    GMA_CUDA(mk.mark("prep_params"));
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(mk.mark("resp_q"));
+    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(mk.mark("resp_k"));
+    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(mk.mark("block_state"));
+    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+    GMA_CUDA(mk.mark("state_reduce"));
+    GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st));
+    GMA_CUDA(mk.mark("bidir_read"));
+    GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
+    GMA_CUDA(mk.finish());
+    return GMA_OK;
+}
+
+gma_status run_decode(const gma_shape *shape, gma_params params, const void *qx, const void *kx, const void *v,
+                      float *state, float *out, void *ws, size_t ws_bytes, gma_stream_t stream, gma_profile *prof)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_DECODE));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx));
+    GMA_TRY(check_ptr(kx));
+    GMA_TRY(check_ptr(v));
+    GMA_TRY(check_ptr(state));
+    GMA_TRY(check_ptr(out));
+    const WsPlan wp = plan(dm, GMA_OP_DECODE);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    GMA_TRY(check_prof(prof));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Marks mk{prof, 0, st};
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    GMA_CUDA(mk.mark("prep_params"));
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(mk.mark("decode"));
+    GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
+    GMA_CUDA(mk.finish());
+    return GMA_OK;
+}
+
 gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
                       const void *v, const float *state_in, float *state_out, float *out, void *ws,
                       size_t ws_bytes, gma_stream_t stream, gma_profile *prof)
@@ -225,11 +273,7 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
     GMA_TRY(check_ptr(state_out, false));
     const WsPlan wp = plan(dm, GMA_OP_CAUSAL);
     GMA_TRY(check_ws(ws, ws_bytes, wp));
-    if (prof) {
-        for (int i = 0; i <= GMA_PROFILE_MAX_STAGES; ++i)
-            if (!prof->events[i]) return GMA_ERR_INVALID_ARG;
-        prof->n_stages = 0;
-    }
+    GMA_TRY(check_prof(prof));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Marks mk{prof, 0, st};
     if (dm.N == 0) {
@@ -283,6 +327,35 @@ gma_status gma_forward_causal(const gma_shape *shape, gma_params params, const v
     return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, nullptr);
 }
 
+gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                             const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
+{
+    return run_bidir(shape, params, qx, kx, v, out, ws, ws_bytes, stream, nullptr);
+}
+
+gma_status gma_forward_bidir_profiled(const gma_shape *shape, gma_params params, const void *qx,
+                                      const void *kx, const void *v, float *out, void *ws, size_t ws_bytes,
+                                      gma_stream_t stream, gma_profile *prof)
+{
+    if (!prof) return GMA_ERR_INVALID_ARG;
+    return run_bidir(shape, params, qx, kx, v, out, ws, ws_bytes, stream, prof);
+}
+
+gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                           const void *v, float *state, float *out, void *ws, size_t ws_bytes,
+                           gma_stream_t stream)
+{
+    return run_decode(shape, params, qx, kx, v, state, out, ws, ws_bytes, stream, nullptr);
+}
+
+gma_status gma_decode_step_profiled(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
+                                    const void *v, float *state, float *out, void *ws, size_t ws_bytes,
+                                    gma_stream_t stream, gma_profile *prof)
+{
+    if (!prof) return GMA_ERR_INVALID_ARG;
+    return run_decode(shape, params, qx, kx, v, state, out, ws, ws_bytes, stream, prof);
+}
+
 gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params, const void *qx,
                                        const void *kx, const void *v, const float *state_in,
                                        float *state_out, float *out, void *ws, size_t ws_bytes,
@@ -292,27 +365,6 @@ gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params
     return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, prof);
 }
 
-gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
-                           const void *v, float *state, float *out, void *ws, size_t ws_bytes,
-                           gma_stream_t stream)
-{
-    Dims dm;
-    GMA_TRY(make_dims(shape, &dm, GMA_OP_DECODE));
-    GMA_TRY(check_params(params));
-    GMA_TRY(check_ptr(qx));
-    GMA_TRY(check_ptr(kx));
-    GMA_TRY(check_ptr(v));
-    GMA_TRY(check_ptr(state));
-    GMA_TRY(check_ptr(out));
-    const WsPlan wp = plan(dm, GMA_OP_DECODE);
-    GMA_TRY(check_ws(ws, ws_bytes, wp));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float4 *prm = at<float4>(ws, wp.prm);
-    float *cst = at<float>(ws, wp.cst);
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
-    return GMA_OK;
-}
 
 } // extern "C"
 

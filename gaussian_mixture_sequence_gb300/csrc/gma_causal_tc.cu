@@ -4,7 +4,7 @@
 // O_i depends on j <= i only) is evaluated in the chunkwise-parallel form of
 // the linear-attention page ("선형 어텐션 원리 정리", "쉽게 이해하기"): chunks of
 // C = 128 tokens, dense products inside a chunk, and a carried memory
-// [Vt | Z] between chunks.  Two kernels, one CTA (4 warps) per chunk:
+// [Vt | Z] between chunks.  Two kernels, one CTA (8 warps) per chunk:
 //
 //   k_chunk_state_tc : L_c = Gamma_K,c^T [V_c | 1]            (chunk contribution)
 //   (k_scan, generic) : S_{c-1} = state_in + sum_{c' < c} L_c'   (carried memory)
@@ -14,8 +14,10 @@
 //
 // Every contraction is one tcgen05.mma sequence with M = 128 and the fp32
 // accumulator in TMEM.  The A operand (Gamma rows, or P_m) is written to TMEM by
-// the thread that owns the row; B operands sit in shared memory in the K-major
-// 128-byte-swizzled layout.  GEMM operand precision:
+// the warps that own the rows (two warps per 32-lane quarter, each taking half
+// of the columns); B operands sit in shared memory in the K-major
+// 128-byte-swizzled layout, staged with coalesced 16-byte loads that are all
+// issued before the first store.  GEMM operand precision:
 //   BF16 = false: each fp32 operand is split into a tf32 "hi" part and an
 //                 exact remainder "lo"; a*b ~ hi*hi + hi*lo + lo*hi (three MMA
 //                 passes, relative error ~1e-6), the fp32-operand path;
@@ -24,6 +26,8 @@
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
+#include <type_traits>
+
 namespace gma {
 namespace {
 
@@ -31,7 +35,7 @@ using namespace tc;
 
 constexpr int kC = 128;       // chunk rows (= MMA M)
 constexpr int kK = 128;       // components handled by this path
-constexpr int kTCThreads = 128;
+constexpr int kTCThreads = 256;   // 8 warps: two per TMEM lane quarter
 
 template <bool BF16>
 struct Elem {
@@ -39,7 +43,6 @@ struct Elem {
     static constexpr int PASSES = BF16 ? 1 : 3;
     static constexpr uint32_t FMT = BF16 ? kFmtBF16 : kFmtTF32;
     static constexpr int COLS_PER_KSTEP = 8;               // TMEM columns per 32-byte K step
-    static constexpr int ACOLS = BF16 ? kK / 2 : kK;        // TMEM columns of a 128-wide A row
 };
 
 // Stores element (r, k) of a K-major SW128 tile (hi image, and lo image for fp32).
@@ -62,182 +65,244 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 }
 __device__ __forceinline__ float bf16r(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
 
-// Writes a full 128-wide A row held in 32-value pieces via a callback get(j0, float[32]).
-// Returns the sum of the (rounded, for bf16) values when `want_sum`.
-template <bool BF16, typename Get>
-__device__ __forceinline__ float put_a_row(uint32_t tbase, uint32_t lane0, uint32_t col_hi, uint32_t col_lo,
-                                           Get get)
-{
-    float sum = 0.f;
-#pragma unroll 1
-    for (int j0 = 0; j0 < kK; j0 += 32) {
-        float x[32];
-        get(j0, x);
-        if constexpr (BF16) {
-            uint32_t p[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                p[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
-                sum += bf16r(x[2 * j]) + bf16r(x[2 * j + 1]);
-            }
-            tmem_st16(tmem_at(tbase, lane0, col_hi + j0 / 2), p);
-        } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v = x[16 * h + j];
-                    const float hv = tf32_hi(v);
-                    hi[j] = __float_as_uint(hv);
-                    lo[j] = __float_as_uint(v - hv);
-                    sum += v;
-                }
-                tmem_st16(tmem_at(tbase, lane0, col_hi + j0 + 16 * h), hi);
-                tmem_st16(tmem_at(tbase, lane0, col_lo + j0 + 16 * h), lo);
-            }
-        }
-    }
-    return sum;
-}
-
-// Issues D (+)= A * B^T over a 128-deep contraction with A in TMEM and B a
-// K-major SW128 tile of `nrows` rows (hi/lo images), PASSES passes.
-template <bool BF16>
-__device__ __forceinline__ void mma_tb(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, unsigned char *b_hi,
-                                       unsigned char *b_lo, uint32_t nrows, bool accumulate)
-{
-    using El = Elem<BF16>;
-    const uint32_t id = idesc(128, nrows, El::FMT);
-    bool acc = accumulate;
-#pragma unroll 1
-    for (int p = 0; p < El::PASSES; ++p) {
-        const uint32_t a = (p == 2) ? a_lo : a_hi;
-        unsigned char *b = (p == 1) ? b_lo : b_hi;
-        const int ksteps = kK * El::E / 32;
-#pragma unroll 1
-        for (int kk = 0; kk < ksteps; ++kk) {
-            const uint32_t kb = kk * 32;
-            const uint32_t boff = (kb >> 7) * (nrows * 128) + (kb & 127);
-            mma_ts(!BF16, d_tmem, a + kk * El::COLS_PER_KSTEP, sdesc_sw128(smem_addr(b + boff)), id, acc ? 1u : 0u);
-            acc = true;
-        }
-    }
-}
-
 // Bytes of a K-major tile of `rows` x 128 elements.
 template <bool BF16>
 constexpr uint32_t tile_bytes(uint32_t rows) { return rows * kK * Elem<BF16>::E; }
 
+// One MMA pass D (+)= A * B^T over the 128-deep contraction: A in TMEM
+// (columns from a_col), B a K-major SW128 tile of `nrows` rows.
+template <bool BF16>
+__device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a_col, const unsigned char *b, uint32_t nrows,
+                                         bool accumulate)
+{
+    using El = Elem<BF16>;
+    const uint32_t id = idesc(128, nrows, El::FMT);
+    constexpr int ksteps = kK * El::E / 32;
+#pragma unroll 1
+    for (int kk = 0; kk < ksteps; ++kk) {
+        const uint32_t kb = kk * 32;
+        const uint32_t boff = (kb >> 7) * (nrows * 128) + (kb & 127);
+        mma_ts(!BF16, d_tmem, a_col + kk * El::COLS_PER_KSTEP, sdesc_sw128(smem_addr(b + boff)), id,
+               (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// All passes of D (+)= A * B^T: fp32 operands as hi*hi + hi*lo + lo*hi.
+template <bool BF16>
+__device__ __forceinline__ void mma_all(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, const unsigned char *b_hi,
+                                        const unsigned char *b_lo, uint32_t nrows, bool accumulate)
+{
+    mma_pass<BF16>(d_tmem, a_hi, b_hi, nrows, accumulate);
+    if constexpr (!BF16) {
+        mma_pass<BF16>(d_tmem, a_hi, b_lo, nrows, true);
+        mma_pass<BF16>(d_tmem, a_lo, b_hi, nrows, true);
+    }
+}
+
+// Writes 64 consecutive A-operand values of this thread's TMEM lane, starting
+// at operand column j0 (a multiple of 64): fp32 -> tf32 part at a_hi and the
+// exact remainder at a_lo (part = 0: parts only, 1: remainders only, 2: both);
+// bf16 -> packed pairs at a_hi.
+template <bool BF16>
+__device__ __forceinline__ void put_a64(uint32_t tbase, uint32_t lane0, uint32_t a_hi, uint32_t a_lo, int j0,
+                                        const float (&x)[64], int part = 2)
+{
+    if constexpr (BF16) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) p[j] = pack_bf16(x[32 * b + 2 * j], x[32 * b + 2 * j + 1]);
+            tmem_st16(tmem_at(tbase, lane0, a_hi + j0 / 2 + 16 * b), p);
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float v = x[16 * b + j];
+                const float hv = tf32_hi(v);
+                hi[j] = __float_as_uint(hv);
+                lo[j] = __float_as_uint(v - hv);
+            }
+            if (part != 1) tmem_st16(tmem_at(tbase, lane0, a_hi + j0 + 16 * b), hi);
+            if (part != 0) tmem_st16(tmem_at(tbase, lane0, a_lo + j0 + 16 * b), lo);
+        }
+    }
+}
+
+// B = V^T of the chunk: element (c, j) of a DV x 128 K-major tile, from
+// V [tokens][DV].  Lanes run over tokens, so the transposed stores of a warp
+// fall in one swizzled row (no bank conflicts).
+template <bool BF16, int DV>
+__device__ __forceinline__ void stage_vt(const void *v, bool v_bf16, long long row0, int nr, unsigned char *hi,
+                                         unsigned char *lo, int tid)
+{
+    using El = Elem<BF16>;
+    constexpr int PER = (kC * DV / 4) / kTCThreads;
+    float4 t[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int f = tid + u * kTCThreads, j = f % kC, c4 = f / kC;
+        t[u] = j < nr ? load4(v, (row0 + j) * DV + 4 * c4, v_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int f = tid + u * kTCThreads, j = f % kC, c4 = f / kC;
+        put<BF16>(hi, lo, sw128_offset(4 * c4 + 0, j, DV, El::E), t[u].x);
+        put<BF16>(hi, lo, sw128_offset(4 * c4 + 1, j, DV, El::E), t[u].y);
+        put<BF16>(hi, lo, sw128_offset(4 * c4 + 2, j, DV, El::E), t[u].z);
+        put<BF16>(hi, lo, sw128_offset(4 * c4 + 3, j, DV, El::E), t[u].w);
+    }
+}
+
+// 64 consecutive Gamma values of one row (fp32 or bf16 storage) -> x[64].
+template <bool BF16>
+__device__ __forceinline__ void load_g64(const void *g, long long off, bool valid, float (&x)[64])
+{
+    if constexpr (BF16) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g) + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 t = valid ? src[q] : make_uint4(0, 0, 0, 0);
+            const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * q + 2 * e] = __uint_as_float(w[e] << 16);
+                x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(g) + off);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 t = valid ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[4 * q] = t.x; x[4 * q + 1] = t.y; x[4 * q + 2] = t.z; x[4 * q + 3] = t.w;
+        }
+    }
+}
+
 // ------------------------------------------------------------------------
 // L_c = Gamma_K,c^T [V_c | 1]: M = components, N = d_v, contraction over the
-// chunk's tokens.  A = Gamma_K^T in TMEM (thread k owns component k's row of
-// 128 token values), B = V^T in shared memory.
+// chunk's 128 tokens.  A = Gamma_K^T in TMEM: warp w owns components
+// 32 (w % 4) + lane and tokens [64 (w / 4), +64).  For fp32 operands the
+// 128 A columns first hold the tf32 parts (passes hi*hi, hi*lo), then the
+// remainders (pass lo*hi), so that 256 TMEM columns suffice and two CTAs
+// share an SM.  B = V^T in shared memory.
 template <bool BF16, int DV>
 struct StateSmem {
     static constexpr uint32_t VT = tile_bytes<BF16>(DV);
-    static constexpr size_t bytes = 1024 + 2 * (size_t)VT + 64;
+    static constexpr size_t bytes = 1024 + 2 * (size_t)VT + 2 * kK * 4 + 64;
 };
 
 template <bool BF16, int DV>
-__global__ void __launch_bounds__(kTCThreads, 1)
+__global__ void __launch_bounds__(kTCThreads, 2)
     k_chunk_state_tc(int N, const void *__restrict__ gk, const void *__restrict__ v, bool v_bf16,
                      float *__restrict__ partial, int nblk)
 {
-    using El = Elem<BF16>;
+    using Sm = StateSmem<BF16, DV>;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *vt_hi = sm, *vt_lo = sm + StateSmem<BF16, DV>::VT;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + 2 * StateSmem<BF16, DV>::VT);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 1);
+    unsigned char *vt_hi = sm, *vt_lo = sm + Sm::VT;
+    float *zp = reinterpret_cast<float *>(sm + 2 * Sm::VT);         // [2][128] partial Z
+    uint64_t *bar = reinterpret_cast<uint64_t *>(zp + 2 * kK);      // [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, h = warp >> 2;
+    const uint32_t lane0 = 32 * quarter;
+    const int k = lane0 + lane;
     const long long bh = blockIdx.y;
     const int c0 = blockIdx.x * kC;
     const int nr = min(kC, N - c0);
-    constexpr uint32_t A_HI = 0, A_LO = 128, D_COL = 256;
+    constexpr uint32_t A = 0, D_COL = 128;
 
     if (warp == 0) {
-        tmem_alloc(smem_addr(tslot), 512);
+        tmem_alloc(smem_addr(tslot), 256);
         tmem_relinquish();
     }
     if (tid == 0) {
         mbar_init(smem_addr(bar), 1);
+        mbar_init(smem_addr(bar + 1), 1);
         mbar_init_fence();
     }
-    // B = V^T: element (c, j) of a DV x 128 tile; thread j writes token j's values.
-    {
-        const int j = tid;
-        const long long base = (bh * N + c0 + j) * (long long)DV;
-#pragma unroll 4
-        for (int c = 0; c < DV; ++c) {
-            const float x = j < nr ? load_elem(v, base + c, v_bf16) : 0.f;
-            put<BF16>(vt_hi, vt_lo, sw128_offset(c, j, DV, El::E), x);
-        }
+    // this thread's 64 A values: Gamma_K[c0 + 64h + jj][k] (coalesced across k)
+    float x[64];
+#pragma unroll
+    for (int jj = 0; jj < 64; ++jj) {
+        const int r = 64 * h + jj;
+        x[jj] = r < nr ? load_elem(gk, (bh * N + c0 + r) * (long long)kK + k, BF16) : 0.f;
     }
+    stage_vt<BF16, DV>(v, v_bf16, bh * N + c0, nr, vt_hi, vt_lo, tid);
+    float z = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 64; ++jj) z += x[jj];
+    zp[h * kK + k] = z;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t lane0 = 32 * warp;
-
-    // A = Gamma_K^T: thread k loads column k of the chunk's Gamma_K (coalesced across k).
-    const int k = tid;
-    const void *g = gk;
-    float z = 0.f;
-    {
-        auto get = [&](int j0, float (&x)[32]) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = j0 + j;
-                x[j] = r < nr ? load_elem(g, (bh * N + c0 + r) * (long long)kK + k, BF16) : 0.f;
-            }
-        };
-        float zs = put_a_row<BF16>(tbase, lane0, A_HI, A_LO, get);
-        z = zs;
-    }
+    put_a64<BF16>(tbase, lane0, A, A, 64 * h, x, 0);
     tmem_wait_st();
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-        mma_tb<BF16>(tbase + D_COL, tbase + A_HI, tbase + A_LO, vt_hi, vt_lo, DV, false);
+        mma_pass<BF16>(tbase + D_COL, tbase + A, vt_hi, DV, false);
+        if constexpr (!BF16) mma_pass<BF16>(tbase + D_COL, tbase + A, vt_lo, DV, true);
         mma_commit(smem_addr(bar));
     }
     __syncwarp();
-    const bool ok = mbar_wait(smem_addr(bar), 0);
+    bool ok = mbar_wait(smem_addr(bar), 0);
     fence_after_sync();
+    if constexpr (!BF16) {
+        put_a64<BF16>(tbase, lane0, A, A, 64 * h, x, 1);   // remainders into the same columns
+        tmem_wait_st();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+            mma_pass<BF16>(tbase + D_COL, tbase + A, vt_hi, DV, true);
+            mma_commit(smem_addr(bar + 1));
+        }
+        __syncwarp();
+        ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
+        fence_after_sync();
+    }
     const long long SZ = (long long)kK * DV + kK;
     float *o = partial + (bh * nblk + blockIdx.x) * SZ;
-#pragma unroll 1
-    for (int c = 0; c < DV; c += 16) {
+    const float qnan = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int cb = 0; cb < DV / 32; ++cb) {
+        const int c = h * (DV / 2) + 16 * cb;
         uint32_t r[16];
         tmem_ld16(tmem_at(tbase, lane0, D_COL + c), r);
         tmem_wait_ld();
         float4 *dst = reinterpret_cast<float4 *>(o + (long long)k * DV + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float4 t = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                   __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            if (!ok) t = make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
-            dst[q] = t;
-        }
+        for (int q = 0; q < 4; ++q)
+            dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]))
+                        : make_float4(qnan, qnan, qnan, qnan);
     }
-    o[(long long)kK * DV + k] = ok ? z : __int_as_float(0x7fc00000);
+    if (h == 0) o[(long long)kK * DV + k] = ok ? zp[k] + zp[kK + k] : qnan;
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 512);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ------------------------------------------------------------------------
+// Chunk output.  Warp w owns TMEM lanes (rows) 32 (w % 4) + lane and column
+// half w / 4 of every row-wise step.  Shared memory: region X holds Gamma_K
+// (B of P); region Y holds the carried memory Vt^T (B of U = Gq Vt) and, once
+// that product is done, V^T (B of U += P_m V), staged while P is computed.
 template <bool BF16, int DV>
 struct OutSmem {
     static constexpr uint32_t GK = tile_bytes<BF16>(kC);   // Gamma_K chunk, 128 x 128
-    static constexpr uint32_t VT = tile_bytes<BF16>(DV);   // V^T, DV x 128
-    static constexpr uint32_t ST = tile_bytes<BF16>(DV);   // Vt^T (memory), DV x 128
-    static constexpr uint32_t X = GK > VT ? GK : VT;       // region reused: Gamma_K, then V^T
-    static constexpr size_t bytes = 1024 + 2 * (size_t)X + 2 * (size_t)ST + kK * 4 + 64;
+    static constexpr uint32_t Y = tile_bytes<BF16>(DV);    // Vt^T, then V^T: DV x 128
+    static constexpr size_t bytes = 1024 + 2 * (size_t)GK + 2 * (size_t)Y + kK * 4 + 4 * kK * 4 + 64;
 };
 
 template <bool BF16, int DV>
@@ -250,17 +315,20 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     using Sm = OutSmem<BF16, DV>;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *x_hi = sm, *x_lo = sm + Sm::X;                  // Gamma_K, later V^T
-    unsigned char *s_hi = sm + 2 * Sm::X, *s_lo = s_hi + Sm::ST;   // memory Vt^T
-    float *z_s = reinterpret_cast<float *>(s_lo + Sm::ST);         // Z of the carried memory
-    uint64_t *bar = reinterpret_cast<uint64_t *>(z_s + kK);        // [2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    unsigned char *x_hi = sm, *x_lo = sm + Sm::GK;                  // Gamma_K
+    unsigned char *y_hi = sm + 2 * Sm::GK, *y_lo = y_hi + Sm::Y;    // Vt^T, later V^T
+    float *z_s = reinterpret_cast<float *>(y_lo + Sm::Y);           // [128] Z of the carried memory
+    float *part = z_s + kK;                                         // [4][128]: qz halves, row-sum halves
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [3]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, h = warp >> 2;
+    const uint32_t lane0 = 32 * quarter;
+    const int i = lane0 + lane;                 // row of the chunk owned in TMEM
     const long long bh = blockIdx.y;
     const int c0 = blockIdx.x * kC;
     const int nr = min(kC, N - c0);
-    const uint32_t lane0 = 32 * warp;
     // TMEM columns: A operand (Gamma_Q, later P_m) hi/lo, P accumulator, U accumulator.
     constexpr uint32_t A_HI = 0, A_LO = 128, D_P = 256, D_U = 384;
 
@@ -269,50 +337,62 @@ __global__ void __launch_bounds__(kTCThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(smem_addr(bar), 1);
-        mbar_init(smem_addr(bar + 1), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
     }
     const long long SZ = (long long)kK * DV + kK;
     const float *st = states + (bh * nblk + blockIdx.x) * SZ;
-    // carried memory: B = Vt^T (element (c, k)), thread k reads row k of Vt; Z to shared memory
-    {
-        const int k = tid;
-        const float4 *src = reinterpret_cast<const float4 *>(st + (long long)k * DV);
-#pragma unroll 4
-        for (int c4 = 0; c4 < DV / 4; ++c4) {
-            const float4 t = src[c4];
-            put<BF16>(s_hi, s_lo, sw128_offset(4 * c4 + 0, k, DV, El::E), t.x);
-            put<BF16>(s_hi, s_lo, sw128_offset(4 * c4 + 1, k, DV, El::E), t.y);
-            put<BF16>(s_hi, s_lo, sw128_offset(4 * c4 + 2, k, DV, El::E), t.z);
-            put<BF16>(s_hi, s_lo, sw128_offset(4 * c4 + 3, k, DV, El::E), t.w);
-        }
-        const float zk = st[(long long)kK * DV + k];
-        z_s[k] = BF16 ? bf16r(zk) : zk;
+
+    // Issue every global load of the chunk before the first store: the carried
+    // memory (lanes run over components, so that the transposed stores below
+    // fall in one swizzled row), Gamma_K, and this thread's Gamma_Q row.
+    constexpr int PS = (kK * DV / 4) / kTCThreads;
+    float4 ts[PS];
+#pragma unroll
+    for (int u = 0; u < PS; ++u) {
+        const int f = tid + u * kTCThreads, kk = f % kK, c4 = f / kK;
+        ts[u] = reinterpret_cast<const float4 *>(st + (long long)kk * DV)[c4];
     }
-    // Gamma_K chunk as B (element (j, k)): thread j copies its row.
+    const float zk = tid < kK ? st[(long long)kK * DV + tid] : 0.f;
+    constexpr int PER_ROW = kK * El::E / 16;
+    constexpr int PG = kC * PER_ROW / kTCThreads;
+    using GV = typename std::conditional<BF16, uint4, float4>::type;
+    GV tg[PG];
     {
-        const int j = tid;
+        const GV *src = reinterpret_cast<const GV *>(static_cast<const unsigned char *>(gk) +
+                                                     (bh * N + c0) * (long long)kK * El::E);
+#pragma unroll
+        for (int u = 0; u < PG; ++u) {
+            const int f = tid + u * kTCThreads, j = f / PER_ROW;
+            tg[u] = j < nr ? src[f] : GV{};
+        }
+    }
+    float xq[64];
+    load_g64<BF16>(gq, (bh * N + c0 + i) * (long long)kK + 64 * h, i < nr, xq);
+
+    // carried memory -> Y as Vt^T (element (c, k)); Z -> z_s
+#pragma unroll
+    for (int u = 0; u < PS; ++u) {
+        const int f = tid + u * kTCThreads, kk = f % kK, c = 4 * (f / kK);
+        put<BF16>(y_hi, y_lo, sw128_offset(c + 0, kk, DV, El::E), ts[u].x);
+        put<BF16>(y_hi, y_lo, sw128_offset(c + 1, kk, DV, El::E), ts[u].y);
+        put<BF16>(y_hi, y_lo, sw128_offset(c + 2, kk, DV, El::E), ts[u].z);
+        put<BF16>(y_hi, y_lo, sw128_offset(c + 3, kk, DV, El::E), ts[u].w);
+    }
+    if (tid < kK) z_s[tid] = BF16 ? bf16r(zk) : zk;
+    // Gamma_K chunk -> X (element (j, k)); a warp covers whole rows
+#pragma unroll
+    for (int u = 0; u < PG; ++u) {
+        const int f = tid + u * kTCThreads, j = f / PER_ROW, q = f % PER_ROW;
         if constexpr (BF16) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(gk) +
-                                                               (bh * N + c0 + j) * (long long)kK);
-#pragma unroll 4
-            for (int q = 0; q < kK / 8; ++q) {
-                const uint4 t = j < nr ? src[q] : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(x_hi + sw128_offset(j, 8 * q, kC, 2)) = t;
-            }
+            *reinterpret_cast<uint4 *>(x_hi + sw128_offset(j, 8 * q, kC, 2)) = tg[u];
         } else {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(gk) +
-                                                                 (bh * N + c0 + j) * (long long)kK);
-#pragma unroll 4
-            for (int q = 0; q < kK / 4; ++q) {
-                const float4 t = j < nr ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float4 h = make_float4(tf32_hi(t.x), tf32_hi(t.y), tf32_hi(t.z), tf32_hi(t.w));
-                const float4 l = make_float4(t.x - h.x, t.y - h.y, t.z - h.z, t.w - h.w);
-                const uint32_t off = sw128_offset(j, 4 * q, kC, 4);
-                *reinterpret_cast<float4 *>(x_hi + off) = h;
-                *reinterpret_cast<float4 *>(x_lo + off) = l;
-            }
+            const float4 t = tg[u];
+            const float4 hv = make_float4(tf32_hi(t.x), tf32_hi(t.y), tf32_hi(t.z), tf32_hi(t.w));
+            const float4 lv = make_float4(t.x - hv.x, t.y - hv.y, t.z - hv.z, t.w - hv.w);
+            const uint32_t off = sw128_offset(j, 4 * q, kC, 4);
+            *reinterpret_cast<float4 *>(x_hi + off) = hv;
+            *reinterpret_cast<float4 *>(x_lo + off) = lv;
         }
     }
     fence_before_sync();
@@ -320,37 +400,13 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     fence_after_sync();
     const uint32_t tbase = *tslot;
 
-    // A = Gamma_Q chunk (thread i owns row i), and Gamma_Q,i . Z
-    const int i = tid;
-    float qz = 0.f;
+    // A = Gamma_Q: this thread's row i, operand columns [64h, 64h + 64); partial Gamma_Q,i . Z
     {
-        auto get = [&](int j0, float (&x)[32]) {
-            if constexpr (BF16) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(gq) +
-                                                                   (bh * N + c0 + i) * (long long)kK + j0);
+        float qz = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 t = i < nr ? src[q] : make_uint4(0, 0, 0, 0);
-                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        x[8 * q + 2 * e] = __uint_as_float(w[e] << 16);
-                        x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                    }
-                }
-            } else {
-                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(gq) +
-                                                                     (bh * N + c0 + i) * (long long)kK + j0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 t = i < nr ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[4 * q] = t.x; x[4 * q + 1] = t.y; x[4 * q + 2] = t.z; x[4 * q + 3] = t.w;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) qz = fmaf(x[j], z_s[j0 + j], qz);
-        };
-        put_a_row<BF16>(tbase, lane0, A_HI, A_LO, get);
+        for (int j = 0; j < 64; ++j) qz = fmaf(xq[j], z_s[64 * h + j], qz);
+        part[h * kK + i] = qz;
+        put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, xq);
     }
     tmem_wait_st();
     fence_proxy_async();
@@ -358,41 +414,37 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-        mma_tb<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);   // P = Gq Gk^T
-        mma_tb<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, s_hi, s_lo, DV, false);   // U = Gq Vt
+        mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, false);    // U = Gq Vt
         mma_commit(smem_addr(bar));
+        mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
+        mma_commit(smem_addr(bar + 1));
     }
     __syncwarp();
     bool ok = mbar_wait(smem_addr(bar), 0);
     fence_after_sync();
-
-    // P_m = P with j > i zeroed; it replaces Gamma_Q as the A operand.  Row sums on CUDA cores.
-    float psum = 0.f;
+    // Y is free again: stage V^T while P is being computed
+    stage_vt<BF16, DV>(v, v_bf16, bh * N + c0, nr, y_hi, y_lo, tid);
+    ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
+    fence_after_sync();
+    // P_m = P with j > i zeroed replaces Gamma_Q as the A operand; row sums on CUDA cores
     {
-        auto get = [&](int j0, float (&x)[32]) {
+        float x[64];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[16];
-                tmem_ld16(tmem_at(tbase, lane0, D_P + j0 + 16 * h), r);
-                tmem_wait_ld();
+        for (int b = 0; b < 4; ++b) {
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, lane0, D_P + 64 * h + 16 * b), r);
+            tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int jj = j0 + 16 * h + j;
-                    x[16 * h + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
-                }
+            for (int j = 0; j < 16; ++j) {
+                const int jj = 64 * h + 16 * b + j;
+                x[16 * b + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
             }
-        };
-        psum = put_a_row<BF16>(tbase, lane0, A_HI, A_LO, get);
-    }
-    // B = V^T (element (c, j)) into the region that held Gamma_K (its MMAs are complete).
-    {
-        const int j = tid;
-        const long long base = (bh * N + c0 + j) * (long long)DV;
-#pragma unroll 4
-        for (int c = 0; c < DV; ++c) {
-            const float x = j < nr ? load_elem(v, base + c, v_bf16) : 0.f;
-            put<BF16>(x_hi, x_lo, sw128_offset(c, j, DV, El::E), x);
         }
+        float ps = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) ps += BF16 ? bf16r(x[j]) : x[j];
+        part[(2 + h) * kK + i] = ps;
+        put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, x);
     }
     tmem_wait_st();
     fence_proxy_async();
@@ -400,17 +452,18 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-        mma_tb<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, x_hi, x_lo, DV, true);   // U += P_m V
-        mma_commit(smem_addr(bar + 1));
+        mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, true);     // U += P_m V
+        mma_commit(smem_addr(bar + 2));
     }
     __syncwarp();
-    ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
+    ok = mbar_wait(smem_addr(bar + 2), 0) && ok;
     fence_after_sync();
 
-    const float den = psum + qz + eps;
-    const float inv_nan = __int_as_float(0x7fc00000);
-#pragma unroll 1
-    for (int c = 0; c < DV; c += 16) {
+    const float den = part[i] + part[kK + i] + part[2 * kK + i] + part[3 * kK + i] + eps;
+    const float qnan = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int cb = 0; cb < DV / 32; ++cb) {
+        const int c = h * (DV / 2) + 16 * cb;
         uint32_t r[16];
         tmem_ld16(tmem_at(tbase, lane0, D_U + c), r);
         tmem_wait_ld();
@@ -420,7 +473,7 @@ __global__ void __launch_bounds__(kTCThreads, 1)
             for (int q = 0; q < 4; ++q)
                 dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]) / den, __uint_as_float(r[4 * q + 1]) / den,
                                           __uint_as_float(r[4 * q + 2]) / den, __uint_as_float(r[4 * q + 3]) / den)
-                            : make_float4(inv_nan, inv_nan, inv_nan, inv_nan);
+                            : make_float4(qnan, qnan, qnan, qnan);
         }
     }
     fence_before_sync();

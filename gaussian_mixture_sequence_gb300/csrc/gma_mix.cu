@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) k_scan(long long SZ, int nblk, float
     const long long bh = blockIdx.y;
     float run = state_in ? state_in[bh * SZ + e] : 0.f;
     float *__restrict__ p = partial + bh * nblk * SZ + e;
-    constexpr int U = 8; // loads in flight per thread
+    constexpr int U = 32; // loads in flight per thread
     int b = 0;
     for (; b + U <= nblk; b += U) {
         float t[U];

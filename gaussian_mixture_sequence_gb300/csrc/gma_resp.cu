@@ -168,28 +168,40 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncthreads();
             const int k0 = t * KT, kn = min(KT, K - k0);
-            for (int kk = wig; kk < kn; kk += WPG) {
-                const float4 *pk = prm_s + kk * DP + half;
-                float2 acc[RPT][2];
+            // two components per pass: four independent accumulation chains per row pair
+            for (int kk = wig; kk < kn; kk += 2 * WPG) {
+                const bool two = kk + WPG < kn;
+                const float4 *pa = prm_s + kk * DP + half;
+                const float4 *pb = prm_s + (two ? kk + WPG : kk) * DP + half;
+                float2 acc[2][RPT][2];
 #pragma unroll
-                for (int j = 0; j < RPT; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int j = 0; j < RPT; ++j) acc[c][j][0] = acc[c][j][1] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int dp = 0; dp < DH / 2; ++dp) {
-                    const float4 p = pk[dp * HALVES];
-                    const float2 sc = make_float2(p.x, p.y), nm = make_float2(p.z, p.w);
+                    const float4 p = pa[dp * HALVES], q = pb[dp * HALVES];
+                    const float2 sa = make_float2(p.x, p.y), na = make_float2(p.z, p.w);
+                    const float2 sb = make_float2(q.x, q.y), nb = make_float2(q.z, q.w);
 #pragma unroll
                     for (int j = 0; j < RPT; ++j) {
-                        const float2 y = __ffma2_rn(xr[j][dp], sc, nm); // (x - mu) / sigma
-                        acc[j][dp & 1] = __ffma2_rn(y, y, acc[j][dp & 1]);
+                        const float2 ya = __ffma2_rn(xr[j][dp], sa, na); // (x - mu) / sigma
+                        acc[0][j][dp & 1] = __ffma2_rn(ya, ya, acc[0][j][dp & 1]);
+                        const float2 yb = __ffma2_rn(xr[j][dp], sb, nb);
+                        acc[1][j][dp & 1] = __ffma2_rn(yb, yb, acc[1][j][dp & 1]);
                     }
                 }
-                const float c = cst_s[kk];
 #pragma unroll
-                for (int j = 0; j < RPT; ++j) {
-                    float q = (acc[j][0].x + acc[j][0].y) + (acc[j][1].x + acc[j][1].y);
+                for (int c = 0; c < 2; ++c) {
+                    const int kc = kk + c * WPG;
+                    const float cc = cst_s[two ? kc : kk];
 #pragma unroll
-                    for (int o = 1; o < HALVES; o <<= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-                    if (half == 0) ell[lrow[j] * LDE + k0 + kk] = fmaf(-0.5f, q, c);
+                    for (int j = 0; j < RPT; ++j) {
+                        float q = (acc[c][j][0].x + acc[c][j][0].y) + (acc[c][j][1].x + acc[c][j][1].y);
+#pragma unroll
+                        for (int o = 1; o < HALVES; o <<= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                        if (half == 0 && (c == 0 || two)) ell[lrow[j] * LDE + k0 + kc] = fmaf(-0.5f, q, cc);
+                    }
                 }
             }
         }

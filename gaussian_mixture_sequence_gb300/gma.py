@@ -84,8 +84,13 @@ def load():
         lib.gma_decode_step_noalloc.argtypes = [S, _Params, P, P, P, P, P, P]
         lib.gma_forward_causal_profiled.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P,
                                                     ctypes.POINTER(Profile)]
+        lib.gma_forward_bidir_profiled.argtypes = [S, _Params, P, P, P, P, P, ctypes.c_size_t, P,
+                                                   ctypes.POINTER(Profile)]
+        lib.gma_decode_step_profiled.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P,
+                                                 ctypes.POINTER(Profile)]
         for fn in ("gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
-                   "gma_forward_causal_profiled", "gma_decode_step_noalloc"):
+                   "gma_forward_causal_profiled", "gma_decode_step_noalloc",
+                   "gma_forward_bidir_profiled", "gma_decode_step_profiled"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -206,14 +211,53 @@ def gma_forward_causal_profiled(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, 
     so = _ptr(state_out, "state_out", sshape, torch.float32, dev, optional=True)
     prm = _params(s, mu, var_raw, logit_pi, dev)
     wp, wn = _ws(s, OP_CAUSAL, ws, dev)
-    prof = Profile()
-    if len(events) != PROFILE_MAX_STAGES + 1:
-        raise ValueError(f"need {PROFILE_MAX_STAGES + 1} events")
-    for i, e in enumerate(events):
-        prof.events[i] = e.cuda_event
+    prof = _profile(events)
     _check("gma_forward_causal_profiled",
            load().gma_forward_causal_profiled(ctypes.byref(s), prm, q, k, vv, si, so, o, wp, wn,
                                               _stream(dev, stream), ctypes.byref(prof)))
+    return [prof.stage_name[i].decode() for i in range(prof.n_stages)]
+
+
+def _profile(events):
+    if len(events) != PROFILE_MAX_STAGES + 1:
+        raise ValueError(f"need {PROFILE_MAX_STAGES + 1} events")
+    prof = Profile()
+    for i, e in enumerate(events):
+        prof.events[i] = e.cuda_event
+    return prof
+
+
+def gma_forward_bidir_profiled(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, out, events, ws=None,
+                               stream=None):
+    """gma_forward_bidir with CUDA events around every launch (see gma_forward_causal_profiled)."""
+    dev = qx.device
+    q, k, vv, o = _fwd_ptrs(shape, qx, kx, v, out, dev)
+    prm = _params(shape, mu, var_raw, logit_pi, dev)
+    wp, wn = _ws(shape, OP_BIDIR, ws, dev)
+    prof = _profile(events)
+    _check("gma_forward_bidir_profiled",
+           load().gma_forward_bidir_profiled(ctypes.byref(shape), prm, q, k, vv, o, wp, wn,
+                                             _stream(dev, stream), ctypes.byref(prof)))
+    return [prof.stage_name[i].decode() for i in range(prof.n_stages)]
+
+
+def gma_decode_step_profiled(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, state, out, events, ws=None,
+                             stream=None):
+    """gma_decode_step with CUDA events around every launch (see gma_forward_causal_profiled)."""
+    dev = qx.device
+    s = shape
+    xdt, vdt = _TORCH_DT[s.x_dtype], _TORCH_DT[s.v_dtype]
+    q = _ptr(qx, "qx", (s.B, s.H, s.d_route), xdt, dev)
+    k = _ptr(kx, "kx", (s.B, s.H, s.d_route), xdt, dev)
+    vv = _ptr(v, "v", (s.B, s.H, s.d_v), vdt, dev)
+    st = _ptr(state, "state", (s.B, s.H, s.K * s.d_v + s.K), torch.float32, dev)
+    o = _ptr(out, "out", (s.B, s.H, s.d_v), torch.float32, dev)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    wp, wn = _ws(s, OP_DECODE, ws, dev)
+    prof = _profile(events)
+    _check("gma_decode_step_profiled",
+           load().gma_decode_step_profiled(ctypes.byref(s), prm, q, k, vv, st, o, wp, wn, _stream(dev, stream),
+                                           ctypes.byref(prof)))
     return [prof.stage_name[i].decode() for i in range(prof.n_stages)]
 
 

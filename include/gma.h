@@ -157,6 +157,16 @@ gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params
                                        float *state_out, float *out, void *ws, size_t ws_bytes,
                                        gma_stream_t stream, gma_profile *prof);
 
+/* Profiling variants of gma_forward_bidir and gma_decode_step, with the same
+ * event protocol as gma_forward_causal_profiled.                             */
+gma_status gma_forward_bidir_profiled(const gma_shape *shape, gma_params params, const void *qx,
+                                      const void *kx, const void *v, float *out, void *ws,
+                                      size_t ws_bytes, gma_stream_t stream, gma_profile *prof);
+gma_status gma_decode_step_profiled(const gma_shape *shape, gma_params params, const void *qx,
+                                    const void *kx, const void *v, float *state, float *out,
+                                    void *ws, size_t ws_bytes, gma_stream_t stream,
+                                    gma_profile *prof);
+
 /* Decode step for callers that cannot allocate device memory.
  *
  * No counterpart in the paper: this is a deployment convenience.  Some hosts
