@@ -74,6 +74,11 @@ cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const 
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
                           const void *kx, const void *v, float *state, float *out, cudaStream_t st);
 
+// Responsibilities for K = 128, d_route = 64 with a tensor-core bound (gma_resp_tc.cu).
+bool resp_pruned_applies(const Dims &dm);
+cudaError_t launch_resp_pruned(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
+                               int ldg, bool gamma_bf16, cudaStream_t st);
+
 // Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
 bool tc_path_eligible(int K, int DV, bool g_bf16);
 bool tc_path_applies(const Dims &dm);

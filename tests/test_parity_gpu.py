@@ -44,6 +44,35 @@ def test_responsibilities(wl, sample):
         _report(f"gamma_{which} {wl.name} K={wl.K}", normwise(g, ref), TOL["f32"])
 
 
+def test_responsibilities_adversarial_rows():
+    """Rows that stress the component bound of the K = 128, d = 64 routing path:
+    on a centre, midway between two centres, far from every centre (|x| = 1e3,
+    logits ~ -1e6), and widely spread; each must match the oracle."""
+    import oracle
+    from gaussian_mixture_sequence_gb300 import gma
+    from gpu_cases import shape_of
+    wl = W["causal_4k"].with_(B=1, H=2, N=600)
+    mu, vr, lp = workloads.params(wl)
+    rng = np.random.default_rng(3)
+    rows = []
+    for h in range(wl.H):
+        r = [mu[h, k] for k in range(0, 128, 8)]
+        r += [0.5 * (mu[h, a] + mu[h, b]) for a, b in zip(range(0, 64), range(64, 128))]
+        r += [np.full(64, 1e3, np.float32), np.full(64, -1e3, np.float32), np.full(64, 37.0, np.float32)]
+        r += [rng.normal(0, 3.0, 64).astype(np.float32) for _ in range(100)]
+        r += [rng.normal(0, 1.0, 64).astype(np.float32) for _ in range(wl.N - len(r))]
+        rows.append(np.stack(r)[: wl.N])
+    x = np.stack(rows)[None].astype(np.float32)              # [1, H, N, 64]
+    dev = "cuda:0"
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    g = torch.empty(1, wl.H, wl.N, wl.K, device=dev)
+    gma.gma_responsibilities(shape_of(wl), t(mu), t(vr), t(lp), t(x), g)
+    ref = oracle.responsibilities(mu, vr, lp, x.reshape(wl.H, wl.N, 64))
+    out = g.reshape(wl.H, wl.N, wl.K).cpu().numpy()
+    _report("gamma adversarial rows", normwise(out, ref), TOL["f32"])
+    assert np.abs(out.sum(-1) - 1).max() < 1e-5
+
+
 # --------------------------------------------------------- S2 + S3 -------------
 
 @pytest.mark.parametrize("wl,sample", [
