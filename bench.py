@@ -101,7 +101,10 @@ def stage_work(stage, wl):
     blk = C if tc else 256
     nblk = wl.B * wl.H * -(-wl.N // blk)
     if stage in ("resp_q", "resp_k"):
-        return 4.0 * K * d * ht, "alu", (d * xb + K * gb) * ht
+        # K = 128, d = 64: the bound GEMM [x^2 | x] W has the same 4*K*d flop per row and runs on the
+        # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work
+        pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
+        return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
     if stage in ("block_state", "chunk_state_tc"):
         return 2.0 * K * (dv + 1) * ht, ("tensor" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
     if stage in ("chunk_out", "chunk_out_tc"):
@@ -114,18 +117,29 @@ def stage_work(stage, wl):
     return 0.0, "alu", 0.0
 
 
+def bounded_routing(wl):
+    """The library's routing kernel with the tensor-core bound applies (K = 128, d = 64)."""
+    return wl.K == 128 and wl.d == 64
+
+
 def pipe_peak(pipe, wl, pk):
     """Peak of a pipe in flop/s: FP32 lanes x 2 x max SM clock, or the tensor
     rate of the product operands (tf32 = measured bf16 x 1.1/2.25 nominal ratio)."""
     if pipe == "alu":
         return SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
     bf16 = pk["bf16_tflops"] * 1e12
+    if pipe == "tensor_bf16":
+        return bf16
     return bf16 if wl.gemm_dtype == "bf16" else bf16 * (1.1 / 2.25)
 
 
-def path_roofline_s(wl, pk):
-    """Roofline time of one step: max(FP32 time of the routing, HBM time of the
-    minimum traffic, tensor time of the memory products)."""
+def path_roofline_s(wl, pk, kept=None):
+    """Roofline time of one step: max(FP32 time, HBM time of the minimum
+    traffic, tensor time).  With the bounded routing (K = 128, d = 64) the FP32
+    work is the exact evaluation of the kept components (two passes of 4*d flop
+    each per kept component and row; `kept` = mean kept components per row,
+    measured) and the bound GEMMs are tensor work; otherwise the FP32 work is
+    the dense routing, 8*K*d flop per head-token."""
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
     xb = 2 if wl.x_dtype == "bf16" else 4
     vb = 2 if wl.v_dtype == "bf16" else 4
@@ -135,7 +149,6 @@ def path_roofline_s(wl, pk):
         t_hbm = (8.0 * wl.K * (wl.dv + 1) + 2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * bh / (pk["hbm_gbs"] * 1e9)
         return max(t_alu, t_hbm), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=0.0)
     ht = wl.B * wl.H * wl.N
-    t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     t_hbm = ((2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * ht) / (pk["hbm_gbs"] * 1e9)
     C = eff_chunk(wl)
     if wl.mode == "bidir":
@@ -144,6 +157,11 @@ def path_roofline_s(wl, pk):
         mma = (4.0 * wl.K * (wl.dv + 1) + 2.0 * C * wl.K + C * (wl.dv + 1)) * ht
     tens = pk["bf16_tflops"] * 1e12 * (1.0 if wl.gemm_dtype == "bf16" else 1.1 / 2.25)
     t_mma = mma / tens
+    if bounded_routing(wl) and kept is not None:
+        t_alu = 2 * 2 * 4.0 * wl.d * kept * ht / fp32_peak          # Q and K rows, two exact passes
+        t_mma += 8.0 * wl.K * wl.d * ht / (pk["bf16_tflops"] * 1e12)  # the two bound GEMMs
+    else:
+        t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)
 
 
@@ -406,6 +424,20 @@ class Runner:
             g.gma_forward_causal(self.shape, *self.prm, q, k, v, self.out, ws=self.ws)
         self.h_out.copy_(self.out, non_blocking=True)
 
+    def kept_per_row(self):
+        """Mean number of components with a non-zero posterior per routing row
+        (the components the bounded routing evaluates exactly), from one
+        responsibilities call on the Q_X and K_X rows outside the timed region."""
+        import torch
+        g, wl = self.gma, self.wl
+        n = 0.0
+        for x in self.d_in[:2]:
+            gam = torch.empty(wl.B, wl.H, wl.N, wl.K, device=self.dev)
+            g.gma_responsibilities(self.shape, *self.prm, x, gam)
+            n += (gam > 0).sum(-1).float().mean().item()
+            del gam
+        return n / 2
+
     def io_bytes(self):
         return (sum(t.numel() * t.element_size() for t in self.h_in),
                 self.h_out.numel() * self.h_out.element_size())
@@ -501,7 +533,8 @@ def main():
     else:
         bound = "hbm"
         achieved, peak, r_unit = nbytes / t_dom / 1e9, pk["hbm_gbs"], "GB/s"
-    roof_s, roof_parts = path_roofline_s(wl, pk)
+    kept = run.kept_per_row() if (bounded_routing(wl) and wl.mode != "decode") else None
+    roof_s, roof_parts = path_roofline_s(wl, pk, kept)
 
     # end to end through the plain public entry point: pinned host inputs in, result out, every step
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -549,7 +582,8 @@ def main():
                          "peak_source": ("152 SMs x 128 FP32 lanes x 2 x max SM clock (%s)" % pk_kind)
                          if bound == "alu" else pk_kind},
             "path_roofline": {"tokens_per_s": tokens / roof_s, "frac": value / world / (tokens / roof_s),
-                              **{k2: v2 * 1e3 for k2, v2 in roof_parts.items()}, "unit_ms": True},
+                              **{k2.replace("_s", "_ms"): v2 * 1e3 for k2, v2 in roof_parts.items()},
+                              "kept_components_per_row": kept},
             "stages_ms": stage_ms,
             "gpu_launches": len(names) * args.steps,
             "clocks": clocks_summary,

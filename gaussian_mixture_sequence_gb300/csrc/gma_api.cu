@@ -13,7 +13,8 @@ using namespace gma;
 namespace {
 
 struct WsPlan {
-    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, bytes = 0;
+    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, wimg = 0, pimg = 0, cimg = 0, bytes = 0;
+    bool pruned = false;
 };
 
 bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }
@@ -70,6 +71,12 @@ WsPlan plan(const Dims &dm, gma_op op)
     };
     p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
     p.cst = take((size_t)dm.H * dm.K * 4);
+    if (op != GMA_OP_DECODE && resp_pruned_applies(dm)) {
+        p.pruned = true;
+        p.wimg = take((size_t)dm.H * kPrunedWBytes);
+        p.pimg = take((size_t)dm.H * kPrunedPBytes);
+        p.cimg = take((size_t)dm.H * kPrunedCBytes);
+    }
     if (op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL) {
         const size_t gb = dm.g_bf16 ? 2 : 4;
         p.gq = take((size_t)dm.BH() * dm.N * dm.KP * gb);
@@ -116,6 +123,11 @@ gma_status check_ws(void *ws, size_t ws_bytes, const WsPlan &wp)
 template <typename T>
 T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
 
+PrunedImages images(void *ws, const WsPlan &wp)
+{
+    return PrunedImages{at<unsigned char>(ws, wp.wimg), at<float4>(ws, wp.pimg), at<float>(ws, wp.cimg)};
+}
+
 } // namespace
 
 extern "C" {
@@ -154,8 +166,10 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float4 *prm = at<float4>(ws, wp.prm);
     float *cst = at<float>(ws, wp.cst);
+    const PrunedImages img = images(ws, wp);
     GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, x, gamma, dm.K, false, st));
+    if (wp.pruned) GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, false, st));
     return GMA_OK;
 }
 
@@ -216,12 +230,18 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
     float *cst = at<float>(ws, wp.cst);
     void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
+    const PrunedImages img = images(ws, wp);
+    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
     GMA_CUDA(mk.mark("prep_params"));
     GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    if (wp.pruned) {
+        GMA_CUDA(mk.mark("prep_bound"));
+        GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+    }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, dm.g_bf16, st));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, dm.g_bf16, st));
     GMA_CUDA(mk.mark("block_state"));
     GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
     GMA_CUDA(mk.mark("state_reduce"));
@@ -291,12 +311,18 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
     float *cst = at<float>(ws, wp.cst);
     void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial);
+    const PrunedImages img = images(ws, wp);
+    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
     GMA_CUDA(mk.mark("prep_params"));
     GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    if (wp.pruned) {
+        GMA_CUDA(mk.mark("prep_bound"));
+        GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+    }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, dm.g_bf16, st));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, dm.g_bf16, st));
     if (tc_path_applies(dm)) {
         GMA_CUDA(mk.mark("chunk_state_tc"));
         GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));

@@ -26,6 +26,7 @@
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
+#include <cuda.h>
 #include <type_traits>
 
 namespace gma {
@@ -271,6 +272,7 @@ __global__ void __launch_bounds__(kTCThreads, 2)
         ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
         fence_after_sync();
     }
+    // block layout on this path: Vt^T as DV rows of K, then Z as row DV
     const long long SZ = (long long)kK * DV + kK;
     float *o = partial + (bh * nblk + blockIdx.x) * SZ;
     const float qnan = __int_as_float(0x7fc00000);
@@ -280,12 +282,8 @@ __global__ void __launch_bounds__(kTCThreads, 2)
         uint32_t r[16];
         tmem_ld16(tmem_at(tbase, lane0, D_COL + c), r);
         tmem_wait_ld();
-        float4 *dst = reinterpret_cast<float4 *>(o + (long long)k * DV + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]))
-                        : make_float4(qnan, qnan, qnan, qnan);
+        for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = ok ? __uint_as_float(r[q]) : qnan;
     }
     if (h == 0) o[(long long)kK * DV + k] = ok ? zp[k] + zp[kK + k] : qnan;
     fence_before_sync();
@@ -295,9 +293,14 @@ __global__ void __launch_bounds__(kTCThreads, 2)
 
 // ------------------------------------------------------------------------
 // Chunk output.  Warp w owns TMEM lanes (rows) 32 (w % 4) + lane and column
-// half w / 4 of every row-wise step.  Shared memory: region X holds Gamma_K
-// (B of P); region Y holds the carried memory Vt^T (B of U = Gq Vt) and, once
-// that product is done, V^T (B of U += P_m V), staged while P is computed.
+// half w / 4 of every row-wise step.  Every tile arrives by TMA (bulk tensor
+// copies with the 128-byte swizzle) straight into the operand layout:
+//   X_hi <- Gamma_K (B of P), X_lo <- Gamma_Q (moved to TMEM as the A operand),
+//   Y_hi <- carried memory Vt^T (B of U = Gq Vt; fp32 operands only, the bf16
+//           path converts it with threads), later X <- V (transposed by threads
+//           into Y as the B of U += P_m V).
+// For fp32 operands the raw fp32 tile is the tf32 "hi" image (the tensor core
+// reads only the tf32 bits); threads derive the exact remainders in place.
 template <bool BF16, int DV>
 struct OutSmem {
     static constexpr uint32_t GK = tile_bytes<BF16>(kC);   // Gamma_K chunk, 128 x 128
@@ -305,108 +308,124 @@ struct OutSmem {
     static constexpr size_t bytes = 1024 + 2 * (size_t)GK + 2 * (size_t)Y + kK * 4 + 4 * kK * 4 + 64;
 };
 
+struct OutMaps {
+    CUtensorMap gq, gk, v, s;   // s: carried memory blocks (fp32 operands only)
+};
+
 template <bool BF16, int DV>
 __global__ void __launch_bounds__(kTCThreads, 1)
-    k_chunk_out_tc(int N, float eps, const void *__restrict__ gq, const void *__restrict__ gk,
-                   const void *__restrict__ v, bool v_bf16, const float *__restrict__ states, int nblk,
-                   float *__restrict__ out)
+    k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, float eps, bool v_bf16,
+                   const float *__restrict__ states, int nblk, float *__restrict__ out)
 {
     using El = Elem<BF16>;
     using Sm = OutSmem<BF16, DV>;
+    constexpr int EV_MAX = 4;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *x_hi = sm, *x_lo = sm + Sm::GK;                  // Gamma_K
+    unsigned char *x_hi = sm, *x_lo = sm + Sm::GK;                  // Gamma_K / Gamma_Q, later V
     unsigned char *y_hi = sm + 2 * Sm::GK, *y_lo = y_hi + Sm::Y;    // Vt^T, later V^T
     float *z_s = reinterpret_cast<float *>(y_lo + Sm::Y);           // [128] Z of the carried memory
     float *part = z_s + kK;                                         // [4][128]: qz halves, row-sum halves
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [3]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [5]: loads, U, P, V, final
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, h = warp >> 2;
-    const uint32_t lane0 = 32 * quarter;
+    const int h = warp >> 2;
+    const uint32_t lane0 = 32 * (warp & 3);
     const int i = lane0 + lane;                 // row of the chunk owned in TMEM
     const long long bh = blockIdx.y;
     const int c0 = blockIdx.x * kC;
     const int nr = min(kC, N - c0);
-    // TMEM columns: A operand (Gamma_Q, later P_m) hi/lo, P accumulator, U accumulator.
+    const int row0 = (int)(bh * N + c0);
     constexpr uint32_t A_HI = 0, A_LO = 128, D_P = 256, D_U = 384;
+    constexpr int GBOX = 128 / El::E;                       // Gamma columns per TMA box
+    const int ev = v_bf16 ? 2 : 4;
+    const int vbox = 128 / ev;                              // V columns per TMA box
+    (void)EV_MAX;
 
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
+        uint32_t bytes = 2 * Sm::GK + (BF16 ? 0u : (uint32_t)Sm::Y);
+        mbar_expect_tx(smem_addr(bar), bytes);
+        for (int a = 0; a < kK / GBOX; ++a) {
+            tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.gk, a * GBOX, row0, smem_addr(bar));
+            tma_load_2d(smem_addr(x_lo + a * (kC * 128)), &maps.gq, a * GBOX, row0, smem_addr(bar));
+        }
+        if constexpr (!BF16) {
+            const int srow = (int)((bh * nblk + blockIdx.x) * (DV + 1));
+            for (int a = 0; a < kK / 32; ++a)
+                tma_load_2d(smem_addr(y_hi + a * (DV * 128)), &maps.s, a * 32, srow, smem_addr(bar));
+        }
     }
     const long long SZ = (long long)kK * DV + kK;
     const float *st = states + (bh * nblk + blockIdx.x) * SZ;
-
-    // Issue every global load of the chunk before the first store: the carried
-    // memory (lanes run over components, so that the transposed stores below
-    // fall in one swizzled row), Gamma_K, and this thread's Gamma_Q row.
-    constexpr int PS = (kK * DV / 4) / kTCThreads;
-    float4 ts[PS];
-#pragma unroll
-    for (int u = 0; u < PS; ++u) {
-        const int f = tid + u * kTCThreads, kk = f % kK, c4 = f / kK;
-        ts[u] = reinterpret_cast<const float4 *>(st + (long long)kk * DV)[c4];
+    if (tid < kK) {
+        const float zk = st[(long long)kK * DV + tid];
+        z_s[tid] = BF16 ? bf16r(zk) : zk;
     }
-    const float zk = tid < kK ? st[(long long)kK * DV + tid] : 0.f;
-    constexpr int PER_ROW = kK * El::E / 16;
-    constexpr int PG = kC * PER_ROW / kTCThreads;
-    using GV = typename std::conditional<BF16, uint4, float4>::type;
-    GV tg[PG];
-    {
-        const GV *src = reinterpret_cast<const GV *>(static_cast<const unsigned char *>(gk) +
-                                                     (bh * N + c0) * (long long)kK * El::E);
+    if constexpr (BF16) {
+        // carried memory (block rows c of K) -> Y as bf16 Vt^T; lanes run over components
+        constexpr int PER = (DV * kK / 4) / kTCThreads;
 #pragma unroll
-        for (int u = 0; u < PG; ++u) {
-            const int f = tid + u * kTCThreads, j = f / PER_ROW;
-            tg[u] = j < nr ? src[f] : GV{};
-        }
-    }
-    float xq[64];
-    load_g64<BF16>(gq, (bh * N + c0 + i) * (long long)kK + 64 * h, i < nr, xq);
-
-    // carried memory -> Y as Vt^T (element (c, k)); Z -> z_s
-#pragma unroll
-    for (int u = 0; u < PS; ++u) {
-        const int f = tid + u * kTCThreads, kk = f % kK, c = 4 * (f / kK);
-        put<BF16>(y_hi, y_lo, sw128_offset(c + 0, kk, DV, El::E), ts[u].x);
-        put<BF16>(y_hi, y_lo, sw128_offset(c + 1, kk, DV, El::E), ts[u].y);
-        put<BF16>(y_hi, y_lo, sw128_offset(c + 2, kk, DV, El::E), ts[u].z);
-        put<BF16>(y_hi, y_lo, sw128_offset(c + 3, kk, DV, El::E), ts[u].w);
-    }
-    if (tid < kK) z_s[tid] = BF16 ? bf16r(zk) : zk;
-    // Gamma_K chunk -> X (element (j, k)); a warp covers whole rows
-#pragma unroll
-    for (int u = 0; u < PG; ++u) {
-        const int f = tid + u * kTCThreads, j = f / PER_ROW, q = f % PER_ROW;
-        if constexpr (BF16) {
-            *reinterpret_cast<uint4 *>(x_hi + sw128_offset(j, 8 * q, kC, 2)) = tg[u];
-        } else {
-            const float4 t = tg[u];
-            const float4 hv = make_float4(tf32_hi(t.x), tf32_hi(t.y), tf32_hi(t.z), tf32_hi(t.w));
-            const float4 lv = make_float4(t.x - hv.x, t.y - hv.y, t.z - hv.z, t.w - hv.w);
-            const uint32_t off = sw128_offset(j, 4 * q, kC, 4);
-            *reinterpret_cast<float4 *>(x_hi + off) = hv;
-            *reinterpret_cast<float4 *>(x_lo + off) = lv;
+        for (int u = 0; u < PER; ++u) {
+            const int f = tid + u * kTCThreads, c = f / (kK / 4), k4 = 4 * (f % (kK / 4));
+            const float4 t = reinterpret_cast<const float4 *>(st + (long long)c * kK)[k4 / 4];
+            const uint2 p = make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
+            *reinterpret_cast<uint2 *>(y_hi + sw128_offset(c, k4, DV, 2)) = p;
         }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
+    bool ok = mbar_wait(smem_addr(bar), 0);
 
-    // A = Gamma_Q: this thread's row i, operand columns [64h, 64h + 64); partial Gamma_Q,i . Z
+    // A = Gamma_Q (row i, operand columns [64h, 64h + 64)) from its landing tile; partial Gamma_Q,i . Z
     {
+        float xq[64];
+#pragma unroll
+        for (int q = 0; q < 64 / 4; ++q) {
+            const int k = 64 * h + 4 * q;
+            if constexpr (BF16) {
+                const uint2 t = *reinterpret_cast<const uint2 *>(x_lo + sw128_offset(i, k, kC, 2));
+                xq[4 * q] = __uint_as_float(t.x << 16);
+                xq[4 * q + 1] = __uint_as_float(t.x & 0xffff0000u);
+                xq[4 * q + 2] = __uint_as_float(t.y << 16);
+                xq[4 * q + 3] = __uint_as_float(t.y & 0xffff0000u);
+            } else {
+                const float4 t = *reinterpret_cast<const float4 *>(x_lo + sw128_offset(i, k, kC, 4));
+                xq[4 * q] = t.x; xq[4 * q + 1] = t.y; xq[4 * q + 2] = t.z; xq[4 * q + 3] = t.w;
+            }
+        }
         float qz = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) qz = fmaf(xq[j], z_s[64 * h + j], qz);
         part[h * kK + i] = qz;
         put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, xq);
+    }
+    if constexpr (!BF16) {
+        __syncthreads();   // Gamma_Q has been read from X_lo
+        // exact remainders of Gamma_K (X_lo) and of the carried memory (Y_lo), in place
+        constexpr int PX = Sm::GK / 16 / kTCThreads, PY = Sm::Y / 16 / kTCThreads;
+#pragma unroll 4
+        for (int u = 0; u < PX; ++u) {
+            const uint32_t off = 16 * (tid + u * kTCThreads);
+            const float4 t = *reinterpret_cast<const float4 *>(x_hi + off);
+            *reinterpret_cast<float4 *>(x_lo + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
+                                                                  t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
+        }
+#pragma unroll 4
+        for (int u = 0; u < PY; ++u) {
+            const uint32_t off = 16 * (tid + u * kTCThreads);
+            const float4 t = *reinterpret_cast<const float4 *>(y_hi + off);
+            *reinterpret_cast<float4 *>(y_lo + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
+                                                                  t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
+        }
     }
     tmem_wait_st();
     fence_proxy_async();
@@ -415,17 +434,20 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     fence_after_sync();
     if (tid == 0) {
         mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, false);    // U = Gq Vt
-        mma_commit(smem_addr(bar));
-        mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
         mma_commit(smem_addr(bar + 1));
+        mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
+        mma_commit(smem_addr(bar + 2));
     }
     __syncwarp();
-    bool ok = mbar_wait(smem_addr(bar), 0);
+    ok = mbar_wait(smem_addr(bar + 2), 0) && ok;   // P done (and U, committed earlier)
     fence_after_sync();
-    // Y is free again: stage V^T while P is being computed
-    stage_vt<BF16, DV>(v, v_bf16, bh * N + c0, nr, y_hi, y_lo, tid);
-    ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
-    fence_after_sync();
+    if (tid == 0) {
+        // X is free: bring V in while P_m is formed
+        fence_proxy_async();
+        mbar_expect_tx(smem_addr(bar + 3), (uint32_t)(kC * DV * ev));
+        for (int a = 0; a < DV / vbox; ++a)
+            tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.v, a * vbox, row0, smem_addr(bar + 3));
+    }
     // P_m = P with j > i zeroed replaces Gamma_Q as the A operand; row sums on CUDA cores
     {
         float x[64];
@@ -446,6 +468,29 @@ __global__ void __launch_bounds__(kTCThreads, 1)
         part[(2 + h) * kK + i] = ps;
         put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, x);
     }
+    ok = mbar_wait(smem_addr(bar + 3), 0) && ok;
+    // V^T (element (c, j)) into Y from the V tile in X; lanes run over tokens
+    {
+        constexpr int PER = (kC * DV / 4) / kTCThreads;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int f = tid + u * kTCThreads, j = f % kC, c4 = 4 * (f / kC);
+            float4 t;
+            if (j >= nr) {
+                t = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (v_bf16) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(x_hi + sw128_offset(j, c4, kC, 2));
+                t = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            } else {
+                t = *reinterpret_cast<const float4 *>(x_hi + sw128_offset(j, c4, kC, 4));
+            }
+            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 0, j, DV, El::E), t.x);
+            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 1, j, DV, El::E), t.y);
+            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 2, j, DV, El::E), t.z);
+            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 3, j, DV, El::E), t.w);
+        }
+    }
     tmem_wait_st();
     fence_proxy_async();
     fence_before_sync();
@@ -453,10 +498,10 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     fence_after_sync();
     if (tid == 0) {
         mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, true);     // U += P_m V
-        mma_commit(smem_addr(bar + 2));
+        mma_commit(smem_addr(bar + 4));
     }
     __syncwarp();
-    ok = mbar_wait(smem_addr(bar + 2), 0) && ok;
+    ok = mbar_wait(smem_addr(bar + 4), 0) && ok;
     fence_after_sync();
 
     const float den = part[i] + part[kK + i] + part[2 * kK + i] + part[3 * kK + i] + eps;
@@ -506,9 +551,17 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     constexpr size_t smem = OutSmem<BF16, DV>::bytes;
     static cudaError_t attr = allow_smem(k_chunk_out_tc<BF16, DV>, smem);
     if (attr != cudaSuccess) return attr;
+    OutMaps maps;
+    const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
+    bool ok = make_tma_2d(&maps.gq, gq, BF16, rows, kK, kC) && make_tma_2d(&maps.gk, gk, BF16, rows, kK, kC) &&
+              make_tma_2d(&maps.v, v, dm.v_bf16, rows, DV, kC);
+    if (!BF16)
+        ok = ok && make_tma_2d(&maps.s, states, false, (unsigned long long)dm.BH() * dm.nblk() * (DV + 1), kK, DV);
+    else
+        maps.s = maps.gq;
+    if (!ok) return cudaErrorInvalidValue;
     dim3 grid(dm.nblk(), (unsigned)dm.BH());
-    k_chunk_out_tc<BF16, DV><<<grid, kTCThreads, smem, st>>>(dm.N, dm.eps, gq, gk, v, dm.v_bf16, states, dm.nblk(),
-                                                             out);
+    k_chunk_out_tc<BF16, DV><<<grid, kTCThreads, smem, st>>>(maps, dm.N, dm.eps, dm.v_bf16, states, dm.nblk(), out);
     return cudaGetLastError();
 }
 

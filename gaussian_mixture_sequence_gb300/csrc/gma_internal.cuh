@@ -10,6 +10,7 @@
 //                                            s = 1/sigma;  cst[h][k] = log pi_k - 1/2 sum_d log sigma^2
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -63,8 +64,8 @@ __device__ __forceinline__ void store_elem(void *base, long long i, float v, boo
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st);
-cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
-                        int ldg, bool gamma_bf16, cudaStream_t st);
+cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const struct PrunedImages *img,
+                        const void *x, void *gamma, int ldg, bool gamma_bf16, cudaStream_t st);
 cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, float *partial,
                                cudaStream_t st);
 cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total,
@@ -74,10 +75,25 @@ cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const 
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
                           const void *kx, const void *v, float *state, float *out, cudaStream_t st);
 
+// Row-major [rows][cols] tensor map with boxes of 128 bytes x box_rows and the
+// 128-byte swizzle (gma_tma.cu).  Returns false if it cannot be encoded.
+bool make_tma_2d(CUtensorMap *m, const void *base, bool bf16, unsigned long long rows, unsigned long long cols,
+                 unsigned box_rows);
+
+// Per-head images the bounded routing kernel copies into shared memory.
+struct PrunedImages {
+    unsigned char *w;   // [H][32768 B]: bf16 bound matrix, 128-byte-swizzled K-major
+    float4 *p;          // [H][128][33]: packed exact parameters, rows padded by one word
+    float *c;           // [H][4][128]: c_k, c'_k, A_k, M_k
+};
+constexpr size_t kPrunedWBytes = 32768, kPrunedPBytes = 128 * 33 * 16, kPrunedCBytes = 4 * 128 * 4;
+
 // Responsibilities for K = 128, d_route = 64 with a tensor-core bound (gma_resp_tc.cu).
 bool resp_pruned_applies(const Dims &dm);
-cudaError_t launch_resp_pruned(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
-                               int ldg, bool gamma_bf16, cudaStream_t st);
+cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages &img,
+                               cudaStream_t st);
+cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
+                               bool gamma_bf16, cudaStream_t st);
 
 // Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
 bool tc_path_eligible(int K, int DV, bool g_bf16);

@@ -80,13 +80,18 @@ __global__ void __launch_bounds__(kThreads)
 // Serial scan over blocks for every state element (fixed order, deterministic).
 //   exclusive: partial[bh][blk] <- state_in + sum_{b < blk} partial[bh][b]
 //   total (nullable) <- state_in + sum_b partial[bh][b]
+//   tr_k > 0: blocks hold Vt transposed (tr_dv rows of tr_k, then Z); state_in / total
+//   keep the caller layout (Vt as tr_k rows of tr_dv, then Z).
 __global__ void __launch_bounds__(kThreads) k_scan(long long SZ, int nblk, float *__restrict__ partial,
-                                                   const float *state_in, float *total, bool exclusive)
+                                                   const float *state_in, float *total, bool exclusive, int tr_k,
+                                                   int tr_dv)
 {
     const long long e = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (e >= SZ) return;
     const long long bh = blockIdx.y;
-    float run = state_in ? state_in[bh * SZ + e] : 0.f;
+    long long eu = e;   // the same element in the caller's layout
+    if (tr_k > 0 && e < (long long)tr_k * tr_dv) eu = (e % tr_k) * tr_dv + e / tr_k;
+    float run = state_in ? state_in[bh * SZ + eu] : 0.f;
     float *__restrict__ p = partial + bh * nblk * SZ + e;
     constexpr int U = 32; // loads in flight per thread
     int b = 0;
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) k_scan(long long SZ, int nblk, float
         if (exclusive) p[(long long)b * SZ] = run;
         run += t;
     }
-    if (total) total[bh * SZ + e] = run;
+    if (total) total[bh * SZ + eu] = run;
 }
 
 // Output of one block of kBlockRows rows, chunk by chunk (C rows each).
@@ -354,7 +359,9 @@ cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, f
 {
     const long long SZ = dm.state_size();
     dim3 grid((unsigned)((SZ + kThreads - 1) / kThreads), (unsigned)dm.BH());
-    k_scan<<<grid, kThreads, 0, st>>>(SZ, dm.nblk(), partial, state_in, total, exclusive);
+    const bool tr = tc_path_applies(dm);
+    k_scan<<<grid, kThreads, 0, st>>>(SZ, dm.nblk(), partial, state_in, total, exclusive, tr ? dm.K : 0,
+                                      tr ? dm.DV : 0);
     return cudaGetLastError();
 }
 

@@ -248,10 +248,10 @@ cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float 
     return cudaGetLastError();
 }
 
-cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
-                        int ldg, bool gamma_bf16, cudaStream_t st)
+cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages *img,
+                        const void *x, void *gamma, int ldg, bool gamma_bf16, cudaStream_t st)
 {
-    if (resp_pruned_applies(dm)) return launch_resp_pruned(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, gamma_bf16, st);
     switch (dm.D) {
     case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
     case 32: return launch_resp_d<32>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);

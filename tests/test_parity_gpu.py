@@ -126,9 +126,10 @@ def test_causal(wl, sample, chunk):
     _report(f"causal state {wl.name}", normwise(c.pick(st), ref_st), tol)
 
 
-def test_causal_state_carry():
+@pytest.mark.parametrize("K", [32, 128])
+def test_causal_state_carry(K):
     """Two calls chained through state_out -> state_in equal one call on the whole sequence."""
-    wl = W["tiny"].with_(B=2, H=2, N=600, K=32)
+    wl = W["tiny"].with_(B=2, H=2, N=600, K=K, d=64, dv=64)
     c = Case(wl)
     q, k, v = c.dev["seq"]
     from gaussian_mixture_sequence_gb300 import gma
