@@ -80,6 +80,13 @@ cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, c
 bool make_tma_2d(CUtensorMap *m, const void *base, bool bf16, unsigned long long rows, unsigned long long cols,
                  unsigned box_rows);
 
+// Rank-3 variant: [d2][d1][d0] with boxes of 128 bytes x box1 x 1; coordinates
+// past d1 are zero-filled on loads and skipped on stores.
+bool make_tma_3d(CUtensorMap *m, const void *base, bool bf16, unsigned long long d0, unsigned long long d1,
+                 unsigned long long d2, unsigned box1);
+// Number of SMs of the current device (persistent grids).
+int sm_count();
+
 // Per-head images the bounded routing kernel copies into shared memory.
 struct PrunedImages {
     unsigned char *w;   // [H][32768 B]: bf16 bound matrix, 128-byte-swizzled K-major

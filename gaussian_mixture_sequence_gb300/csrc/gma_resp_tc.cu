@@ -19,11 +19,12 @@
 // exact fp32 evaluation as the dense kernel (one packed FMA for (x - mu)/sigma,
 // one for the square-accumulate, per feature pair).
 //
-// One CTA = 16 warps over tiles of 128 rows: the four warps 4q + w' share the
-// TMEM lanes 32 w' .. +31 (one row each) and take component quarter q.  The
-// per-head bound matrix, padded parameters and constants are built once per
-// call by k_prep_pruned and bulk-copied into shared memory; routing rows
-// arrive by double-buffered TMA.
+// One persistent CTA per SM, 16 warps, tiles of 128 rows: the four warps
+// 4q + w' share the TMEM lanes 32 w' .. +31 (one row each) and take component
+// quarter q.  The per-head bound matrix, padded parameters and constants are
+// built once per call by k_prep_pruned and bulk-copied into shared memory;
+// routing rows arrive by TMA (the next tile's load is issued as soon as the
+// current one has been read) and output tiles leave by TMA stores.
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -43,9 +44,10 @@ constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulatio
 struct PrunedSmem {
     static constexpr uint32_t W = kPrunedWBytes;                        // bf16 [128][128], SW128
     static constexpr uint32_t X = kPRows * kPD * 4;                     // one routing tile (fp32 worst case)
+    static constexpr uint32_t O = kPRows * kPK * 4;                     // one output tile (fp32 worst case)
     static constexpr uint32_t P = kPrunedPBytes;                        // float4 [128][33]
     static constexpr uint32_t F = (4 + 12) * kPK * 4;                   // constants + exchange slots
-    static constexpr size_t bytes = 1024 + W + 2 * X + P + F + 64;
+    static constexpr size_t bytes = 1024 + W + X + O + P + F + 64;
 };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b)
@@ -98,83 +100,87 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
     }
 }
 
+// Persistent: CTA b handles the work items [b * per, (b + 1) * per) of the
+// list (slice, tile of 128 rows) in order, reloading the per-head images only
+// when the head changes.  The output tile is assembled in shared memory and
+// written by TMA stores that stop at the slice's last row.
 __global__ void __launch_bounds__(kPThreads, 1)
-    k_resp_pruned(const __grid_constant__ CUtensorMap xmap, int N, int H, bool x_bf16,
-                  const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
-                  const float *__restrict__ cimg, void *__restrict__ gamma, int ldg, bool g_bf16)
+    k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap, int N, int H,
+                  int BH, bool x_bf16, const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
+                  const float *__restrict__ cimg, bool g_bf16)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *w_s = sm;                                                  // B operand W
-    unsigned char *xb = sm + PrunedSmem::W;                                   // [2] routing tiles
-    float4 *p_s = reinterpret_cast<float4 *>(xb + 2 * PrunedSmem::X);        // exact parameters
+    unsigned char *xb = sm + PrunedSmem::W;                                   // routing tile
+    unsigned char *ob = xb + PrunedSmem::X;                                   // output tile
+    float4 *p_s = reinterpret_cast<float4 *>(ob + PrunedSmem::O);            // exact parameters
     float *f_s = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(p_s) + PrunedSmem::P);
     const float *c_s = f_s, *cp_s = f_s + kPK, *a_s = f_s + 2 * kPK, *m_s = f_s + 3 * kPK;
     float *ex0 = f_s + 4 * kPK;    // [4][128] exchange slots between the quarters of a row
     float *ex1 = f_s + 8 * kPK;
     float *ex2 = f_s + 12 * kPK;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 16 * kPK);   // setup, mma, x[2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 16 * kPK);   // images, mma, x
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp >> 2;                      // component quarter
     const uint32_t lane0 = 32 * (warp & 3);
     const int i = lane0 + lane;                   // row of the tile (TMEM lane)
-    const long long bh = blockIdx.y;
-    const int head = (int)(bh % H);
-    const int row_begin = blockIdx.x * kPRowsPerCta;
-    const int row_end = min(N, row_begin + kPRowsPerCta);
-    const int ntiles = (row_end - row_begin + kPRows - 1) / kPRows;
+    const int tps = (N + kPRows - 1) / kPRows;    // tiles per slice
+    const long long items = (long long)BH * tps;
+    const long long per = (items + gridDim.x - 1) / gridDim.x;
+    const long long it0 = (long long)blockIdx.x * per;
+    const long long it1 = it0 + per < items ? it0 + per : items;
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
+    const int ge = g_bf16 ? 2 : 4;
     constexpr uint32_t A_COL = 0, D_COL = 128;
 
-    auto load_x = [&](int t) {   // one thread: TMA of tile t into buffer t & 1
-        const uint32_t b = smem_addr(bar + 2 + (t & 1));
-        unsigned char *dst = xb + (t & 1) * PrunedSmem::X;
-        const int y = (int)(bh * N + row_begin + t * kPRows);
-        mbar_expect_tx(b, xbytes);
-        if (x_bf16) {
-            tma_load_2d(smem_addr(dst), &xmap, 0, y, b);
-        } else {
-            tma_load_2d(smem_addr(dst), &xmap, 0, y, b);
-            tma_load_2d(smem_addr(dst + kPRows * 128), &xmap, 32, y, b);
-        }
+    auto load_x = [&](long long it) {   // one thread: TMA of item it's rows
+        const int bh = (int)(it / tps), t = (int)(it % tps);
+        mbar_expect_tx(smem_addr(bar + 2), xbytes);
+        tma_load_3d(smem_addr(xb), &xmap, 0, t * kPRows, bh, smem_addr(bar + 2));
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kPRows * 128), &xmap, 32, t * kPRows, bh, smem_addr(bar + 2));
     };
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 256);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        mbar_expect_tx(smem_addr(bar), kPrunedWBytes + kPrunedPBytes + kPrunedCBytes);
-        bulk_g2s(smem_addr(w_s), wimg + (long long)head * kPrunedWBytes, kPrunedWBytes, smem_addr(bar));
-        bulk_g2s(smem_addr(p_s), pimg + (long long)head * kPK * kPStride, kPrunedPBytes, smem_addr(bar));
-        bulk_g2s(smem_addr(f_s), cimg + (long long)head * 4 * kPK, kPrunedCBytes, smem_addr(bar));
-        if (ntiles > 0) load_x(0);
+        if (it0 < it1) load_x(it0);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t id = idesc(128, kPK, kFmtBF16);
-    bool ok = mbar_wait(smem_addr(bar), 0);
+    bool ok = true;
+    int head = -1, nimg = 0;
 
-    for (int t = 0; t < ntiles; ++t) {
-        if (tid == 0 && t + 1 < ntiles) {
-            fence_proxy_async();
-            load_x(t + 1);
+    for (long long it = it0; it < it1; ++it) {
+        const int j = (int)(it - it0);
+        const int bh = (int)(it / tps), t = (int)(it % tps);
+        if (bh % H != head) {   // (re)load the images of this item's head
+            head = bh % H;
+            if (tid == 0) {
+                fence_proxy_async();
+                mbar_expect_tx(smem_addr(bar), kPrunedWBytes + kPrunedPBytes + kPrunedCBytes);
+                bulk_g2s(smem_addr(w_s), wimg + (long long)head * kPrunedWBytes, kPrunedWBytes, smem_addr(bar));
+                bulk_g2s(smem_addr(p_s), pimg + (long long)head * kPK * kPStride, kPrunedPBytes, smem_addr(bar));
+                bulk_g2s(smem_addr(f_s), cimg + (long long)head * 4 * kPK, kPrunedCBytes, smem_addr(bar));
+            }
+            ok = mbar_wait(smem_addr(bar), (uint32_t)(nimg & 1)) && ok;
+            ++nimg;
         }
-        const int row = row_begin + t * kPRows + i;
-        const bool valid = row < row_end;
-        ok = mbar_wait(smem_addr(bar + 2 + (t & 1)), (uint32_t)((t >> 1) & 1)) && ok;
+        ok = mbar_wait(smem_addr(bar + 2), (uint32_t)(j & 1)) && ok;
         // the row (every quarter holds all 64 features) and its sums for the bound
-        const unsigned char *xt = xb + (t & 1) * PrunedSmem::X;
         float2 xr[kPDP];
         if (x_bf16) {
 #pragma unroll
             for (int g = 0; g < kPD / 8; ++g) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(xt + sw128_offset(i, 8 * g, kPRows, 2));
+                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 8 * g, kPRows, 2));
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         } else {
 #pragma unroll
             for (int g = 0; g < kPD / 4; ++g) {
-                const float4 u = *reinterpret_cast<const float4 *>(xt + sw128_offset(i, 4 * g, kPRows, 4));
+                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 4 * g, kPRows, 4));
                 xr[2 * g] = make_float2(u.x, u.y);
                 xr[2 * g + 1] = make_float2(u.z, u.w);
             }
@@ -198,17 +204,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         {
             uint32_t p[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float2 v = (q & 1) ? xr[16 + j] : xr[j];   // static indices keep xr in registers
-                p[j] = q < 2 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
+            for (int jj = 0; jj < 16; ++jj) {
+                const float2 v = (q & 1) ? xr[16 + jj] : xr[jj];   // static indices keep xr in registers
+                p[jj] = q < 2 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
             }
             tmem_st16(tmem_at(tbase, lane0, A_COL + 16 * q), p);
         }
         tmem_wait_st();
         fence_before_sync();
-        __syncthreads();
+        __syncthreads();   // the routing tile has been read; A is in TMEM
         fence_after_sync();
         if (tid == 0) {
+            if (it + 1 < it1) {
+                fence_proxy_async();
+                load_x(it + 1);
+            }
 #pragma unroll 1
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t kb = kk * 32;
@@ -219,7 +229,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mma_commit(smem_addr(bar + 1));
         }
         __syncwarp();
-        ok = mbar_wait(smem_addr(bar + 1), (uint32_t)(t & 1)) && ok;
+        ok = mbar_wait(smem_addr(bar + 1), (uint32_t)(j & 1)) && ok;
         fence_after_sync();
 
         // bound: best lower bound of this quarter, then of the row; then the kept set
@@ -228,10 +238,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_ld16(tmem_at(tbase, lane0, D_COL + 32 * q + 16 * b), r);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int k = 32 * q + 16 * b + j;
-                lt[j] = __uint_as_float(r[j]) + cp_s[k];
-                dk[j] = fmaf(kPU, fmaf(0.5f * a_s[k], s2, m_s[k] * s1), 1e-3f);
+            for (int jj = 0; jj < 16; ++jj) {
+                const int k = 32 * q + 16 * b + jj;
+                lt[jj] = __uint_as_float(r[jj]) + cp_s[k];
+                dk[jj] = fmaf(kPU, fmaf(0.5f * a_s[k], s2, m_s[k] * s1), 1e-3f);
             }
         };
         float lo_max = -FLT_MAX;
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             float lt[16], dk[16];
             bound(b, lt, dk);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) lo_max = fmaxf(lo_max, lt[j] - dk[j]);
+            for (int jj = 0; jj < 16; ++jj) lo_max = fmaxf(lo_max, lt[jj] - dk[jj]);
         }
         ex0[q * kPK + i] = lo_max;
         __syncthreads();
@@ -252,8 +262,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             float lt[16], dk[16];
             bound(b, lt, dk);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (!ok || lt[j] + dk[j] >= keep_from) mask |= 1u << (16 * b + j);
+            for (int jj = 0; jj < 16; ++jj)
+                if (!ok || lt[jj] + dk[jj] >= keep_from) mask |= 1u << (16 * b + jj);
         }
 
         // exact log-joint of a kept component
@@ -283,6 +293,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         ex1[q * kPK + i] = mt;
         ex2[q * kPK + i] = st;
+        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
         __syncthreads();
         float m = ex1[i];
 #pragma unroll
@@ -291,27 +302,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int g = 0; g < 4; ++g) ssum += ex2[g * kPK + i] * expf(ex1[g * kPK + i] - m);
         const float inv = 1.0f / ssum;
-        // exact pass 2: zero this quarter of the output row, then write the kept posteriors
-        if (valid) {
-            const long long go = (bh * N + row) * (long long)ldg + 32 * q;
-            if (g_bf16) {
-                uint4 *z = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(gamma) + go);
+        // exact pass 2: this quarter of the output row in the output tile (zeros, then the kept posteriors)
+        if (g_bf16) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) z[g] = make_uint4(0, 0, 0, 0);
-            } else {
-                float4 *z = reinterpret_cast<float4 *>(static_cast<float *>(gamma) + go);
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 32 * q + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+        } else {
 #pragma unroll
-                for (int g = 0; g < 8; ++g) z[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            for (uint32_t mm = mask; mm; mm &= mm - 1) {
-                const int b = __ffs(mm) - 1;
-                store_elem(gamma, go + b, expf(exact(32 * q + b) - m) * inv, g_bf16);
-            }
+            for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * q + 4 * g, kPRows, 4)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        for (uint32_t mm = mask; mm; mm &= mm - 1) {
+            const int k = 32 * q + __ffs(mm) - 1;
+            const float gk = expf(exact(k) - m) * inv;
+            if (g_bf16)
+                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) = __float2bfloat16_rn(gk);
+            else
+                *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = gk;
+        }
+        fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
         fence_before_sync();
-        __syncthreads();   // exchange slots, the accumulator and this x buffer are reused
+        __syncthreads();
         fence_after_sync();
+        if (tid == 0) {
+            for (int a = 0; a < kPK * ge / 128; ++a)
+                tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 256);
@@ -334,11 +354,14 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
     constexpr size_t smem = PrunedSmem::bytes;
     static cudaError_t attr = allow_smem(k_resp_pruned, smem);
     if (attr != cudaSuccess) return attr;
-    CUtensorMap xmap;
-    if (!make_tma_2d(&xmap, x, dm.x_bf16, (unsigned long long)dm.BH() * dm.N, kPD, kPRows))
+    if (ldg != kPK) return cudaErrorInvalidValue;
+    CUtensorMap xmap, gmap;
+    if (!make_tma_3d(&xmap, x, dm.x_bf16, kPD, dm.N, dm.BH(), kPRows) ||
+        !make_tma_3d(&gmap, gamma, gamma_bf16, kPK, dm.N, dm.BH(), kPRows))
         return cudaErrorInvalidValue;
-    dim3 grid((dm.N + kPRowsPerCta - 1) / kPRowsPerCta, (unsigned)dm.BH());
-    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, dm.N, dm.H, dm.x_bf16, img.w, img.p, img.c, gamma, ldg,
+    const long long items = dm.BH() * ((dm.N + kPRows - 1) / kPRows);
+    const int grid = (int)(items < sm_count() ? items : sm_count());
+    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, dm.N, dm.H, (int)dm.BH(), dm.x_bf16, img.w, img.p, img.c,
                                                  gamma_bf16);
     return cudaGetLastError();
 }

@@ -40,4 +40,32 @@ bool make_tma_2d(CUtensorMap *m, const void *base, bool bf16, unsigned long long
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tma_3d(CUtensorMap *m, const void *base, bool bf16, unsigned long long d0, unsigned long long d1,
+                 unsigned long long d2, unsigned box1)
+{
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const unsigned e = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * e, d0 * d1 * e};
+    cuuint32_t box[3] = {128 / e, box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    static int n = [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return 152;
+        return v;
+    }();
+    return n;
+}
+
 } // namespace gma
