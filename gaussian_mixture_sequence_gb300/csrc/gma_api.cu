@@ -25,7 +25,7 @@ gma_status make_dims_raw(const gma_shape *s, Dims *dm);
 gma_status make_dims(const gma_shape *s, Dims *dm, gma_op op = GMA_OP_CAUSAL)
 {
     const gma_status st = make_dims_raw(s, dm);
-    if (st == GMA_OK && op != GMA_OP_CAUSAL && dm->C == 128) {
+    if (st == GMA_OK && op != GMA_OP_CAUSAL && op != GMA_OP_BIDIR && dm->C == 128) {
         dm->C = 64;
         dm->blk = kBlockRows;
     }
@@ -242,12 +242,21 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, dm.g_bf16, st));
     GMA_CUDA(mk.mark("resp_k"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, dm.g_bf16, st));
-    GMA_CUDA(mk.mark("block_state"));
-    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
-    GMA_CUDA(mk.mark("state_reduce"));
-    GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st));
-    GMA_CUDA(mk.mark("bidir_read"));
-    GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
+    if (tc_path_applies(dm)) {
+        GMA_CUDA(mk.mark("chunk_state_tc"));
+        GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
+        GMA_CUDA(mk.mark("state_reduce"));
+        GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st, true));
+        GMA_CUDA(mk.mark("bidir_read_tc"));
+        GMA_CUDA(launch_chunk_out_tc(dm, false, gq, gk, v, total, out, st));
+    } else {
+        GMA_CUDA(mk.mark("block_state"));
+        GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+        GMA_CUDA(mk.mark("state_reduce"));
+        GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st));
+        GMA_CUDA(mk.mark("bidir_read"));
+        GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
+    }
     GMA_CUDA(mk.finish());
     return GMA_OK;
 }
@@ -329,7 +338,7 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
         GMA_CUDA(mk.mark("state_scan"));
         GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
         GMA_CUDA(mk.mark("chunk_out_tc"));
-        GMA_CUDA(launch_chunk_out_tc(dm, gq, gk, v, partial, out, st));
+        GMA_CUDA(launch_chunk_out_tc(dm, true, gq, gk, v, partial, out, st));
     } else {
         GMA_CUDA(mk.mark("block_state"));
         GMA_CUDA(launch_block_state(dm, gk, v, partial, st));

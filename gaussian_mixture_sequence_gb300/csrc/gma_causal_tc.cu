@@ -312,7 +312,9 @@ struct OutMaps {
     CUtensorMap gq, gk, v, s;   // s: carried memory blocks (fp32 operands only)
 };
 
-template <bool BF16, int DV>
+// CAUSAL = false gives the bidirectional read: U = Gamma_Q [Vt | Z] with the
+// total memory of the sequence (the same block for every chunk), no P.
+template <bool BF16, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kTCThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, float eps, bool v_bf16,
                    const float *__restrict__ states, int nblk, float *__restrict__ out)
@@ -350,20 +352,20 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        uint32_t bytes = 2 * Sm::GK + (BF16 ? 0u : (uint32_t)Sm::Y);
+        uint32_t bytes = (CAUSAL ? 2 : 1) * Sm::GK + (BF16 ? 0u : (uint32_t)Sm::Y);
         mbar_expect_tx(smem_addr(bar), bytes);
         for (int a = 0; a < kK / GBOX; ++a) {
-            tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.gk, a * GBOX, row0, smem_addr(bar));
+            if (CAUSAL) tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.gk, a * GBOX, row0, smem_addr(bar));
             tma_load_2d(smem_addr(x_lo + a * (kC * 128)), &maps.gq, a * GBOX, row0, smem_addr(bar));
         }
         if constexpr (!BF16) {
-            const int srow = (int)((bh * nblk + blockIdx.x) * (DV + 1));
+            const int srow = (int)((CAUSAL ? bh * nblk + blockIdx.x : bh) * (DV + 1));
             for (int a = 0; a < kK / 32; ++a)
                 tma_load_2d(smem_addr(y_hi + a * (DV * 128)), &maps.s, a * 32, srow, smem_addr(bar));
         }
     }
     const long long SZ = (long long)kK * DV + kK;
-    const float *st = states + (bh * nblk + blockIdx.x) * SZ;
+    const float *st = states + (CAUSAL ? bh * nblk + blockIdx.x : bh) * SZ;
     if (tid < kK) {
         const float zk = st[(long long)kK * DV + tid];
         z_s[tid] = BF16 ? bf16r(zk) : zk;
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(kTCThreads, 1)
         // exact remainders of Gamma_K (X_lo) and of the carried memory (Y_lo), in place
         constexpr int PX = Sm::GK / 16 / kTCThreads, PY = Sm::Y / 16 / kTCThreads;
 #pragma unroll 4
-        for (int u = 0; u < PX; ++u) {
+        for (int u = 0; u < (CAUSAL ? PX : 0); ++u) {
             const uint32_t off = 16 * (tid + u * kTCThreads);
             const float4 t = *reinterpret_cast<const float4 *>(x_hi + off);
             *reinterpret_cast<float4 *>(x_lo + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
@@ -435,10 +437,16 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     if (tid == 0) {
         mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, false);    // U = Gq Vt
         mma_commit(smem_addr(bar + 1));
-        mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
-        mma_commit(smem_addr(bar + 2));
+        if (CAUSAL) {
+            mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
+            mma_commit(smem_addr(bar + 2));
+        }
     }
     __syncwarp();
+    if constexpr (!CAUSAL) {
+        ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
+        fence_after_sync();
+    } else {
     ok = mbar_wait(smem_addr(bar + 2), 0) && ok;   // P done (and U, committed earlier)
     fence_after_sync();
     if (tid == 0) {
@@ -503,8 +511,9 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     __syncwarp();
     ok = mbar_wait(smem_addr(bar + 4), 0) && ok;
     fence_after_sync();
+    }
 
-    const float den = part[i] + part[kK + i] + part[2 * kK + i] + part[3 * kK + i] + eps;
+    const float den = part[i] + part[kK + i] + (CAUSAL ? part[2 * kK + i] + part[3 * kK + i] : 0.f) + eps;
     const float qnan = __int_as_float(0x7fc00000);
 #pragma unroll
     for (int cb = 0; cb < DV / 32; ++cb) {
@@ -544,24 +553,26 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
     return cudaGetLastError();
 }
 
-template <bool BF16, int DV>
+template <bool BF16, int DV, bool CAUSAL>
 cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v, const float *states, float *out,
                    cudaStream_t st)
 {
     constexpr size_t smem = OutSmem<BF16, DV>::bytes;
-    static cudaError_t attr = allow_smem(k_chunk_out_tc<BF16, DV>, smem);
+    static cudaError_t attr = allow_smem(k_chunk_out_tc<BF16, DV, CAUSAL>, smem);
     if (attr != cudaSuccess) return attr;
     OutMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
     bool ok = make_tma_2d(&maps.gq, gq, BF16, rows, kK, kC) && make_tma_2d(&maps.gk, gk, BF16, rows, kK, kC) &&
               make_tma_2d(&maps.v, v, dm.v_bf16, rows, DV, kC);
     if (!BF16)
-        ok = ok && make_tma_2d(&maps.s, states, false, (unsigned long long)dm.BH() * dm.nblk() * (DV + 1), kK, DV);
+        ok = ok && make_tma_2d(&maps.s, states, false,
+                               (unsigned long long)dm.BH() * (CAUSAL ? dm.nblk() : 1) * (DV + 1), kK, DV);
     else
         maps.s = maps.gq;
     if (!ok) return cudaErrorInvalidValue;
     dim3 grid(dm.nblk(), (unsigned)dm.BH());
-    k_chunk_out_tc<BF16, DV><<<grid, kTCThreads, smem, st>>>(maps, dm.N, dm.eps, dm.v_bf16, states, dm.nblk(), out);
+    k_chunk_out_tc<BF16, DV, CAUSAL><<<grid, kTCThreads, smem, st>>>(maps, dm.N, dm.eps, dm.v_bf16, states,
+                                                                      dm.nblk(), out);
     return cudaGetLastError();
 }
 
@@ -576,14 +587,19 @@ cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v,
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_chunk_out_tc(const Dims &dm, const void *gq, const void *gk, const void *v, const float *states,
-                                float *out, cudaStream_t st)
+cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
+                                const float *states, float *out, cudaStream_t st)
 {
     if (dm.g_bf16) {
-        if (dm.DV == 64) return out_tc<true, 64>(dm, gq, gk, v, states, out, st);
-        if (dm.DV == 128) return out_tc<true, 128>(dm, gq, gk, v, states, out, st);
+        if (dm.DV == 64)
+            return causal ? out_tc<true, 64, true>(dm, gq, gk, v, states, out, st)
+                          : out_tc<true, 64, false>(dm, gq, gk, v, states, out, st);
+        if (dm.DV == 128)
+            return causal ? out_tc<true, 128, true>(dm, gq, gk, v, states, out, st)
+                          : out_tc<true, 128, false>(dm, gq, gk, v, states, out, st);
     } else if (dm.DV == 64) {
-        return out_tc<false, 64>(dm, gq, gk, v, states, out, st);
+        return causal ? out_tc<false, 64, true>(dm, gq, gk, v, states, out, st)
+                      : out_tc<false, 64, false>(dm, gq, gk, v, states, out, st);
     }
     return cudaErrorInvalidValue;
 }

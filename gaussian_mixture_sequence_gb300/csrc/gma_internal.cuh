@@ -69,7 +69,7 @@ cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, con
 cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, float *partial,
                                cudaStream_t st);
 cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total,
-                        bool exclusive, cudaStream_t st);
+                        bool exclusive, cudaStream_t st, bool total_in_block_layout = false);
 cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
                              float *states, float *out, cudaStream_t st);
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
@@ -106,8 +106,8 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
 bool tc_path_eligible(int K, int DV, bool g_bf16);
 bool tc_path_applies(const Dims &dm);
 cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v, float *partial, cudaStream_t st);
-cudaError_t launch_chunk_out_tc(const Dims &dm, const void *gq, const void *gk, const void *v, const float *states,
-                                float *out, cudaStream_t st);
+cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
+                                const float *states, float *out, cudaStream_t st);
 
 // Sets the dynamic shared-memory limit of a kernel once per process.
 template <typename Kern>

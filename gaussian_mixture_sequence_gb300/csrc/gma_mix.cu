@@ -355,11 +355,11 @@ cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, fl
 }
 
 cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total, bool exclusive,
-                        cudaStream_t st)
+                        cudaStream_t st, bool total_in_block_layout)
 {
     const long long SZ = dm.state_size();
     dim3 grid((unsigned)((SZ + kThreads - 1) / kThreads), (unsigned)dm.BH());
-    const bool tr = tc_path_applies(dm);
+    const bool tr = tc_path_applies(dm) && !total_in_block_layout;
     k_scan<<<grid, kThreads, 0, st>>>(SZ, dm.nblk(), partial, state_in, total, exclusive, tr ? dm.K : 0,
                                       tr ? dm.DV : 0);
     return cudaGetLastError();

@@ -12,9 +12,10 @@
 // is one bf16 GEMM [x^2 | x] (128 x 128) times W (128 x 128 components) per
 // tile of 128 rows.  That form cancels badly, so it is used only as a bound:
 // with bf16 operands (unit roundoff 2^-9) and fp32 accumulation,
-//   |l~_ik - l_ik| <= delta_ik = U (1/2 A_k sum_d x_d^2 + M_k sum_d |x_d|) + 1e-3,
-// U = 4e-3, A_k = max_d a_kd, M_k = max_d |a_kd mu_kd|.  Component k is kept
-// when l~_ik + delta_ik >= max_j (l~_ij - delta_ij) - T, which keeps every
+//   |l~_ik - l_ik| <= delta_i = U (1/2 A sum_d x_d^2 + M sum_d |x_d|) + 1e-3,
+// U = 4e-3, A = max_kd a_kd, M = max_kd |a_kd mu_kd| over the head, and
+// sum_d |x_d| <= 8 (sum_d x_d^2)^(1/2) (Cauchy-Schwarz, d = 64).  Component k
+// is kept when l~_ik >= max_j l~_ij - T - 2 delta_i, which keeps every
 // component within T of the true maximum.  The kept components get the same
 // exact fp32 evaluation as the dense kernel (one packed FMA for (x - mu)/sigma,
 // one for the square-accumulate, per feature pair).
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
                 __float2bfloat16_rn(-s[j] * nm[j]);
         }
     }
+    __shared__ float red[2][kPK];
+    float *ch = cimg + (long long)h * 4 * kPK;
     if (tid < kPK) {
         float amu2 = 0.f, amax = 0.f, mmax = 0.f;
         for (int dp = 0; dp < kPDP; ++dp) {
@@ -92,11 +95,20 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
             mmax = fmaxf(mmax, fmaxf(fabsf(p.x * p.z), fabsf(p.y * p.w)));
         }
         const float c = cst[(long long)h * kPK + tid];
-        float *ch = cimg + (long long)h * 4 * kPK;
         ch[tid] = c;
         ch[kPK + tid] = c - 0.5f * amu2;
-        ch[2 * kPK + tid] = amax;
-        ch[3 * kPK + tid] = mmax;
+        red[0][tid] = amax;
+        red[1][tid] = mmax;
+    }
+    __syncthreads();
+    if (tid < kPK) {   // head-wide maxima A and M, stored in every slot
+        float a = 0.f, m = 0.f;
+        for (int k = 0; k < kPK; ++k) {
+            a = fmaxf(a, red[0][k]);
+            m = fmaxf(m, red[1][k]);
+        }
+        ch[2 * kPK + tid] = a;
+        ch[3 * kPK + tid] = m;
     }
 }
 
@@ -194,12 +206,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 xr[2 * g + 1] = make_float2(u.z, u.w);
             }
         }
-        float s2 = 0.f, s1 = 0.f;
+        float2 s2v = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < kPDP; ++g) {
-            s2 = fmaf(xr[g].x, xr[g].x, fmaf(xr[g].y, xr[g].y, s2));
-            s1 += fabsf(xr[g].x) + fabsf(xr[g].y);
-        }
+        for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
+        const float s2 = s2v.x + s2v.y;
+        // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0])
+        const float delta = fmaf(kPU, fmaf(0.5f * a_s[0], s2, m_s[0] * 8.f * sqrtf(s2)), 1e-3f);
         // A = [x^2 | x] in bf16: quarter q writes operand columns [16q, 16q + 16)
         {
             uint32_t p[16];
@@ -232,38 +244,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
         ok = mbar_wait(smem_addr(bar + 1), (uint32_t)(j & 1)) && ok;
         fence_after_sync();
 
-        // bound: best lower bound of this quarter, then of the row; then the kept set
-        auto bound = [&](int b, float (&lt)[16], float (&dk)[16]) {
+        // bound: best estimate of this quarter, then of the row; then the kept set
+        auto est = [&](int b, float (&lt)[16]) {
             uint32_t r[16];
             tmem_ld16(tmem_at(tbase, lane0, D_COL + 32 * q + 16 * b), r);
             tmem_wait_ld();
+            const float4 *c4 = reinterpret_cast<const float4 *>(cp_s + 32 * q + 16 * b);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int k = 32 * q + 16 * b + jj;
-                lt[jj] = __uint_as_float(r[jj]) + cp_s[k];
-                dk[jj] = fmaf(kPU, fmaf(0.5f * a_s[k], s2, m_s[k] * s1), 1e-3f);
+            for (int g = 0; g < 4; ++g) {
+                const float4 c = c4[g];
+                lt[4 * g] = __uint_as_float(r[4 * g]) + c.x;
+                lt[4 * g + 1] = __uint_as_float(r[4 * g + 1]) + c.y;
+                lt[4 * g + 2] = __uint_as_float(r[4 * g + 2]) + c.z;
+                lt[4 * g + 3] = __uint_as_float(r[4 * g + 3]) + c.w;
             }
         };
-        float lo_max = -FLT_MAX;
+        float e_max = -FLT_MAX;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            float lt[16], dk[16];
-            bound(b, lt, dk);
+            float lt[16];
+            est(b, lt);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) lo_max = fmaxf(lo_max, lt[jj] - dk[jj]);
+            for (int jj = 0; jj < 16; ++jj) e_max = fmaxf(e_max, lt[jj]);
         }
-        ex0[q * kPK + i] = lo_max;
+        ex0[q * kPK + i] = e_max;
         __syncthreads();
         const float keep_from =
-            fmaxf(fmaxf(ex0[i], ex0[kPK + i]), fmaxf(ex0[2 * kPK + i], ex0[3 * kPK + i])) - kPT;
+            fmaxf(fmaxf(ex0[i], ex0[kPK + i]), fmaxf(ex0[2 * kPK + i], ex0[3 * kPK + i])) - kPT - 2.f * delta;
         uint32_t mask = 0;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            float lt[16], dk[16];
-            bound(b, lt, dk);
+            float lt[16];
+            est(b, lt);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-                if (!ok || lt[jj] + dk[jj] >= keep_from) mask |= 1u << (16 * b + jj);
+            for (int jj = 0; jj < 16; ++jj) mask |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * b + jj);
         }
 
         // exact log-joint of a kept component

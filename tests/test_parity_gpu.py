@@ -79,6 +79,8 @@ def test_responsibilities_adversarial_rows():
     (W["tiny"].with_(mode="bidir"), None),
     (W["tiny"].with_(mode="bidir", B=2, H=3, N=1000, d=32, dv=128, K=40), None),
     (W["tiny"].with_(mode="bidir", N=1, K=16), None),
+    (W["tiny"].with_(mode="bidir", B=2, H=2, N=1000, d=64, dv=64, K=128), None),
+    (W["tiny"].with_(mode="bidir", B=1, H=2, N=300, d=32, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None),
     (W["bidir_16k_peaked"], 3),
     (W["causal_4k"].with_(mode="bidir", gemm_dtype="bf16"), 2),
 ])
