@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--workload", default="causal_16k_peaked")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batch", type=int, default=0,
+                   help="run the workload with this many sequences instead of its own B (profiling captures)")
     p.add_argument("--min-warmup-s", type=float, default=1.0,
                    help="keep warming up (at least --warmup steps) until this many seconds passed")
     return p.parse_args()
@@ -110,8 +112,8 @@ def stage_work(stage, wl):
     if stage in ("chunk_out", "chunk_out_tc"):
         fl = 2.0 * C * K + C * (dv + 1) + 2.0 * K * (dv + 1) + (0 if tc else 2.0 * K * (dv + 1))
         return fl * ht, ("tensor" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
-    if stage == "bidir_read":
-        return 2.0 * K * (dv + 1) * ht, "alu", (K * gb + 4 * dv) * ht + st * nblk
+    if stage in ("bidir_read", "bidir_read_tc"):
+        return 2.0 * K * (dv + 1) * ht, ("tensor" if tc else "alu"), (K * gb + 4 * dv) * ht + st * wl.B * wl.H
     if stage in ("state_scan", "state_reduce"):
         return 0.0, "alu", 2.0 * st * nblk
     return 0.0, "alu", 0.0
@@ -234,26 +236,38 @@ def dist_env():
     return world, rank, local
 
 
-def traffic_record(stage):
-    """DRAM bytes per launch of `stage` from the committed ncu summary, or None if
-    the kernel source changed since the counters were taken."""
+# The source file holding each stage's kernel; its hash (with the shared headers)
+# keys the committed DRAM counters, so a changed kernel reports no traffic.
+KERNEL_SOURCE = {
+    "prep_params": "gma_resp.cu", "prep_bound": "gma_resp_tc.cu",
+    "chunk_state_tc": "gma_causal_tc.cu", "chunk_out_tc": "gma_causal_tc.cu", "bidir_read_tc": "gma_causal_tc.cu",
+    "block_state": "gma_mix.cu", "state_scan": "gma_mix.cu", "state_reduce": "gma_mix.cu",
+    "chunk_out": "gma_mix.cu", "bidir_read": "gma_mix.cu", "decode": "gma_decode.cu",
+}
+
+
+def traffic_record(stage, wl):
+    """DRAM bytes per launch of `stage` on workload `wl` from the committed ncu
+    summary, or None if the kernel's source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    h = source_hash()
+    h = source_hash(stage, wl)
     for line in open(path):
         f = line.split()
-        if len(f) >= 4 and not line.startswith("#") and f[0] == stage and f[1] == h:
+        if len(f) >= 4 and not line.startswith("#") and f[0] == stage and f[1] == h and f[2] == wl.name:
             return float(f[3])
     return None
 
 
-def source_hash():
+def source_hash(stage, wl):
     d = os.path.join(ROOT, "gaussian_mixture_sequence_gb300", "csrc")
+    src = KERNEL_SOURCE.get(stage)
+    if src is None:  # routing: the pruned kernel where it applies, else the generic one
+        src = "gma_resp_tc.cu" if bounded_routing(wl) else "gma_resp.cu"
     m = hashlib.sha256()
-    for fn in sorted(os.listdir(d)):
-        if fn.endswith((".cu", ".cuh")):
-            m.update(open(os.path.join(d, fn), "rb").read())
+    for fn in ("gma_internal.cuh", "gma_tc.cuh", src):
+        m.update(open(os.path.join(d, fn), "rb").read())
     return m.hexdigest()[:16]
 
 
@@ -450,6 +464,8 @@ def main():
     world, rank, local = dist_env()
     from gaussian_mixture_sequence_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
+    if args.batch > 0:
+        wl = wl.with_(B=args.batch)
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
 
@@ -560,7 +576,7 @@ def main():
         cpu = cpu_baseline(wl)
 
     if rank == 0:
-        tr = traffic_record(dom)
+        tr = traffic_record(dom, wl)
         cfg = {"workload": wl.name, "mode": wl.mode, "B": wl.B, "H": wl.H, "N": wl.N, "d_route": wl.d,
                "d_v": wl.dv, "K": wl.K, "x_dtype": wl.x_dtype, "gemm_dtype": wl.gemm_dtype,
                "inputs": "peaked mixture around the K centres" if wl.dist == "peaked" else "N(0,1)"}

@@ -30,7 +30,10 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// One CTA per head.
+// Grid (H, ceil(K / 32)): each CTA recomputes its head's log-sum-exp of the
+// mixture logits (K <= 512 values) and prepares 32 components.
+constexpr int kPrepComps = 32;
+
 __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__restrict__ mu,
                                                    const float *__restrict__ var_raw,
                                                    const float *__restrict__ logit_pi,
@@ -38,7 +41,9 @@ __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__
 {
     __shared__ float red[kThreads / 32];
     __shared__ float bcast;
+    __shared__ float lsum[kThreads];
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k0 = blockIdx.y * kPrepComps, kn = min(kPrepComps, K - k0);
     const float *l = logit_pi + (long long)h * K;
 
     float m = -FLT_MAX;
@@ -67,18 +72,27 @@ __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__
     __syncthreads();
     const float lse = bcast;
 
+    // sum_d log sigma^2 of the CTA's components: 8 threads per component
     const float *vr = var_raw + (long long)h * K * D;
     const float *mh = mu + (long long)h * K * D;
-    for (int k = tid; k < K; k += kThreads) {
+    {
+        const int kk = tid / 8, part = tid % 8;
         float acc = 0.f;
-        for (int d = 0; d < D; ++d) acc += logf(softplus(vr[(long long)k * D + d]));
-        cst[(long long)h * K + k] = (l[k] - lse) - 0.5f * acc;
+        if (kk < kn)
+            for (int d = part; d < D; d += 8) acc += logf(softplus(vr[(long long)(k0 + kk) * D + d]));
+        lsum[tid] = acc;
+    }
+    __syncthreads();
+    if (tid < kn) {
+        float acc = 0.f;
+        for (int p = 0; p < 8; ++p) acc += lsum[tid * 8 + p];
+        cst[(long long)h * K + k0 + tid] = (l[k0 + tid] - lse) - 0.5f * acc;
     }
     const int DP = D / 2;
-    for (int i = tid; i < K * DP; i += kThreads) {
-        const long long e = 2LL * i; // k * D + 2 * dp
+    for (int i = tid; i < kn * DP; i += kThreads) {
+        const long long e = (long long)k0 * D + 2LL * i; // (k0 + i / DP) * D + 2 * (i % DP)
         float s0 = 1.0f / sqrtf(softplus(vr[e])), s1 = 1.0f / sqrtf(softplus(vr[e + 1]));
-        prm[(long long)h * K * DP + i] = make_float4(s0, s1, -mh[e] * s0, -mh[e + 1] * s1);
+        prm[(long long)h * K * DP + (long long)k0 * DP + i] = make_float4(s0, s1, -mh[e] * s0, -mh[e + 1] * s1);
     }
 }
 
@@ -244,7 +258,8 @@ cudaError_t launch_resp_d(const Dims &dm, const float4 *prm, const float *cst, c
 
 cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st)
 {
-    k_prep<<<dm.H, kThreads, 0, st>>>(dm.K, dm.D, p.mu, p.var_raw, p.logit_pi, prm, cst);
+    dim3 grid(dm.H, (dm.K + kPrepComps - 1) / kPrepComps);
+    k_prep<<<grid, kThreads, 0, st>>>(dm.K, dm.D, p.mu, p.var_raw, p.logit_pi, prm, cst);
     return cudaGetLastError();
 }
 

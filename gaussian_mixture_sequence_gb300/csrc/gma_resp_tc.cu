@@ -63,15 +63,15 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
                                                      unsigned char *__restrict__ wimg, float4 *__restrict__ pimg,
                                                      float *__restrict__ cimg)
 {
-    const int h = blockIdx.x, tid = threadIdx.x;
+    const int h = blockIdx.x, tid = blockIdx.y * 256 + threadIdx.x, nthr = gridDim.y * 256;
     const float4 *ph = prm + (long long)h * kPK * kPDP;
     unsigned char *wh = wimg + (long long)h * kPrunedWBytes;
     float4 *pp = pimg + (long long)h * kPK * kPStride;
-    for (int e = tid; e < kPK * kPStride; e += 256) {
+    for (int e = tid; e < kPK * kPStride; e += nthr) {
         const int k = e / kPStride, dp = e % kPStride;
         pp[e] = dp < kPDP ? ph[k * kPDP + dp] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int e = tid; e < kPK * kPDP; e += 256) {
+    for (int e = tid; e < kPK * kPDP; e += nthr) {
         const int k = e / kPDP, dp = e % kPDP;
         const float4 p = ph[e];
         const float s[2] = {p.x, p.y}, nm[2] = {p.z, p.w};   // 1/sigma, -mu/sigma
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
                 __float2bfloat16_rn(-s[j] * nm[j]);
         }
     }
+    if (blockIdx.y != 0) return;
     __shared__ float red[2][kPK];
     float *ch = cimg + (long long)h * 4 * kPK;
     if (tid < kPK) {
@@ -358,7 +359,7 @@ bool resp_pruned_applies(const Dims &dm) { return dm.K == kPK && dm.D == kPD; }
 cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages &img,
                                cudaStream_t st)
 {
-    k_prep_pruned<<<dm.H, 256, 0, st>>>(prm, cst, img.w, img.p, img.c);
+    k_prep_pruned<<<dim3(dm.H, 4), 256, 0, st>>>(prm, cst, img.w, img.p, img.c);
     return cudaGetLastError();
 }
 
