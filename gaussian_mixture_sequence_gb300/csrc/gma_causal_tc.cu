@@ -71,10 +71,11 @@ template <bool BF16>
 constexpr uint32_t tile_bytes(uint32_t rows) { return rows * kK * Elem<BF16>::E; }
 
 // One MMA pass D (+)= A * B^T over the 128-deep contraction: A in TMEM
-// (columns from a_col), B a K-major SW128 tile of `nrows` rows.
+// (columns from a_col), B a K-major SW128 tile of `nrows` rows whose 128-byte
+// atom columns lie `atom_stride` bytes apart (nrows * 128 when packed).
 template <bool BF16>
-__device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a_col, const unsigned char *b, uint32_t nrows,
-                                         bool accumulate)
+__device__ __forceinline__ void mma_pass_at(uint32_t d_tmem, uint32_t a_col, const unsigned char *b, uint32_t nrows,
+                                            uint32_t atom_stride, bool accumulate)
 {
     using El = Elem<BF16>;
     const uint32_t id = idesc(128, nrows, El::FMT);
@@ -82,21 +83,28 @@ __device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a_col, const 
 #pragma unroll 1
     for (int kk = 0; kk < ksteps; ++kk) {
         const uint32_t kb = kk * 32;
-        const uint32_t boff = (kb >> 7) * (nrows * 128) + (kb & 127);
+        const uint32_t boff = (kb >> 7) * atom_stride + (kb & 127);
         mma_ts(!BF16, d_tmem, a_col + kk * El::COLS_PER_KSTEP, sdesc_sw128(smem_addr(b + boff)), id,
                (accumulate || kk > 0) ? 1u : 0u);
     }
+}
+template <bool BF16>
+__device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a_col, const unsigned char *b, uint32_t nrows,
+                                         bool accumulate)
+{
+    mma_pass_at<BF16>(d_tmem, a_col, b, nrows, nrows * 128, accumulate);
 }
 
 // All passes of D (+)= A * B^T: fp32 operands as hi*hi + hi*lo + lo*hi.
 template <bool BF16>
 __device__ __forceinline__ void mma_all(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo, const unsigned char *b_hi,
-                                        const unsigned char *b_lo, uint32_t nrows, bool accumulate)
+                                        const unsigned char *b_lo, uint32_t nrows, uint32_t atom_stride,
+                                        bool accumulate)
 {
-    mma_pass<BF16>(d_tmem, a_hi, b_hi, nrows, accumulate);
+    mma_pass_at<BF16>(d_tmem, a_hi, b_hi, nrows, atom_stride, accumulate);
     if constexpr (!BF16) {
-        mma_pass<BF16>(d_tmem, a_hi, b_lo, nrows, true);
-        mma_pass<BF16>(d_tmem, a_lo, b_hi, nrows, true);
+        mma_pass_at<BF16>(d_tmem, a_hi, b_lo, nrows, atom_stride, true);
+        mma_pass_at<BF16>(d_tmem, a_lo, b_hi, nrows, atom_stride, true);
     }
 }
 
@@ -292,243 +300,352 @@ __global__ void __launch_bounds__(kTCThreads, 2)
 }
 
 // ------------------------------------------------------------------------
-// Chunk output.  Warp w owns TMEM lanes (rows) 32 (w % 4) + lane and column
-// half w / 4 of every row-wise step.  Every tile arrives by TMA (bulk tensor
-// copies with the 128-byte swizzle) straight into the operand layout:
-//   X_hi <- Gamma_K (B of P), X_lo <- Gamma_Q (moved to TMEM as the A operand),
-//   Y_hi <- carried memory Vt^T (B of U = Gq Vt; fp32 operands only, the bf16
-//           path converts it with threads), later X <- V (transposed by threads
-//           into Y as the B of U += P_m V).
-// For fp32 operands the raw fp32 tile is the tf32 "hi" image (the tensor core
-// reads only the tf32 bits); threads derive the exact remainders in place.
+// Chunk output, persistent: CTA b takes the items [b * per, (b + 1) * per) of
+// the list (slice, chunk) in order.  16 warps: warp w owns TMEM lanes (rows)
+// 32 (w % 4) + lane and column quarter w / 4 of every row-wise step.
+//
+// A tcgen05.mma instruction costs about the same time for any N up to 256,
+// so U = Gq Vt and P = Gq Gk^T, which share the A operand Gq, are one MMA
+// chain with N = C + d_v: its B operand is the tile [Gk ; Vt^T] of C + d_v
+// rows, K-major with the 128-byte swizzle, each 128-byte atom column holding
+// the C rows of Gk followed by the d_v rows of Vt^T, and its accumulator is
+// [P | U] in consecutive TMEM columns.  Shared memory holds two such tiles:
+//   B <- Gk (TMA) and Vt^T (TMA for fp32 operands; bf16: converted by threads)
+//        (raw fp32 = the tf32 part: the tensor core reads only the tf32 bits);
+//   L <- Gq in its Gk rows (TMA; moved to TMEM as the A operand), then the exact
+//        remainders of B (fp32 operands only).
+// After P: the Vt^T rows of B and L take V^T (parts and remainders, written by
+// threads from registers loaded while the tensor core works), the B operand
+// of U += P_m V.  The next item's Gamma tiles are fetched into the Gk rows as
+// soon as [P | U] is done, its carried memory as soon as U += P_m V is done,
+// so that the loads overlap the rest of the item.
+constexpr int kOutThreads = 512;
+
 template <bool BF16, int DV>
 struct OutSmem {
-    static constexpr uint32_t GK = tile_bytes<BF16>(kC);   // Gamma_K chunk, 128 x 128
-    static constexpr uint32_t Y = tile_bytes<BF16>(DV);    // Vt^T, then V^T: DV x 128
-    static constexpr size_t bytes = 1024 + 2 * (size_t)GK + 2 * (size_t)Y + kK * 4 + 4 * kK * 4 + 64;
+    static constexpr uint32_t ATOMS = kK * Elem<BF16>::E / 128;        // 128-byte atom columns
+    static constexpr uint32_t PART = kC * 128;                         // Gk rows of an atom column
+    static constexpr uint32_t ATOM = (kC + DV) * 128;                  // bytes of an atom column
+    static constexpr uint32_t TILE = ATOMS * ATOM;                     // [Gk ; Vt^T]
+    static constexpr size_t bytes = 1024 + 2 * (size_t)TILE + kK * 4 + 8 * kK * 4 + 64;
 };
 
+// Byte offset of element (r, k) in a tile whose atom columns are `stride` apart.
+__device__ __forceinline__ uint32_t fused_off(uint32_t r, uint32_t k, uint32_t E, uint32_t stride)
+{
+    const uint32_t kb = k * E, inner = kb & 127u;
+    return (kb >> 7) * stride + (r >> 3) * 1024u + (r & 7u) * 128u + (((inner >> 4) ^ (r & 7u)) << 4) + (inner & 15u);
+}
+
 struct OutMaps {
-    CUtensorMap gq, gk, v, s;   // s: carried memory blocks (fp32 operands only)
+    CUtensorMap gq, gk, s;   // s: carried memory blocks (fp32 operands only)
 };
+
+// 32 consecutive A-operand values of this thread's TMEM lane from operand
+// column j0 (a multiple of 32): fp32 -> tf32 part at a_hi, remainder at a_lo;
+// bf16 -> packed pairs at a_hi.
+template <bool BF16>
+__device__ __forceinline__ void put_a32(uint32_t tbase, uint32_t lane0, uint32_t a_hi, uint32_t a_lo, int j0,
+                                        const float (&x)[32])
+{
+    if constexpr (BF16) {
+        uint32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) p[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+        tmem_st16(tmem_at(tbase, lane0, a_hi + j0 / 2), p);
+    } else {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float v = x[16 * b + j];
+                const float hv = tf32_hi(v);
+                hi[j] = __float_as_uint(hv);
+                lo[j] = __float_as_uint(v - hv);
+            }
+            tmem_st16(tmem_at(tbase, lane0, a_hi + j0 + 16 * b), hi);
+            tmem_st16(tmem_at(tbase, lane0, a_lo + j0 + 16 * b), lo);
+        }
+    }
+}
 
 // CAUSAL = false gives the bidirectional read: U = Gamma_Q [Vt | Z] with the
 // total memory of the sequence (the same block for every chunk), no P.
 template <bool BF16, int DV, bool CAUSAL>
-__global__ void __launch_bounds__(kTCThreads, 1)
-    k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, float eps, bool v_bf16,
-                   const float *__restrict__ states, int nblk, float *__restrict__ out)
+__global__ void __launch_bounds__(kOutThreads, 1)
+    k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
+                   const void *__restrict__ v, bool v_bf16, const float *__restrict__ states, float *__restrict__ out)
 {
     using El = Elem<BF16>;
     using Sm = OutSmem<BF16, DV>;
-    constexpr int EV_MAX = 4;
+    constexpr int VPER = (kC * DV / 4) / kOutThreads;       // float4 of V per thread
+    constexpr uint32_t AS = Sm::ATOM, PART = Sm::PART;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *x_hi = sm, *x_lo = sm + Sm::GK;                  // Gamma_K / Gamma_Q, later V
-    unsigned char *y_hi = sm + 2 * Sm::GK, *y_lo = y_hi + Sm::Y;    // Vt^T, later V^T
-    float *z_s = reinterpret_cast<float *>(y_lo + Sm::Y);           // [128] Z of the carried memory
-    float *part = z_s + kK;                                         // [4][128]: qz halves, row-sum halves
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [5]: loads, U, P, V, final
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    unsigned char *tb = sm, *tl = sm + Sm::TILE;                     // B tile, L tile
+    float *z_s = reinterpret_cast<float *>(tl + Sm::TILE);          // [128] Z of the carried memory
+    float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [4]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = warp >> 2;
+    const int g = warp >> 2;                    // column quarter
     const uint32_t lane0 = 32 * (warp & 3);
     const int i = lane0 + lane;                 // row of the chunk owned in TMEM
-    const long long bh = blockIdx.y;
-    const int c0 = blockIdx.x * kC;
-    const int nr = min(kC, N - c0);
-    const int row0 = (int)(bh * N + c0);
-    constexpr uint32_t A_HI = 0, A_LO = 128, D_P = 256, D_U = 384;
+    const long long per = (items + gridDim.x - 1) / gridDim.x;
+    const long long it0 = (long long)blockIdx.x * per;
+    const long long it1 = it0 + per < items ? it0 + per : items;
+    constexpr uint32_t A_HI = 0, A_LO = 128, D_P = 256, D_U = D_P + kC;
     constexpr int GBOX = 128 / El::E;                       // Gamma columns per TMA box
-    const int ev = v_bf16 ? 2 : 4;
-    const int vbox = 128 / ev;                              // V columns per TMA box
-    (void)EV_MAX;
+    const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
+                   BAR_V = smem_addr(bar + 3);
+    const long long SZ = (long long)kK * DV + kK;
+
+    // block of the carried memory read by item it
+    auto mem_block = [&](long long it) -> long long { return CAUSAL ? it : it / nblk; };
+    auto load_gamma = [&](long long it) {   // one thread
+        const int row0 = (int)((it / nblk) * N + (it % nblk) * kC);
+        mbar_expect_tx(BAR_G, (CAUSAL ? 2u : 1u) * (uint32_t)(kC * kK * El::E));
+        for (int a = 0; a < (int)Sm::ATOMS; ++a) {
+            if (CAUSAL) tma_load_2d(smem_addr(tb + a * AS), &maps.gk, a * GBOX, row0, BAR_G);
+            tma_load_2d(smem_addr(tl + a * AS), &maps.gq, a * GBOX, row0, BAR_G);
+        }
+    };
+    auto load_memory = [&](long long it) {   // one thread, fp32 operands
+        const int srow = (int)(mem_block(it) * (DV + 1));
+        mbar_expect_tx(BAR_S, (uint32_t)(DV * kK * 4));
+        for (int a = 0; a < kK / 32; ++a)
+            tma_load_2d(smem_addr(tb + a * AS + PART), &maps.s, a * 32, srow, BAR_S);
+    };
 
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
+    // loads in flight that the loop has not waited for (thread 0's record)
+    bool pend_g = false, pend_s = false;
+    uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        uint32_t bytes = (CAUSAL ? 2 : 1) * Sm::GK + (BF16 ? 0u : (uint32_t)Sm::Y);
-        mbar_expect_tx(smem_addr(bar), bytes);
-        for (int a = 0; a < kK / GBOX; ++a) {
-            if (CAUSAL) tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.gk, a * GBOX, row0, smem_addr(bar));
-            tma_load_2d(smem_addr(x_lo + a * (kC * 128)), &maps.gq, a * GBOX, row0, smem_addr(bar));
-        }
-        if constexpr (!BF16) {
-            const int srow = (int)((CAUSAL ? bh * nblk + blockIdx.x : bh) * (DV + 1));
-            for (int a = 0; a < kK / 32; ++a)
-                tma_load_2d(smem_addr(y_hi + a * (DV * 128)), &maps.s, a * 32, srow, smem_addr(bar));
+        if (it0 < it1) {
+            load_gamma(it0);
+            pend_g = true;
+            if (!BF16) {
+                load_memory(it0);
+                pend_s = true;
+            }
         }
     }
-    const long long SZ = (long long)kK * DV + kK;
-    const float *st = states + (CAUSAL ? bh * nblk + blockIdx.x : bh) * SZ;
-    if (tid < kK) {
-        const float zk = st[(long long)kK * DV + tid];
-        z_s[tid] = BF16 ? bf16r(zk) : zk;
-    }
-    if constexpr (BF16) {
-        // carried memory (block rows c of K) -> Y as bf16 Vt^T; lanes run over components
-        constexpr int PER = (DV * kK / 4) / kTCThreads;
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int f = tid + u * kTCThreads, c = f / (kK / 4), k4 = 4 * (f % (kK / 4));
-            const float4 t = reinterpret_cast<const float4 *>(st + (long long)c * kK)[k4 / 4];
-            const uint2 p = make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
-            *reinterpret_cast<uint2 *>(y_hi + sw128_offset(c, k4, DV, 2)) = p;
-        }
-    }
+    // Z of the carried memory, loaded one item ahead
+    float zreg = (tid < kK && it0 < it1) ? states[mem_block(it0) * SZ + (long long)kK * DV + tid] : 0.f;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    bool ok = mbar_wait(smem_addr(bar), 0);
-
-    // A = Gamma_Q (row i, operand columns [64h, 64h + 64)) from its landing tile; partial Gamma_Q,i . Z
-    {
-        float xq[64];
-#pragma unroll
-        for (int q = 0; q < 64 / 4; ++q) {
-            const int k = 64 * h + 4 * q;
-            if constexpr (BF16) {
-                const uint2 t = *reinterpret_cast<const uint2 *>(x_lo + sw128_offset(i, k, kC, 2));
-                xq[4 * q] = __uint_as_float(t.x << 16);
-                xq[4 * q + 1] = __uint_as_float(t.x & 0xffff0000u);
-                xq[4 * q + 2] = __uint_as_float(t.y << 16);
-                xq[4 * q + 3] = __uint_as_float(t.y & 0xffff0000u);
-            } else {
-                const float4 t = *reinterpret_cast<const float4 *>(x_lo + sw128_offset(i, k, kC, 4));
-                xq[4 * q] = t.x; xq[4 * q + 1] = t.y; xq[4 * q + 2] = t.z; xq[4 * q + 3] = t.w;
-            }
-        }
-        float qz = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) qz = fmaf(xq[j], z_s[64 * h + j], qz);
-        part[h * kK + i] = qz;
-        put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, xq);
-    }
-    if constexpr (!BF16) {
-        __syncthreads();   // Gamma_Q has been read from X_lo
-        // exact remainders of Gamma_K (X_lo) and of the carried memory (Y_lo), in place
-        constexpr int PX = Sm::GK / 16 / kTCThreads, PY = Sm::Y / 16 / kTCThreads;
-#pragma unroll 4
-        for (int u = 0; u < (CAUSAL ? PX : 0); ++u) {
-            const uint32_t off = 16 * (tid + u * kTCThreads);
-            const float4 t = *reinterpret_cast<const float4 *>(x_hi + off);
-            *reinterpret_cast<float4 *>(x_lo + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
-                                                                  t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
-        }
-#pragma unroll 4
-        for (int u = 0; u < PY; ++u) {
-            const uint32_t off = 16 * (tid + u * kTCThreads);
-            const float4 t = *reinterpret_cast<const float4 *>(y_hi + off);
-            *reinterpret_cast<float4 *>(y_lo + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
-                                                                  t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
-        }
-    }
-    tmem_wait_st();
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-        mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, false);    // U = Gq Vt
-        mma_commit(smem_addr(bar + 1));
-        if (CAUSAL) {
-            mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, x_hi, x_lo, kC, false);    // P = Gq Gk^T
-            mma_commit(smem_addr(bar + 2));
-        }
-    }
-    __syncwarp();
-    if constexpr (!CAUSAL) {
-        ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
-        fence_after_sync();
-    } else {
-    ok = mbar_wait(smem_addr(bar + 2), 0) && ok;   // P done (and U, committed earlier)
-    fence_after_sync();
-    if (tid == 0) {
-        // X is free: bring V in while P_m is formed
-        fence_proxy_async();
-        mbar_expect_tx(smem_addr(bar + 3), (uint32_t)(kC * DV * ev));
-        for (int a = 0; a < DV / vbox; ++a)
-            tma_load_2d(smem_addr(x_hi + a * (kC * 128)), &maps.v, a * vbox, row0, smem_addr(bar + 3));
-    }
-    // P_m = P with j > i zeroed replaces Gamma_Q as the A operand; row sums on CUDA cores
-    {
-        float x[64];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            uint32_t r[16];
-            tmem_ld16(tmem_at(tbase, lane0, D_P + 64 * h + 16 * b), r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int jj = 64 * h + 16 * b + j;
-                x[16 * b + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
-            }
-        }
-        float ps = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) ps += BF16 ? bf16r(x[j]) : x[j];
-        part[(2 + h) * kK + i] = ps;
-        put_a64<BF16>(tbase, lane0, A_HI, A_LO, 64 * h, x);
-    }
-    ok = mbar_wait(smem_addr(bar + 3), 0) && ok;
-    // V^T (element (c, j)) into Y from the V tile in X; lanes run over tokens
-    {
-        constexpr int PER = (kC * DV / 4) / kTCThreads;
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int f = tid + u * kTCThreads, j = f % kC, c4 = 4 * (f / kC);
-            float4 t;
-            if (j >= nr) {
-                t = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (v_bf16) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(x_hi + sw128_offset(j, c4, kC, 2));
-                t = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-            } else {
-                t = *reinterpret_cast<const float4 *>(x_hi + sw128_offset(j, c4, kC, 4));
-            }
-            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 0, j, DV, El::E), t.x);
-            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 1, j, DV, El::E), t.y);
-            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 2, j, DV, El::E), t.z);
-            put<BF16>(y_hi, y_lo, sw128_offset(c4 + 3, j, DV, El::E), t.w);
-        }
-    }
-    tmem_wait_st();
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-        mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, y_hi, y_lo, DV, true);     // U += P_m V
-        mma_commit(smem_addr(bar + 4));
-    }
-    __syncwarp();
-    ok = mbar_wait(smem_addr(bar + 4), 0) && ok;
-    fence_after_sync();
-    }
-
-    const float den = part[i] + part[kK + i] + (CAUSAL ? part[2 * kK + i] + part[3 * kK + i] : 0.f) + eps;
+    bool ok = true;
     const float qnan = __int_as_float(0x7fc00000);
+
+    for (long long it = it0; it < it1 && ok; ++it) {
+        const uint32_t ph = (uint32_t)((it - it0) & 1);
+        const long long bh = it / nblk;
+        const int c0 = (int)(it % nblk) * kC;
+        const int nr = min(kC, N - c0);
+        const long long rowbase = bh * N + c0;
+        const bool more = it + 1 < it1;
+        if (tid < kK) z_s[tid] = BF16 ? bf16r(zreg) : zreg;
+        if constexpr (BF16) {
+            // carried memory (block rows c of K) -> Vt^T rows of B as bf16; lanes run over components
+            const float *st = states + mem_block(it) * SZ;
+            constexpr int PER = (DV * kK / 4) / kOutThreads;
 #pragma unroll
-    for (int cb = 0; cb < DV / 32; ++cb) {
-        const int c = h * (DV / 2) + 16 * cb;
-        uint32_t r[16];
-        tmem_ld16(tmem_at(tbase, lane0, D_U + c), r);
-        tmem_wait_ld();
-        if (i < nr) {
-            float4 *dst = reinterpret_cast<float4 *>(out + (bh * N + c0 + i) * (long long)DV + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]) / den, __uint_as_float(r[4 * q + 1]) / den,
-                                          __uint_as_float(r[4 * q + 2]) / den, __uint_as_float(r[4 * q + 3]) / den)
-                            : make_float4(qnan, qnan, qnan, qnan);
+            for (int u = 0; u < PER; ++u) {
+                const int f = tid + u * kOutThreads, c = f / (kK / 4), k4 = 4 * (f % (kK / 4));
+                const float4 t = reinterpret_cast<const float4 *>(st + (long long)c * kK)[k4 / 4];
+                const uint2 p = make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
+                *reinterpret_cast<uint2 *>(tb + fused_off(kC + c, k4, 2, AS)) = p;
+            }
         }
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        const bool ok_g = mbar_wait(BAR_G, ph), ok_s = BF16 || mbar_wait(BAR_S, ph);
+        ok = ok && ok_g && ok_s;
+        if (tid == 0) {   // a load whose wait gave up is still in flight
+            pend_g = pend_g && !ok_g;
+            pend_s = pend_s && !ok_s;
+        }
+
+        // A = Gamma_Q (row i, operand columns [32g, 32g + 32)) from its landing rows; partial Gamma_Q,i . Z
+        {
+            float xq[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int k = 32 * g + 4 * q;
+                if constexpr (BF16) {
+                    const uint2 t = *reinterpret_cast<const uint2 *>(tl + fused_off(i, k, 2, AS));
+                    xq[4 * q] = __uint_as_float(t.x << 16);
+                    xq[4 * q + 1] = __uint_as_float(t.x & 0xffff0000u);
+                    xq[4 * q + 2] = __uint_as_float(t.y << 16);
+                    xq[4 * q + 3] = __uint_as_float(t.y & 0xffff0000u);
+                } else {
+                    const float4 t = *reinterpret_cast<const float4 *>(tl + fused_off(i, k, 4, AS));
+                    xq[4 * q] = t.x; xq[4 * q + 1] = t.y; xq[4 * q + 2] = t.z; xq[4 * q + 3] = t.w;
+                }
+            }
+            float qz = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) qz = fmaf(xq[j], z_s[32 * g + j], qz);
+            part[g * kK + i] = qz;
+            put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, xq);
+        }
+        if constexpr (!BF16) {
+            __syncthreads();   // Gamma_Q has been read from L
+            // exact remainders of B into L, in place (bidirectional read: the Vt^T rows only)
+            if constexpr (CAUSAL) {
+                constexpr int PX = Sm::TILE / 16 / kOutThreads;
+#pragma unroll 4
+                for (int u = 0; u < PX; ++u) {
+                    const uint32_t off = 16 * (tid + u * kOutThreads);
+                    const float4 t = *reinterpret_cast<const float4 *>(tb + off);
+                    *reinterpret_cast<float4 *>(tl + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
+                                                                        t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
+                }
+            } else {
+                constexpr int PV16 = DV * 128 / 16;                       // 16-byte words per atom's Vt^T rows
+                constexpr int PY = Sm::ATOMS * PV16 / kOutThreads;
+#pragma unroll
+                for (int u = 0; u < PY; ++u) {
+                    const int w = tid + u * kOutThreads;
+                    const uint32_t off = (w / PV16) * AS + PART + 16 * (w % PV16);
+                    const float4 t = *reinterpret_cast<const float4 *>(tb + off);
+                    *reinterpret_cast<float4 *>(tl + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
+                                                                        t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
+                }
+            }
+        }
+        tmem_wait_st();
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+            if (CAUSAL)   // [P | U] = Gq [Gk ; Vt^T]^T
+                mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, tb, tl, kC + DV, AS, false);
+            else          // U = Gq Vt
+                mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, tb + PART, tl + PART, DV, AS, false);
+            mma_commit(BAR_M);
+        }
+        __syncwarp();
+        // V of this chunk (lanes over tokens), loaded while the tensor core works, consumed after P
+        float4 vr[CAUSAL ? VPER : 1];
+        if constexpr (CAUSAL) {
+#pragma unroll
+            for (int u = 0; u < VPER; ++u) {
+                const int f = tid + u * kOutThreads, j = f % kC, c4 = f / kC;
+                vr[u] = j < nr ? load4(v, (rowbase + j) * DV + 4 * c4, v_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        ok = mbar_wait(BAR_M, ph) && ok;
+        fence_after_sync();
+        if constexpr (!CAUSAL) {
+            if (tid == 0 && more && ok) {   // B and L are free: the next item's tiles
+                fence_proxy_async();
+                load_gamma(it + 1);
+                pend_g = true;
+                ph_g = ph ^ 1u;
+                if (!BF16) {
+                    load_memory(it + 1);
+                    pend_s = true;
+                    ph_s = ph ^ 1u;
+                }
+            }
+        } else {
+            if (tid == 0 && more && ok) {   // the Gamma rows are free: the next item's Gamma tiles
+                fence_proxy_async();
+                load_gamma(it + 1);
+                pend_g = true;
+                ph_g = ph ^ 1u;
+            }
+            // P_m = P with j > i zeroed replaces Gamma_Q as the A operand; row sums on CUDA cores
+            {
+                float x[32];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem_at(tbase, lane0, D_P + 32 * g + 16 * b), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int jj = 32 * g + 16 * b + j;
+                        x[16 * b + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
+                    }
+                }
+                float ps = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ps += BF16 ? bf16r(x[j]) : x[j];
+                part[(4 + g) * kK + i] = ps;
+                put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, x);
+            }
+            // V^T (element (c, j)) into the Vt^T rows of B and L from registers; lanes run over tokens
+#pragma unroll
+            for (int u = 0; u < VPER; ++u) {
+                const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
+                put<BF16>(tb, tl, fused_off(kC + c4 + 0, j, El::E, AS), vr[u].x);
+                put<BF16>(tb, tl, fused_off(kC + c4 + 1, j, El::E, AS), vr[u].y);
+                put<BF16>(tb, tl, fused_off(kC + c4 + 2, j, El::E, AS), vr[u].z);
+                put<BF16>(tb, tl, fused_off(kC + c4 + 3, j, El::E, AS), vr[u].w);
+            }
+            tmem_wait_st();
+            fence_proxy_async();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+            if (tid == 0) {   // U += P_m V
+                mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, tb + PART, tl + PART, DV, AS, true);
+                mma_commit(BAR_V);
+            }
+            __syncwarp();
+            ok = mbar_wait(BAR_V, ph) && ok;
+            fence_after_sync();
+            if (!BF16 && tid == 0 && more && ok) {   // the Vt^T rows are free: the next item's carried memory
+                fence_proxy_async();
+                load_memory(it + 1);
+                pend_s = true;
+                ph_s = ph ^ 1u;
+            }
+        }
+
+        if (tid < kK && more) zreg = states[mem_block(it + 1) * SZ + (long long)kK * DV + tid];
+        float den = eps;
+#pragma unroll
+        for (int q = 0; q < (CAUSAL ? 8 : 4); ++q) den += part[q * kK + i];
+        const float inv = 1.0f / den;
+#pragma unroll
+        for (int cb = 0; cb < DV / 64; ++cb) {
+            const int c = g * (DV / 4) + 16 * cb;
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, lane0, D_U + c), r);
+            tmem_wait_ld();
+            if (i < nr) {
+                float4 *dst = reinterpret_cast<float4 *>(out + (rowbase + i) * (long long)DV + c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                              __uint_as_float(r[4 * q + 2]) * inv,
+                                              __uint_as_float(r[4 * q + 3]) * inv)
+                                : make_float4(qnan, qnan, qnan, qnan);
+            }
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
+        fence_after_sync();
+    }
+    // after a failed wait: let the copies still in flight land before the shared memory is released
+    if (tid == 0) {
+        if (pend_g) (void)mbar_wait(BAR_G, ph_g);
+        if (pend_s) (void)mbar_wait(BAR_S, ph_s);
     }
     fence_before_sync();
     __syncthreads();
@@ -562,17 +679,17 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     if (attr != cudaSuccess) return attr;
     OutMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
-    bool ok = make_tma_2d(&maps.gq, gq, BF16, rows, kK, kC) && make_tma_2d(&maps.gk, gk, BF16, rows, kK, kC) &&
-              make_tma_2d(&maps.v, v, dm.v_bf16, rows, DV, kC);
+    bool ok = make_tma_2d(&maps.gq, gq, BF16, rows, kK, kC) && make_tma_2d(&maps.gk, gk, BF16, rows, kK, kC);
     if (!BF16)
         ok = ok && make_tma_2d(&maps.s, states, false,
                                (unsigned long long)dm.BH() * (CAUSAL ? dm.nblk() : 1) * (DV + 1), kK, DV);
     else
         maps.s = maps.gq;
     if (!ok) return cudaErrorInvalidValue;
-    dim3 grid(dm.nblk(), (unsigned)dm.BH());
-    k_chunk_out_tc<BF16, DV, CAUSAL><<<grid, kTCThreads, smem, st>>>(maps, dm.N, dm.eps, dm.v_bf16, states,
-                                                                      dm.nblk(), out);
+    const long long items = dm.BH() * (long long)dm.nblk();
+    const int grid = (int)(items < sm_count() ? items : sm_count());
+    k_chunk_out_tc<BF16, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, dm.eps, v,
+                                                                       dm.v_bf16, states, out);
     return cudaGetLastError();
 }
 

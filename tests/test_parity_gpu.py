@@ -32,6 +32,8 @@ def _report(name, err, tol):
     (W["tiny"].with_(K=200, d=128, N=300, H=2), None),
     (W["causal_4k"], 4),
     (W["bidir_16k_peaked"], 3),
+    # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
+    (W["tiny"].with_(mode="bidir", B=4, H=16, N=1100, d=64, dv=64, K=128), None),
     (W["causal_8k_K512"], 2),
     (W["causal_64k_bf16"], 2),
 ])
@@ -82,6 +84,8 @@ def test_responsibilities_adversarial_rows():
     (W["tiny"].with_(mode="bidir", B=2, H=2, N=1000, d=64, dv=64, K=128), None),
     (W["tiny"].with_(mode="bidir", B=1, H=2, N=300, d=32, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None),
     (W["bidir_16k_peaked"], 3),
+    # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
+    (W["tiny"].with_(mode="bidir", B=4, H=16, N=1100, d=64, dv=64, K=128), None),
     (W["causal_4k"].with_(mode="bidir", gemm_dtype="bf16"), 2),
 ])
 def test_bidir(wl, sample):
@@ -109,6 +113,9 @@ CAUSAL = [
     (W["tiny"].with_(B=1, H=2, N=129, d=16, dv=64, K=128), None, 0),
     (W["tiny"].with_(B=1, H=1, N=1, d=64, dv=64, K=128), None, 0),
     (W["tiny"].with_(B=1, H=2, N=700, d=32, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
+    # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
+    (W["tiny"].with_(B=4, H=16, N=1100, d=64, dv=64, K=128), None, 0),
+    (W["tiny"].with_(B=2, H=16, N=1100, d=64, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     (W["causal_16k_peaked"], 3, 0),
     (W["causal_64k_bf16"], 2, 0),
     (W["causal_8k_K32"], 2, 0),
