@@ -27,6 +27,7 @@
 #include "gma_tc.cuh"
 
 #include <cuda.h>
+#include <climits>
 #include <type_traits>
 
 namespace gma {
@@ -339,14 +340,15 @@ __device__ __forceinline__ uint32_t fused_off(uint32_t r, uint32_t k, uint32_t E
 
 struct OutMaps {
     CUtensorMap gq, gk, s;   // s: carried memory blocks (fp32 operands only)
+    CUtensorMap o;           // output [slices][N][d_v], boxes of 64 rows x 32 columns (fp32 operands only)
 };
 
 // 32 consecutive A-operand values of this thread's TMEM lane from operand
-// column j0 (a multiple of 32): fp32 -> tf32 part at a_hi, remainder at a_lo;
-// bf16 -> packed pairs at a_hi.
+// column j0 (a multiple of 32): fp32 -> tf32 part at a_hi, remainder at a_lo
+// (part = 0: parts only, 1: remainders only, 2: both); bf16 -> packed pairs at a_hi.
 template <bool BF16>
 __device__ __forceinline__ void put_a32(uint32_t tbase, uint32_t lane0, uint32_t a_hi, uint32_t a_lo, int j0,
-                                        const float (&x)[32])
+                                        const float (&x)[32], int part = 2)
 {
     if constexpr (BF16) {
         uint32_t p[16];
@@ -364,8 +366,8 @@ __device__ __forceinline__ void put_a32(uint32_t tbase, uint32_t lane0, uint32_t
                 hi[j] = __float_as_uint(hv);
                 lo[j] = __float_as_uint(v - hv);
             }
-            tmem_st16(tmem_at(tbase, lane0, a_hi + j0 + 16 * b), hi);
-            tmem_st16(tmem_at(tbase, lane0, a_lo + j0 + 16 * b), lo);
+            if (part != 1) tmem_st16(tmem_at(tbase, lane0, a_hi + j0 + 16 * b), hi);
+            if (part != 0) tmem_st16(tmem_at(tbase, lane0, a_lo + j0 + 16 * b), lo);
         }
     }
 }
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 {
     using El = Elem<BF16>;
     using Sm = OutSmem<BF16, DV>;
+    static_assert(BF16 || DV == 64, "fp32 operands: d_v = 64 only (the output staging assumes it)");
     constexpr int VPER = (kC * DV / 4) / kOutThreads;       // float4 of V per thread
     constexpr uint32_t AS = Sm::ATOM, PART = Sm::PART;
     extern __shared__ unsigned char sm_raw[];
@@ -500,42 +503,51 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             part[g * kK + i] = qz;
             put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, xq);
         }
+        tmem_wait_st();
+        fence_proxy_async();
+        fence_before_sync();
+        if (!BF16 && tid == 0) bulk_wait_read();   // the previous output tile has left L
+        __syncthreads();   // Gamma_Q has been read from L and is in TMEM
+        fence_after_sync();
+        // the passes that do not read the remainders of B start at once:
+        // [P | U] = Gq [Gk ; Vt^T]^T (bidirectional read: U = Gq Vt)
+        const unsigned char *b0 = CAUSAL ? tb : tb + PART, *l0 = CAUSAL ? tl : tl + PART;
+        const uint32_t d0 = CAUSAL ? D_P : D_U, nb = CAUSAL ? kC + DV : DV;
+        if (tid == 0) {
+            mma_pass_at<BF16>(tbase + d0, tbase + A_HI, b0, nb, AS, false);
+            if constexpr (!BF16) mma_pass_at<BF16>(tbase + d0, tbase + A_LO, b0, nb, AS, true);
+            else mma_commit(BAR_M);
+        }
         if constexpr (!BF16) {
-            __syncthreads();   // Gamma_Q has been read from L
-            // exact remainders of B into L, in place (bidirectional read: the Vt^T rows only)
+            // exact remainders of B into L, in place (bidirectional read: the Vt^T rows only),
+            // by warps 1..15 while warp 0 issues the passes above
+            const int w0 = tid >= 32 ? tid - 32 : INT_MAX;   // warp 0 takes no words
             if constexpr (CAUSAL) {
-                constexpr int PX = Sm::TILE / 16 / kOutThreads;
-#pragma unroll 4
-                for (int u = 0; u < PX; ++u) {
-                    const uint32_t off = 16 * (tid + u * kOutThreads);
+#pragma unroll 1
+                for (int w = w0; w < (int)(Sm::TILE / 16); w += kOutThreads - 32) {
+                    const uint32_t off = 16 * w;
                     const float4 t = *reinterpret_cast<const float4 *>(tb + off);
                     *reinterpret_cast<float4 *>(tl + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
                                                                         t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
                 }
             } else {
                 constexpr int PV16 = DV * 128 / 16;                       // 16-byte words per atom's Vt^T rows
-                constexpr int PY = Sm::ATOMS * PV16 / kOutThreads;
-#pragma unroll
-                for (int u = 0; u < PY; ++u) {
-                    const int w = tid + u * kOutThreads;
+#pragma unroll 4
+                for (int w = w0; w < (int)Sm::ATOMS * PV16; w += kOutThreads - 32) {
                     const uint32_t off = (w / PV16) * AS + PART + 16 * (w % PV16);
                     const float4 t = *reinterpret_cast<const float4 *>(tb + off);
                     *reinterpret_cast<float4 *>(tl + off) = make_float4(t.x - tf32_hi(t.x), t.y - tf32_hi(t.y),
                                                                         t.z - tf32_hi(t.z), t.w - tf32_hi(t.w));
                 }
             }
-        }
-        tmem_wait_st();
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-        if (tid == 0) {
-            if (CAUSAL)   // [P | U] = Gq [Gk ; Vt^T]^T
-                mma_all<BF16>(tbase + D_P, tbase + A_HI, tbase + A_LO, tb, tl, kC + DV, AS, false);
-            else          // U = Gq Vt
-                mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, tb + PART, tl + PART, DV, AS, false);
-            mma_commit(BAR_M);
+            fence_proxy_async();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+            if (tid == 0) {   // the pass that reads the remainders
+                mma_pass_at<BF16>(tbase + d0, tbase + A_HI, l0, nb, AS, true);
+                mma_commit(BAR_M);
+            }
         }
         __syncwarp();
         // V of this chunk (lanes over tokens), loaded while the tensor core works, consumed after P
@@ -569,8 +581,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 ph_g = ph ^ 1u;
             }
             // P_m = P with j > i zeroed replaces Gamma_Q as the A operand; row sums on CUDA cores
-            {
-                float x[32];
+            auto load_pm = [&](float (&x)[32]) {
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     uint32_t r[16];
@@ -582,29 +593,61 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         x[16 * b + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
                     }
                 }
+            };
+            {
+                float x[32];
+                load_pm(x);
                 float ps = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ps += BF16 ? bf16r(x[j]) : x[j];
                 part[(4 + g) * kK + i] = ps;
-                put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, x);
-            }
-            // V^T (element (c, j)) into the Vt^T rows of B and L from registers; lanes run over tokens
+                // U += P_m V: the tf32 parts first (pass hi * hi), then the remainders (hi * lo, lo * hi)
+                put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, x, BF16 ? 2 : 0);
+                // V^T (element (c, j)) into the Vt^T rows of B from registers; lanes run over tokens
 #pragma unroll
-            for (int u = 0; u < VPER; ++u) {
-                const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
-                put<BF16>(tb, tl, fused_off(kC + c4 + 0, j, El::E, AS), vr[u].x);
-                put<BF16>(tb, tl, fused_off(kC + c4 + 1, j, El::E, AS), vr[u].y);
-                put<BF16>(tb, tl, fused_off(kC + c4 + 2, j, El::E, AS), vr[u].z);
-                put<BF16>(tb, tl, fused_off(kC + c4 + 3, j, El::E, AS), vr[u].w);
-            }
-            tmem_wait_st();
-            fence_proxy_async();
-            fence_before_sync();
-            __syncthreads();
-            fence_after_sync();
-            if (tid == 0) {   // U += P_m V
-                mma_all<BF16>(tbase + D_U, tbase + A_HI, tbase + A_LO, tb + PART, tl + PART, DV, AS, true);
-                mma_commit(BAR_V);
+                for (int u = 0; u < VPER; ++u) {
+                    const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
+                    const float e4[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t off = fused_off(kC + c4 + e, j, El::E, AS);
+                        if constexpr (BF16)
+                            *reinterpret_cast<__nv_bfloat16 *>(tb + off) = __float2bfloat16_rn(e4[e]);
+                        else
+                            *reinterpret_cast<float *>(tb + off) = tf32_hi(e4[e]);
+                    }
+                }
+                tmem_wait_st();
+                fence_proxy_async();
+                fence_before_sync();
+                __syncthreads();
+                fence_after_sync();
+                if (tid == 0) {
+                    mma_pass_at<BF16>(tbase + D_U, tbase + A_HI, tb + PART, DV, AS, true);
+                    if constexpr (BF16) mma_commit(BAR_V);
+                }
+                if constexpr (!BF16) {
+                    load_pm(x);   // P is still in TMEM: reloading beats keeping 32 values live
+                    put_a32<BF16>(tbase, lane0, A_HI, A_LO, 32 * g, x, 1);
+#pragma unroll
+                    for (int u = 0; u < VPER; ++u) {
+                        const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
+                        const float e4[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<float *>(tl + fused_off(kC + c4 + e, j, 4, AS)) = e4[e] - tf32_hi(e4[e]);
+                    }
+                    tmem_wait_st();
+                    fence_proxy_async();
+                    fence_before_sync();
+                    __syncthreads();
+                    fence_after_sync();
+                    if (tid == 0) {
+                        mma_pass_at<BF16>(tbase + D_U, tbase + A_HI, tl + PART, DV, AS, true);
+                        mma_pass_at<BF16>(tbase + D_U, tbase + A_LO, tb + PART, DV, AS, true);
+                        mma_commit(BAR_V);
+                    }
+                }
             }
             __syncwarp();
             ok = mbar_wait(BAR_V, ph) && ok;
@@ -628,20 +671,40 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             uint32_t r[16];
             tmem_ld16(tmem_at(tbase, lane0, D_U + c), r);
             tmem_wait_ld();
-            if (i < nr) {
-                float4 *dst = reinterpret_cast<float4 *>(out + (rowbase + i) * (long long)DV + c);
+            float4 o4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o4[q] = ok ? make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                         __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv)
+                           : make_float4(qnan, qnan, qnan, qnan);
+            if constexpr (!BF16) {
+                // fp32 operands (d_v = 64): the output tile goes through the Vt^T rows of L
+                // (free until the next item's remainders) and leaves by TMA stores, in
+                // four boxes of 64 rows x 32 columns (box a: rows 64 (a / 2), columns 32 (a % 2))
+                unsigned char *ob = tl + ((i >> 6) * 2 + (g >> 1)) * AS + PART + (i & 63) * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    dst[q] = ok ? make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                                              __uint_as_float(r[4 * q + 2]) * inv,
-                                              __uint_as_float(r[4 * q + 3]) * inv)
-                                : make_float4(qnan, qnan, qnan, qnan);
+                    *reinterpret_cast<float4 *>(ob + (((4 * (g & 1) + q) ^ (i & 7)) << 4)) = o4[q];
+            } else if (i < nr) {
+                float4 *dst = reinterpret_cast<float4 *>(out + (rowbase + i) * (long long)DV + c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = o4[q];
             }
         }
+        if constexpr (!BF16) fence_proxy_async();   // the staged tile is read by the TMA store
         fence_before_sync();
         ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
         fence_after_sync();
+        if constexpr (!BF16) {
+            if (tid == 0) {
+                for (int a = 0; a < 4; ++a)
+                    tma_store_3d(&maps.o, (a & 1) * 32, c0 + (a >> 1) * 64, (int)bh,
+                                 smem_addr(tl + a * AS + PART));
+                bulk_commit();
+            }
+        }
     }
+    if (!BF16 && tid == 0) bulk_wait_all();
     // after a failed wait: let the copies still in flight land before the shared memory is released
     if (tid == 0) {
         if (pend_g) (void)mbar_wait(BAR_G, ph_g);
@@ -682,9 +745,10 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     bool ok = make_tma_2d(&maps.gq, gq, BF16, rows, kK, kC) && make_tma_2d(&maps.gk, gk, BF16, rows, kK, kC);
     if (!BF16)
         ok = ok && make_tma_2d(&maps.s, states, false,
-                               (unsigned long long)dm.BH() * (CAUSAL ? dm.nblk() : 1) * (DV + 1), kK, DV);
+                               (unsigned long long)dm.BH() * (CAUSAL ? dm.nblk() : 1) * (DV + 1), kK, DV) &&
+             make_tma_3d(&maps.o, out, false, DV, dm.N, dm.BH(), 64);
     else
-        maps.s = maps.gq;
+        maps.s = maps.o = maps.gq;
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
