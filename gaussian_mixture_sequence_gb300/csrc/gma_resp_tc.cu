@@ -296,71 +296,86 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
         };
-        // this quarter of the output row starts as zeros
+        // kept counts of the four quarters of the row
+        ex1[q * kPK + i] = (float)__popc(mask);
+        __syncthreads();
+        const int total = (int)(ex1[i] + ex1[kPK + i] + ex1[2 * kPK + i] + ex1[3 * kPK + i]);
+        // this quarter of the output row starts as zeros; a row with a single kept
+        // component has posterior exactly 1 there and needs no exact evaluation
         if (g_bf16) {
 #pragma unroll
             for (int g = 0; g < 4; ++g)
                 *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 32 * q + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+            if (total == 1 && mask)
+                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 32 * q + __ffs(mask) - 1, kPRows, 2)) =
+                    __float2bfloat16_rn(1.0f);
         } else {
 #pragma unroll
             for (int g = 0; g < 8; ++g)
                 *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * q + 4 * g, kPRows, 4)) =
                     make_float4(0.f, 0.f, 0.f, 0.f);
+            if (total == 1 && mask)
+                *reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + __ffs(mask) - 1, kPRows, 4)) = 1.0f;
         }
-        // Runs f(k, l_k) for every kept component k of this lane.  Few kept per lane
-        // (concentrated posteriors): each lane walks its own set, reading the
-        // parameters of its own components.  Many: the warp walks the union of
-        // its lanes' sets with one component at a time, so that the parameter
-        // reads are broadcasts (per-lane reads would cost 32 times the
-        // shared-memory traffic).
-        const uint32_t uni = __reduce_or_sync(0xffffffffu, mask);
-        const bool per_lane = 4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mask)) <= (uint32_t)__popc(uni);
-        auto for_kept = [&](auto &&f) {
-            if (per_lane) {
-                for (uint32_t mm = mask; mm; mm &= mm - 1) {
-                    const int k = 32 * q + __ffs(mm) - 1;
-                    f(k, exact(k));
+        const uint32_t xmask = total > 1 ? mask : 0u;   // the components of rows that need the softmax
+        if (__syncthreads_or(xmask != 0u)) {
+            // Runs f(k, l_k) for every component k of xmask.  Few per lane: each lane
+            // walks its own set, reading the parameters of its own components.  Many:
+            // the warp walks the union of its lanes' sets one component at a time, so
+            // that the parameter reads are broadcasts (per-lane reads would cost 32
+            // times the shared-memory traffic).
+            const uint32_t uni = __reduce_or_sync(0xffffffffu, xmask);
+            const bool per_lane =
+                4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(xmask)) <= (uint32_t)__popc(uni);
+            auto for_kept = [&](auto &&f) {
+                if (per_lane) {
+                    for (uint32_t mm = xmask; mm; mm &= mm - 1) {
+                        const int k = 32 * q + __ffs(mm) - 1;
+                        f(k, exact(k));
+                    }
+                } else {
+                    for (uint32_t mm = uni; mm; mm &= mm - 1) {
+                        const int kq = __ffs(mm) - 1;
+                        const float l = exact(32 * q + kq);
+                        if ((xmask >> kq) & 1u) f(32 * q + kq, l);
+                    }
                 }
-            } else {
-                for (uint32_t mm = uni; mm; mm &= mm - 1) {
-                    const int kq = __ffs(mm) - 1;
-                    const float l = exact(32 * q + kq);
-                    if ((mask >> kq) & 1u) f(32 * q + kq, l);
-                }
-            }
-        };
-        // exact pass: online maximum and sum over the kept components of this quarter;
-        // with an fp32 output tile the log-joints wait in it for the normalisation
-        float mt = -FLT_MAX, st = 0.f;
-        for_kept([&](int k, float l) {
-            if (!g_bf16) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
-            if (l > mt) {
-                st = st * expf(mt - l) + 1.f;
-                mt = l;
-            } else {
-                st += expf(l - mt);
-            }
-        });
-        ex1[q * kPK + i] = mt;
-        ex2[q * kPK + i] = st;
-        __syncthreads();
-        float m = ex1[i];
-#pragma unroll
-        for (int g = 1; g < 4; ++g) m = fmaxf(m, ex1[g * kPK + i]);
-        float ssum = 0.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) ssum += ex2[g * kPK + i] * expf(ex1[g * kPK + i] - m);
-        const float inv = 1.0f / ssum;
-        // the kept posteriors of this quarter into the output tile
-        if (g_bf16) {
+            };
+            // exact pass: online maximum and sum over the kept components of this quarter;
+            // with an fp32 output tile the log-joints wait in it for the normalisation
+            float mt = -FLT_MAX, st = 0.f;
             for_kept([&](int k, float l) {
-                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) =
-                    __float2bfloat16_rn(expf(l - m) * inv);
+                if (!g_bf16) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                if (l > mt) {
+                    st = st * expf(mt - l) + 1.f;
+                    mt = l;
+                } else {
+                    st += expf(l - mt);
+                }
             });
-        } else {
-            for (uint32_t mm = mask; mm; mm &= mm - 1) {
-                float *o = reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + __ffs(mm) - 1, kPRows, 4));
-                *o = expf(*o - m) * inv;
+            ex1[q * kPK + i] = mt;
+            ex2[q * kPK + i] = st;
+            __syncthreads();
+            if (xmask) {
+                float m = ex1[i];
+#pragma unroll
+                for (int g = 1; g < 4; ++g) m = fmaxf(m, ex1[g * kPK + i]);
+                float ssum = 0.f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) ssum += ex2[g * kPK + i] * expf(ex1[g * kPK + i] - m);
+                const float inv = 1.0f / ssum;
+                // the kept posteriors of this quarter into the output tile
+                if (g_bf16) {
+                    for_kept([&](int k, float l) {
+                        *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) =
+                            __float2bfloat16_rn(expf(l - m) * inv);
+                    });
+                } else {
+                    for (uint32_t mm = xmask; mm; mm &= mm - 1) {
+                        float *o = reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + __ffs(mm) - 1, kPRows, 4));
+                        *o = expf(*o - m) * inv;
+                    }
+                }
             }
         }
         fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
