@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         tmem_wait_st();
         fence_before_sync();
+        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
         __syncthreads();   // the routing tile has been read; A is in TMEM
         fence_after_sync();
         if (tid == 0) {
@@ -242,6 +243,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mma_commit(smem_addr(bar + 1));
         }
         __syncwarp();
+        // while the tensor core works: this quarter of the output row starts as zeros
+        if (g_bf16) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 32 * q + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+        } else {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * q + 4 * g, kPRows, 4)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         ok = mbar_wait(smem_addr(bar + 1), (uint32_t)(j & 1)) && ok;
         fence_after_sync();
 
@@ -260,26 +272,51 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 lt[4 * g + 3] = __uint_as_float(r[4 * g + 3]) + c.w;
             }
         };
-        float e_max = -FLT_MAX;
+        // best and second-best estimate of this quarter (and where the best is)
+        float e1 = -FLT_MAX, e2 = -FLT_MAX;
+        int a1 = 0;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             float lt[16];
             est(b, lt);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) e_max = fmaxf(e_max, lt[jj]);
+            for (int jj = 0; jj < 16; ++jj) {
+                const float v = lt[jj];
+                if (v > e1) {
+                    e2 = e1;
+                    e1 = v;
+                    a1 = 16 * b + jj;
+                } else {
+                    e2 = fmaxf(e2, v);
+                }
+            }
         }
-        ex0[q * kPK + i] = e_max;
-        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
+        ex0[q * kPK + i] = e1;
+        ex2[q * kPK + i] = e2;
         __syncthreads();
-        const float keep_from =
-            fmaxf(fmaxf(ex0[i], ex0[kPK + i]), fmaxf(ex0[2 * kPK + i], ex0[3 * kPK + i])) - kPT - 2.f * delta;
-        uint32_t mask = 0;
+        // the row's best M1 and second-best M2 estimate: the kept set is
+        // {k : l~_k >= M1 - T - 2 delta}; it is {argmax} alone iff M2 falls below that
+        float m1 = -FLT_MAX, m2 = -FLT_MAX;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            float lt[16];
-            est(b, lt);
+        for (int g = 0; g < 4; ++g) {
+            const float v1 = ex0[g * kPK + i], v2 = ex2[g * kPK + i];
+            m2 = fmaxf(m2, fmaxf(v2, fminf(v1, m1)));
+            m1 = fmaxf(m1, v1);
+        }
+        const float keep_from = m1 - kPT - 2.f * delta;
+        const bool single = ok && m2 < keep_from;
+        // single: a posterior of exactly 1 at the argmax (dropped mass < 128 e^-30)
+        uint32_t mask = single && e1 == m1 ? 1u << a1 : 0u;
+        if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
+            uint32_t mk = 0;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) mask |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * b + jj);
+            for (int b = 0; b < 2; ++b) {
+                float lt[16];
+                est(b, lt);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) mk |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * b + jj);
+            }
+            if (!single) mask = mk;
         }
 
         // exact log-joint of a kept component
@@ -296,28 +333,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
         };
-        // kept counts of the four quarters of the row
-        ex1[q * kPK + i] = (float)__popc(mask);
-        __syncthreads();
-        const int total = (int)(ex1[i] + ex1[kPK + i] + ex1[2 * kPK + i] + ex1[3 * kPK + i]);
-        // this quarter of the output row starts as zeros; a row with a single kept
-        // component has posterior exactly 1 there and needs no exact evaluation
-        if (g_bf16) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-                *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 32 * q + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
-            if (total == 1 && mask)
-                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 32 * q + __ffs(mask) - 1, kPRows, 2)) =
+        if (single && mask) {
+            if (g_bf16)
+                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 32 * q + a1, kPRows, 2)) =
                     __float2bfloat16_rn(1.0f);
-        } else {
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * q + 4 * g, kPRows, 4)) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-            if (total == 1 && mask)
-                *reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + __ffs(mask) - 1, kPRows, 4)) = 1.0f;
+            else
+                *reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + a1, kPRows, 4)) = 1.0f;
         }
-        const uint32_t xmask = total > 1 ? mask : 0u;   // the components of rows that need the softmax
+        const uint32_t xmask = single ? 0u : mask;   // the components of rows that need the softmax
         if (__syncthreads_or(xmask != 0u)) {
             // Runs f(k, l_k) for every component k of xmask.  Few per lane: each lane
             // walks its own set, reading the parameters of its own components.  Many:

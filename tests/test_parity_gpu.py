@@ -34,6 +34,7 @@ def _report(name, err, tol):
     (W["bidir_16k_peaked"], 3),
     # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
     (W["tiny"].with_(mode="bidir", B=4, H=16, N=1100, d=64, dv=64, K=128), None),
+    (W["tiny"].with_(mode="bidir", B=8, H=25, N=200, d=64, dv=64, K=128), None),
     (W["causal_8k_K512"], 2),
     (W["causal_64k_bf16"], 2),
 ])
@@ -86,6 +87,7 @@ def test_responsibilities_adversarial_rows():
     (W["bidir_16k_peaked"], 3),
     # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
     (W["tiny"].with_(mode="bidir", B=4, H=16, N=1100, d=64, dv=64, K=128), None),
+    (W["tiny"].with_(mode="bidir", B=8, H=25, N=200, d=64, dv=64, K=128), None),
     (W["causal_4k"].with_(mode="bidir", gemm_dtype="bf16"), 2),
 ])
 def test_bidir(wl, sample):
@@ -115,6 +117,8 @@ CAUSAL = [
     (W["tiny"].with_(B=1, H=2, N=700, d=32, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
     (W["tiny"].with_(B=4, H=16, N=1100, d=64, dv=64, K=128), None, 0),
+    # two-chunk slices, three chunks per CTA: the state kernel's ranges span slices
+    (W["tiny"].with_(B=8, H=25, N=200, d=64, dv=64, K=128), None, 0),
     (W["tiny"].with_(B=2, H=16, N=1100, d=64, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     (W["causal_16k_peaked"], 3, 0),
     (W["causal_64k_bf16"], 2, 0),
