@@ -20,12 +20,15 @@
 // exact fp32 evaluation as the dense kernel (one packed FMA for (x - mu)/sigma,
 // one for the square-accumulate, per feature pair).
 //
-// One persistent CTA per SM, 16 warps, tiles of 128 rows: the four warps
-// 4q + w' share the TMEM lanes 32 w' .. +31 (one row each) and take component
-// quarter q.  The per-head bound matrix, padded parameters and constants are
-// built once per call by k_prep_pruned and bulk-copied into shared memory;
-// routing rows arrive by TMA (the next tile's load is issued as soon as the
-// current one has been read) and output tiles leave by TMA stores.
+// One persistent CTA per SM, 16 warps in two independent groups of 8 that
+// take alternate tiles of 128 rows, so that one group's tensor-core, TMA and
+// barrier waits overlap the other's arithmetic.  In a group, the two warps
+// 4h + w' share the TMEM lanes 32 w' .. +31 (one row each) and take component
+// half h.  The per-head bound matrix and constants are built once per call by
+// k_prep_pruned and bulk-copied into each group's shared memory; the exact
+// parameters, needed only by rows with two or more kept components, are read
+// from global memory (L2-resident).  Routing rows arrive by TMA into the
+// group's buffer, which then takes the output tile that leaves by TMA stores.
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -37,19 +40,50 @@ namespace {
 using namespace tc;
 
 constexpr int kPK = 128, kPD = 64, kPDP = kPD / 2;
-constexpr int kPThreads = 512, kPRows = 128, kPRowsPerCta = 1024;
+constexpr int kPThreads = 512, kPRows = 128;
+constexpr int kPGroups = 2, kPGThreads = kPThreads / kPGroups;
 constexpr int kPStride = kPDP + 1;            // padded float4 row of exact parameters
 constexpr float kPT = 30.f;                   // log-joint window kept exactly
 constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulation bound
 
+// Shared memory of one group: the bound matrix, the routing tile / output
+// tile buffer, constants c, c', A, M, exchange slots between the two halves of
+// a row, and three mbarriers (images, MMA, routing tile).
 struct PrunedSmem {
     static constexpr uint32_t W = kPrunedWBytes;                        // bf16 [128][128], SW128
-    static constexpr uint32_t X = kPRows * kPD * 4;                     // one routing tile (fp32 worst case)
-    static constexpr uint32_t O = kPRows * kPK * 4;                     // one output tile (fp32 worst case)
-    static constexpr uint32_t P = kPrunedPBytes;                        // float4 [128][33]
-    static constexpr uint32_t F = (4 + 12) * kPK * 4;                   // constants + exchange slots
-    static constexpr size_t bytes = 1024 + W + X + O + P + F + 64;
+    static constexpr uint32_t BUF = kPRows * kPK * 4;                   // output tile (fp32 worst case)
+    static constexpr uint32_t C = kPrunedCBytes;                        // c, c', A, M
+    static constexpr uint32_t EX = 3 * 2 * kPK * 4;                     // [3][2][128]
+    static constexpr uint32_t SMALL = C + EX + 64;
+    static constexpr size_t bytes = 1024 + kPGroups * ((size_t)W + BUF + SMALL) + 64;   // + the TMEM slot
 };
+
+// Named barrier of one group (ids 1, 2; id 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int g)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(kPGThreads) : "memory");
+}
+// Named barrier of one group that also returns the AND (or the OR) of `pred` over its threads.
+__device__ __forceinline__ bool group_and(int g, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(1 + g), "r"(kPGThreads)
+                 : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool group_or(int g, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(1 + g), "r"(kPGThreads)
+                 : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ uint32_t pack2(float a, float b)
 {
@@ -114,9 +148,10 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
 }
 
 // Persistent: CTA b handles the work items [b * per, (b + 1) * per) of the
-// list (slice, tile of 128 rows) in order, reloading the per-head images only
-// when the head changes.  The output tile is assembled in shared memory and
-// written by TMA stores that stop at the slice's last row.
+// list (slice, tile of 128 rows); group g takes items it0 + g, it0 + g + 2, ...
+// and reloads its images only when the head changes.  The output tile is
+// assembled in shared memory and written by TMA stores that stop at the
+// slice's last row.
 __global__ void __launch_bounds__(kPThreads, 1)
     k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap, int N, int H,
                   int BH, bool x_bf16, const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
@@ -124,22 +159,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *w_s = sm;                                                  // B operand W
-    unsigned char *xb = sm + PrunedSmem::W;                                   // routing tile
-    unsigned char *ob = xb + PrunedSmem::X;                                   // output tile
-    float4 *p_s = reinterpret_cast<float4 *>(ob + PrunedSmem::O);            // exact parameters
-    float *f_s = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(p_s) + PrunedSmem::P);
-    const float *c_s = f_s, *cp_s = f_s + kPK, *a_s = f_s + 2 * kPK, *m_s = f_s + 3 * kPK;
-    float *ex0 = f_s + 4 * kPK;    // [4][128] exchange slots between the quarters of a row
-    float *ex1 = f_s + 8 * kPK;
-    float *ex2 = f_s + 12 * kPK;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 16 * kPK);   // images, mma, x
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp >> 2;                      // component quarter
+    const int grp = warp >> 3;                    // group
+    const int gt = tid - grp * kPGThreads;        // thread in the group
+    const int hf = (warp >> 2) & 1;               // component half
     const uint32_t lane0 = 32 * (warp & 3);
     const int i = lane0 + lane;                   // row of the tile (TMEM lane)
+
+    unsigned char *w_s = sm + grp * PrunedSmem::W;                              // B operand W
+    unsigned char *buf = sm + kPGroups * PrunedSmem::W + grp * PrunedSmem::BUF; // routing tile, then output tile
+    float *f_s = reinterpret_cast<float *>(sm + kPGroups * (PrunedSmem::W + PrunedSmem::BUF) +
+                                           grp * PrunedSmem::SMALL);
+    const float *c_s = f_s, *cp_s = f_s + kPK, *a_s = f_s + 2 * kPK, *m_s = f_s + 3 * kPK;
+    float *ex0 = f_s + 4 * kPK;    // [2][128] exchange slots between the halves of a row
+    float *ex1 = f_s + 6 * kPK;
+    float *ex2 = f_s + 8 * kPK;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 10 * kPK);   // images, mma, x
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kPGroups * (PrunedSmem::W + PrunedSmem::BUF) +
+                                                   kPGroups * PrunedSmem::SMALL);
+    const uint32_t BAR_I = smem_addr(bar), BAR_M = smem_addr(bar + 1), BAR_X = smem_addr(bar + 2);
+
     const int tps = (N + kPRows - 1) / kPRows;    // tiles per slice
     const long long items = (long long)BH * tps;
     const long long per = (items + gridDim.x - 1) / gridDim.x;
@@ -147,53 +186,67 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const long long it1 = it0 + per < items ? it0 + per : items;
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
     const int ge = g_bf16 ? 2 : 4;
-    constexpr uint32_t A_COL = 0, D_COL = 128;
 
-    auto load_x = [&](long long it) {   // one thread: TMA of item it's rows
+    auto load_x = [&](long long it) {   // one thread: TMA of item it's rows into the group's buffer
         const int bh = (int)(it / tps), t = (int)(it % tps);
-        mbar_expect_tx(smem_addr(bar + 2), xbytes);
-        tma_load_3d(smem_addr(xb), &xmap, 0, t * kPRows, bh, smem_addr(bar + 2));
-        if (!x_bf16) tma_load_3d(smem_addr(xb + kPRows * 128), &xmap, 32, t * kPRows, bh, smem_addr(bar + 2));
+        mbar_expect_tx(BAR_X, xbytes);
+        tma_load_3d(smem_addr(buf), &xmap, 0, t * kPRows, bh, BAR_X);
+        if (!x_bf16) tma_load_3d(smem_addr(buf + kPRows * 128), &xmap, 32, t * kPRows, bh, BAR_X);
     };
     if (warp == 0) {
-        tmem_alloc(smem_addr(tslot), 256);
+        tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
-    if (tid == 0) {
+    // loads in flight that the loop has not waited for (each group's thread 0)
+    bool pend_x = false, pend_i = false;
+    uint32_t ph_x = 0, ph_i = 0;
+    if (gt == 0) {
         for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        if (it0 < it1) load_x(it0);
+        if (it0 + grp < it1) {
+            load_x(it0 + grp);
+            pend_x = true;
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tbase = *tslot;
+    const uint32_t tcol = *tslot + 256u * grp;   // the group's 256 TMEM columns
+    constexpr uint32_t A_COL = 0, D_COL = 128;
     const uint32_t id = idesc(128, kPK, kFmtBF16);
     bool ok = true;
-    int head = -1, nimg = 0;
+    int head = -1, nimg = 0, nx = 0, j = 0;
 
-    for (long long it = it0; it < it1; ++it) {
-        const int j = (int)(it - it0);
+    for (long long it = it0 + grp; it < it1 && ok; it += kPGroups, ++j) {
         const int bh = (int)(it / tps), t = (int)(it % tps);
         if (bh % H != head) {   // (re)load the images of this item's head
             head = bh % H;
-            if (tid == 0) {
+            if (gt == 0) {
                 fence_proxy_async();
-                mbar_expect_tx(smem_addr(bar), kPrunedWBytes + kPrunedPBytes + kPrunedCBytes);
-                bulk_g2s(smem_addr(w_s), wimg + (long long)head * kPrunedWBytes, kPrunedWBytes, smem_addr(bar));
-                bulk_g2s(smem_addr(p_s), pimg + (long long)head * kPK * kPStride, kPrunedPBytes, smem_addr(bar));
-                bulk_g2s(smem_addr(f_s), cimg + (long long)head * 4 * kPK, kPrunedCBytes, smem_addr(bar));
+                mbar_expect_tx(BAR_I, kPrunedWBytes + kPrunedCBytes);
+                bulk_g2s(smem_addr(w_s), wimg + (long long)head * kPrunedWBytes, kPrunedWBytes, BAR_I);
+                bulk_g2s(smem_addr(f_s), cimg + (long long)head * 4 * kPK, kPrunedCBytes, BAR_I);
+                pend_i = true;
+                ph_i = (uint32_t)(nimg & 1);
             }
-            ok = mbar_wait(smem_addr(bar), (uint32_t)(nimg & 1)) && ok;
+            const bool oki = mbar_wait(BAR_I, (uint32_t)(nimg & 1));
+            ok = ok && oki;
+            if (gt == 0 && oki) pend_i = false;
             ++nimg;
         }
-        ok = mbar_wait(smem_addr(bar + 2), (uint32_t)(j & 1)) && ok;
-        // the row (every quarter holds all 64 features) and its sums for the bound
+        const float4 *ph = pimg + (long long)head * kPK * kPStride;
+        {
+            const bool okx = mbar_wait(BAR_X, (uint32_t)(nx & 1));
+            ok = ok && okx;
+            if (gt == 0 && okx) pend_x = false;
+            ++nx;
+        }
+        // the row (both halves hold all 64 features) and its sums for the bound
         float2 xr[kPDP];
         if (x_bf16) {
 #pragma unroll
             for (int g = 0; g < kPD / 8; ++g) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 8 * g, kPRows, 2));
+                const uint4 u = *reinterpret_cast<const uint4 *>(buf + sw128_offset(i, 8 * g, kPRows, 2));
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -202,7 +255,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         } else {
 #pragma unroll
             for (int g = 0; g < kPD / 4; ++g) {
-                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 4 * g, kPRows, 4));
+                const float4 u = *reinterpret_cast<const float4 *>(buf + sw128_offset(i, 4 * g, kPRows, 4));
                 xr[2 * g] = make_float2(u.x, u.y);
                 xr[2 * g + 1] = make_float2(u.z, u.w);
             }
@@ -213,56 +266,52 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const float s2 = s2v.x + s2v.y;
         // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0])
         const float delta = fmaf(kPU, fmaf(0.5f * a_s[0], s2, m_s[0] * 8.f * sqrtf(s2)), 1e-3f);
-        // A = [x^2 | x] in bf16: quarter q writes operand columns [16q, 16q + 16)
-        {
+        // A = [x^2 | x] in bf16: half 0 writes the squares (columns 0..31), half 1 the values (32..63)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
             uint32_t p[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-                const float2 v = (q & 1) ? xr[16 + jj] : xr[jj];   // static indices keep xr in registers
-                p[jj] = q < 2 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
+                const float2 v = xr[16 * b + jj];
+                p[jj] = hf == 0 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
             }
-            tmem_st16(tmem_at(tbase, lane0, A_COL + 16 * q), p);
+            tmem_st16(tmem_at(tcol, lane0, A_COL + 32 * hf + 16 * b), p);
         }
         tmem_wait_st();
         fence_before_sync();
-        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
-        __syncthreads();   // the routing tile has been read; A is in TMEM
+        group_sync(grp);   // the routing tile has been read; A is in TMEM
         fence_after_sync();
-        if (tid == 0) {
-            if (it + 1 < it1) {
-                fence_proxy_async();
-                load_x(it + 1);
-            }
+        if (gt == 0) {
 #pragma unroll 1
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t kb = kk * 32;
                 const uint32_t boff = (kb >> 7) * (kPK * 128) + (kb & 127);
-                mma_ts(0u, tbase + D_COL, tbase + A_COL + kk * 8, sdesc_sw128(smem_addr(w_s + boff)), id,
+                mma_ts(0u, tcol + D_COL, tcol + A_COL + kk * 8, sdesc_sw128(smem_addr(w_s + boff)), id,
                        kk > 0 ? 1u : 0u);
             }
-            mma_commit(smem_addr(bar + 1));
+            mma_commit(BAR_M);
         }
         __syncwarp();
-        // while the tensor core works: this quarter of the output row starts as zeros
+        // while the tensor core works: this half of the output row starts as zeros
         if (g_bf16) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-                *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 32 * q + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+            for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<uint4 *>(buf + sw128_offset(i, 64 * hf + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
         } else {
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-                *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * q + 4 * g, kPRows, 4)) =
+            for (int g = 0; g < 16; ++g)
+                *reinterpret_cast<float4 *>(buf + sw128_offset(i, 64 * hf + 4 * g, kPRows, 4)) =
                     make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        ok = mbar_wait(smem_addr(bar + 1), (uint32_t)(j & 1)) && ok;
+        ok = mbar_wait(BAR_M, (uint32_t)(j & 1)) && ok;
         fence_after_sync();
 
-        // bound: best estimate of this quarter, then of the row; then the kept set
+        // bound estimates of this half: l~_k = D_k + c'_k
         auto est = [&](int b, float (&lt)[16]) {
             uint32_t r[16];
-            tmem_ld16(tmem_at(tbase, lane0, D_COL + 32 * q + 16 * b), r);
+            tmem_ld16(tmem_at(tcol, lane0, D_COL + 64 * hf + 16 * b), r);
             tmem_wait_ld();
-            const float4 *c4 = reinterpret_cast<const float4 *>(cp_s + 32 * q + 16 * b);
+            const float4 *c4 = reinterpret_cast<const float4 *>(cp_s + 64 * hf + 16 * b);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 const float4 c = c4[g];
@@ -272,11 +321,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 lt[4 * g + 3] = __uint_as_float(r[4 * g + 3]) + c.w;
             }
         };
-        // best and second-best estimate of this quarter (and where the best is)
+        // best and second-best estimate of this half (and where the best is)
         float e1 = -FLT_MAX, e2 = -FLT_MAX;
         int a1 = 0;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             float lt[16];
             est(b, lt);
 #pragma unroll
@@ -291,84 +340,93 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
         }
-        ex0[q * kPK + i] = e1;
-        ex2[q * kPK + i] = e2;
-        __syncthreads();
-        // the row's best M1 and second-best M2 estimate: the kept set is
-        // {k : l~_k >= M1 - T - 2 delta}; it is {argmax} alone iff M2 falls below that
-        float m1 = -FLT_MAX, m2 = -FLT_MAX;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const float v1 = ex0[g * kPK + i], v2 = ex2[g * kPK + i];
-            m2 = fmaxf(m2, fmaxf(v2, fminf(v1, m1)));
-            m1 = fmaxf(m1, v1);
-        }
+        ex0[hf * kPK + i] = e1;
+        ex2[hf * kPK + i] = e2;
+        group_sync(grp);
+        // the row's best m1 and second-best m2: the kept set is {k : l~_k >= m1 - T - 2 delta};
+        // it is {argmax} alone iff m2 falls below that
+        const float o1 = ex0[(1 - hf) * kPK + i], o2 = ex2[(1 - hf) * kPK + i];
+        const float m1 = fmaxf(e1, o1), m2 = fmaxf(fmaxf(e2, o2), fminf(e1, o1));
         const float keep_from = m1 - kPT - 2.f * delta;
         const bool single = ok && m2 < keep_from;
         // single: a posterior of exactly 1 at the argmax (dropped mass < 128 e^-30)
-        uint32_t mask = single && e1 == m1 ? 1u << a1 : 0u;
+        uint32_t mask[2] = {0u, 0u};
+        if (single && e1 == m1) {
+            mask[a1 >> 5] = 1u << (a1 & 31);
+            if (g_bf16)
+                *reinterpret_cast<__nv_bfloat16 *>(buf + sw128_offset(i, 64 * hf + a1, kPRows, 2)) =
+                    __float2bfloat16_rn(1.0f);
+            else
+                *reinterpret_cast<float *>(buf + sw128_offset(i, 64 * hf + a1, kPRows, 4)) = 1.0f;
+        }
         if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
-            uint32_t mk = 0;
+            uint32_t mk[2] = {0u, 0u};
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < 4; ++b) {
                 float lt[16];
                 est(b, lt);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) mk |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * b + jj);
+                for (int jj = 0; jj < 16; ++jj)
+                    mk[b >> 1] |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * (b & 1) + jj);
             }
-            if (!single) mask = mk;
+            if (!single) {
+                mask[0] = mk[0];
+                mask[1] = mk[1];
+            }
         }
-
-        // exact log-joint of a kept component
-        auto exact = [&](int k) {
-            const float4 *pk = p_s + k * kPStride;
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        const uint32_t xm0 = single ? 0u : mask[0], xm1 = single ? 0u : mask[1];   // rows that need the softmax
+        if (group_or(grp, (xm0 | xm1) != 0u)) {
+            // exact log-joint of a component (parameters from global memory, L2-resident)
+            auto exact = [&](int k) {
+                const float4 *pk = ph + k * kPStride;
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int dp = 0; dp < kPDP; dp += 2) {
-                const float4 p = pk[dp], r = pk[dp + 1];
-                const float2 y0 = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
-                acc0 = __ffma2_rn(y0, y0, acc0);
-                const float2 y1 = __ffma2_rn(xr[dp + 1], make_float2(r.x, r.y), make_float2(r.z, r.w));
-                acc1 = __ffma2_rn(y1, y1, acc1);
+                for (int dp = 0; dp < kPDP; dp += 2) {
+                    const float4 p = __ldg(pk + dp), r = __ldg(pk + dp + 1);
+                    const float2 y0 = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
+                    acc0 = __ffma2_rn(y0, y0, acc0);
+                    const float2 y1 = __ffma2_rn(xr[dp + 1], make_float2(r.x, r.y), make_float2(r.z, r.w));
+                    acc1 = __ffma2_rn(y1, y1, acc1);
+                }
+                return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
+            };
+            // Runs f(k, l_k) for every component k of the two masks, by 32-component word.
+            // Few per lane: each lane walks its own set.  Many: the warp walks the union of
+            // its lanes' sets one component at a time, so that the parameter reads are
+            // shared by the warp.  The warp-wide choice is made here, where every lane is
+            // present (for_kept itself also runs in lane-divergent code).
+            uint32_t unis[2];
+            bool lanes[2];
+#pragma unroll
+            for (int wd = 0; wd < 2; ++wd) {
+                const uint32_t mk = wd ? xm1 : xm0;
+                unis[wd] = __reduce_or_sync(0xffffffffu, mk);
+                lanes[wd] = 4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(unis[wd]);
             }
-            return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
-        };
-        if (single && mask) {
-            if (g_bf16)
-                *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 32 * q + a1, kPRows, 2)) =
-                    __float2bfloat16_rn(1.0f);
-            else
-                *reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + a1, kPRows, 4)) = 1.0f;
-        }
-        const uint32_t xmask = single ? 0u : mask;   // the components of rows that need the softmax
-        if (__syncthreads_or(xmask != 0u)) {
-            // Runs f(k, l_k) for every component k of xmask.  Few per lane: each lane
-            // walks its own set, reading the parameters of its own components.  Many:
-            // the warp walks the union of its lanes' sets one component at a time, so
-            // that the parameter reads are broadcasts (per-lane reads would cost 32
-            // times the shared-memory traffic).
-            const uint32_t uni = __reduce_or_sync(0xffffffffu, xmask);
-            const bool per_lane =
-                4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(xmask)) <= (uint32_t)__popc(uni);
             auto for_kept = [&](auto &&f) {
-                if (per_lane) {
-                    for (uint32_t mm = xmask; mm; mm &= mm - 1) {
-                        const int k = 32 * q + __ffs(mm) - 1;
-                        f(k, exact(k));
-                    }
-                } else {
-                    for (uint32_t mm = uni; mm; mm &= mm - 1) {
-                        const int kq = __ffs(mm) - 1;
-                        const float l = exact(32 * q + kq);
-                        if ((xmask >> kq) & 1u) f(32 * q + kq, l);
+#pragma unroll
+                for (int wd = 0; wd < 2; ++wd) {
+                    const int k0 = 64 * hf + 32 * wd;
+                    const uint32_t mk = wd ? xm1 : xm0, uni = unis[wd];
+                    if (lanes[wd]) {
+                        for (uint32_t mm = mk; mm; mm &= mm - 1) {
+                            const int k = k0 + __ffs(mm) - 1;
+                            f(k, exact(k));
+                        }
+                    } else {
+                        for (uint32_t mm = uni; mm; mm &= mm - 1) {
+                            const int kq = __ffs(mm) - 1;
+                            const float l = exact(k0 + kq);
+                            if ((mk >> kq) & 1u) f(k0 + kq, l);
+                        }
                     }
                 }
             };
-            // exact pass: online maximum and sum over the kept components of this quarter;
+            // exact pass: online maximum and sum over the kept components of this half;
             // with an fp32 output tile the log-joints wait in it for the normalisation
             float mt = -FLT_MAX, st = 0.f;
             for_kept([&](int k, float l) {
-                if (!g_bf16) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                if (!g_bf16) *reinterpret_cast<float *>(buf + sw128_offset(i, k, kPRows, 4)) = l;
                 if (l > mt) {
                     st = st * expf(mt - l) + 1.f;
                     mt = l;
@@ -376,45 +434,56 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     st += expf(l - mt);
                 }
             });
-            ex1[q * kPK + i] = mt;
-            ex2[q * kPK + i] = st;
-            __syncthreads();
-            if (xmask) {
-                float m = ex1[i];
-#pragma unroll
-                for (int g = 1; g < 4; ++g) m = fmaxf(m, ex1[g * kPK + i]);
-                float ssum = 0.f;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) ssum += ex2[g * kPK + i] * expf(ex1[g * kPK + i] - m);
-                const float inv = 1.0f / ssum;
-                // the kept posteriors of this quarter into the output tile
+            ex1[hf * kPK + i] = mt;
+            ex2[hf * kPK + i] = st;
+            group_sync(grp);
+            if (xm0 | xm1) {
+                const float q1 = ex1[(1 - hf) * kPK + i], q2 = ex2[(1 - hf) * kPK + i];
+                const float m = fmaxf(mt, q1);
+                const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
+                // the kept posteriors of this half into the output tile
                 if (g_bf16) {
                     for_kept([&](int k, float l) {
-                        *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) =
+                        *reinterpret_cast<__nv_bfloat16 *>(buf + sw128_offset(i, k, kPRows, 2)) =
                             __float2bfloat16_rn(expf(l - m) * inv);
                     });
                 } else {
-                    for (uint32_t mm = xmask; mm; mm &= mm - 1) {
-                        float *o = reinterpret_cast<float *>(ob + sw128_offset(i, 32 * q + __ffs(mm) - 1, kPRows, 4));
-                        *o = expf(*o - m) * inv;
-                    }
+#pragma unroll
+                    for (int wd = 0; wd < 2; ++wd)
+                        for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
+                            float *o = reinterpret_cast<float *>(
+                                buf + sw128_offset(i, 64 * hf + 32 * wd + __ffs(mm) - 1, kPRows, 4));
+                            *o = expf(*o - m) * inv;
+                        }
                 }
             }
         }
         fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
         fence_before_sync();
-        __syncthreads();
+        ok = group_and(grp, ok);   // the group leaves the loop together
         fence_after_sync();
-        if (tid == 0) {
+        if (gt == 0) {
             for (int a = 0; a < kPK * ge / 128; ++a)
-                tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+                tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(buf + a * (kPRows * 128)));
             bulk_commit();
+            if (it + kPGroups < it1 && ok) {   // the buffer takes the group's next routing tile once read
+                bulk_wait_read();
+                fence_proxy_async();
+                load_x(it + kPGroups);
+                pend_x = true;
+                ph_x = (uint32_t)(nx & 1);
+            }
         }
     }
-    if (tid == 0) bulk_wait_all();
+    // after a failed wait: let the copies still in flight land before the shared memory is released
+    if (gt == 0) {
+        if (pend_x) (void)mbar_wait(BAR_X, ph_x);
+        if (pend_i) (void)mbar_wait(BAR_I, ph_i);
+        bulk_wait_all();
+    }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(*tslot, 512);
 }
 
 } // namespace
