@@ -20,15 +20,18 @@
 // exact fp32 evaluation as the dense kernel (one packed FMA for (x - mu)/sigma,
 // one for the square-accumulate, per feature pair).
 //
-// One persistent CTA per SM, 16 warps in two independent groups of 8 that
-// take alternate tiles of 128 rows, so that one group's tensor-core, TMA and
-// barrier waits overlap the other's arithmetic.  In a group, the two warps
-// 4h + w' share the TMEM lanes 32 w' .. +31 (one row each) and take component
-// half h.  The per-head bound matrix and constants are built once per call by
-// k_prep_pruned and bulk-copied into each group's shared memory; the exact
-// parameters, needed only by rows with two or more kept components, are read
-// from global memory (L2-resident).  Routing rows arrive by TMA into the
-// group's buffer, which then takes the output tile that leaves by TMA stores.
+// One persistent CTA per SM, 16 warps in two groups of 8 that take alternate
+// tiles of 128 rows, so that one group's tensor-core, TMA and barrier waits
+// overlap the other's arithmetic.  In a group, the two warps 4h + w' share the
+// TMEM lanes 32 w' .. +31 (one row each) and take component half h.  The
+// per-head bound matrix and constants are built once per call by
+// k_prep_pruned and bulk-copied into shared memory (both groups work on the
+// same head: the CTA's range is walked slice by slice); the exact parameters,
+// needed only by rows with two or more kept components, are read from global
+// memory (L2-resident).  Routing tiles arrive by TMA into one buffer that the
+// groups consume in item order (the consumer of tile n fetches tile n + 1);
+// each group assembles its output tile in its own buffer, which leaves by TMA
+// stores.
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -46,16 +49,16 @@ constexpr int kPStride = kPDP + 1;            // padded float4 row of exact para
 constexpr float kPT = 30.f;                   // log-joint window kept exactly
 constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulation bound
 
-// Shared memory of one group: the bound matrix, the routing tile / output
-// tile buffer, constants c, c', A, M, exchange slots between the two halves of
-// a row, and three mbarriers (images, MMA, routing tile).
+// Shared memory: the bound matrix, the routing tile, each group's output tile,
+// the constants c, c', A, M, each group's exchange slots between the two
+// halves of a row, and the mbarriers (images, routing tile, each group's MMA).
 struct PrunedSmem {
     static constexpr uint32_t W = kPrunedWBytes;                        // bf16 [128][128], SW128
-    static constexpr uint32_t BUF = kPRows * kPK * 4;                   // output tile (fp32 worst case)
+    static constexpr uint32_t X = kPRows * kPD * 4;                     // routing tile (fp32 worst case)
+    static constexpr uint32_t O = kPRows * kPK * 4;                     // output tile (fp32 worst case)
     static constexpr uint32_t C = kPrunedCBytes;                        // c, c', A, M
-    static constexpr uint32_t EX = 3 * 2 * kPK * 4;                     // [3][2][128]
-    static constexpr uint32_t SMALL = C + EX + 64;
-    static constexpr size_t bytes = 1024 + kPGroups * ((size_t)W + BUF + SMALL) + 64;   // + the TMEM slot
+    static constexpr uint32_t EX = 3 * 2 * kPK * 4;                     // [3][2][128] per group
+    static constexpr size_t bytes = 1024 + W + X + kPGroups * (size_t)O + C + kPGroups * (size_t)EX + 64;
 };
 
 // Named barrier of one group (ids 1, 2; id 0 is __syncthreads).
@@ -148,10 +151,9 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
 }
 
 // Persistent: CTA b handles the work items [b * per, (b + 1) * per) of the
-// list (slice, tile of 128 rows); group g takes items it0 + g, it0 + g + 2, ...
-// and reloads its images only when the head changes.  The output tile is
-// assembled in shared memory and written by TMA stores that stop at the
-// slice's last row.
+// list (slice, tile of 128 rows), slice by slice; within a slice group g takes
+// the items s + g, s + g + 2, ...  The output tile is assembled in shared memory
+// and written by TMA stores that stop at the slice's last row.
 __global__ void __launch_bounds__(kPThreads, 1)
     k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap, int N, int H,
                   int BH, bool x_bf16, const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
@@ -166,18 +168,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane0 = 32 * (warp & 3);
     const int i = lane0 + lane;                   // row of the tile (TMEM lane)
 
-    unsigned char *w_s = sm + grp * PrunedSmem::W;                              // B operand W
-    unsigned char *buf = sm + kPGroups * PrunedSmem::W + grp * PrunedSmem::BUF; // routing tile, then output tile
-    float *f_s = reinterpret_cast<float *>(sm + kPGroups * (PrunedSmem::W + PrunedSmem::BUF) +
-                                           grp * PrunedSmem::SMALL);
+    unsigned char *w_s = sm;                                                  // B operand W
+    unsigned char *xb = sm + PrunedSmem::W;                                   // routing tile
+    unsigned char *ob = xb + PrunedSmem::X + grp * PrunedSmem::O;             // this group's output tile
+    float *f_s = reinterpret_cast<float *>(xb + PrunedSmem::X + kPGroups * PrunedSmem::O);
     const float *c_s = f_s, *cp_s = f_s + kPK, *a_s = f_s + 2 * kPK, *m_s = f_s + 3 * kPK;
-    float *ex0 = f_s + 4 * kPK;    // [2][128] exchange slots between the halves of a row
-    float *ex1 = f_s + 6 * kPK;
-    float *ex2 = f_s + 8 * kPK;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 10 * kPK);   // images, mma, x
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kPGroups * (PrunedSmem::W + PrunedSmem::BUF) +
-                                                   kPGroups * PrunedSmem::SMALL);
-    const uint32_t BAR_I = smem_addr(bar), BAR_M = smem_addr(bar + 1), BAR_X = smem_addr(bar + 2);
+    float *ex0 = f_s + 4 * kPK + grp * 6 * kPK;   // [2][128] exchange slots between the halves of a row
+    float *ex1 = ex0 + 2 * kPK;
+    float *ex2 = ex0 + 4 * kPK;
+    // images, routing tile for group 0 / 1, MMA of group 0 / 1
+    uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 4 * kPK + kPGroups * 6 * kPK);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1 + grp), BAR_M = smem_addr(bar + 3 + grp);
 
     const int tps = (N + kPRows - 1) / kPRows;    // tiles per slice
     const long long items = (long long)BH * tps;
@@ -187,26 +189,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
     const int ge = g_bf16 ? 2 : 4;
 
-    auto load_x = [&](long long it) {   // one thread: TMA of item it's rows into the group's buffer
+    // one thread: TMA of item it's rows, counted on the barrier of the group that takes it
+    // (group 0 takes a slice's first item in the range, then the groups alternate)
+    auto load_x = [&](long long it) {
         const int bh = (int)(it / tps), t = (int)(it % tps);
-        mbar_expect_tx(BAR_X, xbytes);
-        tma_load_3d(smem_addr(buf), &xmap, 0, t * kPRows, bh, BAR_X);
-        if (!x_bf16) tma_load_3d(smem_addr(buf + kPRows * 128), &xmap, 32, t * kPRows, bh, BAR_X);
+        const long long first = max((it / tps) * tps, it0);
+        const uint32_t bx = smem_addr(bar + 1 + (int)((it - first) & 1));
+        mbar_expect_tx(bx, xbytes);
+        tma_load_3d(smem_addr(xb), &xmap, 0, t * kPRows, bh, bx);
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kPRows * 128), &xmap, 32, t * kPRows, bh, bx);
     };
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
-    // loads in flight that the loop has not waited for (each group's thread 0)
-    bool pend_x = false, pend_i = false;
-    uint32_t ph_x = 0, ph_i = 0;
-    if (gt == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
+    if (tid == 0) {
+        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        if (it0 + grp < it1) {
-            load_x(it0 + grp);
-            pend_x = true;
-        }
+        if (it0 < it1) load_x(it0);
     }
     fence_before_sync();
     __syncthreads();
@@ -215,270 +215,265 @@ __global__ void __launch_bounds__(kPThreads, 1)
     constexpr uint32_t A_COL = 0, D_COL = 128;
     const uint32_t id = idesc(128, kPK, kFmtBF16);
     bool ok = true;
-    int head = -1, nimg = 0, nx = 0, j = 0;
+    int head = -1, nimg = 0, j = 0;   // j: this group's items so far (its MMA and routing-tile phases)
 
-    for (long long it = it0 + grp; it < it1 && ok; it += kPGroups, ++j) {
-        const int bh = (int)(it / tps), t = (int)(it % tps);
-        if (bh % H != head) {   // (re)load the images of this item's head
-            head = bh % H;
-            if (gt == 0) {
+    for (long long s0 = it0; s0 < it1 && ok;) {
+        const long long s1 = min(it1, (s0 / tps + 1) * tps);   // this slice's items in the range
+        const int hd = (int)((s0 / tps) % H);
+        if (hd != head) {   // both groups are done with the previous head: (re)load the images
+            head = hd;
+            fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
                 fence_proxy_async();
                 mbar_expect_tx(BAR_I, kPrunedWBytes + kPrunedCBytes);
                 bulk_g2s(smem_addr(w_s), wimg + (long long)head * kPrunedWBytes, kPrunedWBytes, BAR_I);
                 bulk_g2s(smem_addr(f_s), cimg + (long long)head * 4 * kPK, kPrunedCBytes, BAR_I);
-                pend_i = true;
-                ph_i = (uint32_t)(nimg & 1);
             }
-            const bool oki = mbar_wait(BAR_I, (uint32_t)(nimg & 1));
-            ok = ok && oki;
-            if (gt == 0 && oki) pend_i = false;
+            ok = mbar_wait(BAR_I, (uint32_t)(nimg & 1)) && ok;
             ++nimg;
         }
         const float4 *ph = pimg + (long long)head * kPK * kPStride;
-        {
-            const bool okx = mbar_wait(BAR_X, (uint32_t)(nx & 1));
-            ok = ok && okx;
-            if (gt == 0 && okx) pend_x = false;
-            ++nx;
-        }
-        // the row (both halves hold all 64 features) and its sums for the bound
-        float2 xr[kPDP];
-        if (x_bf16) {
+        for (long long it = s0 + grp; it < s1; it += kPGroups, ++j) {
+            const int bh = (int)(it / tps), t = (int)(it % tps);
+            // this group's routing tiles land in order on its own barrier; the consumer of
+            // tile n fetches tile n + 1, so a group's next tile is never fetched before it
+            // has consumed the previous one (its barrier runs at most one phase ahead)
+            ok = mbar_wait(BAR_X, (uint32_t)(j & 1)) && ok;
+            // the row (both halves hold all 64 features) and its sums for the bound
+            float2 xr[kPDP];
+            if (x_bf16) {
 #pragma unroll
-            for (int g = 0; g < kPD / 8; ++g) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(buf + sw128_offset(i, 8 * g, kPRows, 2));
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                for (int g = 0; g < kPD / 8; ++g) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 8 * g, kPRows, 2));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    xr[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
-            }
-        } else {
+                    for (int e = 0; e < 4; ++e)
+                        xr[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+                }
+            } else {
 #pragma unroll
-            for (int g = 0; g < kPD / 4; ++g) {
-                const float4 u = *reinterpret_cast<const float4 *>(buf + sw128_offset(i, 4 * g, kPRows, 4));
-                xr[2 * g] = make_float2(u.x, u.y);
-                xr[2 * g + 1] = make_float2(u.z, u.w);
-            }
-        }
-        float2 s2v = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
-        const float s2 = s2v.x + s2v.y;
-        // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0])
-        const float delta = fmaf(kPU, fmaf(0.5f * a_s[0], s2, m_s[0] * 8.f * sqrtf(s2)), 1e-3f);
-        // A = [x^2 | x] in bf16: half 0 writes the squares (columns 0..31), half 1 the values (32..63)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            uint32_t p[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const float2 v = xr[16 * b + jj];
-                p[jj] = hf == 0 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
-            }
-            tmem_st16(tmem_at(tcol, lane0, A_COL + 32 * hf + 16 * b), p);
-        }
-        tmem_wait_st();
-        fence_before_sync();
-        group_sync(grp);   // the routing tile has been read; A is in TMEM
-        fence_after_sync();
-        if (gt == 0) {
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t kb = kk * 32;
-                const uint32_t boff = (kb >> 7) * (kPK * 128) + (kb & 127);
-                mma_ts(0u, tcol + D_COL, tcol + A_COL + kk * 8, sdesc_sw128(smem_addr(w_s + boff)), id,
-                       kk > 0 ? 1u : 0u);
-            }
-            mma_commit(BAR_M);
-        }
-        __syncwarp();
-        // while the tensor core works: this half of the output row starts as zeros
-        if (g_bf16) {
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                *reinterpret_cast<uint4 *>(buf + sw128_offset(i, 64 * hf + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
-        } else {
-#pragma unroll
-            for (int g = 0; g < 16; ++g)
-                *reinterpret_cast<float4 *>(buf + sw128_offset(i, 64 * hf + 4 * g, kPRows, 4)) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        ok = mbar_wait(BAR_M, (uint32_t)(j & 1)) && ok;
-        fence_after_sync();
-
-        // bound estimates of this half: l~_k = D_k + c'_k
-        auto est = [&](int b, float (&lt)[16]) {
-            uint32_t r[16];
-            tmem_ld16(tmem_at(tcol, lane0, D_COL + 64 * hf + 16 * b), r);
-            tmem_wait_ld();
-            const float4 *c4 = reinterpret_cast<const float4 *>(cp_s + 64 * hf + 16 * b);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float4 c = c4[g];
-                lt[4 * g] = __uint_as_float(r[4 * g]) + c.x;
-                lt[4 * g + 1] = __uint_as_float(r[4 * g + 1]) + c.y;
-                lt[4 * g + 2] = __uint_as_float(r[4 * g + 2]) + c.z;
-                lt[4 * g + 3] = __uint_as_float(r[4 * g + 3]) + c.w;
-            }
-        };
-        // best and second-best estimate of this half (and where the best is)
-        float e1 = -FLT_MAX, e2 = -FLT_MAX;
-        int a1 = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            float lt[16];
-            est(b, lt);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const float v = lt[jj];
-                if (v > e1) {
-                    e2 = e1;
-                    e1 = v;
-                    a1 = 16 * b + jj;
-                } else {
-                    e2 = fmaxf(e2, v);
+                for (int g = 0; g < kPD / 4; ++g) {
+                    const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 4 * g, kPRows, 4));
+                    xr[2 * g] = make_float2(u.x, u.y);
+                    xr[2 * g + 1] = make_float2(u.z, u.w);
                 }
             }
-        }
-        ex0[hf * kPK + i] = e1;
-        ex2[hf * kPK + i] = e2;
-        group_sync(grp);
-        // the row's best m1 and second-best m2: the kept set is {k : l~_k >= m1 - T - 2 delta};
-        // it is {argmax} alone iff m2 falls below that
-        const float o1 = ex0[(1 - hf) * kPK + i], o2 = ex2[(1 - hf) * kPK + i];
-        const float m1 = fmaxf(e1, o1), m2 = fmaxf(fmaxf(e2, o2), fminf(e1, o1));
-        const float keep_from = m1 - kPT - 2.f * delta;
-        const bool single = ok && m2 < keep_from;
-        // single: a posterior of exactly 1 at the argmax (dropped mass < 128 e^-30)
-        uint32_t mask[2] = {0u, 0u};
-        if (single && e1 == m1) {
-            mask[a1 >> 5] = 1u << (a1 & 31);
-            if (g_bf16)
-                *reinterpret_cast<__nv_bfloat16 *>(buf + sw128_offset(i, 64 * hf + a1, kPRows, 2)) =
-                    __float2bfloat16_rn(1.0f);
-            else
-                *reinterpret_cast<float *>(buf + sw128_offset(i, 64 * hf + a1, kPRows, 4)) = 1.0f;
-        }
-        if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
-            uint32_t mk[2] = {0u, 0u};
+            float2 s2v = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
+            const float s2 = s2v.x + s2v.y;
+            // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0])
+            const float delta = fmaf(kPU, fmaf(0.5f * a_s[0], s2, m_s[0] * 8.f * sqrtf(s2)), 1e-3f);
+            // A = [x^2 | x] in bf16: half 0 writes the squares (columns 0..31), half 1 the values (32..63)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                uint32_t p[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float2 v = xr[16 * b + jj];
+                    p[jj] = hf == 0 ? pack2(v.x * v.x, v.y * v.y) : pack2(v.x, v.y);
+                }
+                tmem_st16(tmem_at(tcol, lane0, A_COL + 32 * hf + 16 * b), p);
+            }
+            tmem_wait_st();
+            fence_before_sync();
+            if (gt == 0) bulk_wait_read();   // this group's previous output tile has left shared memory
+            group_sync(grp);   // the routing tile has been read; A is in TMEM
+            fence_after_sync();
+            if (gt == 0) {
+                if (it + 1 < it1) {   // the next item's tile
+                    fence_proxy_async();
+                    load_x(it + 1);
+                }
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t kb = kk * 32;
+                    const uint32_t boff = (kb >> 7) * (kPK * 128) + (kb & 127);
+                    mma_ts(0u, tcol + D_COL, tcol + A_COL + kk * 8, sdesc_sw128(smem_addr(w_s + boff)), id,
+                           kk > 0 ? 1u : 0u);
+                }
+                mma_commit(BAR_M);
+            }
+            __syncwarp();
+            // while the tensor core works: this half of the output row starts as zeros
+            if (g_bf16) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 64 * hf + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 16; ++g)
+                    *reinterpret_cast<float4 *>(ob + sw128_offset(i, 64 * hf + 4 * g, kPRows, 4)) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            ok = mbar_wait(BAR_M, (uint32_t)(j & 1)) && ok;
+            fence_after_sync();
+
+            // bound estimates of this half: l~_k = D_k + c'_k
+            auto est = [&](int b, float (&lt)[16]) {
+                uint32_t r[16];
+                tmem_ld16(tmem_at(tcol, lane0, D_COL + 64 * hf + 16 * b), r);
+                tmem_wait_ld();
+                const float4 *c4 = reinterpret_cast<const float4 *>(cp_s + 64 * hf + 16 * b);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 c = c4[g];
+                    lt[4 * g] = __uint_as_float(r[4 * g]) + c.x;
+                    lt[4 * g + 1] = __uint_as_float(r[4 * g + 1]) + c.y;
+                    lt[4 * g + 2] = __uint_as_float(r[4 * g + 2]) + c.z;
+                    lt[4 * g + 3] = __uint_as_float(r[4 * g + 3]) + c.w;
+                }
+            };
+            // best and second-best estimate of this half (and where the best is), without branches
+            float e1 = -FLT_MAX, e2 = -FLT_MAX;
+            int a1 = 0;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 float lt[16];
                 est(b, lt);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    mk[b >> 1] |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * (b & 1) + jj);
-            }
-            if (!single) {
-                mask[0] = mk[0];
-                mask[1] = mk[1];
-            }
-        }
-        const uint32_t xm0 = single ? 0u : mask[0], xm1 = single ? 0u : mask[1];   // rows that need the softmax
-        if (group_or(grp, (xm0 | xm1) != 0u)) {
-            // exact log-joint of a component (parameters from global memory, L2-resident)
-            auto exact = [&](int k) {
-                const float4 *pk = ph + k * kPStride;
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int dp = 0; dp < kPDP; dp += 2) {
-                    const float4 p = __ldg(pk + dp), r = __ldg(pk + dp + 1);
-                    const float2 y0 = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
-                    acc0 = __ffma2_rn(y0, y0, acc0);
-                    const float2 y1 = __ffma2_rn(xr[dp + 1], make_float2(r.x, r.y), make_float2(r.z, r.w));
-                    acc1 = __ffma2_rn(y1, y1, acc1);
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float v = lt[jj];
+                    e2 = fmaxf(e2, fminf(v, e1));
+                    a1 = v > e1 ? 16 * b + jj : a1;
+                    e1 = fmaxf(e1, v);
                 }
-                return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
-            };
-            // Runs f(k, l_k) for every component k of the two masks, by 32-component word.
-            // Few per lane: each lane walks its own set.  Many: the warp walks the union of
-            // its lanes' sets one component at a time, so that the parameter reads are
-            // shared by the warp.  The warp-wide choice is made here, where every lane is
-            // present (for_kept itself also runs in lane-divergent code).
-            uint32_t unis[2];
-            bool lanes[2];
-#pragma unroll
-            for (int wd = 0; wd < 2; ++wd) {
-                const uint32_t mk = wd ? xm1 : xm0;
-                unis[wd] = __reduce_or_sync(0xffffffffu, mk);
-                lanes[wd] = 4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(unis[wd]);
             }
-            auto for_kept = [&](auto &&f) {
+            ex0[hf * kPK + i] = e1;
+            ex2[hf * kPK + i] = e2;
+            group_sync(grp);
+            // the row's best m1 and second-best m2: the kept set is {k : l~_k >= m1 - T - 2 delta};
+            // it is {argmax} alone iff m2 falls below that
+            const float o1 = ex0[(1 - hf) * kPK + i], o2 = ex2[(1 - hf) * kPK + i];
+            const float m1 = fmaxf(e1, o1), m2 = fmaxf(fmaxf(e2, o2), fminf(e1, o1));
+            const float keep_from = m1 - kPT - 2.f * delta;
+            const bool single = ok && m2 < keep_from;
+            // single: a posterior of exactly 1 at the argmax (dropped mass < 128 e^-30)
+            if (single && e1 == m1) {
+                if (g_bf16)
+                    *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 64 * hf + a1, kPRows, 2)) =
+                        __float2bfloat16_rn(1.0f);
+                else
+                    *reinterpret_cast<float *>(ob + sw128_offset(i, 64 * hf + a1, kPRows, 4)) = 1.0f;
+            }
+            uint32_t xm0 = 0u, xm1 = 0u;   // the kept components of rows that need the softmax
+            if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
+                uint32_t mk[2] = {0u, 0u};
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float lt[16];
+                    est(b, lt);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        mk[b >> 1] |= (uint32_t)(!ok || lt[jj] >= keep_from) << (16 * (b & 1) + jj);
+                }
+                if (!single) {
+                    xm0 = mk[0];
+                    xm1 = mk[1];
+                }
+            }
+            if (group_or(grp, (xm0 | xm1) != 0u)) {
+                // exact log-joint of a component (parameters from global memory, L2-resident)
+                auto exact = [&](int k) {
+                    const float4 *pk = ph + k * kPStride;
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int dp = 0; dp < kPDP; dp += 2) {
+                        const float4 p = __ldg(pk + dp), r = __ldg(pk + dp + 1);
+                        const float2 y0 = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
+                        acc0 = __ffma2_rn(y0, y0, acc0);
+                        const float2 y1 = __ffma2_rn(xr[dp + 1], make_float2(r.x, r.y), make_float2(r.z, r.w));
+                        acc1 = __ffma2_rn(y1, y1, acc1);
+                    }
+                    return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
+                };
+                // Runs f(k, l_k) for every component k of the two masks, by 32-component word.
+                // Few per lane: each lane walks its own set.  Many: the warp walks the union of
+                // its lanes' sets one component at a time, so that the parameter reads are
+                // shared by the warp.  The warp-wide choice is made here, where every lane is
+                // present (for_kept itself also runs in lane-divergent code).
+                uint32_t unis[2];
+                bool lanes[2];
 #pragma unroll
                 for (int wd = 0; wd < 2; ++wd) {
-                    const int k0 = 64 * hf + 32 * wd;
-                    const uint32_t mk = wd ? xm1 : xm0, uni = unis[wd];
-                    if (lanes[wd]) {
-                        for (uint32_t mm = mk; mm; mm &= mm - 1) {
-                            const int k = k0 + __ffs(mm) - 1;
-                            f(k, exact(k));
-                        }
-                    } else {
-                        for (uint32_t mm = uni; mm; mm &= mm - 1) {
-                            const int kq = __ffs(mm) - 1;
-                            const float l = exact(k0 + kq);
-                            if ((mk >> kq) & 1u) f(k0 + kq, l);
+                    const uint32_t mk = wd ? xm1 : xm0;
+                    unis[wd] = __reduce_or_sync(0xffffffffu, mk);
+                    lanes[wd] = 4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(unis[wd]);
+                }
+                auto for_kept = [&](auto &&f) {
+#pragma unroll
+                    for (int wd = 0; wd < 2; ++wd) {
+                        const int k0 = 64 * hf + 32 * wd;
+                        const uint32_t mk = wd ? xm1 : xm0, uni = unis[wd];
+                        if (lanes[wd]) {
+                            for (uint32_t mm = mk; mm; mm &= mm - 1) {
+                                const int k = k0 + __ffs(mm) - 1;
+                                f(k, exact(k));
+                            }
+                        } else {
+                            for (uint32_t mm = uni; mm; mm &= mm - 1) {
+                                const int kq = __ffs(mm) - 1;
+                                const float l = exact(k0 + kq);
+                                if ((mk >> kq) & 1u) f(k0 + kq, l);
+                            }
                         }
                     }
-                }
-            };
-            // exact pass: online maximum and sum over the kept components of this half;
-            // with an fp32 output tile the log-joints wait in it for the normalisation
-            float mt = -FLT_MAX, st = 0.f;
-            for_kept([&](int k, float l) {
-                if (!g_bf16) *reinterpret_cast<float *>(buf + sw128_offset(i, k, kPRows, 4)) = l;
-                if (l > mt) {
-                    st = st * expf(mt - l) + 1.f;
-                    mt = l;
-                } else {
-                    st += expf(l - mt);
-                }
-            });
-            ex1[hf * kPK + i] = mt;
-            ex2[hf * kPK + i] = st;
-            group_sync(grp);
-            if (xm0 | xm1) {
-                const float q1 = ex1[(1 - hf) * kPK + i], q2 = ex2[(1 - hf) * kPK + i];
-                const float m = fmaxf(mt, q1);
-                const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
-                // the kept posteriors of this half into the output tile
-                if (g_bf16) {
-                    for_kept([&](int k, float l) {
-                        *reinterpret_cast<__nv_bfloat16 *>(buf + sw128_offset(i, k, kPRows, 2)) =
-                            __float2bfloat16_rn(expf(l - m) * inv);
-                    });
-                } else {
+                };
+                // exact pass: online maximum and sum over the kept components of this half;
+                // with an fp32 output tile the log-joints wait in it for the normalisation
+                float mt = -FLT_MAX, st = 0.f;
+                for_kept([&](int k, float l) {
+                    if (!g_bf16) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                    if (l > mt) {
+                        st = st * expf(mt - l) + 1.f;
+                        mt = l;
+                    } else {
+                        st += expf(l - mt);
+                    }
+                });
+                ex1[hf * kPK + i] = mt;
+                ex2[hf * kPK + i] = st;
+                group_sync(grp);
+                if (xm0 | xm1) {
+                    const float q1 = ex1[(1 - hf) * kPK + i], q2 = ex2[(1 - hf) * kPK + i];
+                    const float m = fmaxf(mt, q1);
+                    const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
+                    // the kept posteriors of this half into the output tile
+                    if (g_bf16) {
+                        for_kept([&](int k, float l) {
+                            *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) =
+                                __float2bfloat16_rn(expf(l - m) * inv);
+                        });
+                    } else {
 #pragma unroll
-                    for (int wd = 0; wd < 2; ++wd)
-                        for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
-                            float *o = reinterpret_cast<float *>(
-                                buf + sw128_offset(i, 64 * hf + 32 * wd + __ffs(mm) - 1, kPRows, 4));
-                            *o = expf(*o - m) * inv;
-                        }
+                        for (int wd = 0; wd < 2; ++wd)
+                            for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
+                                float *o = reinterpret_cast<float *>(
+                                    ob + sw128_offset(i, 64 * hf + 32 * wd + __ffs(mm) - 1, kPRows, 4));
+                                *o = expf(*o - m) * inv;
+                            }
+                    }
                 }
             }
-        }
-        fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
-        fence_before_sync();
-        ok = group_and(grp, ok);   // the group leaves the loop together
-        fence_after_sync();
-        if (gt == 0) {
-            for (int a = 0; a < kPK * ge / 128; ++a)
-                tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(buf + a * (kPRows * 128)));
-            bulk_commit();
-            if (it + kPGroups < it1 && ok) {   // the buffer takes the group's next routing tile once read
-                bulk_wait_read();
-                fence_proxy_async();
-                load_x(it + kPGroups);
-                pend_x = true;
-                ph_x = (uint32_t)(nx & 1);
+            fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
+            fence_before_sync();
+            group_sync(grp);
+            fence_after_sync();
+            if (gt == 0) {
+                for (int a = 0; a < kPK * ge / 128; ++a)
+                    tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+                bulk_commit();
             }
         }
+        s0 = s1;
+        ok = __syncthreads_and(ok) != 0;   // both groups leave the loop together
     }
-    // after a failed wait: let the copies still in flight land before the shared memory is released
+    // after a failed wait a routing tile may still be in flight for either group: let it land
+    // (bounded) before the shared memory is released; after a normal end every fetched tile
+    // has been consumed
     if (gt == 0) {
-        if (pend_x) (void)mbar_wait(BAR_X, ph_x);
-        if (pend_i) (void)mbar_wait(BAR_I, ph_i);
+        if (!ok) (void)mbar_wait(BAR_X, (uint32_t)(j & 1));
         bulk_wait_all();
     }
     fence_before_sync();
