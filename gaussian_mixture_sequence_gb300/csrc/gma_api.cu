@@ -13,7 +13,8 @@ using namespace gma;
 namespace {
 
 struct WsPlan {
-    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, wimg = 0, pimg = 0, cimg = 0, bytes = 0;
+    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, pimg = 0, cimg = 0,
+           bytes = 0;
     bool pruned = false;
 };
 
@@ -83,10 +84,15 @@ WsPlan plan(const Dims &dm, gma_op op)
         p.gk = take((size_t)dm.BH() * dm.N * dm.KP * gb);
         p.partial = take((size_t)dm.BH() * dm.nblk() * dm.state_size() * 4);
         if (op == GMA_OP_BIDIR) p.total = take((size_t)dm.BH() * dm.state_size() * 4);
+        if (op == GMA_OP_CAUSAL && tc_path_applies(dm))   // the carried memory in operand form
+            p.mem = take((size_t)dm.BH() * dm.nblk() * dm.state_size() * 4);
     }
     p.bytes = off;
     return p;
 }
+
+// Workspace form of the responsibilities: the fp32 tensor-core path takes split bf16 planes.
+int gamma_layout(const Dims &dm) { return dm.g_bf16 ? GL_BF16 : (tc_path_applies(dm) ? GL_SPLIT : GL_F32); }
 
 bool aligned(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -169,7 +175,7 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     const PrunedImages img = images(ws, wp);
     GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     if (wp.pruned) GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, false, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st));
     return GMA_OK;
 }
 
@@ -239,16 +245,17 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
         GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st));
     if (tc_path_applies(dm)) {
         GMA_CUDA(mk.mark("chunk_state_tc"));
         GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
         GMA_CUDA(mk.mark("state_reduce"));
-        GMA_CUDA(launch_scan(dm, partial, nullptr, total, false, st, true));
+        unsigned char *tot = at<unsigned char>(ws, wp.total);
+        GMA_CUDA(launch_scan_split(dm, partial, nullptr, nullptr, tot, nullptr, st));
         GMA_CUDA(mk.mark("bidir_read_tc"));
-        GMA_CUDA(launch_chunk_out_tc(dm, false, gq, gk, v, total, out, st));
+        GMA_CUDA(launch_chunk_out_tc(dm, false, gq, gk, v, tot, out, st));
     } else {
         GMA_CUDA(mk.mark("block_state"));
         GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
@@ -329,16 +336,17 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
         GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, dm.g_bf16, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st));
     if (tc_path_applies(dm)) {
         GMA_CUDA(mk.mark("chunk_state_tc"));
         GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
         GMA_CUDA(mk.mark("state_scan"));
-        GMA_CUDA(launch_scan(dm, partial, state_in, state_out, true, st));
+        unsigned char *mem = at<unsigned char>(ws, wp.mem);
+        GMA_CUDA(launch_scan_split(dm, partial, state_in, mem, nullptr, state_out, st));
         GMA_CUDA(mk.mark("chunk_out_tc"));
-        GMA_CUDA(launch_chunk_out_tc(dm, true, gq, gk, v, partial, out, st));
+        GMA_CUDA(launch_chunk_out_tc(dm, true, gq, gk, v, mem, out, st));
     } else {
         GMA_CUDA(mk.mark("block_state"));
         GMA_CUDA(launch_block_state(dm, gk, v, partial, st));

@@ -3,8 +3,9 @@
 // Data layout in device memory (all row-major):
 //   routing rows     x[bh][n][d_route]      (fp32 or bf16)
 //   values           v[bh][n][d_v]          (fp32 or bf16)
-//   responsibilities g[bh][n][KP]           (workspace; fp32 or bf16, KP = K rounded up to 8,
-//                                            the padding columns hold zeros)
+//   responsibilities g[bh][n][KP]           (workspace; fp32, bf16 or split, KP = K rounded up
+//                                            to 8, the padding columns hold zeros; split = two
+//                                            bf16 planes, hi then lo, see GLayout)
 //   memory state     s[bh][K*d_v + K]       (Vt as K rows of d_v, then Z)
 //   packed params    prm[h][k][d_route/2]   float4 {s_d, s_d+1, -mu_d s_d, -mu_d+1 s_d+1},
 //                                            s = 1/sigma;  cst[h][k] = log pi_k - 1/2 sum_d log sigma^2
@@ -54,6 +55,18 @@ __device__ __forceinline__ float4 load4(const void *base, long long i, bool bf16
     return *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + i);
 }
 
+// Storage of the responsibilities in the workspace.  GL_SPLIT is the operand
+// form of the fp32 tensor-core path: two bf16 planes hi = RN_bf16(g) and
+// lo = RN_bf16(g - hi) (16 significant bits, |g - hi - lo| <= 2^-17 |g|); an
+// array of R rows x ld holds the hi plane, then the lo plane.
+enum GLayout : int { GL_F32 = 0, GL_BF16 = 1, GL_SPLIT = 2 };
+
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16 &hi, __nv_bfloat16 &lo)
+{
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 __device__ __forceinline__ void store_elem(void *base, long long i, float v, bool bf16)
 {
     if (bf16)
@@ -62,10 +75,26 @@ __device__ __forceinline__ void store_elem(void *base, long long i, float v, boo
         static_cast<float *>(base)[i] = v;
 }
 
+// Element i of a responsibility array of `plane` elements per plane, in `layout`.
+__device__ __forceinline__ void store_g(void *base, long long i, long long plane, float v, int layout)
+{
+    if (layout == GL_F32) {
+        static_cast<float *>(base)[i] = v;
+    } else if (layout == GL_BF16) {
+        static_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+    } else {
+        __nv_bfloat16 hi, lo;
+        split_bf16(v, hi, lo);
+        static_cast<__nv_bfloat16 *>(base)[i] = hi;
+        static_cast<__nv_bfloat16 *>(base)[plane + i] = lo;
+    }
+}
+
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st);
+// gamma: responsibilities in `layout` (GLayout), ldg columns per row
 cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const struct PrunedImages *img,
-                        const void *x, void *gamma, int ldg, bool gamma_bf16, cudaStream_t st);
+                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st);
 cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, float *partial,
                                cudaStream_t st);
 cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total,
@@ -100,14 +129,19 @@ bool resp_pruned_applies(const Dims &dm);
 cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages &img,
                                cudaStream_t st);
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
-                               bool gamma_bf16, cudaStream_t st);
+                               int layout, cudaStream_t st);
 
 // Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
 bool tc_path_eligible(int K, int DV, bool g_bf16);
 bool tc_path_applies(const Dims &dm);
+// Tensor-core path: gq / gk in GL_SPLIT (fp32 products) or GL_BF16 form; the
+// carried memory in operand form (k_scan_split), one block per chunk (causal)
+// or per slice (bidirectional total).
 cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v, float *partial, cudaStream_t st);
+cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float *state_in, unsigned char *mem,
+                              unsigned char *total, float *state_out, cudaStream_t st);
 cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
-                                const float *states, float *out, cudaStream_t st);
+                                const unsigned char *mem, float *out, cudaStream_t st);
 
 // Sets the dynamic shared-memory limit of a kernel once per process.
 template <typename Kern>

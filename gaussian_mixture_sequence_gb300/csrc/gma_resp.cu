@@ -121,7 +121,7 @@ struct RespCfg {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     k_resp(int N, int K, int H, const void *__restrict__ x, bool x_bf16, const float4 *__restrict__ prm,
-           const float *__restrict__ cst, void *__restrict__ gamma, int ldg, bool g_bf16)
+           const float *__restrict__ cst, void *__restrict__ gamma, int ldg, int layout)
 {
     using Cfg = RespCfg<D>;
     constexpr int DP = D / 2, HALVES = Cfg::HALVES, DH = Cfg::DH, RPT = Cfg::RPT, ROWS = Cfg::ROWS,
@@ -234,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 s += e;
             }
             const float inv = 1.0f / warp_sum(s);
-            const long long go = (bh * N + row) * (long long)ldg;
-            for (int k = lane; k < ldg; k += 32) store_elem(gamma, go + k, k < K ? er[k] * inv : 0.f, g_bf16);
+            const long long go = (bh * N + row) * (long long)ldg, plane = (long long)gridDim.y * N * ldg;
+            for (int k = lane; k < ldg; k += 32) store_g(gamma, go + k, plane, k < K ? er[k] * inv : 0.f, layout);
         }
         __syncthreads();
     }
@@ -243,14 +243,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D>
 cudaError_t launch_resp_d(const Dims &dm, const float4 *prm, const float *cst, const void *x, void *gamma,
-                          int ldg, bool gamma_bf16, cudaStream_t st)
+                          int ldg, int layout, cudaStream_t st)
 {
     using Cfg = RespCfg<D>;
     const size_t smem = Cfg::smem(dm.K);
     static cudaError_t attr = allow_smem(k_resp<D>, Cfg::smem(512));
     if (attr != cudaSuccess) return attr;
     dim3 grid((dm.N + Cfg::ROWS_PER_CTA - 1) / Cfg::ROWS_PER_CTA, (unsigned)dm.BH());
-    k_resp<D><<<grid, kThreads, smem, st>>>(dm.N, dm.K, dm.H, x, dm.x_bf16, prm, cst, gamma, ldg, gamma_bf16);
+    k_resp<D><<<grid, kThreads, smem, st>>>(dm.N, dm.K, dm.H, x, dm.x_bf16, prm, cst, gamma, ldg, layout);
     return cudaGetLastError();
 }
 
@@ -264,14 +264,14 @@ cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float 
 }
 
 cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages *img,
-                        const void *x, void *gamma, int ldg, bool gamma_bf16, cudaStream_t st)
+                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st)
 {
-    if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, gamma_bf16, st);
+    if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, layout, st);
     switch (dm.D) {
-    case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
-    case 32: return launch_resp_d<32>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
-    case 64: return launch_resp_d<64>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
-    case 128: return launch_resp_d<128>(dm, prm, cst, x, gamma, ldg, gamma_bf16, st);
+    case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, layout, st);
+    case 32: return launch_resp_d<32>(dm, prm, cst, x, gamma, ldg, layout, st);
+    case 64: return launch_resp_d<64>(dm, prm, cst, x, gamma, ldg, layout, st);
+    case 128: return launch_resp_d<128>(dm, prm, cst, x, gamma, ldg, layout, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
 // the items s + g, s + g + 2, ...  The output tile is assembled in shared memory
 // and written by TMA stores that stop at the slice's last row.
 __global__ void __launch_bounds__(kPThreads, 1)
-    k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap, int N, int H,
-                  int BH, bool x_bf16, const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
-                  const float *__restrict__ cimg, bool g_bf16)
+    k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
+                  const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int BH, bool x_bf16,
+                  const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
+                  const float *__restrict__ cimg, int layout)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -187,7 +188,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const long long it0 = (long long)blockIdx.x * per;
     const long long it1 = it0 + per < items ? it0 + per : items;
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
-    const int ge = g_bf16 ? 2 : 4;
+    const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
+    const int ge = g_f32 ? 4 : 2;
+    constexpr uint32_t LO = kPRows * kPK * 2;   // split: the lo plane's tile follows the hi plane's
 
     // one thread: TMA of item it's rows, counted on the barrier of the group that takes it
     // (group 0 takes a slice's first item in the range, then the groups alternate)
@@ -297,10 +300,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             __syncwarp();
             // while the tensor core works: this half of the output row starts as zeros
-            if (g_bf16) {
+            if (!g_f32) {
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    *reinterpret_cast<uint4 *>(ob + sw128_offset(i, 64 * hf + 8 * g, kPRows, 2)) = make_uint4(0, 0, 0, 0);
+                for (int g = 0; g < 8; ++g) {
+                    const uint32_t off = sw128_offset(i, 64 * hf + 8 * g, kPRows, 2);
+                    *reinterpret_cast<uint4 *>(ob + off) = make_uint4(0, 0, 0, 0);
+                    if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(0, 0, 0, 0);
+                }
             } else {
 #pragma unroll
                 for (int g = 0; g < 16; ++g)
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const bool single = ok && m2 < keep_from;
             // single: a posterior of exactly 1 at the argmax (dropped mass < 128 e^-30)
             if (single && e1 == m1) {
-                if (g_bf16)
+                if (!g_f32)   // split: hi = 1, lo = 0
                     *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, 64 * hf + a1, kPRows, 2)) =
                         __float2bfloat16_rn(1.0f);
                 else
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // with an fp32 output tile the log-joints wait in it for the normalisation
                 float mt = -FLT_MAX, st = 0.f;
                 for_kept([&](int k, float l) {
-                    if (!g_bf16) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                    if (g_f32) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
                     if (l > mt) {
                         st = st * expf(mt - l) + 1.f;
                         mt = l;
@@ -440,10 +446,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const float m = fmaxf(mt, q1);
                     const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
                     // the kept posteriors of this half into the output tile
-                    if (g_bf16) {
+                    if (!g_f32) {
                         for_kept([&](int k, float l) {
-                            *reinterpret_cast<__nv_bfloat16 *>(ob + sw128_offset(i, k, kPRows, 2)) =
-                                __float2bfloat16_rn(expf(l - m) * inv);
+                            __nv_bfloat16 hi, lo;
+                            split_bf16(expf(l - m) * inv, hi, lo);
+                            const uint32_t off = sw128_offset(i, k, kPRows, 2);
+                            *reinterpret_cast<__nv_bfloat16 *>(ob + off) = hi;
+                            if (g_split) *reinterpret_cast<__nv_bfloat16 *>(ob + LO + off) = lo;
                         });
                     } else {
 #pragma unroll
@@ -461,8 +470,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             group_sync(grp);
             fence_after_sync();
             if (gt == 0) {
-                for (int a = 0; a < kPK * ge / 128; ++a)
+                for (int a = 0; a < kPK * ge / 128; ++a) {
                     tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+                    if (g_split)
+                        tma_store_3d(&gmap_lo, a * (128 / ge), t * kPRows, bh, smem_addr(ob + LO + a * (kPRows * 128)));
+                }
                 bulk_commit();
             }
         }
@@ -493,20 +505,28 @@ cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *c
 }
 
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
-                               bool gamma_bf16, cudaStream_t st)
+                               int layout, cudaStream_t st)
 {
     constexpr size_t smem = PrunedSmem::bytes;
     static cudaError_t attr = allow_smem(k_resp_pruned, smem);
     if (attr != cudaSuccess) return attr;
     if (ldg != kPK) return cudaErrorInvalidValue;
-    CUtensorMap xmap, gmap;
+    CUtensorMap xmap, gmap, gmap_lo;
+    const bool g16 = layout != GL_F32;
+    const long long plane = dm.BH() * dm.N * (long long)kPK;   // elements per plane (split)
     if (!make_tma_3d(&xmap, x, dm.x_bf16, kPD, dm.N, dm.BH(), kPRows) ||
-        !make_tma_3d(&gmap, gamma, gamma_bf16, kPK, dm.N, dm.BH(), kPRows))
+        !make_tma_3d(&gmap, gamma, g16, kPK, dm.N, dm.BH(), kPRows))
         return cudaErrorInvalidValue;
+    if (layout == GL_SPLIT) {
+        if (!make_tma_3d(&gmap_lo, static_cast<__nv_bfloat16 *>(gamma) + plane, true, kPK, dm.N, dm.BH(), kPRows))
+            return cudaErrorInvalidValue;
+    } else {
+        gmap_lo = gmap;
+    }
     const long long items = dm.BH() * ((dm.N + kPRows - 1) / kPRows);
     const int grid = (int)(items < sm_count() ? items : sm_count());
-    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, dm.N, dm.H, (int)dm.BH(), dm.x_bf16, img.w, img.p, img.c,
-                                                 gamma_bf16);
+    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, (int)dm.BH(), dm.x_bf16, img.w,
+                                                 img.p, img.c, layout);
     return cudaGetLastError();
 }
 
