@@ -108,12 +108,12 @@ def stage_work(stage, wl):
         pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
         return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
     if stage in ("block_state", "chunk_state_tc"):
-        return 2.0 * K * (dv + 1) * ht, ("tensor" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
+        return 2.0 * K * (dv + 1) * ht, ("tensor_bf16" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
     if stage in ("chunk_out", "chunk_out_tc"):
         fl = 2.0 * C * K + C * (dv + 1) + 2.0 * K * (dv + 1) + (0 if tc else 2.0 * K * (dv + 1))
-        return fl * ht, ("tensor" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
+        return fl * ht, ("tensor_bf16" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
     if stage in ("bidir_read", "bidir_read_tc"):
-        return 2.0 * K * (dv + 1) * ht, ("tensor" if tc else "alu"), (K * gb + 4 * dv) * ht + st * wl.B * wl.H
+        return 2.0 * K * (dv + 1) * ht, ("tensor_bf16" if tc else "alu"), (K * gb + 4 * dv) * ht + st * wl.B * wl.H
     if stage in ("state_scan", "state_reduce"):
         return 0.0, "alu", 2.0 * st * nblk
     return 0.0, "alu", 0.0
@@ -265,6 +265,8 @@ def source_hash(stage, wl):
     src = KERNEL_SOURCE.get(stage)
     if src is None:  # routing: the pruned kernel where it applies, else the generic one
         src = "gma_resp_tc.cu" if bounded_routing(wl) else "gma_resp.cu"
+    if stage in ("state_scan", "state_reduce") and eff_chunk(wl) == 128:   # the tensor-core path's scan
+        src = "gma_causal_tc.cu"
     m = hashlib.sha256()
     for fn in ("gma_internal.cuh", "gma_tc.cuh", src):
         m.update(open(os.path.join(d, fn), "rb").read())
