@@ -7,6 +7,7 @@ generator (:mod:`.workloads`) can be imported on machines without a GPU.
 """
 _BINDING_NAMES = (
     "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
+    "gma_forward_causal_host", "gma_forward_bidir_profiled", "gma_decode_step_profiled",
     "gma_workspace_size", "gma_status_string", "gma_forward_causal_profiled", "Profile", "gma_decode_step_noalloc", "Shape", "GMAError", "library_path", "load",
 )
 

@@ -129,6 +129,26 @@ gma_status check_ws(void *ws, size_t ws_bytes, const WsPlan &wp)
 template <typename T>
 T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
 
+// Device copies of the inputs and the output for gma_forward_causal_host.
+struct HostStaging {
+    size_t q = 0, k = 0, v = 0, out = 0, bytes = 0;
+};
+HostStaging host_staging(const Dims &dm)
+{
+    HostStaging h;
+    const size_t rows = (size_t)dm.BH() * dm.N;
+    auto take = [&](size_t n) {
+        const size_t o = h.bytes;
+        h.bytes = (size_t)round_up((long long)(h.bytes + n), 256);
+        return o;
+    };
+    h.q = take(rows * dm.D * (dm.x_bf16 ? 2 : 4));
+    h.k = take(rows * dm.D * (dm.x_bf16 ? 2 : 4));
+    h.v = take(rows * dm.DV * (dm.v_bf16 ? 2 : 4));
+    h.out = take(rows * dm.DV * 4);
+    return h;
+}
+
 PrunedImages images(void *ws, const WsPlan &wp)
 {
     return PrunedImages{at<unsigned char>(ws, wp.wimg), at<float4>(ws, wp.pimg), at<float>(ws, wp.cimg)};
@@ -141,6 +161,10 @@ extern "C" {
 size_t gma_workspace_size(const gma_shape *shape, gma_op op)
 {
     Dims dm;
+    if (op == GMA_OP_CAUSAL_HOST) {
+        if (make_dims(shape, &dm, GMA_OP_CAUSAL) != GMA_OK) return 0;
+        return host_staging(dm).bytes + plan(dm, GMA_OP_CAUSAL).bytes;
+    }
     if ((unsigned)op > 3u || make_dims(shape, &dm, op) != GMA_OK) return 0;
     return plan(dm, op).bytes;
 }
@@ -410,6 +434,104 @@ gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params
 
 
 } // extern "C"
+
+// ---- causal forward on host buffers ----------------------------------------
+namespace {
+
+constexpr int kMaxCopyDevices = 64;
+std::once_flag g_copy_once[kMaxCopyDevices];
+cudaStream_t g_copy_in[kMaxCopyDevices], g_copy_out[kMaxCopyDevices];
+cudaError_t g_copy_err[kMaxCopyDevices];
+
+// The two copy streams of the current device (created once, never destroyed).
+gma_status copy_streams(cudaStream_t *in, cudaStream_t *out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxCopyDevices) return GMA_ERR_UNSUPPORTED;
+    std::call_once(g_copy_once[dev], [dev] {
+        g_copy_err[dev] = cudaStreamCreateWithFlags(&g_copy_in[dev], cudaStreamNonBlocking);
+        if (g_copy_err[dev] == cudaSuccess)
+            g_copy_err[dev] = cudaStreamCreateWithFlags(&g_copy_out[dev], cudaStreamNonBlocking);
+    });
+    if (g_copy_err[dev] != cudaSuccess) return GMA_ERR_CUDA;
+    *in = g_copy_in[dev];
+    *out = g_copy_out[dev];
+    return GMA_OK;
+}
+
+// Records an event on `from` and makes `to` wait for it.
+cudaError_t join(cudaStream_t to, cudaStream_t from)
+{
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (err != cudaSuccess) return err;
+    err = cudaEventRecord(e, from);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(to, e, 0);
+    cudaEventDestroy(e);   // released once the recorded work completes
+    return err;
+}
+
+} // namespace
+
+extern "C" gma_status gma_forward_causal_host(const gma_shape *shape, gma_params params, const void *qx,
+                                              const void *kx, const void *v, const float *state_in,
+                                              float *state_out, float *out, void *ws, size_t ws_bytes,
+                                              gma_stream_t stream)
+{
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm));
+    GMA_TRY(check_params(params));
+    if (dm.N > 0 && (!qx || !kx || !v || !out)) return GMA_ERR_INVALID_ARG;
+    GMA_TRY(check_ptr(state_in, false));
+    GMA_TRY(check_ptr(state_out, false));
+    const HostStaging hs = host_staging(dm);
+    const WsPlan wp = plan(dm, GMA_OP_CAUSAL);
+    if (!ws || ws_bytes < hs.bytes + wp.bytes) return GMA_ERR_WORKSPACE;
+    if (!aligned(ws)) return GMA_ERR_ALIGNMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char *w = static_cast<char *>(ws);
+    char *cws = w + hs.bytes;
+    const size_t cws_bytes = ws_bytes - hs.bytes;
+    if (dm.N == 0)
+        return run_causal(shape, params, nullptr, nullptr, nullptr, state_in, state_out, nullptr, cws, cws_bytes,
+                          stream, nullptr);
+    cudaStream_t cin, cout_;
+    GMA_TRY(copy_streams(&cin, &cout_));
+    // groups of slices: one batch entry and a range of heads, about eight groups in all
+    const int split = dm.B >= 8 ? 1 : (8 + dm.B - 1) / dm.B;
+    const int hg = (dm.H + split - 1) / split;
+    const size_t xe = dm.x_bf16 ? 2 : 4, ve = dm.v_bf16 ? 2 : 4;
+    const size_t xrow = (size_t)dm.N * dm.D * xe, vrow = (size_t)dm.N * dm.DV * ve, orow = (size_t)dm.N * dm.DV * 4;
+    const long long SZ = dm.state_size();
+    // the staging buffers may still be read by earlier work on `stream`
+    GMA_CUDA(join(cin, st));
+    for (int b = 0; b < dm.B; ++b)
+        for (int h0 = 0; h0 < dm.H; h0 += hg) {
+            const int hn = dm.H - h0 < hg ? dm.H - h0 : hg;
+            const size_t s0 = (size_t)b * dm.H + h0;   // first slice of the group
+            GMA_CUDA(cudaMemcpyAsync(w + hs.q + s0 * xrow, static_cast<const char *>(qx) + s0 * xrow, hn * xrow,
+                                     cudaMemcpyHostToDevice, cin));
+            GMA_CUDA(cudaMemcpyAsync(w + hs.k + s0 * xrow, static_cast<const char *>(kx) + s0 * xrow, hn * xrow,
+                                     cudaMemcpyHostToDevice, cin));
+            GMA_CUDA(cudaMemcpyAsync(w + hs.v + s0 * vrow, static_cast<const char *>(v) + s0 * vrow, hn * vrow,
+                                     cudaMemcpyHostToDevice, cin));
+            GMA_CUDA(join(st, cin));
+            gma_shape sg = *shape;
+            sg.B = 1;
+            sg.H = hn;
+            const gma_params pg{params.mu + (size_t)h0 * dm.K * dm.D, params.var_raw + (size_t)h0 * dm.K * dm.D,
+                                params.logit_pi + (size_t)h0 * dm.K};
+            GMA_TRY(run_causal(&sg, pg, w + hs.q + s0 * xrow, w + hs.k + s0 * xrow, w + hs.v + s0 * vrow,
+                               state_in ? state_in + s0 * SZ : nullptr, state_out ? state_out + s0 * SZ : nullptr,
+                               reinterpret_cast<float *>(w + hs.out + s0 * orow), cws, cws_bytes, stream, nullptr));
+            GMA_CUDA(join(cout_, st));
+            GMA_CUDA(cudaMemcpyAsync(reinterpret_cast<char *>(out) + s0 * orow, w + hs.out + s0 * orow, hn * orow,
+                                     cudaMemcpyDeviceToHost, cout_));
+        }
+    GMA_CUDA(join(st, cout_));   // `stream` completes after the last output copy
+    return GMA_OK;
+}
 
 // ---- decode step whose scratch is a file-scope device array ----------------
 namespace {

@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "libgma.so")
 _lib = None
 
 F32, BF16 = 0, 1
-OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_DECODE = 0, 1, 2, 3
+OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_DECODE, OP_CAUSAL_HOST = 0, 1, 2, 3, 4
 _DT = {"f32": F32, "bf16": BF16, torch.float32: F32, torch.bfloat16: BF16}
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -80,6 +80,7 @@ def load():
         lib.gma_responsibilities.argtypes = [S, _Params, P, P, P, ctypes.c_size_t, P]
         lib.gma_forward_bidir.argtypes = [S, _Params, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_forward_causal.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.gma_forward_causal_host.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_decode_step.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_decode_step_noalloc.argtypes = [S, _Params, P, P, P, P, P, P]
         lib.gma_forward_causal_profiled.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P,
@@ -89,7 +90,7 @@ def load():
         lib.gma_decode_step_profiled.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P,
                                                  ctypes.POINTER(Profile)]
         for fn in ("gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
-                   "gma_forward_causal_profiled", "gma_decode_step_noalloc",
+                   "gma_forward_causal_host", "gma_forward_causal_profiled", "gma_decode_step_noalloc",
                    "gma_forward_bidir_profiled", "gma_decode_step_profiled"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
@@ -193,6 +194,40 @@ def gma_forward_causal(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, out, stat
     wp, wn = _ws(s, OP_CAUSAL, ws, dev)
     _check("gma_forward_causal",
            load().gma_forward_causal(ctypes.byref(s), prm, q, k, vv, si, so, o, wp, wn, _stream(dev, stream)))
+    return out
+
+
+def _host_ptr(t, name, shape, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def gma_forward_causal_host(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, out, state_in=None,
+                            state_out=None, ws=None, stream=None):
+    """gma_forward_causal on host tensors qx, kx, v, out (page-locked for asynchronous copies);
+    the library copies in and out itself, overlapping the copies with the computation.
+    Parameters and the optional states are device tensors.  Returns after enqueueing."""
+    dev = mu.device
+    s = shape
+    xdt, vdt = _TORCH_DT[s.x_dtype], _TORCH_DT[s.v_dtype]
+    q = _host_ptr(qx, "qx", (s.B, s.H, s.N, s.d_route), xdt)
+    k = _host_ptr(kx, "kx", (s.B, s.H, s.N, s.d_route), xdt)
+    vv = _host_ptr(v, "v", (s.B, s.H, s.N, s.d_v), vdt)
+    o = _host_ptr(out, "out", (s.B, s.H, s.N, s.d_v), torch.float32)
+    sshape = (s.B, s.H, s.K * s.d_v + s.K)
+    si = _ptr(state_in, "state_in", sshape, torch.float32, dev, optional=True)
+    so = _ptr(state_out, "state_out", sshape, torch.float32, dev, optional=True)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    wp, wn = _ws(s, OP_CAUSAL_HOST, ws, dev)
+    _check("gma_forward_causal_host",
+           load().gma_forward_causal_host(ctypes.byref(s), prm, q, k, vv, si, so, o, wp, wn, _stream(dev, stream)))
     return out
 
 

@@ -68,7 +68,8 @@ typedef enum {
     GMA_OP_RESPONSIBILITIES = 0,
     GMA_OP_BIDIR = 1,
     GMA_OP_CAUSAL = 2,
-    GMA_OP_DECODE = 3
+    GMA_OP_DECODE = 3,
+    GMA_OP_CAUSAL_HOST = 4   /* gma_forward_causal_host: staging + the causal workspace */
 } gma_op;
 
 typedef struct {
@@ -126,6 +127,25 @@ gma_status gma_forward_causal(const gma_shape *shape, gma_params params, const v
                               const void *kx, const void *v, const float *state_in,
                               float *state_out, float *out, void *ws, size_t ws_bytes,
                               gma_stream_t stream);
+
+/* Causal forward on HOST buffers: the library copies the inputs in and the
+ * output out itself, in groups of (batch, head) slices, so that the copies of
+ * one group overlap the computation of another (slices are independent in
+ * the method).  Same arithmetic and results as gma_forward_causal.
+ *   qx, kx, v   host [B, H, N, ...] as gma_forward_causal (page-locked memory
+ *               gives asynchronous copies; pageable memory works, slower)
+ *   out         host [B, H, N, d_v] fp32
+ *   state_in, state_out   device, as gma_forward_causal
+ *   ws          device scratch of gma_workspace_size(shape, GMA_OP_CAUSAL_HOST)
+ *               bytes: device copies of the inputs and the output, then the
+ *               causal workspace.
+ * The call enqueues its work after everything already on `stream` and returns;
+ * the output is on the host once `stream` has completed.  The copies run on
+ * two internal streams joined to `stream` by events.                       */
+gma_status gma_forward_causal_host(const gma_shape *shape, gma_params params, const void *qx,
+                                   const void *kx, const void *v, const float *state_in,
+                                   float *state_out, float *out, void *ws, size_t ws_bytes,
+                                   gma_stream_t stream);
 
 /* One recurrent decode step (the causal form advanced by one token; constant
  * memory per head as in "선형 어텐션 원리 정리"): the token is written into the

@@ -12,7 +12,8 @@ import pytest
 import torch
 
 from gaussian_mixture_sequence_gb300 import workloads
-from gpu_cases import TOL, Case, normwise
+from gpu_cases import DEV, TOL, Case, normwise, shape_of
+import gaussian_mixture_sequence_gb300 as gma
 
 pytestmark = pytest.mark.gpu
 W = workloads.WORKLOADS
@@ -247,3 +248,22 @@ def test_decode_after_prefill(wl, sample):
                                                heads=c.heads)
     _report(f"decode {wl.name} B={wl.B}", normwise(c.pick(outs), ref), TOL["f32"])
     _report(f"decode state {wl.name}", normwise(c.pick(final), ref_st), TOL["f32"])
+
+
+# ------------------------------------------------- host-buffer causal entry ----
+
+@pytest.mark.parametrize("wl", [W["causal_16k_peaked"].with_(H=5, N=3000), W["tiny"].with_(B=3, H=2, N=300, K=128, d=64, dv=64),
+                                W["tiny"].with_(B=2, H=3, N=257, K=40, d=32, dv=32)])
+def test_causal_host_entry_matches_device_entry(wl):
+    """The host-buffer entry copies in groups of slices and overlaps copies with compute:
+    its output and final state equal the device entry's bit for bit (slices are independent)."""
+    c = Case(wl)
+    out_dev, st_dev = c.causal(want_state=True)
+    q, k, v = (t.cpu().pin_memory() for t in c.dev["seq"])
+    out_host = torch.empty(wl.B, wl.H, wl.N, wl.dv).pin_memory()
+    st = torch.empty(wl.B, wl.H, wl.K * wl.dv + wl.K, device=DEV)
+    gma.gma_forward_causal_host(shape_of(wl), *c.prm, q, k, v, out_host, state_out=st)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, out_dev.cpu())
+    assert torch.equal(st, st_dev)
+    _report(f"causal host entry {wl.name}", normwise(c.pick(out_host), c.ref_causal()), TOL[wl.gemm_dtype])
