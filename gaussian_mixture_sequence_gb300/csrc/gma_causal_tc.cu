@@ -113,136 +113,193 @@ __device__ __forceinline__ void put_split(unsigned char *hi, unsigned char *lo, 
 
 // ------------------------------------------------------------------------
 // L_c = Gamma_K,c^T [V_c | 1]: M = components, N = d_v, contraction over the
-// chunk's 128 tokens.  The Gamma_K planes of the chunk land by TMA; A =
-// Gamma_K^T goes to TMEM: warp w owns components 32 (w % 4) + lane and tokens
-// [64 (w / 4), +64), read across the landing rows (conflict-free: a warp reads
-// 64 contiguous bytes of one row).  B = V^T in shared memory (split by
-// threads).  Two CTAs share an SM.  The block is written transposed: d_v rows
-// of K, then Z as row d_v.
+// chunk's 128 tokens.  Persistent: CTA b takes the chunks [b * per, (b + 1) *
+// per) of the list (slice, chunk) in order.  The chunk's Gamma_K planes and V
+// land by TMA; A = Gamma_K^T goes to TMEM: warp w owns components
+// 32 (w % 4) + lane and tokens [32 (w / 4), +32), read across the landing rows
+// (a warp reads 64 contiguous bytes of one row); B = V^T is split by threads
+// into its images.  Once the landing tiles have been read, the next chunk's are
+// fetched; the MMA of chunk c runs while the threads write out chunk c - 1
+// from the other of two accumulator buffers.  The block is written transposed:
+// d_v rows of K, then Z as row d_v.
+constexpr int kStateThreads = 512;
+
 template <bool SPLIT, int DV>
 struct StateSmem {
     static constexpr uint32_t G = kC * kRowB;    // one Gamma_K plane tile (128 tokens x 128 components)
+    static constexpr uint32_t VL = kC * DV * 4;  // V landing tile (fp32 worst case)
     static constexpr uint32_t VT = DV * kRowB;   // one V^T image: d_v rows of 128 tokens
-    static constexpr size_t bytes = 1024 + 2 * (size_t)G + 2 * (size_t)VT + 2 * kK * 4 + 64;
+    static constexpr size_t bytes = 1024 + 2 * (size_t)G + VL + 2 * (size_t)VT + 2 * 4 * kK * 4 + 64;
 };
 
 struct StateMaps {
-    CUtensorMap gk[2];   // hi / lo planes
+    CUtensorMap gk[2], v;   // Gamma_K hi / lo planes; V
 };
 
 template <bool SPLIT, int DV>
-__global__ void __launch_bounds__(256, 2)
-    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, const void *__restrict__ v, bool v_bf16,
-                     float *__restrict__ partial, int nblk)
+__global__ void __launch_bounds__(kStateThreads, 1)
+    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items, bool v_bf16,
+                     float *__restrict__ partial)
 {
     using Sm = StateSmem<SPLIT, DV>;
+    constexpr int NP = SPLIT ? 2 : 1;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *gl = sm;                                         // Gamma_K planes (hi, lo)
-    unsigned char *vt_hi = sm + 2 * Sm::G, *vt_lo = vt_hi + Sm::VT;
-    float *zp = reinterpret_cast<float *>(vt_lo + Sm::VT);          // [2][128] partial Z
-    uint64_t *bar = reinterpret_cast<uint64_t *>(zp + 2 * kK);      // landing, MMA
+    unsigned char *vl = sm + 2 * Sm::G;                             // V landing tile
+    unsigned char *vt_hi = vl + Sm::VL, *vt_lo = vt_hi + Sm::VT;    // V^T images
+    float *zp = reinterpret_cast<float *>(vt_lo + Sm::VT);          // [2][4][128] token-group sums of Gamma_K
+    uint64_t *bar = reinterpret_cast<uint64_t *>(zp + 2 * 4 * kK);  // landing, MMA
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    const uint32_t BAR_L = smem_addr(bar), BAR_M = smem_addr(bar + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = warp >> 2;
+    const int tg = warp >> 2;                   // token group of A, column group of D
     const uint32_t lane0 = 32 * (warp & 3);
-    const int k = lane0 + lane;
-    const long long bh = blockIdx.y;
-    const int c0 = blockIdx.x * kC;
-    const int nr = min(kC, N - c0);
-    constexpr int NP = SPLIT ? 2 : 1;
-    constexpr uint32_t A_HI = 0, A_LO = 64, D_COL = 128;
+    const int k = lane0 + lane;                 // component (TMEM lane)
+    const long long per = (items + gridDim.x - 1) / gridDim.x;
+    const long long it0 = (long long)blockIdx.x * per;
+    const long long it1 = it0 + per < items ? it0 + per : items;
+    constexpr uint32_t A_HI = 0, A_LO = 64, D0 = 128;
+    const int ev = v_bf16 ? 2 : 4;
+    const long long SZ = (long long)kK * DV + kK;
+    const float qnan = __int_as_float(0x7fc00000);
 
-    if (warp == 0) {
-        tmem_alloc(smem_addr(tslot), 256);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(smem_addr(bar), 1);
-        mbar_init(smem_addr(bar + 1), 1);
-        mbar_init_fence();
-        const int row0 = (int)(bh * N + c0);
-        mbar_expect_tx(smem_addr(bar), (uint32_t)(NP * Sm::G));
+    auto load = [&](long long it) {   // one thread: the chunk's Gamma_K planes and V
+        const int row0 = (int)((it / nblk) * N + (it % nblk) * kC);
+        mbar_expect_tx(BAR_L, (uint32_t)(NP * Sm::G + kC * DV * ev));
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a)
-                tma_load_2d(smem_addr(gl + pl * Sm::G + a * kAtom), &maps.gk[pl], a * 64, row0, smem_addr(bar));
+                tma_load_2d(smem_addr(gl + pl * Sm::G + a * kAtom), &maps.gk[pl], a * 64, row0, BAR_L);
+        for (int a = 0; a < DV * ev / 128; ++a)
+            tma_load_2d(smem_addr(vl + a * kAtom), &maps.v, a * (128 / ev), row0, BAR_L);
+    };
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tslot), 512);
+        tmem_relinquish();
     }
-    // B = V^T (element (c, j)) of the chunk, split; lanes run over tokens
-    {
-        constexpr int PER = (kC * DV / 4) / 256;
-        float4 t[PER];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int f = tid + u * 256, j = f % kC, c4 = f / kC;
-            t[u] = j < nr ? load4(v, (bh * N + c0 + j) * DV + 4 * c4, v_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int f = tid + u * 256, j = f % kC, c4 = 4 * (f / kC);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 0, j, DV, 2), t[u].x);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 1, j, DV, 2), t[u].y);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 2, j, DV, 2), t[u].z);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 3, j, DV, 2), t[u].w);
+    bool pend_l = false;   // a landing in flight that the loop has not waited for (thread 0's record)
+    uint32_t ph_l = 0;
+    if (tid == 0) {
+        mbar_init(BAR_L, 1);
+        mbar_init(BAR_M, 1);
+        mbar_init_fence();
+        if (it0 < it1) {
+            load(it0);
+            pend_l = true;
         }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    bool ok = mbar_wait(smem_addr(bar), 0);
-    // A = Gamma_K^T: this thread's 64 tokens of component k, plane by plane; their sum for Z
-    float z = 0.f;
+    bool ok = true;
+    int nm = 0;   // MMA chains committed
+    // L of chunk it from accumulator buffer db (and Z from zp[db]) into its block
+    auto take = [&](long long it, int db, bool okv) {
+        float *o = partial + it * SZ;
 #pragma unroll
-    for (int pl = 0; pl < NP; ++pl) {
-        const uint16_t *gp = reinterpret_cast<const uint16_t *>(gl + pl * Sm::G);
-        uint32_t p[2][16];
+        for (int cb = 0; cb < DV / 64; ++cb) {
+            const int c = tg * (DV / 4) + 16 * cb;
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, lane0, D0 + db * DV + c), r);
+            tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j0 = 64 * h + 2 * jj;
-            const uint32_t a = j0 < nr ? (uint32_t)gp[sw128_offset(j0, k, kC, 2) / 2] : 0u;
-            const uint32_t b = j0 + 1 < nr ? (uint32_t)gp[sw128_offset(j0 + 1, k, kC, 2) / 2] : 0u;
-            z += bf(a) + bf(b);
-            p[jj >> 4][jj & 15] = a | (b << 16);
+            for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = okv ? __uint_as_float(r[q]) : qnan;
         }
-        const uint32_t col = (pl ? A_LO : A_HI) + 32 * h;
-        tmem_st16(tmem_at(tbase, lane0, col), p[0]);
-        tmem_st16(tmem_at(tbase, lane0, col + 16), p[1]);
+        if (tg == 0) {
+            const float *z = zp + db * 4 * kK;
+            o[(long long)kK * DV + k] = okv ? (z[k] + z[kK + k]) + (z[2 * kK + k] + z[3 * kK + k]) : qnan;
+        }
+    };
+
+
+    for (long long it = it0; it < it1 && ok; ++it) {
+        const int j = (int)(it - it0), db = j & 1;
+        const int nr = min(kC, N - (int)(it % nblk) * kC);
+        const bool ok_l = mbar_wait(BAR_L, (uint32_t)(j & 1));
+        if (tid == 0) pend_l = pend_l && !ok_l;
+        ok = ok && ok_l;
+        if (j > 0) {   // A and the V^T images are free once the previous chunk's MMA is done
+            ok = mbar_wait(BAR_M, (uint32_t)((nm - 1) & 1)) && ok;
+            fence_after_sync();
+        }
+        // A = Gamma_K^T: this thread's 32 tokens of component k, plane by plane; their sum for Z
+        float z = 0.f;
+#pragma unroll
+        for (int pl = 0; pl < NP; ++pl) {
+            const uint16_t *gp = reinterpret_cast<const uint16_t *>(gl + pl * Sm::G);
+            uint32_t p[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j0 = 32 * tg + 2 * jj;
+                const uint32_t a = j0 < nr ? (uint32_t)gp[sw128_offset(j0, k, kC, 2) / 2] : 0u;
+                const uint32_t b = j0 + 1 < nr ? (uint32_t)gp[sw128_offset(j0 + 1, k, kC, 2) / 2] : 0u;
+                z += bf(a) + bf(b);
+                p[jj] = a | (b << 16);
+            }
+            tmem_st16(tmem_at(tbase, lane0, (pl ? A_LO : A_HI) + 16 * tg), p);
+        }
+        zp[(db * 4 + tg) * kK + k] = z;
+        // B = V^T (element (c, j)) from the landing tile, split; lanes run over tokens
+        constexpr int VPER = kC * DV / 4 / kStateThreads;
+#pragma unroll
+        for (int u = 0; u < VPER; ++u) {
+            const int f = tid + u * kStateThreads, jt = f % kC, c4 = 4 * (f / kC);
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (jt < nr) {
+                if (v_bf16) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(vl + sw128_offset(jt, c4, kC, 2));
+                    t = make_float4(bf(w.x & 0xffffu), __uint_as_float(w.x & 0xffff0000u), bf(w.y & 0xffffu),
+                                    __uint_as_float(w.y & 0xffff0000u));
+                } else {
+                    t = *reinterpret_cast<const float4 *>(vl + sw128_offset(jt, c4, kC, 4));
+                }
+            }
+            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 0, jt, DV, 2), t.x);
+            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 1, jt, DV, 2), t.y);
+            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 2, jt, DV, 2), t.z);
+            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 3, jt, DV, 2), t.w);
+        }
+        tmem_wait_st();
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();   // the landing tiles have been read; A and V^T are in place
+        fence_after_sync();
+        if (tid == 0) {
+            if (it + 1 < it1 && ok) {
+                fence_proxy_async();
+                load(it + 1);
+                pend_l = true;
+                ph_l = (uint32_t)((j + 1) & 1);
+            }
+            const uint32_t d = tbase + D0 + db * DV;
+            mma_pass_ts(d, tbase + A_HI, vt_hi, DV, DV * 128, false);
+            if constexpr (SPLIT) {
+                mma_pass_ts(d, tbase + A_HI, vt_lo, DV, DV * 128, true);
+                mma_pass_ts(d, tbase + A_LO, vt_hi, DV, DV * 128, true);
+            }
+            mma_commit(BAR_M);
+        }
+        __syncwarp();
+        ++nm;
+        if (j > 0) take(it - 1, db ^ 1, ok);   // the previous chunk, while this chunk's MMA runs
+        fence_before_sync();
+        ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
+        fence_after_sync();
     }
-    zp[h * kK + k] = z;
-    tmem_wait_st();
-    fence_proxy_async();
+    // the last chunk, once its MMA is done (or the MMA in flight after a failure)
+    if (nm > 0) {
+        const bool okm = mbar_wait(BAR_M, (uint32_t)((nm - 1) & 1));
+        fence_after_sync();
+        ok = __syncthreads_and(ok && okm) != 0;
+        if (ok) take(it0 + nm - 1, (nm - 1) & 1, true);
+    }
+    // after a failed wait: let a landing in flight arrive before the shared memory is released
+    if (tid == 0 && pend_l) (void)mbar_wait(BAR_L, ph_l);
     fence_before_sync();
     __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-        mma_pass_ts(tbase + D_COL, tbase + A_HI, vt_hi, DV, DV * 128, false);
-        if constexpr (SPLIT) {
-            mma_pass_ts(tbase + D_COL, tbase + A_HI, vt_lo, DV, DV * 128, true);
-            mma_pass_ts(tbase + D_COL, tbase + A_LO, vt_hi, DV, DV * 128, true);
-        }
-        mma_commit(smem_addr(bar + 1));
-    }
-    __syncwarp();
-    ok = mbar_wait(smem_addr(bar + 1), 0) && ok;
-    fence_after_sync();
-    // block layout on this path: Vt^T as DV rows of K, then Z as row DV
-    const long long SZ = (long long)kK * DV + kK;
-    float *o = partial + (bh * nblk + blockIdx.x) * SZ;
-    const float qnan = __int_as_float(0x7fc00000);
-#pragma unroll
-    for (int cb = 0; cb < DV / 32; ++cb) {
-        const int c = h * (DV / 2) + 16 * cb;
-        uint32_t r[16];
-        tmem_ld16(tmem_at(tbase, lane0, D_COL + c), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = ok ? __uint_as_float(r[q]) : qnan;
-    }
-    if (h == 0) o[(long long)kK * DV + k] = ok ? zp[k] + zp[kK + k] : qnan;
-    fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 // ------------------------------------------------------------------------
@@ -599,14 +656,17 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
     StateMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
     const uint16_t *k16 = static_cast<const uint16_t *>(gk);
-    if (!make_tma_2d(&maps.gk[0], k16, true, rows, kK, kC)) return cudaErrorInvalidValue;
+    if (!make_tma_2d(&maps.gk[0], k16, true, rows, kK, kC) || !make_tma_2d(&maps.v, v, dm.v_bf16, rows, DV, kC))
+        return cudaErrorInvalidValue;
     if (SPLIT) {
         if (!make_tma_2d(&maps.gk[1], k16 + (long long)rows * kK, true, rows, kK, kC)) return cudaErrorInvalidValue;
     } else {
         maps.gk[1] = maps.gk[0];
     }
-    dim3 grid(dm.nblk(), (unsigned)dm.BH());
-    k_chunk_state_tc<SPLIT, DV><<<grid, 256, smem, st>>>(maps, dm.N, v, dm.v_bf16, partial, dm.nblk());
+    const long long items = dm.BH() * (long long)dm.nblk();
+    const int grid = (int)(items < sm_count() ? items : sm_count());
+    k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, dm.v_bf16,
+                                                                   partial);
     return cudaGetLastError();
 }
 
