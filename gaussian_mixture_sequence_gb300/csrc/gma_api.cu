@@ -121,9 +121,15 @@ gma_status check_ws(void *ws, size_t ws_bytes, const WsPlan &wp)
         gma_status _s = (expr);                                                                            \
         if (_s != GMA_OK) return _s;                                                                       \
     } while (0)
+// The CUDA error behind the last GMA_ERR_CUDA returned on this thread.
+thread_local cudaError_t g_last_cuda = cudaSuccess;
 #define GMA_CUDA(expr)                                                                                     \
     do {                                                                                                   \
-        if ((expr) != cudaSuccess) return GMA_ERR_CUDA;                                                    \
+        const cudaError_t _e = (expr);                                                                     \
+        if (_e != cudaSuccess) {                                                                           \
+            g_last_cuda = _e;                                                                              \
+            return GMA_ERR_CUDA;                                                                           \
+        }                                                                                                  \
     } while (0)
 
 template <typename T>
@@ -168,6 +174,8 @@ size_t gma_workspace_size(const gma_shape *shape, gma_op op)
     if ((unsigned)op > 3u || make_dims(shape, &dm, op) != GMA_OK) return 0;
     return plan(dm, op).bytes;
 }
+
+const char *gma_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda); }
 
 const char *gma_status_string(gma_status status)
 {

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 {
     using Sm = StateSmem<SPLIT, DV>;
     constexpr int NP = SPLIT ? 2 : 1;
+    static_assert(StateSmem<SPLIT, DV>::bytes <= 232448, "shared memory of one CTA");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *gl = sm;                                         // Gamma_K planes (hi, lo)
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
+    static_assert(OutSmem<SPLIT, DV>::bytes <= 232448, "shared memory of one CTA");
     constexpr int VPER = (kC * DV / 4) / kOutThreads;       // float4 of V per thread
     constexpr uint32_t AS = Sm::ATOM, PART = Sm::PART;
     constexpr int SROWS = 2 * DV + 2;                       // 256-byte rows of a memory block

@@ -77,6 +77,8 @@ def load():
         lib.gma_workspace_size.restype = ctypes.c_size_t
         lib.gma_status_string.argtypes = [ctypes.c_int]
         lib.gma_status_string.restype = ctypes.c_char_p
+        lib.gma_last_cuda_error.argtypes = []
+        lib.gma_last_cuda_error.restype = ctypes.c_char_p
         lib.gma_responsibilities.argtypes = [S, _Params, P, P, P, ctypes.c_size_t, P]
         lib.gma_forward_bidir.argtypes = [S, _Params, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_forward_causal.argtypes = [S, _Params, P, P, P, P, P, P, P, ctypes.c_size_t, P]
@@ -107,7 +109,10 @@ def gma_workspace_size(shape: Shape, op: int) -> int:
 
 def _check(fn, status):
     if status != 0:
-        raise GMAError(fn, status, gma_status_string(status))
+        msg = gma_status_string(status)
+        if status == 5:
+            msg += " (" + load().gma_last_cuda_error().decode() + ")"
+        raise GMAError(fn, status, msg)
 
 
 def _ptr(t, name, shape=None, dtype=None, device=None, optional=False):

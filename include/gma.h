@@ -218,6 +218,10 @@ gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params params, co
 /* Static description of a status code (never NULL). */
 const char *gma_status_string(gma_status status);
 
+/* Name of the CUDA error behind the last GMA_ERR_CUDA returned on the calling
+ * thread ("cudaSuccess" if there was none).  Static string.                 */
+const char *gma_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
