@@ -98,6 +98,24 @@ def test_rejects_bad_pointers_and_workspace(lib):
     assert _call_causal(lib, bad) == 1
 
 
+def test_host_entry_workspace_and_validation(lib):
+    s = _shape(N=4096)
+    # the host-buffer entry's scratch holds device copies of q, k, v and out, then the causal workspace
+    need = gma.gma_workspace_size(s, gma.OP_CAUSAL_HOST)
+    stage = 2 * 3 * 4096 * (2 * 64 * 4 + 64 * 4 + 64 * 4)   # B * H * N rows of q, k, v, out (fp32)
+    assert need == gma.gma_workspace_size(s, gma.OP_CAUSAL) + stage
+    prm = gma._Params(FAKE, FAKE, FAKE)
+    call = lambda **kw: lib.gma_forward_causal_host(
+        ctypes.byref(s), prm, kw.get("q", FAKE), kw.get("k", FAKE), kw.get("v", FAKE), None, None,
+        kw.get("o", FAKE), kw.get("ws", FAKE), kw.get("wn", need), None)
+    assert call(q=None) == 1
+    assert call(o=None) == 1
+    assert call(ws=None) == 4
+    assert call(wn=need - 1) == 4
+    assert call(ws=FAKE + 8) == 3
+    assert lib.gma_last_cuda_error() == b"cudaSuccess"
+
+
 def test_empty_sequence_is_a_no_op(lib):
     # N = 0: nothing to launch for the bidirectional form
     s = _shape(N=0)
