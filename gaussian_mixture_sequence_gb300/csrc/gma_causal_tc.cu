@@ -268,8 +268,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         __syncthreads();   // the landing tiles have been read; A and V^T are in place
         fence_after_sync();
         if (tid == 0) {
-            if (it + 1 < it1 && ok) {
-                fence_proxy_async();
+            if (it + 1 < it1 && ok) {   // the threads only read the landing tiles: no proxy fence
                 load(it + 1);
                 pend_l = true;
                 ph_l = (uint32_t)((j + 1) & 1);
@@ -562,8 +561,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             __syncthreads();                  // every thread is past its reads of the A images
             fence_after_sync();
             if (tid == 0) {
-                if (more && ok) {   // the Gamma rows and A images are free: the next item's tiles
-                    fence_proxy_async();
+                // the Gamma rows and A images are free: the next item's tiles (the threads only
+                // read them; the writes of V^T were fenced before the barrier)
+                if (more && ok) {
                     load_gamma(it + 1);
                     pend_g = true;
                     ph_g = ph ^ 1u;
@@ -579,8 +579,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             __syncwarp();
             ok = mbar_wait(BAR_V, ph) && ok;
             fence_after_sync();
-            if (tid == 0 && more && ok) {   // the Vt^T rows are free: the next item's memory
-                fence_proxy_async();
+            // the Vt^T rows are free: the next item's memory (the threads' writes of V^T were
+            // fenced before the MMA that read them, which has completed)
+            if (tid == 0 && more && ok) {
                 load_memory(it + 1);
                 pend_s = true;
                 ph_s = ph ^ 1u;
@@ -591,7 +592,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             __syncthreads();                  // every thread is past its reads of the A images
             fence_after_sync();
             if (tid == 0 && more && ok) {     // B and the A images are free: the next item's tiles
-                fence_proxy_async();
                 load_gamma(it + 1);
                 load_memory(it + 1);
                 pend_g = pend_s = true;

@@ -51,15 +51,19 @@ constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulatio
 
 // Shared memory: the bound matrix, the routing tile, each group's output tile,
 // the constants c, c', A, M, each group's exchange slots between the two
-// halves of a row, and the mbarriers (images, routing tile, each group's MMA).
+// halves of a row, the mbarriers (images, routing tile, each group's MMA), and
+// each warp's copy of one component's exact parameters.
 struct PrunedSmem {
     static constexpr uint32_t W = kPrunedWBytes;                        // bf16 [128][128], SW128
     static constexpr uint32_t X = kPRows * kPD * 4;                     // routing tile (fp32 worst case)
     static constexpr uint32_t O = kPRows * kPK * 4;                     // output tile (fp32 worst case)
     static constexpr uint32_t C = kPrunedCBytes;                        // c, c', A, M
     static constexpr uint32_t EX = 3 * 2 * kPK * 4;                     // [3][2][128] per group
-    static constexpr size_t bytes = 1024 + W + X + kPGroups * (size_t)O + C + kPGroups * (size_t)EX + 64;
+    static constexpr uint32_t PW = kPDP * 16;                           // one component's parameters
+    static constexpr size_t bytes =
+        1024 + W + X + kPGroups * (size_t)O + C + kPGroups * (size_t)EX + 64 + (kPThreads / 32) * (size_t)PW;
 };
+static_assert(PrunedSmem::bytes <= 232448, "routing kernel: shared memory above the per-block limit");
 
 // Named barrier of one group (ids 1, 2; id 0 is __syncthreads).
 __device__ __forceinline__ void group_sync(int g)
@@ -93,6 +97,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
 }
+
 
 // One CTA per head: the bound matrix W (bf16, in the swizzled B-operand
 // layout), the exact parameters with padded rows, and c, c', A, M.
@@ -180,6 +185,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // images, routing tile for group 0 / 1, MMA of group 0 / 1
     uint64_t *bar = reinterpret_cast<uint64_t *>(f_s + 4 * kPK + kPGroups * 6 * kPK);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    float4 *pw_s = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(bar) + 64) + warp * kPDP;
     const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1 + grp), BAR_M = smem_addr(bar + 3 + grp);
 
     const int tps = (N + kPRows - 1) / kPRows;    // tiles per slice
@@ -262,6 +268,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     xr[2 * g + 1] = make_float2(u.z, u.w);
                 }
             }
+            group_sync(grp);   // the routing tile has been read: the next item's tile may land in it
+            if (gt == 0 && it + 1 < it1) load_x(it + 1);   // (the threads only read it: no proxy fence)
             float2 s2v = make_float2(0.f, 0.f);
 #pragma unroll
             for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
@@ -282,13 +290,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_wait_st();
             fence_before_sync();
             if (gt == 0) bulk_wait_read();   // this group's previous output tile has left shared memory
-            group_sync(grp);   // the routing tile has been read; A is in TMEM
+            group_sync(grp);   // A is in TMEM
             fence_after_sync();
             if (gt == 0) {
-                if (it + 1 < it1) {   // the next item's tile
-                    fence_proxy_async();
-                    load_x(it + 1);
-                }
 #pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t kb = kk * 32;
@@ -380,7 +384,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             if (group_or(grp, (xm0 | xm1) != 0u)) {
-                // exact log-joint of a component (parameters from global memory, L2-resident)
+                // exact log-joint of a component for this lane's row (parameters from global
+                // memory, L2-resident)
                 auto exact = [&](int k) {
                     const float4 *pk = ph + k * kPStride;
                     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -394,43 +399,69 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                     return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
                 };
-                // Runs f(k, l_k) for every component k of the two masks, by 32-component word.
-                // Few per lane: each lane walks its own set.  Many: the warp walks the union of
-                // its lanes' sets one component at a time, so that the parameter reads are
-                // shared by the warp.  The warp-wide choice is made here, where every lane is
-                // present (for_kept itself also runs in lane-divergent code).
-                uint32_t unis[2];
-                bool lanes[2];
+                // the same value for a component k common to the warp, every lane present: lane
+                // dp holds the parameter word dp of k (one coalesced read per warp) and puts it in
+                // the warp's shared copy, which every lane then reads as broadcasts
+                auto exact_w = [&](int k, const float4 w) {
+                    __syncwarp();   // the previous component's copy has been read
+                    pw_s[lane] = w;
+                    __syncwarp();
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int wd = 0; wd < 2; ++wd) {
-                    const uint32_t mk = wd ? xm1 : xm0;
-                    unis[wd] = __reduce_or_sync(0xffffffffu, mk);
-                    lanes[wd] = 4 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(unis[wd]);
-                }
+                    for (int dp = 0; dp < kPDP; dp += 2) {
+                        const float4 p = pw_s[dp], r = pw_s[dp + 1];
+                        const float2 y0 = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
+                        acc0 = __ffma2_rn(y0, y0, acc0);
+                        const float2 y1 = __ffma2_rn(xr[dp + 1], make_float2(r.x, r.y), make_float2(r.z, r.w));
+                        acc1 = __ffma2_rn(y1, y1, acc1);
+                    }
+                    return fmaf(-0.5f, (acc0.x + acc0.y) + (acc1.x + acc1.y), c_s[k]);
+                };
+                // Runs f(k, l_k) for every component k of the two masks, by 32-component word.
+                // Lanes whose sets are small against their union (16 times or more) walk their
+                // own sets; otherwise the warp walks the union one component at a time, reading
+                // the next component's parameters while it evaluates the current one.
+                // Warp-converged code only.
                 auto for_kept = [&](auto &&f) {
 #pragma unroll
                     for (int wd = 0; wd < 2; ++wd) {
                         const int k0 = 64 * hf + 32 * wd;
-                        const uint32_t mk = wd ? xm1 : xm0, uni = unis[wd];
-                        if (lanes[wd]) {
+                        const uint32_t mk = wd ? xm1 : xm0;
+                        const uint32_t uni = __reduce_or_sync(0xffffffffu, mk);
+                        const bool lanes =
+                            16 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(uni);
+                        if (lanes) {
                             for (uint32_t mm = mk; mm; mm &= mm - 1) {
                                 const int k = k0 + __ffs(mm) - 1;
                                 f(k, exact(k));
                             }
-                        } else {
-                            for (uint32_t mm = uni; mm; mm &= mm - 1) {
+                        } else if (uni) {
+                            const float4 *pw = ph + lane;
+                            uint32_t mm = uni;
+                            float4 w = __ldg(pw + (k0 + __ffs(mm) - 1) * kPStride);
+                            while (mm) {
                                 const int kq = __ffs(mm) - 1;
-                                const float l = exact(k0 + kq);
+                                mm &= mm - 1;
+                                const float4 wn = mm ? __ldg(pw + (k0 + __ffs(mm) - 1) * kPStride) : w;
+                                const float l = exact_w(k0 + kq, w);
                                 if ((mk >> kq) & 1u) f(k0 + kq, l);
+                                w = wn;
                             }
                         }
                     }
                 };
-                // exact pass: online maximum and sum over the kept components of this half;
-                // with an fp32 output tile the log-joints wait in it for the normalisation
+                // exact pass: online maximum and sum over the kept components of this half; the
+                // log-joints wait in the output tile for the normalisation (fp32 tile: as floats;
+                // split tile: high half-word in the hi plane, low half-word in the lo plane)
                 float mt = -FLT_MAX, st = 0.f;
                 for_kept([&](int k, float l) {
-                    if (g_f32) *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                    if (g_f32) {
+                        *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
+                    } else if (g_split) {
+                        const uint32_t off = sw128_offset(i, k, kPRows, 2), u = __float_as_uint(l);
+                        *reinterpret_cast<unsigned short *>(ob + off) = (unsigned short)(u >> 16);
+                        *reinterpret_cast<unsigned short *>(ob + LO + off) = (unsigned short)(u & 0xffffu);
+                    }
                     if (l > mt) {
                         st = st * expf(mt - l) + 1.f;
                         mt = l;
@@ -445,24 +476,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const float q1 = ex1[(1 - hf) * kPK + i], q2 = ex2[(1 - hf) * kPK + i];
                     const float m = fmaxf(mt, q1);
                     const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
-                    // the kept posteriors of this half into the output tile
-                    if (!g_f32) {
-                        for_kept([&](int k, float l) {
-                            __nv_bfloat16 hi, lo;
-                            split_bf16(expf(l - m) * inv, hi, lo);
-                            const uint32_t off = sw128_offset(i, k, kPRows, 2);
-                            *reinterpret_cast<__nv_bfloat16 *>(ob + off) = hi;
-                            if (g_split) *reinterpret_cast<__nv_bfloat16 *>(ob + LO + off) = lo;
-                        });
-                    } else {
+                    // the kept posteriors of this half into the output tile (a single-plane bf16
+                    // tile has no room for the log-joints: they are evaluated again)
 #pragma unroll
-                        for (int wd = 0; wd < 2; ++wd)
-                            for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
-                                float *o = reinterpret_cast<float *>(
-                                    ob + sw128_offset(i, 64 * hf + 32 * wd + __ffs(mm) - 1, kPRows, 4));
+                    for (int wd = 0; wd < 2; ++wd)
+                        for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
+                            const int k = 64 * hf + 32 * wd + __ffs(mm) - 1;
+                            if (g_f32) {
+                                float *o = reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4));
                                 *o = expf(*o - m) * inv;
+                            } else {
+                                const uint32_t off = sw128_offset(i, k, kPRows, 2);
+                                const float l =
+                                    g_split ? __uint_as_float(
+                                                  ((uint32_t)*reinterpret_cast<const unsigned short *>(ob + off) << 16) |
+                                                  *reinterpret_cast<const unsigned short *>(ob + LO + off))
+                                            : exact(k);
+                                __nv_bfloat16 hi, lo;
+                                split_bf16(expf(l - m) * inv, hi, lo);
+                                *reinterpret_cast<__nv_bfloat16 *>(ob + off) = hi;
+                                if (g_split) *reinterpret_cast<__nv_bfloat16 *>(ob + LO + off) = lo;
                             }
-                    }
+                        }
                 }
             }
             fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
