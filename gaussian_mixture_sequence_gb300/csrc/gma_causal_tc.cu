@@ -390,6 +390,7 @@ struct OutMaps {
     CUtensorMap gq[2], gk[2];   // hi / lo planes of the responsibilities
     CUtensorMap s;              // memory blocks in operand form, as rows of 256 bytes
     CUtensorMap o;              // output [slices][N][d_v], boxes of 64 rows x 32 columns
+    CUtensorMap v;              // V [slices][N][d_v], boxes of C rows x 128 bytes (causal form)
 };
 
 // CAUSAL = false gives the bidirectional read: U = Gamma_Q [Vt | Z] with the
@@ -397,7 +398,7 @@ struct OutMaps {
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
-                   const void *__restrict__ v, bool v_bf16, const float *__restrict__ zsrc, float *__restrict__ out)
+                   bool v_bf16, const float *__restrict__ zsrc, float *__restrict__ out)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
@@ -412,8 +413,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
     float *z_s = reinterpret_cast<float *>(os + Sm::OUT);          // [128] Z of the carried memory
     float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [4]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [5]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const long long it1 = it0 + per < items ? it0 + per : items;
     constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC;
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3);
+                   BAR_V = smem_addr(bar + 3), BAR_VL = smem_addr(bar + 4);
     const long long SZ = (long long)kK * DV + kK;
 
     // block of the carried memory read by item it
@@ -440,10 +441,11 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     };
     auto load_memory = [&](long long it) {   // one thread
         const int srow = (int)(mem_block(it) * SROWS);
-        mbar_expect_tx(BAR_S, (uint32_t)(NP * DV * kRowB));
+        mbar_expect_tx(BAR_S, (uint32_t)(NP * DV * kRowB + kK * 4));
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a)
                 tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS + PART), &maps.s, a * 64, srow + pl * DV, BAR_S);
+        bulk_g2s(smem_addr(z_s), zsrc + mem_block(it) * SZ + (long long)kK * DV, kK * 4, BAR_S);   // Z
     };
 
     if (warp == 0) {
@@ -451,10 +453,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tmem_relinquish();
     }
     // loads in flight that the loop has not waited for (thread 0's record)
-    bool pend_g = false, pend_s = false;
-    uint32_t ph_g = 0, ph_s = 0;
+    bool pend_g = false, pend_s = false, pend_v = false;
+    uint32_t ph_g = 0, ph_s = 0, ph_v = 0;
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0);
@@ -462,8 +464,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             pend_g = pend_s = true;
         }
     }
-    // Z of the carried memory, read one item ahead
-    float zreg = (tid < kK && it0 < it1) ? zsrc[mem_block(it0) * SZ + (long long)kK * DV + tid] : 0.f;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -476,12 +476,17 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         const long long bh = it / nblk;
         const int c0 = (int)(it % nblk) * kC;
         const int nr = min(kC, N - c0);
-        const long long rowbase = bh * N + c0;
         const bool more = it + 1 < it1;
-        if (tid < kK) z_s[tid] = zreg;
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+        if (CAUSAL && tid == 0) {
+            // V of this chunk lands in the output staging tile once the previous output tile has
+            // left it (the threads' writes of that tile were fenced before the last barrier)
+            bulk_wait_read();
+            mbar_expect_tx(BAR_VL, (uint32_t)(kC * DV * (v_bf16 ? 2 : 4)));
+            for (int a = 0; a < DV * (v_bf16 ? 2 : 4) / 128; ++a)
+                tma_load_3d(smem_addr(os + a * kC * 128), &maps.v, a * (v_bf16 ? 64 : 32), c0, (int)bh, BAR_VL);
+            pend_v = true;
+            ph_v = ph;
+        }
         const bool ok_g = mbar_wait(BAR_G, ph), ok_s = mbar_wait(BAR_S, ph);
         ok = ok && ok_g && ok_s;
         if (tid == 0) {   // a load whose wait gave up is still in flight
@@ -498,16 +503,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             mma_commit(BAR_M);
         }
         __syncwarp();
-        // while the tensor core works: V of this chunk into registers (lanes over tokens),
-        // and the partial Gamma_Q,i . Z over this thread's 32 components
-        float4 vr[CAUSAL ? VPER : 1];
-        if constexpr (CAUSAL) {
-#pragma unroll
-            for (int u = 0; u < VPER; ++u) {
-                const int f = tid + u * kOutThreads, j = f % kC, c4 = f / kC;
-                vr[u] = j < nr ? load4(v, (rowbase + j) * DV + 4 * c4, v_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
+        // while the tensor core works: the partial Gamma_Q,i . Z over this thread's 32 components
         {
             float qz = 0.f;
 #pragma unroll
@@ -545,11 +541,27 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 }
                 part[(4 + g) * kK + i] = put_a32<SPLIT>(tbase, lane0, A_PM_HI, A_PM_LO, 32 * g, x);
             }
-            // V^T (element (c, j)) into the Vt^T rows of the B images; lanes run over tokens
+            // V^T (element (c, j)) from the landing tile into the Vt^T rows of the B images;
+            // lanes run over tokens
+            {
+                const bool ok_v = mbar_wait(BAR_VL, ph);
+                ok = ok && ok_v;
+                if (tid == 0) pend_v = !ok_v;
+            }
 #pragma unroll
             for (int u = 0; u < VPER; ++u) {
                 const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
-                const float e4[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < nr) {
+                    if (v_bf16) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(os + sw128_offset(j, c4, kC, 2));
+                        t = make_float4(bf(w.x & 0xffffu), __uint_as_float(w.x & 0xffff0000u), bf(w.y & 0xffffu),
+                                        __uint_as_float(w.y & 0xffff0000u));
+                    } else {
+                        t = *reinterpret_cast<const float4 *>(os + sw128_offset(j, c4, kC, 4));
+                    }
+                }
+                const float e4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     put_split<SPLIT>(tb0, tb1, (j >> 6) * AS + PART + sw128_offset(c4 + e, j & 63, DV, 2), e4[e]);
@@ -557,8 +569,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             tmem_wait_st();
             fence_proxy_async();
             fence_before_sync();
-            if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
-            __syncthreads();                  // every thread is past its reads of the A images
+            __syncthreads();   // every thread is past its reads of the A images and of V
             fence_after_sync();
             if (tid == 0) {
                 // the Gamma rows and A images are free: the next item's tiles (the threads only
@@ -599,7 +610,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             }
         }
 
-        if (tid < kK && more) zreg = zsrc[mem_block(it + 1) * SZ + (long long)kK * DV + tid];
         float den = eps;
 #pragma unroll
         for (int q = 0; q < (CAUSAL ? 8 : 4); ++q) den += part[q * kK + i];
@@ -635,6 +645,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // after a failed wait: let the copies still in flight land before the shared memory is released
     if (tid == 0) {
         if (pend_g) (void)mbar_wait(BAR_G, ph_g);
+        if (pend_v) (void)mbar_wait(BAR_VL, ph_v);
         if (pend_s) (void)mbar_wait(BAR_S, ph_s);
         bulk_wait_all();
     }
@@ -695,11 +706,13 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     // memory blocks in operand form: rows of 256 bytes (hi plane, lo plane, Z), d_v rows per box
     ok = ok && make_tma_2d(&maps.s, mem, true, blocks * (2 * DV + 2), kK, DV) &&
          make_tma_3d(&maps.o, out, false, DV, dm.N, dm.BH(), 64);
+    if (CAUSAL) ok = ok && make_tma_3d(&maps.v, v, dm.v_bf16, DV, dm.N, dm.BH(), kC);
+    else maps.v = maps.o;
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, reinterpret_cast<const float *>(mem), out);
+        maps, dm.N, dm.nblk(), items, dm.eps, dm.v_bf16, reinterpret_cast<const float *>(mem), out);
     return cudaGetLastError();
 }
 

@@ -368,6 +368,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *reinterpret_cast<float *>(ob + sw128_offset(i, 64 * hf + a1, kPRows, 4)) = 1.0f;
             }
             uint32_t xm0 = 0u, xm1 = 0u;   // the kept components of rows that need the softmax
+            // per 32-component word: the union of the warp's kept sets, whether its lanes walk
+            // their own sets, and the parameters of the union's first component (read here, so
+            // that the read overlaps the group barrier below)
+            uint32_t uni[2] = {0u, 0u};
+            bool lanes[2] = {true, true};
+            float4 wpre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
             if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
                 uint32_t mk[2] = {0u, 0u};
 #pragma unroll
@@ -381,6 +387,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (!single) {
                     xm0 = mk[0];
                     xm1 = mk[1];
+                }
+#pragma unroll
+                for (int wd = 0; wd < 2; ++wd) {
+                    const uint32_t m = wd ? xm1 : xm0;
+                    uni[wd] = __reduce_or_sync(0xffffffffu, m);
+                    lanes[wd] = 16 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(m)) <= (uint32_t)__popc(uni[wd]);
+                    if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
                 }
             }
             if (group_or(grp, (xm0 | xm1) != 0u)) {
@@ -427,18 +440,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int wd = 0; wd < 2; ++wd) {
                         const int k0 = 64 * hf + 32 * wd;
                         const uint32_t mk = wd ? xm1 : xm0;
-                        const uint32_t uni = __reduce_or_sync(0xffffffffu, mk);
-                        const bool lanes =
-                            16 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(mk)) <= (uint32_t)__popc(uni);
-                        if (lanes) {
+                        if (lanes[wd]) {
                             for (uint32_t mm = mk; mm; mm &= mm - 1) {
                                 const int k = k0 + __ffs(mm) - 1;
                                 f(k, exact(k));
                             }
-                        } else if (uni) {
+                        } else {
                             const float4 *pw = ph + lane;
-                            uint32_t mm = uni;
-                            float4 w = __ldg(pw + (k0 + __ffs(mm) - 1) * kPStride);
+                            uint32_t mm = uni[wd];
+                            float4 w = wpre[wd];
                             while (mm) {
                                 const int kq = __ffs(mm) - 1;
                                 mm &= mm - 1;
