@@ -112,191 +112,229 @@ __device__ __forceinline__ void put_split(unsigned char *hi, unsigned char *lo, 
 }
 
 // ------------------------------------------------------------------------
-// L_c = Gamma_K,c^T [V_c | 1]: M = components, N = d_v, contraction over the
-// chunk's 128 tokens.  Persistent: CTA b takes the chunks [b * per, (b + 1) *
-// per) of the list (slice, chunk) in order.  The chunk's Gamma_K planes and V
-// land by TMA; A = Gamma_K^T goes to TMEM: warp w owns components
-// 32 (w % 4) + lane and tokens [32 (w / 4), +32), read across the landing rows
-// (a warp reads 64 contiguous bytes of one row); B = V^T is split by threads
-// into its images.  Once the landing tiles have been read, the next chunk's are
-// fetched; the MMA of chunk c runs while the threads write out chunk c - 1
-// from the other of two accumulator buffers.  The block is written transposed:
-// d_v rows of K, then Z as row d_v.
+// L_c = Gamma_K,c^T [V_c | 1]: M = components, contraction over the chunk's
+// 128 tokens, with both operands MN-major in shared memory, so that no thread
+// transposes anything:
+//   A = Gamma_K^T: the chunk's Gamma_K planes as TMA lands them ([tokens][components]);
+//   B = [V_hi | V_lo | 1] (split planes) or [V | 1]: token-major bf16 images that the
+//       threads write from V, read from global memory one row per d_v / 4 lanes.
+// One MMA chain per plane of A over the whole of B (N = value columns + 16), so with
+// split planes D[:, c] + D[:, d_v + c] = (A_hi + A_lo)(V_hi + V_lo), and every column
+// of the ones block holds Z_k = sum_j Gamma_K[j][k].  Rows past the sequence end
+// land as zeros (3D maps; V rows are not read) and contribute nothing.
+// Persistent: CTA b takes the chunks [b * per, (b + 1) * per) of the list (slice,
+// chunk) in order.  Landing tiles, B images and accumulators are double-buffered:
+// the MMA of chunk c runs while the threads write out chunk c - 1 and build the B
+// image of chunk c + 1, whose Gamma_K planes are in flight.  The block is written
+// transposed: d_v rows of K, then Z as row d_v.
 constexpr int kStateThreads = 512;
 
 template <bool SPLIT, int DV>
 struct StateSmem {
-    static constexpr uint32_t G = kC * kRowB;    // one Gamma_K plane tile (128 tokens x 128 components)
-    static constexpr uint32_t VL = kC * DV * 4;  // V landing tile (fp32 worst case)
-    static constexpr uint32_t VT = DV * kRowB;   // one V^T image: d_v rows of 128 tokens
-    static constexpr size_t bytes = 1024 + 2 * (size_t)G + VL + 2 * (size_t)VT + 2 * 4 * kK * 4 + 64;
+    static constexpr int NP = SPLIT ? 2 : 1;               // planes of Gamma_K
+    static constexpr int NBV = NP * DV / 64;               // 64-column value blocks of B
+    static constexpr int N = NBV * 64 + 16;                // MMA N: the value columns, then 16 ones
+    static constexpr uint32_t BLK = kC * 128;              // one 64-column block of 128 token rows
+    static constexpr uint32_t G = kC * kRowB;              // one Gamma_K plane tile (two blocks)
+    static constexpr uint32_t L = NP * G;                  // landing tiles of one chunk
+    static constexpr uint32_t BI = (NBV + 1) * BLK;        // B image of one chunk (values, ones)
+    static constexpr size_t bytes = 1024 + 2 * ((size_t)L + BI) + 64;
 };
 
 struct StateMaps {
-    CUtensorMap gk[2], v;   // Gamma_K hi / lo planes; V
+    CUtensorMap gk[2];   // Gamma_K hi / lo planes as [slices][N][K], boxes of C rows x 64 components
 };
 
 template <bool SPLIT, int DV>
 __global__ void __launch_bounds__(kStateThreads, 1)
-    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items, bool v_bf16,
-                     float *__restrict__ partial)
+    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items,
+                     const void *__restrict__ v, bool v_bf16, float *__restrict__ partial)
 {
     using Sm = StateSmem<SPLIT, DV>;
-    constexpr int NP = SPLIT ? 2 : 1;
-    static_assert(StateSmem<SPLIT, DV>::bytes <= 232448, "shared memory of one CTA");
+    constexpr int NP = Sm::NP, NBV = Sm::NBV;
+    constexpr int F4 = DV / 4;                              // groups of four in a row of V
+    constexpr int VPER = kC * F4 / kStateThreads;           // groups of V per thread
+    static_assert(Sm::bytes <= 232448, "shared memory of one CTA");
+    static_assert(Sm::N <= 256 && Sm::N % 16 == 0, "MMA N");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *gl = sm;                                         // Gamma_K planes (hi, lo)
-    unsigned char *vl = sm + 2 * Sm::G;                             // V landing tile
-    unsigned char *vt_hi = vl + Sm::VL, *vt_lo = vt_hi + Sm::VT;    // V^T images
-    float *zp = reinterpret_cast<float *>(vt_lo + Sm::VT);          // [2][4][128] token-group sums of Gamma_K
-    uint64_t *bar = reinterpret_cast<uint64_t *>(zp + 2 * 4 * kK);  // landing, MMA
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
-    const uint32_t BAR_L = smem_addr(bar), BAR_M = smem_addr(bar + 1);
+    unsigned char *land = sm;                               // [2] Gamma_K landing tiles
+    unsigned char *bimg = sm + 2 * Sm::L;                   // [2] B images
+    uint64_t *bar = reinterpret_cast<uint64_t *>(bimg + 2 * Sm::BI);   // landing [2], MMA [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tg = warp >> 2;                   // token group of A, column group of D
+    const int tg = warp >> 2;                   // column group of D
     const uint32_t lane0 = 32 * (warp & 3);
     const int k = lane0 + lane;                 // component (TMEM lane)
     const long long per = (items + gridDim.x - 1) / gridDim.x;
     const long long it0 = (long long)blockIdx.x * per;
     const long long it1 = it0 + per < items ? it0 + per : items;
-    constexpr uint32_t A_HI = 0, A_LO = 64, D0 = 128;
-    const int ev = v_bf16 ? 2 : 4;
     const long long SZ = (long long)kK * DV + kK;
     const float qnan = __int_as_float(0x7fc00000);
 
-    auto load = [&](long long it) {   // one thread: the chunk's Gamma_K planes and V
-        const int row0 = (int)((it / nblk) * N + (it % nblk) * kC);
-        mbar_expect_tx(BAR_L, (uint32_t)(NP * Sm::G + kC * DV * ev));
+    auto load = [&](long long it, int b) {   // one thread: the chunk's Gamma_K planes into landing buffer b
+        const int sl = (int)(it / nblk), c0 = (int)(it % nblk) * kC;
+        const uint32_t bl = smem_addr(bar + b);
+        mbar_expect_tx(bl, Sm::L);
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a)
-                tma_load_2d(smem_addr(gl + pl * Sm::G + a * kAtom), &maps.gk[pl], a * 64, row0, BAR_L);
-        for (int a = 0; a < DV * ev / 128; ++a)
-            tma_load_2d(smem_addr(vl + a * kAtom), &maps.v, a * (128 / ev), row0, BAR_L);
+                tma_load_3d(smem_addr(land + b * Sm::L + pl * Sm::G + a * Sm::BLK), &maps.gk[pl], a * 64, c0, sl, bl);
+    };
+    // V of chunk it as raw words (fp32, or bf16 pairs in .x and .y); F4 consecutive threads read a row
+    auto load_v = [&](long long it, uint4 (&r)[VPER]) {
+        const int c0 = (int)(it % nblk) * kC, nr = min(kC, N - c0);
+        const long long rowbase = (it / nblk) * N + c0;
+#pragma unroll
+        for (int u = 0; u < VPER; ++u) {
+            const int f = tid + u * kStateThreads, j = f / F4, c4 = 4 * (f % F4);
+            r[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (j < nr) {
+                if (v_bf16) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(v) + (rowbase + j) * DV + c4);
+                    r[u].x = w.x;
+                    r[u].y = w.y;
+                } else {
+                    r[u] = *reinterpret_cast<const uint4 *>(static_cast<const float *>(v) + (rowbase + j) * DV + c4);
+                }
+            }
+        }
+    };
+    // the value columns of B image b: hi plane at column c, lo plane at column d_v + c
+    auto put_b = [&](int b, const uint4 (&r)[VPER]) {
+        unsigned char *bi = bimg + b * Sm::BI;
+#pragma unroll
+        for (int u = 0; u < VPER; ++u) {
+            const int f = tid + u * kStateThreads, j = f / F4, c4 = 4 * (f % F4);
+            const float x[4] = {v_bf16 ? __uint_as_float(r[u].x << 16) : __uint_as_float(r[u].x),
+                                v_bf16 ? __uint_as_float(r[u].x & 0xffff0000u) : __uint_as_float(r[u].y),
+                                v_bf16 ? __uint_as_float(r[u].y << 16) : __uint_as_float(r[u].z),
+                                v_bf16 ? __uint_as_float(r[u].y & 0xffff0000u) : __uint_as_float(r[u].w)};
+            uint32_t hw[2], lw[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                __nv_bfloat16 h0, l0, h1, l1;
+                split_bf16(x[2 * e], h0, l0);
+                split_bf16(x[2 * e + 1], h1, l1);
+                hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+            }
+            *reinterpret_cast<uint2 *>(bi + sw128_offset(j, c4, kC, 2)) = make_uint2(hw[0], hw[1]);
+            if (SPLIT) *reinterpret_cast<uint2 *>(bi + sw128_offset(j, DV + c4, kC, 2)) = make_uint2(lw[0], lw[1]);
+        }
     };
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
-    bool pend_l = false;   // a landing in flight that the loop has not waited for (thread 0's record)
-    uint32_t ph_l = 0;
+    bool pend[2] = {false, false};   // landings in flight that the loop has not waited for (thread 0's record)
+    uint32_t ph_l[2] = {0u, 0u};
     if (tid == 0) {
-        mbar_init(BAR_L, 1);
-        mbar_init(BAR_M, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        if (it0 < it1) {
-            load(it0);
-            pend_l = true;
-        }
+        for (int b = 0; b < 2; ++b)
+            if (it0 + b < it1) {
+                load(it0 + b, b);
+                pend[b] = true;
+            }
     }
+    // the ones columns of both B images (they never change)
+    for (int e = tid; e < 2 * kC * 2; e += kStateThreads) {
+        const int b = e / (2 * kC), j = (e / 2) % kC, h = e % 2;
+        *reinterpret_cast<uint4 *>(bimg + b * Sm::BI + sw128_offset(j, NBV * 64 + 8 * h, kC, 2)) =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
+    uint4 vr[VPER];
+    if (it0 < it1) load_v(it0, vr);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    bool ok = true;
-    int nm = 0;   // MMA chains committed
-    // L of chunk it from accumulator buffer db (and Z from zp[db]) into its block
-    auto take = [&](long long it, int db, bool okv) {
+    // L of chunk it from accumulator b (its MMA complete), into its block
+    auto take = [&](long long it, int b, bool okv) {
         float *o = partial + it * SZ;
+        const uint32_t d = 256u * b;
 #pragma unroll
-        for (int cb = 0; cb < DV / 64; ++cb) {
-            const int c = tg * (DV / 4) + 16 * cb;
+        for (int cb = 0; cb < DV / 4; cb += 16) {
+            const int c = tg * (DV / 4) + cb;
             uint32_t r[16];
-            tmem_ld16(tmem_at(tbase, lane0, D0 + db * DV + c), r);
-            tmem_wait_ld();
+            tmem_ld16(tmem_at(tbase, lane0, d + c), r);
+            float x[16];
+            if constexpr (SPLIT) {
+                uint32_t s[16];
+                tmem_ld16(tmem_at(tbase, lane0, d + DV + c), s);
+                tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = okv ? __uint_as_float(r[q]) : qnan;
+                for (int q = 0; q < 16; ++q) x[q] = __uint_as_float(r[q]) + __uint_as_float(s[q]);
+            } else {
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) x[q] = __uint_as_float(r[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = okv ? x[q] : qnan;
         }
-        if (tg == 0) {
-            const float *z = zp + db * 4 * kK;
-            o[(long long)kK * DV + k] = okv ? (z[k] + z[kK + k]) + (z[2 * kK + k] + z[3 * kK + k]) : qnan;
+        if (tg == 0) {   // Z: any column of the ones block
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, lane0, d + NBV * 64), r);
+            tmem_wait_ld();
+            o[(long long)kK * DV + k] = okv ? __uint_as_float(r[0]) : qnan;
         }
     };
 
+    const uint32_t id = idesc(128, Sm::N, kFmtBF16) | kAMajorMN | kBMajorMN;
+    bool ok = true, okp = true;   // ok: agreed at the last barrier; okp: this thread's waits since
+    int nm = 0;                   // MMA chains issued
 
     for (long long it = it0; it < it1 && ok; ++it) {
-        const int j = (int)(it - it0), db = j & 1;
-        const int nr = min(kC, N - (int)(it % nblk) * kC);
-        const bool ok_l = mbar_wait(BAR_L, (uint32_t)(j & 1));
-        if (tid == 0) pend_l = pend_l && !ok_l;
-        ok = ok && ok_l;
-        if (j > 0) {   // A and the V^T images are free once the previous chunk's MMA is done
-            ok = mbar_wait(BAR_M, (uint32_t)((nm - 1) & 1)) && ok;
-            fence_after_sync();
-        }
-        // A = Gamma_K^T: this thread's 32 tokens of component k, plane by plane; their sum for Z
-        float z = 0.f;
-#pragma unroll
-        for (int pl = 0; pl < NP; ++pl) {
-            const uint16_t *gp = reinterpret_cast<const uint16_t *>(gl + pl * Sm::G);
-            uint32_t p[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int j0 = 32 * tg + 2 * jj;
-                const uint32_t a = j0 < nr ? (uint32_t)gp[sw128_offset(j0, k, kC, 2) / 2] : 0u;
-                const uint32_t b = j0 + 1 < nr ? (uint32_t)gp[sw128_offset(j0 + 1, k, kC, 2) / 2] : 0u;
-                z += bf(a) + bf(b);
-                p[jj] = a | (b << 16);
-            }
-            tmem_st16(tmem_at(tbase, lane0, (pl ? A_LO : A_HI) + 16 * tg), p);
-        }
-        zp[(db * 4 + tg) * kK + k] = z;
-        // B = V^T (element (c, j)) from the landing tile, split; lanes run over tokens
-        constexpr int VPER = kC * DV / 4 / kStateThreads;
-#pragma unroll
-        for (int u = 0; u < VPER; ++u) {
-            const int f = tid + u * kStateThreads, jt = f % kC, c4 = 4 * (f / kC);
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (jt < nr) {
-                if (v_bf16) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(vl + sw128_offset(jt, c4, kC, 2));
-                    t = make_float4(bf(w.x & 0xffffu), __uint_as_float(w.x & 0xffff0000u), bf(w.y & 0xffffu),
-                                    __uint_as_float(w.y & 0xffff0000u));
-                } else {
-                    t = *reinterpret_cast<const float4 *>(vl + sw128_offset(jt, c4, kC, 4));
-                }
-            }
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 0, jt, DV, 2), t.x);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 1, jt, DV, 2), t.y);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 2, jt, DV, 2), t.z);
-            put_split<SPLIT>(vt_hi, vt_lo, sw128_offset(c4 + 3, jt, DV, 2), t.w);
-        }
-        tmem_wait_st();
-        fence_proxy_async();
+        const int j = (int)(it - it0), b = j & 1;
+        put_b(b, vr);   // its buffer was last read by the MMA of chunk j - 2, complete
+        if (it + 1 < it1) load_v(it + 1, vr);   // in flight while this chunk's MMA runs
+        const bool ok_l = mbar_wait(smem_addr(bar + b), (uint32_t)((j >> 1) & 1));
+        if (tid == 0 && ok_l) pend[b] = false;
+        okp = okp && ok_l;
+        fence_proxy_async();   // the B image, written by threads, is read by the tensor core
         fence_before_sync();
-        __syncthreads();   // the landing tiles have been read; A and V^T are in place
+        ok = __syncthreads_and(okp) != 0;
         fence_after_sync();
+        if (!ok) break;
         if (tid == 0) {
-            if (it + 1 < it1 && ok) {   // the threads only read the landing tiles: no proxy fence
-                load(it + 1);
-                pend_l = true;
-                ph_l = (uint32_t)((j + 1) & 1);
-            }
-            const uint32_t d = tbase + D0 + db * DV;
-            mma_pass_ts(d, tbase + A_HI, vt_hi, DV, DV * 128, false);
-            if constexpr (SPLIT) {
-                mma_pass_ts(d, tbase + A_HI, vt_lo, DV, DV * 128, true);
-                mma_pass_ts(d, tbase + A_LO, vt_hi, DV, DV * 128, true);
-            }
-            mma_commit(BAR_M);
+            const uint32_t d = tbase + 256u * b;
+            const unsigned char *a0 = land + b * Sm::L, *b0 = bimg + b * Sm::BI;
+#pragma unroll 1
+            for (int pl = 0; pl < NP; ++pl)
+#pragma unroll 1
+                for (int s = 0; s < kKSteps; ++s)
+                    mma_ss(0u, d, sdesc_mn_sw128(smem_addr(a0 + pl * Sm::G + 2048 * s), Sm::BLK),
+                           sdesc_mn_sw128(smem_addr(b0 + 2048 * s), Sm::BLK), id, (pl > 0 || s > 0) ? 1u : 0u);
+            mma_commit(smem_addr(bar + 2 + b));
         }
         __syncwarp();
         ++nm;
-        if (j > 0) take(it - 1, db ^ 1, ok);   // the previous chunk, while this chunk's MMA runs
-        fence_before_sync();
-        ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
-        fence_after_sync();
+        if (j > 0) {   // the previous chunk: its landing buffer takes chunk j + 1, its accumulator goes out
+            const bool okm = mbar_wait(smem_addr(bar + 2 + (b ^ 1)), (uint32_t)(((j - 1) >> 1) & 1));
+            okp = okp && okm;
+            fence_after_sync();
+            if (tid == 0 && okm && it + 1 < it1) {
+                load(it + 1, b ^ 1);
+                pend[b ^ 1] = true;
+                ph_l[b ^ 1] = (uint32_t)(((j + 1) >> 1) & 1);
+            }
+            take(it - 1, b ^ 1, okm);
+        }
     }
-    // the last chunk, once its MMA is done (or the MMA in flight after a failure)
+    // the last chunk issued, once its MMA is done (chains complete in order, so this also
+    // covers every earlier one after a failure)
     if (nm > 0) {
-        const bool okm = mbar_wait(BAR_M, (uint32_t)((nm - 1) & 1));
+        const int jl = nm - 1, bl = jl & 1;
+        const bool okm = mbar_wait(smem_addr(bar + 2 + bl), (uint32_t)((jl >> 1) & 1));
         fence_after_sync();
-        ok = __syncthreads_and(ok && okm) != 0;
-        if (ok) take(it0 + nm - 1, (nm - 1) & 1, true);
+        take(it0 + jl, bl, ok && okm);
     }
-    // after a failed wait: let a landing in flight arrive before the shared memory is released
-    if (tid == 0 && pend_l) (void)mbar_wait(BAR_L, ph_l);
+    // after a failed wait: let the landings in flight arrive before the shared memory is released
+    if (tid == 0)
+        for (int b = 0; b < 2; ++b)
+            if (pend[b]) (void)mbar_wait(smem_addr(bar + b), ph_l[b]);
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 512);
@@ -669,16 +707,13 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
     StateMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
     const uint16_t *k16 = static_cast<const uint16_t *>(gk);
-    if (!make_tma_2d(&maps.gk[0], k16, true, rows, kK, kC) || !make_tma_2d(&maps.v, v, dm.v_bf16, rows, DV, kC))
-        return cudaErrorInvalidValue;
-    if (SPLIT) {
-        if (!make_tma_2d(&maps.gk[1], k16 + (long long)rows * kK, true, rows, kK, kC)) return cudaErrorInvalidValue;
-    } else {
-        maps.gk[1] = maps.gk[0];
-    }
+    for (int pl = 0; pl < (SPLIT ? 2 : 1); ++pl)
+        if (!make_tma_3d(&maps.gk[pl], k16 + pl * (long long)rows * kK, true, kK, dm.N, dm.BH(), kC))
+            return cudaErrorInvalidValue;
+    if (!SPLIT) maps.gk[1] = maps.gk[0];
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
-    k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, dm.v_bf16,
+    k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, v, dm.v_bf16,
                                                                    partial);
     return cudaGetLastError();
 }

@@ -49,12 +49,28 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  The operand is
+// stored as blocks of 64 MN-elements (16-bit) by K rows of 128 bytes; groups of 8
+// rows along K are 1024 bytes apart and the blocks along MN are `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16; // leading byte offset: MN block pitch
+    d |= (uint64_t)(1024u >> 4) << 32;          // stride byte offset: 8-row group pitch along K
+    d |= (uint64_t)1u << 46;                    // descriptor version
+    d |= (uint64_t)2u << 61;                    // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor: D fp32, A/B of format `fmt` (0 f16, 1 bf16, 2 tf32), both K-major.
 __host__ __device__ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t fmt)
 {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 constexpr uint32_t kFmtBF16 = 1, kFmtTF32 = 2;
+// Instruction descriptor bits: A, B read MN-major (transposed) instead of K-major.
+constexpr uint32_t kAMajorMN = 1u << 15, kBMajorMN = 1u << 16;
 
 // ---- TMEM allocation (executed by one full warp) ----
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
