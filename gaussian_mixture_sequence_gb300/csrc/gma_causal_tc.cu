@@ -53,16 +53,6 @@ __device__ __forceinline__ float bf(uint32_t u) { return __uint_as_float(u << 16
 // tile of n rows whose 128-byte atom columns lie bstride bytes apart.  A: TMEM
 // columns from a_col (two bf16 per column), or a K-major SW128 bf16 tile of
 // 128 rows in shared memory (atom columns astride apart).
-__device__ __forceinline__ void mma_pass_ts(uint32_t d, uint32_t a_col, const unsigned char *b, uint32_t n,
-                                            uint32_t bstride, bool accumulate)
-{
-    const uint32_t id = idesc(128, n, kFmtBF16);
-#pragma unroll 1
-    for (int kk = 0; kk < kKSteps; ++kk) {
-        const uint32_t kb = kk * 32, boff = (kb >> 7) * bstride + (kb & 127);
-        mma_ts(0u, d, a_col + kk * 8, sdesc_sw128(smem_addr(b + boff)), id, (accumulate || kk > 0) ? 1u : 0u);
-    }
-}
 __device__ __forceinline__ void mma_pass_ss(uint32_t d, const unsigned char *a, uint32_t astride,
                                             const unsigned char *b, uint32_t n, uint32_t bstride, bool accumulate)
 {
@@ -406,11 +396,13 @@ __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const floa
 // straight from shared memory.  Every operand plane arrives by TMA:
 //   B images (hi, lo) <- Gk planes (rows 0 .. C-1), memory planes (rows C ..)
 //   A images (hi, lo) <- Gq planes
-// Then P_m, split by threads, goes to TMEM as the A operand of U += P_m V, and
-// the Vt^T rows take V^T (split by threads from registers loaded while the
-// tensor core works).  The next item's Gamma tiles are fetched once every
-// thread is past its reads of the A images, its memory once U += P_m V is done.
-// The output tile is staged in shared memory and leaves by TMA stores.
+// Then P_m, split by threads, goes to TMEM as the A operand of P_m [V_hi | V_lo]:
+// V, read with row-contiguous loads while the tensor core works, is split by
+// threads into token-major bf16 images in the staging tile, the B operand
+// (MN-major), and the two column halves of the product add up to
+// (P_hi + P_lo)(V_hi + V_lo).  The next item's Gamma tiles and memory are
+// fetched once every thread is past its reads of the A images and of Z.  The
+// output tile is staged in shared memory and leaves by TMA stores.
 constexpr int kOutThreads = 512;
 
 template <bool SPLIT, int DV>
@@ -428,7 +420,6 @@ struct OutMaps {
     CUtensorMap gq[2], gk[2];   // hi / lo planes of the responsibilities
     CUtensorMap s;              // memory blocks in operand form, as rows of 256 bytes
     CUtensorMap o;              // output [slices][N][d_v], boxes of 64 rows x 32 columns
-    CUtensorMap v;              // V [slices][N][d_v], boxes of C rows x 128 bytes (causal form)
 };
 
 // CAUSAL = false gives the bidirectional read: U = Gamma_Q [Vt | Z] with the
@@ -436,12 +427,14 @@ struct OutMaps {
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
-                   bool v_bf16, const float *__restrict__ zsrc, float *__restrict__ out)
+                   const void *__restrict__ v, bool v_bf16, const float *__restrict__ zsrc, float *__restrict__ out)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
     static_assert(OutSmem<SPLIT, DV>::bytes <= 232448, "shared memory of one CTA");
-    constexpr int VPER = (kC * DV / 4) / kOutThreads;       // float4 of V per thread
+    constexpr int F4 = DV / 4;                              // groups of four in a row of V
+    constexpr int VPER = kC * F4 / kOutThreads;             // groups of V per thread
+    constexpr int NBV = NP * DV / 64;                       // 64-column blocks of the V images
     constexpr uint32_t AS = Sm::ATOM, PART = Sm::PART;
     constexpr int SROWS = 2 * DV + 2;                       // 256-byte rows of a memory block
     extern __shared__ unsigned char sm_raw[];
@@ -451,8 +444,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
     float *z_s = reinterpret_cast<float *>(os + Sm::OUT);          // [128] Z of the carried memory
     float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [5]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [4]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -461,9 +454,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const long long per = (items + gridDim.x - 1) / gridDim.x;
     const long long it0 = (long long)blockIdx.x * per;
     const long long it1 = it0 + per < items ? it0 + per : items;
-    constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC;
+    constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV;
+    static_assert(D_PV + NBV * 64 <= 512, "TMEM columns");
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3), BAR_VL = smem_addr(bar + 4);
+                   BAR_V = smem_addr(bar + 3);
     const long long SZ = (long long)kK * DV + kK;
 
     // block of the carried memory read by item it
@@ -491,10 +485,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tmem_relinquish();
     }
     // loads in flight that the loop has not waited for (thread 0's record)
-    bool pend_g = false, pend_s = false, pend_v = false;
-    uint32_t ph_g = 0, ph_s = 0, ph_v = 0;
+    bool pend_g = false, pend_s = false;
+    uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0);
@@ -515,21 +509,34 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         const int c0 = (int)(it % nblk) * kC;
         const int nr = min(kC, N - c0);
         const bool more = it + 1 < it1;
-        if (CAUSAL && tid == 0) {
-            // V of this chunk lands in the output staging tile once the previous output tile has
-            // left it (the threads' writes of that tile were fenced before the last barrier)
-            bulk_wait_read();
-            mbar_expect_tx(BAR_VL, (uint32_t)(kC * DV * (v_bf16 ? 2 : 4)));
-            for (int a = 0; a < DV * (v_bf16 ? 2 : 4) / 128; ++a)
-                tma_load_3d(smem_addr(os + a * kC * 128), &maps.v, a * (v_bf16 ? 64 : 32), c0, (int)bh, BAR_VL);
-            pend_v = true;
-            ph_v = ph;
+        // V of this chunk as raw words (fp32, or bf16 pairs in .x and .y), F4 consecutive threads
+        // to a row, in flight while the tensor core works
+        uint4 vr[CAUSAL ? VPER : 1];
+        if constexpr (CAUSAL) {
+            const long long rowbase = bh * N + c0;
+#pragma unroll
+            for (int u = 0; u < VPER; ++u) {
+                const int f = tid + u * kOutThreads, j = f / F4, c4 = 4 * (f % F4);
+                vr[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (j < nr) {
+                    if (v_bf16) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(v) + (rowbase + j) * DV + c4);
+                        vr[u].x = w.x;
+                        vr[u].y = w.y;
+                    } else {
+                        vr[u] = *reinterpret_cast<const uint4 *>(static_cast<const float *>(v) + (rowbase + j) * DV + c4);
+                    }
+                }
+            }
         }
         const bool ok_g = mbar_wait(BAR_G, ph), ok_s = mbar_wait(BAR_S, ph);
         ok = ok && ok_g && ok_s;
         if (tid == 0) {   // a load whose wait gave up is still in flight
             pend_g = pend_g && !ok_g;
             pend_s = pend_s && !ok_s;
+            // the previous output tile has left the staging tile, which takes the V images of
+            // this chunk once [P | U] is done (the other threads know it from that completion)
+            if (CAUSAL) bulk_wait_read();
             // [P | U] = Gq [Gk ; Vt^T]^T  (bidirectional read: U = Gq Vt)
             const uint32_t b0 = CAUSAL ? 0u : PART;
             const uint32_t d0 = CAUSAL ? D_P : D_U, nb = CAUSAL ? kC + DV : DV;
@@ -562,6 +569,27 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         ok = mbar_wait(BAR_M, ph) && ok;
         fence_after_sync();
         if constexpr (CAUSAL) {
+            // V into token-major images in the staging tile, the B operand (MN-major) of
+            // U += P_m V: hi plane in columns [0, d_v), lo plane in [d_v, 2 d_v)
+#pragma unroll
+            for (int u = 0; u < VPER; ++u) {
+                const int f = tid + u * kOutThreads, j = f / F4, c4 = 4 * (f % F4);
+                const float x[4] = {v_bf16 ? __uint_as_float(vr[u].x << 16) : __uint_as_float(vr[u].x),
+                                    v_bf16 ? __uint_as_float(vr[u].x & 0xffff0000u) : __uint_as_float(vr[u].y),
+                                    v_bf16 ? __uint_as_float(vr[u].y << 16) : __uint_as_float(vr[u].z),
+                                    v_bf16 ? __uint_as_float(vr[u].y & 0xffff0000u) : __uint_as_float(vr[u].w)};
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    __nv_bfloat16 h0, l0, h1, l1;
+                    split_bf16(x[2 * e], h0, l0);
+                    split_bf16(x[2 * e + 1], h1, l1);
+                    hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                    lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                *reinterpret_cast<uint2 *>(os + sw128_offset(j, c4, kC, 2)) = make_uint2(hw[0], hw[1]);
+                if (SPLIT) *reinterpret_cast<uint2 *>(os + sw128_offset(j, DV + c4, kC, 2)) = make_uint2(lw[0], lw[1]);
+            }
             // P_m = P with j > i zeroed, split, is the A operand of U += P_m V; the row sums
             // of the split values on CUDA cores
             {
@@ -579,62 +607,33 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 }
                 part[(4 + g) * kK + i] = put_a32<SPLIT>(tbase, lane0, A_PM_HI, A_PM_LO, 32 * g, x);
             }
-            // V^T (element (c, j)) from the landing tile into the Vt^T rows of the B images;
-            // lanes run over tokens
-            {
-                const bool ok_v = mbar_wait(BAR_VL, ph);
-                ok = ok && ok_v;
-                if (tid == 0) pend_v = !ok_v;
-            }
-#pragma unroll
-            for (int u = 0; u < VPER; ++u) {
-                const int f = tid + u * kOutThreads, j = f % kC, c4 = 4 * (f / kC);
-                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < nr) {
-                    if (v_bf16) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(os + sw128_offset(j, c4, kC, 2));
-                        t = make_float4(bf(w.x & 0xffffu), __uint_as_float(w.x & 0xffff0000u), bf(w.y & 0xffffu),
-                                        __uint_as_float(w.y & 0xffff0000u));
-                    } else {
-                        t = *reinterpret_cast<const float4 *>(os + sw128_offset(j, c4, kC, 4));
-                    }
-                }
-                const float e4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    put_split<SPLIT>(tb0, tb1, (j >> 6) * AS + PART + sw128_offset(c4 + e, j & 63, DV, 2), e4[e]);
-            }
             tmem_wait_st();
             fence_proxy_async();
             fence_before_sync();
-            __syncthreads();   // every thread is past its reads of the A images and of V
+            __syncthreads();   // every thread is past its reads of the A images and of Z
             fence_after_sync();
             if (tid == 0) {
-                // the Gamma rows and A images are free: the next item's tiles (the threads only
-                // read them; the writes of V^T were fenced before the barrier)
+                // B (Gamma_K and carried-memory rows), the A images and Z are free: the next
+                // item's tiles and memory (the threads only read them)
                 if (more && ok) {
                     load_gamma(it + 1);
-                    pend_g = true;
-                    ph_g = ph ^ 1u;
+                    load_memory(it + 1);
+                    pend_g = pend_s = true;
+                    ph_g = ph_s = ph ^ 1u;
                 }
-                // U += P_m V
-                mma_pass_ts(tbase + D_U, tbase + A_PM_HI, tb0 + PART, DV, AS, true);
-                if constexpr (SPLIT) {
-                    mma_pass_ts(tbase + D_U, tbase + A_PM_HI, tb1 + PART, DV, AS, true);
-                    mma_pass_ts(tbase + D_U, tbase + A_PM_LO, tb0 + PART, DV, AS, true);
-                }
+                // U' = P_m [V_hi | V_lo] from both planes of P_m: (P_hi + P_lo)(V_hi + V_lo) in two halves
+                const uint32_t idv = idesc(128, NBV * 64, kFmtBF16) | kBMajorMN;
+#pragma unroll 1
+                for (int pl = 0; pl < NP; ++pl)
+#pragma unroll 1
+                    for (int s = 0; s < kKSteps; ++s)
+                        mma_ts(0u, tbase + D_PV, tbase + (pl ? A_PM_LO : A_PM_HI) + 8 * s,
+                               sdesc_mn_sw128(smem_addr(os + 2048 * s), kC * 128), idv, (pl > 0 || s > 0) ? 1u : 0u);
                 mma_commit(BAR_V);
             }
             __syncwarp();
             ok = mbar_wait(BAR_V, ph) && ok;
             fence_after_sync();
-            // the Vt^T rows are free: the next item's memory (the threads' writes of V^T were
-            // fenced before the MMA that read them, which has completed)
-            if (tid == 0 && more && ok) {
-                load_memory(it + 1);
-                pend_s = true;
-                ph_s = ph ^ 1u;
-            }
         } else {
             fence_before_sync();
             if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
@@ -656,15 +655,29 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < DV / 64; ++cb) {
             const int c = g * (DV / 4) + 16 * cb;
+            // U = Gamma_Q Vt_prev (+ the halves of P_m [V_hi | V_lo])
             uint32_t r[16];
+            float y[16];
             tmem_ld16(tmem_at(tbase, lane0, D_U + c), r);
-            tmem_wait_ld();
+            if constexpr (CAUSAL) {
+                uint32_t a[16], b2[16];
+                tmem_ld16(tmem_at(tbase, lane0, D_PV + c), a);
+                if constexpr (SPLIT) tmem_ld16(tmem_at(tbase, lane0, D_PV + DV + c), b2);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    y[q] = __uint_as_float(r[q]) +
+                           (SPLIT ? __uint_as_float(a[q]) + __uint_as_float(b2[q]) : __uint_as_float(a[q]));
+            } else {
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) y[q] = __uint_as_float(r[q]);
+            }
             unsigned char *ob = os + ((i >> 6) * (DV / 32) + (c >> 5)) * 8192 + (i & 63) * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 o4 = ok ? make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                                                   __uint_as_float(r[4 * q + 2]) * inv,
-                                                   __uint_as_float(r[4 * q + 3]) * inv)
+                const float4 o4 = ok ? make_float4(y[4 * q] * inv, y[4 * q + 1] * inv, y[4 * q + 2] * inv,
+                                                   y[4 * q + 3] * inv)
                                      : make_float4(qnan, qnan, qnan, qnan);
                 *reinterpret_cast<float4 *>(ob + ((((c & 31) >> 2) + q) ^ (i & 7)) * 16) = o4;
             }
@@ -683,7 +696,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // after a failed wait: let the copies still in flight land before the shared memory is released
     if (tid == 0) {
         if (pend_g) (void)mbar_wait(BAR_G, ph_g);
-        if (pend_v) (void)mbar_wait(BAR_VL, ph_v);
         if (pend_s) (void)mbar_wait(BAR_S, ph_s);
         bulk_wait_all();
     }
@@ -741,13 +753,11 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     // memory blocks in operand form: rows of 256 bytes (hi plane, lo plane, Z), d_v rows per box
     ok = ok && make_tma_2d(&maps.s, mem, true, blocks * (2 * DV + 2), kK, DV) &&
          make_tma_3d(&maps.o, out, false, DV, dm.N, dm.BH(), 64);
-    if (CAUSAL) ok = ok && make_tma_3d(&maps.v, v, dm.v_bf16, DV, dm.N, dm.BH(), kC);
-    else maps.v = maps.o;
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, dm.eps, dm.v_bf16, reinterpret_cast<const float *>(mem), out);
+        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, reinterpret_cast<const float *>(mem), out);
     return cudaGetLastError();
 }
 
