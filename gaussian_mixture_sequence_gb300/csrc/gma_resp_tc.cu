@@ -45,6 +45,7 @@ using namespace tc;
 constexpr int kPK = 128, kPD = 64, kPDP = kPD / 2;
 constexpr int kPThreads = 512, kPRows = 128;
 constexpr int kPGroups = 2, kPGThreads = kPThreads / kPGroups;
+constexpr int kPRun = 16;                      // tiles of a slice taken in a row
 constexpr int kPStride = kPDP + 1;            // padded float4 row of exact parameters
 constexpr float kPT = 30.f;                   // log-joint window kept exactly
 constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulation bound
@@ -70,17 +71,7 @@ __device__ __forceinline__ void group_sync(int g)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(kPGThreads) : "memory");
 }
-// Named barrier of one group that also returns the AND (or the OR) of `pred` over its threads.
-__device__ __forceinline__ bool group_and(int g, bool pred)
-{
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                 "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r)
-                 : "r"((uint32_t)pred), "r"(1 + g), "r"(kPGThreads)
-                 : "memory");
-    return r != 0;
-}
+// Named barrier of one group that also returns the OR of `pred` over its threads.
 __device__ __forceinline__ bool group_or(int g, bool pred)
 {
     uint32_t r;
@@ -155,15 +146,15 @@ __global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ 
     }
 }
 
-// Persistent: CTA b handles the work items [b * per, (b + 1) * per) of the
-// list (slice, tile of 128 rows), slice by slice; within a slice group g takes
-// the items s + g, s + g + 2, ...  The output tile is assembled in shared memory
-// and written by TMA stores that stop at the slice's last row.
+// Persistent: CTA b handles the slots [b * per, (b + 1) * per) of the work order
+// (runs of tiles of 128 rows, below), run by run; within a run group g takes the
+// slots s + g, s + g + 2, ...  The output tile is assembled in shared memory and
+// written by TMA stores that stop at the slice's last row.
 __global__ void __launch_bounds__(kPThreads, 1)
     k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
                   const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int BH, bool x_bf16,
                   const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
-                  const float *__restrict__ cimg, int layout)
+                  const float *__restrict__ cimg, int layout, int pstride)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -188,21 +179,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     float4 *pw_s = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(bar) + 64) + warp * kPDP;
     const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1 + grp), BAR_M = smem_addr(bar + 3 + grp);
 
+    // Work order: runs of kPRun consecutive tiles of one slice; run r is run r / BH of
+    // slice (r % BH) * pstride % BH (pstride coprime with BH), so that consecutive runs
+    // come from slices far apart and a CTA's range mixes heads of unequal cost.  A
+    // slot v of this order is tile (v % kPRun) of run v / kPRun; slots past a slice's
+    // last tile are empty and skipped.
     const int tps = (N + kPRows - 1) / kPRows;    // tiles per slice
-    const long long items = (long long)BH * tps;
-    const long long per = (items + gridDim.x - 1) / gridDim.x;
+    const int rps = (tps + kPRun - 1) / kPRun;    // runs per slice
+    const long long slots = (long long)BH * rps * kPRun;
+    const long long per = (slots + gridDim.x - 1) / gridDim.x;
     const long long it0 = (long long)blockIdx.x * per;
-    const long long it1 = it0 + per < items ? it0 + per : items;
+    const long long it1 = it0 + per < slots ? it0 + per : slots;
+    auto run_slice = [&](long long r) { return (int)((r % BH) * (long long)pstride % BH); };
+    auto run_tiles = [&](long long r) { return min(kPRun, tps - (int)(r / BH) * kPRun); };   // filled slots
+    auto tile_of = [&](long long v) { return (int)((v / kPRun) / BH) * kPRun + (int)(v % kPRun); };
+    auto next_filled = [&](long long v) {   // the first filled slot at or after v
+        const long long r = v / kPRun;
+        return (v % kPRun) < run_tiles(r) ? v : (r + 1) * kPRun;
+    };
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kPRows * kPK * 2;   // split: the lo plane's tile follows the hi plane's
 
-    // one thread: TMA of item it's rows, counted on the barrier of the group that takes it
-    // (group 0 takes a slice's first item in the range, then the groups alternate)
+    // one thread: TMA of slot it's rows, counted on the barrier of the group that takes it
+    // (group 0 takes a run's first slot in the range, then the groups alternate)
     auto load_x = [&](long long it) {
-        const int bh = (int)(it / tps), t = (int)(it % tps);
-        const long long first = max((it / tps) * tps, it0);
+        const int bh = run_slice(it / kPRun), t = tile_of(it);
+        const long long first = max((it / kPRun) * kPRun, it0);
         const uint32_t bx = smem_addr(bar + 1 + (int)((it - first) & 1));
         mbar_expect_tx(bx, xbytes);
         tma_load_3d(smem_addr(xb), &xmap, 0, t * kPRows, bh, bx);
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        if (it0 < it1) load_x(it0);
+        if (next_filled(it0) < it1) load_x(next_filled(it0));
     }
     fence_before_sync();
     __syncthreads();
@@ -226,9 +230,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     int head = -1, nimg = 0, j = 0;   // j: this group's items so far (its MMA and routing-tile phases)
 
-    for (long long s0 = it0; s0 < it1 && ok;) {
-        const long long s1 = min(it1, (s0 / tps + 1) * tps);   // this slice's items in the range
-        const int hd = (int)((s0 / tps) % H);
+    for (long long s0 = next_filled(it0); s0 < it1 && ok;) {
+        const long long s1 = min(it1, (s0 / kPRun) * kPRun + run_tiles(s0 / kPRun));   // this run's tiles in the range
+        const int hd = run_slice(s0 / kPRun) % H;
         if (hd != head) {   // both groups are done with the previous head: (re)load the images
             head = hd;
             fence_before_sync();
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         const float4 *ph = pimg + (long long)head * kPK * kPStride;
         for (long long it = s0 + grp; it < s1; it += kPGroups, ++j) {
-            const int bh = (int)(it / tps), t = (int)(it % tps);
+            const int bh = run_slice(it / kPRun), t = tile_of(it);
             // this group's routing tiles land in order on its own barrier; the consumer of
             // tile n fetches tile n + 1, so a group's next tile is never fetched before it
             // has consumed the previous one (its barrier runs at most one phase ahead)
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             group_sync(grp);   // the routing tile has been read: the next item's tile may land in it
-            if (gt == 0 && it + 1 < it1) load_x(it + 1);   // (the threads only read it: no proxy fence)
+            if (gt == 0 && next_filled(it + 1) < it1) load_x(next_filled(it + 1));   // (read only: no proxy fence)
             float2 s2v = make_float2(0.f, 0.f);
 #pragma unroll
             for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 bulk_commit();
             }
         }
-        s0 = s1;
+        s0 = next_filled(s1);
         ok = __syncthreads_and(ok) != 0;   // both groups leave the loop together
     }
     // after a failed wait a routing tile may still be in flight for either group: let it land
@@ -570,8 +574,13 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
     }
     const long long items = dm.BH() * ((dm.N + kPRows - 1) / kPRows);
     const int grid = (int)(items < sm_count() ? items : sm_count());
-    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, (int)dm.BH(), dm.x_bf16, img.w,
-                                                 img.p, img.c, layout);
+    // run order stride: odd, near a fifth of the slices, coprime with their number
+    const int nsl = (int)dm.BH();
+    int pstride = (nsl / 5) | 1;
+    auto gcd = [](int a, int b) { while (b) { const int t = a % b; a = b; b = t; } return a; };
+    while (gcd(pstride, nsl) != 1) pstride += 2;
+    k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, nsl, dm.x_bf16, img.w, img.p,
+                                                 img.c, layout, pstride);
     return cudaGetLastError();
 }
 
