@@ -239,7 +239,7 @@ def dist_env():
 # The source file holding each stage's kernel; its hash (with the shared headers)
 # keys the committed DRAM counters, so a changed kernel reports no traffic.
 KERNEL_SOURCE = {
-    "prep_params": "gma_resp.cu", "prep_bound": "gma_resp_tc.cu",
+    "prep_params": "gma_resp.cu", "prep": "gma_resp_tc.cu",
     "chunk_state_tc": "gma_causal_tc.cu", "chunk_out_tc": "gma_causal_tc.cu", "bidir_read_tc": "gma_causal_tc.cu",
     "block_state": "gma_mix.cu", "state_scan": "gma_mix.cu", "state_reduce": "gma_mix.cu",
     "chunk_out": "gma_mix.cu", "bidir_read": "gma_mix.cu", "decode": "gma_decode.cu",

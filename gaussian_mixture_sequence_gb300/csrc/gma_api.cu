@@ -205,8 +205,8 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     float4 *prm = at<float4>(ws, wp.prm);
     float *cst = at<float>(ws, wp.cst);
     const PrunedImages img = images(ws, wp);
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    if (wp.pruned) GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+    if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
+    else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st));
     return GMA_OK;
 }
@@ -270,11 +270,12 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
     float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
     const PrunedImages img = images(ws, wp);
     const PrunedImages *imgp = wp.pruned ? &img : nullptr;
-    GMA_CUDA(mk.mark("prep_params"));
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     if (wp.pruned) {
-        GMA_CUDA(mk.mark("prep_bound"));
-        GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+        GMA_CUDA(mk.mark("prep"));
+        GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
+    } else {
+        GMA_CUDA(mk.mark("prep_params"));
+        GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));
@@ -361,11 +362,12 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
     float *partial = at<float>(ws, wp.partial);
     const PrunedImages img = images(ws, wp);
     const PrunedImages *imgp = wp.pruned ? &img : nullptr;
-    GMA_CUDA(mk.mark("prep_params"));
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     if (wp.pruned) {
-        GMA_CUDA(mk.mark("prep_bound"));
-        GMA_CUDA(launch_prep_pruned(dm, prm, cst, img, st));
+        GMA_CUDA(mk.mark("prep"));
+        GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
+    } else {
+        GMA_CUDA(mk.mark("prep_params"));
+        GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));

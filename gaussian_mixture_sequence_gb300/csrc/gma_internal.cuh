@@ -126,8 +126,10 @@ constexpr size_t kPrunedWBytes = 32768, kPrunedPBytes = 128 * 33 * 16, kPrunedCB
 
 // Responsibilities for K = 128, d_route = 64 with a tensor-core bound (gma_resp_tc.cu).
 bool resp_pruned_applies(const Dims &dm);
-cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages &img,
-                               cudaStream_t st);
+// The per-head parameters (as launch_prep writes them) and the routing images in one
+// kernel, for the shapes resp_pruned_applies accepts.
+cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, float *cst, const PrunedImages &img,
+                            cudaStream_t st);
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
                                int layout, cudaStream_t st);
 

@@ -25,8 +25,8 @@
 // overlap the other's arithmetic.  In a group, the two warps 4h + w' share the
 // TMEM lanes 32 w' .. +31 (one row each) and take component half h.  The
 // per-head bound matrix and constants are built once per call by
-// k_prep_pruned and bulk-copied into shared memory (both groups work on the
-// same head: the CTA's range is walked slice by slice); the exact parameters,
+// k_prep_all and bulk-copied into shared memory (both groups work on the
+// same head: the CTA's range is walked run by run); the exact parameters,
 // needed only by rows with two or more kept components, are read from global
 // memory (L2-resident).  Routing tiles arrive by TMA into one buffer that the
 // groups consume in item order (the consumer of tile n fetches tile n + 1);
@@ -90,59 +90,107 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 }
 
 
-// One CTA per head: the bound matrix W (bf16, in the swizzled B-operand
-// layout), the exact parameters with padded rows, and c, c', A, M.
-__global__ void __launch_bounds__(256) k_prep_pruned(const float4 *__restrict__ prm, const float *__restrict__ cst,
-                                                     unsigned char *__restrict__ wimg, float4 *__restrict__ pimg,
-                                                     float *__restrict__ cimg)
+// The per-head parameters and the images of the bounded routing in one pass
+// (K = 128, d = 64): one CTA per head, four threads per component (16 features each).
+//   prm[k][dp] = {s_2dp, s_2dp+1, -mu_2dp s_2dp, -mu_2dp+1 s_2dp+1}, s = 1/sigma, sigma^2 = softplus(r)
+//   cst[k]     = log pi_k - 1/2 sum_d log sigma^2_kd, pi = softmax(logit_pi)
+// and W, the padded parameters and c, c', A, M as the routing kernel reads them.
+constexpr int kPrepAllThreads = 4 * kPK;
+
+__device__ __forceinline__ float softplus_f(float r) { return fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))); }
+
+__global__ void __launch_bounds__(kPrepAllThreads)
+    k_prep_all(const float *__restrict__ mu, const float *__restrict__ var_raw, const float *__restrict__ logit_pi,
+               float4 *__restrict__ prm, float *__restrict__ cst, unsigned char *__restrict__ wimg,
+               float4 *__restrict__ pimg, float *__restrict__ cimg)
 {
-    const int h = blockIdx.x, tid = blockIdx.y * 256 + threadIdx.x, nthr = gridDim.y * 256;
-    const float4 *ph = prm + (long long)h * kPK * kPDP;
-    unsigned char *wh = wimg + (long long)h * kPrunedWBytes;
-    float4 *pp = pimg + (long long)h * kPK * kPStride;
-    for (int e = tid; e < kPK * kPStride; e += nthr) {
-        const int k = e / kPStride, dp = e % kPStride;
-        pp[e] = dp < kPDP ? ph[k * kPDP + dp] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int e = tid; e < kPK * kPDP; e += nthr) {
-        const int k = e / kPDP, dp = e % kPDP;
-        const float4 p = ph[e];
-        const float s[2] = {p.x, p.y}, nm[2] = {p.z, p.w};   // 1/sigma, -mu/sigma
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int f = 2 * dp + j;
-            *reinterpret_cast<__nv_bfloat16 *>(wh + sw128_offset(k, f, kPK, 2)) =
-                __float2bfloat16_rn(-0.5f * s[j] * s[j]);
-            *reinterpret_cast<__nv_bfloat16 *>(wh + sw128_offset(k, kPD + f, kPK, 2)) =
-                __float2bfloat16_rn(-s[j] * nm[j]);
-        }
-    }
-    if (blockIdx.y != 0) return;
-    __shared__ float red[2][kPK];
-    float *ch = cimg + (long long)h * 4 * kPK;
-    if (tid < kPK) {
-        float amu2 = 0.f, amax = 0.f, mmax = 0.f;
-        for (int dp = 0; dp < kPDP; ++dp) {
-            const float4 p = ph[tid * kPDP + dp];
-            amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
-            amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
-            mmax = fmaxf(mmax, fmaxf(fabsf(p.x * p.z), fabsf(p.y * p.w)));
-        }
-        const float c = cst[(long long)h * kPK + tid];
-        ch[tid] = c;
-        ch[kPK + tid] = c - 0.5f * amu2;
-        red[0][tid] = amax;
-        red[1][tid] = mmax;
+    constexpr int NW = kPrepAllThreads / 32;
+    __shared__ float red[4][NW];
+    __shared__ float lmax_s, lse_s, amax_s, mmax_s;
+    const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = tid >> 2, part = tid & 3;   // component, quarter of its features
+    const float *l = logit_pi + (long long)h * kPK;
+
+    // log-sum-exp of the head's logits (thread k < K holds logit k)
+    const float lv = tid < kPK ? l[tid] : -FLT_MAX;
+    float t = lv;
+    for (int o = 16; o; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (lane == 0) red[0][warp] = t;
+    __syncthreads();
+    if (warp == 0) {
+        float u = lane < NW ? red[0][lane] : -FLT_MAX;
+        for (int o = 16; o; o >>= 1) u = fmaxf(u, __shfl_xor_sync(0xffffffffu, u, o));
+        if (lane == 0) lmax_s = u;
     }
     __syncthreads();
-    if (tid < kPK) {   // head-wide maxima A and M, stored in every slot
-        float a = 0.f, m = 0.f;
-        for (int k = 0; k < kPK; ++k) {
-            a = fmaxf(a, red[0][k]);
-            m = fmaxf(m, red[1][k]);
+    const float lmax = lmax_s;
+    t = tid < kPK ? expf(lv - lmax) : 0.f;
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) red[1][warp] = t;
+
+    // this thread's 16 features of component k: packed parameters, W, sums and maxima
+    const long long row = (long long)h * kPK + k;
+    const float *vr = var_raw + row * kPD + 16 * part, *mr = mu + row * kPD + 16 * part;
+    float4 *pr = prm + row * kPDP + 8 * part, *pp = pimg + row * kPStride + 8 * part;
+    unsigned char *wh = wimg + (long long)h * kPrunedWBytes;
+    float lsum = 0.f, amu2 = 0.f, amax = 0.f, mmax = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int f = 16 * part + 2 * q;
+        const float2 r = *reinterpret_cast<const float2 *>(vr + 2 * q);
+        const float2 u = *reinterpret_cast<const float2 *>(mr + 2 * q);
+        const float v0 = softplus_f(r.x), v1 = softplus_f(r.y);
+        const float s0 = 1.0f / sqrtf(v0), s1 = 1.0f / sqrtf(v1);
+        const float4 p = make_float4(s0, s1, -u.x * s0, -u.y * s1);
+        pr[q] = p;
+        pp[q] = p;
+        lsum += logf(v0) + logf(v1);
+        amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
+        amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
+        mmax = fmaxf(mmax, fmaxf(fabsf(p.x * p.z), fabsf(p.y * p.w)));
+        // W row k: -1/2 s^2 at features f, f + 1 and -s (-mu s) at d + f, d + f + 1
+        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, f, kPK, 2)) = pack2(-0.5f * p.x * p.x, -0.5f * p.y * p.y);
+        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, kPD + f, kPK, 2)) = pack2(-p.x * p.z, -p.y * p.w);
+    }
+    if (part == 3) pp[8] = make_float4(0.f, 0.f, 0.f, 0.f);   // the row's padding word
+    for (int o = 1; o < 4; o <<= 1) {   // the component's four quarters
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        amu2 += __shfl_xor_sync(0xffffffffu, amu2, o);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    }
+    float am = amax, mm = mmax;   // head-wide maxima A, M
+    for (int o = 4; o < 32; o <<= 1) {
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    }
+    if (lane == 0) {
+        red[2][warp] = am;
+        red[3][warp] = mm;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float a = lane < NW ? red[1][lane] : 0.f, b = lane < NW ? red[2][lane] : 0.f, c = lane < NW ? red[3][lane] : 0.f;
+        for (int o = 16; o; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+            c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
         }
-        ch[2 * kPK + tid] = a;
-        ch[3 * kPK + tid] = m;
+        if (lane == 0) {
+            lse_s = lmax + logf(a);
+            amax_s = b;
+            mmax_s = c;
+        }
+    }
+    __syncthreads();
+    if (part == 0) {
+        float *ch = cimg + (long long)h * 4 * kPK;
+        const float c = (l[k] - lse_s) - 0.5f * lsum;
+        cst[row] = c;
+        ch[k] = c;
+        ch[kPK + k] = c - 0.5f * amu2;
+        ch[2 * kPK + k] = amax_s;
+        ch[3 * kPK + k] = mmax_s;
     }
 }
 
@@ -546,10 +594,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 bool resp_pruned_applies(const Dims &dm) { return dm.K == kPK && dm.D == kPD; }
 
-cudaError_t launch_prep_pruned(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages &img,
-                               cudaStream_t st)
+cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, float *cst, const PrunedImages &img,
+                            cudaStream_t st)
 {
-    k_prep_pruned<<<dim3(dm.H, 4), 256, 0, st>>>(prm, cst, img.w, img.p, img.c);
+    if (!resp_pruned_applies(dm)) return cudaErrorInvalidValue;
+    k_prep_all<<<dm.H, kPrepAllThreads, 0, st>>>(p.mu, p.var_raw, p.logit_pi, prm, cst, img.w, img.p, img.c);
     return cudaGetLastError();
 }
 
