@@ -91,11 +91,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 
 
 // The per-head parameters and the images of the bounded routing in one pass
-// (K = 128, d = 64): one CTA per head, four threads per component (16 features each).
+// (K = 128, d = 64): CTA (h, q) takes the 32 components [32 q, 32 q + 32) of head h,
+// 16 threads per component (4 features each).
 //   prm[k][dp] = {s_2dp, s_2dp+1, -mu_2dp s_2dp, -mu_2dp+1 s_2dp+1}, s = 1/sigma, sigma^2 = softplus(r)
 //   cst[k]     = log pi_k - 1/2 sum_d log sigma^2_kd, pi = softmax(logit_pi)
-// and W, the padded parameters and c, c', A, M as the routing kernel reads them.
-constexpr int kPrepAllThreads = 4 * kPK;
+// and W, the padded parameters and c, c', A_k, M_k (the component's largest a = s^2 and
+// |a mu|; the routing kernel takes the head-wide maxima when it loads the images).
+constexpr int kPrepAllThreads = 512, kPrepAllComps = kPrepAllThreads / 16;
 
 __device__ __forceinline__ float softplus_f(float r) { return fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))); }
 
@@ -105,10 +107,10 @@ __global__ void __launch_bounds__(kPrepAllThreads)
                float4 *__restrict__ pimg, float *__restrict__ cimg)
 {
     constexpr int NW = kPrepAllThreads / 32;
-    __shared__ float red[4][NW];
-    __shared__ float lmax_s, lse_s, amax_s, mmax_s;
+    __shared__ float red[2][NW];
+    __shared__ float lmax_s, lse_s;
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int k = tid >> 2, part = tid & 3;   // component, quarter of its features
+    const int k = blockIdx.y * kPrepAllComps + (tid >> 4), part = tid & 15;   // component, features 4 part ..
     const float *l = logit_pi + (long long)h * kPK;
 
     // log-sum-exp of the head's logits (thread k < K holds logit k)
@@ -123,27 +125,31 @@ __global__ void __launch_bounds__(kPrepAllThreads)
         if (lane == 0) lmax_s = u;
     }
     __syncthreads();
-    const float lmax = lmax_s;
-    t = tid < kPK ? expf(lv - lmax) : 0.f;
+    t = tid < kPK ? expf(lv - lmax_s) : 0.f;
     for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     if (lane == 0) red[1][warp] = t;
+    __syncthreads();
+    if (warp == 0) {
+        float u = lane < NW ? red[1][lane] : 0.f;
+        for (int o = 16; o; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+        if (lane == 0) lse_s = lmax_s + logf(u);
+    }
 
-    // this thread's 16 features of component k: packed parameters, W, sums and maxima
+    // this thread's 4 features of component k: packed parameters, W, sums and maxima
     const long long row = (long long)h * kPK + k;
-    const float *vr = var_raw + row * kPD + 16 * part, *mr = mu + row * kPD + 16 * part;
-    float4 *pr = prm + row * kPDP + 8 * part, *pp = pimg + row * kPStride + 8 * part;
+    const float4 r4 = *reinterpret_cast<const float4 *>(var_raw + row * kPD + 4 * part);
+    const float4 u4 = *reinterpret_cast<const float4 *>(mu + row * kPD + 4 * part);
+    const float rv[4] = {r4.x, r4.y, r4.z, r4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
     unsigned char *wh = wimg + (long long)h * kPrunedWBytes;
     float lsum = 0.f, amu2 = 0.f, amax = 0.f, mmax = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int f = 16 * part + 2 * q;
-        const float2 r = *reinterpret_cast<const float2 *>(vr + 2 * q);
-        const float2 u = *reinterpret_cast<const float2 *>(mr + 2 * q);
-        const float v0 = softplus_f(r.x), v1 = softplus_f(r.y);
+    for (int q = 0; q < 2; ++q) {
+        const int f = 4 * part + 2 * q, dp = f / 2;
+        const float v0 = softplus_f(rv[2 * q]), v1 = softplus_f(rv[2 * q + 1]);
         const float s0 = 1.0f / sqrtf(v0), s1 = 1.0f / sqrtf(v1);
-        const float4 p = make_float4(s0, s1, -u.x * s0, -u.y * s1);
-        pr[q] = p;
-        pp[q] = p;
+        const float4 p = make_float4(s0, s1, -uv[2 * q] * s0, -uv[2 * q + 1] * s1);
+        prm[row * kPDP + dp] = p;
+        pimg[row * kPStride + dp] = p;
         lsum += logf(v0) + logf(v1);
         amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
         amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
@@ -152,45 +158,22 @@ __global__ void __launch_bounds__(kPrepAllThreads)
         *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, f, kPK, 2)) = pack2(-0.5f * p.x * p.x, -0.5f * p.y * p.y);
         *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, kPD + f, kPK, 2)) = pack2(-p.x * p.z, -p.y * p.w);
     }
-    if (part == 3) pp[8] = make_float4(0.f, 0.f, 0.f, 0.f);   // the row's padding word
-    for (int o = 1; o < 4; o <<= 1) {   // the component's four quarters
+    if (part == 15) pimg[row * kPStride + kPDP] = make_float4(0.f, 0.f, 0.f, 0.f);   // the row's padding word
+    for (int o = 1; o < 16; o <<= 1) {   // the component's 16 threads
         lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
         amu2 += __shfl_xor_sync(0xffffffffu, amu2, o);
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     }
-    float am = amax, mm = mmax;   // head-wide maxima A, M
-    for (int o = 4; o < 32; o <<= 1) {
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    }
-    if (lane == 0) {
-        red[2][warp] = am;
-        red[3][warp] = mm;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        float a = lane < NW ? red[1][lane] : 0.f, b = lane < NW ? red[2][lane] : 0.f, c = lane < NW ? red[3][lane] : 0.f;
-        for (int o = 16; o; o >>= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, o);
-            b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
-            c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
-        }
-        if (lane == 0) {
-            lse_s = lmax + logf(a);
-            amax_s = b;
-            mmax_s = c;
-        }
-    }
-    __syncthreads();
+    __syncthreads();   // lse_s
     if (part == 0) {
         float *ch = cimg + (long long)h * 4 * kPK;
         const float c = (l[k] - lse_s) - 0.5f * lsum;
         cst[row] = c;
         ch[k] = c;
         ch[kPK + k] = c - 0.5f * amu2;
-        ch[2 * kPK + k] = amax_s;
-        ch[3 * kPK + k] = mmax_s;
+        ch[2 * kPK + k] = amax;
+        ch[3 * kPK + k] = mmax;
     }
 }
 
@@ -293,6 +276,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             ok = mbar_wait(BAR_I, (uint32_t)(nimg & 1)) && ok;
             ++nimg;
+            if (warp == 0) {   // the head-wide maxima A, M of the per-component ones, into slot 0
+                float a = 0.f, m = 0.f;
+#pragma unroll
+                for (int q = 0; q < kPK / 32; ++q) {
+                    a = fmaxf(a, a_s[lane + 32 * q]);
+                    m = fmaxf(m, m_s[lane + 32 * q]);
+                }
+                for (int o = 16; o; o >>= 1) {
+                    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                }
+                if (lane == 0) {
+                    f_s[2 * kPK] = a;
+                    f_s[3 * kPK] = m;
+                }
+            }
+            __syncthreads();
         }
         const float4 *ph = pimg + (long long)head * kPK * kPStride;
         for (long long it = s0 + grp; it < s1; it += kPGroups, ++j) {
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
             for (int g = 0; g < kPDP; ++g) s2v = __ffma2_rn(xr[g], xr[g], s2v);
             const float s2 = s2v.x + s2v.y;
-            // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0])
+            // per-row error bound of the bf16 log-joints (head-wide A = a_s[0], M = m_s[0], reduced
+            // from the per-component values when the images were loaded)
             const float delta = fmaf(kPU, fmaf(0.5f * a_s[0], s2, m_s[0] * 8.f * sqrtf(s2)), 1e-3f);
             // A = [x^2 | x] in bf16: half 0 writes the squares (columns 0..31), half 1 the values (32..63)
 #pragma unroll
@@ -598,7 +599,8 @@ cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, fl
                             cudaStream_t st)
 {
     if (!resp_pruned_applies(dm)) return cudaErrorInvalidValue;
-    k_prep_all<<<dm.H, kPrepAllThreads, 0, st>>>(p.mu, p.var_raw, p.logit_pi, prm, cst, img.w, img.p, img.c);
+    k_prep_all<<<dim3(dm.H, kPK / kPrepAllComps), kPrepAllThreads, 0, st>>>(p.mu, p.var_raw, p.logit_pi, prm, cst,
+                                                                           img.w, img.p, img.c);
     return cudaGetLastError();
 }
 
