@@ -564,6 +564,8 @@ def main():
     # end to end through the plain public entry point: pinned host inputs in, result out, every step
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ne = max(1, min(args.e2e_steps, args.steps))
+    for _ in range(2):   # untimed: the first calls create the copy streams and load the kernels
+        run.e2e_step()
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
