@@ -29,9 +29,15 @@ __device__ __forceinline__ float block_reduce(float v, float *red, bool is_max)
     return r;
 }
 
-template <int DV>
-__global__ void __launch_bounds__(kThreads)
-    k_decode(int H, int D, int K, float eps, const void *__restrict__ qx, const void *__restrict__ kx, bool x_bf16,
+// One CTA per (b, h).  The log-joints of the new token's q and k rows: a warp
+// per component row of parameters at a time (coalesced, shared by both rows);
+// then the two softmaxes; then one pass over the state that updates and reads
+// it, four columns per thread with
+// 16-byte loads and stores (a scalar pass when K is not a multiple of 4, where
+// the slices of the state are not 16-byte aligned).
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads, 6)
+    k_decode(int H, int K, float eps, const void *__restrict__ qx, const void *__restrict__ kx, bool x_bf16,
              const void *__restrict__ v, bool v_bf16, const float4 *__restrict__ prm,
              const float *__restrict__ cst, float *__restrict__ state, float *__restrict__ out)
 {
@@ -42,9 +48,17 @@ __global__ void __launch_bounds__(kThreads)
     float *gq = vv + DV;       // [K]
     float *gk = gq + K;        // [K]
     float *red = gk + K;       // [kThreads]
+    float4 *red4 = reinterpret_cast<float4 *>((reinterpret_cast<uintptr_t>(red + kThreads) + 15) & ~uintptr_t(15));   // [kThreads]
 
     const long long bh = blockIdx.x;
     const int h = (int)(bh % H), tid = threadIdx.x;
+    // the state of this slice: thread t updates column group t % G4 of rows t / G4 + j RP
+    constexpr int G4 = DV / 4, RP = kThreads / G4, U = 4;
+    const bool vec = (K & 3) == 0;   // 16-byte aligned slices
+    const int c4 = tid % G4, r0 = tid / G4;
+    float *st = state + bh * ((long long)K * DV + K);
+    float4 *st4 = reinterpret_cast<float4 *>(st);
+    const int total = K * DV;
     for (int i = tid; i < D; i += kThreads) {
         xq[i] = load_elem(qx, bh * D + i, x_bf16);
         xk[i] = load_elem(kx, bh * D + i, x_bf16);
@@ -52,24 +66,59 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = tid; i < DV; i += kThreads) vv[i] = load_elem(v, bh * DV + i, v_bf16);
     __syncthreads();
 
+    // log-joints -1/2 sum_d ((x_d - mu_d) / sigma_d)^2 + c_k of both rows.  A warp takes a
+    // component's parameter row with consecutive lanes on consecutive words (one coalesced
+    // read serves both rows), and its partial sums meet by shuffles.
+    {
+        constexpr int DP = D / 2;
+        constexpr int LPC = DP < 32 ? DP : 32;   // lanes per component (a power of two)
+        constexpr int CPW = 32 / LPC;            // components per warp and pass
+        constexpr int WPL = DP / LPC;            // parameter words per lane
+        constexpr int STEP = (kThreads / 32) * CPW, PB = WPL > 1 ? 2 : 4;   // passes whose reads overlap
+        const int warp = tid >> 5, lane = tid & 31, sub = lane / LPC, l = lane % LPC;
+        const float4 *ph = prm + (long long)h * K * DP;
+        for (int kb = warp * CPW + sub; kb < K + sub; kb += STEP * PB) {
+            float4 pw[PB][WPL];
+#pragma unroll
+            for (int b = 0; b < PB; ++b)
+#pragma unroll
+                for (int w = 0; w < WPL; ++w) {
+                    const int k = kb + b * STEP;
+                    pw[b][w] = k < K ? ph[(long long)k * DP + l + w * LPC] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int b = 0; b < PB; ++b) {
+                const int k = kb + b * STEP;
+                float aq = 0.f, ak = 0.f;
+#pragma unroll
+                for (int w = 0; w < WPL; ++w) {
+                    const int dp = l + w * LPC;
+                    const float4 p = pw[b][w];
+                    float y = fmaf(xq[2 * dp], p.x, p.z);
+                    aq = fmaf(y, y, aq);
+                    y = fmaf(xq[2 * dp + 1], p.y, p.w);
+                    aq = fmaf(y, y, aq);
+                    y = fmaf(xk[2 * dp], p.x, p.z);
+                    ak = fmaf(y, y, ak);
+                    y = fmaf(xk[2 * dp + 1], p.y, p.w);
+                    ak = fmaf(y, y, ak);
+                }
+#pragma unroll
+                for (int o = LPC / 2; o; o >>= 1) {
+                    aq += __shfl_xor_sync(0xffffffffu, aq, o);
+                    ak += __shfl_xor_sync(0xffffffffu, ak, o);
+                }
+                if (k < K && l == 0) {
+                    const float c = cst[(long long)h * K + k];
+                    gq[k] = fmaf(-0.5f, aq, c);
+                    gk[k] = fmaf(-0.5f, ak, c);
+                }
+            }
+        }
+    }
+    __syncthreads();
     float mq = -FLT_MAX, mk = -FLT_MAX;
     for (int k = tid; k < K; k += kThreads) {
-        const float4 *pk = prm + ((long long)h * K + k) * (D / 2);
-        float aq = 0.f, ak = 0.f;
-        for (int dp = 0; dp < D / 2; ++dp) {
-            const float4 p = pk[dp];
-            float y = fmaf(xq[2 * dp], p.x, p.z);
-            aq = fmaf(y, y, aq);
-            y = fmaf(xq[2 * dp + 1], p.y, p.w);
-            aq = fmaf(y, y, aq);
-            y = fmaf(xk[2 * dp], p.x, p.z);
-            ak = fmaf(y, y, ak);
-            y = fmaf(xk[2 * dp + 1], p.y, p.w);
-            ak = fmaf(y, y, ak);
-        }
-        const float c = cst[(long long)h * K + k];
-        gq[k] = fmaf(-0.5f, aq, c);
-        gk[k] = fmaf(-0.5f, ak, c);
         mq = fmaxf(mq, gq[k]);
         mk = fmaxf(mk, gk[k]);
     }
@@ -91,31 +140,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
 
-    // Vt[k][c] += gk[k] v[c]; num[c] += gq[k] Vt_new[k][c].  Thread t always owns column t % DV.
-    float *st = state + bh * ((long long)K * DV + K);
-    const int c = tid % DV;
-    const float vc = vv[c];
-    float num = 0.f;
-    const int total = K * DV;
-    int e = tid;
-    for (; e + 3 * kThreads < total; e += 4 * kThreads) {
-        float s[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) s[u] = st[e + u * kThreads];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int k = (e + u * kThreads) / DV;
-            s[u] = fmaf(gk[k], vc, s[u]);
-            st[e + u * kThreads] = s[u];
-            num = fmaf(gq[k], s[u], num);
-        }
-    }
-    for (; e < total; e += kThreads) {
-        const int k = e / DV;
-        const float s = fmaf(gk[k], vc, st[e]);
-        st[e] = s;
-        num = fmaf(gq[k], s, num);
-    }
+    // Vt[k][c] += gk[k] v[c]; num[c] += gq[k] Vt_new[k][c]; Z[k] += gk[k]; den += gq[k] Z_new[k]
     float den = 0.f;
     for (int k = tid; k < K; k += kThreads) {
         const float z = st[total + k] + gk[k];
@@ -123,24 +148,97 @@ __global__ void __launch_bounds__(kThreads)
         den = fmaf(gq[k], z, den);
     }
     den = block_reduce(den, red, false);
-    __syncthreads();
-    red[tid] = num;
-    __syncthreads();
-    if (tid < DV) {
-        float n = 0.f;
-        for (int t = tid; t < kThreads; t += DV) n += red[t];
-        out[bh * DV + tid] = n / (den + eps);
+    if (vec) {
+        const float4 vc = reinterpret_cast<const float4 *>(vv)[c4];
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto row = [&](int k, float4 t) {
+            const float a = gk[k], b = gq[k];
+            t.x = fmaf(a, vc.x, t.x);
+            t.y = fmaf(a, vc.y, t.y);
+            t.z = fmaf(a, vc.z, t.z);
+            t.w = fmaf(a, vc.w, t.w);
+            st4[k * G4 + c4] = t;
+            num.x = fmaf(b, t.x, num.x);
+            num.y = fmaf(b, t.y, num.y);
+            num.z = fmaf(b, t.z, num.z);
+            num.w = fmaf(b, t.w, num.w);
+        };
+        for (int k0 = r0; k0 < K; k0 += U * RP) {   // U rows at a time: the loads of a batch first
+            float4 t[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (k0 + u * RP < K) t[u] = st4[(k0 + u * RP) * G4 + c4];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (k0 + u * RP < K) row(k0 + u * RP, t[u]);
+        }
+        red4[tid] = num;
+        __syncthreads();
+        if (tid < DV) {
+            float n = 0.f;
+            for (int r = 0; r < RP; ++r) {
+                const float4 q = red4[r * G4 + tid / 4];
+                n += (tid & 3) == 0 ? q.x : (tid & 3) == 1 ? q.y : (tid & 3) == 2 ? q.z : q.w;
+            }
+            out[bh * DV + tid] = n / (den + eps);
+        }
+    } else {   // thread t owns column t % DV
+        const int c = tid % DV;
+        const float vc = vv[c];
+        float num = 0.f;
+        int e = tid;
+        for (; e + 3 * kThreads < total; e += 4 * kThreads) {
+            float sv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sv[u] = st[e + u * kThreads];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = (e + u * kThreads) / DV;
+                sv[u] = fmaf(gk[k], vc, sv[u]);
+                st[e + u * kThreads] = sv[u];
+                num = fmaf(gq[k], sv[u], num);
+            }
+        }
+        for (; e < total; e += kThreads) {
+            const int k = e / DV;
+            const float sv = fmaf(gk[k], vc, st[e]);
+            st[e] = sv;
+            num = fmaf(gq[k], sv, num);
+        }
+        __syncthreads();
+        red[tid] = num;
+        __syncthreads();
+        if (tid < DV) {
+            float n = 0.f;
+            for (int t = tid; t < kThreads; t += DV) n += red[t];
+            out[bh * DV + tid] = n / (den + eps);
+        }
     }
 }
 
-template <int DV>
+template <int D, int DV>
 cudaError_t launch_decode_dv(const Dims &dm, const float4 *prm, const float *cst, const void *qx, const void *kx,
                              const void *v, float *state, float *out, cudaStream_t st)
 {
-    const size_t smem = (size_t)(2 * dm.D + DV + 2 * dm.K + kThreads) * 4;
-    k_decode<DV><<<(unsigned)dm.BH(), kThreads, smem, st>>>(dm.H, dm.D, dm.K, dm.eps, qx, kx, dm.x_bf16, v,
-                                                            dm.v_bf16, prm, cst, state, out);
+    // xq, xk, v, gq, gk, red, then red4 at a 16-byte aligned offset
+    const size_t head = ((size_t)(2 * dm.D + DV + 2 * dm.K + kThreads) * 4 + 15) / 16 * 16;
+    const size_t smem = head + (size_t)kThreads * 16;
+    k_decode<D, DV><<<(unsigned)dm.BH(), kThreads, smem, st>>>(dm.H, dm.K, dm.eps, qx, kx, dm.x_bf16, v,
+                                                               dm.v_bf16, prm, cst, state, out);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const Dims &dm, const float4 *prm, const float *cst, const void *qx, const void *kx,
+                            const void *v, float *state, float *out, cudaStream_t st)
+{
+    switch (dm.DV) {
+    case 16: return launch_decode_dv<D, 16>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 32: return launch_decode_dv<D, 32>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 64: return launch_decode_dv<D, 64>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 128: return launch_decode_dv<D, 128>(dm, prm, cst, qx, kx, v, state, out, st);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 } // namespace
@@ -148,11 +246,11 @@ cudaError_t launch_decode_dv(const Dims &dm, const float4 *prm, const float *cst
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx, const void *kx,
                           const void *v, float *state, float *out, cudaStream_t st)
 {
-    switch (dm.DV) {
-    case 16: return launch_decode_dv<16>(dm, prm, cst, qx, kx, v, state, out, st);
-    case 32: return launch_decode_dv<32>(dm, prm, cst, qx, kx, v, state, out, st);
-    case 64: return launch_decode_dv<64>(dm, prm, cst, qx, kx, v, state, out, st);
-    case 128: return launch_decode_dv<128>(dm, prm, cst, qx, kx, v, state, out, st);
+    switch (dm.D) {
+    case 16: return launch_decode_d<16>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 32: return launch_decode_d<32>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 64: return launch_decode_d<64>(dm, prm, cst, qx, kx, v, state, out, st);
+    case 128: return launch_decode_d<128>(dm, prm, cst, qx, kx, v, state, out, st);
     default: return cudaErrorInvalidValue;
     }
 }

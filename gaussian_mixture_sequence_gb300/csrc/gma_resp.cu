@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__
         const int kk = tid / 8, part = tid % 8;
         float acc = 0.f;
         if (kk < kn)
+#pragma unroll 4
             for (int d = part; d < D; d += 8) acc += logf(softplus(vr[(long long)(k0 + kk) * D + d]));
         lsum[tid] = acc;
     }
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__
         cst[(long long)h * K + k0 + tid] = (l[k0 + tid] - lse) - 0.5f * acc;
     }
     const int DP = D / 2;
+#pragma unroll 4
     for (int i = tid; i < kn * DP; i += kThreads) {
         const long long e = (long long)k0 * D + 2LL * i; // (k0 + i / DP) * D + 2 * (i % DP)
         float s0 = 1.0f / sqrtf(softplus(vr[e])), s1 = 1.0f / sqrtf(softplus(vr[e + 1]));

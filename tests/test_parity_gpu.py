@@ -233,6 +233,9 @@ def _decode_run(c, prefill_state):
 
 @pytest.mark.parametrize("wl,sample", [
     (W["decode_b256"].with_(B=2, H=2, N=300, decode_steps=40, K=24, d=16, dv=32), None),
+    # K not a multiple of 4: slices of the state are not 16-byte aligned (the scalar state pass)
+    (W["decode_b256"].with_(B=1, H=3, N=70, decode_steps=12, K=7, d=16, dv=16), None),
+    (W["decode_b256"].with_(B=2, H=2, N=130, decode_steps=9, K=128, d=64, dv=128), None),
     (W["decode_b256"], 3),
 ])
 def test_decode_after_prefill(wl, sample):
