@@ -515,12 +515,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 };
                 // exact pass: online maximum and sum over the kept components of this half; the
                 // log-joints wait in the output tile for the normalisation (fp32 tile: as floats;
-                // split tile: high half-word in the hi plane, low half-word in the lo plane)
+                // 16-bit tiles: high half-word in the hi plane, low half-word in the lo plane, which
+                // a single-plane tile has room for and never stores)
                 float mt = -FLT_MAX, st = 0.f;
                 for_kept([&](int k, float l) {
                     if (g_f32) {
                         *reinterpret_cast<float *>(ob + sw128_offset(i, k, kPRows, 4)) = l;
-                    } else if (g_split) {
+                    } else {
                         const uint32_t off = sw128_offset(i, k, kPRows, 2), u = __float_as_uint(l);
                         *reinterpret_cast<unsigned short *>(ob + off) = (unsigned short)(u >> 16);
                         *reinterpret_cast<unsigned short *>(ob + LO + off) = (unsigned short)(u & 0xffffu);
@@ -539,8 +540,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const float q1 = ex1[(1 - hf) * kPK + i], q2 = ex2[(1 - hf) * kPK + i];
                     const float m = fmaxf(mt, q1);
                     const float inv = 1.0f / (st * expf(mt - m) + q2 * expf(q1 - m));
-                    // the kept posteriors of this half into the output tile (a single-plane bf16
-                    // tile has no room for the log-joints: they are evaluated again)
+                    // the kept posteriors of this half into the output tile
 #pragma unroll
                     for (int wd = 0; wd < 2; ++wd)
                         for (uint32_t mm = wd ? xm1 : xm0; mm; mm &= mm - 1) {
@@ -550,11 +550,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 *o = expf(*o - m) * inv;
                             } else {
                                 const uint32_t off = sw128_offset(i, k, kPRows, 2);
-                                const float l =
-                                    g_split ? __uint_as_float(
-                                                  ((uint32_t)*reinterpret_cast<const unsigned short *>(ob + off) << 16) |
-                                                  *reinterpret_cast<const unsigned short *>(ob + LO + off))
-                                            : exact(k);
+                                const float l = __uint_as_float(
+                                    ((uint32_t)*reinterpret_cast<const unsigned short *>(ob + off) << 16) |
+                                    *reinterpret_cast<const unsigned short *>(ob + LO + off));
                                 __nv_bfloat16 hi, lo;
                                 split_bf16(expf(l - m) * inv, hi, lo);
                                 *reinterpret_cast<__nv_bfloat16 *>(ob + off) = hi;
