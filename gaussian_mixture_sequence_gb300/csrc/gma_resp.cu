@@ -31,71 +31,74 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // Grid (H, ceil(K / 32)): each CTA recomputes its head's log-sum-exp of the
-// mixture logits (K <= 512 values) and prepares 32 components.
-constexpr int kPrepComps = 32;
+// mixture logits (K <= 512 values, one per thread) and prepares 32 components,
+// 16 threads per component over groups of four features (all of a thread's
+// loads are issued before their results are used).
+constexpr int kPrepComps = 32, kPrepThreads = 512;
 
-__global__ void __launch_bounds__(kThreads) k_prep(int K, int D, const float *__restrict__ mu,
-                                                   const float *__restrict__ var_raw,
-                                                   const float *__restrict__ logit_pi,
-                                                   float4 *__restrict__ prm, float *__restrict__ cst)
+__global__ void __launch_bounds__(kPrepThreads) k_prep(int K, int D, const float *__restrict__ mu,
+                                                       const float *__restrict__ var_raw,
+                                                       const float *__restrict__ logit_pi,
+                                                       float4 *__restrict__ prm, float *__restrict__ cst)
 {
-    __shared__ float red[kThreads / 32];
-    __shared__ float bcast;
-    __shared__ float lsum[kThreads];
+    constexpr int NW = kPrepThreads / 32;
+    __shared__ float red[NW];
+    __shared__ float bcast[2];
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int k0 = blockIdx.y * kPrepComps, kn = min(kPrepComps, K - k0);
+    const int k = blockIdx.y * kPrepComps + (tid >> 4), part = tid & 15;
     const float *l = logit_pi + (long long)h * K;
 
-    float m = -FLT_MAX;
-    for (int k = tid; k < K; k += kThreads) m = fmaxf(m, l[k]);
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-        float t = lane < kThreads / 32 ? red[lane] : -FLT_MAX;
-        t = warp_max(t);
-        if (lane == 0) bcast = t;
+    // this thread's features 4 part + 64 j of component k (D / 4 groups of four, up to 2 per thread)
+    const int G = D / 4;
+    float4 r4[2], u4[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int g = part + 16 * j;
+        const bool on = k < K && g < G;
+        const long long e = ((long long)h * K + k) * D + 4 * g;
+        r4[j] = on ? *reinterpret_cast<const float4 *>(var_raw + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        u4[j] = on ? *reinterpret_cast<const float4 *>(mu + e) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
-    const float lmax = bcast;
-    float s = 0.f;
-    for (int k = tid; k < K; k += kThreads) s += expf(l[k] - lmax);
-    s = warp_sum(s);
-    __syncthreads();
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    if (warp == 0) {
-        float t = lane < kThreads / 32 ? red[lane] : 0.f;
-        t = warp_sum(t);
-        if (lane == 0) bcast = lmax + logf(t);
-    }
-    __syncthreads();
-    const float lse = bcast;
+    const float lv = tid < K ? l[tid] : -FLT_MAX;
 
-    // sum_d log sigma^2 of the CTA's components: 8 threads per component
-    const float *vr = var_raw + (long long)h * K * D;
-    const float *mh = mu + (long long)h * K * D;
-    {
-        const int kk = tid / 8, part = tid % 8;
-        float acc = 0.f;
-        if (kk < kn)
-#pragma unroll 4
-            for (int d = part; d < D; d += 8) acc += logf(softplus(vr[(long long)(k0 + kk) * D + d]));
-        lsum[tid] = acc;
+    float t = warp_max(lv);
+    if (lane == 0) red[warp] = t;
+    __syncthreads();
+    if (warp == 0) {
+        t = warp_max(lane < NW ? red[lane] : -FLT_MAX);
+        if (lane == 0) bcast[0] = t;
     }
     __syncthreads();
-    if (tid < kn) {
-        float acc = 0.f;
-        for (int p = 0; p < 8; ++p) acc += lsum[tid * 8 + p];
-        cst[(long long)h * K + k0 + tid] = (l[k0 + tid] - lse) - 0.5f * acc;
+    const float lmax = bcast[0];
+    t = warp_sum(tid < K ? expf(lv - lmax) : 0.f);
+    __syncthreads();   // red is reused
+    if (lane == 0) red[warp] = t;
+    __syncthreads();
+    if (warp == 0) {
+        t = warp_sum(lane < NW ? red[lane] : 0.f);
+        if (lane == 0) bcast[1] = lmax + logf(t);
     }
-    const int DP = D / 2;
-#pragma unroll 4
-    for (int i = tid; i < kn * DP; i += kThreads) {
-        const long long e = (long long)k0 * D + 2LL * i; // (k0 + i / DP) * D + 2 * (i % DP)
-        float s0 = 1.0f / sqrtf(softplus(vr[e])), s1 = 1.0f / sqrtf(softplus(vr[e + 1]));
-        prm[(long long)h * K * DP + (long long)k0 * DP + i] = make_float4(s0, s1, -mh[e] * s0, -mh[e + 1] * s1);
+
+    float lsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int g = part + 16 * j;
+        if (k < K && g < G) {
+            const float rv[4] = {r4[j].x, r4[j].y, r4[j].z, r4[j].w}, uv[4] = {u4[j].x, u4[j].y, u4[j].z, u4[j].w};
+            float4 *pr = prm + ((long long)h * K + k) * (D / 2) + 2 * g;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float v0 = softplus(rv[2 * q]), v1 = softplus(rv[2 * q + 1]);
+                const float s0 = 1.0f / sqrtf(v0), s1 = 1.0f / sqrtf(v1);
+                pr[q] = make_float4(s0, s1, -uv[2 * q] * s0, -uv[2 * q + 1] * s1);
+                lsum += logf(v0) + logf(v1);
+            }
+        }
     }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);   // the component's 16 threads
+    __syncthreads();   // bcast[1]
+    if (part == 0 && k < K) cst[(long long)h * K + k] = (l[k] - bcast[1]) - 0.5f * lsum;
 }
 
 // Responsibilities of a range of rows of one (b, h) slice.
@@ -261,7 +264,7 @@ cudaError_t launch_resp_d(const Dims &dm, const float4 *prm, const float *cst, c
 cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st)
 {
     dim3 grid(dm.H, (dm.K + kPrepComps - 1) / kPrepComps);
-    k_prep<<<grid, kThreads, 0, st>>>(dm.K, dm.D, p.mu, p.var_raw, p.logit_pi, prm, cst);
+    k_prep<<<grid, kPrepThreads, 0, st>>>(dm.K, dm.D, p.mu, p.var_raw, p.logit_pi, prm, cst);
     return cudaGetLastError();
 }
 

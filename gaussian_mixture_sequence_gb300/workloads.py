@@ -71,6 +71,9 @@ WORKLOADS = {
                                  dist="peaked", seed=1002),
     "causal_16k_peaked": Workload("causal_16k_peaked", 2, 16, 16384, 64, 64, 128, "causal",
                                   dist="peaked", seed=1002),
+    # the same sequence with bf16 chunk-product operands (fp32 accumulation)
+    "causal_16k_peaked_bf16": Workload("causal_16k_peaked_bf16", 2, 16, 16384, 64, 64, 128, "causal",
+                                       gemm_dtype="bf16", dist="peaked", seed=1002),
     "causal_64k_bf16": Workload("causal_64k_bf16", 1, 16, 65536, 64, 128, 128, "causal",
                                 x_dtype="bf16", v_dtype="bf16", gemm_dtype="bf16", seed=1003),
     "causal_8k_K32": Workload("causal_8k_K32", 4, 8, 8192, 64, 64, 32, "causal", seed=1004),

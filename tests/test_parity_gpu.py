@@ -122,6 +122,7 @@ CAUSAL = [
     (W["tiny"].with_(B=8, H=25, N=200, d=64, dv=64, K=128), None, 0),
     (W["tiny"].with_(B=2, H=16, N=1100, d=64, dv=128, K=128, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     (W["causal_16k_peaked"], 3, 0),
+    (W["causal_16k_peaked_bf16"], 2, 0),
     (W["causal_64k_bf16"], 2, 0),
     (W["causal_8k_K32"], 2, 0),
     (W["causal_8k_K64"], 2, 0),
