@@ -236,6 +236,28 @@ def dist_env():
     return world, rank, local
 
 
+def replica_seed(wl, rank):
+    """Seed of the inputs of rank `rank`: every rank runs its own replica of the workload
+    (the (batch, head) slices are independent, so there is no exchange between ranks)."""
+    return wl.seed + rank
+
+
+def max_over_ranks(pg, x, device):
+    """The maximum of a per-rank number over all ranks (`pg` None: one rank)."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_rank, ms):
+    """Tokens per second of the whole job: every rank processes tokens_per_rank in ms (the
+    slowest rank's time)."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 # The source file holding each stage's kernel; its hash (with the shared headers)
 # keys the committed DRAM counters, so a changed kernel reports no traffic.
 KERNEL_SOURCE = {
@@ -491,7 +513,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     gma.load()
-    run = Runner(wl, dev, wl.seed + rank)
+    run = Runner(wl, dev, replica_seed(wl, rank))
     stream = torch.cuda.current_stream(dev)
     NE = gma.PROFILE_MAX_STAGES + 1
 
@@ -532,16 +554,12 @@ def main():
     t_host1 = time.time()
     if pg:
         pg.barrier()
-    total_ms = start.elapsed_time(end)
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, start.elapsed_time(end), dev)
     clocks_summary = clocks.summary(t_host0, t_host1)
 
     ms = total_ms / args.steps
     tokens = tokens_per_step(wl)
-    value = world * tokens / (ms * 1e-3)
+    value = whole_job_rate(world, tokens, ms)
     stage_ms = {}
     for i, nm in enumerate(names):
         stage_ms[nm] = statistics.mean(step_events[s_][i].elapsed_time(step_events[s_][i + 1])
@@ -574,11 +592,7 @@ def main():
         run.e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize(dev)
-    e_ms = e_start.elapsed_time(e_end) / ne
-    if pg:
-        t = torch.tensor([e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(pg, e_start.elapsed_time(e_end) / ne, dev)
     clocks.stop()
     h2d, d2h = run.io_bytes()
 
@@ -614,7 +628,7 @@ def main():
             "stages_ms": stage_ms,
             "gpu_launches": len(names) * args.steps,
             "clocks": clocks_summary,
-            "e2e": {"value": world * tokens / (e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e_ms,
+            "e2e": {"value": whole_job_rate(world, tokens, e_ms), "unit": "tokens/s", "ms_per_step": e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "entry": "gma_forward_causal_host" if wl.mode == "causal" else "device entry + torch copies"},
             "cpu_baseline": cpu,
