@@ -444,8 +444,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
     float *z_s = reinterpret_cast<float *>(os + Sm::OUT);          // [128] Z of the carried memory
     float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [4]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [5]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV;
     static_assert(D_PV + NBV * 64 <= 512, "TMEM columns");
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3);
+                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4);
     const long long SZ = (long long)kK * DV + kK;
 
     // block of the carried memory read by item it
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     bool pend_g = false, pend_s = false;
     uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0);
@@ -534,9 +534,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         if (tid == 0) {   // a load whose wait gave up is still in flight
             pend_g = pend_g && !ok_g;
             pend_s = pend_s && !ok_s;
-            // the previous output tile has left the staging tile, which takes the V images of
-            // this chunk once [P | U] is done (the other threads know it from that completion)
-            if (CAUSAL) bulk_wait_read();
             // [P | U] = Gq [Gk ; Vt^T]^T  (bidirectional read: U = Gq Vt)
             const uint32_t b0 = CAUSAL ? 0u : PART;
             const uint32_t d0 = CAUSAL ? D_P : D_U, nb = CAUSAL ? kC + DV : DV;
@@ -546,17 +543,23 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
             }
             mma_commit(BAR_M);
+            if (CAUSAL) {   // the previous output tile has left the staging tile, which takes V next
+                bulk_wait_read();
+                mbar_arrive(BAR_O);
+            }
         }
         __syncwarp();
         // while the tensor core works: the partial Gamma_Q,i . Z over this thread's 32 components
-        {
+        // (thread 0, which issues the MMA, leaves its part to thread 128: the same row, the next
+        // quarter)
+        auto qz_part = [&](int row, int gq) {
             float qz = 0.f;
 #pragma unroll
             for (int pl = 0; pl < NP; ++pl)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int k = 32 * g + 8 * q;
-                    const uint4 t = *reinterpret_cast<const uint4 *>((pl ? ta1 : ta0) + sw128_offset(i, k, kC, 2));
+                    const int k = 32 * gq + 8 * q;
+                    const uint4 t = *reinterpret_cast<const uint4 *>((pl ? ta1 : ta0) + sw128_offset(row, k, kC, 2));
                     const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -564,13 +567,17 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         qz = fmaf(__uint_as_float(w[e] & 0xffff0000u), z_s[k + 2 * e + 1], qz);
                     }
                 }
-            part[g * kK + i] = qz;
-        }
+            part[gq * kK + row] = qz;
+        };
+        if (tid != 0) qz_part(i, g);
+        if (tid == 128) qz_part(0, 0);
         ok = mbar_wait(BAR_M, ph) && ok;
         fence_after_sync();
         if constexpr (CAUSAL) {
             // V into token-major images in the staging tile, the B operand (MN-major) of
-            // U += P_m V: hi plane in columns [0, d_v), lo plane in [d_v, 2 d_v)
+            // U += P_m V: hi plane in columns [0, d_v), lo plane in [d_v, 2 d_v), once the
+            // previous output tile has left it
+            ok = mbar_wait(BAR_O, ph) && ok;
 #pragma unroll
             for (int u = 0; u < VPER; ++u) {
                 const int f = tid + u * kOutThreads, j = f / F4, c4 = 4 * (f % F4);
