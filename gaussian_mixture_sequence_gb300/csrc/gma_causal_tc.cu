@@ -278,6 +278,17 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
     for (long long it = it0; it < it1 && ok; ++it) {
         const int j = (int)(it - it0), b = j & 1;
+        bool okm = true;
+        if (j > 0) {   // the previous chunk's MMA (issued a whole item ago): its landing buffer takes chunk j + 1
+            okm = mbar_wait(smem_addr(bar + 2 + (b ^ 1)), (uint32_t)(((j - 1) >> 1) & 1));
+            okp = okp && okm;
+            fence_after_sync();
+            if (tid == 0 && okm && it + 1 < it1) {
+                load(it + 1, b ^ 1);
+                pend[b ^ 1] = true;
+                ph_l[b ^ 1] = (uint32_t)(((j + 1) >> 1) & 1);
+            }
+        }
         put_b(b, vr);   // its buffer was last read by the MMA of chunk j - 2, complete
         if (it + 1 < it1) load_v(it + 1, vr);   // in flight while this chunk's MMA runs
         const bool ok_l = mbar_wait(smem_addr(bar + b), (uint32_t)((j >> 1) & 1));
@@ -301,17 +312,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         }
         __syncwarp();
         ++nm;
-        if (j > 0) {   // the previous chunk: its landing buffer takes chunk j + 1, its accumulator goes out
-            const bool okm = mbar_wait(smem_addr(bar + 2 + (b ^ 1)), (uint32_t)(((j - 1) >> 1) & 1));
-            okp = okp && okm;
-            fence_after_sync();
-            if (tid == 0 && okm && it + 1 < it1) {
-                load(it + 1, b ^ 1);
-                pend[b ^ 1] = true;
-                ph_l[b ^ 1] = (uint32_t)(((j + 1) >> 1) & 1);
-            }
-            take(it - 1, b ^ 1, okm);
-        }
+        if (j > 0) take(it - 1, b ^ 1, okm);   // the previous chunk's accumulator goes out meanwhile
     }
     // the last chunk issued, once its MMA is done (chains complete in order, so this also
     // covers every earlier one after a failure)
