@@ -77,6 +77,13 @@ __global__ void __launch_bounds__(kThreads, 6)
         constexpr int STEP = (kThreads / 32) * CPW, PB = WPL > 1 ? 2 : 4;   // passes whose reads overlap
         const int warp = tid >> 5, lane = tid & 31, sub = lane / LPC, l = lane % LPC;
         const float4 *ph = prm + (long long)h * K * DP;
+        float2 xqr[WPL], xkr[WPL];   // this lane's features: the same for every component
+#pragma unroll
+        for (int w = 0; w < WPL; ++w) {
+            const int dp = l + w * LPC;
+            xqr[w] = *reinterpret_cast<const float2 *>(xq + 2 * dp);
+            xkr[w] = *reinterpret_cast<const float2 *>(xk + 2 * dp);
+        }
         for (int kb = warp * CPW + sub; kb < K + sub; kb += STEP * PB) {
             float4 pw[PB][WPL];
 #pragma unroll
@@ -86,32 +93,65 @@ __global__ void __launch_bounds__(kThreads, 6)
                     const int k = kb + b * STEP;
                     pw[b][w] = k < K ? ph[(long long)k * DP + l + w * LPC] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+            // the lane's partial sums: v[2 b] for the q row, v[2 b + 1] for the k row of pass b
+            float v[2 * PB];
 #pragma unroll
             for (int b = 0; b < PB; ++b) {
-                const int k = kb + b * STEP;
                 float aq = 0.f, ak = 0.f;
 #pragma unroll
                 for (int w = 0; w < WPL; ++w) {
-                    const int dp = l + w * LPC;
                     const float4 p = pw[b][w];
-                    float y = fmaf(xq[2 * dp], p.x, p.z);
+                    float y = fmaf(xqr[w].x, p.x, p.z);
                     aq = fmaf(y, y, aq);
-                    y = fmaf(xq[2 * dp + 1], p.y, p.w);
+                    y = fmaf(xqr[w].y, p.y, p.w);
                     aq = fmaf(y, y, aq);
-                    y = fmaf(xk[2 * dp], p.x, p.z);
+                    y = fmaf(xkr[w].x, p.x, p.z);
                     ak = fmaf(y, y, ak);
-                    y = fmaf(xk[2 * dp + 1], p.y, p.w);
+                    y = fmaf(xkr[w].y, p.y, p.w);
                     ak = fmaf(y, y, ak);
                 }
+                v[2 * b] = aq;
+                v[2 * b + 1] = ak;
+            }
+            if constexpr (LPC == 32) {
+                // sums over the warp by recursive halving: each step a lane keeps half of its
+                // values and adds the partner's copy of them, so that lane l ends with value
+                // (l >> (5 - S)) over the lanes that differ in the top S bits, S = log2(2 PB),
+                // and the last 5 - S steps add the rest
+                constexpr int NV = 2 * PB, S = NV == 8 ? 3 : 2;
+                int n = NV;
 #pragma unroll
-                for (int o = LPC / 2; o; o >>= 1) {
-                    aq += __shfl_xor_sync(0xffffffffu, aq, o);
-                    ak += __shfl_xor_sync(0xffffffffu, ak, o);
+                for (int o = 16; o > (16 >> S); o >>= 1) {
+                    const bool up = (lane & o) != 0;
+                    n >>= 1;
+#pragma unroll
+                    for (int e = 0; e < NV / 2; ++e)
+                        if (e < n) {
+                            const float send = up ? v[e] : v[e + n], keep = up ? v[e + n] : v[e];
+                            v[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
                 }
-                if (k < K && l == 0) {
-                    const float c = cst[(long long)h * K + k];
-                    gq[k] = fmaf(-0.5f, aq, c);
-                    gk[k] = fmaf(-0.5f, ak, c);
+                float t = v[0];
+#pragma unroll
+                for (int o = 16 >> S; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                const int idx = lane >> (5 - S), k = kb + (idx >> 1) * STEP;
+                if ((lane & ((32 >> S) - 1)) == 0 && k < K)
+                    (idx & 1 ? gk : gq)[k] = fmaf(-0.5f, t, cst[(long long)h * K + k]);
+            } else {
+#pragma unroll
+                for (int b = 0; b < PB; ++b) {
+                    const int k = kb + b * STEP;
+                    float aq = v[2 * b], ak = v[2 * b + 1];
+#pragma unroll
+                    for (int o = LPC / 2; o; o >>= 1) {
+                        aq += __shfl_xor_sync(0xffffffffu, aq, o);
+                        ak += __shfl_xor_sync(0xffffffffu, ak, o);
+                    }
+                    if (k < K && l == 0) {
+                        const float c = cst[(long long)h * K + k];
+                        gq[k] = fmaf(-0.5f, aq, c);
+                        gk[k] = fmaf(-0.5f, ak, c);
+                    }
                 }
             }
         }
