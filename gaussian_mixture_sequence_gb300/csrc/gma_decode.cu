@@ -13,28 +13,12 @@
 namespace gma {
 namespace {
 
-__device__ __forceinline__ float block_reduce(float v, float *red, bool is_max)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const float t = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, t) : v + t;
-    }
-    __syncthreads(); // red may still be read from a previous reduction
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = red[0];
-    for (int w = 1; w < kThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-    return r;
-}
-
 // One CTA per (b, h).  The log-joints of the new token's q and k rows: a warp
-// per component row of parameters at a time (coalesced, shared by both rows);
-// then the two softmaxes; then one pass over the state that updates and reads
-// it, four columns per thread with
-// 16-byte loads and stores (a scalar pass when K is not a multiple of 4, where
-// the slices of the state are not 16-byte aligned).
+// per component row of parameters at a time (coalesced, shared by both rows,
+// sums over the warp by shuffles); then the two softmaxes, a warp each; then
+// one pass over the state that updates and reads it, four columns per thread
+// with 16-byte loads and stores (a scalar pass when K is not a multiple of 4,
+// where the slices of the state are not 16-byte aligned).
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 6)
     k_decode(int H, int K, float eps, const void *__restrict__ qx, const void *__restrict__ kx, bool x_bf16,
@@ -49,6 +33,7 @@ __global__ void __launch_bounds__(kThreads, 6)
     float *gk = gq + K;        // [K]
     float *red = gk + K;       // [kThreads]
     float4 *red4 = reinterpret_cast<float4 *>((reinterpret_cast<uintptr_t>(red + kThreads) + 15) & ~uintptr_t(15));   // [kThreads]
+    float *dz = reinterpret_cast<float *>(red4 + kThreads);   // [kThreads / 32] den partials
 
     const long long bh = blockIdx.x;
     const int h = (int)(bh % H), tid = threadIdx.x;
@@ -157,37 +142,45 @@ __global__ void __launch_bounds__(kThreads, 6)
         }
     }
     __syncthreads();
-    float mq = -FLT_MAX, mk = -FLT_MAX;
-    for (int k = tid; k < K; k += kThreads) {
-        mq = fmaxf(mq, gq[k]);
-        mk = fmaxf(mk, gk[k]);
-    }
-    mq = block_reduce(mq, red, true);
-    mk = block_reduce(mk, red, true);
-    float sq = 0.f, sk = 0.f;
-    for (int k = tid; k < K; k += kThreads) {
-        gq[k] = expf(gq[k] - mq);
-        gk[k] = expf(gk[k] - mk);
-        sq += gq[k];
-        sk += gk[k];
-    }
-    sq = block_reduce(sq, red, false);
-    sk = block_reduce(sk, red, false);
-    const float iq = 1.0f / sq, ik = 1.0f / sk;
-    for (int k = tid; k < K; k += kThreads) {
-        gq[k] *= iq;
-        gk[k] *= ik;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < 2) {   // the two softmaxes: warp 0 the q row, warp 1 the k row
+        float *gr = warp ? gk : gq;
+        float m = -FLT_MAX;
+        for (int k = lane; k < K; k += 32) m = fmaxf(m, gr[k]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float sum = 0.f;
+        for (int k = lane; k < K; k += 32) {
+            const float e = expf(gr[k] - m);
+            gr[k] = e;
+            sum += e;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = 1.0f / sum;
+        for (int k = lane; k < K; k += 32) gr[k] *= inv;
     }
     __syncthreads();
 
     // Vt[k][c] += gk[k] v[c]; num[c] += gq[k] Vt_new[k][c]; Z[k] += gk[k]; den += gq[k] Z_new[k]
-    float den = 0.f;
-    for (int k = tid; k < K; k += kThreads) {
-        const float z = st[total + k] + gk[k];
-        st[total + k] = z;
-        den = fmaf(gq[k], z, den);
+    // (den: a partial per warp, added up by the threads that write the output)
+    {
+        float dp = 0.f;
+        for (int k = tid; k < K; k += kThreads) {
+            const float z = st[total + k] + gk[k];
+            st[total + k] = z;
+            dp = fmaf(gq[k], z, dp);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+        if (lane == 0) dz[warp] = dp;
     }
-    den = block_reduce(den, red, false);
+    auto den_total = [&]() {   // after a barrier
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) d += dz[w];
+        return d;
+    };
     if (vec) {
         const float4 vc = reinterpret_cast<const float4 *>(vv)[c4];
         float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -220,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 6)
                 const float4 q = red4[r * G4 + tid / 4];
                 n += (tid & 3) == 0 ? q.x : (tid & 3) == 1 ? q.y : (tid & 3) == 2 ? q.z : q.w;
             }
-            out[bh * DV + tid] = n / (den + eps);
+            out[bh * DV + tid] = n / (den_total() + eps);
         }
     } else {   // thread t owns column t % DV
         const int c = tid % DV;
@@ -251,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 6)
         if (tid < DV) {
             float n = 0.f;
             for (int t = tid; t < kThreads; t += DV) n += red[t];
-            out[bh * DV + tid] = n / (den + eps);
+            out[bh * DV + tid] = n / (den_total() + eps);
         }
     }
 }
@@ -262,7 +255,7 @@ cudaError_t launch_decode_dv(const Dims &dm, const float4 *prm, const float *cst
 {
     // xq, xk, v, gq, gk, red, then red4 at a 16-byte aligned offset
     const size_t head = ((size_t)(2 * dm.D + DV + 2 * dm.K + kThreads) * 4 + 15) / 16 * 16;
-    const size_t smem = head + (size_t)kThreads * 16;
+    const size_t smem = head + (size_t)kThreads * 16 + (kThreads / 32) * 4;
     k_decode<D, DV><<<(unsigned)dm.BH(), kThreads, smem, st>>>(dm.H, dm.K, dm.eps, qx, kx, dm.x_bf16, v,
                                                                dm.v_bf16, prm, cst, state, out);
     return cudaGetLastError();
