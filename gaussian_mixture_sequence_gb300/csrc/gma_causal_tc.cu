@@ -402,8 +402,10 @@ __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const floa
 // threads into token-major bf16 images in the staging tile, the B operand
 // (MN-major), and the two column halves of the product add up to
 // (P_hi + P_lo)(V_hi + V_lo).  The next item's Gamma tiles and memory are
-// fetched once every thread is past its reads of the A images and of Z.  The
-// output tile is staged in shared memory and leaves by TMA stores.
+// fetched as soon as the fused MMA has read its operands and every warp is past
+// its reads of the A images and of Z (an mbarrier with one arrival per warp),
+// while P_m and the V images are built.  The output tile is staged in shared
+// memory and leaves by TMA stores.
 constexpr int kOutThreads = 512;
 
 template <bool SPLIT, int DV>
@@ -445,8 +447,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
     float *z_s = reinterpret_cast<float *>(os + Sm::OUT);          // [128] Z of the carried memory
     float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [5]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [6]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV;
     static_assert(D_PV + NBV * 64 <= 512, "TMEM columns");
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4);
+                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4), BAR_Q = smem_addr(bar + 5);
     const long long SZ = (long long)kK * DV + kK;
 
     // block of the carried memory read by item it
@@ -490,6 +492,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
+        mbar_init(BAR_Q, kOutThreads / 32);   // one arrival per warp and item
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0);
@@ -572,8 +575,22 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         };
         if (tid != 0) qz_part(i, g);
         if (tid == 128) qz_part(0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR_Q);   // this warp is past its reads of the A images and of Z
         ok = mbar_wait(BAR_M, ph) && ok;
         fence_after_sync();
+        if (tid == 0) {
+            // the MMA has read B and the A images and every warp is past its reads of the A
+            // images and Z: the next item's tiles and memory may land in them
+            ok = mbar_wait(BAR_Q, ph) && ok;
+            fence_proxy_async();
+            if (more && ok) {
+                load_gamma(it + 1);
+                load_memory(it + 1);
+                pend_g = pend_s = true;
+                ph_g = ph_s = ph ^ 1u;
+            }
+        }
         if constexpr (CAUSAL) {
             // V into token-major images in the staging tile, the B operand (MN-major) of
             // U += P_m V: hi plane in columns [0, d_v), lo plane in [d_v, 2 d_v), once the
@@ -618,17 +635,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             tmem_wait_st();
             fence_proxy_async();
             fence_before_sync();
-            __syncthreads();   // every thread is past its reads of the A images and of Z
+            __syncthreads();   // the V images and P_m are in place
             fence_after_sync();
             if (tid == 0) {
-                // B (Gamma_K and carried-memory rows), the A images and Z are free: the next
-                // item's tiles and memory (the threads only read them)
-                if (more && ok) {
-                    load_gamma(it + 1);
-                    load_memory(it + 1);
-                    pend_g = pend_s = true;
-                    ph_g = ph_s = ph ^ 1u;
-                }
                 // U' = P_m [V_hi | V_lo] from both planes of P_m: (P_hi + P_lo)(V_hi + V_lo) in two halves
                 const uint32_t idv = idesc(128, NBV * 64, kFmtBF16) | kBMajorMN;
 #pragma unroll 1
@@ -645,14 +654,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         } else {
             fence_before_sync();
             if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
-            __syncthreads();                  // every thread is past its reads of the A images
+            __syncthreads();
             fence_after_sync();
-            if (tid == 0 && more && ok) {     // B and the A images are free: the next item's tiles
-                load_gamma(it + 1);
-                load_memory(it + 1);
-                pend_g = pend_s = true;
-                ph_g = ph_s = ph ^ 1u;
-            }
         }
 
         float den = eps;
