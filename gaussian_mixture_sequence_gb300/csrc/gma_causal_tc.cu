@@ -25,8 +25,9 @@
 //   SPLIT = false:  bf16 operands, one plane, one pass.
 // Gamma_Q and Gamma_K arrive in this form from the routing kernels and the
 // carried memory from k_scan_split; V and P_m are split by threads.  The row
-// sums of P_m and Gamma_Q . Z are taken on CUDA cores from the same split
-// values the tensor core multiplies.
+// sums of P_m are taken on CUDA cores from the same split values the tensor
+// core multiplies; Gamma_Q . Z is one more product, of both planes of Gamma_Q
+// against the hi and lo rows of Z (all four cross terms, in two columns).
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -47,7 +48,6 @@ __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 a, __nv_bfloat16 b)
 {
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
-__device__ __forceinline__ float bf(uint32_t u) { return __uint_as_float(u << 16); }
 
 // One MMA pass D (+)= A B^T over a 128-deep contraction.  B: K-major SW128 bf16
 // tile of n rows whose 128-byte atom columns lie bstride bytes apart.  A: TMEM
@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 //   total (inclusive, bidirectional)   <- the sum over all chunks
 //   state_out (caller layout)          <- state_in + the sum over all chunks
 // A memory block in operand form holds the hi plane [d_v][K] (bf16), the lo
-// plane (split form only), then Z [K] (fp32), within the bytes of an fp32
-// block.  state_in / state_out keep the caller layout (Vt as K rows of d_v,
+// plane (split form only), then Z as a hi row and a lo row [K] (bf16), within
+// the bytes of an fp32 block.  state_in / state_out keep the caller layout (Vt as K rows of d_v,
 // then Z).
 __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const float *__restrict__ partial,
                                                     const float *__restrict__ state_in, unsigned char *__restrict__ mem,
@@ -354,13 +354,14 @@ __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const floa
     const long long eu = e < VK ? (e % kK) * DV + e / kK : e;   // the same element in the caller layout
     float run = state_in ? state_in[bh * SZ + eu] : 0.f;
     auto put = [&](unsigned char *blk, float x) {
+        __nv_bfloat16 hi, lo;
+        split_bf16(x, hi, lo);
         if (e < VK) {
-            __nv_bfloat16 hi, lo;
-            split_bf16(x, hi, lo);
             reinterpret_cast<__nv_bfloat16 *>(blk)[e] = hi;
             if (lo_plane) reinterpret_cast<__nv_bfloat16 *>(blk)[VK + e] = lo;
-        } else {
-            reinterpret_cast<float *>(blk)[e] = x;
+        } else {   // Z: a hi row and a lo row after both planes
+            reinterpret_cast<__nv_bfloat16 *>(blk)[VK + e] = hi;
+            reinterpret_cast<__nv_bfloat16 *>(blk)[VK + kK + e] = lo;
         }
     };
     const float *__restrict__ p = partial + bh * nblk * SZ + e;
@@ -390,38 +391,47 @@ __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const floa
 // the list (slice, chunk) in order.  16 warps: warp w owns TMEM lanes (rows)
 // 32 (w % 4) + lane and column quarter w / 4 of every row-wise step.
 //
-// U = Gq Vt and P = Gq Gk^T share the A operand Gq, so they are one MMA chain
-// with N = C + d_v over the B tile [Gk ; Vt^T] (K-major, 128-byte swizzle; each
-// 128-byte atom column holds the C rows of Gk, then the d_v rows of Vt^T); its
-// accumulator is [P | U] in consecutive TMEM columns.  Gq is the A operand
-// straight from shared memory.  Every operand plane arrives by TMA:
-//   B images (hi, lo) <- Gk planes (rows 0 .. C-1), memory planes (rows C ..)
+// U = Gq Vt, P = Gq Gk^T and the denominator's Gq Z share the A operand Gq, so
+// they are one MMA chain with N = C + d_v + 16 over the B tile [Gk ; Vt^T ; Z]
+// (K-major, 128-byte swizzle; each 128-byte atom column holds the C rows of Gk,
+// the d_v rows of Vt^T, then Z_hi, Z_lo and 14 zero rows, the lo image's Z rows
+// all zero so that the three passes give (Gq_hi + Gq_lo)(Z_hi + Z_lo) in two
+// columns); its accumulator is [P | U | Gq Z] in consecutive TMEM columns.  Gq
+// is the A operand straight from shared memory.  Every operand plane arrives by
+// TMA:
+//   B images (hi, lo) <- Gk planes (rows 0 .. C-1), memory planes and Z rows
 //   A images (hi, lo) <- Gq planes
+// (with d_v = 128, N would pass 256: there the Z rows are a B operand of their
+// own and one more chain of N = 16).
 // Then P_m, split by threads, goes to TMEM as the A operand of P_m [V_hi | V_lo]:
 // V, read with row-contiguous loads while the tensor core works, is split by
 // threads into token-major bf16 images in the staging tile, the B operand
 // (MN-major), and the two column halves of the product add up to
-// (P_hi + P_lo)(V_hi + V_lo).  The next item's Gamma tiles and memory are
-// fetched as soon as the fused MMA has read its operands and every warp is past
-// its reads of the A images and of Z (an mbarrier with one arrival per warp),
-// while P_m and the V images are built.  The output tile is staged in shared
-// memory and leaves by TMA stores.
+// (P_hi + P_lo)(V_hi + V_lo).  No thread reads the operand images, so the next
+// item's Gamma tiles and memory are fetched as soon as the first chain has
+// completed, while P_m and the V images are built.  The output tile is staged
+// in shared memory and leaves by TMA stores.
 constexpr int kOutThreads = 512;
 
 template <bool SPLIT, int DV>
 struct OutSmem {
     static constexpr int NP = SPLIT ? 2 : 1;                           // planes
     static constexpr uint32_t PART = kC * 128;                         // Gk rows of an atom column
-    static constexpr uint32_t ATOM = (kC + DV) * 128;                  // bytes of an atom column of B
+    // the Z rows [Z_hi; Z_lo; 14 zero rows] join B when N stays within 256, else a B of their own
+    static constexpr bool ZF = kC + DV + 16 <= 256;
+    static constexpr uint32_t ATOM = (kC + DV + (ZF ? 16 : 0)) * 128;  // bytes of an atom column of B
     static constexpr uint32_t BIMG = 2 * ATOM;                         // one B image (two atom columns)
     static constexpr uint32_t AIMG = 2 * kAtom;                        // one A image
     static constexpr uint32_t OUT = kC * DV * 4;                       // output tile (fp32)
-    static constexpr size_t bytes = 1024 + NP * ((size_t)BIMG + AIMG) + OUT + kK * 4 + 8 * kK * 4 + 64;
+    static constexpr uint32_t ZATOM = 16 * 128;                        // atom column of the Z rows
+    static constexpr uint32_t BZ = ZF ? 0 : 2 * ZATOM;                 // their own B operand
+    static constexpr size_t bytes = 1024 + NP * ((size_t)BIMG + AIMG) + OUT + BZ + 4 * kK * 4 + 64;
 };
 
 struct OutMaps {
     CUtensorMap gq[2], gk[2];   // hi / lo planes of the responsibilities
     CUtensorMap s;              // memory blocks in operand form, as rows of 256 bytes
+    CUtensorMap z;              // the same rows, boxes of the two Z rows
     CUtensorMap o;              // output [slices][N][d_v], boxes of 64 rows x 32 columns
 };
 
@@ -430,7 +440,7 @@ struct OutMaps {
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
-                   const void *__restrict__ v, bool v_bf16, const float *__restrict__ zsrc, float *__restrict__ out)
+                   const void *__restrict__ v, bool v_bf16, float *__restrict__ out)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
@@ -445,10 +455,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const tb0 = sm, *const tb1 = sm + Sm::BIMG;                     // B images (hi, lo)
     unsigned char *const ta0 = sm + NP * Sm::BIMG, *const ta1 = ta0 + Sm::AIMG;    // A images (hi, lo)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
-    float *z_s = reinterpret_cast<float *>(os + Sm::OUT);          // [128] Z of the carried memory
-    float *part = z_s + kK;                                         // [8][128]: qz quarters, row-sum quarters
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 8 * kK);    // [6]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
+    unsigned char *const bz = os + Sm::OUT;                                        // B operand of Gq Z (!ZF)
+    float *part = reinterpret_cast<float *>(bz + Sm::BZ);           // [4][128]: row-sum quarters of P_m
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [5]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -457,11 +467,14 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const long long per = (items + gridDim.x - 1) / gridDim.x;
     const long long it0 = (long long)blockIdx.x * per;
     const long long it1 = it0 + per < items ? it0 + per : items;
-    constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV;
-    static_assert(D_PV + NBV * 64 <= 512, "TMEM columns");
+    // TMEM: P_m (hi, lo), then [P | U | Gq Z], P_m [V_hi | V_lo]; without ZF, Gq Z in the unused
+    // lo half of P_m (bf16 operands only)
+    constexpr bool ZF = Sm::ZF;
+    constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV + (ZF ? 64 : 0);
+    constexpr uint32_t D_Z = ZF ? D_U + DV : A_PM_LO;
+    static_assert(D_PV + NBV * 64 <= 512 && (ZF || !SPLIT), "TMEM columns");
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4), BAR_Q = smem_addr(bar + 5);
-    const long long SZ = (long long)kK * DV + kK;
+                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4);
 
     // block of the carried memory read by item it
     auto mem_block = [&](long long it) -> long long { return CAUSAL ? it : it / nblk; };
@@ -476,11 +489,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     };
     auto load_memory = [&](long long it) {   // one thread
         const int srow = (int)(mem_block(it) * SROWS);
-        mbar_expect_tx(BAR_S, (uint32_t)(NP * DV * kRowB + kK * 4));
-        for (int pl = 0; pl < NP; ++pl)
-            for (int a = 0; a < 2; ++a)
+        mbar_expect_tx(BAR_S, (uint32_t)((NP * DV + 2) * kRowB));
+        for (int a = 0; a < 2; ++a) {
+            for (int pl = 0; pl < NP; ++pl)
                 tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS + PART), &maps.s, a * 64, srow + pl * DV, BAR_S);
-        bulk_g2s(smem_addr(z_s), zsrc + mem_block(it) * SZ + (long long)kK * DV, kK * 4, BAR_S);   // Z
+            tma_load_2d(smem_addr(ZF ? tb0 + a * AS + PART + DV * 128 : bz + a * Sm::ZATOM), &maps.z, a * 64,
+                        srow + 2 * DV, BAR_S);   // Z_hi, Z_lo
+        }
     };
 
     if (warp == 0) {
@@ -492,7 +507,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
-        mbar_init(BAR_Q, kOutThreads / 32);   // one arrival per warp and item
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0);
@@ -500,6 +514,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             pend_g = pend_s = true;
         }
     }
+    // the Z rows that TMA never writes stay zero: rows 2 .. 15 of the hi image's (TMA writes
+    // Z_hi, Z_lo), all 16 of the lo image's
+    for (int e = tid; e < NP * 2 * 16 * 8; e += kOutThreads) {
+        const int pl = e / (2 * 16 * 8), a = (e / (16 * 8)) % 2, r = (e / 8) % 16, c = e % 8;
+        if (pl == 0 && r < 2) continue;
+        unsigned char *zb = ZF ? (pl ? tb1 : tb0) + a * AS + PART + DV * 128 : bz + a * Sm::ZATOM;
+        *reinterpret_cast<uint4 *>(zb + (r >> 3) * 1024 + (r & 7) * 128 + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();   // read by the tensor core
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -540,12 +563,14 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             pend_s = pend_s && !ok_s;
             // [P | U] = Gq [Gk ; Vt^T]^T  (bidirectional read: U = Gq Vt)
             const uint32_t b0 = CAUSAL ? 0u : PART;
-            const uint32_t d0 = CAUSAL ? D_P : D_U, nb = CAUSAL ? kC + DV : DV;
+            const uint32_t d0 = CAUSAL ? D_P : D_U, nb = (CAUSAL ? kC + DV : DV) + (ZF ? 16 : 0);
             mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, false);
             if constexpr (SPLIT) {
                 mma_pass_ss(tbase + d0, ta0, kAtom, tb1 + b0, nb, AS, true);
                 mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
             }
+            if constexpr (!ZF)   // Gq [Z_hi | Z_lo] on its own
+                mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, false);
             mma_commit(BAR_M);
             if (CAUSAL) {   // the previous output tile has left the staging tile, which takes V next
                 bulk_wait_read();
@@ -553,43 +578,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             }
         }
         __syncwarp();
-        // while the tensor core works: the partial Gamma_Q,i . Z over this thread's 32 components
-        // (thread 0, which issues the MMA, leaves its part to thread 128: the same row, the next
-        // quarter)
-        auto qz_part = [&](int row, int gq) {
-            float qz = 0.f;
-#pragma unroll
-            for (int pl = 0; pl < NP; ++pl)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int k = 32 * gq + 8 * q;
-                    const uint4 t = *reinterpret_cast<const uint4 *>((pl ? ta1 : ta0) + sw128_offset(row, k, kC, 2));
-                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        qz = fmaf(bf(w[e] & 0xffffu), z_s[k + 2 * e], qz);
-                        qz = fmaf(__uint_as_float(w[e] & 0xffff0000u), z_s[k + 2 * e + 1], qz);
-                    }
-                }
-            part[gq * kK + row] = qz;
-        };
-        if (tid != 0) qz_part(i, g);
-        if (tid == 128) qz_part(0, 0);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR_Q);   // this warp is past its reads of the A images and of Z
         ok = mbar_wait(BAR_M, ph) && ok;
         fence_after_sync();
-        if (tid == 0) {
-            // the MMA has read B and the A images and every warp is past its reads of the A
-            // images and Z: the next item's tiles and memory may land in them
-            ok = mbar_wait(BAR_Q, ph) && ok;
-            fence_proxy_async();
-            if (more && ok) {
-                load_gamma(it + 1);
-                load_memory(it + 1);
-                pend_g = pend_s = true;
-                ph_g = ph_s = ph ^ 1u;
-            }
+        if (tid == 0 && more && ok) {
+            // the MMA has read B, the A images and the Z rows (no thread reads them): the next
+            // item's tiles and memory may land in them
+            load_gamma(it + 1);
+            load_memory(it + 1);
+            pend_g = pend_s = true;
+            ph_g = ph_s = ph ^ 1u;
         }
         if constexpr (CAUSAL) {
             // V into token-major images in the staging tile, the B operand (MN-major) of
@@ -630,7 +627,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         x[16 * b + j] = jj <= i ? __uint_as_float(r[j]) : 0.f;
                     }
                 }
-                part[(4 + g) * kK + i] = put_a32<SPLIT>(tbase, lane0, A_PM_HI, A_PM_LO, 32 * g, x);
+                part[g * kK + i] = put_a32<SPLIT>(tbase, lane0, A_PM_HI, A_PM_LO, 32 * g, x);
             }
             tmem_wait_st();
             fence_proxy_async();
@@ -658,9 +655,18 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             fence_after_sync();
         }
 
-        float den = eps;
+        // den = Gq . Z (two halves) + the row sum of P_m + eps
+        float den;
+        {
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, lane0, D_Z), r);
+            tmem_wait_ld();
+            den = eps + (__uint_as_float(r[0]) + __uint_as_float(r[1]));
+        }
+        if constexpr (CAUSAL) {
 #pragma unroll
-        for (int q = 0; q < (CAUSAL ? 8 : 4); ++q) den += part[q * kK + i];
+            for (int q = 0; q < 4; ++q) den += part[q * kK + i];
+        }
         const float inv = 1.0f / den;
         // the output tile, in boxes of 64 rows x 32 columns (box (i / 64) (d_v / 32) + c / 32)
 #pragma unroll
@@ -763,12 +769,13 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     }
     // memory blocks in operand form: rows of 256 bytes (hi plane, lo plane, Z), d_v rows per box
     ok = ok && make_tma_2d(&maps.s, mem, true, blocks * (2 * DV + 2), kK, DV) &&
+         make_tma_2d(&maps.z, mem, true, blocks * (2 * DV + 2), kK, 2) &&
          make_tma_3d(&maps.o, out, false, DV, dm.N, dm.BH(), 64);
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, reinterpret_cast<const float *>(mem), out);
+        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, out);
     return cudaGetLastError();
 }
 
