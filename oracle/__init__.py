@@ -32,13 +32,25 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_to(src: str, lib: str) -> None:
+    """gcc, plain IEEE double: no fast-math, no FMA contraction."""
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-ffp-contract=off", "-fPIC",
+                           "-shared", "-o", lib, src, "-lm"])
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain IEEE double: no fast-math, no FMA contraction)."""
+    """Compile the oracle (once; again when the C source is newer).
+
+    GMA_ORACLE_LIB, when set, names an already built library to load instead:
+    the tests that plant a mistake in a copy of the oracle use it to run the
+    pins against the mutated build."""
+    override = os.environ.get("GMA_ORACLE_LIB")
+    if override:
+        return override
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-ffp-contract=off", "-fPIC",
-                               "-shared", "-o", tmp, _SRC, "-lm"])
+        compile_to(_SRC, tmp)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
