@@ -84,8 +84,9 @@ def stage_work(stage, wl):
       bidir_read          2*K*(d_v+1)           (Gq [Vt | Z])
       decode (per (b,h))  8*K*d + 4*K*(d_v+1)   (two routings, update and read)
     Bytes are the minimum each launch must move: its inputs once and its
-    outputs once (fp32 state of K*(d_v+1) per block of the scan; for the
-    decode step the whole state in and out).
+    outputs once (fp32 state of K*(d_v+1) per block of the scan, blocks of C
+    rows on the tensor-core path and of 256 rows otherwise; for the decode
+    step the whole state in and out).
     """
     K, d, dv = wl.K, wl.d, wl.dv
     xb = 2 if wl.x_dtype == "bf16" else 4
@@ -100,7 +101,9 @@ def stage_work(stage, wl):
     ht = wl.B * wl.H * wl.N
     C = eff_chunk(wl)
     tc = stage.endswith("_tc")
-    blk = C if tc else 256
+    # blocks of the carried memory: chunks of C rows on the tensor-core path (its scan too),
+    # blocks of 256 rows on the CUDA-core path
+    blk = C if tc or (stage in ("state_scan", "state_reduce") and C == 128) else 256
     nblk = wl.B * wl.H * -(-wl.N // blk)
     if stage in ("resp_q", "resp_k"):
         # K = 128, d = 64: the bound GEMM [x^2 | x] W has the same 4*K*d flop per row and runs on the
@@ -114,8 +117,10 @@ def stage_work(stage, wl):
         return fl * ht, ("tensor_bf16" if tc else "alu"), (2 * K * gb + dv * vb + 4 * dv) * ht + st * nblk
     if stage in ("bidir_read", "bidir_read_tc"):
         return 2.0 * K * (dv + 1) * ht, ("tensor_bf16" if tc else "alu"), (K * gb + 4 * dv) * ht + st * wl.B * wl.H
-    if stage in ("state_scan", "state_reduce"):
+    if stage == "state_scan":     # every block's partial in, its carried memory out
         return 0.0, "alu", 2.0 * st * nblk
+    if stage == "state_reduce":   # every block's partial in, one total per (b, h) out
+        return 0.0, "alu", st * (nblk + wl.B * wl.H)
     return 0.0, "alu", 0.0
 
 
