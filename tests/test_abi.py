@@ -129,3 +129,68 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gma, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         gma.load()
+
+
+def _prm():
+    return gma._Params(FAKE, FAKE, FAKE)
+
+
+def test_bidir_validation(lib):
+    s = _shape(N=300)
+    need = gma.gma_workspace_size(s, gma.OP_BIDIR)
+    call = lambda shape=s, q=FAKE, k=FAKE, v=FAKE, o=FAKE, ws=FAKE, wn=need: lib.gma_forward_bidir(
+        ctypes.byref(shape) if shape is not None else None, _prm(), q, k, v, o, ws, wn, None)
+    assert call(shape=None) == 1
+    assert call(q=None) == 1 and call(k=None) == 1 and call(v=None) == 1 and call(o=None) == 1
+    assert call(v=FAKE + 4) == 3 and call(o=FAKE + 8) == 3
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    assert call(shape=_shape(d_route=48)) == 2 and call(shape=_shape(K=513)) == 2
+    assert call(shape=_shape(eps=float("inf"))) == 1
+    bad = gma._Params(FAKE, None, FAKE)
+    assert lib.gma_forward_bidir(ctypes.byref(s), bad, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 1
+    bad = gma._Params(FAKE, FAKE, FAKE + 4)
+    assert lib.gma_forward_bidir(ctypes.byref(s), bad, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 3
+
+
+def test_decode_validation(lib):
+    s = _shape(B=4, N=0)
+    need = gma.gma_workspace_size(s, gma.OP_DECODE)
+    assert need > 0
+    call = lambda q=FAKE, k=FAKE, v=FAKE, st=FAKE, o=FAKE, ws=FAKE, wn=need: lib.gma_decode_step(
+        ctypes.byref(s), _prm(), q, k, v, st, o, ws, wn, None)
+    # every pointer is required (one token per sequence, whatever N says)
+    for kw in ("q", "k", "v", "st", "o"):
+        assert call(**{kw: None}) == 1, kw
+        assert call(**{kw: FAKE + 4}) == 3, kw
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    # the decode step's scratch holds only the prepared parameters: packed {1/sigma, -mu/sigma}
+    # (16 bytes per component and feature pair) and c_k, each rounded up to 256 bytes
+    up = lambda n: -(-n // 256) * 256
+    assert need == up(s.H * s.K * (s.d_route // 2) * 16) + up(s.H * s.K * 4)
+
+
+def test_responsibilities_validation(lib):
+    s = _shape(N=300)
+    need = gma.gma_workspace_size(s, gma.OP_RESPONSIBILITIES)
+    call = lambda x=FAKE, g=FAKE, ws=FAKE, wn=need: lib.gma_responsibilities(
+        ctypes.byref(s), _prm(), x, g, ws, wn, None)
+    assert call(x=None) == 1 and call(g=None) == 1
+    assert call(x=FAKE + 2) == 3 and call(g=FAKE + 12) == 3
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    # the caller's Gamma is the output: the scratch is smaller than a forward's
+    assert need < gma.gma_workspace_size(s, gma.OP_CAUSAL)
+
+
+def test_profiled_entries_need_a_profile(lib):
+    s = _shape(N=300)
+    wn = 1 << 40
+    assert lib.gma_forward_causal_profiled(ctypes.byref(s), _prm(), FAKE, FAKE, FAKE, None, None, FAKE,
+                                           FAKE, wn, None, None) == 1
+    assert lib.gma_forward_bidir_profiled(ctypes.byref(s), _prm(), FAKE, FAKE, FAKE, FAKE, FAKE, wn, None,
+                                          None) == 1
+    assert lib.gma_decode_step_profiled(ctypes.byref(s), _prm(), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, wn,
+                                        None, None) == 1
+    # a profile whose events are missing is rejected before anything is recorded
+    prof = gma.Profile()
+    assert lib.gma_forward_causal_profiled(ctypes.byref(s), _prm(), FAKE, FAKE, FAKE, None, None, FAKE,
+                                           FAKE, wn, None, ctypes.byref(prof)) == 1
