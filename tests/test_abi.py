@@ -194,3 +194,17 @@ def test_profiled_entries_need_a_profile(lib):
     prof = gma.Profile()
     assert lib.gma_forward_causal_profiled(ctypes.byref(s), _prm(), FAKE, FAKE, FAKE, None, None, FAKE,
                                            FAKE, wn, None, ctypes.byref(prof)) == 1
+
+
+def test_binding_refuses_host_tensors():
+    """No CPU fallback: the device entries take CUDA tensors only, and say so before any call."""
+    import torch
+    s = _shape(B=1, H=1, N=8, d_route=64, d_v=64, K=128)
+    x = torch.zeros(1, 1, 8, 64)
+    o = torch.zeros(1, 1, 8, 64)
+    p = (torch.zeros(1, 128, 64), torch.zeros(1, 128, 64), torch.zeros(1, 128))
+    for call in (lambda: gma.gma_forward_causal(s, *p, x, x, x, o),
+                 lambda: gma.gma_forward_bidir(s, *p, x, x, x, o),
+                 lambda: gma.gma_responsibilities(s, *p, x, torch.zeros(1, 1, 8, 128))):
+        with pytest.raises(TypeError, match="CUDA tensor"):
+            call()
