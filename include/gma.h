@@ -33,7 +33,10 @@
  *     gma_workspace_size(shape, op) bytes (GMA_ERR_WORKSPACE otherwise).  Its
  *     contents on entry are ignored and on return are unspecified.  Calls
  *     that run concurrently must use different workspaces.
- *   - The library keeps no global state; calls are reentrant.
+ *   - Calls are reentrant.  The library's only global state is created once
+ *     and never changes results: the two copy streams per device of
+ *     gma_forward_causal_host (created by its first call), the scratch array
+ *     of gma_decode_step_noalloc, and the thread-local last CUDA error.
  *
  * Supported sizes: d_route in {16, 32, 64, 128}; d_v in {16, 32, 64, 128};
  * 1 <= K <= 512; B, H, N >= 1 with B*H*N*max(d_route, d_v, K) < 2^40;
