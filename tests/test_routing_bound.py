@@ -21,15 +21,13 @@ def _bf(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
 
 
-def _estimate_error(mu, var_raw, logit_pi, x):
-    """(max over rows and components of |l~ - l| / delta, max |l~ - l|, max |c'|)."""
-    K, d = mu.shape
-    # fp64 log-joints (the 2 pi term cancels in the posterior and is left out on both sides)
+def _estimates(mu, var_raw, logit_pi, x):
+    """(l~ [n,K] as the kernel forms it, delta [n], fp64 log-joints [n,K], c' [K]).
+    The 2 pi term cancels in the posterior and is left out on both sides."""
     v64 = np.logaddexp(0.0, var_raw.astype(np.float64))
     lpi = logit_pi.astype(np.float64) - np.logaddexp.reduce(logit_pi.astype(np.float64))
     dx = x.astype(np.float64)[:, None, :] - mu.astype(np.float64)[None]
     exact = lpi[None] - 0.5 * np.log(v64).sum(1)[None] - 0.5 * (dx * dx / v64[None]).sum(-1)
-    # the estimate as the kernel forms it
     v32 = np.logaddexp(np.float32(0), var_raw.astype(np.float32)).astype(np.float32)
     s = (1.0 / np.sqrt(v32)).astype(np.float32)
     ms = (-mu.astype(np.float32) * s).astype(np.float32)
@@ -38,9 +36,14 @@ def _estimate_error(mu, var_raw, logit_pi, x):
     cp = (c - np.float32(0.5) * (ms * ms).sum(1, dtype=np.float32)).astype(np.float32)
     w = np.concatenate([_bf(-0.5 * s * s), _bf(-s * ms)], 1)
     a = np.concatenate([_bf(x * x), _bf(x)], 1)
-    est = a @ w.T + cp[None]
     s2 = (x.astype(np.float32) ** 2).sum(1)
-    delta = 4e-3 * (0.5 * (s * s).max() * s2 + np.abs(s * ms).max() * np.sqrt(d) * np.sqrt(s2)) + 1e-3
+    delta = 4e-3 * (0.5 * (s * s).max() * s2 + np.abs(s * ms).max() * np.sqrt(mu.shape[1]) * np.sqrt(s2)) + 1e-3
+    return a @ w.T + cp[None], delta, exact, cp
+
+
+def _estimate_error(mu, var_raw, logit_pi, x):
+    """(max over rows and components of |l~ - l| / delta, max |l~ - l|, max |c'|)."""
+    est, delta, exact, cp = _estimates(mu, var_raw, logit_pi, x)
     err = np.abs(est - exact)
     return (err / delta[:, None]).max(), err.max(), np.abs(cp).max()
 
@@ -78,3 +81,24 @@ def test_constant_rounding_beyond_the_bound_stays_far_inside_the_margin():
     ratio, err, cmax = _estimate_error(mu, vr, lp, np.zeros((4, 64), np.float32))
     assert cmax > 1e4 and ratio > 1.0            # the regime the 1e-3 does not cover
     assert err <= 1e-6 * cmax and err < 1.0 < T
+
+
+@pytest.mark.parametrize("dist", ["normal", "peaked"])
+def test_kept_set_posterior_equals_the_dense_one(dist):
+    """The softmax over the kept set {k : l~_k >= max l~ - T - 2 delta} (a row whose
+    second-best estimate falls below that threshold keeps its argmax alone, with
+    posterior 1) differs from the dense posterior by at most the dropped mass,
+    K e^-30 ~ 1.2e-11 of the row."""
+    wl, mu, vr, lp = _head()
+    x = workloads.full_inputs(wl.with_(dist=dist))[0][0, 0]
+    est, delta, exact, _ = _estimates(mu, vr, lp, x)
+    keep = est >= est.max(1, keepdims=True) - T - 2.0 * delta[:, None]
+    dense = np.exp(exact - exact.max(1, keepdims=True))
+    dense /= dense.sum(1, keepdims=True)
+    kept = np.where(keep, np.exp(exact - exact.max(1, keepdims=True)), 0.0)
+    kept /= kept.sum(1, keepdims=True)
+    assert np.abs(kept - dense).max() <= 128 * np.exp(-30.0)
+    single = keep.sum(1) == 1
+    if dist == "peaked":
+        assert single.mean() > 0.9           # most peaked rows take the single-component shortcut
+    assert np.all(kept[single].max(1) == 1.0)
