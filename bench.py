@@ -44,8 +44,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--batch", type=int, default=0,
                    help="run the workload with this many sequences instead of its own B (profiling captures)")
-    p.add_argument("--min-warmup-s", type=float, default=1.0,
-                   help="keep warming up (at least --warmup steps) until this many seconds passed")
+    p.add_argument("--clock-soak-s", type=float, default=1.0,
+                   help="after the --warmup steps, run untimed steps for this many seconds right before "
+                        "the timed region, so that the clock sampler (100 ms period) sees the GPU under "
+                        "this load (reported as clock_soak, not as warm-up)")
     return p.parse_args()
 
 
@@ -69,7 +71,10 @@ def eff_chunk(wl):
 
 
 def stage_work(stage, wl):
-    """Algorithmic work of one launch of a stage: (flop, pipe, bytes).
+    """Work of one launch of a stage as the kernel runs it: (flop, pipe, bytes),
+    the bytes being everything the launch must move, the materialised
+    responsibilities and the per-chunk memory included (the kernel-byte model;
+    compare it with the DRAM counters).
 
     Per head-token (ht), with d = d_route, K components, d_v values, chunk C
     (flop):
@@ -122,6 +127,77 @@ def stage_work(stage, wl):
     if stage == "state_reduce":   # every block's partial in, one total per (b, h) out
         return 0.0, "alu", st * (nblk + wl.B * wl.H)
     return 0.0, "alu", 0.0
+
+
+def algorithmic_work(stage, wl, kept=None):
+    """Algorithmic work of one launch of a stage, as the roofline charges it:
+    (flop, pipe, bytes).
+
+    Bytes: only the method's own input and output (read Q_X, K_X and V once,
+    write O once; for the decode step also the recurrent state in and out,
+    which is the method's memory).  Each launch is charged with the part of
+    that I/O it consumes or produces:
+      resp_q / resp_k      Q_X or K_X in
+      chunk_state(_tc) /
+      block_state          V in
+      chunk_out(_tc)       V in, O out
+      bidir_read(_tc)      O out
+      scans, reductions,
+      parameter prep       nothing
+    Materialised responsibilities and the per-chunk carried memory are
+    overhead of this implementation and are not counted (they appear in
+    `stage_work`, the kernel-byte model).
+
+    Flop: the method's contractions as `stage_work` counts them.  For the
+    bounded routing (K = 128, d = 64) the flop are the bound GEMM on the bf16
+    tensor pipe plus the exact evaluation of the kept components on the FP32
+    pipe (`kept` = mean kept components per row, measured), whichever takes
+    longer at its peak; elsewhere the dense FP32 routing."""
+    flop, pipe, _ = stage_work(stage, wl)
+    if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k"):
+        pipe = "tensor"   # the chunk products at the rate of their operand type (tf32 for fp32)
+    d, dv = wl.d, wl.dv
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    vb = 2 if wl.v_dtype == "bf16" else 4
+    if wl.mode == "decode":
+        return stage_work(stage, wl)
+    ht = wl.B * wl.H * wl.N
+    if stage in ("resp_q", "resp_k"):
+        nbytes = d * xb * ht
+        if bounded_routing(wl) and kept is not None:
+            return 4.0 * d * kept * ht, "alu_kept", nbytes
+        return flop, pipe, nbytes
+    if stage in ("block_state", "chunk_state_tc"):
+        return flop, pipe, dv * vb * ht
+    if stage in ("chunk_out", "chunk_out_tc"):
+        return flop, pipe, (dv * vb + 4 * dv) * ht
+    if stage in ("bidir_read", "bidir_read_tc"):
+        return flop, pipe, 4 * dv * ht
+    return flop, pipe, 0.0
+
+
+def roofline_of(stage, wl, t_launch, pk, kept=None):
+    """The roofline object of one launch taking t_launch seconds: the bound is the
+    slower of its algorithmic flop at the pipe's peak and its algorithmic bytes at
+    the measured HBM rate; `frac` = achieved / peak on that bound.  Also the same
+    launch against the kernel-byte model (`kernel_bytes`, `frac_kernel_bytes`)."""
+    flop, pipe, nbytes = algorithmic_work(stage, wl, kept)
+    if pipe == "alu_kept":   # bounded routing: the bound GEMM (tensor) or the kept exact work (FP32)
+        t_fp = flop / pipe_peak("alu", wl, pk)
+        t_tc = stage_work(stage, wl)[0] / pipe_peak("tensor_bf16", wl, pk)
+        flop, pipe = (flop, "alu") if t_fp >= t_tc else (stage_work(stage, wl)[0], "tensor_bf16")
+    t_flop = flop / pipe_peak(pipe, wl, pk) if flop else 0.0
+    t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_flop >= t_mem:
+        bound = "alu" if pipe == "alu" else "tensor"
+        achieved, peak, unit = flop / t_launch / 1e12, pipe_peak(pipe, wl, pk) / 1e12, "TFLOP/s"
+    else:
+        bound = "hbm"
+        achieved, peak, unit = nbytes / t_launch / 1e9, pk["hbm_gbs"], "GB/s"
+    kb = stage_work(stage, wl)[2]
+    return {"bound": bound, "kernel": stage, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "algorithmic_bytes": nbytes, "algorithmic_flop": flop,
+            "kernel_bytes": kb, "frac_kernel_bytes": kb / t_launch / 1e9 / pk["hbm_gbs"]}
 
 
 def bounded_routing(wl):
@@ -211,9 +287,17 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, t_soak=None):
+        """Clock record of the timed region [t0, t1]; when it holds fewer than three
+        samples, of the clock soak and the timed region [t_soak, t1] (the same load
+        just before it), else of the whole record.  `window` says which."""
+        window = "timed"
         win = [p for t, p in self.samples if t0 <= t <= t1]
+        if len(win) < 3 and t_soak is not None:
+            window = "soak+timed"
+            win = [p for t, p in self.samples if t_soak <= t <= t1]
         if len(win) < 3:
+            window = "run"
             win = [p for _, p in self.samples]
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
@@ -229,7 +313,8 @@ class ClockSampler:
         reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower().startswith("active")})
         pw = [num(p[2]) for p in win if num(p[2]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(win), "power_w_max": max(pw) if pw else None}
+                "reasons": reasons, "samples": len(win), "power_w_max": max(pw) if pw else None,
+                "window": window}
 
 
 # ----------------------------------------------------------------- helpers ----
@@ -535,15 +620,23 @@ def main():
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", ""))
     clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
-    # warm-up: at least --warmup steps and --min-warmup-s seconds (keeps the clock sampler fed)
-    t_w = time.time()
-    nw = 0
-    while nw < args.warmup or time.time() - t_w < args.min_warmup_s:
+    # warm-up: exactly --warmup steps
+    for i in range(args.warmup):
         run.profiled(warm_events)
-        nw += 1
-        if nw % 20 == 0:
+        if i % 20 == 19:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
+    # clock soak: untimed steps right before the timed region, so that nvidia-smi samples the
+    # clocks under this load (a timed region of a few ms holds no 100 ms sample of its own)
+    t_soak0 = time.time()
+    n_soak = 0
+    while time.time() - t_soak0 < args.clock_soak_s:
+        run.profiled(warm_events)
+        n_soak += 1
+        if n_soak % 20 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    soak_s = time.time() - t_soak0
 
     if pg:
         pg.barrier()
@@ -560,7 +653,7 @@ def main():
     if pg:
         pg.barrier()
     total_ms = max_over_ranks(pg, start.elapsed_time(end), dev)
-    clocks_summary = clocks.summary(t_host0, t_host1)
+    clocks_summary = clocks.summary(t_host0, t_host1, t_soak0)
 
     ms = total_ms / args.steps
     tokens = tokens_per_step(wl)
@@ -571,17 +664,8 @@ def main():
                                        for s_ in range(args.steps))
     dom = max(stage_ms, key=stage_ms.get)
     pk, pk_kind = peaks()
-    flop, pipe, nbytes = stage_work(dom, wl)
-    t_dom = stage_ms[dom] * 1e-3
-    t_flop = flop / pipe_peak(pipe, wl, pk)
-    t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
-    if t_flop >= t_mem:
-        bound = "alu" if pipe == "alu" else "tensor"
-        achieved, peak, r_unit = flop / t_dom / 1e12, pipe_peak(pipe, wl, pk) / 1e12, "TFLOP/s"
-    else:
-        bound = "hbm"
-        achieved, peak, r_unit = nbytes / t_dom / 1e9, pk["hbm_gbs"], "GB/s"
     kept = run.kept_per_row() if (bounded_routing(wl) and wl.mode != "decode") else None
+    roof = roofline_of(dom, wl, stage_ms[dom] * 1e-3, pk, kept)
     roof_s, roof_parts = path_roofline_s(wl, pk, kept)
 
     # end to end through the plain public entry point: pinned host inputs in, result out, every step
@@ -620,19 +704,19 @@ def main():
         line = {
             "metric": METRIC if wl.mode == "causal" else f"GMA {wl.mode} tokens/sec ({wl.name})",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": nw, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if wl.gemm_dtype == "f32" else "f32+bf16",
             "data": "synthetic", "config": cfg,
-            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": r_unit,
-                         "frac": achieved / peak, "traffic": tr,
+            "roofline": {**roof, "traffic": tr,
                          "peak_source": ("152 SMs x 128 FP32 lanes x 2 x max SM clock (%s)" % pk_kind)
-                         if bound == "alu" else pk_kind},
+                         if roof["bound"] == "alu" else pk_kind},
             "path_roofline": {"tokens_per_s": tokens / roof_s, "frac": value / world / (tokens / roof_s),
                               **{k2.replace("_s", "_ms"): v2 * 1e3 for k2, v2 in roof_parts.items()},
                               "kept_components_per_row": kept},
             "stages_ms": stage_ms,
             "gpu_launches": len(names) * args.steps,
             "clocks": clocks_summary,
+            "clock_soak": {"steps": n_soak, "s": round(soak_s, 3)},
             "e2e": {"value": whole_job_rate(world, tokens, e_ms), "unit": "tokens/s", "ms_per_step": e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "entry": "gma_forward_causal_host" if wl.mode == "causal" else "device entry + torch copies"},
