@@ -6,6 +6,7 @@
 
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 using namespace gma;
@@ -132,6 +133,20 @@ thread_local cudaError_t g_last_cuda = cudaSuccess;
         }                                                                                                  \
     } while (0)
 
+// A bounded device wait that expired since the last report on the current device:
+// GMA_ERR_TIMEOUT once (the flag is cleared), else GMA_OK.  Never allocates and
+// never synchronises: a timeout becomes visible once the kernel that hit it has
+// written the flag.
+gma_status take_timeout()
+{
+    volatile unsigned int *f = timeout_flag_host();
+    if (f && *f) {
+        *f = 0u;
+        return GMA_ERR_TIMEOUT;
+    }
+    return GMA_OK;
+}
+
 template <typename T>
 T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
 
@@ -186,6 +201,7 @@ const char *gma_status_string(gma_status status)
     case GMA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case GMA_ERR_WORKSPACE: return "workspace missing or too small";
     case GMA_ERR_CUDA: return "CUDA error";
+    case GMA_ERR_TIMEOUT: return "a bounded device wait expired";
     default: return "unknown status";
     }
 }
@@ -193,6 +209,7 @@ const char *gma_status_string(gma_status status)
 gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const void *x, float *gamma,
                                 void *ws, size_t ws_bytes, gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     Dims dm;
     GMA_TRY(make_dims(shape, &dm, GMA_OP_RESPONSIBILITIES));
     GMA_TRY(check_params(params));
@@ -401,12 +418,14 @@ gma_status gma_forward_causal(const gma_shape *shape, gma_params params, const v
                               const void *v, const float *state_in, float *state_out, float *out, void *ws,
                               size_t ws_bytes, gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, nullptr);
 }
 
 gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx, const void *kx,
                              const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     return run_bidir(shape, params, qx, kx, v, out, ws, ws_bytes, stream, nullptr);
 }
 
@@ -414,6 +433,7 @@ gma_status gma_forward_bidir_profiled(const gma_shape *shape, gma_params params,
                                       const void *kx, const void *v, float *out, void *ws, size_t ws_bytes,
                                       gma_stream_t stream, gma_profile *prof)
 {
+    GMA_TRY(take_timeout());
     if (!prof) return GMA_ERR_INVALID_ARG;
     return run_bidir(shape, params, qx, kx, v, out, ws, ws_bytes, stream, prof);
 }
@@ -422,6 +442,7 @@ gma_status gma_decode_step(const gma_shape *shape, gma_params params, const void
                            const void *v, float *state, float *out, void *ws, size_t ws_bytes,
                            gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     return run_decode(shape, params, qx, kx, v, state, out, ws, ws_bytes, stream, nullptr);
 }
 
@@ -429,6 +450,7 @@ gma_status gma_decode_step_profiled(const gma_shape *shape, gma_params params, c
                                     const void *v, float *state, float *out, void *ws, size_t ws_bytes,
                                     gma_stream_t stream, gma_profile *prof)
 {
+    GMA_TRY(take_timeout());
     if (!prof) return GMA_ERR_INVALID_ARG;
     return run_decode(shape, params, qx, kx, v, state, out, ws, ws_bytes, stream, prof);
 }
@@ -438,6 +460,7 @@ gma_status gma_forward_causal_profiled(const gma_shape *shape, gma_params params
                                        float *state_out, float *out, void *ws, size_t ws_bytes,
                                        gma_stream_t stream, gma_profile *prof)
 {
+    GMA_TRY(take_timeout());
     if (!prof) return GMA_ERR_INVALID_ARG;
     return run_causal(shape, params, qx, kx, v, state_in, state_out, out, ws, ws_bytes, stream, prof);
 }
@@ -489,6 +512,7 @@ extern "C" gma_status gma_forward_causal_host(const gma_shape *shape, gma_params
                                               float *state_out, float *out, void *ws, size_t ws_bytes,
                                               gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     Dims dm;
     GMA_TRY(make_dims(shape, &dm));
     GMA_TRY(check_params(params));
@@ -549,25 +573,27 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[GMA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_noalloc_once[kMaxDevices];
-void *g_noalloc_addr[kMaxDevices];
-cudaError_t g_noalloc_err[kMaxDevices];
+std::atomic<void *> g_noalloc_addr[kMaxDevices];
 
 // Device address of the array on the current device.  In host code the
-// array's name only stands in for it, so the address is looked up once per
-// device, with that device current.
+// array's name only stands in for it, so the address is looked up with that
+// device current, and kept once a lookup has succeeded (a failed lookup, for
+// example one made during a stream capture, is retried by the next call).
 gma_status noalloc_scratch(void **addr)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return GMA_ERR_UNSUPPORTED;
-    std::call_once(g_noalloc_once[dev], [dev] {
-        void *p = nullptr;
-        g_noalloc_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_noalloc_addr[dev] = p;
-    });
-    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_addr[dev]) return GMA_ERR_CUDA;
-    *addr = g_noalloc_addr[dev];
+    void *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            g_last_cuda = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            return GMA_ERR_CUDA;
+        }
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *addr = p;
     return GMA_OK;
 }
 
@@ -577,6 +603,7 @@ extern "C" gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params
                                               const void *kx, const void *v, float *state, float *out,
                                               gma_stream_t stream)
 {
+    GMA_TRY(take_timeout());
     Dims dm;
     GMA_TRY(make_dims(shape, &dm, GMA_OP_DECODE));
     GMA_TRY(check_params(params));
@@ -594,5 +621,22 @@ extern "C" gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params
     float *cst = at<float>(ws, wp.cst);
     GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
+    return GMA_OK;
+}
+
+extern "C" gma_status gma_sync_status(gma_stream_t stream)
+{
+    const cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        g_last_cuda = e;
+        return GMA_ERR_CUDA;
+    }
+    return take_timeout();
+}
+
+extern "C" gma_status gma_test_wait_timeout(long long limit_cycles, gma_stream_t stream)
+{
+    if (limit_cycles < 1 || limit_cycles > 4000000000LL) return GMA_ERR_INVALID_ARG;
+    GMA_CUDA(launch_expire_wait(limit_cycles, reinterpret_cast<cudaStream_t>(stream)));
     return GMA_OK;
 }

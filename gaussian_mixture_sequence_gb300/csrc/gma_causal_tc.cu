@@ -138,7 +138,7 @@ struct StateMaps {
 template <bool SPLIT, int DV>
 __global__ void __launch_bounds__(kStateThreads, 1)
     k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items,
-                     const void *__restrict__ v, bool v_bf16, float *__restrict__ partial)
+                     const void *__restrict__ v, bool v_bf16, float *__restrict__ partial, unsigned int *timeout)
 {
     using Sm = StateSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP, NBV = Sm::NBV;
@@ -316,18 +316,20 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     }
     // the last chunk issued, once its MMA is done (chains complete in order, so this also
     // covers every earlier one after a failure)
+    bool ok_end = ok;
     if (nm > 0) {
         const int jl = nm - 1, bl = jl & 1;
         const bool okm = mbar_wait(smem_addr(bar + 2 + bl), (uint32_t)((jl >> 1) & 1));
         fence_after_sync();
         take(it0 + jl, bl, ok && okm);
+        ok_end = ok_end && okm;
     }
     // after a failed wait: let the landings in flight arrive before the shared memory is released
     if (tid == 0)
         for (int b = 0; b < 2; ++b)
-            if (pend[b]) (void)mbar_wait(smem_addr(bar + b), ph_l[b]);
+            if (pend[b]) ok_end = mbar_wait(smem_addr(bar + b), ph_l[b]) && ok_end;
     fence_before_sync();
-    __syncthreads();
+    if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -440,7 +442,7 @@ struct OutMaps {
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
-                   const void *__restrict__ v, bool v_bf16, float *__restrict__ out)
+                   const void *__restrict__ v, bool v_bf16, float *__restrict__ out, unsigned int *timeout)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
@@ -711,17 +713,44 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         }
     }
     // after a failed wait: let the copies still in flight land before the shared memory is released
+    bool ok_end = ok;
     if (tid == 0) {
-        if (pend_g) (void)mbar_wait(BAR_G, ph_g);
-        if (pend_s) (void)mbar_wait(BAR_S, ph_s);
+        if (pend_g) ok_end = mbar_wait(BAR_G, ph_g) && ok_end;
+        if (pend_s) ok_end = mbar_wait(BAR_S, ph_s) && ok_end;
         bulk_wait_all();
     }
     fence_before_sync();
-    __syncthreads();
+    if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ------------------------------------------------------------------------
+// A kernel whose only work is one bounded wait that expires: it waits for the
+// first phase of an mbarrier that nothing arrives on (no copy and no MMA is
+// ever issued against it), gives up after `limit` SM cycles and records the
+// timeout exactly as the kernels above do.  Nothing asynchronous is in flight
+// when it returns.
+__global__ void __launch_bounds__(32, 1) k_expire_wait(long long limit, unsigned int *timeout)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(smem_addr(&bar), 0u, limit);
+    if (__syncthreads_and(ok) == 0 && threadIdx.x == 0) report_timeout(timeout);
+}
+
 } // namespace
+
+cudaError_t launch_expire_wait(long long limit_cycles, cudaStream_t st)
+{
+    unsigned int *flag = timeout_flag_dev();
+    if (!flag) return cudaErrorMemoryAllocation;
+    k_expire_wait<<<1, 32, 0, st>>>(limit_cycles, flag);
+    return cudaGetLastError();
+}
 
 bool tc_path_eligible(int K, int DV, bool g_bf16) { return K == kK && (DV == 64 || (DV == 128 && g_bf16)); }
 
@@ -731,7 +760,8 @@ template <bool SPLIT, int DV>
 cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *partial, cudaStream_t st)
 {
     constexpr size_t smem = StateSmem<SPLIT, DV>::bytes;
-    static cudaError_t attr = allow_smem(k_chunk_state_tc<SPLIT, DV>, smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_chunk_state_tc<SPLIT, DV>, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     StateMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
@@ -742,8 +772,10 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
     if (!SPLIT) maps.gk[1] = maps.gk[0];
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
+    unsigned int *flag = timeout_flag_dev();
+    if (!flag) return cudaErrorMemoryAllocation;
     k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, v, dm.v_bf16,
-                                                                   partial);
+                                                                   partial, flag);
     return cudaGetLastError();
 }
 
@@ -752,7 +784,8 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
                    float *out, cudaStream_t st)
 {
     constexpr size_t smem = OutSmem<SPLIT, DV>::bytes;
-    static cudaError_t attr = allow_smem(k_chunk_out_tc<SPLIT, DV, CAUSAL>, smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_chunk_out_tc<SPLIT, DV, CAUSAL>, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     OutMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
@@ -774,8 +807,10 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
     const int grid = (int)(items < sm_count() ? items : sm_count());
+    unsigned int *flag = timeout_flag_dev();
+    if (!flag) return cudaErrorMemoryAllocation;
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, out);
+        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, out, flag);
     return cudaGetLastError();
 }
 

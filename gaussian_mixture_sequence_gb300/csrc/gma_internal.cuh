@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/gma.h"
 
 namespace gma {
@@ -116,6 +118,15 @@ bool make_tma_3d(CUtensorMap *m, const void *base, bool bf16, unsigned long long
 // Number of SMs of the current device (persistent grids).
 int sm_count();
 
+// Timeout flag of the current device: one word in page-locked host memory
+// mapped into the device, set by a kernel whose bounded wait expired (device
+// pointer, for kernels) and read / cleared by the host (host pointer).  The
+// storage for all devices is allocated by the first call of timeout_flag_dev
+// (nullptr if that fails); timeout_flag_host never allocates and returns
+// nullptr until then.
+unsigned int *timeout_flag_dev();
+volatile unsigned int *timeout_flag_host();
+
 // Per-head images the bounded routing kernel copies into shared memory.
 struct PrunedImages {
     unsigned char *w;   // [H][32768 B]: bf16 bound matrix, 128-byte-swizzled K-major
@@ -144,13 +155,25 @@ cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float 
                               unsigned char *total, float *state_out, cudaStream_t st);
 cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
                                 const unsigned char *mem, float *out, cudaStream_t st);
+// One kernel whose single bounded wait (limit_cycles SM cycles) expires and is reported
+// through the timeout flag like the waits of the kernels above.
+cudaError_t launch_expire_wait(long long limit_cycles, cudaStream_t st);
 
-// Sets the dynamic shared-memory limit of a kernel once per process.
+// Sets the dynamic shared-memory limit of a kernel on the current device, once
+// per device (the attribute belongs to the kernel's module in that device's
+// context).  `done` is the call site's record of the devices already set.
 template <typename Kern>
-inline cudaError_t allow_smem(Kern k, size_t bytes)
+inline cudaError_t allow_smem(Kern k, size_t bytes, std::atomic<unsigned long long> &done)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
 }
 
 } // namespace gma

@@ -318,7 +318,8 @@ cudaError_t launch_chunk_out_c(const Dims &dm, bool causal, const void *gq, cons
                                float *states, float *out, cudaStream_t st)
 {
     constexpr size_t smem = ChunkSmem<DV, C>::bytes;
-    static cudaError_t attr = allow_smem(k_chunk_out<DV, C>, smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_chunk_out<DV, C>, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     const long long SZ = dm.state_size();
     const long long bh_stride = causal ? (long long)dm.nblk() * SZ : SZ;

@@ -252,7 +252,8 @@ cudaError_t launch_resp_d(const Dims &dm, const float4 *prm, const float *cst, c
 {
     using Cfg = RespCfg<D>;
     const size_t smem = Cfg::smem(dm.K);
-    static cudaError_t attr = allow_smem(k_resp<D>, Cfg::smem(512));
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_resp<D>, Cfg::smem(512), smem_set);
     if (attr != cudaSuccess) return attr;
     dim3 grid((dm.N + Cfg::ROWS_PER_CTA - 1) / Cfg::ROWS_PER_CTA, (unsigned)dm.BH());
     k_resp<D><<<grid, kThreads, smem, st>>>(dm.N, dm.K, dm.H, x, dm.x_bf16, prm, cst, gamma, ldg, layout);

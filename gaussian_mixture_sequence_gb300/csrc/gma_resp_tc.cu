@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
                   const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int BH, bool x_bf16,
                   const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
-                  const float *__restrict__ cimg, int layout, int pstride)
+                  const float *__restrict__ cimg, int layout, int pstride, unsigned int *timeout)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -580,12 +580,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // after a failed wait a routing tile may still be in flight for either group: let it land
     // (bounded) before the shared memory is released; after a normal end every fetched tile
     // has been consumed
+    bool ok_end = ok;
     if (gt == 0) {
-        if (!ok) (void)mbar_wait(BAR_X, (uint32_t)(j & 1));
+        if (!ok) ok_end = mbar_wait(BAR_X, (uint32_t)(j & 1)) && ok_end;
         bulk_wait_all();
     }
     fence_before_sync();
-    __syncthreads();
+    if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
     if (warp == 0) tmem_dealloc(*tslot, 512);
 }
 
@@ -606,7 +607,8 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
                                int layout, cudaStream_t st)
 {
     constexpr size_t smem = PrunedSmem::bytes;
-    static cudaError_t attr = allow_smem(k_resp_pruned, smem);
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_resp_pruned, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     if (ldg != kPK) return cudaErrorInvalidValue;
     CUtensorMap xmap, gmap, gmap_lo;
@@ -628,8 +630,10 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
     int pstride = (nsl / 5) | 1;
     auto gcd = [](int a, int b) { while (b) { const int t = a % b; a = b; b = t; } return a; };
     while (gcd(pstride, nsl) != 1) pstride += 2;
+    unsigned int *flag = timeout_flag_dev();
+    if (!flag) return cudaErrorMemoryAllocation;
     k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, nsl, dm.x_bf16, img.w, img.p,
-                                                 img.c, layout, pstride);
+                                                 img.c, layout, pstride, flag);
     return cudaGetLastError();
 }
 

@@ -187,6 +187,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
     return true;
 }
 
+// Records that a bounded wait of this kernel expired: one word per device in
+// host memory mapped into the device (see timeout_flag_dev), read and cleared
+// by the host.  Idempotent; any thread may call it.
+__device__ __forceinline__ void report_timeout(unsigned int *flag)
+{
+    if (flag) {
+        *reinterpret_cast<volatile unsigned int *>(flag) = 1u;
+        __threadfence_system();
+    }
+}
+
 // ---- TMA (bulk tensor copies) ----
 // Arms the barrier's current phase for one arrival plus `bytes` of transactions.
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)

@@ -1,6 +1,11 @@
 // Tensor maps for TMA (bulk tensor) loads, encoded on the host.
 #include "gma_internal.cuh"
 
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
 namespace gma {
 namespace {
 
@@ -56,16 +61,63 @@ bool make_tma_3d(CUtensorMap *m, const void *base, bool bf16, unsigned long long
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SM count per device ordinal, looked up once per device (0 = not yet known).
 int sm_count()
 {
-    static int n = [] {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-            return 152;
-        return v;
-    }();
-    return n;
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (dev < 0 || dev >= kMaxDev) {
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 152;
+    }
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+namespace {
+constexpr int kFlagDevices = 64;
+std::mutex g_flag_mu;
+std::atomic<unsigned int *> g_flags{nullptr};   // host pointer, kFlagDevices words
+
+int current_device()
+{
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kFlagDevices ? dev : -1;
+}
+} // namespace
+
+unsigned int *timeout_flag_dev()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    unsigned int *h = g_flags.load(std::memory_order_acquire);
+    if (!h) {
+        std::lock_guard<std::mutex> lk(g_flag_mu);
+        h = g_flags.load(std::memory_order_relaxed);
+        if (!h) {
+            void *p = nullptr;
+            if (cudaHostAlloc(&p, kFlagDevices * sizeof(unsigned int), cudaHostAllocMapped | cudaHostAllocPortable) !=
+                cudaSuccess)
+                return nullptr;
+            memset(p, 0, kFlagDevices * sizeof(unsigned int));
+            h = static_cast<unsigned int *>(p);
+            g_flags.store(h, std::memory_order_release);
+        }
+    }
+    void *d = nullptr;
+    if (cudaHostGetDevicePointer(&d, h + dev, 0) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(d);
+}
+
+volatile unsigned int *timeout_flag_host()
+{
+    const int dev = current_device();
+    unsigned int *h = g_flags.load(std::memory_order_acquire);
+    return dev >= 0 && h ? h + dev : nullptr;
 }
 
 } // namespace gma

@@ -91,7 +91,9 @@ def load():
                                                    ctypes.POINTER(Profile)]
         lib.gma_decode_step_profiled.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P,
                                                  ctypes.POINTER(Profile)]
-        for fn in ("gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
+        lib.gma_sync_status.argtypes = [P]
+        lib.gma_test_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        for fn in ("gma_sync_status", "gma_test_wait_timeout", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
                    "gma_forward_causal_host", "gma_forward_causal_profiled", "gma_decode_step_noalloc",
                    "gma_forward_bidir_profiled", "gma_decode_step_profiled"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -338,3 +340,21 @@ def gma_decode_step_noalloc(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, stat
     _check("gma_decode_step_noalloc",
            load().gma_decode_step_noalloc(ctypes.byref(s), prm, q, k, vv, st, o, _stream(dev, stream)))
     return out
+
+
+TIMEOUT = 6
+
+
+def gma_sync_status(device=None, stream=None):
+    """Waits for the stream (default: the current stream of `device`, default the
+    current device), then raises GMAError (status 6) if a bounded wait inside one of
+    the library's kernels expired on that device since the last report."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check("gma_sync_status", load().gma_sync_status(_stream(dev, stream)))
+
+
+def gma_test_wait_timeout(limit_cycles: int, device=None, stream=None):
+    """Enqueues the library's test kernel whose one bounded wait expires after
+    limit_cycles SM cycles (nothing is in flight when it gives up)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check("gma_test_wait_timeout", load().gma_test_wait_timeout(int(limit_cycles), _stream(dev, stream)))

@@ -33,10 +33,23 @@
  *     gma_workspace_size(shape, op) bytes (GMA_ERR_WORKSPACE otherwise).  Its
  *     contents on entry are ignored and on return are unspecified.  Calls
  *     that run concurrently must use different workspaces.
+ *   - Bounded waits.  The tensor-core kernels wait on mbarriers (for TMA
+ *     copies and tensor-core products) with a limit of about 2 s of SM
+ *     cycles.  If a wait expires, the kernel writes NaN for the rows it owns,
+ *     stops issuing work, waits (again bounded) for what it has already
+ *     issued, and returns; it also sets the device's timeout flag.  The next
+ *     compute call on that device that sees the flag returns GMA_ERR_TIMEOUT
+ *     (launching nothing) and clears it; gma_sync_status(stream) waits for
+ *     the stream and reports it deterministically.  An expired wait means the
+ *     asynchronous units did not make progress: treat the CUDA context as
+ *     unusable.
  *   - Calls are reentrant.  The library's only global state is created once
  *     and never changes results: the two copy streams per device of
  *     gma_forward_causal_host (created by its first call), the scratch array
- *     of gma_decode_step_noalloc, and the thread-local last CUDA error.
+ *     of gma_decode_step_noalloc, the timeout flags (one word per device in
+ *     page-locked host memory, allocated by the first call that launches a
+ *     tensor-core kernel: make that call before any stream capture), and the
+ *     thread-local last CUDA error.
  *
  * Supported sizes: d_route in {16, 32, 64, 128}; d_v in {16, 32, 64, 128};
  * 1 <= K <= 512; B, H, N >= 1 with B*H*N*max(d_route, d_v, K) < 2^40;
@@ -62,7 +75,8 @@ typedef enum {
     GMA_ERR_UNSUPPORTED = 2, /* valid but not implemented: d_route, d_v, K or chunk */
     GMA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
     GMA_ERR_WORKSPACE = 4,   /* ws is null or smaller than gma_workspace_size() */
-    GMA_ERR_CUDA = 5         /* a CUDA launch or runtime call failed */
+    GMA_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed */
+    GMA_ERR_TIMEOUT = 6      /* a bounded wait inside a kernel expired (see gma_sync_status) */
 } gma_status;
 
 typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype;
@@ -217,6 +231,24 @@ gma_status gma_decode_step_profiled(const gma_shape *shape, gma_params params, c
 gma_status gma_decode_step_noalloc(const gma_shape *shape, gma_params params, const void *qx,
                                    const void *kx, const void *v, float *state, float *out,
                                    gma_stream_t stream);
+
+/* Waits for `stream` to complete, then reports a bounded wait that expired in
+ * one of the library's kernels on the calling thread's current device since
+ * the last report: GMA_ERR_TIMEOUT (and the flag is cleared), GMA_ERR_CUDA if
+ * the synchronisation failed (gma_last_cuda_error names the error), else
+ * GMA_OK.  This is the status-reporting half of the bounded waits described
+ * under "Bounded waits" above (no counterpart on the pages: a property of
+ * this implementation's asynchronous kernels).                              */
+gma_status gma_sync_status(gma_stream_t stream);
+
+/* Test hook of the timeout path, with no counterpart on the pages: enqueues
+ * one kernel whose only work is a wait, bounded by limit_cycles SM cycles,
+ * on an mbarrier that nothing ever arrives on (no copy or product is issued
+ * against it, so nothing is in flight when it gives up).  The wait expires
+ * and is reported like those of the compute kernels: the next compute call
+ * or gma_sync_status returns GMA_ERR_TIMEOUT.  limit_cycles in [1, 4e9]
+ * (GMA_ERR_INVALID_ARG otherwise); about 2e6 is one millisecond at 2 GHz.  */
+gma_status gma_test_wait_timeout(long long limit_cycles, gma_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *gma_status_string(gma_status status);

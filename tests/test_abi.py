@@ -37,8 +37,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
-        assert gma.gma_status_string(code)
+    for code in range(7):
+        assert gma.gma_status_string(code) and gma.gma_status_string(code) != "unknown status"
     assert gma.gma_status_string(99) == "unknown status"
 
 
@@ -208,3 +208,11 @@ def test_binding_refuses_host_tensors():
                  lambda: gma.gma_responsibilities(s, *p, x, torch.zeros(1, 1, 8, 128))):
         with pytest.raises(TypeError, match="CUDA tensor"):
             call()
+
+
+def test_timeout_hooks_validate_on_the_host(lib):
+    """The timeout test hook rejects limits outside [1, 4e9] before any launch."""
+    assert lib.gma_test_wait_timeout(0, None) == 1
+    assert lib.gma_test_wait_timeout(-5, None) == 1
+    assert lib.gma_test_wait_timeout(4000000001, None) == 1
+    assert gma.gma_status_string(gma.TIMEOUT) == "a bounded device wait expired"
