@@ -71,6 +71,8 @@ def _load():
             lib.gma_oracle_write.argtypes = [i, P, i, i, i, i, i, P, P, P, P, P, P]
             lib.gma_oracle_read.argtypes = [i, P, i, i, i, i, i, P, P, P, P, P, dbl, P]
             lib.gma_oracle_decode_step.argtypes = [i, P, i, i, i, i, P, P, P, P, P, P, dbl, P, P]
+            lib.gma_oracle_cross.argtypes = [i, P, i, i, i, i, i, i, P, P, P, P, P, P, dbl, P]
+            lib.gma_oracle_usage.argtypes = [i, P, i, i, i, i, P, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -189,3 +191,35 @@ def decode_step(mu, var_raw, logit_pi, qx, kx, v, eps, state, heads=None):
     _load().gma_oracle_decode_step(S, _p(hs), H, d, dv, K, _p(mu), _p(vr), _p(lp),
                                    _p(qx), _p(kx), _p(v), float(eps), _p(st), _p(out))
     return out, st
+
+
+def cross(mu, var_raw, logit_pi, qx, kx, v, eps, heads=None):
+    """Cross-attention: queries qx [S,nq,d] read the memory written by kx [S,nk,d], v [S,nk,dv]."""
+    mu, vr, lp = _f64(mu), _f64(var_raw), _f64(logit_pi)
+    qx, kx, v = _f64(qx), _f64(kx), _f64(v)
+    H, K, d = mu.shape
+    S, nq, _ = qx.shape
+    _, nk, dv = v.shape
+    if kx.shape[:2] != (S, nk):
+        raise ValueError("kx and v must hold the same key rows")
+    hs = _heads(S, H, heads)
+    out = np.empty((S, nq, dv))
+    _load().gma_oracle_cross(S, _p(hs), H, nq, nk, d, dv, K, _p(mu), _p(vr), _p(lp),
+                             _p(qx), _p(kx), _p(v), float(eps), _p(out))
+    return out
+
+
+def usage(mu, var_raw, logit_pi, x, heads=None):
+    """Responsibility diagnostics of routing rows x [S,n,d], per head:
+    (usage [H,K] soft sums, counts [H,K] hard-assignment counts (int64),
+     assign [S,n] argmax per row (int32), entropy [H,2]: soft, hard, divided by log K)."""
+    mu, vr, lp, x = _f64(mu), _f64(var_raw), _f64(logit_pi), _f64(x)
+    H, K, d = mu.shape
+    S, n, _ = x.shape
+    hs = _heads(S, H, heads)
+    u = np.empty((H, K))
+    c = np.empty((H, K), dtype=np.int64)
+    a = np.empty((S, n), dtype=np.int32)
+    e = np.empty((H, 2))
+    _load().gma_oracle_usage(S, _p(hs), H, n, d, K, _p(mu), _p(vr), _p(lp), _p(x), _p(u), _p(c), _p(a), _p(e))
+    return u, c, a, e

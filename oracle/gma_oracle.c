@@ -24,6 +24,14 @@
  *       ("변형 및 학습", bidirectional and causal variants)
  *   S5  decode: the causal recurrence advanced by one token (state updated
  *       with the token, then read).
+ *   X   cross-attention ("의의 및 주장": cross-attention as an extension): the
+ *       bidirectional write over N_k key/value rows, read by N_q query rows of
+ *       another sequence.
+ *   D   responsibility diagnostics ("결과 및 성능", interpretability: the
+ *       components used, usage entropy, hard assignments): per head, the soft
+ *       usage u_k = sum_i gamma_ik, the hard assignment argmax_k gamma_ik of
+ *       every row (lowest k on ties) and its counts, and the entropies of the
+ *       soft and hard usage distributions divided by log K.
  *
  * Readings where the page is silent (each is listed in the design notes):
  *   - one GMM per head, shared by Q_X and K_X and by every batch element;
@@ -295,4 +303,91 @@ void gma_oracle_decode_step(int S, const int *head, int H, int d, int dv, int K,
 {
     gma_oracle_causal(S, head, H, 1, d, dv, K, mu, var_raw, logit_pi, qx, kx, v, eps,
                       state, state, out);
+}
+
+/* X: cross-attention.  Every query row of slice s (Nq of them) reads the
+ * memory written by all Nk key/value rows of the same slice. */
+void gma_oracle_cross(int S, const int *head, int H, int Nq, int Nk, int d, int dv, int K,
+                      const double *mu, const double *var_raw, const double *logit_pi,
+                      const double *qx, const double *kx, const double *v, double eps, double *out)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        const double *mu_h = mu + (long)h * K * d, *var_h = p.var + (long)h * K * d;
+        const double *lp_h = p.log_pi + (long)h * K;
+        double *Vt = (double *)calloc((size_t)K * dv, sizeof(double));
+        double *Z = (double *)calloc((size_t)K, sizeof(double));
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int j = 0; j < Nk; ++j) {
+            posterior(d, K, mu_h, var_h, lp_h, kx + ((long)s * Nk + j) * d, g, ll);
+            write_row(K, dv, g, v + ((long)s * Nk + j) * dv, Vt, Z);
+        }
+        for (int i = 0; i < Nq; ++i) {
+            posterior(d, K, mu_h, var_h, lp_h, qx + ((long)s * Nq + i) * d, g, ll);
+            read_row(K, dv, g, Vt, Z, eps, out + ((long)s * Nq + i) * dv);
+        }
+        free(Vt); free(Z); free(g); free(ll);
+    }
+    release(p);
+}
+
+/* Entropy of the distribution proportional to w[0..K-1] (w >= 0), divided by
+ * log K (0 for K = 1 or an all-zero w); 0 log 0 = 0. */
+static double normalised_entropy(int K, const double *w)
+{
+    double tot = 0.0, h = 0.0;
+    for (int k = 0; k < K; ++k) tot += w[k];
+    if (K < 2 || tot <= 0.0) return 0.0;
+    for (int k = 0; k < K; ++k)
+        if (w[k] > 0.0) {
+            double q = w[k] / tot;
+            h -= q * log(q);
+        }
+    return h / log((double)K);
+}
+
+/* D: responsibility diagnostics over the N routing rows of every slice,
+ * accumulated per head (slices of the same head add up):
+ *   usage[h][k]   = sum over rows of gamma_ik          (soft usage)
+ *   counts[h][k]  = number of rows whose argmax is k    (hard assignments)
+ *   assign[s][i]  = argmax_k gamma_ik (lowest k on ties; nullable)
+ *   entropy[h][0] = normalised entropy of usage[h], entropy[h][1] of counts[h]
+ * Slices run one after another (no parallel sum), so the result is exact
+ * up to the order the rows are visited in. */
+void gma_oracle_usage(int S, const int *head, int H, int N, int d, int K,
+                      const double *mu, const double *var_raw, const double *logit_pi,
+                      const double *x, double *usage, long long *counts, int *assign, double *entropy)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+    double *g = (double *)malloc(sizeof(double) * (size_t)K);
+    double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+    double *w = (double *)malloc(sizeof(double) * (size_t)K);
+    for (long i = 0; i < (long)H * K; ++i) {
+        usage[i] = 0.0;
+        counts[i] = 0;
+    }
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        for (int i = 0; i < N; ++i) {
+            posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
+                      x + ((long)s * N + i) * d, g, ll);
+            int best = 0;
+            for (int k = 0; k < K; ++k) {
+                usage[(long)h * K + k] += g[k];
+                if (g[k] > g[best]) best = k;
+            }
+            counts[(long)h * K + best] += 1;
+            if (assign) assign[(long)s * N + i] = best;
+        }
+    }
+    for (int h = 0; h < H; ++h) {
+        entropy[2 * h] = normalised_entropy(K, usage + (long)h * K);
+        for (int k = 0; k < K; ++k) w[k] = (double)counts[(long)h * K + k];
+        entropy[2 * h + 1] = normalised_entropy(K, w);
+    }
+    free(g); free(ll); free(w);
+    release(p);
 }

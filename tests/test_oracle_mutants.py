@@ -72,6 +72,19 @@ MUTANTS = [
      CAUSAL_STEP, CAUSAL_STEP.replace("kx + ((long)s", "qx + ((long)s"), False),
     ("S4/S5 incoming state ignored",
      "        if (state_in) memcpy(st, state_in + s * sz, sizeof(double) * (size_t)sz);\n", "", False),
+    ("X cross-attention writes only the first key row",
+     "for (int j = 0; j < Nk; ++j) {", "for (int j = 0; j < (Nk > 0 ? 1 : 0); ++j) {", False),
+    ("D ties assigned to the highest component",
+     "if (g[k] > g[best]) best = k;", "if (g[k] >= g[best]) best = k;", False),
+    ("D soft usage sums the squared posterior",
+     "usage[(long)h * K + k] += g[k];", "usage[(long)h * K + k] += g[k] * g[k];", False),
+    ("D every head's usage accumulated on head 0",
+     "usage[(long)h * K + k] += g[k];", "usage[k] += g[k];", False),
+    ("D entropy not divided by log K",
+     "return h / log((double)K);", "return h;", False),
+    ("D hard-assignment entropy taken from the soft usage",
+     "entropy[2 * h + 1] = normalised_entropy(K, w);",
+     "entropy[2 * h + 1] = normalised_entropy(K, usage + (long)h * K);", False),
 ]
 
 

@@ -262,6 +262,101 @@ def test_bidir_is_write_then_read_and_splits(orc):
     np.testing.assert_allclose(orc.read(mu, vr, lp, qx, s1 + s2, 1e-6), b, rtol=1e-11, atol=1e-14)
 
 
+# ----------------------------------------------------- cross-attention -----
+
+@pytest.mark.parametrize("nq,nk", [(40, 256), (256, 40), (1, 7)])
+def test_cross_matches_rectangular_bruteforce(orc, nq, nk):
+    """Queries of one sequence read the memory written by the keys of another: the
+    latent-memory form equals the rectangular affinity Gamma_Q Gamma_K^T (nq x nk)
+    materialised from the library GMM posterior."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    q, k, vv = qx[:, :nq], kx[:, wl.N - nk:], v[:, wl.N - nk:]
+    gq = _sklearn_posterior(mu[0], vr[0], lp[0], q[0])
+    gk = _sklearn_posterior(mu[0], vr[0], lp[0], k[0])
+    for eps in (1e-6, 0.37):
+        ref = _bruteforce(gq, gk, vv[0].astype(np.float64), eps, False)
+        out = orc.cross(mu, vr, lp, q, k, vv, eps)[0]
+        assert out.shape == (nq, wl.dv)
+        np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12)
+
+
+def test_cross_special_cases(orc):
+    """Equal lengths and the same rows give the bidirectional form; K = 1 gives the
+    mean of the key sequence's values for every query; no keys give 0 / eps."""
+    wl, mu, vr, lp, qx, kx, v = _tiny()
+    np.testing.assert_array_equal(orc.cross(mu, vr, lp, qx, kx, v, 1e-6), orc.bidir(mu, vr, lp, qx, kx, v, 1e-6))
+    wl1, mu1, vr1, lp1, q1, k1, v1 = _tiny(K=1)
+    out = orc.cross(mu1, vr1, lp1, q1[:, :9], k1[:, 100:], v1[:, 100:], 0.25)[0]
+    expect = v1[0, 100:].astype(np.float64).sum(0) / (wl1.N - 100 + 0.25)
+    np.testing.assert_allclose(out, np.tile(expect, (9, 1)), rtol=1e-12, atol=1e-15)
+    empty = orc.cross(mu, vr, lp, qx[:, :5], kx[:, :0], v[:, :0], 0.5)
+    np.testing.assert_array_equal(empty, np.zeros((1, 5, wl.dv)))
+
+
+# ----------------------------------------------------------- diagnostics -----
+
+def test_usage_is_the_sum_and_argmax_of_the_posterior(orc):
+    """Soft usage = column sums of Gamma, hard assignments = row argmax, summed per head
+    over the slices of that head; checked against numpy on the library GMM posterior."""
+    wl = TINY.with_(B=2, H=2, N=300, K=12, d=8)
+    mu, vr, lp = wlmod.params(wl)
+    xs, heads = [], []
+    for b in range(wl.B):
+        for h in range(wl.H):
+            xs.append(wlmod.slice_inputs(wl, b, h, mu=mu)[0])
+            heads.append(h)
+    x = np.stack(xs)
+    u, c, a, e = orc.usage(mu, vr, lp, x, heads=heads)
+    for h in range(wl.H):
+        g = np.concatenate([_sklearn_posterior(mu[h], vr[h], lp[h], x[s]) for s in range(len(xs))
+                            if heads[s] == h])
+        np.testing.assert_allclose(u[h], g.sum(0), rtol=1e-10, atol=1e-10)
+        top2 = np.sort(g, 1)[:, -2:]
+        clear = top2[:, 1] - top2[:, 0] > 1e-9        # rows whose argmax is not a near-tie
+        assign = np.concatenate([a[s] for s in range(len(xs)) if heads[s] == h])
+        np.testing.assert_array_equal(assign[clear], g.argmax(1)[clear])
+        np.testing.assert_array_equal(c[h], np.bincount(assign, minlength=wl.K))
+        p = u[h] / u[h].sum()
+        np.testing.assert_allclose(e[h, 0], -(p * np.log(p)).sum() / np.log(wl.K), rtol=1e-12)
+        q = c[h][c[h] > 0] / c[h].sum()
+        np.testing.assert_allclose(e[h, 1], -(q * np.log(q)).sum() / np.log(wl.K), rtol=1e-12)
+    assert u.sum() == pytest.approx(wl.B * wl.H * wl.N, rel=1e-12)
+    assert c.sum() == wl.B * wl.H * wl.N
+
+
+def test_usage_closed_forms(orc):
+    """Equal components: every row's posterior is pi, so the soft usage is N pi, every row
+    is assigned to argmax pi and the hard entropy is 0; K = 1: all mass on one component."""
+    rng = np.random.default_rng(11)
+    K, d, N = 7, 5, 90
+    mu = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    vr = np.tile(rng.normal(size=(1, 1, d)), (1, K, 1))
+    l = rng.normal(size=(1, K))
+    u, c, a, e = orc.usage(mu, vr, l, rng.normal(size=(1, N, d)))
+    pi = softmax(l[0])
+    np.testing.assert_allclose(u[0], N * pi, rtol=1e-12)
+    assert (a == pi.argmax()).all() and c[0, pi.argmax()] == N
+    np.testing.assert_allclose(e[0, 0], -(pi * np.log(pi)).sum() / np.log(K), rtol=1e-12)
+    assert e[0, 1] == 0.0
+    # uniform priors and equal components: the soft usage has the largest entropy, 1
+    u, c, a, e = orc.usage(mu, vr, np.zeros((1, K)), rng.normal(size=(1, N, d)))
+    assert e[0, 0] == pytest.approx(1.0, rel=1e-12)
+    assert (a == 0).all()                              # ties go to the lowest component
+    wl1, mu1, vr1, lp1, q1, _, _ = _tiny(K=1)
+    u, c, a, e = orc.usage(mu1, vr1, lp1, q1)
+    assert u[0, 0] == pytest.approx(wl1.N, rel=1e-14) and c[0, 0] == wl1.N and (e == 0).all()
+
+
+def test_usage_follows_component_permutation(orc):
+    wl, mu, vr, lp, qx, _, _ = _tiny()
+    perm = np.random.default_rng(12).permutation(wl.K)
+    u, c, a, e = orc.usage(mu, vr, lp, qx)
+    up, cp, ap, ep = orc.usage(mu[:, perm], vr[:, perm], lp[:, perm], qx)
+    np.testing.assert_allclose(up[0], u[0, perm], rtol=1e-12)
+    np.testing.assert_array_equal(cp[0], c[0, perm])
+    np.testing.assert_allclose(ep, e, rtol=1e-12)
+
+
 # ---------------------------------------------------------------- S5 -------
 
 def test_s5_decode_continues_prefill(orc):
