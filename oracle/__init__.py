@@ -73,6 +73,8 @@ def _load():
             lib.gma_oracle_decode_step.argtypes = [i, P, i, i, i, i, P, P, P, P, P, P, dbl, P, P]
             lib.gma_oracle_cross.argtypes = [i, P, i, i, i, i, i, i, P, P, P, P, P, P, dbl, P]
             lib.gma_oracle_usage.argtypes = [i, P, i, i, i, i, P, P, P, P, P, P, P, P]
+            lib.gma_oracle_backward.argtypes = [i, P, i, i, i, i, i, i, P, P, P, P, P, P, dbl, P, P, P, P, P, P,
+                                                P]
             _lib = lib
     return _lib
 
@@ -223,3 +225,20 @@ def usage(mu, var_raw, logit_pi, x, heads=None):
     e = np.empty((H, 2))
     _load().gma_oracle_usage(S, _p(hs), H, n, d, K, _p(mu), _p(vr), _p(lp), _p(x), _p(u), _p(c), _p(a), _p(e))
     return u, c, a, e
+
+
+def backward(mu, var_raw, logit_pi, qx, kx, v, eps, dout, causal=True, heads=None):
+    """Gradients of the causal (or bidirectional) forward given dL/dO = dout [S,n,dv]:
+    (dqx [S,n,d], dkx [S,n,d], dv [S,n,dv], dmu [H,K,d], dvar_raw [H,K,d], dlogit_pi [H,K]);
+    the parameter gradients sum over the slices of each head and both routings."""
+    mu, vr, lp = _f64(mu), _f64(var_raw), _f64(logit_pi)
+    qx, kx, v, g = _f64(qx), _f64(kx), _f64(v), _f64(dout)
+    H, K, d = mu.shape
+    S, n, dv = v.shape
+    hs = _heads(S, H, heads)
+    dq, dk, dvv = np.empty((S, n, d)), np.empty((S, n, d)), np.empty((S, n, dv))
+    dmu, dvr, dlp = np.empty((H, K, d)), np.empty((H, K, d)), np.empty((H, K))
+    _load().gma_oracle_backward(S, _p(hs), H, n, d, dv, K, int(bool(causal)), _p(mu), _p(vr), _p(lp),
+                                _p(qx), _p(kx), _p(v), float(eps), _p(g), _p(dq), _p(dk), _p(dvv),
+                                _p(dmu), _p(dvr), _p(dlp))
+    return dq, dk, dvv, dmu, dvr, dlp

@@ -27,6 +27,12 @@
  *   X   cross-attention ("의의 및 주장": cross-attention as an extension): the
  *       bidirectional write over N_k key/value rows, read by N_q query rows of
  *       another sequence.
+ *   G   gradients ("변형 및 학습": the parameters are trained end to end by
+ *       backpropagation, with softplus and softmax reparameterisations; "주요
+ *       기여", gradient structure: the gradients pass through the
+ *       responsibilities): dL/dO given, the gradients of Q_X, K_X, V, mu,
+ *       the raw variances and the mixture logits, by the chain rule through
+ *       the read, the write, the posterior and the reparameterisation.
  *   D   responsibility diagnostics ("결과 및 성능", interpretability: the
  *       components used, usage entropy, hard assignments): per head, the soft
  *       usage u_k = sum_i gamma_ik, the hard assignment argmax_k gamma_ik of
@@ -355,39 +361,193 @@ static double normalised_entropy(int K, const double *w)
  *   counts[h][k]  = number of rows whose argmax is k    (hard assignments)
  *   assign[s][i]  = argmax_k gamma_ik (lowest k on ties; nullable)
  *   entropy[h][0] = normalised entropy of usage[h], entropy[h][1] of counts[h]
- * Slices run one after another (no parallel sum), so the result is exact
- * up to the order the rows are visited in. */
+ * The slices of a head run one after another (no parallel sum), so the
+ * result does not depend on the thread count. */
 void gma_oracle_usage(int S, const int *head, int H, int N, int d, int K,
                       const double *mu, const double *var_raw, const double *logit_pi,
                       const double *x, double *usage, long long *counts, int *assign, double *entropy)
 {
     prepared p = prepare(H, K, d, var_raw, logit_pi);
-    double *g = (double *)malloc(sizeof(double) * (size_t)K);
-    double *ll = (double *)malloc(sizeof(double) * (size_t)K);
-    double *w = (double *)malloc(sizeof(double) * (size_t)K);
     for (long i = 0; i < (long)H * K; ++i) {
         usage[i] = 0.0;
         counts[i] = 0;
     }
-    for (int s = 0; s < S; ++s) {
-        int h = head[s];
-        for (int i = 0; i < N; ++i) {
-            posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
-                      x + ((long)s * N + i) * d, g, ll);
-            int best = 0;
-            for (int k = 0; k < K; ++k) {
-                usage[(long)h * K + k] += g[k];
-                if (g[k] > g[best]) best = k;
-            }
-            counts[(long)h * K + best] += 1;
-            if (assign) assign[(long)s * N + i] = best;
-        }
-    }
+    /* heads are independent: one thread per head, its slices in order */
+#pragma omp parallel for schedule(dynamic)
     for (int h = 0; h < H; ++h) {
+        double *g = (double *)malloc(sizeof(double) * (size_t)K);
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        double *w = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int s = 0; s < S; ++s) {
+            if (head[s] != h) continue;
+            for (int i = 0; i < N; ++i) {
+                posterior(d, K, mu + (long)h * K * d, p.var + (long)h * K * d, p.log_pi + (long)h * K,
+                          x + ((long)s * N + i) * d, g, ll);
+                int best = 0;
+                for (int k = 0; k < K; ++k) {
+                    usage[(long)h * K + k] += g[k];
+                    if (g[k] > g[best]) best = k;
+                }
+                counts[(long)h * K + best] += 1;
+                if (assign) assign[(long)s * N + i] = best;
+            }
+        }
         entropy[2 * h] = normalised_entropy(K, usage + (long)h * K);
         for (int k = 0; k < K; ++k) w[k] = (double)counts[(long)h * K + k];
         entropy[2 * h + 1] = normalised_entropy(K, w);
+        free(g); free(ll); free(w);
     }
-    free(g); free(ll); free(w);
+    release(p);
+}
+
+/* G: gradients of the causal (causal = 1) or bidirectional (causal = 0) form.
+ *
+ * With U_i = gq_i S_i ([numerator | denominator - eps]), o_i = U_i[:dv] / den_i
+ * and g_i = dL/do_i:
+ *   u_i          = dL/dU_i = [g_i / den_i | -(g_i . o_i) / den_i]
+ *   dL/dgq_i     = S_i u_i                     (S_i: the memory row i reads)
+ *   R_j          = sum over the rows i that read key j of gq_i (x) u_i
+ *   dL/dgk_j     = R_j [v_j | 1],   dL/dv_j = (gk_j R_j)[:dv]
+ * (causal: S_i = sum_{j <= i}, R_j = sum_{i >= j}; bidirectional: all rows).
+ * Through the softmax over components, delta_ik = gamma_ik (dL/dgamma_ik -
+ * sum_k' gamma_ik' dL/dgamma_ik'), and through the log-joint
+ *   l_ik = log pi_k - 1/2 sum_d [(x_id - mu_kd)^2 / s_kd + log s_kd + log 2 pi],
+ * s = sigma^2:
+ *   dL/dx_id   = -sum_k delta_ik (x_id - mu_kd) / s_kd
+ *   dL/dmu_kd += delta_ik (x_id - mu_kd) / s_kd
+ *   dL/ds_kd  += delta_ik (1/2 (x_id - mu_kd)^2 / s_kd^2 - 1/2 / s_kd)
+ *   dL/dlogpi_k += delta_ik
+ * over the query and key rows of every slice of the head; finally
+ *   dL/dvar_raw = dL/ds * sigmoid(var_raw)      (softplus' = sigmoid)
+ *   dL/dlogit_k = G_k - pi_k sum_k' G_k'        (log-softmax), G = dL/dlogpi.
+ * Outputs dqx, dkx [S][N][d], dv [S][N][dv]; dmu, dvar_raw [H][K][d] and
+ * dlogit [H][K] are overwritten (the sum over the slices of each head, taken
+ * in slice order). */
+void gma_oracle_backward(int S, const int *head, int H, int N, int d, int dv, int K, int causal,
+                         const double *mu, const double *var_raw, const double *logit_pi,
+                         const double *qx, const double *kx, const double *v, double eps,
+                         const double *dout, double *dqx, double *dkx, double *dv_out,
+                         double *dmu, double *dvar_raw, double *dlogit)
+{
+    prepared p = prepare(H, K, d, var_raw, logit_pi);
+    const long w = (long)dv + 1, kd = (long)K * d;
+    /* per-slice parameter gradients, summed in slice order after the parallel loop */
+    double *pmu = (double *)calloc((size_t)S * kd, sizeof(double));
+    double *pvar = (double *)calloc((size_t)S * kd, sizeof(double));
+    double *plp = (double *)calloc((size_t)S * K, sizeof(double));
+#pragma omp parallel for schedule(dynamic)
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        const double *mu_h = mu + (long)h * kd, *var_h = p.var + (long)h * kd;
+        const double *lp_h = p.log_pi + (long)h * K;
+        const double *xq = qx + (long)s * N * d, *xk = kx + (long)s * N * d;
+        const double *vs = v + (long)s * N * dv, *gs = dout + (long)s * N * dv;
+        double *gq = (double *)malloc(sizeof(double) * (size_t)N * K);
+        double *gk = (double *)malloc(sizeof(double) * (size_t)N * K);
+        double *dgq = (double *)malloc(sizeof(double) * (size_t)N * K);
+        double *dgk = (double *)malloc(sizeof(double) * (size_t)N * K);
+        double *u = (double *)malloc(sizeof(double) * (size_t)N * w);
+        double *M = (double *)calloc((size_t)K * w, sizeof(double));   /* S_i, then R_j */
+        double *ll = (double *)malloc(sizeof(double) * (size_t)K);
+        double *vrow = (double *)malloc(sizeof(double) * (size_t)w);
+        for (int i = 0; i < N; ++i) {
+            posterior(d, K, mu_h, var_h, lp_h, xq + (long)i * d, gq + (long)i * K, ll);
+            posterior(d, K, mu_h, var_h, lp_h, xk + (long)i * d, gk + (long)i * K, ll);
+        }
+        /* the write: S accumulates gk_j (x) [v_j | 1]; bidirectional: all of it first */
+        if (!causal)
+            for (int j = 0; j < N; ++j)
+                for (int k = 0; k < K; ++k) {
+                    for (int c = 0; c < dv; ++c) M[k * w + c] += gk[(long)j * K + k] * vs[(long)j * dv + c];
+                    M[k * w + dv] += gk[(long)j * K + k];
+                }
+        for (int i = 0; i < N; ++i) {
+            if (causal)
+                for (int k = 0; k < K; ++k) {
+                    for (int c = 0; c < dv; ++c) M[k * w + c] += gk[(long)i * K + k] * vs[(long)i * dv + c];
+                    M[k * w + dv] += gk[(long)i * K + k];
+                }
+            /* the read of row i, then u_i and dL/dgq_i */
+            double den = eps, go = 0.0;
+            for (int k = 0; k < K; ++k) den += gq[(long)i * K + k] * M[k * w + dv];
+            for (int c = 0; c < dv; ++c) {
+                double num = 0.0;
+                for (int k = 0; k < K; ++k) num += gq[(long)i * K + k] * M[k * w + c];
+                go += gs[(long)i * dv + c] * (num / den);
+            }
+            double *ui = u + (long)i * w;
+            for (int c = 0; c < dv; ++c) ui[c] = gs[(long)i * dv + c] / den;
+            ui[dv] = -go / den;
+            for (int k = 0; k < K; ++k) {
+                double t = 0.0;
+                for (int c = 0; c < w; ++c) t += M[k * w + c] * ui[c];
+                dgq[(long)i * K + k] = t;
+            }
+        }
+        /* R: the rows that read key j; causal: i >= j (a suffix, inclusive) */
+        for (long e = 0; e < (long)K * w; ++e) M[e] = 0.0;
+        if (!causal)
+            for (int i = 0; i < N; ++i)
+                for (int k = 0; k < K; ++k)
+                    for (int c = 0; c < w; ++c) M[k * w + c] += gq[(long)i * K + k] * u[(long)i * w + c];
+        for (int j = N - 1; j >= 0; --j) {
+            if (causal)
+                for (int k = 0; k < K; ++k)
+                    for (int c = 0; c < w; ++c) M[k * w + c] += gq[(long)j * K + k] * u[(long)j * w + c];
+            for (int c = 0; c < dv; ++c) vrow[c] = vs[(long)j * dv + c];
+            vrow[dv] = 1.0;
+            for (int k = 0; k < K; ++k) {
+                double t = 0.0;
+                for (int c = 0; c < w; ++c) t += M[k * w + c] * vrow[c];
+                dgk[(long)j * K + k] = t;
+            }
+            for (int c = 0; c < dv; ++c) {
+                double t = 0.0;
+                for (int k = 0; k < K; ++k) t += gk[(long)j * K + k] * M[k * w + c];
+                dv_out[((long)s * N + j) * dv + c] = t;
+            }
+        }
+        /* through the softmax and the log-joint, for the query rows then the key rows */
+        for (int pass = 0; pass < 2; ++pass) {
+            const double *x = pass ? xk : xq, *g = pass ? gk : gq, *dg = pass ? dgk : dgq;
+            double *dx = (pass ? dkx : dqx) + (long)s * N * d;
+            for (int i = 0; i < N; ++i) {
+                double dot = 0.0;
+                for (int k = 0; k < K; ++k) dot += g[(long)i * K + k] * dg[(long)i * K + k];
+                for (int j2 = 0; j2 < d; ++j2) dx[(long)i * d + j2] = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    const double delta = g[(long)i * K + k] * (dg[(long)i * K + k] - dot);
+                    plp[(long)s * K + k] += delta;
+                    for (int j2 = 0; j2 < d; ++j2) {
+                        const double t = x[(long)i * d + j2] - mu_h[(long)k * d + j2], sk = var_h[(long)k * d + j2];
+                        dx[(long)i * d + j2] -= delta * t / sk;
+                        pmu[(long)s * kd + (long)k * d + j2] += delta * t / sk;
+                        pvar[(long)s * kd + (long)k * d + j2] += delta * (0.5 * t * t / (sk * sk) - 0.5 / sk);
+                    }
+                }
+            }
+        }
+        free(gq); free(gk); free(dgq); free(dgk); free(u); free(M); free(ll); free(vrow);
+    }
+    for (long e = 0; e < (long)H * kd; ++e) {
+        dmu[e] = 0.0;
+        dvar_raw[e] = 0.0;
+    }
+    for (long e = 0; e < (long)H * K; ++e) dlogit[e] = 0.0;
+    for (int s = 0; s < S; ++s) {
+        int h = head[s];
+        for (long e = 0; e < kd; ++e) {
+            dmu[(long)h * kd + e] += pmu[(long)s * kd + e];
+            dvar_raw[(long)h * kd + e] += pvar[(long)s * kd + e];
+        }
+        for (int k = 0; k < K; ++k) dlogit[(long)h * K + k] += plp[(long)s * K + k];
+    }
+    for (long e = 0; e < (long)H * kd; ++e) dvar_raw[e] *= 1.0 / (1.0 + exp(-var_raw[e]));
+    for (int h = 0; h < H; ++h) {
+        double tot = 0.0;
+        for (int k = 0; k < K; ++k) tot += dlogit[(long)h * K + k];
+        for (int k = 0; k < K; ++k) dlogit[(long)h * K + k] -= exp(p.log_pi[(long)h * K + k]) * tot;
+    }
+    free(pmu); free(pvar); free(plp);
     release(p);
 }

@@ -74,6 +74,23 @@ MUTANTS = [
      "        if (state_in) memcpy(st, state_in + s * sz, sizeof(double) * (size_t)sz);\n", "", False),
     ("X cross-attention writes only the first key row",
      "for (int j = 0; j < Nk; ++j) {", "for (int j = 0; j < (Nk > 0 ? 1 : 0); ++j) {", False),
+    ("G denominator gradient with the wrong sign",
+     "    ui[dv] = -go / den;", "    ui[dv] = go / den;", False),
+    ("G softmax backward without the row term",
+     "const double delta = g[(long)i * K + k] * (dg[(long)i * K + k] - dot);",
+     "const double delta = g[(long)i * K + k] * dg[(long)i * K + k];", False),
+    ("G causal key side summed over the prefix instead of the suffix",
+     "        for (int j = N - 1; j >= 0; --j) {", "        for (int j = 0; j < N; ++j) {", False),
+    ("G softplus derivative dropped",
+     "dvar_raw[e] *= 1.0 / (1.0 + exp(-var_raw[e]));", "dvar_raw[e] *= 1.0;", False),
+    ("G logit gradient from the query rows only",
+     "                    plp[(long)s * K + k] += delta;", "                    if (!pass) plp[(long)s * K + k] += delta;",
+     False),
+    ("G variance gradient without the log-determinant term",
+     "delta * (0.5 * t * t / (sk * sk) - 0.5 / sk);", "delta * (0.5 * t * t / (sk * sk));", False),
+    ("G value gradient from the query responsibilities",
+     "for (int k = 0; k < K; ++k) t += gk[(long)j * K + k] * M[k * w + c];",
+     "for (int k = 0; k < K; ++k) t += gq[(long)j * K + k] * M[k * w + c];", False),
     ("D ties assigned to the highest component",
      "if (g[k] > g[best]) best = k;", "if (g[k] >= g[best]) best = k;", False),
     ("D soft usage sums the squared posterior",

@@ -357,6 +357,99 @@ def test_usage_follows_component_permutation(orc):
     np.testing.assert_allclose(ep, e, rtol=1e-12)
 
 
+# ------------------------------------------------------------- gradients -----
+
+def _torch_bruteforce_grads(mu, vr, lp, qx, kx, v, eps, W, causal):
+    """Gradients of L = sum(W * O) by torch autograd through a brute-force fp64 forward
+    (library softplus / log-softmax / softmax, the N x N affinity materialised): an
+    implementation that shares nothing with the oracle."""
+    torch = pytest.importorskip("torch")
+    t = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    mu_t, vr_t, lp_t, q_t, k_t, v_t = (t(a) for a in (mu[0], vr[0], lp[0], qx[0], kx[0], v[0]))
+    var = torch.nn.functional.softplus(vr_t)
+    logpi = torch.log_softmax(lp_t, 0)
+
+    def post(x):
+        ll = logpi[None] - 0.5 * (((x[:, None, :] - mu_t[None]) ** 2) / var[None] + torch.log(var)[None]
+                                  + math.log(2 * math.pi)).sum(-1)
+        return torch.softmax(ll, 1)
+
+    A = post(q_t) @ post(k_t).T
+    if causal:
+        A = torch.tril(A)
+    O = (A @ v_t) / (A.sum(1, keepdim=True) + eps)
+    (O * torch.tensor(W[0])).sum().backward()
+    return [a.grad.numpy() for a in (q_t, k_t, v_t, mu_t, vr_t, lp_t)]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("eps", [1e-6, 0.3])
+def test_backward_matches_autograd_of_bruteforce(orc, causal, eps):
+    wl, mu, vr, lp, qx, kx, v = _tiny(N=96, K=6, d=5, dv=7)
+    W = np.random.default_rng(21).normal(size=(1, wl.N, wl.dv))
+    got = orc.backward(mu, vr, lp, qx, kx, v, eps, W, causal=causal)
+    ref = _torch_bruteforce_grads(mu, vr, lp, qx, kx, v, eps, W, causal)
+    names = ("dqx", "dkx", "dv", "dmu", "dvar_raw", "dlogit_pi")
+    for name, a, b in zip(names, got, ref):
+        a = a.reshape(b.shape)
+        assert np.abs(a - b).max() <= 1e-9 * max(np.abs(b).max(), 1e-300), name
+
+
+def test_backward_matches_central_differences(orc):
+    """Every gradient against central differences of the oracle's own (pinned) forward."""
+    wl, mu, vr, lp, qx, kx, v = _tiny(N=40, K=5, d=4, dv=3)
+    rng = np.random.default_rng(22)
+    W = rng.normal(size=(1, wl.N, wl.dv))
+    eps = 1e-3
+    for causal in (True, False):
+        fwd = orc.causal if causal else orc.bidir
+        args = [np.asarray(a, np.float64).copy() for a in (qx, kx, v, mu, vr, lp)]
+
+        def loss(a):
+            q, k, vv, m, r, l = a
+            return float((fwd(m, r, l, q, k, vv, eps) * W).sum())
+
+        grads = orc.backward(args[3], args[4], args[5], args[0], args[1], args[2], eps, W, causal=causal)
+        for which in range(6):
+            flat = args[which].reshape(-1)
+            for idx in rng.choice(flat.size, size=min(6, flat.size), replace=False):
+                h = 1e-5 * max(1.0, abs(flat[idx]))
+                old = flat[idx]
+                flat[idx] = old + h
+                lp_ = loss(args)
+                flat[idx] = old - h
+                lm_ = loss(args)
+                flat[idx] = old
+                fd = (lp_ - lm_) / (2 * h)
+                g = grads[which].reshape(-1)[idx]
+                assert abs(g - fd) <= 1e-6 * max(1.0, abs(fd)), (causal, which, idx, g, fd)
+
+
+def test_backward_structure(orc):
+    """Causal: dL/dO_i touches only rows <= i through the queries' side, so the query-row
+    gradient of row i does not depend on dL/dO of other rows; the value gradient of the
+    last row comes from the last output alone; the logit gradient of a head sums to zero
+    (softmax); K = 1: routing gradients vanish."""
+    wl, mu, vr, lp, qx, kx, v = _tiny(N=50)
+    rng = np.random.default_rng(23)
+    W = rng.normal(size=(1, wl.N, wl.dv))
+    dq, dk, dv, dmu, dvr, dlp = orc.backward(mu, vr, lp, qx, kx, v, 1e-6, W)
+    W2 = W.copy()
+    W2[0, :10] = rng.normal(size=(10, wl.dv))
+    dq2, dk2, dv2, *_ = orc.backward(mu, vr, lp, qx, kx, v, 1e-6, W2)
+    np.testing.assert_array_equal(dq2[0, 10:], dq[0, 10:])
+    W3 = np.zeros_like(W)
+    W3[0, -1] = W[0, -1]
+    _, _, dv3, *_ = orc.backward(mu, vr, lp, qx, kx, v, 1e-6, W3)
+    np.testing.assert_allclose(dv3[0, -1], dv[0, -1] - orc.backward(mu, vr, lp, qx, kx, v, 1e-6, W - W3)[2][0, -1],
+                               rtol=1e-10, atol=1e-14)
+    assert abs(dlp.sum()) < 1e-10 * np.abs(dlp).max()
+    wl1, mu1, vr1, lp1, q1, k1, v1 = _tiny(K=1, N=30)
+    g1 = orc.backward(mu1, vr1, lp1, q1, k1, v1, 1e-6, rng.normal(size=(1, 30, wl1.dv)))
+    for a in (g1[0], g1[1], g1[3], g1[4], g1[5]):
+        assert np.abs(a).max() == 0.0
+
+
 # ---------------------------------------------------------------- S5 -------
 
 def test_s5_decode_continues_prefill(orc):
