@@ -81,6 +81,8 @@ def stage_work(stage, wl):
       resp_q / resp_k     4*K*d on the FP32 pipe (one fp32x2 FMA for (x-mu)/sigma
                           and one for the square-accumulate, per component and
                           feature pair)
+      resp_dense          4*K*d per row of the tiles the bounded routings leave to
+                          the dense pass (K = 128, d = 64), both routings
       block_state /
       chunk_state_tc      2*K*(d_v+1)           (Gamma_K^T [V | 1])
       chunk_out(_tc)      2*C*K + C*(d_v+1) + 2*K*(d_v+1)   (P = Gq Gk^T, lower half
@@ -104,6 +106,8 @@ def stage_work(stage, wl):
             return (8.0 * K * d + 4.0 * K * (dv + 1)) * bh, "alu", (2 * st + 2 * d * xb + dv * vb + 4 * dv) * bh
         return 0.0, "alu", 0.0
     ht = wl.B * wl.H * wl.N
+    if wl.mode == "backward":
+        return backward_work(wl)
     C = eff_chunk(wl)
     tc = stage.endswith("_tc")
     # blocks of the carried memory: chunks of C rows on the tensor-core path (its scan too),
@@ -115,6 +119,10 @@ def stage_work(stage, wl):
         # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work
         pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
         return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
+    if stage == "resp_dense":
+        # the dense exact pass over the tiles the bounded routings left to it, charged as if every
+        # tile of both routings were dense (on the inputs where this stage dominates, all are)
+        return 2 * 4.0 * K * d * ht, "alu", 2 * (d * xb + K * gb) * ht
     if stage in ("block_state", "chunk_state_tc"):
         return 2.0 * K * (dv + 1) * ht, ("tensor_bf16" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
     if stage in ("chunk_out", "chunk_out_tc"):
@@ -127,6 +135,22 @@ def stage_work(stage, wl):
     if stage == "state_reduce":   # every block's partial in, one total per (b, h) out
         return 0.0, "alu", st * (nblk + wl.B * wl.H)
     return 0.0, "alu", 0.0
+
+
+def backward_work(wl):
+    """Work of one gradient pass (causal form, chunks of C = 64 on CUDA cores), per head-token:
+    FP32 flop: routing recomputed for Q_X and K_X (8 K d), dx (8 K d: y and the
+    delta-weighted sum), the parameter partial sums (12 K d), and the chunk products of
+    the forward recompute, the query side and the key/value side (three times those of
+    the forward, 3 (4 K (d_v + 1) + 2 C K + C (d_v + 1)));
+    bytes: Q_X, K_X, V and dL/dO in, dQ_X, dK_X and dV out (fp32)."""
+    K, d, dv, C = wl.K, wl.d, wl.dv, 64
+    xb = 2 if wl.x_dtype == "bf16" else 4
+    vb = 2 if wl.v_dtype == "bf16" else 4
+    ht = wl.B * wl.H * wl.N
+    flop = (28.0 * K * d + 3.0 * (4.0 * K * (dv + 1) + 2.0 * C * K + C * (dv + 1))) * ht
+    nbytes = (2 * d * xb + dv * vb + 4 * dv + 8 * d + 4 * dv) * ht
+    return flop, "alu", nbytes
 
 
 def algorithmic_work(stage, wl, kept=None):
@@ -153,6 +177,8 @@ def algorithmic_work(stage, wl, kept=None):
     tensor pipe plus the exact evaluation of the kept components on the FP32
     pipe (`kept` = mean kept components per row, measured), whichever takes
     longer at its peak; elsewhere the dense FP32 routing."""
+    if wl.mode == "backward":
+        return backward_work(wl)
     flop, pipe, _ = stage_work(stage, wl)
     if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k"):
         pipe = "tensor"   # the chunk products at the rate of their operand type (tf32 for fp32)
@@ -167,6 +193,8 @@ def algorithmic_work(stage, wl, kept=None):
         if bounded_routing(wl) and kept is not None:
             return 4.0 * d * kept * ht, "alu_kept", nbytes
         return flop, pipe, nbytes
+    if stage == "resp_dense":   # its routing rows were charged to resp_q / resp_k
+        return flop, pipe, 0.0
     if stage in ("block_state", "chunk_state_tc"):
         return flop, pipe, dv * vb * ht
     if stage in ("chunk_out", "chunk_out_tc"):
@@ -232,6 +260,10 @@ def path_roofline_s(wl, pk, kept=None):
         t_hbm = (8.0 * wl.K * (wl.dv + 1) + 2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * bh / (pk["hbm_gbs"] * 1e9)
         return max(t_alu, t_hbm), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=0.0)
     ht = wl.B * wl.H * wl.N
+    if wl.mode == "backward":
+        flop, _, nbytes = backward_work(wl)
+        t_alu, t_hbm = flop / fp32_peak, nbytes / (pk["hbm_gbs"] * 1e9)
+        return max(t_alu, t_hbm), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=0.0)
     t_hbm = ((2 * wl.d * xb + wl.dv * vb + 4 * wl.dv) * ht) / (pk["hbm_gbs"] * 1e9)
     C = eff_chunk(wl)
     if wl.mode == "bidir":
@@ -351,7 +383,7 @@ def whole_job_rate(world, tokens_per_rank, ms):
 # The source file holding each stage's kernel; its hash (with the shared headers)
 # keys the committed DRAM counters, so a changed kernel reports no traffic.
 KERNEL_SOURCE = {
-    "prep_params": "gma_resp.cu", "prep": "gma_resp_tc.cu",
+    "prep_params": "gma_resp.cu", "prep": "gma_resp_tc.cu", "resp_dense": "gma_resp_tc.cu",
     "chunk_state_tc": "gma_causal_tc.cu", "chunk_out_tc": "gma_causal_tc.cu", "bidir_read_tc": "gma_causal_tc.cu",
     "block_state": "gma_mix.cu", "state_scan": "gma_mix.cu", "state_reduce": "gma_mix.cu",
     "chunk_out": "gma_mix.cu", "bidir_read": "gma_mix.cu", "decode": "gma_decode.cu",
@@ -395,6 +427,9 @@ def _oracle_call(wl, mu, vr, lp, q, k, v, heads):
         S = q.shape[0]
         state = np.ones((S, wl.K * wl.dv + wl.K))
         return oracle.decode_step(mu, vr, lp, q[:, 0], k[:, 0], v[:, 0], wl.eps, state, heads=heads)
+    if wl.mode == "backward":
+        g = np.ones_like(v)   # dL/dO: any values cost the same
+        return oracle.backward(mu, vr, lp, q, k, v, wl.eps, g, causal=True, heads=heads)
     return oracle.causal(mu, vr, lp, q, k, v, wl.eps, heads=heads)
 
 
@@ -522,6 +557,15 @@ class Runner:
             self.d_in = [t.to(dev) for t in self.h_in]
             self.out = torch.empty(wl.B, wl.H, wl.N, wl.dv, device=dev)
             op = gma.OP_BIDIR if wl.mode == "bidir" else gma.OP_CAUSAL
+            if wl.mode == "backward":
+                op = gma.OP_BACKWARD
+                self.h_in.append(torch.from_numpy(workloads.full_dout(wl, seed)).pin_memory())
+                self.d_in.append(self.h_in[-1].to(dev))
+                f32 = dict(device=dev, dtype=torch.float32)
+                self.grads = (torch.empty(wl.B, wl.H, wl.N, wl.d, **f32), torch.empty(wl.B, wl.H, wl.N, wl.d, **f32),
+                              torch.empty(wl.B, wl.H, wl.N, wl.dv, **f32), torch.empty(wl.H, wl.K, wl.d, **f32),
+                              torch.empty(wl.H, wl.K, wl.d, **f32), torch.empty(wl.H, wl.K, **f32))
+                self.h_grads = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.grads]
         self.ws = torch.empty(gma.gma_workspace_size(self.shape, op), dtype=torch.uint8, device=dev)
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.host_ws = (torch.empty(gma.gma_workspace_size(self.shape, gma.OP_CAUSAL_HOST), dtype=torch.uint8,
@@ -530,6 +574,13 @@ class Runner:
 
     def profiled(self, evs):
         g, wl = self.gma, self.wl
+        if wl.mode == "backward":   # one launch sequence, timed as one stage
+            import torch
+            st = torch.cuda.current_stream(self.dev)
+            evs[0].record(st)
+            g.gma_backward(self.shape, *self.prm, *self.d_in, *self.grads, causal=True, ws=self.ws)
+            evs[1].record(st)
+            return ["backward"]
         if wl.mode == "decode":
             t = self.i % self.tq.shape[0]
             self.i += 1
@@ -550,6 +601,11 @@ class Runner:
             return
         for d, h in zip(self.d_in, self.h_in):
             d.copy_(h, non_blocking=True)
+        if wl.mode == "backward":
+            g.gma_backward(self.shape, *self.prm, *self.d_in, *self.grads, causal=True, ws=self.ws)
+            for h, d in zip(self.h_grads, self.grads):
+                h.copy_(d, non_blocking=True)
+            return
         q, k, v = self.d_in
         if wl.mode == "decode":
             g.gma_decode_step(self.shape, *self.prm, q, k, v, self.state, self.out, ws=self.ws)
@@ -574,8 +630,9 @@ class Runner:
         return n / 2
 
     def io_bytes(self):
-        return (sum(t.numel() * t.element_size() for t in self.h_in),
-                self.h_out.numel() * self.h_out.element_size())
+        out = (sum(t.numel() * t.element_size() for t in self.h_grads) if self.wl.mode == "backward"
+               else self.h_out.numel() * self.h_out.element_size())
+        return sum(t.numel() * t.element_size() for t in self.h_in), out
 
 
 # ----------------------------------------------------------------- main -------
@@ -664,7 +721,7 @@ def main():
                                        for s_ in range(args.steps))
     dom = max(stage_ms, key=stage_ms.get)
     pk, pk_kind = peaks()
-    kept = run.kept_per_row() if (bounded_routing(wl) and wl.mode != "decode") else None
+    kept = run.kept_per_row() if (bounded_routing(wl) and wl.mode in ("causal", "bidir")) else None
     roof = roofline_of(dom, wl, stage_ms[dom] * 1e-3, pk, kept)
     roof_s, roof_parts = path_roofline_s(wl, pk, kept)
 

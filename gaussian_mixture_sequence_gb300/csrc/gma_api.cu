@@ -15,13 +15,19 @@ namespace {
 
 struct WsPlan {
     size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, pimg = 0, cimg = 0,
-           bytes = 0;
+           pimg2 = 0, dctl = 0, dlist = 0, bytes = 0;
+    long long dcap = 0;   // dense-list entries per head
     bool pruned = false;
 };
 
 bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }
 
 gma_status make_dims_raw(const gma_shape *s, Dims *dm);
+#define GMA_TRY_DIMS(expr)                                                                                 \
+    do {                                                                                                   \
+        const gma_status _d = (expr);                                                                      \
+        if (_d != GMA_OK) return _d;                                                                       \
+    } while (0)
 
 // Dims of one operation: only the causal form uses the tensor-core chunking.
 gma_status make_dims(const gma_shape *s, Dims *dm, gma_op op = GMA_OP_CAUSAL)
@@ -32,6 +38,18 @@ gma_status make_dims(const gma_shape *s, Dims *dm, gma_op op = GMA_OP_CAUSAL)
         dm->blk = kBlockRows;
     }
     return st;
+}
+
+// Dims of the gradient pass: the CUDA-core chunking (C = 64, blocks of kBlockRows rows) and
+// fp32 responsibilities whatever the shape's chunk and product type.
+gma_status make_dims_bwd(const gma_shape *s, Dims *dm)
+{
+    if (!s) return GMA_ERR_INVALID_ARG;
+    gma_shape t = *s;
+    t.chunk = 64;
+    t.gemm_dtype = GMA_F32;
+    GMA_TRY_DIMS(make_dims_raw(&t, dm));
+    return GMA_OK;
 }
 
 gma_status make_dims_raw(const gma_shape *s, Dims *dm)
@@ -78,6 +96,15 @@ WsPlan plan(const Dims &dm, gma_op op)
         p.wimg = take((size_t)dm.H * kPrunedWBytes);
         p.pimg = take((size_t)dm.H * kPrunedPBytes);
         p.cimg = take((size_t)dm.H * kPrunedCBytes);
+        p.pimg2 = take((size_t)dm.H * kPrunedP2Bytes);
+        p.dcap = 2 * routing_tiles(dm.B, dm.N);   // both routings of a head
+        p.dctl = take((size_t)dm.H * 4);
+        p.dlist = take((size_t)dm.H * p.dcap * 8);
+    }
+    if (op == GMA_OP_USAGE) {   // Gamma in fp32, then the per-block partial sums and counts
+        p.gq = take((size_t)dm.BH() * dm.N * dm.K * 4);
+        p.partial = take((size_t)dm.BH() * usage_blocks(dm) * dm.K * 4);
+        p.total = take((size_t)dm.BH() * usage_blocks(dm) * dm.K * 4);
     }
     if (op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL) {
         const size_t gb = dm.g_bf16 ? 2 : 4;
@@ -170,9 +197,55 @@ HostStaging host_staging(const Dims &dm)
     return h;
 }
 
+// Workspace of the gradient pass.
+struct BwdPlan {
+    WsPlan w;   // parameters, routing images, gq / gk (fp32), forward memory (partial, total)
+    size_t dgq = 0, dgk = 0, u = 0, mem = 0, rtot = 0, pmu = 0, pvar = 0, plp = 0, bytes = 0;
+};
+BwdPlan plan_bwd_full(const Dims &dm)
+{
+    BwdPlan b;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off = (size_t)round_up((long long)(off + n), 256);
+        return o;
+    };
+    WsPlan &p = b.w;
+    p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
+    p.cst = take((size_t)dm.H * dm.K * 4);
+    if (resp_pruned_applies(dm)) {
+        p.pruned = true;
+        p.wimg = take((size_t)dm.H * kPrunedWBytes);
+        p.pimg = take((size_t)dm.H * kPrunedPBytes);
+        p.cimg = take((size_t)dm.H * kPrunedCBytes);
+        p.pimg2 = take((size_t)dm.H * kPrunedP2Bytes);
+        p.dcap = 2 * routing_tiles(dm.B, dm.N);   // both routings of a head
+        p.dctl = take((size_t)dm.H * 4);
+        p.dlist = take((size_t)dm.H * p.dcap * 8);
+    }
+    const size_t rows = (size_t)dm.BH() * dm.N, nb = (size_t)dm.BH() * dm.nblk();
+    p.gq = take(rows * dm.KP * 4);
+    p.gk = take(rows * dm.KP * 4);
+    p.partial = take(nb * dm.state_size() * 4);
+    p.total = take((size_t)dm.BH() * dm.state_size() * 4);
+    b.dgq = take(rows * dm.KP * 4);
+    b.dgk = take(rows * dm.KP * 4);
+    b.u = take(rows * bwd_u_pitch(dm) * 4);
+    b.mem = take(nb * dm.K * bwd_u_pitch(dm) * 4);
+    b.rtot = take((size_t)dm.BH() * dm.K * bwd_u_pitch(dm) * 4);
+    b.pmu = take(2 * nb * dm.K * dm.D * 4);
+    b.pvar = take(2 * nb * dm.K * dm.D * 4);
+    b.plp = take(2 * nb * dm.K * 4);
+    b.bytes = p.bytes = off;
+    return b;
+}
+WsPlan plan_bwd(const Dims &dm) { return plan_bwd_full(dm).w; }
+
 PrunedImages images(void *ws, const WsPlan &wp)
 {
-    return PrunedImages{at<unsigned char>(ws, wp.wimg), at<float4>(ws, wp.pimg), at<float>(ws, wp.cimg)};
+    return PrunedImages{at<unsigned char>(ws, wp.wimg), at<float4>(ws, wp.pimg), at<float>(ws, wp.cimg),
+                        at<float4>(ws, wp.pimg2), at<unsigned int>(ws, wp.dctl), at<int2>(ws, wp.dlist), wp.dcap};
 }
 
 } // namespace
@@ -186,7 +259,8 @@ size_t gma_workspace_size(const gma_shape *shape, gma_op op)
         if (make_dims(shape, &dm, GMA_OP_CAUSAL) != GMA_OK) return 0;
         return host_staging(dm).bytes + plan(dm, GMA_OP_CAUSAL).bytes;
     }
-    if ((unsigned)op > 3u || make_dims(shape, &dm, op) != GMA_OK) return 0;
+    if (op == GMA_OP_BACKWARD) return make_dims_bwd(shape, &dm) == GMA_OK ? plan_bwd(dm).bytes : 0;
+    if (((unsigned)op > 3u && op != GMA_OP_USAGE) || make_dims(shape, &dm, op) != GMA_OK) return 0;
     return plan(dm, op).bytes;
 }
 
@@ -224,7 +298,39 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     const PrunedImages img = images(ws, wp);
     if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
     else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st, 0));
+    if (wp.pruned) GMA_CUDA(launch_resp_dense(dm, x, gamma, dm, nullptr, nullptr, img, GL_F32, st));
+    return GMA_OK;
+}
+
+gma_status gma_responsibility_stats(const gma_shape *shape, gma_params params, const void *x, float *usage,
+                                    long long *counts, float *entropy, int *assign, void *ws, size_t ws_bytes,
+                                    gma_stream_t stream)
+{
+    GMA_TRY(take_timeout());
+    Dims dm;
+    GMA_TRY(make_dims(shape, &dm, GMA_OP_USAGE));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(x, dm.N > 0));
+    GMA_TRY(check_ptr(usage));
+    GMA_TRY(check_ptr(counts));
+    GMA_TRY(check_ptr(entropy));
+    GMA_TRY(check_ptr(assign, false));
+    const WsPlan wp = plan(dm, GMA_OP_USAGE);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *gamma = at<float>(ws, wp.gq);
+    if (dm.N > 0) {
+        float4 *prm = at<float4>(ws, wp.prm);
+        float *cst = at<float>(ws, wp.cst);
+        const PrunedImages img = images(ws, wp);
+        if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
+        else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+        GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st, 0));
+        if (wp.pruned) GMA_CUDA(launch_resp_dense(dm, x, gamma, dm, nullptr, nullptr, img, GL_F32, st));
+    }
+    GMA_CUDA(launch_usage(dm, gamma, dm.K, at<float>(ws, wp.partial), at<int>(ws, wp.total), assign, usage, counts,
+                          entropy, st));
     return GMA_OK;
 }
 
@@ -295,9 +401,13 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
         GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st, 1));
+    if (imgp) {
+        GMA_CUDA(mk.mark("resp_dense"));
+        GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));
+    }
     if (tc_path_applies(dm)) {
         GMA_CUDA(mk.mark("chunk_state_tc"));
         GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
@@ -315,6 +425,94 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
         GMA_CUDA(launch_chunk_out(dm, false, gq, gk, v, total, out, st));
     }
     GMA_CUDA(mk.finish());
+    return GMA_OK;
+}
+
+// Workspace of the cross form: queries of dm_q, keys and values of dm_kv (same B, H, d, K).
+WsPlan plan_cross(const Dims &dq, const Dims &dk)
+{
+    WsPlan p;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off = (size_t)round_up((long long)(off + n), 256);
+        return o;
+    };
+    p.prm = take((size_t)dq.H * dq.K * (dq.D / 2) * 16);
+    p.cst = take((size_t)dq.H * dq.K * 4);
+    if (resp_pruned_applies(dq)) {
+        p.pruned = true;
+        p.wimg = take((size_t)dq.H * kPrunedWBytes);
+        p.pimg = take((size_t)dq.H * kPrunedPBytes);
+        p.cimg = take((size_t)dq.H * kPrunedCBytes);
+        p.pimg2 = take((size_t)dq.H * kPrunedP2Bytes);
+        p.dcap = routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N);
+        p.dctl = take((size_t)dq.H * 4);
+        p.dlist = take((size_t)dq.H * p.dcap * 8);
+    }
+    const size_t gb = dq.g_bf16 ? 2 : 4;
+    p.gq = take((size_t)dq.BH() * dq.N * dq.KP * gb);
+    p.gk = take((size_t)dk.BH() * dk.N * dk.KP * gb);
+    p.partial = take((size_t)dk.BH() * dk.nblk() * dk.state_size() * 4);
+    p.total = take((size_t)dk.BH() * dk.state_size() * 4);
+    p.bytes = off;
+    return p;
+}
+
+gma_status cross_dims(const gma_shape *shape, int n_kv, Dims *dq, Dims *dk)
+{
+    GMA_TRY(make_dims(shape, dq, GMA_OP_BIDIR));
+    if (n_kv < 0) return GMA_ERR_INVALID_ARG;
+    gma_shape sk = *shape;
+    sk.N = n_kv;
+    return make_dims(&sk, dk, GMA_OP_BIDIR);
+}
+
+// Queries of dq read the memory written by all keys of dk: the bidirectional write over
+// dk's rows, then the bidirectional read over dq's rows.
+gma_status run_cross(const gma_shape *shape, int n_kv, gma_params params, const void *qx, const void *kx,
+                     const void *v, float *out, void *ws, size_t ws_bytes, gma_stream_t stream)
+{
+    Dims dq, dk;
+    GMA_TRY(cross_dims(shape, n_kv, &dq, &dk));
+    GMA_TRY(check_params(params));
+    GMA_TRY(check_ptr(qx, dq.N > 0));
+    GMA_TRY(check_ptr(out, dq.N > 0));
+    GMA_TRY(check_ptr(kx, dk.N > 0 && dq.N > 0));
+    GMA_TRY(check_ptr(v, dk.N > 0 && dq.N > 0));
+    const WsPlan wp = plan_cross(dq, dk);
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    if (dq.N == 0) return GMA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
+    float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
+    const PrunedImages img = images(ws, wp);
+    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
+    if (wp.pruned) GMA_CUDA(launch_prep_all(dq, params, prm, cst, img, st));
+    else GMA_CUDA(launch_prep(dq, params, prm, cst, st));
+    GMA_CUDA(launch_resp(dq, prm, cst, imgp, qx, gq, dq.KP, gamma_layout(dq), st, 0));
+    if (dk.N > 0) GMA_CUDA(launch_resp(dk, prm, cst, imgp, kx, gk, dk.KP, gamma_layout(dk), st, 1));
+    if (imgp)
+        GMA_CUDA(launch_resp_dense(dq, qx, gq, dk, dk.N > 0 ? kx : nullptr, gk, img, gamma_layout(dq), st));
+    const bool tc = tc_path_applies(dq);
+    if (dk.N == 0) {   // no keys: an empty memory (zeros in either layout)
+        GMA_CUDA(cudaMemsetAsync(total, 0, (size_t)dk.BH() * dk.state_size() * 4, st));
+    } else {
+        if (tc) {
+            GMA_CUDA(launch_chunk_state_tc(dk, gk, v, partial, st));
+            GMA_CUDA(launch_scan_split(dk, partial, nullptr, nullptr, reinterpret_cast<unsigned char *>(total),
+                                       nullptr, st));
+        } else {
+            GMA_CUDA(launch_block_state(dk, gk, v, partial, st));
+            GMA_CUDA(launch_scan(dk, partial, nullptr, total, false, st));
+        }
+    }
+    if (tc)
+        GMA_CUDA(launch_chunk_out_tc(dq, false, gq, gq, nullptr, reinterpret_cast<unsigned char *>(total), out, st));
+    else
+        GMA_CUDA(launch_chunk_out(dq, false, gq, gq, nullptr, total, out, st));
     return GMA_OK;
 }
 
@@ -336,9 +534,10 @@ gma_status run_decode(const gma_shape *shape, gma_params params, const void *qx,
     Marks mk{prof, 0, st};
     float4 *prm = at<float4>(ws, wp.prm);
     float *cst = at<float>(ws, wp.cst);
-    GMA_CUDA(mk.mark("prep_params"));
-    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    // one stage: the decode kernel is a programmatic dependent of the parameter preparation and
+    // overlaps it (an event recorded between the two would serialise them)
     GMA_CUDA(mk.mark("decode"));
+    GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     GMA_CUDA(launch_decode(dm, prm, cst, qx, kx, v, state, out, st));
     GMA_CUDA(mk.finish());
     return GMA_OK;
@@ -387,9 +586,13 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
         GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st, 1));
+    if (imgp) {
+        GMA_CUDA(mk.mark("resp_dense"));
+        GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));
+    }
     if (tc_path_applies(dm)) {
         GMA_CUDA(mk.mark("chunk_state_tc"));
         GMA_CUDA(launch_chunk_state_tc(dm, gk, v, partial, st));
@@ -638,5 +841,77 @@ extern "C" gma_status gma_test_wait_timeout(long long limit_cycles, gma_stream_t
 {
     if (limit_cycles < 1 || limit_cycles > 4000000000LL) return GMA_ERR_INVALID_ARG;
     GMA_CUDA(launch_expire_wait(limit_cycles, reinterpret_cast<cudaStream_t>(stream)));
+    return GMA_OK;
+}
+
+extern "C" size_t gma_cross_workspace_size(const gma_shape *shape, int n_kv)
+{
+    Dims dq, dk;
+    if (cross_dims(shape, n_kv, &dq, &dk) != GMA_OK) return 0;
+    return plan_cross(dq, dk).bytes;
+}
+
+extern "C" gma_status gma_forward_cross(const gma_shape *shape, int n_kv, gma_params params, const void *qx,
+                                        const void *kx, const void *v, float *out, void *ws, size_t ws_bytes,
+                                        gma_stream_t stream)
+{
+    GMA_TRY(take_timeout());
+    return run_cross(shape, n_kv, params, qx, kx, v, out, ws, ws_bytes, stream);
+}
+
+extern "C" gma_status gma_backward(const gma_shape *shape, int causal, gma_params params, const void *qx,
+                                   const void *kx, const void *v, const float *dout, float *dqx, float *dkx,
+                                   float *dv, float *dmu, float *dvar_raw, float *dlogit_pi, void *ws,
+                                   size_t ws_bytes, gma_stream_t stream)
+{
+    GMA_TRY(take_timeout());
+    Dims dm;
+    GMA_TRY(make_dims_bwd(shape, &dm));
+    if (causal != 0 && causal != 1) return GMA_ERR_INVALID_ARG;
+    GMA_TRY(check_params(params));
+    const bool any = dm.N > 0;
+    GMA_TRY(check_ptr(qx, any));
+    GMA_TRY(check_ptr(kx, any));
+    GMA_TRY(check_ptr(v, any));
+    GMA_TRY(check_ptr(dout, any));
+    GMA_TRY(check_ptr(dqx, any));
+    GMA_TRY(check_ptr(dkx, any));
+    GMA_TRY(check_ptr(dv, any));
+    GMA_TRY(check_ptr(dmu));
+    GMA_TRY(check_ptr(dvar_raw));
+    GMA_TRY(check_ptr(dlogit_pi));
+    const BwdPlan bp = plan_bwd_full(dm);
+    const WsPlan &wp = bp.w;
+    GMA_TRY(check_ws(ws, ws_bytes, wp));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!any) {
+        GMA_CUDA(cudaMemsetAsync(dmu, 0, (size_t)dm.H * dm.K * dm.D * 4, st));
+        GMA_CUDA(cudaMemsetAsync(dvar_raw, 0, (size_t)dm.H * dm.K * dm.D * 4, st));
+        GMA_CUDA(cudaMemsetAsync(dlogit_pi, 0, (size_t)dm.H * dm.K * 4, st));
+        return GMA_OK;
+    }
+    float4 *prm = at<float4>(ws, wp.prm);
+    float *cst = at<float>(ws, wp.cst);
+    float *gq = at<float>(ws, wp.gq), *gk = at<float>(ws, wp.gk);
+    float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
+    const PrunedImages img = images(ws, wp);
+    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
+    // the forward's responsibilities (fp32) and memory
+    if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
+    else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, GL_F32, st, 0));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, GL_F32, st, 1));
+    if (imgp) GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, GL_F32, st));
+    GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
+    GMA_CUDA(launch_scan(dm, partial, nullptr, causal ? nullptr : total, causal != 0, st));
+    // query side, key / value side, then the routings and the parameters
+    float *dgq = at<float>(ws, bp.dgq), *dgk = at<float>(ws, bp.dgk), *u = at<float>(ws, bp.u);
+    GMA_CUDA(launch_bwd_q(dm, causal != 0, gq, gk, v, dout, causal ? partial : total, u, dgq, st));
+    GMA_CUDA(launch_bwd_kv(dm, causal != 0, gq, gk, v, u, at<float>(ws, bp.mem), at<float>(ws, bp.rtot), dgk, dv, st));
+    const size_t pass = (size_t)dm.BH() * dm.nblk() * dm.K;
+    float *pmu = at<float>(ws, bp.pmu), *pvar = at<float>(ws, bp.pvar), *plp = at<float>(ws, bp.plp);
+    GMA_CUDA(launch_bwd_route(dm, qx, prm, gq, dgq, dqx, pmu, pvar, plp, st));
+    GMA_CUDA(launch_bwd_route(dm, kx, prm, gk, dgk, dkx, pmu + pass * dm.D, pvar + pass * dm.D, plp + pass, st));
+    GMA_CUDA(launch_bwd_final(dm, params, pmu, pvar, plp, dmu, dvar_raw, dlogit_pi, st));
     return GMA_OK;
 }

@@ -13,12 +13,15 @@
 namespace gma {
 namespace {
 
-// One CTA per (b, h).  The log-joints of the new token's q and k rows: a warp
-// per component row of parameters at a time (coalesced, shared by both rows,
-// sums over the warp by shuffles); then the two softmaxes, a warp each; then
-// one pass over the state that updates and reads it, four columns per thread
-// with 16-byte loads and stores (a scalar pass when K is not a multiple of 4,
-// where the slices of the state are not 16-byte aligned).
+// One CTA per (b, h).  The kernel is launched as a programmatic dependent of the
+// parameter preparation, whose results it reads only after griddepcontrol.wait
+// (the token rows it reads first were written before the preparation kernel
+// started), so that the preparation overlaps its start.  The log-joints of the new
+// token's q and k rows: a warp per component row of parameters at a time
+// (coalesced, shared by both rows, sums over the warp by shuffles); then the two
+// softmaxes, a warp each; then one pass over the state that updates and reads
+// it, four columns per thread with 16-byte accesses (a scalar pass when K is not
+// a multiple of 4, where the slices of the state are not 16-byte aligned).
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 6)
     k_decode(int H, int K, float eps, const void *__restrict__ qx, const void *__restrict__ kx, bool x_bf16,
@@ -31,9 +34,10 @@ __global__ void __launch_bounds__(kThreads, 6)
     float *vv = xk + D;        // [DV]
     float *gq = vv + DV;       // [K]
     float *gk = gq + K;        // [K]
-    float *red = gk + K;       // [kThreads]
-    float4 *red4 = reinterpret_cast<float4 *>((reinterpret_cast<uintptr_t>(red + kThreads) + 15) & ~uintptr_t(15));   // [kThreads]
-    float *dz = reinterpret_cast<float *>(red4 + kThreads);   // [kThreads / 32] den partials
+    float *dz = gk + K;        // [kThreads / 32] den partials
+    // then, 16-byte aligned: red4 [kThreads] followed by red [kThreads]
+    float4 *red4 = reinterpret_cast<float4 *>((reinterpret_cast<uintptr_t>(dz + kThreads / 32) + 15) & ~uintptr_t(15));
+    float *red = reinterpret_cast<float *>(red4 + kThreads);
 
     const long long bh = blockIdx.x;
     const int h = (int)(bh % H), tid = threadIdx.x;
@@ -49,6 +53,8 @@ __global__ void __launch_bounds__(kThreads, 6)
         xk[i] = load_elem(kx, bh * D + i, x_bf16);
     }
     for (int i = tid; i < DV; i += kThreads) vv[i] = load_elem(v, bh * DV + i, v_bf16);
+    // the prepared parameters are written by the preceding kernel (programmatic launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
 
     // log-joints -1/2 sum_d ((x_d - mu_d) / sigma_d)^2 + c_k of both rows.  A warp takes a
@@ -253,12 +259,22 @@ template <int D, int DV>
 cudaError_t launch_decode_dv(const Dims &dm, const float4 *prm, const float *cst, const void *qx, const void *kx,
                              const void *v, float *state, float *out, cudaStream_t st)
 {
-    // xq, xk, v, gq, gk, red, then red4 at a 16-byte aligned offset
-    const size_t head = ((size_t)(2 * dm.D + DV + 2 * dm.K + kThreads) * 4 + 15) / 16 * 16;
-    const size_t smem = head + (size_t)kThreads * 16 + (kThreads / 32) * 4;
-    k_decode<D, DV><<<(unsigned)dm.BH(), kThreads, smem, st>>>(dm.H, dm.K, dm.eps, qx, kx, dm.x_bf16, v,
-                                                               dm.v_bf16, prm, cst, state, out);
-    return cudaGetLastError();
+    // xq, xk, v, gq, gk, dz, then at a 16-byte aligned offset red4 and red
+    const size_t head = ((size_t)(2 * dm.D + DV + 2 * dm.K + kThreads / 32) * 4 + 15) / 16 * 16;
+    const size_t smem = head + (size_t)kThreads * 20;
+    // a programmatic dependent of the preceding launch (the parameter preparation)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)dm.BH());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_decode<D, DV>, dm.H, dm.K, dm.eps, qx, kx, dm.x_bf16, v, dm.v_bf16, prm, cst,
+                              state, out);
 }
 
 template <int D>
@@ -275,6 +291,8 @@ cudaError_t launch_decode_d(const Dims &dm, const float4 *prm, const float *cst,
 }
 
 } // namespace
+
+
 
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx, const void *kx,
                           const void *v, float *state, float *out, cudaStream_t st)

@@ -94,9 +94,11 @@ __device__ __forceinline__ void store_g(void *base, long long i, long long plane
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float *cst, cudaStream_t st);
-// gamma: responsibilities in `layout` (GLayout), ldg columns per row
+// gamma: responsibilities in `layout` (GLayout), ldg columns per row.  With the bounded
+// routing (img non-null and resp_pruned_applies), tiles whose rows keep many components are
+// listed for launch_resp_dense under source tag `src` (0 or 1) instead of being finished here.
 cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const struct PrunedImages *img,
-                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st);
+                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st, int src = 0);
 cudaError_t launch_block_state(const Dims &dm, const void *gk, const void *v, float *partial,
                                cudaStream_t st);
 cudaError_t launch_scan(const Dims &dm, float *partial, const float *state_in, float *total,
@@ -105,6 +107,7 @@ cudaError_t launch_chunk_out(const Dims &dm, bool causal, const void *gq, const 
                              float *states, float *out, cudaStream_t st);
 cudaError_t launch_decode(const Dims &dm, const float4 *prm, const float *cst, const void *qx,
                           const void *kx, const void *v, float *state, float *out, cudaStream_t st);
+
 
 // Row-major [rows][cols] tensor map with boxes of 128 bytes x box_rows and the
 // 128-byte swizzle (gma_tma.cu).  Returns false if it cannot be encoded.
@@ -132,8 +135,16 @@ struct PrunedImages {
     unsigned char *w;   // [H][32768 B]: bf16 bound matrix, 128-byte-swizzled K-major
     float4 *p;          // [H][128][33]: packed exact parameters, rows padded by one word
     float *c;           // [H][4][128]: c_k, c'_k, A_k, M_k
+    float4 *p2;         // [H][128][32]: the packed exact parameters for the dense kernel, feature
+                        // pair 4 e + j of a component at position 8 j + e (e = feature eighth)
+    unsigned int *ctl;  // [H]: tiles of each head listed for the dense kernel (zeroed by k_prep_all)
+    int2 *list;         // [H][cap]: (slice | source tag << 30, tile) of the tiles left to the dense kernel
+    long long cap;      // list entries per head (the tiles of both routings of a head)
 };
-constexpr size_t kPrunedWBytes = 32768, kPrunedPBytes = 128 * 33 * 16, kPrunedCBytes = 4 * 128 * 4;
+constexpr size_t kPrunedWBytes = 32768, kPrunedPBytes = 128 * 33 * 16, kPrunedCBytes = 4 * 128 * 4,
+                 kPrunedP2Bytes = 128 * 32 * 16;
+// Routing tiles of 128 rows of a call with BH slices of N rows.
+inline long long routing_tiles(long long BH, int N) { return BH * ((N + 127) / 128); }
 
 // Responsibilities for K = 128, d_route = 64 with a tensor-core bound (gma_resp_tc.cu).
 bool resp_pruned_applies(const Dims &dm);
@@ -142,7 +153,13 @@ bool resp_pruned_applies(const Dims &dm);
 cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, float *cst, const PrunedImages &img,
                             cudaStream_t st);
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
-                               int layout, cudaStream_t st);
+                               int layout, cudaStream_t st, int src = 0);
+// The dense exact pass over the tiles the bounded routings listed: source 0 is (d0, x0,
+// g0), source 1 (d1, x1, g1) (x1 may be null when only one routing ran).  Launched as a
+// programmatic dependent of the preceding launch; k_prep_all empties the list at the start
+// of every call that routes with the bound.
+cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
+                              const PrunedImages &img, int layout, cudaStream_t st);
 
 // Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
 bool tc_path_eligible(int K, int DV, bool g_bf16);
@@ -155,6 +172,24 @@ cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float 
                               unsigned char *total, float *state_out, cudaStream_t st);
 cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
                                 const unsigned char *mem, float *out, cudaStream_t st);
+// Responsibility diagnostics (gma_stats.cu): blocks of rows per slice of the partial
+// pass, and the two launches (partial sums per block, then per head in fixed order).
+int usage_blocks(const Dims &dm);
+cudaError_t launch_usage(const Dims &dm, const float *gamma, int ldg, float *pu, int *pc, int *assign, float *usage,
+                         long long *counts, float *entropy, cudaStream_t st);
+
+// Gradients, CUDA-core path (gma_bwd.cu): Dims with C = 64 and blocks of kBlockRows rows,
+// responsibilities fp32 [BH][N][KP].
+size_t bwd_u_pitch(const Dims &dm);   // row pitch (floats) of u = dL/d[numerator | denominator]
+cudaError_t launch_bwd_q(const Dims &dm, bool causal, const float *gq, const float *gk, const void *v,
+                         const float *dout, float *states, float *u, float *dgq, cudaStream_t st);
+cudaError_t launch_bwd_kv(const Dims &dm, bool causal, const float *gq, const float *gk, const void *v,
+                          const float *u, float *mem, float *rtot, float *dgk, float *dv, cudaStream_t st);
+cudaError_t launch_bwd_route(const Dims &dm, const void *x, const float4 *prm, const float *gamma, float *dgamma,
+                             float *dx, float *pmu, float *pvar, float *plp, cudaStream_t st);
+cudaError_t launch_bwd_final(const Dims &dm, const gma_params &p, const float *pmu, const float *pvar,
+                             const float *plp, float *dmu, float *dvar, float *dlogit, cudaStream_t st);
+
 // One kernel whose single bounded wait (limit_cycles SM cycles) expires and is reported
 // through the timeout flag like the waits of the kernels above.
 cudaError_t launch_expire_wait(long long limit_cycles, cudaStream_t st);

@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(int K, int D, const float
     constexpr int NW = kPrepThreads / 32;
     __shared__ float red[NW];
     __shared__ float bcast[2];
+    // a kernel launched as a programmatic dependent of this one (the decode step) may start
+    // now; it waits for this grid's results before it reads them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = blockIdx.y * kPrepComps + (tid >> 4), part = tid & 15;
     const float *l = logit_pi + (long long)h * K;
@@ -270,9 +273,9 @@ cudaError_t launch_prep(const Dims &dm, const gma_params &p, float4 *prm, float 
 }
 
 cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, const PrunedImages *img,
-                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st)
+                        const void *x, void *gamma, int ldg, int layout, cudaStream_t st, int src)
 {
-    if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, layout, st);
+    if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, layout, st, src);
     switch (dm.D) {
     case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, layout, st);
     case 32: return launch_resp_d<32>(dm, prm, cst, x, gamma, ldg, layout, st);

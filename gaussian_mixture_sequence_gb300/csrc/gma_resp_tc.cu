@@ -49,6 +49,9 @@ constexpr int kPRun = 16;                      // tiles of a slice taken in a ro
 constexpr int kPStride = kPDP + 1;            // padded float4 row of exact parameters
 constexpr float kPT = 30.f;                   // log-joint window kept exactly
 constexpr float kPU = 4.0e-3f;                // bf16 product + fp32 accumulation bound
+// A tile is left to the dense kernel when at least kDenseRows of its (row, component half)
+// pairs keep kDenseKept or more of the half's 64 components.
+constexpr int kDenseKept = 8, kDenseRows = 64;
 
 // Shared memory: the bound matrix, the routing tile, each group's output tile,
 // the constants c, c', A, M, each group's exchange slots between the two
@@ -83,6 +86,18 @@ __device__ __forceinline__ bool group_or(int g, bool pred)
     return r != 0;
 }
 
+// Named barrier of one group that also returns how many of its threads have `pred` set.
+__device__ __forceinline__ uint32_t group_popc(int g, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(1 + g), "r"(kPGThreads)
+                 : "memory");
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b)
 {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
@@ -104,7 +119,8 @@ __device__ __forceinline__ float softplus_f(float r) { return fmaxf(r, 0.f) + lo
 __global__ void __launch_bounds__(kPrepAllThreads)
     k_prep_all(const float *__restrict__ mu, const float *__restrict__ var_raw, const float *__restrict__ logit_pi,
                float4 *__restrict__ prm, float *__restrict__ cst, unsigned char *__restrict__ wimg,
-               float4 *__restrict__ pimg, float *__restrict__ cimg)
+               float4 *__restrict__ pimg, float *__restrict__ cimg, float4 *__restrict__ pimg2,
+               unsigned int *__restrict__ dctl)
 {
     constexpr int NW = kPrepAllThreads / 32;
     __shared__ float red[2][NW];
@@ -112,6 +128,7 @@ __global__ void __launch_bounds__(kPrepAllThreads)
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = blockIdx.y * kPrepAllComps + (tid >> 4), part = tid & 15;   // component, features 4 part ..
     const float *l = logit_pi + (long long)h * kPK;
+    if (blockIdx.y == 0 && tid == 0) dctl[h] = 0u;   // no tile of this head listed for the dense kernel yet
 
     // log-sum-exp of the head's logits (thread k < K holds logit k)
     const float lv = tid < kPK ? l[tid] : -FLT_MAX;
@@ -150,6 +167,7 @@ __global__ void __launch_bounds__(kPrepAllThreads)
         const float4 p = make_float4(s0, s1, -uv[2 * q] * s0, -uv[2 * q + 1] * s1);
         prm[row * kPDP + dp] = p;
         pimg[row * kPStride + dp] = p;
+        pimg2[row * kPDP + 8 * (dp % 4) + dp / 4] = p;   // pair 4 e + j at 8 j + e
         lsum += logf(v0) + logf(v1);
         amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
         amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
@@ -185,10 +203,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
     k_resp_pruned(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
                   const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int BH, bool x_bf16,
                   const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
-                  const float *__restrict__ cimg, int layout, int pstride, unsigned int *timeout)
+                  const float *__restrict__ cimg, int layout, int pstride, unsigned int *timeout,
+                  int2 *__restrict__ dlist, unsigned int *__restrict__ dctl, long long dcap, int src)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    // a dense pass launched as a programmatic dependent of this kernel may be scheduled as soon as
+    // SMs free up; it waits for this grid's completion before it reads the tiles listed here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp >> 3;                    // group
     const int gt = tid - grp * kPGThreads;        // thread in the group
@@ -449,6 +471,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
                 }
             }
+            // a tile where many rows keep many components goes to the dense exact kernel
+            // (k_resp_dense), which evaluates every component with register blocking; walking
+            // the kept sets here one component at a time would be bound by shared-memory reads
+            if (group_popc(grp, __popc(xm0) + __popc(xm1) >= kDenseKept) >= kDenseRows) {
+                if (gt == 0) dlist[(long long)head * dcap + atomicAdd(dctl + head, 1u)] = make_int2(bh | (src << 30), t);
+                continue;   // no exact pass and no output tile here
+            }
             if (group_or(grp, (xm0 | xm1) != 0u)) {
                 // exact log-joint of a component for this lane's row (parameters from global
                 // memory, L2-resident)
@@ -590,6 +619,214 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) tmem_dealloc(*tslot, 512);
 }
 
+// ------------------------------------------------------------------------
+// Dense exact responsibilities of the tiles k_resp_pruned listed (rows that keep
+// many components): every one of the 128 log-joints of every row, the same
+// packed-FMA quadratic form ((x - mu) / sigma)^2, then the softmax.
+//
+// Two persistent CTAs of 8 warps per SM (one CTA's loads, softmax and stores
+// overlap the other's FMAs), each taking a contiguous range of the listed tiles
+// in head order, so that it works on one or two heads whose parameters stay in
+// L1; every tile's result depends on that tile alone.  Warp w
+// covers rows 32 (w % 4) .. + 31 and components 64 (w / 4) .. + 63; lane (g, e)
+// holds rows 8 g .. 8 g + 7 of those and feature eighth e (features 8 e .. + 7)
+// in registers and takes two components at a time: the parameter words of
+// feature pair 4 e + j of both components are read through L1 with the
+// evict-last hint (the eighths of one feature-pair slot are 128 contiguous bytes
+// in the interleaved image; the routing rows are read L2-only so that they do
+// not evict them), so every 16-byte read feeds 16 packed FMAs (8 rows, square
+// and accumulate).  The 16 partial sums (2 components x 8 rows) meet over the
+// eighth lanes by recursive halving (14 shuffles), each lane keeping one
+// component for two rows.  Log-joints go to a shared [128][132] tile; 2 threads per row take the
+// softmax (components strided by 2); rows then leave in the requested layout
+// with coalesced stores.  The kernel
+// is a programmatic dependent of the last routing launch: it reads the list
+// only after griddepcontrol.wait.
+constexpr int kDThreads = 256, kDPitch = 132;
+
+// A read-only 16-byte load that L1 keeps in preference to other lines (the
+// parameters of the head, reused by every tile of that head).
+__device__ __forceinline__ float4 ld_keep(const float4 *p)
+{
+    float4 r;
+    asm("ld.global.nc.L1::evict_last.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p));
+    return r;
+}
+
+struct DenseSrc {
+    const void *x;
+    void *gamma;
+    int N;
+    long long plane;   // elements of one plane of the split layout
+};
+
+__global__ void __launch_bounds__(kDThreads, 2)
+    k_resp_dense(DenseSrc s0, DenseSrc s1, bool x_bf16, int H, const float4 *__restrict__ pimg2,
+                 const float *__restrict__ cimg, int layout, const int2 *__restrict__ dlist,
+                 const unsigned int *__restrict__ dctl, long long dcap)
+{
+    extern __shared__ float ell[];   // [128][kDPitch]
+    __shared__ unsigned int s_red[kDThreads / 32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the routing launches have listed their tiles
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = lane & 7, rg = lane >> 3;      // q: feature eighth (pairs 4 q .. 4 q + 3)
+    const int r0 = 32 * (warp & 3) + 8 * rg;     // this thread's rows r0 .. r0 + 7 of the tile
+    const int k0 = 64 * (warp >> 2);             // its half of the components
+    // the listed tiles in head order; this CTA takes a contiguous range of them, so that it
+    // works on one or two heads (their parameters stay in L1) and needs no atomics
+    unsigned int listed = 0;
+    for (int h = tid; h < H; h += kDThreads) listed += dctl[h];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) listed += __shfl_xor_sync(0xffffffffu, listed, o);
+    if (lane == 0) s_red[warp] = listed;
+    __syncthreads();
+    listed = 0;
+#pragma unroll
+    for (int w = 0; w < kDThreads / 32; ++w) listed += s_red[w];
+    if (listed == 0) return;   // nothing listed (peaked inputs)
+    const unsigned int per = (listed + gridDim.x - 1) / gridDim.x;
+    const unsigned int g0 = blockIdx.x * per, g1 = min(listed, g0 + per);
+    int hc = 0;                // the head of position g: hbase = sum of the counts of heads < hc
+    unsigned int hbase = 0, hcnt = g0 < g1 ? dctl[0] : 0;
+    for (unsigned int g = g0; g < g1; ++g) {
+        while (g >= hbase + hcnt) {   // uniform: every thread walks the same counts
+            hbase += hcnt;
+            hcnt = dctl[++hc];
+        }
+        const int2 e = dlist[(long long)hc * dcap + (g - hbase)];
+        const DenseSrc src = (e.x >> 30) ? s1 : s0;
+        const long long bh = e.x & 0x3fffffff;
+        const int N = src.N, row0 = e.y * kPRows, h = (int)(bh % H);
+        // the eight rows' feature eighth (zeros past the slice end)
+        float2 xr[8][4];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int row = row0 + r0 + r;
+            const long long off = (bh * N + row) * kPD + 8 * q;
+            if (row < N) {
+                if (x_bf16) {
+                    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src.x) + off));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        xr[r][c] = make_float2(__uint_as_float(ww[c] << 16), __uint_as_float(ww[c] & 0xffff0000u));
+                } else {
+                    const float4 *p4 = reinterpret_cast<const float4 *>(static_cast<const float *>(src.x) + off);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {   // routing rows: L2 only, L1 keeps the parameters
+                        const float4 w = __ldcg(p4 + u);
+                        xr[r][2 * u] = make_float2(w.x, w.y);
+                        xr[r][2 * u + 1] = make_float2(w.z, w.w);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xr[r][j] = make_float2(0.f, 0.f);
+            }
+        }
+        const float4 *ph = pimg2 + (long long)h * kPK * kPDP + q;
+        const float *ch = cimg + (long long)h * 4 * kPK;   // c_k
+#pragma unroll 1
+        for (int kb = k0; kb < k0 + 64; kb += 2) {
+            float2 acc[2][8];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[c][r] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 pa = ld_keep(ph + kb * kPDP + 8 * j), pb = ld_keep(ph + (kb + 1) * kPDP + 8 * j);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float2 ya = __ffma2_rn(xr[r][j], make_float2(pa.x, pa.y), make_float2(pa.z, pa.w));
+                    acc[0][r] = __ffma2_rn(ya, ya, acc[0][r]);
+                    const float2 yb = __ffma2_rn(xr[r][j], make_float2(pb.x, pb.y), make_float2(pb.z, pb.w));
+                    acc[1][r] = __ffma2_rn(yb, yb, acc[1][r]);
+                }
+            }
+            // v[8 c + r]: this lane's partial sum of component kb + c, row r0 + r; recursive halving
+            // over the eighth lanes: xor 1 keeps one component, xor 2 four of the rows, xor 4 two
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) v[8 * c + r] = acc[c][r].x + acc[c][r].y;
+#pragma unroll
+            for (int o = 1, n = 8; o <= 4; o <<= 1, n >>= 1) {
+                const bool up = (q & o) != 0;
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2)
+                    if (e2 < n) {
+                        const float send = up ? v[e2] : v[e2 + n], keep = up ? v[e2 + n] : v[e2];
+                        v[e2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+            }
+            // this lane now holds component kb + (q & 1) for rows r0 + 4 ((q >> 1) & 1) + 2 (q >> 2) + {0, 1}
+            const int k = kb + (q & 1), rr = r0 + 4 * ((q >> 1) & 1) + 2 * (q >> 2);
+            const float c = __ldg(ch + k);
+            ell[rr * kDPitch + k] = fmaf(-0.5f, v[0], c);
+            ell[(rr + 1) * kDPitch + k] = fmaf(-0.5f, v[1], c);
+        }
+        __syncthreads();
+        // softmax of row tid / 2 over components 2 m + tid % 2 (in place)
+        {
+            float *er = ell + (tid >> 1) * kDPitch + (tid & 1);
+            float m = -FLT_MAX;
+#pragma unroll 8
+            for (int i = 0; i < kPK / 2; ++i) m = fmaxf(m, er[2 * i]);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            float sum = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < kPK / 2; ++i) {
+                const float ex = expf(er[2 * i] - m);
+                er[2 * i] = ex;
+                sum += ex;
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            const float inv = 1.0f / sum;
+#pragma unroll 8
+            for (int i = 0; i < kPK / 2; ++i) er[2 * i] *= inv;
+        }
+        __syncthreads();
+        // rows out: warp w takes rows 16 w .. + 15, one row per instruction (fp32: 32 lanes x 16 B)
+        // or two (16-bit planes: 16 lanes x 16 B each)
+        if (layout == GL_F32) {
+            float *g = static_cast<float *>(src.gamma);
+#pragma unroll 4
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * warp + rr, row = row0 + r;
+                if (row < N)
+                    reinterpret_cast<float4 *>(g + (bh * N + row) * kPK)[lane] =
+                        *reinterpret_cast<const float4 *>(ell + r * kDPitch + 4 * lane);
+            }
+        } else {
+            __nv_bfloat16 *g = static_cast<__nv_bfloat16 *>(src.gamma);
+#pragma unroll 2
+            for (int rr = 0; rr < 16; rr += 2) {
+                const int r = 16 * warp + rr + (lane >> 4), row = row0 + r, c8 = 8 * (lane & 15);
+                if (row < N) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat16 h0, l0, h1, l1;
+                        split_bf16(ell[r * kDPitch + c8 + 2 * u], h0, l0);
+                        split_bf16(ell[r * kDPitch + c8 + 2 * u + 1], h1, l1);
+                        hw[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                        lw[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                    }
+                    const long long o = (bh * N + row) * kPK + c8;
+                    *reinterpret_cast<uint4 *>(g + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    if (layout == GL_SPLIT)
+                        *reinterpret_cast<uint4 *>(g + src.plane + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+        }
+        __syncthreads();   // the tile of log-joints is reused by the next tile
+    }
+}
+
 } // namespace
 
 bool resp_pruned_applies(const Dims &dm) { return dm.K == kPK && dm.D == kPD; }
@@ -599,12 +836,12 @@ cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, fl
 {
     if (!resp_pruned_applies(dm)) return cudaErrorInvalidValue;
     k_prep_all<<<dim3(dm.H, kPK / kPrepAllComps), kPrepAllThreads, 0, st>>>(p.mu, p.var_raw, p.logit_pi, prm, cst,
-                                                                           img.w, img.p, img.c);
+                                                                           img.w, img.p, img.c, img.p2, img.ctl);
     return cudaGetLastError();
 }
 
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
-                               int layout, cudaStream_t st)
+                               int layout, cudaStream_t st, int src)
 {
     constexpr size_t smem = PrunedSmem::bytes;
     static std::atomic<unsigned long long> smem_set{0};
@@ -633,8 +870,34 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, nsl, dm.x_bf16, img.w, img.p,
-                                                 img.c, layout, pstride, flag);
+                                                 img.c, layout, pstride, flag, img.list, img.ctl, img.cap, src);
     return cudaGetLastError();
+}
+
+cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
+                              const PrunedImages &img, int layout, cudaStream_t st)
+{
+    constexpr size_t smem = (size_t)kPRows * kDPitch * 4;
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t e = allow_smem(k_resp_dense, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const DenseSrc s0{x0, g0, d0.N, d0.BH() * d0.N * (long long)kPK};
+    const DenseSrc s1 = x1 ? DenseSrc{x1, g1, d1.N, d1.BH() * d1.N * (long long)kPK} : s0;
+    const long long items = routing_tiles(d0.BH(), d0.N) + (x1 ? routing_tiles(d1.BH(), d1.N) : 0);
+    cudaLaunchConfig_t cfg = {};
+    const long long ctas = 2LL * sm_count();   // two resident per SM
+    cfg.gridDim = dim3((unsigned)(items < ctas ? (items > 0 ? items : 1) : ctas));
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_resp_dense, s0, s1, d0.x_bf16, d0.H, (const float4 *)img.p2,
+                              (const float *)img.c, layout, (const int2 *)img.list, (const unsigned int *)img.ctl,
+                              img.cap);
 }
 
 } // namespace gma

@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "libgma.so")
 _lib = None
 
 F32, BF16 = 0, 1
-OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_DECODE, OP_CAUSAL_HOST = 0, 1, 2, 3, 4
+OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_DECODE, OP_CAUSAL_HOST, OP_USAGE, OP_BACKWARD = 0, 1, 2, 3, 4, 5, 6
 _DT = {"f32": F32, "bf16": BF16, torch.float32: F32, torch.bfloat16: BF16}
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -91,9 +91,15 @@ def load():
                                                    ctypes.POINTER(Profile)]
         lib.gma_decode_step_profiled.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P,
                                                  ctypes.POINTER(Profile)]
+        lib.gma_responsibility_stats.argtypes = [S, _Params, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.gma_cross_workspace_size.argtypes = [S, ctypes.c_int]
+        lib.gma_cross_workspace_size.restype = ctypes.c_size_t
+        lib.gma_forward_cross.argtypes = [S, ctypes.c_int, _Params, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.gma_backward.argtypes = [S, ctypes.c_int, _Params, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.gma_sync_status.argtypes = [P]
         lib.gma_test_wait_timeout.argtypes = [ctypes.c_longlong, P]
-        for fn in ("gma_sync_status", "gma_test_wait_timeout", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
+        for fn in ("gma_backward", "gma_responsibility_stats", "gma_forward_cross", "gma_sync_status",
+                   "gma_test_wait_timeout", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_decode_step",
                    "gma_forward_causal_host", "gma_forward_causal_profiled", "gma_decode_step_noalloc",
                    "gma_forward_bidir_profiled", "gma_decode_step_profiled"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -167,6 +173,73 @@ def gma_responsibilities(shape: Shape, mu, var_raw, logit_pi, x, gamma, ws=None,
     _check("gma_responsibilities",
            load().gma_responsibilities(ctypes.byref(s), prm, xp, gp, wp, wn, _stream(dev, stream)))
     return gamma
+
+
+def gma_responsibility_stats(shape: Shape, mu, var_raw, logit_pi, x, usage, counts, entropy, assign=None,
+                             ws=None, stream=None):
+    """Per-head diagnostics of the responsibilities of routing rows x [B,H,N,d_route]:
+    usage [H,K] fp32 (soft sums), counts [H,K] int64 (hard assignments), entropy [H,2]
+    fp32 (normalised entropies of usage and counts), assign [B,H,N] int32 (optional)."""
+    dev = x.device
+    s = shape
+    xp = _ptr(x, "x", (s.B, s.H, s.N, s.d_route), _TORCH_DT[s.x_dtype], dev)
+    up = _ptr(usage, "usage", (s.H, s.K), torch.float32, dev)
+    cp = _ptr(counts, "counts", (s.H, s.K), torch.int64, dev)
+    ep = _ptr(entropy, "entropy", (s.H, 2), torch.float32, dev)
+    ap = _ptr(assign, "assign", (s.B, s.H, s.N), torch.int32, dev, optional=True)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    wp, wn = _ws(s, OP_USAGE, ws, dev)
+    _check("gma_responsibility_stats",
+           load().gma_responsibility_stats(ctypes.byref(s), prm, xp, up, cp, ep, ap, wp, wn, _stream(dev, stream)))
+    return usage, counts, entropy
+
+
+def gma_backward(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, dout, dqx, dkx, dv, dmu, dvar_raw, dlogit_pi,
+                 causal=True, ws=None, stream=None):
+    """Gradients of the causal (or bidirectional) forward given dout = dL/dO [B,H,N,d_v] (fp32):
+    dqx, dkx [B,H,N,d_route], dv [B,H,N,d_v], dmu, dvar_raw [H,K,d_route], dlogit_pi [H,K], all fp32."""
+    dev = qx.device
+    s = shape
+    f32 = torch.float32
+    q, k, vv, _ = _fwd_ptrs(s, qx, kx, v, dout, dev)
+    g = _ptr(dout, "dout", (s.B, s.H, s.N, s.d_v), f32, dev)
+    dq = _ptr(dqx, "dqx", (s.B, s.H, s.N, s.d_route), f32, dev)
+    dk = _ptr(dkx, "dkx", (s.B, s.H, s.N, s.d_route), f32, dev)
+    dvp = _ptr(dv, "dv", (s.B, s.H, s.N, s.d_v), f32, dev)
+    dm = _ptr(dmu, "dmu", (s.H, s.K, s.d_route), f32, dev)
+    dr = _ptr(dvar_raw, "dvar_raw", (s.H, s.K, s.d_route), f32, dev)
+    dl = _ptr(dlogit_pi, "dlogit_pi", (s.H, s.K), f32, dev)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    wp, wn = _ws(s, OP_BACKWARD, ws, dev)
+    _check("gma_backward",
+           load().gma_backward(ctypes.byref(s), int(bool(causal)), prm, q, k, vv, g, dq, dk, dvp, dm, dr, dl, wp, wn,
+                               _stream(dev, stream)))
+    return dqx, dkx, dv, dmu, dvar_raw, dlogit_pi
+
+
+def gma_cross_workspace_size(shape: Shape, n_kv: int) -> int:
+    return int(load().gma_cross_workspace_size(ctypes.byref(shape), int(n_kv)))
+
+
+def gma_forward_cross(shape: Shape, mu, var_raw, logit_pi, qx, kx, v, out, ws=None, stream=None):
+    """out [B,H,N,d_v]: queries qx [B,H,N,d_route] read the memory written by kx
+    [B,H,n_kv,d_route] and v [B,H,n_kv,d_v] (n_kv taken from kx)."""
+    dev = qx.device
+    s = shape
+    xdt, vdt = _TORCH_DT[s.x_dtype], _TORCH_DT[s.v_dtype]
+    n_kv = kx.shape[2]
+    q = _ptr(qx, "qx", (s.B, s.H, s.N, s.d_route), xdt, dev)
+    k = _ptr(kx, "kx", (s.B, s.H, n_kv, s.d_route), xdt, dev)
+    vv = _ptr(v, "v", (s.B, s.H, n_kv, s.d_v), vdt, dev)
+    o = _ptr(out, "out", (s.B, s.H, s.N, s.d_v), torch.float32, dev)
+    prm = _params(s, mu, var_raw, logit_pi, dev)
+    need = gma_cross_workspace_size(s, n_kv)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    wp = _ptr(ws, "ws", dtype=torch.uint8, device=dev)
+    _check("gma_forward_cross",
+           load().gma_forward_cross(ctypes.byref(s), n_kv, prm, q, k, vv, o, wp, ws.numel(), _stream(dev, stream)))
+    return out
 
 
 def _fwd_ptrs(s, qx, kx, v, out, dev):

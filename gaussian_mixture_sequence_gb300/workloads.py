@@ -33,7 +33,7 @@ _CODES = {
     "mu": 1, "var_raw": 2, "logit_pi": 3,
     "qx": 4, "kx": 5, "v": 6,
     "qx_dec": 7, "kx_dec": 8, "v_dec": 9,
-    "qcomp": 10, "kcomp": 11, "qcomp_dec": 12, "kcomp_dec": 13,
+    "qcomp": 10, "kcomp": 11, "qcomp_dec": 12, "kcomp_dec": 13, "dout": 14,
 }
 
 
@@ -47,7 +47,7 @@ class Workload:
     d: int            # d_route: width of Q_X and K_X rows
     dv: int           # d_v: width of V rows
     K: int            # number of Gaussian components
-    mode: str         # "causal", "bidir" or "decode"
+    mode: str         # "causal", "bidir", "decode" or "backward" (gradients of the causal form)
     eps: float = 1e-6
     x_dtype: str = "f32"      # storage of Q_X / K_X: "f32" or "bf16"
     v_dtype: str = "f32"      # storage of V
@@ -82,6 +82,10 @@ WORKLOADS = {
     "causal_8k_K512": Workload("causal_8k_K512", 4, 8, 8192, 64, 64, 512, "causal", seed=1004),
     "decode_b256": Workload("decode_b256", 256, 16, 4096, 64, 64, 128, "decode",
                             decode_steps=1024, seed=1005),
+    # gradients of the causal form (dL/dO drawn N(0,1) per slice)
+    "backward_4k": Workload("backward_4k", 4, 8, 4096, 64, 64, 128, "backward", seed=1001),
+    "backward_16k_peaked": Workload("backward_16k_peaked", 2, 16, 16384, 64, 64, 128, "backward",
+                                    dist="peaked", seed=1002),
 }
 
 
@@ -169,3 +173,18 @@ def sample_slices(wl: Workload, count: int, seed: int = 7):
     pick = set(rng.choice(total - 1, size=count - 1, replace=False).tolist())
     pick.add(total - 1)
     return sorted(pick)
+
+
+def dout_slice(wl: Workload, b: int, h: int, seed: int | None = None):
+    """dL/dO [N, dv] of slice (b, h) for the gradient workloads, N(0,1), float32."""
+    seed = wl.seed if seed is None else seed
+    return _rng(seed, _CODES["dout"], b, h).standard_normal((wl.N, wl.dv), dtype=np.float32)
+
+
+def full_dout(wl: Workload, seed: int | None = None):
+    """dL/dO [B, H, N, dv] for the gradient workloads."""
+    g = np.empty((wl.B, wl.H, wl.N, wl.dv), np.float32)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            g[b, h] = dout_slice(wl, b, h, seed)
+    return g

@@ -86,7 +86,9 @@ typedef enum {
     GMA_OP_BIDIR = 1,
     GMA_OP_CAUSAL = 2,
     GMA_OP_DECODE = 3,
-    GMA_OP_CAUSAL_HOST = 4   /* gma_forward_causal_host: staging + the causal workspace */
+    GMA_OP_CAUSAL_HOST = 4,  /* gma_forward_causal_host: staging + the causal workspace */
+    GMA_OP_USAGE = 5,        /* gma_responsibility_stats */
+    GMA_OP_BACKWARD = 6      /* gma_backward (causal or bidirectional) */
 } gma_op;
 
 typedef struct {
@@ -126,12 +128,46 @@ size_t gma_workspace_size(const gma_shape *shape, gma_op op);
 gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const void *x,
                                 float *gamma, void *ws, size_t ws_bytes, gma_stream_t stream);
 
+/* Responsibility diagnostics (the interpretability reading of "결과 및 성능":
+ * components in use, usage entropy, hard assignments), as a reduction over
+ * the responsibilities of the routing rows x [B, H, N, d_route] (x_dtype),
+ * which the call computes in its workspace.  Per head h, over the B*N rows
+ * of that head:
+ *   usage    [H, K] fp32    soft usage, sum_i gamma_ik
+ *   counts   [H, K] int64   hard assignments: rows whose argmax is k (the
+ *                           lowest k among equal values)
+ *   entropy  [H, 2] fp32    entropy of usage[h] / sum(usage[h]) and of
+ *                           counts[h] / (B N), each divided by log K (0 when
+ *                           K = 1); a value of 1 means uniform use
+ *   assign   nullable [B, H, N] int32: the argmax of every row
+ * The number of components in use is the count of k with counts[h][k] > 0.
+ * Sums run in a fixed order: repeated calls give identical results.
+ * Workspace: gma_workspace_size(shape, GMA_OP_USAGE).                        */
+gma_status gma_responsibility_stats(const gma_shape *shape, gma_params params, const void *x,
+                                    float *usage, long long *counts, float *entropy, int *assign,
+                                    void *ws, size_t ws_bytes, gma_stream_t stream);
+
 /* Bidirectional forward (write phase then read phase of "핵심 메커니즘"):
  *   qx, kx [B, H, N, d_route] (x_dtype);  v [B, H, N, d_v] (v_dtype)
  *   out    [B, H, N, d_v] fp32:  O = Gamma_Q Vt / (Gamma_Q Z + eps).        */
 gma_status gma_forward_bidir(const gma_shape *shape, gma_params params, const void *qx,
                              const void *kx, const void *v, float *out, void *ws,
                              size_t ws_bytes, gma_stream_t stream);
+
+/* Cross-attention (named as an extension in "의의 및 주장"): the queries of one
+ * sequence read the latent memory written by the keys and values of another.
+ * shape->N is the number of query rows; n_kv >= 0 the number of key/value
+ * rows (every other field is shared).  Same arithmetic as the bidirectional
+ * form, which it equals when the two sequences are the same.
+ *   qx  [B, H, N, d_route] (x_dtype)      kx [B, H, n_kv, d_route] (x_dtype)
+ *   v   [B, H, n_kv, d_v]  (v_dtype)      out [B, H, N, d_v] fp32
+ * With n_kv = 0 the memory is empty and out = 0 / (0 + eps).  kx and v may be
+ * NULL when n_kv = 0; every pointer may be NULL when N = 0 (nothing is done).
+ * Workspace: gma_cross_workspace_size(shape, n_kv) bytes (0 on invalid input). */
+size_t gma_cross_workspace_size(const gma_shape *shape, int n_kv);
+gma_status gma_forward_cross(const gma_shape *shape, int n_kv, gma_params params, const void *qx,
+                             const void *kx, const void *v, float *out, void *ws, size_t ws_bytes,
+                             gma_stream_t stream);
 
 /* Causal forward (prefix-sum variant of "변형 및 학습"): O_i reads the memory
  * written by positions j <= i.
@@ -163,6 +199,25 @@ gma_status gma_forward_causal_host(const gma_shape *shape, gma_params params, co
                                    const void *kx, const void *v, const float *state_in,
                                    float *state_out, float *out, void *ws, size_t ws_bytes,
                                    gma_stream_t stream);
+
+/* Gradients of the causal (causal = 1) or bidirectional (causal = 0) forward,
+ * for end-to-end training ("변형 및 학습": the GMM parameters are learned by
+ * backpropagation through the softplus and softmax reparameterisations).
+ * Given dout = dL/dO [B, H, N, d_v] (fp32), the call recomputes the forward
+ * (responsibilities, memory) and writes, all fp32:
+ *   dqx, dkx  [B, H, N, d_route]   (gradients of the stored Q_X, K_X values)
+ *   dv        [B, H, N, d_v]
+ *   dmu, dvar_raw [H, K, d_route], dlogit_pi [H, K]: summed over the batch
+ *             and over both routings (one GMM per head), overwritten.
+ * The arithmetic is fp32 on CUDA cores (shape->gemm_dtype and shape->chunk
+ * are ignored: chunks of 64 rows); every reduction runs in a fixed order, so
+ * repeated calls give identical results.  The causal form starts from an
+ * empty memory (no state_in).  Workspace: gma_workspace_size(shape,
+ * GMA_OP_BACKWARD).  N = 0 gives zero parameter gradients.                  */
+gma_status gma_backward(const gma_shape *shape, int causal, gma_params params, const void *qx,
+                        const void *kx, const void *v, const float *dout, float *dqx, float *dkx,
+                        float *dv, float *dmu, float *dvar_raw, float *dlogit_pi, void *ws,
+                        size_t ws_bytes, gma_stream_t stream);
 
 /* One recurrent decode step (the causal form advanced by one token; constant
  * memory per head as in "선형 어텐션 원리 정리"): the token is written into the

@@ -216,3 +216,54 @@ def test_timeout_hooks_validate_on_the_host(lib):
     assert lib.gma_test_wait_timeout(-5, None) == 1
     assert lib.gma_test_wait_timeout(4000000001, None) == 1
     assert gma.gma_status_string(gma.TIMEOUT) == "a bounded device wait expired"
+
+
+def test_cross_validation(lib):
+    """Cross-attention: host-side checks of the key length, pointers and workspace."""
+    s = _shape(N=300)
+    need = gma.gma_cross_workspace_size(s, 1000)
+    assert need > gma.gma_cross_workspace_size(s, 100) > 0
+    assert gma.gma_cross_workspace_size(s, -1) == 0
+    assert gma.gma_cross_workspace_size(_shape(d_route=48), 10) == 0
+    # equal lengths: the bidirectional workspace
+    assert gma.gma_cross_workspace_size(s, 300) == gma.gma_workspace_size(s, gma.OP_BIDIR)
+    call = lambda n_kv=1000, q=FAKE, k=FAKE, v=FAKE, o=FAKE, ws=FAKE, wn=need: lib.gma_forward_cross(
+        ctypes.byref(s), n_kv, _prm(), q, k, v, o, ws, wn, None)
+    assert call(n_kv=-1) == 1
+    assert call(q=None) == 1 and call(o=None) == 1 and call(k=None) == 1 and call(v=None) == 1
+    assert call(k=FAKE + 4) == 3 and call(o=FAKE + 8) == 3
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    # no query rows: nothing to do, every pointer may be null
+    s0 = _shape(N=0)
+    assert lib.gma_forward_cross(ctypes.byref(s0), 50, _prm(), None, None, None, None, FAKE, 1 << 30, None) == 0
+
+
+def test_stats_validation(lib):
+    s = _shape(N=300)
+    need = gma.gma_workspace_size(s, gma.OP_USAGE)
+    assert need > 0
+    call = lambda x=FAKE, u=FAKE, c=FAKE, e=FAKE, a=None, ws=FAKE, wn=need: lib.gma_responsibility_stats(
+        ctypes.byref(s), _prm(), x, u, c, e, a, ws, wn, None)
+    assert call(x=None) == 1 and call(u=None) == 1 and call(c=None) == 1 and call(e=None) == 1
+    assert call(u=FAKE + 4) == 3 and call(a=FAKE + 4) == 3
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    assert gma.gma_workspace_size(_shape(K=513), gma.OP_USAGE) == 0
+
+
+def test_backward_validation(lib):
+    s = _shape(N=300)
+    need = gma.gma_workspace_size(s, gma.OP_BACKWARD)
+    assert need > gma.gma_workspace_size(s, gma.OP_CAUSAL)
+    call = lambda causal=1, **kw: lib.gma_backward(
+        ctypes.byref(s), causal, _prm(), *(kw.get(n, FAKE) for n in ("q", "k", "v", "g", "dq", "dk", "dv", "dm",
+                                                                        "dr", "dl", "ws")),
+        kw.get("wn", need), None)
+    assert call(causal=2) == 1
+    for n in ("q", "k", "v", "g", "dq", "dk", "dv", "dm", "dr", "dl"):
+        assert call(**{n: None}) == 1, n
+        assert call(**{n: FAKE + 4}) == 3, n
+    assert call(ws=None) == 4 and call(wn=need - 1) == 4
+    assert gma.gma_workspace_size(_shape(d_v=8), gma.OP_BACKWARD) == 0
+    # the gradient pass ignores the chunk length and the product type of the shape
+    assert gma.gma_workspace_size(_shape(N=300, chunk=16), gma.OP_BACKWARD) == need
+    assert gma.gma_workspace_size(_shape(N=300, gemm_dtype="bf16"), gma.OP_BACKWARD) == need
