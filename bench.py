@@ -66,7 +66,8 @@ def eff_chunk(wl):
     """Chunk length the library uses for this workload (its default when 0)."""
     if wl.chunk:
         return wl.chunk
-    tc = wl.K == 128 and (wl.dv == 64 or (wl.dv == 128 and wl.gemm_dtype == "bf16"))
+    tc = ((wl.K <= 128 or (wl.K % 128 == 0 and wl.K <= 512))
+          and (wl.dv == 64 or (wl.dv == 128 and wl.gemm_dtype == "bf16")))
     return 128 if tc else 64
 
 

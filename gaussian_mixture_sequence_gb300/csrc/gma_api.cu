@@ -36,6 +36,7 @@ gma_status make_dims(const gma_shape *s, Dims *dm, gma_op op = GMA_OP_CAUSAL)
     if (st == GMA_OK && op != GMA_OP_CAUSAL && op != GMA_OP_BIDIR && dm->C == 128) {
         dm->C = 64;
         dm->blk = kBlockRows;
+        dm->KG = dm->KP;
     }
     return st;
 }
@@ -71,6 +72,7 @@ gma_status make_dims_raw(const gma_shape *s, Dims *dm)
     if (BH * (long long)s->N * w >= (1LL << 40)) return GMA_ERR_UNSUPPORTED;
     dm->B = s->B; dm->H = s->H; dm->N = s->N; dm->D = s->d_route; dm->DV = s->d_v; dm->K = s->K;
     dm->KP = (int)round_up(s->K, 8);
+    dm->KG = C == 128 ? tc_kpad(s->K) : dm->KP;
     dm->C = C;
     dm->blk = C == 128 ? 128 : kBlockRows;
     dm->eps = s->eps;
@@ -108,12 +110,14 @@ WsPlan plan(const Dims &dm, gma_op op)
     }
     if (op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL) {
         const size_t gb = dm.g_bf16 ? 2 : 4;
-        p.gq = take((size_t)dm.BH() * dm.N * dm.KP * gb);
-        p.gk = take((size_t)dm.BH() * dm.N * dm.KP * gb);
+        p.gq = take((size_t)dm.BH() * dm.N * dm.KG * gb);
+        p.gk = take((size_t)dm.BH() * dm.N * dm.KG * gb);
         p.partial = take((size_t)dm.BH() * dm.nblk() * dm.state_size() * 4);
-        if (op == GMA_OP_BIDIR) p.total = take((size_t)dm.BH() * dm.state_size() * 4);
-        if (op == GMA_OP_CAUSAL && tc_path_applies(dm))   // the carried memory in operand form
-            p.mem = take((size_t)dm.BH() * dm.nblk() * dm.state_size() * 4);
+        const bool tc = tc_path_applies(dm);
+        if (op == GMA_OP_BIDIR)   // the total memory: fp32, or in operand form on the tensor-core path
+            p.total = take((size_t)dm.BH() * (tc ? tc_mem_words(dm) : dm.state_size()) * 4);
+        if (op == GMA_OP_CAUSAL && tc)   // the carried memory of every chunk in operand form
+            p.mem = take((size_t)dm.BH() * dm.nblk() * tc_mem_words(dm) * 4);
     }
     p.bytes = off;
     return p;
@@ -401,9 +405,9 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
         GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st, 0));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KG, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st, 1));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KG, gamma_layout(dm), st, 1));
     if (imgp) {
         GMA_CUDA(mk.mark("resp_dense"));
         GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));
@@ -451,10 +455,10 @@ WsPlan plan_cross(const Dims &dq, const Dims &dk)
         p.dlist = take((size_t)dq.H * p.dcap * 8);
     }
     const size_t gb = dq.g_bf16 ? 2 : 4;
-    p.gq = take((size_t)dq.BH() * dq.N * dq.KP * gb);
-    p.gk = take((size_t)dk.BH() * dk.N * dk.KP * gb);
+    p.gq = take((size_t)dq.BH() * dq.N * dq.KG * gb);
+    p.gk = take((size_t)dk.BH() * dk.N * dk.KG * gb);
     p.partial = take((size_t)dk.BH() * dk.nblk() * dk.state_size() * 4);
-    p.total = take((size_t)dk.BH() * dk.state_size() * 4);
+    p.total = take((size_t)dk.BH() * (tc_path_applies(dq) ? tc_mem_words(dq) : dk.state_size()) * 4);
     p.bytes = off;
     return p;
 }
@@ -492,13 +496,13 @@ gma_status run_cross(const gma_shape *shape, int n_kv, gma_params params, const 
     const PrunedImages *imgp = wp.pruned ? &img : nullptr;
     if (wp.pruned) GMA_CUDA(launch_prep_all(dq, params, prm, cst, img, st));
     else GMA_CUDA(launch_prep(dq, params, prm, cst, st));
-    GMA_CUDA(launch_resp(dq, prm, cst, imgp, qx, gq, dq.KP, gamma_layout(dq), st, 0));
-    if (dk.N > 0) GMA_CUDA(launch_resp(dk, prm, cst, imgp, kx, gk, dk.KP, gamma_layout(dk), st, 1));
+    GMA_CUDA(launch_resp(dq, prm, cst, imgp, qx, gq, dq.KG, gamma_layout(dq), st, 0));
+    if (dk.N > 0) GMA_CUDA(launch_resp(dk, prm, cst, imgp, kx, gk, dk.KG, gamma_layout(dk), st, 1));
     if (imgp)
         GMA_CUDA(launch_resp_dense(dq, qx, gq, dk, dk.N > 0 ? kx : nullptr, gk, img, gamma_layout(dq), st));
     const bool tc = tc_path_applies(dq);
     if (dk.N == 0) {   // no keys: an empty memory (zeros in either layout)
-        GMA_CUDA(cudaMemsetAsync(total, 0, (size_t)dk.BH() * dk.state_size() * 4, st));
+        GMA_CUDA(cudaMemsetAsync(total, 0, (size_t)dk.BH() * (tc ? tc_mem_words(dk) : dk.state_size()) * 4, st));
     } else {
         if (tc) {
             GMA_CUDA(launch_chunk_state_tc(dk, gk, v, partial, st));
@@ -586,9 +590,9 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
         GMA_CUDA(launch_prep(dm, params, prm, cst, st));
     }
     GMA_CUDA(mk.mark("resp_q"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, gamma_layout(dm), st, 0));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KG, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
-    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, gamma_layout(dm), st, 1));
+    GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KG, gamma_layout(dm), st, 1));
     if (imgp) {
         GMA_CUDA(mk.mark("resp_dense"));
         GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));

@@ -6,6 +6,11 @@
 // C = 128 tokens, dense products inside a chunk, and a carried memory
 // [Vt | Z] between chunks.
 //
+// K components are taken in groups of 128 (K = 256 .. 512: the contraction over
+// components accumulates group by group into the same tensor-memory accumulator,
+// and the chunk contribution is written group by group; K < 128: operands padded
+// with zero components to 128).
+//
 //   k_chunk_state_tc : L_c = Gamma_K,c^T [V_c | 1]                 (chunk contribution)
 //   k_scan_split     : S_{c-1} = state_in + sum_{c' < c} L_c'        (carried memory)
 //   k_chunk_out_tc   : [P | U] = Gamma_Q,c [Gamma_K,c ; Vt_{c-1}^T]^T
@@ -39,7 +44,7 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 128;                      // chunk rows (= MMA M)
-constexpr int kK = 128;                      // components handled by this path
+constexpr int kK = 128;                      // components per group (the MMA M / contraction tile)
 constexpr int kKSteps = kK * 2 / 32;         // MMA k-steps (16 bf16 each) of a 128-deep contraction
 constexpr uint32_t kRowB = kK * 2;           // bytes of one 128-element bf16 row
 constexpr uint32_t kAtom = kC * 128;         // bytes of one 128-row atom column
@@ -137,7 +142,7 @@ struct StateMaps {
 
 template <bool SPLIT, int DV>
 __global__ void __launch_bounds__(kStateThreads, 1)
-    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items,
+    k_chunk_state_tc(const __grid_constant__ StateMaps maps, int N, int nblk, long long items, int K, int KH,
                      const void *__restrict__ v, bool v_bf16, float *__restrict__ partial, unsigned int *timeout)
 {
     using Sm = StateSmem<SPLIT, DV>;
@@ -160,21 +165,27 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     const long long per = (items + gridDim.x - 1) / gridDim.x;
     const long long it0 = (long long)blockIdx.x * per;
     const long long it1 = it0 + per < items ? it0 + per : items;
-    const long long SZ = (long long)kK * DV + kK;
+    const long long SZ = (long long)K * DV + K;
     const float qnan = __int_as_float(0x7fc00000);
+    // item it: component group it % KH of chunk it / KH (of the list (slice, chunk))
 
-    auto load = [&](long long it, int b) {   // one thread: the chunk's Gamma_K planes into landing buffer b
-        const int sl = (int)(it / nblk), c0 = (int)(it % nblk) * kC;
+    // chunk and component group of item it (one group: no division)
+    auto chunk_of = [&](long long it) { return KH == 1 ? it : it / KH; };
+    auto group_of = [&](long long it) { return KH == 1 ? 0 : (int)(it % KH); };
+    auto load = [&](long long it, int b) {   // one thread: the group's Gamma_K planes into landing buffer b
+        const long long ch = chunk_of(it);
+        const int sl = (int)(ch / nblk), c0 = (int)(ch % nblk) * kC, x0 = kK * group_of(it);
         const uint32_t bl = smem_addr(bar + b);
         mbar_expect_tx(bl, Sm::L);
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a)
-                tma_load_3d(smem_addr(land + b * Sm::L + pl * Sm::G + a * Sm::BLK), &maps.gk[pl], a * 64, c0, sl, bl);
+                tma_load_3d(smem_addr(land + b * Sm::L + pl * Sm::G + a * Sm::BLK), &maps.gk[pl], x0 + a * 64, c0, sl, bl);
     };
     // V of chunk it as raw words (fp32, or bf16 pairs in .x and .y); F4 consecutive threads read a row
     auto load_v = [&](long long it, uint4 (&r)[VPER]) {
-        const int c0 = (int)(it % nblk) * kC, nr = min(kC, N - c0);
-        const long long rowbase = (it / nblk) * N + c0;
+        const long long ch = chunk_of(it);
+        const int c0 = (int)(ch % nblk) * kC, nr = min(kC, N - c0);
+        const long long rowbase = (ch / nblk) * N + c0;
 #pragma unroll
         for (int u = 0; u < VPER; ++u) {
             const int f = tid + u * kStateThreads, j = f / F4, c4 = 4 * (f % F4);
@@ -242,7 +253,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     const uint32_t tbase = *tslot;
     // L of chunk it from accumulator b (its MMA complete), into its block
     auto take = [&](long long it, int b, bool okv) {
-        float *o = partial + it * SZ;
+        float *o = partial + chunk_of(it) * SZ;
+        const int kg = kK * group_of(it) + k;    // this thread's component
+        const bool kin = kg < K;                 // not a padding component
         const uint32_t d = 256u * b;
 #pragma unroll
         for (int cb = 0; cb < DV / 4; cb += 16) {
@@ -261,14 +274,15 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 16; ++q) x[q] = __uint_as_float(r[q]);
             }
+            if (kin)
 #pragma unroll
-            for (int q = 0; q < 16; ++q) o[(long long)(c + q) * kK + k] = okv ? x[q] : qnan;
+                for (int q = 0; q < 16; ++q) o[(long long)(c + q) * K + kg] = okv ? x[q] : qnan;
         }
         if (tg == 0) {   // Z: any column of the ones block
             uint32_t r[16];
             tmem_ld16(tmem_at(tbase, lane0, d + NBV * 64), r);
             tmem_wait_ld();
-            o[(long long)kK * DV + k] = okv ? __uint_as_float(r[0]) : qnan;
+            if (kin) o[(long long)K * DV + kg] = okv ? __uint_as_float(r[0]) : qnan;
         }
     };
 
@@ -334,39 +348,54 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 }
 
 // ------------------------------------------------------------------------
-// Carried memory in operand form.  One thread per state element (block layout:
-// element e < K d_v is Vt^T[e / K][e % K], then Z), serial over the chunks of
-// its slice (fixed order, deterministic):
+// Carried memory in operand form.  One thread per element of the operand-form
+// block (d_v rows of KT components, then Z; KT = K padded to whole groups of 128,
+// padding components written as zeros), serial over the chunks of its slice
+// (fixed order, deterministic):
 //   memory block c (exclusive prefix)  <- state_in + sum_{c' < c} L_c'
 //   total (inclusive, bidirectional)   <- the sum over all chunks
 //   state_out (caller layout)          <- state_in + the sum over all chunks
-// A memory block in operand form holds the hi plane [d_v][K] (bf16), the lo
-// plane (split form only), then Z as a hi row and a lo row [K] (bf16), within
-// the bytes of an fp32 block.  state_in / state_out keep the caller layout (Vt as K rows of d_v,
-// then Z).
-__global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const float *__restrict__ partial,
+// The chunk contributions L are fp32 blocks of K d_v + K words (Vt^T as d_v rows of
+// K, then Z).  A memory block in operand form holds the hi plane [d_v][KT] (bf16),
+// the lo plane (split form only), then Z as a hi row and a lo row [KT] (bf16),
+// within (d_v + 1) KT fp32 words.  state_in / state_out keep the caller layout (Vt
+// as K rows of d_v, then Z).
+__global__ void __launch_bounds__(256) k_scan_split(int DV, int K, int KT, int nblk, const float *__restrict__ partial,
                                                     const float *__restrict__ state_in, unsigned char *__restrict__ mem,
                                                     unsigned char *__restrict__ total, float *__restrict__ state_out,
                                                     bool lo_plane)
 {
-    const long long SZ = (long long)kK * DV + kK, VK = (long long)kK * DV;
-    const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
-    if (e >= SZ) return;
+    const int MW = (DV + 1) * KT;                        // operand-form block (fp32 words)
+    const int e = blockIdx.x * 256 + threadIdx.x;
+    if (e >= MW) return;
     const long long bh = blockIdx.y;
-    const long long eu = e < VK ? (e % kK) * DV + e / kK : e;   // the same element in the caller layout
-    float run = state_in ? state_in[bh * SZ + eu] : 0.f;
+    const long long SZ = (long long)K * DV + K;
+    const int VT = KT * DV;
+    const bool zrow = e >= VT;
+    const int c = zrow ? DV : e / KT, k = zrow ? e - VT : e - c * KT;
+    const bool pad = k >= K;
+    const long long ep = zrow ? (long long)K * DV + k : (long long)c * K + k;   // element in the L blocks
+    const long long eu = zrow ? ep : (long long)k * DV + c;                     // element in the caller layout
     auto put = [&](unsigned char *blk, float x) {
         __nv_bfloat16 hi, lo;
         split_bf16(x, hi, lo);
-        if (e < VK) {
-            reinterpret_cast<__nv_bfloat16 *>(blk)[e] = hi;
-            if (lo_plane) reinterpret_cast<__nv_bfloat16 *>(blk)[VK + e] = lo;
+        __nv_bfloat16 *b16 = reinterpret_cast<__nv_bfloat16 *>(blk);
+        if (!zrow) {
+            b16[e] = hi;
+            if (lo_plane) b16[VT + e] = lo;
         } else {   // Z: a hi row and a lo row after both planes
-            reinterpret_cast<__nv_bfloat16 *>(blk)[VK + e] = hi;
-            reinterpret_cast<__nv_bfloat16 *>(blk)[VK + kK + e] = lo;
+            b16[2 * VT + k] = hi;
+            b16[2 * VT + KT + k] = lo;
         }
     };
-    const float *__restrict__ p = partial + bh * nblk * SZ + e;
+    if (pad) {   // padding components: zeros in every block
+        for (int b = 0; b < nblk; ++b)
+            if (mem) put(mem + (bh * nblk + b) * MW * 4LL, 0.f);
+        if (total) put(total + bh * MW * 4LL, 0.f);
+        return;
+    }
+    float run = state_in ? state_in[bh * SZ + eu] : 0.f;
+    const float *__restrict__ p = partial + bh * nblk * SZ + ep;
     constexpr int U = 32;   // loads in flight per thread
     int b = 0;
     for (; b + U <= nblk; b += U) {
@@ -375,16 +404,16 @@ __global__ void __launch_bounds__(256) k_scan_split(int DV, int nblk, const floa
         for (int u = 0; u < U; ++u) t[u] = p[(long long)(b + u) * SZ];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (mem) put(mem + (bh * nblk + b + u) * SZ * 4, run);
+            if (mem) put(mem + (bh * nblk + b + u) * MW * 4LL, run);
             run += t[u];
         }
     }
     for (; b < nblk; ++b) {
         const float t = p[(long long)b * SZ];
-        if (mem) put(mem + (bh * nblk + b) * SZ * 4, run);
+        if (mem) put(mem + (bh * nblk + b) * MW * 4LL, run);
         run += t;
     }
-    if (total) put(total + bh * SZ * 4, run);
+    if (total) put(total + bh * MW * 4LL, run);
     if (state_out) state_out[bh * SZ + eu] = run;
 }
 
@@ -441,7 +470,7 @@ struct OutMaps {
 // total memory of the sequence (the same block for every chunk), no P.
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
-    k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, float eps,
+    k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, int KH, float eps,
                    const void *__restrict__ v, bool v_bf16, float *__restrict__ out, unsigned int *timeout)
 {
     using Sm = OutSmem<SPLIT, DV>;
@@ -451,7 +480,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     constexpr int VPER = kC * F4 / kOutThreads;             // groups of V per thread
     constexpr int NBV = NP * DV / 64;                       // 64-column blocks of the V images
     constexpr uint32_t AS = Sm::ATOM, PART = Sm::PART;
-    constexpr int SROWS = 2 * DV + 2;                       // 256-byte rows of a memory block
+    constexpr int SROWS = 2 * DV + 2;                       // rows of a memory block (KH groups of 128)
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *const tb0 = sm, *const tb1 = sm + Sm::BIMG;                     // B images (hi, lo)
@@ -480,22 +509,23 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 
     // block of the carried memory read by item it
     auto mem_block = [&](long long it) -> long long { return CAUSAL ? it : it / nblk; };
-    auto load_gamma = [&](long long it) {   // one thread
-        const int row0 = (int)((it / nblk) * N + (it % nblk) * kC);
+    // one thread: component group g (components 128 g .. + 127) of item it
+    auto load_gamma = [&](long long it, int g) {
+        const int row0 = (int)((it / nblk) * N + (it % nblk) * kC), x0 = kK * g;
         mbar_expect_tx(BAR_G, (uint32_t)((CAUSAL ? 2 : 1) * NP * kC * kRowB));
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a) {
-                if (CAUSAL) tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS), &maps.gk[pl], a * 64, row0, BAR_G);
-                tma_load_2d(smem_addr((pl ? ta1 : ta0) + a * kAtom), &maps.gq[pl], a * 64, row0, BAR_G);
+                if (CAUSAL) tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS), &maps.gk[pl], x0 + a * 64, row0, BAR_G);
+                tma_load_2d(smem_addr((pl ? ta1 : ta0) + a * kAtom), &maps.gq[pl], x0 + a * 64, row0, BAR_G);
             }
     };
-    auto load_memory = [&](long long it) {   // one thread
-        const int srow = (int)(mem_block(it) * SROWS);
+    auto load_memory = [&](long long it, int g) {
+        const int srow = (int)(mem_block(it) * SROWS), x0 = kK * g;
         mbar_expect_tx(BAR_S, (uint32_t)((NP * DV + 2) * kRowB));
         for (int a = 0; a < 2; ++a) {
             for (int pl = 0; pl < NP; ++pl)
-                tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS + PART), &maps.s, a * 64, srow + pl * DV, BAR_S);
-            tma_load_2d(smem_addr(ZF ? tb0 + a * AS + PART + DV * 128 : bz + a * Sm::ZATOM), &maps.z, a * 64,
+                tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS + PART), &maps.s, x0 + a * 64, srow + pl * DV, BAR_S);
+            tma_load_2d(smem_addr(ZF ? tb0 + a * AS + PART + DV * 128 : bz + a * Sm::ZATOM), &maps.z, x0 + a * 64,
                         srow + 2 * DV, BAR_S);   // Z_hi, Z_lo
         }
     };
@@ -511,8 +541,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
-            load_gamma(it0);
-            load_memory(it0);
+            load_gamma(it0, 0);
+            load_memory(it0, 0);
             pend_g = pend_s = true;
         }
     }
@@ -531,9 +561,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const uint32_t tbase = *tslot;
     bool ok = true;
     const float qnan = __int_as_float(0x7fc00000);
+    uint32_t un = 0;   // component groups consumed (phases of the group barriers G, S, M)
 
     for (long long it = it0; it < it1 && ok; ++it) {
-        const uint32_t ph = (uint32_t)((it - it0) & 1);
+        const uint32_t ph = (uint32_t)((it - it0) & 1);   // phase of the item barriers V, O
         const long long bh = it / nblk;
         const int c0 = (int)(it % nblk) * kC;
         const int nr = min(kC, N - c0);
@@ -558,37 +589,43 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 }
             }
         }
-        const bool ok_g = mbar_wait(BAR_G, ph), ok_s = mbar_wait(BAR_S, ph);
-        ok = ok && ok_g && ok_s;
-        if (tid == 0) {   // a load whose wait gave up is still in flight
-            pend_g = pend_g && !ok_g;
-            pend_s = pend_s && !ok_s;
-            // [P | U] = Gq [Gk ; Vt^T]^T  (bidirectional read: U = Gq Vt)
-            const uint32_t b0 = CAUSAL ? 0u : PART;
-            const uint32_t d0 = CAUSAL ? D_P : D_U, nb = (CAUSAL ? kC + DV : DV) + (ZF ? 16 : 0);
-            mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, false);
-            if constexpr (SPLIT) {
-                mma_pass_ss(tbase + d0, ta0, kAtom, tb1 + b0, nb, AS, true);
-                mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
+        // [P | U | Gq Z] = Gq [Gk ; Vt^T ; Z]^T (bidirectional read: [U | Gq Z]), the contraction
+        // over the components taken one group of 128 at a time into the same accumulator
+        for (int g = 0; g < KH; ++g, ++un) {
+            const uint32_t pu = un & 1u;   // phase of the per-group barriers
+            const bool ok_g = mbar_wait(BAR_G, pu), ok_s = mbar_wait(BAR_S, pu);
+            ok = ok && ok_g && ok_s;
+            if (tid == 0) {   // a load whose wait gave up is still in flight
+                pend_g = pend_g && !ok_g;
+                pend_s = pend_s && !ok_s;
+                const uint32_t b0 = CAUSAL ? 0u : PART;
+                const uint32_t d0 = CAUSAL ? D_P : D_U, nb = (CAUSAL ? kC + DV : DV) + (ZF ? 16 : 0);
+                mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, g > 0);
+                if constexpr (SPLIT) {
+                    mma_pass_ss(tbase + d0, ta0, kAtom, tb1 + b0, nb, AS, true);
+                    mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
+                }
+                if constexpr (!ZF)   // Gq [Z_hi | Z_lo] on its own
+                    mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, g > 0);
+                mma_commit(BAR_M);
+                if (CAUSAL && g == 0) {   // the previous output tile has left the staging tile, which takes V next
+                    bulk_wait_read();
+                    mbar_arrive(BAR_O);
+                }
             }
-            if constexpr (!ZF)   // Gq [Z_hi | Z_lo] on its own
-                mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, false);
-            mma_commit(BAR_M);
-            if (CAUSAL) {   // the previous output tile has left the staging tile, which takes V next
-                bulk_wait_read();
-                mbar_arrive(BAR_O);
+            __syncwarp();
+            ok = mbar_wait(BAR_M, pu) && ok;
+            fence_after_sync();
+            if (tid == 0 && ok && (g + 1 < KH || more)) {
+                // the MMA has read B, the A images and the Z rows (no thread reads them): the next
+                // group's (or the next item's first group's) tiles and memory may land in them
+                const long long in = g + 1 < KH ? it : it + 1;
+                const int gn = g + 1 < KH ? g + 1 : 0;
+                load_gamma(in, gn);
+                load_memory(in, gn);
+                pend_g = pend_s = true;
+                ph_g = ph_s = pu ^ 1u;
             }
-        }
-        __syncwarp();
-        ok = mbar_wait(BAR_M, ph) && ok;
-        fence_after_sync();
-        if (tid == 0 && more && ok) {
-            // the MMA has read B, the A images and the Z rows (no thread reads them): the next
-            // item's tiles and memory may land in them
-            load_gamma(it + 1);
-            load_memory(it + 1);
-            pend_g = pend_s = true;
-            ph_g = ph_s = ph ^ 1u;
         }
         if constexpr (CAUSAL) {
             // V into token-major images in the staging tile, the B operand (MN-major) of
@@ -752,7 +789,10 @@ cudaError_t launch_expire_wait(long long limit_cycles, cudaStream_t st)
     return cudaGetLastError();
 }
 
-bool tc_path_eligible(int K, int DV, bool g_bf16) { return K == kK && (DV == 64 || (DV == 128 && g_bf16)); }
+bool tc_path_eligible(int K, int DV, bool g_bf16)
+{
+    return (K <= kK || (K % kK == 0 && K <= 4 * kK)) && (DV == 64 || (DV == 128 && g_bf16));
+}
 
 bool tc_path_applies(const Dims &dm) { return dm.C == kC && tc_path_eligible(dm.K, dm.DV, dm.g_bf16); }
 
@@ -766,16 +806,17 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
     StateMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
     const uint16_t *k16 = static_cast<const uint16_t *>(gk);
+    const int KT = tc_kpad(dm.K), KH = KT / kK;   // component groups of 128
     for (int pl = 0; pl < (SPLIT ? 2 : 1); ++pl)
-        if (!make_tma_3d(&maps.gk[pl], k16 + pl * (long long)rows * kK, true, kK, dm.N, dm.BH(), kC))
+        if (!make_tma_3d(&maps.gk[pl], k16 + pl * (long long)rows * KT, true, KT, dm.N, dm.BH(), kC))
             return cudaErrorInvalidValue;
     if (!SPLIT) maps.gk[1] = maps.gk[0];
-    const long long items = dm.BH() * (long long)dm.nblk();
+    const long long items = dm.BH() * (long long)dm.nblk() * KH;   // (chunk, component group)
     const int grid = (int)(items < sm_count() ? items : sm_count());
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
-    k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, v, dm.v_bf16,
-                                                                   partial, flag);
+    k_chunk_state_tc<SPLIT, DV><<<grid, kStateThreads, smem, st>>>(maps, dm.N, dm.nblk(), items, dm.K, KH, v,
+                                                                   dm.v_bf16, partial, flag);
     return cudaGetLastError();
 }
 
@@ -789,20 +830,21 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     if (attr != cudaSuccess) return attr;
     OutMaps maps;
     const unsigned long long rows = (unsigned long long)dm.BH() * dm.N;
-    const long long plane = (long long)rows * kK;
+    const int KT = tc_kpad(dm.K), KH = KT / kK;   // component groups of 128
+    const long long plane = (long long)rows * KT;
     const unsigned long long blocks = (unsigned long long)dm.BH() * (CAUSAL ? dm.nblk() : 1);
     const uint16_t *q16 = static_cast<const uint16_t *>(gq), *k16 = static_cast<const uint16_t *>(gk);
     bool ok = true;
     for (int pl = 0; pl < (SPLIT ? 2 : 1); ++pl)
-        ok = ok && make_tma_2d(&maps.gq[pl], q16 + pl * plane, true, rows, kK, kC) &&
-             make_tma_2d(&maps.gk[pl], k16 + pl * plane, true, rows, kK, kC);
+        ok = ok && make_tma_2d(&maps.gq[pl], q16 + pl * plane, true, rows, KT, kC) &&
+             make_tma_2d(&maps.gk[pl], k16 + pl * plane, true, rows, KT, kC);
     if (!SPLIT) {
         maps.gq[1] = maps.gq[0];
         maps.gk[1] = maps.gk[0];
     }
-    // memory blocks in operand form: rows of 256 bytes (hi plane, lo plane, Z), d_v rows per box
-    ok = ok && make_tma_2d(&maps.s, mem, true, blocks * (2 * DV + 2), kK, DV) &&
-         make_tma_2d(&maps.z, mem, true, blocks * (2 * DV + 2), kK, 2) &&
+    // memory blocks in operand form: rows of KT bf16 (hi plane, lo plane, Z), d_v rows per box
+    ok = ok && make_tma_2d(&maps.s, mem, true, blocks * (2 * DV + 2), KT, DV) &&
+         make_tma_2d(&maps.z, mem, true, blocks * (2 * DV + 2), KT, 2) &&
          make_tma_3d(&maps.o, out, false, DV, dm.N, dm.BH(), 64);
     if (!ok) return cudaErrorInvalidValue;
     const long long items = dm.BH() * (long long)dm.nblk();
@@ -810,7 +852,7 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, dm.eps, v, dm.v_bf16, out, flag);
+        maps, dm.N, dm.nblk(), items, KH, dm.eps, v, dm.v_bf16, out, flag);
     return cudaGetLastError();
 }
 
@@ -828,9 +870,10 @@ cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v,
 cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float *state_in, unsigned char *mem,
                               unsigned char *total, float *state_out, cudaStream_t st)
 {
-    const long long SZ = (long long)kK * dm.DV + kK;
-    dim3 grid((unsigned)((SZ + 255) / 256), (unsigned)dm.BH());
-    k_scan_split<<<grid, 256, 0, st>>>(dm.DV, dm.nblk(), partial, state_in, mem, total, state_out, !dm.g_bf16);
+    const long long MW = tc_mem_words(dm);
+    dim3 grid((unsigned)((MW + 255) / 256), (unsigned)dm.BH());
+    k_scan_split<<<grid, 256, 0, st>>>(dm.DV, dm.K, tc_kpad(dm.K), dm.nblk(), partial, state_in, mem, total,
+                                       state_out, !dm.g_bf16);
     return cudaGetLastError();
 }
 

@@ -27,6 +27,8 @@ constexpr int kBlockRows = 256;   // rows per block of the block-state / causal-
 
 struct Dims {
     int B, H, N, D, DV, K, KP, C;
+    int KG;    // row length of the responsibilities in the workspace: KP, or on the tensor-core
+               // path the components padded to whole groups of 128 (tc_kpad)
     int blk;   // rows per block of the memory scan (kBlockRows, or C on the tensor-core path)
     float eps;
     bool x_bf16, v_bf16, g_bf16;
@@ -161,9 +163,16 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
 cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
                               const PrunedImages &img, int layout, cudaStream_t st);
 
-// Tensor-core path of the causal form (K = 128, chunk 128; see gma_causal_tc.cu).
+// Tensor-core path of the causal and bidirectional forms (chunk 128; see gma_causal_tc.cu):
+// K <= 128 (zero-padded to 128) or a multiple of 128 up to 512, d_v = 64, or d_v = 128 with
+// bf16 products.
 bool tc_path_eligible(int K, int DV, bool g_bf16);
 bool tc_path_applies(const Dims &dm);
+// Components of the tensor-core path's operands: K padded to 128 below 128, else K.
+inline int tc_kpad(int K) { return K < 128 ? 128 : K; }
+// fp32 words of one block of the carried memory in operand form (hi and lo planes of
+// d_v rows of tc_kpad(K), then the Z rows).
+inline long long tc_mem_words(const Dims &dm) { return (long long)(dm.DV + 1) * tc_kpad(dm.K); }
 // Tensor-core path: gq / gk in GL_SPLIT (fp32 products) or GL_BF16 form; the
 // carried memory in operand form (k_scan_split), one block per chunk (causal)
 // or per slice (bidirectional total).

@@ -97,9 +97,9 @@ typedef struct {
     int d_v;            /* width of the value rows and of the output */
     int K;              /* number of Gaussian components per head */
     int chunk;          /* causal chunk length C in {16, 32, 64, 128}; 0 selects
-                           128 where the tensor-core path applies (K = 128 and
-                           d_v = 64, or d_v = 128 with bf16 products), else 64;
-                           128 is accepted only there */
+                           128 where the tensor-core path applies (K <= 128 or
+                           K in {256, 384, 512}, and d_v = 64, or d_v = 128 with
+                           bf16 products), else 64; 128 is accepted only there */
     float eps;          /* read-phase stabiliser, added to Gamma_Q Z (>= 0) */
     gma_dtype x_dtype;  /* storage type of Q_X and K_X */
     gma_dtype v_dtype;  /* storage type of V */

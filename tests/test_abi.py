@@ -75,7 +75,7 @@ def _call_causal(lib, shape, ptrs=None, ws_bytes=1 << 40):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(d_route=48), 2), (dict(d_v=8), 2), (dict(K=600), 2), (dict(chunk=48), 2),
-    (dict(K=64, chunk=128), 2), (dict(d_v=128, chunk=128), 2),
+    (dict(K=200, chunk=128), 2), (dict(K=640, chunk=128), 2), (dict(d_v=128, chunk=128), 2),
     (dict(B=0), 1), (dict(N=-1), 1), (dict(K=0), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
     (dict(B=300, H=300), 2),
 ])

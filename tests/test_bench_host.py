@@ -15,7 +15,9 @@ W = workloads.WORKLOADS
 
 def test_chunk_length_per_workload():
     assert bench.eff_chunk(W["causal_16k_peaked"]) == 128                 # K = 128, d_v = 64: tensor cores
-    assert bench.eff_chunk(W["causal_8k_K64"]) == 64                      # other K: CUDA cores, C = 64
+    assert bench.eff_chunk(W["causal_8k_K64"]) == 128                     # K < 128: padded to 128
+    assert bench.eff_chunk(W["causal_8k_K512"]) == 128                    # whole groups of 128
+    assert bench.eff_chunk(W["causal_8k_K64"].with_(K=200)) == 64         # other K: CUDA cores, C = 64
     assert bench.eff_chunk(W["causal_64k_bf16"]) == 128                   # d_v = 128 with bf16 products
     assert bench.eff_chunk(W["causal_16k_peaked"].with_(dv=128)) == 64    # d_v = 128, fp32 products
     assert bench.eff_chunk(W["causal_16k_peaked"].with_(chunk=32)) == 32  # a caller's choice wins
@@ -42,8 +44,8 @@ def test_headline_bytes_per_launch():
     # the bidirectional total: every chunk's partial in, one block per (b, h) out
     assert bench.stage_work("state_reduce", W["bidir_16k_peaked"])[2] == (chunks + 2 * 16) * state
     # the CUDA-core path scans blocks of 256 rows
-    g = W["causal_8k_K64"]
-    assert bench.stage_work("state_scan", g)[2] == 2 * (4 * 8 * (8192 // 256)) * 64 * 65 * 4
+    g = W["causal_8k_K64"].with_(K=200)
+    assert bench.stage_work("state_scan", g)[2] == 2 * (4 * 8 * (8192 // 256)) * 200 * 65 * 4
 
 
 def test_algorithmic_bytes_follow_the_method_io():

@@ -35,6 +35,9 @@ CROSS = [
     (W["tiny"].with_(mode="bidir", B=2, H=2, d=64, dv=64, K=128), 1, 77),
     (W["tiny"].with_(mode="bidir", B=2, H=2, d=16, dv=16, K=8), 50, 0),           # empty memory
     (W["tiny"].with_(mode="bidir", B=2, H=2, d=64, dv=64, K=128), 50, 0),
+    (W["tiny"].with_(mode="bidir", B=2, H=2, d=64, dv=64, K=256), 700, 300),  # component groups
+    (W["tiny"].with_(mode="bidir", B=2, H=2, d=32, dv=64, K=48), 300, 900),   # padded components
+    (W["tiny"].with_(mode="bidir", B=2, H=2, d=64, dv=64, K=256), 50, 0),
 ]
 
 

@@ -90,6 +90,10 @@ def test_responsibilities_adversarial_rows():
     (W["tiny"].with_(mode="bidir", B=4, H=16, N=1100, d=64, dv=64, K=128), None),
     (W["tiny"].with_(mode="bidir", B=8, H=25, N=200, d=64, dv=64, K=128), None),
     (W["causal_4k"].with_(mode="bidir", gemm_dtype="bf16"), 2),
+    # tensor-core path with component groups
+    (W["tiny"].with_(mode="bidir", B=2, H=2, N=1000, d=64, dv=64, K=256), None),
+    (W["tiny"].with_(mode="bidir", B=2, H=2, N=900, d=64, dv=64, K=40), None),
+    (W["causal_8k_K512"].with_(mode="bidir"), 2),
 ])
 def test_bidir(wl, sample):
     c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
@@ -128,6 +132,15 @@ CAUSAL = [
     (W["causal_8k_K64"], 2, 0),
     (W["causal_8k_K256"], 2, 0),
     (W["causal_8k_K512"], 2, 0),
+    # tensor-core path with component groups: K < 128 padded, K = 256 / 384, bf16 and split operands,
+    # ragged chunks, more chunks than SMs; K = 200 stays on CUDA cores
+    (W["tiny"].with_(B=2, H=2, N=1000, d=64, dv=64, K=100), None, 0),
+    (W["tiny"].with_(B=2, H=2, N=700, d=32, dv=64, K=8), None, 0),
+    (W["tiny"].with_(B=2, H=2, N=1000, d=64, dv=64, K=256), None, 0),
+    (W["tiny"].with_(B=1, H=3, N=1300, d=16, dv=64, K=384), None, 0),
+    (W["tiny"].with_(B=1, H=2, N=700, d=32, dv=128, K=256, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
+    (W["tiny"].with_(B=4, H=16, N=1100, d=64, dv=64, K=512), None, 0),
+    (W["tiny"].with_(B=1, H=2, N=600, d=64, dv=64, K=200), None, 0),
 ]
 
 
@@ -141,7 +154,7 @@ def test_causal(wl, sample, chunk):
     _report(f"causal state {wl.name}", normwise(c.pick(st), ref_st), tol)
 
 
-@pytest.mark.parametrize("K", [32, 128])
+@pytest.mark.parametrize("K", [32, 128, 256])
 def test_causal_state_carry(K):
     """Two calls chained through state_out -> state_in equal one call on the whole sequence."""
     wl = W["tiny"].with_(B=2, H=2, N=600, K=K, d=64, dv=64)
@@ -191,7 +204,7 @@ def test_causal_prefix_property_bitwise(K):
     c.dev["seq"] = (q, k, v)
 
 
-@pytest.mark.parametrize("K,chunks", [(64, (16, 32, 64)), (128, (16, 64, 128))])
+@pytest.mark.parametrize("K,chunks", [(64, (16, 32, 64, 128)), (128, (16, 64, 128)), (256, (64, 128))])
 def test_chunk_size_invariance(K, chunks):
     """The chunkwise form is exact: chunk lengths (and the tensor-core path at
     chunk 128 against the CUDA-core path at 16/64) agree to rounding."""
