@@ -488,8 +488,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     unsigned char *const os = sm + NP * (Sm::BIMG + Sm::AIMG);                     // output tile
     unsigned char *const bz = os + Sm::OUT;                                        // B operand of Gq Z (!ZF)
     float *part = reinterpret_cast<float *>(bz + Sm::BZ);           // [4][128]: row-sum quarters of P_m
-    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [5]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(part + 4 * kK);    // [6]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 2;                    // column quarter
@@ -504,8 +504,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     constexpr uint32_t A_PM_HI = 0, A_PM_LO = 64, D_P = 128, D_U = D_P + kC, D_PV = D_U + DV + (ZF ? 64 : 0);
     constexpr uint32_t D_Z = ZF ? D_U + DV : A_PM_LO;
     static_assert(D_PV + NBV * 64 <= 512 && (ZF || !SPLIT), "TMEM columns");
+    // G, S: loads of a group's tiles and memory; M: a chain that is not an item's last; L: an
+    // item's last chain; V: P_m V; O: the output staging tile is free
     const uint32_t BAR_G = smem_addr(bar), BAR_S = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2),
-                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4);
+                   BAR_V = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4), BAR_L = smem_addr(bar + 5);
 
     // block of the carried memory read by item it
     auto mem_block = [&](long long it) -> long long { return CAUSAL ? it : it / nblk; };
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     bool pend_g = false, pend_s = false;
     uint32_t ph_g = 0, ph_s = 0;
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 6; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
             load_gamma(it0, 0);
@@ -561,10 +563,11 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const uint32_t tbase = *tslot;
     bool ok = true;
     const float qnan = __int_as_float(0x7fc00000);
-    uint32_t un = 0;   // component groups consumed (phases of the group barriers G, S, M)
+    uint32_t un = 0;   // component groups consumed (phases of the load barriers G, S)
+    uint32_t um = 0;   // chains completed on M (thread 0)
 
     for (long long it = it0; it < it1 && ok; ++it) {
-        const uint32_t ph = (uint32_t)((it - it0) & 1);   // phase of the item barriers V, O
+        const uint32_t ph = (uint32_t)((it - it0) & 1);   // phase of the item barriers L, V, O
         const long long bh = it / nblk;
         const int c0 = (int)(it % nblk) * kC;
         const int nr = min(kC, N - c0);
@@ -591,36 +594,50 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         }
         // [P | U | Gq Z] = Gq [Gk ; Vt^T ; Z]^T (bidirectional read: [U | Gq Z]), the contraction
         // over the components taken one group of 128 at a time into the same accumulator
-        for (int g = 0; g < KH; ++g, ++un) {
-            const uint32_t pu = un & 1u;   // phase of the per-group barriers
-            const bool ok_g = mbar_wait(BAR_G, pu), ok_s = mbar_wait(BAR_S, pu);
-            ok = ok && ok_g && ok_s;
-            if (tid == 0) {   // a load whose wait gave up is still in flight
+        // Thread 0 alone waits for the loads (G, S) and for the chains before an item's last (M):
+        // it re-arms those barriers for the next group or item as soon as a chain is done, with
+        // no CTA barrier in between, so another thread waiting on them could find a barrier two
+        // phases on (and wait for a phase that has passed) or start a phase early (and take the
+        // phase before for it).  An item's last chain completes on L, one phase per item, waited
+        // by every thread and committed again only after the item's closing barrier.
+        for (int gr = 0; gr < KH; ++gr, ++un) {
+            const uint32_t pu = un & 1u;   // phase of the per-group load barriers
+            const bool last = gr + 1 == KH;
+            if (tid == 0) {
+                const bool ok_g = mbar_wait(BAR_G, pu), ok_s = mbar_wait(BAR_S, pu);
+                ok = ok && ok_g && ok_s;
+                // a load whose wait gave up is still in flight
                 pend_g = pend_g && !ok_g;
                 pend_s = pend_s && !ok_s;
                 const uint32_t b0 = CAUSAL ? 0u : PART;
                 const uint32_t d0 = CAUSAL ? D_P : D_U, nb = (CAUSAL ? kC + DV : DV) + (ZF ? 16 : 0);
-                mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, g > 0);
+                mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, gr > 0);
                 if constexpr (SPLIT) {
                     mma_pass_ss(tbase + d0, ta0, kAtom, tb1 + b0, nb, AS, true);
                     mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
                 }
                 if constexpr (!ZF)   // Gq [Z_hi | Z_lo] on its own
-                    mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, g > 0);
-                mma_commit(BAR_M);
-                if (CAUSAL && g == 0) {   // the previous output tile has left the staging tile, which takes V next
+                    mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, gr > 0);
+                mma_commit(last ? BAR_L : BAR_M);
+                if (CAUSAL && gr == 0) {   // the previous output tile has left the staging tile, which takes V next
                     bulk_wait_read();
                     mbar_arrive(BAR_O);
                 }
             }
             __syncwarp();
-            ok = mbar_wait(BAR_M, pu) && ok;
-            fence_after_sync();
-            if (tid == 0 && ok && (g + 1 < KH || more)) {
+            if (last) {
+                ok = mbar_wait(BAR_L, ph) && ok;
+                fence_after_sync();
+            } else if (tid == 0) {
+                ok = mbar_wait(BAR_M, um & 1u) && ok;
+                ++um;
+                fence_after_sync();
+            }
+            if (tid == 0 && ok && (gr + 1 < KH || more)) {
                 // the MMA has read B, the A images and the Z rows (no thread reads them): the next
                 // group's (or the next item's first group's) tiles and memory may land in them
-                const long long in = g + 1 < KH ? it : it + 1;
-                const int gn = g + 1 < KH ? g + 1 : 0;
+                const long long in = gr + 1 < KH ? it : it + 1;
+                const int gn = gr + 1 < KH ? gr + 1 : 0;
                 load_gamma(in, gn);
                 load_memory(in, gn);
                 pend_g = pend_s = true;

@@ -35,9 +35,10 @@
  *     that run concurrently must use different workspaces.
  *   - Bounded waits.  The tensor-core kernels wait on mbarriers (for TMA
  *     copies and tensor-core products) with a limit of about 2 s of SM
- *     cycles.  If a wait expires, the kernel writes NaN for the rows it owns,
- *     stops issuing work, waits (again bounded) for what it has already
- *     issued, and returns; it also sets the device's timeout flag.  The next
+ *     cycles.  If a wait expires, the kernel stops issuing work, waits (again
+ *     bounded) for what it has already issued, and returns, leaving the
+ *     call's outputs undefined (NaN where the waiting threads owned the rows);
+ *     it also sets the device's timeout flag.  The next
  *     compute call on that device that sees the flag returns GMA_ERR_TIMEOUT
  *     (launching nothing) and clears it; gma_sync_status(stream) waits for
  *     the stream and reports it deterministically.  An expired wait means the

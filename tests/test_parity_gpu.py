@@ -31,6 +31,10 @@ def _report(name, err, tol):
     (W["tiny"].with_(K=1, B=2, H=2), None),
     (W["tiny"].with_(K=3, d=32, N=77), None),
     (W["tiny"].with_(K=200, d=128, N=300, H=2), None),
+    # generic routing: odd K above 256 (64-row tiles, parameters in chunks), bf16 rows, d = 16
+    (W["tiny"].with_(K=257, d=64, N=513, H=3, x_dtype="bf16"), None),
+    (W["tiny"].with_(K=48, d=16, N=1000, B=2), None),
+    (W["tiny"].with_(K=512, d=128, N=200, H=2), None),
     (W["causal_4k"], 4),
     (W["bidir_16k_peaked"], 3),
     # more chunks than SMs, ragged last chunk: persistent CTAs cross slice boundaries
