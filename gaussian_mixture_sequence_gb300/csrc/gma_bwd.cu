@@ -67,8 +67,9 @@ __device__ __forceinline__ void stage_rows(float *dst, int LG, const float *src,
 template <int DV>
 struct BwdQSmem {
     static constexpr int UW = BwdCfg<DV>::UW, LG = BwdCfg<DV>::LG, LP = BwdCfg<DV>::LP;
-    static constexpr size_t floats = (size_t)kBC * LG * 2 + (size_t)kBC * DV * 2 + (size_t)kBC * LP +
-                                     (size_t)kBKC * DV + kBKC + (size_t)kBC * UW + kBC + (size_t)kBC * 16 + kThreads;
+    static constexpr int VP = DV + 1;   // row pitch of the V rows and the memory rows (odd: no bank conflicts)
+    static constexpr size_t floats = (size_t)kBC * LG * 2 + (size_t)kBC * VP + (size_t)kBC * DV + (size_t)kBC * LP +
+                                     (size_t)kBKC * VP + kBKC + (size_t)kBC * UW + kBC + (size_t)kBC * 16 + kThreads;
     static constexpr size_t bytes = floats * 4;
 };
 
@@ -79,16 +80,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long st_bh_stride, long long st_blk_stride, float *__restrict__ u, float *__restrict__ dgq)
 {
     using Cfg = BwdCfg<DV>;
-    constexpr int C = kBC, KC = kBKC, UW = Cfg::UW, LG = Cfg::LG, LP = Cfg::LP;
+    constexpr int C = kBC, KC = kBKC, UW = Cfg::UW, LG = Cfg::LG, LP = Cfg::LP, VP = BwdQSmem<DV>::VP;
     constexpr int TM = C / 16, TN = DV / 16, TP = C / 16, TK = KC / 16, PARTS = kThreads / C;
     extern __shared__ __align__(16) float sm[];
     float *gq_s = sm;                  // [C][LG]
     float *gk_s = gq_s + C * LG;       // [C][LG]
-    float *v_s = gk_s + C * LG;        // [C][DV]
-    float *g_s = v_s + C * DV;         // [C][DV]  dL/dO rows
+    float *v_s = gk_s + C * LG;        // [C][VP]
+    float *g_s = v_s + C * VP;         // [C][DV]  dL/dO rows
     float *p_s = g_s + C * DV;         // [C][LP]
-    float *s_s = p_s + C * LP;         // [KC][DV]
-    float *z_s = s_s + KC * DV;        // [KC]
+    float *s_s = p_s + C * LP;         // [KC][VP]
+    float *z_s = s_s + KC * VP;        // [KC]
     float *u_s = z_s + KC;             // [C][UW]
     float *den_s = u_s + C * UW;       // [C]
     float *dot_s = den_s + C;          // [C][16]
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_s = [&](int k0) {
         for (int i = tid; i < KC * DV; i += kThreads) {
             const int k = i / DV, c = i % DV;
-            s_s[i] = (k0 + k < K) ? st[(long long)(k0 + k) * DV + c] : 0.f;
+            s_s[k * VP + c] = (k0 + k < K) ? st[(long long)(k0 + k) * DV + c] : 0.f;
         }
         for (int i = tid; i < KC; i += kThreads) z_s[i] = (k0 + i < K) ? st[(long long)K * DV + k0 + i] : 0.f;
     };
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vv = load4(v, (row0 + r) * DV + c, v_bf16);
                 gg = *reinterpret_cast<const float4 *>(dout + (row0 + r) * DV + c);
             }
-            *reinterpret_cast<float4 *>(v_s + r * DV + c) = vv;
+            float *vd = v_s + r * VP + c;
+            vd[0] = vv.x; vd[1] = vv.y; vd[2] = vv.z; vd[3] = vv.w;
             *reinterpret_cast<float4 *>(g_s + r * DV + c) = gg;
         }
         // the forward read: numerator (acc), P, Gq . Z
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = gq_s[(tm * TM + i) * LG + kk];
 #pragma unroll
-                for (int j = 0; j < TN; ++j) b[j] = s_s[kk * DV + tn * TN + j];
+                for (int j = 0; j < TN; ++j) b[j] = s_s[kk * VP + tn * TN + j];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = p_s[(tm * TM + i) * LP + jj];
 #pragma unroll
-                for (int j = 0; j < TN; ++j) b[j] = v_s[jj * DV + tn * TN + j];
+                for (int j = 0; j < TN; ++j) b[j] = v_s[jj * VP + tn * TN + j];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TP; ++i) a[i] = u_s[(tm * TP + i) * UW + c];
 #pragma unroll
-                for (int j = 0; j < TP; ++j) b[j] = v_s[(tn * TP + j) * DV + c];
+                for (int j = 0; j < TP; ++j) b[j] = v_s[(tn * TP + j) * VP + c];
 #pragma unroll
                 for (int i = 0; i < TP; ++i)
 #pragma unroll
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = u_s[(tm * TM + i) * UW + c];
 #pragma unroll
-                for (int j = 0; j < TK; ++j) b[j] = s_s[(tn * TK + j) * DV + c];
+                for (int j = 0; j < TK; ++j) b[j] = s_s[(tn * TK + j) * VP + c];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -313,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TU; ++i)
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) a2[i][j] = s_s[(tm * TU + i) * DV + tn * TN + j];
+                    for (int j = 0; j < TN; ++j) a2[i][j] = s_s[(tm * TU + i) * VP + tn * TN + j];
                 for (int jj = 0; jj < C; ++jj) {
                     float a[TU], b[TN];
 #pragma unroll
                     for (int i = 0; i < TU; ++i) a[i] = gk_s[jj * LG + tm * TU + i];
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) b[j] = v_s[jj * DV + tn * TN + j];
+                    for (int j = 0; j < TN; ++j) b[j] = v_s[jj * VP + tn * TN + j];
 #pragma unroll
                     for (int i = 0; i < TU; ++i)
 #pragma unroll
@@ -427,8 +429,9 @@ __global__ void __launch_bounds__(kThreads) k_scan_rev(long long SZ, int nblk, f
 template <int DV>
 struct BwdKSmem {
     static constexpr int UW = BwdCfg<DV>::UW, LG = BwdCfg<DV>::LG, LP = BwdCfg<DV>::LP;
-    static constexpr size_t floats = (size_t)kBC * LG * 2 + (size_t)kBC * DV + (size_t)kBC * UW + (size_t)kBC * LP * 2 +
-                                     (size_t)kBKC * UW;
+    static constexpr int UP = UW + 1;   // row pitch of the u rows and the memory rows (odd: no bank conflicts)
+    static constexpr size_t floats = (size_t)kBC * LG * 2 + (size_t)kBC * DV + (size_t)kBC * UP + (size_t)kBC * LP * 2 +
+                                     (size_t)kBKC * UP;
     static constexpr size_t bytes = floats * 4;
 };
 
@@ -439,16 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long r_bh_stride, long long r_blk_stride, float *__restrict__ dgk, float *__restrict__ dv)
 {
     using Cfg = BwdCfg<DV>;
-    constexpr int C = kBC, KC = kBKC, UW = Cfg::UW, LG = Cfg::LG, LP = Cfg::LP;
+    constexpr int C = kBC, KC = kBKC, UW = Cfg::UW, LG = Cfg::LG, LP = Cfg::LP, UP = BwdKSmem<DV>::UP;
     constexpr int TM = C / 16, TN = DV / 16, TP = C / 16, TK = KC / 16;
     extern __shared__ __align__(16) float sm[];
     float *gq_s = sm;                  // [C][LG]
     float *gk_s = gq_s + C * LG;       // [C][LG]
     float *v_s = gk_s + C * LG;        // [C][DV]
-    float *u_s = v_s + C * DV;         // [C][UW]
-    float *q_s = u_s + C * UW;         // [C][LP]  Q''_ji = u_i . [v_j | 1], i >= j
+    float *u_s = v_s + C * DV;         // [C][UP]
+    float *q_s = u_s + C * UP;         // [C][LP]  Q''_ji = u_i . [v_j | 1], i >= j
     float *p_s = q_s + C * LP;         // [C][LP]  P_ji = Gk_j . Gq_i, i >= j
-    float *r_s = p_s + C * LP;         // [KC][UW]
+    float *r_s = p_s + C * LP;         // [KC][UP]
 
     const long long bh = blockIdx.y;
     const int blk = blockIdx.x;
@@ -462,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k = i / (UW / 4), c = (i % (UW / 4)) * 4;
             float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
             if (k0 + k < K) val = *reinterpret_cast<const float4 *>(rm + (long long)(k0 + k) * UW + c);
-            *reinterpret_cast<float4 *>(r_s + k * UW + c) = val;
+            float *rd = r_s + k * UP + c;
+            rd[0] = val.x; rd[1] = val.y; rd[2] = val.z; rd[3] = val.w;
         }
     };
 
@@ -481,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = i / (UW / 4), c = (i % (UW / 4)) * 4;
             float4 uu = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < nr) uu = *reinterpret_cast<const float4 *>(u + (row0 + r) * UW + c);
-            *reinterpret_cast<float4 *>(u_s + r * UW + c) = uu;
+            float *ud = u_s + r * UP + c;
+            ud[0] = uu.x; ud[1] = uu.y; ud[2] = uu.z; ud[3] = uu.w;
         }
         __syncthreads();
         if (causal) {   // Q''_ji (rows j, columns i) for i >= j
@@ -489,13 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < TP; ++j)
 #pragma unroll
-                for (int i = 0; i < TP; ++i) qacc[j][i] = u_s[(tn * TP + i) * UW + DV];
+                for (int i = 0; i < TP; ++i) qacc[j][i] = u_s[(tn * TP + i) * UP + DV];
             for (int c = 0; c < DV; ++c) {
                 float a[TP], b[TP];
 #pragma unroll
                 for (int j = 0; j < TP; ++j) a[j] = v_s[(tm * TP + j) * DV + c];
 #pragma unroll
-                for (int i = 0; i < TP; ++i) b[i] = u_s[(tn * TP + i) * UW + c];
+                for (int i = 0; i < TP; ++i) b[i] = u_s[(tn * TP + i) * UP + c];
 #pragma unroll
                 for (int j = 0; j < TP; ++j)
 #pragma unroll
@@ -530,13 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TK; ++j) d2[i][j] = r_s[(tn * TK + j) * UW + DV];
+                for (int j = 0; j < TK; ++j) d2[i][j] = r_s[(tn * TK + j) * UP + DV];
             for (int c = 0; c < DV; ++c) {
                 float a[TM], b[TK];
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = v_s[(tm * TM + i) * DV + c];
 #pragma unroll
-                for (int j = 0; j < TK; ++j) b[j] = r_s[(tn * TK + j) * UW + c];
+                for (int j = 0; j < TK; ++j) b[j] = r_s[(tn * TK + j) * UP + c];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -571,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = gk_s[(tm * TM + i) * LG + kk];
 #pragma unroll
-                for (int j = 0; j < TN; ++j) b[j] = r_s[kk * UW + tn * TN + j];
+                for (int j = 0; j < TN; ++j) b[j] = r_s[kk * UP + tn * TN + j];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -605,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TM; ++i) a[i] = p_s[(tm * TM + i) * LP + ii];
 #pragma unroll
-                for (int j = 0; j < TN; ++j) b[j] = u_s[ii * UW + tn * TN + j];
+                for (int j = 0; j < TN; ++j) b[j] = u_s[ii * UP + tn * TN + j];
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -632,13 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < TU; ++i)
 #pragma unroll
-                    for (int j = 0; j < TW; ++j) a2[i][j] = r_s[(tm * TU + i) * UW + tn * TW + j];
+                    for (int j = 0; j < TW; ++j) a2[i][j] = r_s[(tm * TU + i) * UP + tn * TW + j];
                 for (int ii = 0; ii < C; ++ii) {
                     float a[TU], b[TW];
 #pragma unroll
                     for (int i = 0; i < TU; ++i) a[i] = gq_s[ii * LG + tm * TU + i];
 #pragma unroll
-                    for (int j = 0; j < TW; ++j) b[j] = u_s[ii * UW + tn * TW + j];
+                    for (int j = 0; j < TW; ++j) b[j] = u_s[ii * UP + tn * TW + j];
 #pragma unroll
                     for (int i = 0; i < TU; ++i)
 #pragma unroll
