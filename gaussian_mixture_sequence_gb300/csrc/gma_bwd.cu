@@ -680,55 +680,80 @@ __global__ void __launch_bounds__(kThreads) k_bwd_delta(long long rows, int K, i
 }
 
 // dx_d = -sum_k delta_k y_kd s_kd with y = x s - mu s: rows of one slice, a thread per
-// (row, feature pair), the parameters of KT components at a time in shared memory.
+// (four consecutive rows, feature pair), the parameters of KT components at a time in
+// shared memory.  One 16-byte parameter word and one 16-byte word of delta (the tile is
+// held transposed, [component][row]) serve the thread's four rows.
+constexpr int kDxRows = 4;   // rows per thread
+template <int D>
+struct DxCfg {
+    static constexpr int DP = D / 2, RG = kThreads / DP, RT = RG * kDxRows;   // row groups, rows per CTA
+    static constexpr int KT = D == 128 ? 32 : 64;                                // components per tile
+    static constexpr int DPITCH = RT + 4;   // delta tile pitch: 16-byte rows, 4-way conflicts when staged
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_bwd_dx(int N, int K, int KP, int H, const void *__restrict__ x,
                                                      bool x_bf16, const float4 *__restrict__ prm,
                                                      const float *__restrict__ delta, float *__restrict__ dx)
 {
-    constexpr int DP = D / 2, RT = kThreads / DP;   // rows per pass
-    constexpr int KT = D == 128 ? 32 : 64;          // components per tile (static shared memory <= 48 KB)
+    using Cfg = DxCfg<D>;
+    constexpr int DP = Cfg::DP, RT = Cfg::RT, KT = Cfg::KT, DPITCH = Cfg::DPITCH;
     __shared__ float4 p_s[KT * DP];
-    __shared__ float d_s[RT][KT + 1];
+    __shared__ __align__(16) float d_s[KT * DPITCH];
     const long long bh = blockIdx.y;
-    const int h = (int)(bh % H), tid = threadIdx.x, dp = tid % DP, rr = tid / DP;
-    const int row = blockIdx.x * RT + rr;
-    const bool on = row < N;
-    const long long xo = (bh * N + row) * D + 2 * dp;
-    float2 xv = make_float2(0.f, 0.f);
-    if (on) {
-        if (x_bf16) {
-            const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(x) + xo);
-            xv = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-        } else {
-            xv = *reinterpret_cast<const float2 *>(static_cast<const float *>(x) + xo);
+    const int h = (int)(bh % H), tid = threadIdx.x, dp = tid % DP, rg = tid / DP;
+    const int row0 = blockIdx.x * RT + rg * kDxRows;   // this thread's rows row0 .. row0 + 3
+    float2 xv[kDxRows], acc[kDxRows];
+#pragma unroll
+    for (int i = 0; i < kDxRows; ++i) {
+        const int row = row0 + i;
+        const long long xo = (bh * N + row) * D + 2 * dp;
+        xv[i] = make_float2(0.f, 0.f);
+        acc[i] = make_float2(0.f, 0.f);
+        if (row < N) {
+            if (x_bf16) {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(x) + xo);
+                xv[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            } else {
+                xv[i] = *reinterpret_cast<const float2 *>(static_cast<const float *>(x) + xo);
+            }
         }
     }
-    float2 acc = make_float2(0.f, 0.f);
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
         for (int i = tid; i < kn * DP; i += kThreads) p_s[i] = prm[((long long)h * K + k0) * DP + i];
-        for (int i = tid; i < RT * KT; i += kThreads) {
+        for (int i = tid; i < RT * KT; i += kThreads) {   // coalesced along the components
             const int r = i / KT, k = i % KT, rw = blockIdx.x * RT + r;
-            d_s[r][k] = (rw < N && k < kn) ? delta[(bh * N + rw) * KP + k0 + k] : 0.f;
+            d_s[k * DPITCH + r] = (rw < N && k < kn) ? delta[(bh * N + rw) * KP + k0 + k] : 0.f;
         }
         __syncthreads();
         for (int k = 0; k < kn; ++k) {
             const float4 p = p_s[k * DP + dp];
-            const float dk = d_s[rr][k];
-            const float y0 = fmaf(xv.x, p.x, p.z), y1 = fmaf(xv.y, p.y, p.w);
-            acc.x = fmaf(dk * p.x, y0, acc.x);
-            acc.y = fmaf(dk * p.y, y1, acc.y);
+            const float4 d4 = *reinterpret_cast<const float4 *>(d_s + k * DPITCH + rg * kDxRows);
+            const float dk[kDxRows] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int i = 0; i < kDxRows; ++i) {
+                const float y0 = fmaf(xv[i].x, p.x, p.z), y1 = fmaf(xv[i].y, p.y, p.w);
+                acc[i].x = fmaf(dk[i] * p.x, y0, acc[i].x);
+                acc[i].y = fmaf(dk[i] * p.y, y1, acc[i].y);
+            }
         }
     }
-    if (on) *reinterpret_cast<float2 *>(dx + xo) = make_float2(-acc.x, -acc.y);
+#pragma unroll
+    for (int i = 0; i < kDxRows; ++i) {
+        const int row = row0 + i;
+        if (row < N)
+            *reinterpret_cast<float2 *>(dx + (bh * N + row) * D + 2 * dp) = make_float2(-acc[i].x, -acc[i].y);
+    }
 }
 
 // Parameter partial sums of one block of kBlockRows rows of one slice: a thread per
 // (component, feature pair) of a tile of KT components, rows RS at a time.
 //   pmu[bh][blk][k][d] = sum_rows delta_k y s,  pvar[..] = sum_rows delta_k s^2 (y^2 - 1) / 2,
 //   plp[bh][blk][k]    = sum_rows delta_k
+// s is constant over the rows, so the row loop sums delta y and delta y^2 (four packed
+// operations per feature pair and row) and the factors s and s^2 / 2 are applied once.
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_bwd_param(int N, int K, int KP, int H, const void *__restrict__ x,
                                                         bool x_bf16, const float4 *__restrict__ prm,
@@ -744,12 +769,14 @@ __global__ void __launch_bounds__(kThreads) k_bwd_param(int N, int K, int KP, in
     const int h = (int)(bh % H), blk = blockIdx.x, k0 = blockIdx.z * KT, tid = threadIdx.x;
     const int r_begin = blk * kBlockRows, r_end = min(N, r_begin + kBlockRows);
     float4 p[PER];
-    float2 gm[PER], gv[PER];
+    float2 ga[PER], gb[PER];   // sums over the rows of delta y and delta y^2
+    float sd[PER];             // sum over the rows of delta
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
         const int f = tid + e * kThreads, k = f / DP, dp = f % DP;
         p[e] = k0 + k < K ? prm[((long long)h * K + k0 + k) * DP + dp] : make_float4(0.f, 0.f, 0.f, 0.f);
-        gm[e] = gv[e] = make_float2(0.f, 0.f);
+        ga[e] = gb[e] = make_float2(0.f, 0.f);
+        sd[e] = 0.f;
     }
     float lp = 0.f;
     for (int r0 = r_begin; r0 < r_end; r0 += RS) {
@@ -779,12 +806,11 @@ __global__ void __launch_bounds__(kThreads) k_bwd_param(int N, int K, int KP, in
             for (int e = 0; e < PER; ++e) {
                 const int f = tid + e * kThreads, k = f / DP, dp = f % DP;
                 const float dk = d_s[r][k];
-                const float2 xv = x_s[r][dp];
-                const float y0 = fmaf(xv.x, p[e].x, p[e].z), y1 = fmaf(xv.y, p[e].y, p[e].w);
-                gm[e].x = fmaf(dk, y0 * p[e].x, gm[e].x);
-                gm[e].y = fmaf(dk, y1 * p[e].y, gm[e].y);
-                gv[e].x = fmaf(dk, 0.5f * p[e].x * p[e].x * fmaf(y0, y0, -1.f), gv[e].x);
-                gv[e].y = fmaf(dk, 0.5f * p[e].y * p[e].y * fmaf(y1, y1, -1.f), gv[e].y);
+                const float2 y = __ffma2_rn(x_s[r][dp], make_float2(p[e].x, p[e].y), make_float2(p[e].z, p[e].w));
+                const float2 dy = __fmul2_rn(make_float2(dk, dk), y);
+                ga[e] = __fadd2_rn(ga[e], dy);
+                gb[e] = __ffma2_rn(dy, y, gb[e]);
+                sd[e] += dk;
             }
             if (tid < KT) lp += d_s[r][tid];
         }
@@ -794,8 +820,11 @@ __global__ void __launch_bounds__(kThreads) k_bwd_param(int N, int K, int KP, in
     for (int e = 0; e < PER; ++e) {
         const int f = tid + e * kThreads, k = f / DP, dp = f % DP;
         if (k0 + k < K) {
-            reinterpret_cast<float2 *>(pmu + (base + k0 + k) * D)[dp] = gm[e];
-            reinterpret_cast<float2 *>(pvar + (base + k0 + k) * D)[dp] = gv[e];
+            const float2 gm = make_float2(p[e].x * ga[e].x, p[e].y * ga[e].y);
+            const float2 gv = make_float2(0.5f * p[e].x * p[e].x * (gb[e].x - sd[e]),
+                                          0.5f * p[e].y * p[e].y * (gb[e].y - sd[e]));
+            reinterpret_cast<float2 *>(pmu + (base + k0 + k) * D)[dp] = gm;
+            reinterpret_cast<float2 *>(pvar + (base + k0 + k) * D)[dp] = gv;
         }
     }
     if (tid < KT && k0 + tid < K) plp[base + k0 + tid] = lp;
@@ -921,7 +950,7 @@ template <int D>
 cudaError_t launch_bwd_route_d(const Dims &dm, const void *x, const float4 *prm, const float *delta, float *dx,
                                float *pmu, float *pvar, float *plp, cudaStream_t st)
 {
-    constexpr int DP = D / 2, RT = kThreads / DP;
+    constexpr int DP = D / 2, RT = DxCfg<D>::RT;
     k_bwd_dx<D><<<dim3((dm.N + RT - 1) / RT, (unsigned)dm.BH()), kThreads, 0, st>>>(dm.N, dm.K, dm.KP, dm.H, x,
                                                                                   dm.x_bf16, prm, delta, dx);
     cudaError_t e = cudaGetLastError();
