@@ -37,7 +37,7 @@ namespace gma {
 namespace {
 
 constexpr int kBC = 64;    // chunk rows
-constexpr int kBKC = 64;   // components per tile
+constexpr int kBKC = 32;   // components per tile (two CTAs of the chunk kernels fit on an SM)
 
 template <int DV>
 struct BwdCfg {
@@ -74,7 +74,7 @@ struct BwdQSmem {
 };
 
 template <int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_bwd_q(int N, int K, int KP, bool causal, float eps, const float *__restrict__ gq, const float *__restrict__ gk,
             const void *__restrict__ v, bool v_bf16, const float *__restrict__ dout, float *states,
             long long st_bh_stride, long long st_blk_stride, float *__restrict__ u, float *__restrict__ dgq)
@@ -436,7 +436,7 @@ struct BwdKSmem {
 };
 
 template <int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_bwd_k(int N, int K, int KP, bool causal, const float *__restrict__ gq, const float *__restrict__ gk,
             const void *__restrict__ v, bool v_bf16, const float *__restrict__ u, float *rmem,
             long long r_bh_stride, long long r_blk_stride, float *__restrict__ dgk, float *__restrict__ dv)
