@@ -58,6 +58,8 @@ CASES = [
     # difference of O(1) terms; a larger eps keeps the single-row case well conditioned
     (W["tiny"].with_(B=2, H=2, N=1, K=16, eps=0.1), True),
     (W["tiny"].with_(B=1, H=1, N=300, d=128, dv=16, K=512), False),
+    # d = 128 in the causal form, K = 100 (a ragged last tile of 32 components), ragged row blocks
+    (W["tiny"].with_(B=1, H=2, N=650, d=128, dv=64, K=100), True),
     (W["causal_4k"], True),
 ]
 
