@@ -14,8 +14,8 @@ using namespace gma;
 namespace {
 
 struct WsPlan {
-    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, pimg = 0, cimg = 0,
-           pimg2 = 0, dctl = 0, dlist = 0, bytes = 0;
+    size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, wimg3 = 0, pimg = 0,
+           cimg = 0, pimg2 = 0, dctl = 0, dlist = 0, dlist2 = 0, bytes = 0;
     long long dcap = 0;   // dense-list entries per head
     bool pruned = false;
 };
@@ -82,6 +82,22 @@ gma_status make_dims_raw(const gma_shape *s, Dims *dm)
     return GMA_OK;
 }
 
+// The bounded routing's per-head images and its two tile lists (dcap entries per head each).
+template <class Take>
+void plan_pruned(WsPlan &p, int H, long long dcap, Take &&take)
+{
+    p.pruned = true;
+    p.wimg = take((size_t)H * kPrunedWBytes);
+    p.wimg3 = take((size_t)H * kPrunedW3Bytes);
+    p.pimg = take((size_t)H * kPrunedPBytes);
+    p.cimg = take((size_t)H * kPrunedCBytes);
+    p.pimg2 = take((size_t)H * kPrunedP2Bytes);
+    p.dcap = dcap;
+    p.dctl = take((size_t)H * 2 * 4);
+    p.dlist = take((size_t)H * dcap * 8);
+    p.dlist2 = take((size_t)H * dcap * 8);
+}
+
 WsPlan plan(const Dims &dm, gma_op op)
 {
     WsPlan p;
@@ -93,16 +109,8 @@ WsPlan plan(const Dims &dm, gma_op op)
     };
     p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
     p.cst = take((size_t)dm.H * dm.K * 4);
-    if (op != GMA_OP_DECODE && resp_pruned_applies(dm)) {
-        p.pruned = true;
-        p.wimg = take((size_t)dm.H * kPrunedWBytes);
-        p.pimg = take((size_t)dm.H * kPrunedPBytes);
-        p.cimg = take((size_t)dm.H * kPrunedCBytes);
-        p.pimg2 = take((size_t)dm.H * kPrunedP2Bytes);
-        p.dcap = 2 * routing_tiles(dm.B, dm.N);   // both routings of a head
-        p.dctl = take((size_t)dm.H * 4);
-        p.dlist = take((size_t)dm.H * p.dcap * 8);
-    }
+    if (op != GMA_OP_DECODE && resp_pruned_applies(dm))
+        plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take);   // both routings of a head
     if (op == GMA_OP_USAGE) {   // Gamma in fp32, then the per-block partial sums and counts
         p.gq = take((size_t)dm.BH() * dm.N * dm.K * 4);
         p.partial = take((size_t)dm.BH() * usage_blocks(dm) * dm.K * 4);
@@ -218,16 +226,7 @@ BwdPlan plan_bwd_full(const Dims &dm)
     WsPlan &p = b.w;
     p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
     p.cst = take((size_t)dm.H * dm.K * 4);
-    if (resp_pruned_applies(dm)) {
-        p.pruned = true;
-        p.wimg = take((size_t)dm.H * kPrunedWBytes);
-        p.pimg = take((size_t)dm.H * kPrunedPBytes);
-        p.cimg = take((size_t)dm.H * kPrunedCBytes);
-        p.pimg2 = take((size_t)dm.H * kPrunedP2Bytes);
-        p.dcap = 2 * routing_tiles(dm.B, dm.N);   // both routings of a head
-        p.dctl = take((size_t)dm.H * 4);
-        p.dlist = take((size_t)dm.H * p.dcap * 8);
-    }
+    if (resp_pruned_applies(dm)) plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take);
     const size_t rows = (size_t)dm.BH() * dm.N, nb = (size_t)dm.BH() * dm.nblk();
     p.gq = take(rows * dm.KP * 4);
     p.gk = take(rows * dm.KP * 4);
@@ -248,8 +247,9 @@ WsPlan plan_bwd(const Dims &dm) { return plan_bwd_full(dm).w; }
 
 PrunedImages images(void *ws, const WsPlan &wp)
 {
-    return PrunedImages{at<unsigned char>(ws, wp.wimg), at<float4>(ws, wp.pimg), at<float>(ws, wp.cimg),
-                        at<float4>(ws, wp.pimg2), at<unsigned int>(ws, wp.dctl), at<int2>(ws, wp.dlist), wp.dcap};
+    return PrunedImages{at<unsigned char>(ws, wp.wimg), at<unsigned char>(ws, wp.wimg3), at<float4>(ws, wp.pimg),
+                        at<float>(ws, wp.cimg), at<float4>(ws, wp.pimg2), at<unsigned int>(ws, wp.dctl),
+                        at<int2>(ws, wp.dlist), at<int2>(ws, wp.dlist2), wp.dcap};
 }
 
 } // namespace
@@ -444,16 +444,7 @@ WsPlan plan_cross(const Dims &dq, const Dims &dk)
     };
     p.prm = take((size_t)dq.H * dq.K * (dq.D / 2) * 16);
     p.cst = take((size_t)dq.H * dq.K * 4);
-    if (resp_pruned_applies(dq)) {
-        p.pruned = true;
-        p.wimg = take((size_t)dq.H * kPrunedWBytes);
-        p.pimg = take((size_t)dq.H * kPrunedPBytes);
-        p.cimg = take((size_t)dq.H * kPrunedCBytes);
-        p.pimg2 = take((size_t)dq.H * kPrunedP2Bytes);
-        p.dcap = routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N);
-        p.dctl = take((size_t)dq.H * 4);
-        p.dlist = take((size_t)dq.H * p.dcap * 8);
-    }
+    if (resp_pruned_applies(dq)) plan_pruned(p, dq.H, routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N), take);
     const size_t gb = dq.g_bf16 ? 2 : 4;
     p.gq = take((size_t)dq.BH() * dq.N * dq.KG * gb);
     p.gk = take((size_t)dk.BH() * dk.N * dk.KG * gb);

@@ -135,16 +135,20 @@ volatile unsigned int *timeout_flag_host();
 // Per-head images the bounded routing kernel copies into shared memory.
 struct PrunedImages {
     unsigned char *w;   // [H][32768 B]: bf16 bound matrix, 128-byte-swizzled K-major
+    unsigned char *w3;  // [H][3][32768 B]: the log-joint matrix as three bf16 planes (hi, mid, lo)
+                        // in the operand order of the dense tensor-core pass
     float4 *p;          // [H][128][33]: packed exact parameters, rows padded by one word
     float *c;           // [H][4][128]: c_k, c'_k, A_k, M_k
     float4 *p2;         // [H][128][32]: the packed exact parameters for the dense kernel, feature
                         // pair 4 e + j of a component at position 8 j + e (e = feature eighth)
-    unsigned int *ctl;  // [H]: tiles of each head listed for the dense kernel (zeroed by k_prep_all)
-    int2 *list;         // [H][cap]: (slice | source tag << 30, tile) of the tiles left to the dense kernel
+    unsigned int *ctl;  // [2][H]: tiles of each head listed for the dense tensor-core pass, then
+                        // those it leaves to the exact dense pass (both zeroed by k_prep_all)
+    int2 *list;         // [H][cap]: (slice | source tag << 30, tile) of the tiles the routing left
+    int2 *list2;        // [H][cap]: the same for the tiles the tensor-core pass leaves
     long long cap;      // list entries per head (the tiles of both routings of a head)
 };
-constexpr size_t kPrunedWBytes = 32768, kPrunedPBytes = 128 * 33 * 16, kPrunedCBytes = 4 * 128 * 4,
-                 kPrunedP2Bytes = 128 * 32 * 16;
+constexpr size_t kPrunedWBytes = 32768, kPrunedW3Bytes = 3 * kPrunedWBytes, kPrunedPBytes = 128 * 33 * 16,
+                 kPrunedCBytes = 4 * 128 * 4, kPrunedP2Bytes = 128 * 32 * 16;
 // Routing tiles of 128 rows of a call with BH slices of N rows.
 inline long long routing_tiles(long long BH, int N) { return BH * ((N + 127) / 128); }
 
@@ -156,10 +160,11 @@ cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, fl
                             cudaStream_t st);
 cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const void *x, void *gamma, int ldg,
                                int layout, cudaStream_t st, int src = 0);
-// The dense exact pass over the tiles the bounded routings listed: source 0 is (d0, x0,
-// g0), source 1 (d1, x1, g1) (x1 may be null when only one routing ran).  Launched as a
-// programmatic dependent of the preceding launch; k_prep_all empties the list at the start
-// of every call that routes with the bound.
+// The dense pass over the tiles the bounded routings listed: source 0 is (d0, x0, g0),
+// source 1 (d1, x1, g1) (x1 may be null when only one routing ran).  The tensor-core pass
+// takes every listed tile and leaves those with rows of large magnitude to the exact
+// CUDA-core pass; both are launched as programmatic dependents of the preceding launch,
+// and k_prep_all empties both lists at the start of every call that routes with the bound.
 cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
                               const PrunedImages &img, int layout, cudaStream_t st);
 

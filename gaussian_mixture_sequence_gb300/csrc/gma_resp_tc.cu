@@ -111,16 +111,34 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 //   prm[k][dp] = {s_2dp, s_2dp+1, -mu_2dp s_2dp, -mu_2dp+1 s_2dp+1}, s = 1/sigma, sigma^2 = softplus(r)
 //   cst[k]     = log pi_k - 1/2 sum_d log sigma^2_kd, pi = softmax(logit_pi)
 // and W, the padded parameters and c, c', A_k, M_k (the component's largest a = s^2 and
-// |a mu|; the routing kernel takes the head-wide maxima when it loads the images).
+// |a mu|; the routing kernel takes the head-wide maxima when it loads the images), and W
+// again as three bf16 planes in the operand order of the dense tensor-core pass (below).
 constexpr int kPrepAllThreads = 512, kPrepAllComps = kPrepAllThreads / 16;
 
 __device__ __forceinline__ float softplus_f(float r) { return fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))); }
 
+// v = p0 + p1 + p2 + r with p0, p1, p2 bf16 and |r| <= 2^-24 |v|: each plane is the
+// round-to-nearest of what the previous ones leave, and each difference is exact in fp32.
+__device__ __forceinline__ void split3(float v, unsigned short (&p)[3])
+{
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        p[j] = __bfloat16_as_ushort(b);
+        v -= __bfloat162float(b);
+    }
+}
+
+// Operand position of feature f's square in the dense tensor-core pass; its value sits 16
+// positions later.  Column quarter q of the operand holds the squares of features
+// 16 q .. 16 q + 15, then their values.
+__host__ __device__ constexpr int dtc_pos(int f) { return 32 * (f >> 4) + (f & 15); }
+
 __global__ void __launch_bounds__(kPrepAllThreads)
     k_prep_all(const float *__restrict__ mu, const float *__restrict__ var_raw, const float *__restrict__ logit_pi,
                float4 *__restrict__ prm, float *__restrict__ cst, unsigned char *__restrict__ wimg,
-               float4 *__restrict__ pimg, float *__restrict__ cimg, float4 *__restrict__ pimg2,
-               unsigned int *__restrict__ dctl)
+               unsigned char *__restrict__ wimg3, float4 *__restrict__ pimg, float *__restrict__ cimg,
+               float4 *__restrict__ pimg2, unsigned int *__restrict__ dctl)
 {
     constexpr int NW = kPrepAllThreads / 32;
     __shared__ float red[2][NW];
@@ -128,7 +146,10 @@ __global__ void __launch_bounds__(kPrepAllThreads)
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = blockIdx.y * kPrepAllComps + (tid >> 4), part = tid & 15;   // component, features 4 part ..
     const float *l = logit_pi + (long long)h * kPK;
-    if (blockIdx.y == 0 && tid == 0) dctl[h] = 0u;   // no tile of this head listed for the dense kernel yet
+    if (blockIdx.y == 0 && tid == 0) {   // no tile of this head listed for either dense pass yet
+        dctl[h] = 0u;
+        dctl[gridDim.x + h] = 0u;
+    }
 
     // log-sum-exp of the head's logits (thread k < K holds logit k)
     const float lv = tid < kPK ? l[tid] : -FLT_MAX;
@@ -173,8 +194,24 @@ __global__ void __launch_bounds__(kPrepAllThreads)
         amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
         mmax = fmaxf(mmax, fmaxf(fabsf(p.x * p.z), fabsf(p.y * p.w)));
         // W row k: -1/2 s^2 at features f, f + 1 and -s (-mu s) at d + f, d + f + 1
-        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, f, kPK, 2)) = pack2(-0.5f * p.x * p.x, -0.5f * p.y * p.y);
-        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, kPD + f, kPK, 2)) = pack2(-p.x * p.z, -p.y * p.w);
+        const float wa0 = -0.5f * p.x * p.x, wa1 = -0.5f * p.y * p.y, wb0 = -p.x * p.z, wb1 = -p.y * p.w;
+        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, f, kPK, 2)) = pack2(wa0, wa1);
+        *reinterpret_cast<uint32_t *>(wh + sw128_offset(k, kPD + f, kPK, 2)) = pack2(wb0, wb1);
+        // the same row as three planes, squares' weights at dtc_pos(f), values' 16 later
+        unsigned short a0[3], a1[3], b0[3], b1[3];
+        split3(wa0, a0);
+        split3(wa1, a1);
+        split3(wb0, b0);
+        split3(wb1, b1);
+        unsigned char *w3 = wimg3 + (long long)h * kPrunedW3Bytes;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            unsigned char *pl = w3 + j * kPrunedWBytes;
+            *reinterpret_cast<uint32_t *>(pl + sw128_offset(k, dtc_pos(f), kPK, 2)) =
+                (uint32_t)a0[j] | ((uint32_t)a1[j] << 16);
+            *reinterpret_cast<uint32_t *>(pl + sw128_offset(k, dtc_pos(f) + 16, kPK, 2)) =
+                (uint32_t)b0[j] | ((uint32_t)b1[j] << 16);
+        }
     }
     if (part == 15) pimg[row * kPStride + kPDP] = make_float4(0.f, 0.f, 0.f, 0.f);   // the row's padding word
     for (int o = 1; o < 16; o <<= 1) {   // the component's 16 threads
@@ -471,9 +508,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
                 }
             }
-            // a tile where many rows keep many components goes to the dense exact kernel
-            // (k_resp_dense), which evaluates every component with register blocking; walking
-            // the kept sets here one component at a time would be bound by shared-memory reads
+            // a tile where many rows keep many components goes to the dense passes (every
+            // component of every row on the tensor cores, k_resp_dense_tc, and rows of large
+            // magnitude exactly, k_resp_dense); walking the kept sets here one component at a
+            // time would be bound by shared-memory reads
             if (group_popc(grp, __popc(xm0) + __popc(xm1) >= kDenseKept) >= kDenseRows) {
                 if (gt == 0) dlist[(long long)head * dcap + atomicAdd(dctl + head, 1u)] = make_int2(bh | (src << 30), t);
                 continue;   // no exact pass and no output tile here
@@ -620,9 +658,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // ------------------------------------------------------------------------
-// Dense exact responsibilities of the tiles k_resp_pruned listed (rows that keep
-// many components): every one of the 128 log-joints of every row, the same
-// packed-FMA quadratic form ((x - mu) / sigma)^2, then the softmax.
+// Dense exact responsibilities of the tiles the tensor-core dense pass leaves (rows
+// of large magnitude among rows that keep many components): every one of the 128
+// log-joints of every row, the same packed-FMA quadratic form ((x - mu) / sigma)^2,
+// then the softmax.
 //
 // Two persistent CTAs of 8 warps per SM (one CTA's loads, softmax and stores
 // overlap the other's FMAs), each taking a contiguous range of the listed tiles
@@ -640,7 +679,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // component for two rows.  Log-joints go to a shared [128][132] tile; 2 threads per row take the
 // softmax (components strided by 2); rows then leave in the requested layout
 // with coalesced stores.  The kernel
-// is a programmatic dependent of the last routing launch: it reads the list
+// is a programmatic dependent of the tensor-core dense pass: it reads its list
 // only after griddepcontrol.wait.
 constexpr int kDThreads = 256, kDPitch = 132;
 
@@ -827,6 +866,344 @@ __global__ void __launch_bounds__(kDThreads, 2)
     }
 }
 
+// ------------------------------------------------------------------------
+// Dense responsibilities of the listed tiles on the tensor cores.
+//
+// Expanding the square, the log-joint of the GMA explainer's posterior is
+//   l_ik = c'_k + sum_d ( -1/2 a_kd x_id^2 + a_kd mu_kd x_id ),   a = 1/sigma^2,
+// one product of [x^2 | x] (128 rows x 128) with W^T (128 x 128 components) per tile.
+// Each fp32 operand is held as three bf16 planes, v = v0 + v1 + v2 up to 2^-24 |v| (split3),
+// and the six plane products whose orders add up to at most two are accumulated in fp32,
+// smallest first (A2 W0, A1 W1, A1 W0, A0 W2, A0 W1, A0 W0); each of the three dropped ones
+// is below 2^-24 of its term.  So every log-joint carries the rounding of an fp32
+// evaluation of the expanded form: a few fp32 units of
+//   S_i = 1/2 A sum_d x_id^2 + M sum_d |x_id|   (A = max a, M = max |a mu| over the head),
+// which bounds the sum of the terms' magnitudes.  The direct form (x - mu)^2 / sigma^2 of
+// the exact kernels rounds at the scale of the log-joint itself, which on the rows these
+// tiles hold (many components near the best one) is of the same order.  A tile with a row
+// whose S_i exceeds kTSMax (|x| large against the components) goes on a second list, to
+// the exact dense kernel; every other row's posteriors are the softmax of these log-joints.
+//
+// One persistent CTA of 16 warps per SM over a contiguous range of the listed tiles in head
+// order (the head's three planes, 96 KB, are loaded once per head).  Warp w owns TMEM lanes
+// 32 (w % 4) .. + 31 (rows of the tile) and column quarter q = w / 4: operand positions
+// 32 q .. 32 q + 31 (the squares, then the values, of features 16 q .. + 15; dtc_pos) and
+// components 32 q .. + 31 of the result.  Item n: the warps turn the landed routing tile
+// into the operand planes in TMEM; one thread issues the 48 MMAs into accumulator n % 2 and
+// fetches the next routing tile; then the warps take the softmax of item n - 1 from the
+// other accumulator while item n's products run.
+constexpr int kTThreads = 512;
+constexpr float kTSMax = 4096.f;
+
+struct DenseTcSmem {
+    static constexpr uint32_t W3 = kPrunedW3Bytes;      // three planes of W, SW128 K-major
+    static constexpr uint32_t X = kPRows * kPD * 4;     // routing tile (fp32 worst case)
+    static constexpr uint32_t O = kPRows * kPK * 4;     // output tile (fp32 worst case)
+    static constexpr uint32_t C = 2 * kPrunedCBytes;    // c, c', A, M of two heads
+    static constexpr uint32_t EX = 2 * 4 * kPRows * 4;  // per quarter: row maxima, row sums
+    static constexpr uint32_t SS = 2 * 4 * kPRows * 4;  // per quarter: parts of S_i of two items
+    static constexpr size_t bytes = 1024 + (size_t)W3 + X + O + C + EX + SS + 64;
+};
+static_assert(DenseTcSmem::bytes <= 232448, "dense tensor-core routing: shared memory above the per-block limit");
+
+struct DenseTcMaps {
+    CUtensorMap x[2], g[2], glo[2];   // per source: routing rows, output (hi plane), lo plane
+};
+
+__global__ void __launch_bounds__(kTThreads, 1)
+    k_resp_dense_tc(const __grid_constant__ DenseTcMaps maps, bool x_bf16, int H,
+                    const unsigned char *__restrict__ w3img, const float *__restrict__ cimg, int layout,
+                    const int2 *__restrict__ dlist, unsigned int *__restrict__ dctl, int2 *__restrict__ dlist2,
+                    long long dcap, unsigned int *timeout)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the routing launches have listed their tiles
+    extern __shared__ unsigned char sm_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ unsigned int s_red[kTThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, cq = warp >> 2;
+    const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
+
+    // the listed tiles in head order; this CTA takes a contiguous range of them
+    unsigned int listed = 0;
+    for (int h = tid; h < H; h += kTThreads) listed += dctl[h];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) listed += __shfl_xor_sync(0xffffffffu, listed, o);
+    if (lane == 0) s_red[warp] = listed;
+    __syncthreads();
+    listed = 0;
+#pragma unroll
+    for (int w = 0; w < kTThreads / 32; ++w) listed += s_red[w];
+    const unsigned int per = (listed + gridDim.x - 1) / gridDim.x;
+    const unsigned int g0 = min(listed, blockIdx.x * per), g1 = min(listed, g0 + per);
+    if (g0 >= g1) return;
+    const int cnt = (int)(g1 - g0);
+    // entry g of the list in head order, for g increasing: every thread walks the same counts
+    int hc = 0;
+    unsigned int hbase = 0, hcnt = dctl[0];
+    auto entry_at = [&](unsigned int g, int &head) {
+        while (g >= hbase + hcnt) {
+            hbase += hcnt;
+            hcnt = dctl[++hc];
+        }
+        head = hc;
+        return dlist[(long long)hc * dcap + (g - hbase)];
+    };
+
+    unsigned char *w_s = sm;
+    unsigned char *xb = w_s + DenseTcSmem::W3;
+    unsigned char *ob = xb + DenseTcSmem::X;
+    float *c_s = reinterpret_cast<float *>(ob + DenseTcSmem::O);   // [2][4][128]
+    float *mx_s = c_s + 2 * 4 * kPK;                                // [4][128] row maxima per quarter
+    float *sx_s = mx_s + 4 * kPRows;                                // [4][128] row sums per quarter
+    float *ss_s = sx_s + 4 * kPRows;                                // [2][4][128] parts of S_i
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 2 * 4 * kPRows);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1);
+    auto bar_m = [&](int b) { return smem_addr(bar + 2 + b); };
+    const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
+    const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
+    const int ge = g_f32 ? 4 : 2;
+    constexpr uint32_t LO = kPRows * kPK * 2;   // split: the lo plane's tile follows the hi plane's
+    auto load_x = [&](int2 e) {                 // one thread
+        const int s = e.x >> 30, bh = e.x & 0x3fffffff;
+        mbar_expect_tx(BAR_X, xbytes);
+        tma_load_3d(smem_addr(xb), &maps.x[s], 0, e.y * kPRows, bh, BAR_X);
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kPRows * 128), &maps.x[s], 32, e.y * kPRows, bh, BAR_X);
+    };
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tslot), 512);
+        tmem_relinquish();
+    }
+    int hcur = 0;
+    int2 ecur = entry_at(g0, hcur);
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
+        mbar_init_fence();
+        load_x(ecur);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;   // operand planes at columns 0, 64, 128; accumulators at 256, 384
+    const uint32_t id = idesc(128, kPK, kFmtBF16);
+    bool ok = true;
+    int head = -1, hp = 1, nimg = 0;   // the loaded head and the buffer of its constants
+    float amax = 0.f, mmax = 0.f;      // its A and M
+    int2 eprev = ecur;                 // the previous item: entry, head, constants' buffer
+    int hprev = 0, hpprev = 0;
+    int m_last = -1;                   // tid 0: the last item whose products were issued,
+    bool x_pending = true;             // and whether a routing tile is in flight
+    uint32_t x_par = 0;
+
+    // softmax of item m (its products were committed to accumulator m % 2): the posteriors
+    // into the output tile and out by TMA stores, or the tile onto the exact kernel's list
+    auto epilogue = [&](int m, int2 e, int h, int hpx) {
+        ok = mbar_wait(bar_m(m & 1), (uint32_t)((m >> 1) & 1)) && ok;
+        fence_after_sync();
+        uint32_t r[2][16];
+        const uint32_t dcol = 256u + 128u * (uint32_t)(m & 1) + 32u * (uint32_t)cq;
+        tmem_ld16(tmem_at(tbase, 32 * qd, dcol), r[0]);
+        tmem_ld16(tmem_at(tbase, 32 * qd, dcol + 16), r[1]);
+        tmem_wait_ld();
+        fence_before_sync();
+        const float *cp = c_s + hpx * 4 * kPK + kPK + 32 * cq;   // c'_k
+        float l[32], mloc = -FLT_MAX;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            l[j] = __uint_as_float(r[j >> 4][j & 15]) + cp[j];
+            mloc = fmaxf(mloc, l[j]);
+        }
+        mx_s[cq * kPRows + i] = mloc;
+        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
+        __syncthreads();
+        const float mrow = fmaxf(fmaxf(mx_s[i], mx_s[kPRows + i]), fmaxf(mx_s[2 * kPRows + i], mx_s[3 * kPRows + i]));
+        float sloc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            l[j] = expf(l[j] - mrow);
+            sloc += l[j];
+        }
+        sx_s[cq * kPRows + i] = sloc;
+        const float *sp = ss_s + (m & 1) * 4 * kPRows;
+        const bool far = (sp[i] + sp[kPRows + i]) + (sp[2 * kPRows + i] + sp[3 * kPRows + i]) > kTSMax;
+        const bool relist = __syncthreads_or(far) != 0;
+        if (!relist) {
+            const float inv = 1.0f / ((sx_s[i] + sx_s[kPRows + i]) + (sx_s[2 * kPRows + i] + sx_s[3 * kPRows + i]));
+            if (g_f32) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * cq + 4 * g, kPRows, 4)) =
+                        make_float4(l[4 * g] * inv, l[4 * g + 1] * inv, l[4 * g + 2] * inv, l[4 * g + 3] * inv);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat16 h0, l0, h1, l1;
+                        split_bf16(l[8 * g + 2 * u] * inv, h0, l0);
+                        split_bf16(l[8 * g + 2 * u + 1] * inv, h1, l1);
+                        hw[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                        lw[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                    }
+                    const uint32_t off = sw128_offset(i, 32 * cq + 8 * g, kPRows, 2);
+                    *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+        }
+        fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
+        const bool all_ok = __syncthreads_and(ok) != 0;
+        if (tid == 0 && all_ok) {
+            if (relist) {
+                dlist2[(long long)h * dcap + atomicAdd(dctl + H + h, 1u)] = e;
+            } else {
+                const int s = e.x >> 30, bh = e.x & 0x3fffffff;
+                for (int a = 0; a < kPK * ge / 128; ++a) {
+                    tma_store_3d(&maps.g[s], a * (128 / ge), e.y * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+                    if (g_split)
+                        tma_store_3d(&maps.glo[s], a * (128 / ge), e.y * kPRows, bh,
+                                     smem_addr(ob + LO + a * (kPRows * 128)));
+                }
+                bulk_commit();
+            }
+        }
+    };
+
+    for (int n = 0; n <= cnt; ++n) {
+        int2 enext = ecur;
+        int hnext = hcur, hp_n = hp;
+        if (n < cnt) {
+            // the products of item n - 1 are done: the operand planes and W may be replaced
+            if (n >= 1) ok = mbar_wait(bar_m((n - 1) & 1), (uint32_t)(((n - 1) >> 1) & 1)) && ok;
+            if (hcur != head) {
+                head = hcur;
+                hp ^= 1;   // the previous head's constants stay for item n - 1's softmax
+                if (tid == 0) {
+                    fence_proxy_async();   // earlier thread reads of the constants' buffer come first
+                    mbar_expect_tx(BAR_I, (uint32_t)(kPrunedW3Bytes + kPrunedCBytes));
+                    bulk_g2s(smem_addr(w_s), w3img + (long long)head * kPrunedW3Bytes, kPrunedW3Bytes, BAR_I);
+                    bulk_g2s(smem_addr(c_s + hp * 4 * kPK), cimg + (long long)head * 4 * kPK, kPrunedCBytes, BAR_I);
+                }
+                ok = mbar_wait(BAR_I, (uint32_t)(nimg & 1)) && ok;
+                ++nimg;
+                float a = 0.f, mm = 0.f;
+#pragma unroll
+                for (int q = 0; q < kPK / 32; ++q) {
+                    a = fmaxf(a, c_s[hp * 4 * kPK + 2 * kPK + lane + 32 * q]);
+                    mm = fmaxf(mm, c_s[hp * 4 * kPK + 3 * kPK + lane + 32 * q]);
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+                }
+                amax = a;
+                mmax = mm;
+            }
+            hp_n = hp;
+            const bool landed = mbar_wait(BAR_X, (uint32_t)(n & 1));
+            ok = landed && ok;
+            if (tid == 0 && landed) x_pending = false;
+            // features 16 cq .. + 15 of row i: squares and values into the three planes
+            float xv[16];
+            if (x_bf16) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kPRows, 2));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        xv[8 * g + 2 * e] = __uint_as_float(w[e] << 16);
+                        xv[8 * g + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kPRows, 4));
+                    xv[4 * g] = u.x;
+                    xv[4 * g + 1] = u.y;
+                    xv[4 * g + 2] = u.z;
+                    xv[4 * g + 3] = u.w;
+                }
+            }
+            uint32_t pw[3][16];
+            float s2 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float v0 = xv[2 * c], v1 = xv[2 * c + 1];
+                const float q0 = v0 * v0, q1 = v1 * v1;
+                s2 += q0 + q1;
+                s1 += fabsf(v0) + fabsf(v1);
+                unsigned short a0[3], a1[3], b0[3], b1[3];
+                split3(q0, a0);
+                split3(q1, a1);
+                split3(v0, b0);
+                split3(v1, b1);
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    pw[j][c] = (uint32_t)a0[j] | ((uint32_t)a1[j] << 16);
+                    pw[j][8 + c] = (uint32_t)b0[j] | ((uint32_t)b1[j] << 16);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
+            ss_s[(n & 1) * 4 * kPRows + cq * kPRows + i] = fmaf(0.5f * amax, s2, mmax * s1);
+            tmem_wait_st();
+            fence_before_sync();
+            __syncthreads();   // the planes are in TMEM and the routing tile has been read
+            fence_after_sync();
+            if (n + 1 < cnt) enext = entry_at(g0 + n + 1, hnext);
+            if (tid == 0 && ok) {
+                const uint32_t d = tbase + 256u + 128u * (uint32_t)(n & 1);
+#pragma unroll
+                for (int q = 0; q < 6; ++q) {
+                    const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                 // A plane
+                    const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);     // W plane
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+                        const uint32_t boff = pb * (uint32_t)kPrunedWBytes + (kb >> 7) * (kPK * 128) + (kb & 127);
+                        mma_ts(0u, d, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
+                               (q | kk) ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_m(n & 1));
+                m_last = n;
+                if (n + 1 < cnt) {   // (the tile was only read by threads: no proxy fence)
+                    load_x(enext);
+                    x_pending = true;
+                    x_par = (uint32_t)((n + 1) & 1);
+                }
+            }
+        }
+        if (n >= 1) epilogue(n - 1, eprev, hprev, hpprev);
+        eprev = ecur;
+        hprev = hcur;
+        hpprev = hp_n;
+        ecur = enext;
+        hcur = hnext;
+        ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
+        if (!ok) break;
+    }
+    // after a failed wait a routing tile or products may still be in flight: let them finish
+    // (bounded) before TMEM and shared memory are released
+    bool ok_end = ok;
+    if (tid == 0) {
+        if (!ok) {
+            if (x_pending) ok_end = mbar_wait(BAR_X, x_par) && ok_end;
+            if (m_last >= 0) ok_end = mbar_wait(bar_m(m_last & 1), (uint32_t)((m_last >> 1) & 1)) && ok_end;
+        }
+        bulk_wait_all();
+    }
+    fence_before_sync();
+    if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 } // namespace
 
 bool resp_pruned_applies(const Dims &dm) { return dm.K == kPK && dm.D == kPD; }
@@ -836,7 +1213,8 @@ cudaError_t launch_prep_all(const Dims &dm, const gma_params &p, float4 *prm, fl
 {
     if (!resp_pruned_applies(dm)) return cudaErrorInvalidValue;
     k_prep_all<<<dim3(dm.H, kPK / kPrepAllComps), kPrepAllThreads, 0, st>>>(p.mu, p.var_raw, p.logit_pi, prm, cst,
-                                                                           img.w, img.p, img.c, img.p2, img.ctl);
+                                                                           img.w, img.w3, img.p, img.c, img.p2,
+                                                                           img.ctl);
     return cudaGetLastError();
 }
 
@@ -877,27 +1255,67 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
 cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
                               const PrunedImages &img, int layout, cudaStream_t st)
 {
+    const long long items = routing_tiles(d0.BH(), d0.N) + (x1 ? routing_tiles(d1.BH(), d1.N) : 0);
+    if (items == 0) return cudaSuccess;   // no rows, nothing listed
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    {   // every listed tile on the tensor cores
+        constexpr size_t smem = DenseTcSmem::bytes;
+        static std::atomic<unsigned long long> smem_set{0};
+        const cudaError_t e = allow_smem(k_resp_dense_tc, smem, smem_set);
+        if (e != cudaSuccess) return e;
+        DenseTcMaps maps;
+        const bool g16 = layout != GL_F32;
+        for (int s = 0; s < 2; ++s) {
+            const bool one = s == 0 || !x1;   // without a second routing, source 1 repeats source 0
+            const Dims &d = one ? d0 : d1;
+            const void *x = one ? x0 : x1;
+            void *g = one ? g0 : g1;
+            const long long plane = d.BH() * d.N * (long long)kPK;   // elements of one plane (split)
+            if (!make_tma_3d(&maps.x[s], x, d.x_bf16, kPD, d.N, d.BH(), kPRows) ||
+                !make_tma_3d(&maps.g[s], g, g16, kPK, d.N, d.BH(), kPRows))
+                return cudaErrorInvalidValue;
+            if (layout == GL_SPLIT) {
+                if (!make_tma_3d(&maps.glo[s], static_cast<__nv_bfloat16 *>(g) + plane, true, kPK, d.N, d.BH(),
+                                 kPRows))
+                    return cudaErrorInvalidValue;
+            } else {
+                maps.glo[s] = maps.g[s];
+            }
+        }
+        unsigned int *flag = timeout_flag_dev();
+        if (!flag) return cudaErrorMemoryAllocation;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(items < sm_count() ? items : sm_count()));   // one per SM
+        cfg.blockDim = dim3(kTThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t l = cudaLaunchKernelEx(&cfg, k_resp_dense_tc, maps, d0.x_bf16, d0.H,
+                                                 (const unsigned char *)img.w3, (const float *)img.c, layout,
+                                                 (const int2 *)img.list, img.ctl, img.list2, img.cap, flag);
+        if (l != cudaSuccess) return l;
+    }
+    // the tiles it left (rows of large magnitude), exactly on the CUDA cores
     constexpr size_t smem = (size_t)kPRows * kDPitch * 4;
     static std::atomic<unsigned long long> smem_set{0};
     const cudaError_t e = allow_smem(k_resp_dense, smem, smem_set);
     if (e != cudaSuccess) return e;
     const DenseSrc s0{x0, g0, d0.N, d0.BH() * d0.N * (long long)kPK};
     const DenseSrc s1 = x1 ? DenseSrc{x1, g1, d1.N, d1.BH() * d1.N * (long long)kPK} : s0;
-    const long long items = routing_tiles(d0.BH(), d0.N) + (x1 ? routing_tiles(d1.BH(), d1.N) : 0);
     cudaLaunchConfig_t cfg = {};
     const long long ctas = 2LL * sm_count();   // two resident per SM
-    cfg.gridDim = dim3((unsigned)(items < ctas ? (items > 0 ? items : 1) : ctas));
+    cfg.gridDim = dim3((unsigned)(items < ctas ? items : ctas));
     cfg.blockDim = dim3(kDThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_resp_dense, s0, s1, d0.x_bf16, d0.H, (const float4 *)img.p2,
-                              (const float *)img.c, layout, (const int2 *)img.list, (const unsigned int *)img.ctl,
-                              img.cap);
+                              (const float *)img.c, layout, (const int2 *)img.list2,
+                              (const unsigned int *)(img.ctl + d0.H), img.cap);
 }
 
 } // namespace gma

@@ -81,6 +81,38 @@ def test_responsibilities_adversarial_rows():
     assert np.abs(out.sum(-1) - 1).max() < 1e-5
 
 
+@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
+def test_responsibilities_dense_tiles_across_scales(x_dtype):
+    """Tiles of N(0, s^2) rows, one scale per tile of 128 rows, from s = 0.3 to s = 6: the
+    wide tiles keep many components and go to the dense passes, the tensor-core one below
+    its magnitude limit (s up to about 2) and the exact one above it; a last tile mixes
+    N(0, 1) rows with one row of s = 6.  Each tile's posteriors must match the oracle's."""
+    import oracle
+    from gaussian_mixture_sequence_gb300 import gma
+    from gpu_cases import shape_of
+    scales = [0.3, 0.7, 1.0, 1.4, 1.8, 2.2, 3.0, 6.0]
+    wl = W["causal_4k"].with_(B=1, H=2, N=128 * (len(scales) + 1) - 37, x_dtype=x_dtype)
+    mu, vr, lp = workloads.params(wl)
+    rng = np.random.default_rng(11)
+    x = np.concatenate([s * rng.standard_normal((wl.H, 128, 64)) for s in scales] +
+                       [rng.standard_normal((wl.H, 128 - 37, 64))], axis=1).astype(np.float32)
+    x[:, 128 * len(scales) + 40] *= 6.0
+    if x_dtype == "bf16":
+        x = workloads.round_bf16(x)
+    dev = "cuda:0"
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    xd = t(x[None]).to(torch.bfloat16) if x_dtype == "bf16" else t(x[None])
+    g = torch.empty(1, wl.H, wl.N, wl.K, device=dev)
+    gma.gma_responsibilities(shape_of(wl), t(mu), t(vr), t(lp), xd, g)
+    ref = oracle.responsibilities(mu, vr, lp, x)
+    out = g.reshape(wl.H, wl.N, wl.K).cpu().numpy()
+    for j in range(len(scales) + 1):
+        rows = slice(128 * j, min(wl.N, 128 * (j + 1)))
+        _report(f"gamma tile {j} (scale {scales[j] if j < len(scales) else 'mixed'}) {x_dtype}",
+                normwise(out[:, rows], ref[:, rows]), TOL["f32"])
+    assert np.abs(out.sum(-1) - 1).max() < 1e-5
+
+
 # --------------------------------------------------------- S2 + S3 -------------
 
 @pytest.mark.parametrize("wl,sample", [
