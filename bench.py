@@ -82,8 +82,11 @@ def stage_work(stage, wl):
       resp_q / resp_k     4*K*d on the FP32 pipe (one fp32x2 FMA for (x-mu)/sigma
                           and one for the square-accumulate, per component and
                           feature pair)
-      resp_dense          4*K*d per row of the tiles the bounded routings leave to
-                          the dense pass (K = 128, d = 64), both routings
+      resp_dense          24*K*d on the bf16 tensor pipe per row of the tiles the
+                          bounded routings leave to the dense pass (K = 128, d = 64;
+                          six passes of the three-plane product [x^2 | x] W^T, of
+                          4*K*d each; 16*K*d with bf16 rows, whose zero planes are
+                          skipped), both routings
       block_state /
       chunk_state_tc      2*K*(d_v+1)           (Gamma_K^T [V | 1])
       chunk_out(_tc)      2*C*K + C*(d_v+1) + 2*K*(d_v+1)   (P = Gq Gk^T, lower half
@@ -121,9 +124,9 @@ def stage_work(stage, wl):
         pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
         return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
     if stage == "resp_dense":
-        # the dense exact pass over the tiles the bounded routings left to it, charged as if every
-        # tile of both routings were dense (on the inputs where this stage dominates, all are)
-        return 2 * 4.0 * K * d * ht, "alu", 2 * (d * xb + K * gb) * ht
+        # the dense pass over the tiles the bounded routings left to it, charged as if every tile
+        # of both routings were dense (on the inputs where this stage dominates, nearly all are)
+        return 2 * dense_passes(wl) * 4.0 * K * d * ht, "tensor_bf16", 2 * (d * xb + K * gb) * ht
     if stage in ("block_state", "chunk_state_tc"):
         return 2.0 * K * (dv + 1) * ht, ("tensor_bf16" if tc else "alu"), (K * gb + dv * vb) * ht + st * nblk
     if stage in ("chunk_out", "chunk_out_tc"):
@@ -136,6 +139,13 @@ def stage_work(stage, wl):
     if stage == "state_reduce":   # every block's partial in, one total per (b, h) out
         return 0.0, "alu", st * (nblk + wl.B * wl.H)
     return 0.0, "alu", 0.0
+
+
+def dense_passes(wl):
+    """bf16 passes of the dense tensor-core routing, in units of one [x^2 | x] W^T product:
+    six for fp32 rows; with bf16 rows the values' two lower planes and the squares' lowest
+    plane are zero (32 of the 48 MMAs run)."""
+    return 4.0 if wl.x_dtype == "bf16" else 6.0
 
 
 def backward_work(wl):
@@ -154,7 +164,7 @@ def backward_work(wl):
     return flop, "alu", nbytes
 
 
-def algorithmic_work(stage, wl, kept=None):
+def algorithmic_work(stage, wl, kept=None, dense=None):
     """Algorithmic work of one launch of a stage, as the roofline charges it:
     (flop, pipe, bytes).
 
@@ -176,12 +186,14 @@ def algorithmic_work(stage, wl, kept=None):
     Flop: the method's contractions as `stage_work` counts them.  For the
     bounded routing (K = 128, d = 64) the flop are the bound GEMM on the bf16
     tensor pipe plus the exact evaluation of the kept components on the FP32
-    pipe (`kept` = mean kept components per row, measured), whichever takes
-    longer at its peak; elsewhere the dense FP32 routing."""
+    pipe, whichever takes longer at its peak (`kept` = mean kept components per
+    row outside the dense tiles and `dense` = fraction of rows in dense tiles,
+    both measured); the dense pass is charged its tensor passes over that
+    fraction of the rows; elsewhere the dense FP32 routing."""
     if wl.mode == "backward":
         return backward_work(wl)
     flop, pipe, _ = stage_work(stage, wl)
-    if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k"):
+    if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k", "resp_dense"):
         pipe = "tensor"   # the chunk products at the rate of their operand type (tf32 for fp32)
     d, dv = wl.d, wl.dv
     xb = 2 if wl.x_dtype == "bf16" else 4
@@ -192,10 +204,10 @@ def algorithmic_work(stage, wl, kept=None):
     if stage in ("resp_q", "resp_k"):
         nbytes = d * xb * ht
         if bounded_routing(wl) and kept is not None:
-            return 4.0 * d * kept * ht, "alu_kept", nbytes
+            return 4.0 * d * kept * (1.0 - (dense or 0.0)) * ht, "alu_kept", nbytes
         return flop, pipe, nbytes
     if stage == "resp_dense":   # its routing rows were charged to resp_q / resp_k
-        return flop, pipe, 0.0
+        return flop * (1.0 if dense is None else dense), pipe, 0.0
     if stage in ("block_state", "chunk_state_tc"):
         return flop, pipe, dv * vb * ht
     if stage in ("chunk_out", "chunk_out_tc"):
@@ -205,12 +217,12 @@ def algorithmic_work(stage, wl, kept=None):
     return flop, pipe, 0.0
 
 
-def roofline_of(stage, wl, t_launch, pk, kept=None):
+def roofline_of(stage, wl, t_launch, pk, kept=None, dense=None):
     """The roofline object of one launch taking t_launch seconds: the bound is the
     slower of its algorithmic flop at the pipe's peak and its algorithmic bytes at
     the measured HBM rate; `frac` = achieved / peak on that bound.  Also the same
     launch against the kernel-byte model (`kernel_bytes`, `frac_kernel_bytes`)."""
-    flop, pipe, nbytes = algorithmic_work(stage, wl, kept)
+    flop, pipe, nbytes = algorithmic_work(stage, wl, kept, dense)
     if pipe == "alu_kept":   # bounded routing: the bound GEMM (tensor) or the kept exact work (FP32)
         t_fp = flop / pipe_peak("alu", wl, pk)
         t_tc = stage_work(stage, wl)[0] / pipe_peak("tensor_bf16", wl, pk)
@@ -245,13 +257,15 @@ def pipe_peak(pipe, wl, pk):
     return bf16 if wl.gemm_dtype == "bf16" else bf16 * (1.1 / 2.25)
 
 
-def path_roofline_s(wl, pk, kept=None):
+def path_roofline_s(wl, pk, kept=None, dense=None):
     """Roofline time of one step: max(FP32 time, HBM time of the minimum
     traffic, tensor time).  With the bounded routing (K = 128, d = 64) the FP32
-    work is the exact evaluation of the kept components (two passes of 4*d flop
-    each per kept component and row; `kept` = mean kept components per row,
-    measured) and the bound GEMMs are tensor work; otherwise the FP32 work is
-    the dense routing, 8*K*d flop per head-token."""
+    work is the exact evaluation of the kept components of the rows outside the
+    dense tiles (two passes of 4*d flop each per kept component and row; `kept`
+    = their mean kept components, `dense` = fraction of rows in dense tiles,
+    both measured), and the bound GEMMs and the dense tiles' passes are tensor
+    work; otherwise the FP32 work is the dense routing, 8*K*d flop per
+    head-token."""
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6
     xb = 2 if wl.x_dtype == "bf16" else 4
     vb = 2 if wl.v_dtype == "bf16" else 4
@@ -274,8 +288,9 @@ def path_roofline_s(wl, pk, kept=None):
     tens = pk["bf16_tflops"] * 1e12 * (1.0 if wl.gemm_dtype == "bf16" else 1.1 / 2.25)
     t_mma = mma / tens
     if bounded_routing(wl) and kept is not None:
-        t_alu = 2 * 2 * 4.0 * wl.d * kept * ht / fp32_peak          # Q and K rows, two exact passes
-        t_mma += 8.0 * wl.K * wl.d * ht / (pk["bf16_tflops"] * 1e12)  # the two bound GEMMs
+        dn = dense or 0.0
+        t_alu = 2 * 2 * 4.0 * wl.d * kept * (1.0 - dn) * ht / fp32_peak   # Q and K rows, two exact passes
+        t_mma += (8.0 + 8.0 * dense_passes(wl) * dn) * wl.K * wl.d * ht / (pk["bf16_tflops"] * 1e12)
     else:
         t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)
@@ -617,18 +632,24 @@ class Runner:
         self.h_out.copy_(self.out, non_blocking=True)
 
     def kept_per_row(self):
-        """Mean number of components with a non-zero posterior per routing row
-        (the components the bounded routing evaluates exactly), from one
-        responsibilities call on the Q_X and K_X rows outside the timed region."""
+        """(mean number of components with a non-zero posterior per routing row
+        outside the dense tiles -- the components the bounded routing evaluates
+        exactly --, fraction of rows with every posterior non-zero -- the rows of
+        the tiles the dense pass takes), from one responsibilities call on the Q_X
+        and K_X rows outside the timed region."""
         import torch
         g, wl = self.gma, self.wl
-        n = 0.0
+        kept, dense = 0.0, 0.0
         for x in self.d_in[:2]:
             gam = torch.empty(wl.B, wl.H, wl.N, wl.K, device=self.dev)
             g.gma_responsibilities(self.shape, *self.prm, x, gam)
-            n += (gam > 0).sum(-1).float().mean().item()
+            cnt = (gam > 0).sum(-1)
+            full = cnt == wl.K
+            dense += full.float().mean().item()
+            rest = cnt[~full]
+            kept += rest.float().mean().item() if rest.numel() else 0.0
             del gam
-        return n / 2
+        return kept / 2, dense / 2
 
     def resident_bytes(self):
         """Bytes a step streams from HBM that a repeat could find in L2: the state of the
@@ -742,9 +763,10 @@ def main():
                                        for s_ in range(args.steps))
     dom = max(stage_ms, key=stage_ms.get)
     pk, pk_kind = peaks()
-    kept = run.kept_per_row() if (bounded_routing(wl) and wl.mode in ("causal", "bidir")) else None
-    roof = roofline_of(dom, wl, stage_ms[dom] * 1e-3, pk, kept)
-    roof_s, roof_parts = path_roofline_s(wl, pk, kept)
+    kept, dense = (run.kept_per_row() if (bounded_routing(wl) and wl.mode in ("causal", "bidir"))
+                   else (None, None))
+    roof = roofline_of(dom, wl, stage_ms[dom] * 1e-3, pk, kept, dense)
+    roof_s, roof_parts = path_roofline_s(wl, pk, kept, dense)
 
     # end to end through the plain public entry point: pinned host inputs in, result out, every step
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -793,7 +815,7 @@ def main():
                          if roof["bound"] == "alu" else pk_kind},
             "path_roofline": {"tokens_per_s": tokens / roof_s, "frac": value / world / (tokens / roof_s),
                               **{k2.replace("_s", "_ms"): v2 * 1e3 for k2, v2 in roof_parts.items()},
-                              "kept_components_per_row": kept},
+                              "kept_components_per_row": kept, "dense_row_fraction": dense},
             "stages_ms": stage_ms,
             "gpu_launches": len(names) * args.steps,
             "clocks": clocks_summary,

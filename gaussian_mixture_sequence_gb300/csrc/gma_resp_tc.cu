@@ -872,36 +872,40 @@ __global__ void __launch_bounds__(kDThreads, 2)
 // Expanding the square, the log-joint of the GMA explainer's posterior is
 //   l_ik = c'_k + sum_d ( -1/2 a_kd x_id^2 + a_kd mu_kd x_id ),   a = 1/sigma^2,
 // one product of [x^2 | x] (128 rows x 128) with W^T (128 x 128 components) per tile.
-// Each fp32 operand is held as three bf16 planes, v = v0 + v1 + v2 up to 2^-24 |v| (split3),
-// and the six plane products whose orders add up to at most two are accumulated in fp32,
-// smallest first (A2 W0, A1 W1, A1 W0, A0 W2, A0 W1, A0 W0); each of the three dropped ones
-// is below 2^-24 of its term.  So every log-joint carries the rounding of an fp32
-// evaluation of the expanded form: a few fp32 units of
+// Each fp32 operand is held as three bf16 planes, v = v0 + v1 + v2 up to 2^-24 |v| (each
+// plane the round-to-nearest of what the previous ones leave), and the six plane products
+// whose orders add up to at most two are accumulated in fp32, smallest first (A2 W0, A1 W1,
+// A1 W0, A0 W2, A0 W1, A0 W0); each of the three dropped ones is below 2^-24 of its term.
+// So every log-joint carries the rounding of an fp32 evaluation of the expanded form: a few
+// fp32 units of
 //   S_i = 1/2 A sum_d x_id^2 + M sum_d |x_id|   (A = max a, M = max |a mu| over the head),
 // which bounds the sum of the terms' magnitudes.  The direct form (x - mu)^2 / sigma^2 of
 // the exact kernels rounds at the scale of the log-joint itself, which on the rows these
 // tiles hold (many components near the best one) is of the same order.  A tile with a row
 // whose S_i exceeds kTSMax (|x| large against the components) goes on a second list, to
 // the exact dense kernel; every other row's posteriors are the softmax of these log-joints.
+// With bf16 routing rows the values are one plane and their squares two, and the products
+// of the planes that are zero are skipped.
 //
 // One persistent CTA of 16 warps per SM over a contiguous range of the listed tiles in head
 // order (the head's three planes, 96 KB, are loaded once per head).  Warp w owns TMEM lanes
 // 32 (w % 4) .. + 31 (rows of the tile) and column quarter q = w / 4: operand positions
 // 32 q .. 32 q + 31 (the squares, then the values, of features 16 q .. + 15; dtc_pos) and
-// components 32 q .. + 31 of the result.  Item n: the warps turn the landed routing tile
-// into the operand planes in TMEM; one thread issues the 48 MMAs into accumulator n % 2 and
-// fetches the next routing tile; then the warps take the softmax of item n - 1 from the
-// other accumulator while item n's products run.
+// components 32 q .. + 31 of the result.  The operand planes are double-buffered in TMEM
+// and the accumulator is read out before the next products are issued, so the products of
+// item n + 1 run while the warps take the softmax of item n and split the routing tile of
+// item n + 2; two CTA barriers per item.
 constexpr int kTThreads = 512;
 constexpr float kTSMax = 4096.f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct DenseTcSmem {
     static constexpr uint32_t W3 = kPrunedW3Bytes;      // three planes of W, SW128 K-major
     static constexpr uint32_t X = kPRows * kPD * 4;     // routing tile (fp32 worst case)
     static constexpr uint32_t O = kPRows * kPK * 4;     // output tile (fp32 worst case)
     static constexpr uint32_t C = 2 * kPrunedCBytes;    // c, c', A, M of two heads
-    static constexpr uint32_t EX = 2 * 4 * kPRows * 4;  // per quarter: row maxima, row sums
-    static constexpr uint32_t SS = 2 * 4 * kPRows * 4;  // per quarter: parts of S_i of two items
+    static constexpr uint32_t EX = 4 * kPRows * 8;      // per quarter and row: (max, sum)
+    static constexpr uint32_t SS = 2 * 4 * kPRows * 8;  // per item of two, quarter, row: (sum x^2, sum |x|)
     static constexpr size_t bytes = 1024 + (size_t)W3 + X + O + C + EX + SS + 64;
 };
 static_assert(DenseTcSmem::bytes <= 232448, "dense tensor-core routing: shared memory above the per-block limit");
@@ -909,6 +913,21 @@ static_assert(DenseTcSmem::bytes <= 232448, "dense tensor-core routing: shared m
 struct DenseTcMaps {
     CUtensorMap x[2], g[2], glo[2];   // per source: routing rows, output (hi plane), lo plane
 };
+
+// The three bf16 planes of a pair of values, packed two per word (the first value in the
+// low half): each plane the round-to-nearest of what the previous ones leave.
+__device__ __forceinline__ void split3_pair(float2 v, uint32_t &p0, uint32_t &p1, uint32_t &p2)
+{
+    const float2 m1 = make_float2(-1.f, -1.f);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+    p0 = *reinterpret_cast<const uint32_t *>(&b);
+    v = __ffma2_rn(make_float2(__uint_as_float(p0 << 16), __uint_as_float(p0 & 0xffff0000u)), m1, v);
+    b = __floats2bfloat162_rn(v.x, v.y);
+    p1 = *reinterpret_cast<const uint32_t *>(&b);
+    v = __ffma2_rn(make_float2(__uint_as_float(p1 << 16), __uint_as_float(p1 & 0xffff0000u)), m1, v);
+    b = __floats2bfloat162_rn(v.x, v.y);
+    p2 = *reinterpret_cast<const uint32_t *>(&b);
+}
 
 __global__ void __launch_bounds__(kTThreads, 1)
     k_resp_dense_tc(const __grid_constant__ DenseTcMaps maps, bool x_bf16, int H,
@@ -920,6 +939,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     __shared__ unsigned int s_red[kTThreads / 32];
+    __shared__ float2 am_s[2];   // A, M of the heads in the two constants' buffers
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, cq = warp >> 2;
     const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
@@ -953,23 +973,110 @@ __global__ void __launch_bounds__(kTThreads, 1)
     unsigned char *w_s = sm;
     unsigned char *xb = w_s + DenseTcSmem::W3;
     unsigned char *ob = xb + DenseTcSmem::X;
-    float *c_s = reinterpret_cast<float *>(ob + DenseTcSmem::O);   // [2][4][128]
-    float *mx_s = c_s + 2 * 4 * kPK;                                // [4][128] row maxima per quarter
-    float *sx_s = mx_s + 4 * kPRows;                                // [4][128] row sums per quarter
-    float *ss_s = sx_s + 4 * kPRows;                                // [2][4][128] parts of S_i
+    float *c_s = reinterpret_cast<float *>(ob + DenseTcSmem::O);                // [2][4][128]
+    float2 *ex_s = reinterpret_cast<float2 *>(c_s + 2 * 4 * kPK);               // [4][128]
+    float2 *ss_s = ex_s + 4 * kPRows;                                           // [2][4][128]
     uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 2 * 4 * kPRows);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
-    const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1);
-    auto bar_m = [&](int b) { return smem_addr(bar + 2 + b); };
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2);
     const uint32_t xbytes = kPRows * kPD * (x_bf16 ? 2 : 4);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kPRows * kPK * 2;   // split: the lo plane's tile follows the hi plane's
+    constexpr uint32_t D_COL = 384;             // the accumulator; operand planes at 192 b + 64 j
+    uint32_t tbase = 0;                         // TMEM base, once allocated
     auto load_x = [&](int2 e) {                 // one thread
         const int s = e.x >> 30, bh = e.x & 0x3fffffff;
         mbar_expect_tx(BAR_X, xbytes);
         tma_load_3d(smem_addr(xb), &maps.x[s], 0, e.y * kPRows, bh, BAR_X);
         if (!x_bf16) tma_load_3d(smem_addr(xb + kPRows * 128), &maps.x[s], 32, e.y * kPRows, bh, BAR_X);
+    };
+    int nimg = 0;
+    // the planes of W and the constants of `head` into buffer `buf` (every thread; no
+    // products may be running)
+    auto load_head = [&](int head, int buf) {
+        if (tid == 0) {
+            fence_proxy_async();   // earlier thread reads of the constants' buffer come first
+            mbar_expect_tx(BAR_I, (uint32_t)(kPrunedW3Bytes + kPrunedCBytes));
+            bulk_g2s(smem_addr(w_s), w3img + (long long)head * kPrunedW3Bytes, kPrunedW3Bytes, BAR_I);
+            bulk_g2s(smem_addr(c_s + buf * 4 * kPK), cimg + (long long)head * 4 * kPK, kPrunedCBytes, BAR_I);
+        }
+        const bool got = mbar_wait(BAR_I, (uint32_t)(nimg & 1));
+        ++nimg;
+        if (warp == 0) {   // the head-wide maxima of the per-component A_k, M_k
+            float a = 0.f, m = 0.f;
+#pragma unroll
+            for (int q = 0; q < kPK / 32; ++q) {
+                a = fmaxf(a, c_s[buf * 4 * kPK + 2 * kPK + lane + 32 * q]);
+                m = fmaxf(m, c_s[buf * 4 * kPK + 3 * kPK + lane + 32 * q]);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            }
+            if (lane == 0) am_s[buf] = make_float2(a, m);
+        }
+        return got;
+    };
+    // item n's landed routing tile into operand buffer n % 2, and its rows' sums for S_i
+    auto convert = [&](int n) {
+        float2 xv[8];
+        if (x_bf16) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kPRows, 2));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    xv[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kPRows, 4));
+                xv[2 * g] = make_float2(u.x, u.y);
+                xv[2 * g + 1] = make_float2(u.z, u.w);
+            }
+        }
+        uint32_t pw[3][16];
+        float2 s2 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float2 q = __fmul2_rn(xv[c], xv[c]);
+            s2 = __fadd2_rn(s2, q);
+            s1 = __fadd2_rn(s1, make_float2(fabsf(xv[c].x), fabsf(xv[c].y)));
+            split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
+            split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
+        }
+        const uint32_t acol = 192u * (uint32_t)(n & 1) + 16u * (uint32_t)cq;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, acol + 64 * j), pw[j]);
+        ss_s[(n & 1) * 4 * kPRows + cq * kPRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
+        tmem_wait_st();
+    };
+    // one thread: item n's products (operand buffer n % 2) into the accumulator, smallest
+    // first; with bf16 rows the values' higher planes and the squares' third plane are zero
+    const uint32_t id = idesc(128, kPK, kFmtBF16);
+    auto issue = [&](int n) {
+        const uint32_t ab = 192u * (uint32_t)(n & 1);
+        bool first = true;
+#pragma unroll
+        for (int q = 0; q < 6; ++q) {
+            const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                // A plane
+            const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);    // W plane
+            if (x_bf16 && pa == 2) continue;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                if (x_bf16 && pa == 1 && (kk & 1)) continue;   // odd K steps: the values
+                const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+                const uint32_t boff = pb * (uint32_t)kPrunedWBytes + (kb >> 7) * (kPK * 128) + (kb & 127);
+                mma_ts(0u, tbase + D_COL, tbase + ab + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
+                       first ? 0u : 1u);
+                first = false;
+            }
+        }
+        mma_commit(BAR_M);
     };
 
     if (warp == 0) {
@@ -979,215 +1086,191 @@ __global__ void __launch_bounds__(kTThreads, 1)
     int hcur = 0;
     int2 ecur = entry_at(g0, hcur);
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         load_x(ecur);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tbase = *tslot;   // operand planes at columns 0, 64, 128; accumulators at 256, 384
-    const uint32_t id = idesc(128, kPK, kFmtBF16);
-    bool ok = true;
-    int head = -1, hp = 1, nimg = 0;   // the loaded head and the buffer of its constants
-    float amax = 0.f, mmax = 0.f;      // its A and M
-    int2 eprev = ecur;                 // the previous item: entry, head, constants' buffer
-    int hprev = 0, hpprev = 0;
-    int m_last = -1;                   // tid 0: the last item whose products were issued,
-    bool x_pending = true;             // and whether a routing tile is in flight
+    tbase = *tslot;
+    bool ok = load_head(hcur, 0);
+    int hp = 0;                        // constants' buffer of item n's head
+    bool x_pending = true;             // tid 0: a routing tile in flight, and its phase
     uint32_t x_par = 0;
-
-    // softmax of item m (its products were committed to accumulator m % 2): the posteriors
-    // into the output tile and out by TMA stores, or the tile onto the exact kernel's list
-    auto epilogue = [&](int m, int2 e, int h, int hpx) {
-        ok = mbar_wait(bar_m(m & 1), (uint32_t)((m >> 1) & 1)) && ok;
-        fence_after_sync();
-        uint32_t r[2][16];
-        const uint32_t dcol = 256u + 128u * (uint32_t)(m & 1) + 32u * (uint32_t)cq;
-        tmem_ld16(tmem_at(tbase, 32 * qd, dcol), r[0]);
-        tmem_ld16(tmem_at(tbase, 32 * qd, dcol + 16), r[1]);
-        tmem_wait_ld();
+    int m_issued = -1;                 // tid 0: the last item whose products were issued
+    {   // item 0: its operand planes, then its products and the next routing tile
+        const bool landed = mbar_wait(BAR_X, 0u);
+        ok = landed && ok;
+        if (tid == 0 && landed) x_pending = false;
+        convert(0);
         fence_before_sync();
-        const float *cp = c_s + hpx * 4 * kPK + kPK + 32 * cq;   // c'_k
-        float l[32], mloc = -FLT_MAX;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            l[j] = __uint_as_float(r[j >> 4][j & 15]) + cp[j];
-            mloc = fmaxf(mloc, l[j]);
+        ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, am_s is written
+        fence_after_sync();
+    }
+    int2 enext = ecur;
+    int hnext = hcur;
+    if (cnt > 1) enext = entry_at(g0 + 1, hnext);
+    if (tid == 0 && ok) {
+        issue(0);
+        m_issued = 0;
+        if (cnt > 1) {
+            load_x(enext);
+            x_pending = true;
+            x_par = 1u;
         }
-        mx_s[cq * kPRows + i] = mloc;
-        if (tid == 0) bulk_wait_read();   // the previous output tile has left shared memory
-        __syncthreads();
-        const float mrow = fmaxf(fmaxf(mx_s[i], mx_s[kPRows + i]), fmaxf(mx_s[2 * kPRows + i], mx_s[3 * kPRows + i]));
-        float sloc = 0.f;
+    }
+
+    float2 acc[16];                    // the accumulator row of the previous item, 32 components
+    int2 eprev = ecur;                 // the previous item: entry, head, constants' buffer
+    int hprev = hcur, hpprev = hp;
+    bool rel_prev = false;             // whether the previous item goes to the exact kernel
+
+    // softmax of the previous item from acc: posteriors into the output tile unless a row is
+    // beyond the magnitude limit; returns whether the item goes to the exact kernel
+    auto softmax = [&](int m, int hpx) {
+        const float2 *cp = reinterpret_cast<const float2 *>(c_s + hpx * 4 * kPK + kPK + 32 * cq);   // c'_k
+        float mq = -FLT_MAX;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            l[j] = expf(l[j] - mrow);
-            sloc += l[j];
+        for (int p = 0; p < 16; ++p) {
+            acc[p] = __fadd2_rn(acc[p], cp[p]);
+            mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
         }
-        sx_s[cq * kPRows + i] = sloc;
-        const float *sp = ss_s + (m & 1) * 4 * kPRows;
-        const bool far = (sp[i] + sp[kPRows + i]) + (sp[2 * kPRows + i] + sp[3 * kPRows + i]) > kTSMax;
+        const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kLog2e, kLog2e);
+        float2 sq2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+            const float2 t = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
+            acc[p] = make_float2(exp2f(t.x), exp2f(t.y));
+            sq2 = __fadd2_rn(sq2, acc[p]);
+        }
+        ex_s[cq * kPRows + i] = make_float2(mq, sq2.x + sq2.y);
+        const float2 *sp = ss_s + (m & 1) * 4 * kPRows + i;
+        const float2 am = am_s[hpx];
+        const float sx2 = (sp[0].x + sp[kPRows].x) + (sp[2 * kPRows].x + sp[3 * kPRows].x);
+        const float sx1 = (sp[0].y + sp[kPRows].y) + (sp[2 * kPRows].y + sp[3 * kPRows].y);
+        const bool far = fmaf(0.5f * am.x, sx2, am.y * sx1) > kTSMax;
+        if (tid == 0) bulk_wait_read();   // the output tile of the item before has left shared memory
         const bool relist = __syncthreads_or(far) != 0;
         if (!relist) {
-            const float inv = 1.0f / ((sx_s[i] + sx_s[kPRows + i]) + (sx_s[2 * kPRows + i] + sx_s[3 * kPRows + i]));
+            // merge the four quarters' (max, sum): the row's max, and this quarter's scale
+            float2 e4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kPRows + i];
+            const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+            float tot = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, exp2f((e4[q].x - mrow) * kLog2e), tot);
+            const float sc = exp2f((mq - mrow) * kLog2e) / tot;
+            const float2 sc2 = make_float2(sc, sc);
             if (g_f32) {
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
+                for (int g = 0; g < 8; ++g) {
+                    const float2 a = __fmul2_rn(acc[2 * g], sc2), b = __fmul2_rn(acc[2 * g + 1], sc2);
                     *reinterpret_cast<float4 *>(ob + sw128_offset(i, 32 * cq + 4 * g, kPRows, 4)) =
-                        make_float4(l[4 * g] * inv, l[4 * g + 1] * inv, l[4 * g + 2] * inv, l[4 * g + 3] * inv);
+                        make_float4(a.x, a.y, b.x, b.y);
+                }
             } else {
+                const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        __nv_bfloat16 h0, l0, h1, l1;
-                        split_bf16(l[8 * g + 2 * u] * inv, h0, l0);
-                        split_bf16(l[8 * g + 2 * u + 1] * inv, h1, l1);
-                        hw[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                        lw[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                        const float2 v = __fmul2_rn(acc[4 * g + u], sc2);
+                        __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                        hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                        const float2 r = __ffma2_rn(
+                            make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
+                        b = __floats2bfloat162_rn(r.x, r.y);
+                        lw[u] = *reinterpret_cast<const uint32_t *>(&b);
                     }
                     const uint32_t off = sw128_offset(i, 32 * cq + 8 * g, kPRows, 2);
                     *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
+            fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
         }
-        fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
-        const bool all_ok = __syncthreads_and(ok) != 0;
-        if (tid == 0 && all_ok) {
-            if (relist) {
-                dlist2[(long long)h * dcap + atomicAdd(dctl + H + h, 1u)] = e;
-            } else {
-                const int s = e.x >> 30, bh = e.x & 0x3fffffff;
-                for (int a = 0; a < kPK * ge / 128; ++a) {
-                    tma_store_3d(&maps.g[s], a * (128 / ge), e.y * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
-                    if (g_split)
-                        tma_store_3d(&maps.glo[s], a * (128 / ge), e.y * kPRows, bh,
-                                     smem_addr(ob + LO + a * (kPRows * 128)));
-                }
-                bulk_commit();
+        return relist;
+    };
+    // one thread, after a CTA barrier that follows the softmax: the previous item's output
+    // tile out by TMA stores, or the item onto the exact kernel's list
+    auto finish = [&](int2 e, int h, bool relist) {
+        if (relist) {
+            dlist2[(long long)h * dcap + atomicAdd(dctl + H + h, 1u)] = e;
+        } else {
+            const int s = e.x >> 30, bh = e.x & 0x3fffffff;
+            for (int a = 0; a < kPK * ge / 128; ++a) {
+                tma_store_3d(&maps.g[s], a * (128 / ge), e.y * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
+                if (g_split)
+                    tma_store_3d(&maps.glo[s], a * (128 / ge), e.y * kPRows, bh,
+                                 smem_addr(ob + LO + a * (kPRows * 128)));
             }
+            bulk_commit();
         }
     };
 
-    for (int n = 0; n <= cnt; ++n) {
-        int2 enext = ecur;
-        int hnext = hcur, hp_n = hp;
-        if (n < cnt) {
-            // the products of item n - 1 are done: the operand planes and W may be replaced
-            if (n >= 1) ok = mbar_wait(bar_m((n - 1) & 1), (uint32_t)(((n - 1) >> 1) & 1)) && ok;
-            if (hcur != head) {
-                head = hcur;
-                hp ^= 1;   // the previous head's constants stay for item n - 1's softmax
-                if (tid == 0) {
-                    fence_proxy_async();   // earlier thread reads of the constants' buffer come first
-                    mbar_expect_tx(BAR_I, (uint32_t)(kPrunedW3Bytes + kPrunedCBytes));
-                    bulk_g2s(smem_addr(w_s), w3img + (long long)head * kPrunedW3Bytes, kPrunedW3Bytes, BAR_I);
-                    bulk_g2s(smem_addr(c_s + hp * 4 * kPK), cimg + (long long)head * 4 * kPK, kPrunedCBytes, BAR_I);
-                }
-                ok = mbar_wait(BAR_I, (uint32_t)(nimg & 1)) && ok;
-                ++nimg;
-                float a = 0.f, mm = 0.f;
-#pragma unroll
-                for (int q = 0; q < kPK / 32; ++q) {
-                    a = fmaxf(a, c_s[hp * 4 * kPK + 2 * kPK + lane + 32 * q]);
-                    mm = fmaxf(mm, c_s[hp * 4 * kPK + 3 * kPK + lane + 32 * q]);
-                }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) {
-                    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-                    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-                }
-                amax = a;
-                mmax = mm;
-            }
-            hp_n = hp;
-            const bool landed = mbar_wait(BAR_X, (uint32_t)(n & 1));
+    for (int n = 0; n < cnt && ok; ++n) {
+        // item n's products are running; acc holds item n - 1's accumulator row
+        if (n >= 1) rel_prev = softmax(n - 1, hpprev);
+        if (n + 1 < cnt) {   // item n + 1's routing tile into the other operand buffer
+            const bool landed = mbar_wait(BAR_X, (uint32_t)((n + 1) & 1));
             ok = landed && ok;
             if (tid == 0 && landed) x_pending = false;
-            // features 16 cq .. + 15 of row i: squares and values into the three planes
-            float xv[16];
-            if (x_bf16) {
+            convert(n + 1);
+        }
+        // item n's accumulator row into registers (it is free for item n + 1's products after
+        // the barrier below)
+        ok = mbar_wait(BAR_M, (uint32_t)(n & 1)) && ok;
+        fence_after_sync();
+        {
+            uint32_t r[2][16];
+            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 32 * cq), r[0]);
+            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 32 * cq + 16), r[1]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kPRows, 2));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        xv[8 * g + 2 * e] = __uint_as_float(w[e] << 16);
-                        xv[8 * g + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kPRows, 4));
-                    xv[4 * g] = u.x;
-                    xv[4 * g + 1] = u.y;
-                    xv[4 * g + 2] = u.z;
-                    xv[4 * g + 3] = u.w;
-                }
+            for (int p = 0; p < 16; ++p)
+                acc[p] = make_float2(__uint_as_float(r[p >> 3][2 * (p & 7)]), __uint_as_float(r[p >> 3][2 * (p & 7) + 1]));
+        }
+        const int2 en = ecur;
+        const int hn = hcur, hpn = hp;
+        int2 e2 = enext;
+        int h2 = hnext;
+        if (n + 1 < cnt) {
+            if (hnext != hcur) {   // item n + 1 is of another head (item n's products are done)
+                hp ^= 1;           // the constants of item n's head stay for its softmax
+                ok = load_head(hnext, hp) && ok;
             }
-            uint32_t pw[3][16];
-            float s2 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float v0 = xv[2 * c], v1 = xv[2 * c + 1];
-                const float q0 = v0 * v0, q1 = v1 * v1;
-                s2 += q0 + q1;
-                s1 += fabsf(v0) + fabsf(v1);
-                unsigned short a0[3], a1[3], b0[3], b1[3];
-                split3(q0, a0);
-                split3(q1, a1);
-                split3(v0, b0);
-                split3(v1, b1);
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    pw[j][c] = (uint32_t)a0[j] | ((uint32_t)a1[j] << 16);
-                    pw[j][8 + c] = (uint32_t)b0[j] | ((uint32_t)b1[j] << 16);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
-            ss_s[(n & 1) * 4 * kPRows + cq * kPRows + i] = fmaf(0.5f * amax, s2, mmax * s1);
-            tmem_wait_st();
-            fence_before_sync();
-            __syncthreads();   // the planes are in TMEM and the routing tile has been read
-            fence_after_sync();
-            if (n + 1 < cnt) enext = entry_at(g0 + n + 1, hnext);
-            if (tid == 0 && ok) {
-                const uint32_t d = tbase + 256u + 128u * (uint32_t)(n & 1);
-#pragma unroll
-                for (int q = 0; q < 6; ++q) {
-                    const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                 // A plane
-                    const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);     // W plane
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
-                        const uint32_t boff = pb * (uint32_t)kPrunedWBytes + (kb >> 7) * (kPK * 128) + (kb & 127);
-                        mma_ts(0u, d, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
-                               (q | kk) ? 1u : 0u);
-                    }
-                }
-                mma_commit(bar_m(n & 1));
-                m_last = n;
-                if (n + 1 < cnt) {   // (the tile was only read by threads: no proxy fence)
-                    load_x(enext);
+            if (n + 2 < cnt) e2 = entry_at(g0 + n + 2, h2);
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(ok) != 0;   // operand planes written, accumulator read, softmax done
+        fence_after_sync();
+        if (tid == 0 && ok) {
+            if (n >= 1) finish(eprev, hprev, rel_prev);
+            if (n + 1 < cnt) {
+                issue(n + 1);
+                m_issued = n + 1;
+                if (n + 2 < cnt) {   // (the tile was only read by threads: no proxy fence)
+                    load_x(e2);
                     x_pending = true;
-                    x_par = (uint32_t)((n + 1) & 1);
+                    x_par = (uint32_t)((n + 2) & 1);
                 }
             }
         }
-        if (n >= 1) epilogue(n - 1, eprev, hprev, hpprev);
-        eprev = ecur;
-        hprev = hcur;
-        hpprev = hp_n;
+        eprev = en;
+        hprev = hn;
+        hpprev = hpn;
         ecur = enext;
         hcur = hnext;
-        ok = __syncthreads_and(ok) != 0;   // every thread leaves the loop together
-        if (!ok) break;
+        enext = e2;
+        hnext = h2;
+    }
+    if (ok) {   // the last item's softmax and output
+        rel_prev = softmax(cnt - 1, hpprev);
+        ok = __syncthreads_and(ok) != 0;
+        if (tid == 0 && ok) finish(eprev, hprev, rel_prev);
     }
     // after a failed wait a routing tile or products may still be in flight: let them finish
     // (bounded) before TMEM and shared memory are released
@@ -1195,7 +1278,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (tid == 0) {
         if (!ok) {
             if (x_pending) ok_end = mbar_wait(BAR_X, x_par) && ok_end;
-            if (m_last >= 0) ok_end = mbar_wait(bar_m(m_last & 1), (uint32_t)((m_last >> 1) & 1)) && ok_end;
+            if (m_issued >= 0) ok_end = mbar_wait(BAR_M, (uint32_t)(m_issued & 1)) && ok_end;
         }
         bulk_wait_all();
     }
@@ -1203,7 +1286,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
-
 } // namespace
 
 bool resp_pruned_applies(const Dims &dm) { return dm.K == kPK && dm.D == kPD; }

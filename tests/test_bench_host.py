@@ -99,6 +99,24 @@ def test_bounded_routing_roofline():
     assert g["bound"] == "alu" and g["algorithmic_flop"] == 4 * 256 * 64 * 4 * 8 * 8192
 
 
+def test_dense_pass_roofline():
+    """The dense pass is tensor work: six bf16 passes of the [x^2 | x] W^T product (4 K d
+    flop per row each; four with bf16 rows) over both routings' rows in dense tiles; the
+    rows it takes carry no FP32 exact work in the bounded routing launches."""
+    pk = dict(bench.FALLBACK)
+    wl, wb = W["causal_4k"], W["causal_64k_bf16"]
+    ht = wl.B * wl.H * wl.N
+    r = bench.roofline_of("resp_dense", wl, 70e-6, pk, kept=3.0, dense=1.0)
+    assert r["bound"] == "tensor" and r["algorithmic_flop"] == 2 * 6 * 4 * 128 * 64 * ht
+    assert r["algorithmic_bytes"] == 0                # the routing rows are charged to resp_q / resp_k
+    rb = bench.roofline_of("resp_dense", wb, 390e-6, pk, kept=3.0, dense=0.5)
+    assert rb["algorithmic_flop"] == 0.5 * 2 * 4 * 4 * 128 * 64 * wb.B * wb.H * wb.N
+    q = bench.roofline_of("resp_q", wl, 33e-6, pk, kept=3.0, dense=1.0)
+    assert q["bound"] == "hbm" and q["algorithmic_bytes"] == ht * 64 * 4
+    t, parts = bench.path_roofline_s(wl, pk, kept=3.0, dense=1.0)
+    assert parts["alu_s"] == 0.0 and parts["mma_s"] > 0.0
+
+
 def test_decode_bytes_per_launch():
     wl = W["decode_b256"]
     bh = wl.B * wl.H
