@@ -480,13 +480,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *reinterpret_cast<float *>(ob + sw128_offset(i, 64 * hf + a1, kPRows, 4)) = 1.0f;
             }
             uint32_t xm0 = 0u, xm1 = 0u;   // the kept components of rows that need the softmax
-            // per 32-component word: the union of the warp's kept sets, whether its lanes walk
-            // their own sets, and the parameters of the union's first component (read here, so
-            // that the read overlaps the group barrier below)
-            uint32_t uni[2] = {0u, 0u};
-            bool lanes[2] = {true, true};
-            float4 wpre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-            if (__any_sync(0xffffffffu, !single)) {   // tcgen05.ld is warp-collective: the whole warp reloads
+            const bool any_multi = __any_sync(0xffffffffu, !single);
+            if (any_multi) {   // tcgen05.ld is warp-collective: the whole warp reloads
                 uint32_t mk[2] = {0u, 0u};
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
@@ -500,13 +495,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     xm0 = mk[0];
                     xm1 = mk[1];
                 }
-#pragma unroll
-                for (int wd = 0; wd < 2; ++wd) {
-                    const uint32_t m = wd ? xm1 : xm0;
-                    uni[wd] = __reduce_or_sync(0xffffffffu, m);
-                    lanes[wd] = 16 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(m)) <= (uint32_t)__popc(uni[wd]);
-                    if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
-                }
             }
             // a tile where many rows keep many components goes to the dense passes (every
             // component of every row on the tensor cores, k_resp_dense_tc, and rows of large
@@ -515,6 +503,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (group_popc(grp, __popc(xm0) + __popc(xm1) >= kDenseKept) >= kDenseRows) {
                 if (gt == 0) dlist[(long long)head * dcap + atomicAdd(dctl + head, 1u)] = make_int2(bh | (src << 30), t);
                 continue;   // no exact pass and no output tile here
+            }
+            // per 32-component word: the union of the warp's kept sets, whether its lanes walk
+            // their own sets, and the parameters of the union's first component (read here, so
+            // that the read overlaps the group barrier below)
+            uint32_t uni[2] = {0u, 0u};
+            bool lanes[2] = {true, true};
+            float4 wpre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+            if (any_multi) {
+#pragma unroll
+                for (int wd = 0; wd < 2; ++wd) {
+                    const uint32_t m = wd ? xm1 : xm0;
+                    uni[wd] = __reduce_or_sync(0xffffffffu, m);
+                    lanes[wd] = 16 * __reduce_max_sync(0xffffffffu, (uint32_t)__popc(m)) <= (uint32_t)__popc(uni[wd]);
+                    if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
+                }
             }
             if (group_or(grp, (xm0 | xm1) != 0u)) {
                 // exact log-joint of a component for this lane's row (parameters from global
@@ -914,6 +917,14 @@ struct DenseTcMaps {
     CUtensorMap x[2], g[2], glo[2];   // per source: routing rows, output (hi plane), lo plane
 };
 
+// 2^t by the SFU's base-2 exponential (relative error about 2^-22; 0 for t below -126).
+__device__ __forceinline__ float ex2_sfu(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
 // The three bf16 planes of a pair of values, packed two per word (the first value in the
 // low half): each plane the round-to-nearest of what the previous ones leave.
 __device__ __forceinline__ void split3_pair(float2 v, uint32_t &p0, uint32_t &p1, uint32_t &p2)
@@ -1141,7 +1152,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
         for (int p = 0; p < 16; ++p) {
             const float2 t = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
-            acc[p] = make_float2(exp2f(t.x), exp2f(t.y));
+            acc[p] = make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
             sq2 = __fadd2_rn(sq2, acc[p]);
         }
         ex_s[cq * kPRows + i] = make_float2(mq, sq2.x + sq2.y);
@@ -1160,8 +1171,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
             float tot = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, exp2f((e4[q].x - mrow) * kLog2e), tot);
-            const float sc = exp2f((mq - mrow) * kLog2e) / tot;
+            for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kLog2e), tot);
+            const float sc = ex2_sfu((mq - mrow) * kLog2e) / tot;
             const float2 sc2 = make_float2(sc, sc);
             if (g_f32) {
 #pragma unroll
