@@ -81,7 +81,9 @@ def stage_work(stage, wl):
     (flop):
       resp_q / resp_k     4*K*d on the FP32 pipe (one fp32x2 FMA for (x-mu)/sigma
                           and one for the square-accumulate, per component and
-                          feature pair)
+                          feature pair); for 17 <= K <= 64 and d = 64, the six (four
+                          with bf16 rows) bf16 passes of [x^2 | x] W^T, K_N = 32 or
+                          64 wide, on the tensor pipe
       resp_dense          24*K*d on the bf16 tensor pipe per row of the tiles the
                           bounded routings leave to the dense pass (K = 128, d = 64;
                           six passes of the three-plane product [x^2 | x] W^T, of
@@ -120,7 +122,12 @@ def stage_work(stage, wl):
     nblk = wl.B * wl.H * -(-wl.N // blk)
     if stage in ("resp_q", "resp_k"):
         # K = 128, d = 64: the bound GEMM [x^2 | x] W has the same 4*K*d flop per row and runs on the
-        # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work
+        # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work.
+        # 17 <= K <= 64, d = 64: every log-joint on the tensor pipe, the dense pass's bf16 passes of a
+        # product K_N wide (K rounded up to 32 or 64)
+        if tc_routing(wl):
+            kn = 32 if K <= 32 else 64
+            return dense_passes(wl) * 4.0 * kn * d * ht, "tensor_bf16", (d * xb + K * gb) * ht
         pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
         return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
     if stage == "resp_dense":
@@ -193,7 +200,7 @@ def algorithmic_work(stage, wl, kept=None, dense=None):
     if wl.mode == "backward":
         return backward_work(wl)
     flop, pipe, _ = stage_work(stage, wl)
-    if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k", "resp_dense"):
+    if pipe == "tensor_bf16" and stage not in ("resp_q", "resp_k", "resp_dense"):   # routing: bf16 passes
         pipe = "tensor"   # the chunk products at the rate of their operand type (tf32 for fp32)
     d, dv = wl.d, wl.dv
     xb = 2 if wl.x_dtype == "bf16" else 4
@@ -246,6 +253,12 @@ def bounded_routing(wl):
     return wl.K == 128 and wl.d == 64
 
 
+def tc_routing(wl):
+    """The library's tensor-core routing for 17 <= K <= 64 applies (d = 64; the rows of the
+    workspace layout are 128 wide on the chunked tensor-core path, K wide otherwise)."""
+    return wl.d == 64 and 17 <= wl.K <= 64
+
+
 def pipe_peak(pipe, wl, pk):
     """Peak of a pipe in flop/s: FP32 lanes x 2 x max SM clock, or the tensor
     rate of the product operands (tf32 = measured bf16 x 1.1/2.25 nominal ratio)."""
@@ -291,6 +304,9 @@ def path_roofline_s(wl, pk, kept=None, dense=None):
         dn = dense or 0.0
         t_alu = 2 * 2 * 4.0 * wl.d * kept * (1.0 - dn) * ht / fp32_peak   # Q and K rows, two exact passes
         t_mma += (8.0 + 8.0 * dense_passes(wl) * dn) * wl.K * wl.d * ht / (pk["bf16_tflops"] * 1e12)
+    elif tc_routing(wl):   # both routings on the tensor pipe
+        t_alu = 0.0
+        t_mma += 2 * stage_work("resp_q", wl)[0] / (pk["bf16_tflops"] * 1e12)
     else:
         t_alu = 8.0 * wl.K * wl.d * ht / fp32_peak
     return max(t_alu, t_hbm, t_mma), dict(alu_s=t_alu, hbm_s=t_hbm, mma_s=t_mma)

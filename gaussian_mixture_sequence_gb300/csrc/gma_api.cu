@@ -17,7 +17,8 @@ struct WsPlan {
     size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, wimg3 = 0, pimg = 0,
            cimg = 0, pimg2 = 0, dctl = 0, dlist = 0, dlist2 = 0, bytes = 0;
     long long dcap = 0;   // dense-list entries per head
-    bool pruned = false;
+    bool pruned = false;  // the bounded routing (K = 128, d = 64)
+    bool gtc = false;     // the tensor-core routing for 17 <= K <= 64, d = 64
 };
 
 bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }
@@ -111,6 +112,10 @@ WsPlan plan(const Dims &dm, gma_op op)
     p.cst = take((size_t)dm.H * dm.K * 4);
     if (op != GMA_OP_DECODE && resp_pruned_applies(dm))
         plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take);   // both routings of a head
+    if (op != GMA_OP_DECODE && resp_gtc_applies(dm)) {
+        p.gtc = true;
+        p.wimg3 = take(gtc_image_bytes(dm));
+    }
     if (op == GMA_OP_USAGE) {   // Gamma in fp32, then the per-block partial sums and counts
         p.gq = take((size_t)dm.BH() * dm.N * dm.K * 4);
         p.partial = take((size_t)dm.BH() * usage_blocks(dm) * dm.K * 4);
@@ -227,6 +232,10 @@ BwdPlan plan_bwd_full(const Dims &dm)
     p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
     p.cst = take((size_t)dm.H * dm.K * 4);
     if (resp_pruned_applies(dm)) plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take);
+    if (resp_gtc_applies(dm)) {
+        p.gtc = true;
+        p.wimg3 = take(gtc_image_bytes(dm));
+    }
     const size_t rows = (size_t)dm.BH() * dm.N, nb = (size_t)dm.BH() * dm.nblk();
     p.gq = take(rows * dm.KP * 4);
     p.gk = take(rows * dm.KP * 4);
@@ -250,6 +259,22 @@ PrunedImages images(void *ws, const WsPlan &wp)
     return PrunedImages{at<unsigned char>(ws, wp.wimg), at<unsigned char>(ws, wp.wimg3), at<float4>(ws, wp.pimg),
                         at<float>(ws, wp.cimg), at<float4>(ws, wp.pimg2), at<unsigned int>(ws, wp.dctl),
                         at<int2>(ws, wp.dlist), at<int2>(ws, wp.dlist2), wp.dcap};
+}
+
+// The routing images a call passes to launch_resp (null for the generic CUDA-core routing).
+const PrunedImages *routing_images(const WsPlan &wp, const PrunedImages &img)
+{
+    return wp.pruned || wp.gtc ? &img : nullptr;
+}
+
+// The per-head parameters and the images of the routing kernel the shape takes.
+cudaError_t prep_routing(const Dims &dm, const gma_params &params, float4 *prm, float *cst, const WsPlan &wp,
+                         const PrunedImages &img, cudaStream_t st)
+{
+    if (wp.pruned) return launch_prep_all(dm, params, prm, cst, img, st);
+    cudaError_t e = launch_prep(dm, params, prm, cst, st);
+    if (e == cudaSuccess && wp.gtc) e = launch_prep_gtc(dm, prm, cst, img.w3, st);
+    return e;
 }
 
 } // namespace
@@ -300,9 +325,8 @@ gma_status gma_responsibilities(const gma_shape *shape, gma_params params, const
     float4 *prm = at<float4>(ws, wp.prm);
     float *cst = at<float>(ws, wp.cst);
     const PrunedImages img = images(ws, wp);
-    if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
-    else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st, 0));
+    GMA_CUDA(prep_routing(dm, params, prm, cst, wp, img, st));
+    GMA_CUDA(launch_resp(dm, prm, cst, routing_images(wp, img), x, gamma, dm.K, GL_F32, st, 0));
     if (wp.pruned) GMA_CUDA(launch_resp_dense(dm, x, gamma, dm, nullptr, nullptr, img, GL_F32, st));
     return GMA_OK;
 }
@@ -328,9 +352,8 @@ gma_status gma_responsibility_stats(const gma_shape *shape, gma_params params, c
         float4 *prm = at<float4>(ws, wp.prm);
         float *cst = at<float>(ws, wp.cst);
         const PrunedImages img = images(ws, wp);
-        if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
-        else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-        GMA_CUDA(launch_resp(dm, prm, cst, wp.pruned ? &img : nullptr, x, gamma, dm.K, GL_F32, st, 0));
+        GMA_CUDA(prep_routing(dm, params, prm, cst, wp, img, st));
+        GMA_CUDA(launch_resp(dm, prm, cst, routing_images(wp, img), x, gamma, dm.K, GL_F32, st, 0));
         if (wp.pruned) GMA_CUDA(launch_resp_dense(dm, x, gamma, dm, nullptr, nullptr, img, GL_F32, st));
     }
     GMA_CUDA(launch_usage(dm, gamma, dm.K, at<float>(ws, wp.partial), at<int>(ws, wp.total), assign, usage, counts,
@@ -396,19 +419,14 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
     void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
     const PrunedImages img = images(ws, wp);
-    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
-    if (wp.pruned) {
-        GMA_CUDA(mk.mark("prep"));
-        GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
-    } else {
-        GMA_CUDA(mk.mark("prep_params"));
-        GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    }
+    const PrunedImages *imgp = routing_images(wp, img);
+    GMA_CUDA(mk.mark(wp.pruned ? "prep" : "prep_params"));
+    GMA_CUDA(prep_routing(dm, params, prm, cst, wp, img, st));
     GMA_CUDA(mk.mark("resp_q"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KG, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KG, gamma_layout(dm), st, 1));
-    if (imgp) {
+    if (wp.pruned) {
         GMA_CUDA(mk.mark("resp_dense"));
         GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));
     }
@@ -445,6 +463,10 @@ WsPlan plan_cross(const Dims &dq, const Dims &dk)
     p.prm = take((size_t)dq.H * dq.K * (dq.D / 2) * 16);
     p.cst = take((size_t)dq.H * dq.K * 4);
     if (resp_pruned_applies(dq)) plan_pruned(p, dq.H, routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N), take);
+    if (resp_gtc_applies(dq)) {
+        p.gtc = true;
+        p.wimg3 = take(gtc_image_bytes(dq));
+    }
     const size_t gb = dq.g_bf16 ? 2 : 4;
     p.gq = take((size_t)dq.BH() * dq.N * dq.KG * gb);
     p.gk = take((size_t)dk.BH() * dk.N * dk.KG * gb);
@@ -484,12 +506,11 @@ gma_status run_cross(const gma_shape *shape, int n_kv, gma_params params, const 
     void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
     const PrunedImages img = images(ws, wp);
-    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
-    if (wp.pruned) GMA_CUDA(launch_prep_all(dq, params, prm, cst, img, st));
-    else GMA_CUDA(launch_prep(dq, params, prm, cst, st));
+    const PrunedImages *imgp = routing_images(wp, img);
+    GMA_CUDA(prep_routing(dq, params, prm, cst, wp, img, st));
     GMA_CUDA(launch_resp(dq, prm, cst, imgp, qx, gq, dq.KG, gamma_layout(dq), st, 0));
     if (dk.N > 0) GMA_CUDA(launch_resp(dk, prm, cst, imgp, kx, gk, dk.KG, gamma_layout(dk), st, 1));
-    if (imgp)
+    if (wp.pruned)
         GMA_CUDA(launch_resp_dense(dq, qx, gq, dk, dk.N > 0 ? kx : nullptr, gk, img, gamma_layout(dq), st));
     const bool tc = tc_path_applies(dq);
     if (dk.N == 0) {   // no keys: an empty memory (zeros in either layout)
@@ -572,19 +593,14 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
     void *gq = at<char>(ws, wp.gq), *gk = at<char>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial);
     const PrunedImages img = images(ws, wp);
-    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
-    if (wp.pruned) {
-        GMA_CUDA(mk.mark("prep"));
-        GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
-    } else {
-        GMA_CUDA(mk.mark("prep_params"));
-        GMA_CUDA(launch_prep(dm, params, prm, cst, st));
-    }
+    const PrunedImages *imgp = routing_images(wp, img);
+    GMA_CUDA(mk.mark(wp.pruned ? "prep" : "prep_params"));
+    GMA_CUDA(prep_routing(dm, params, prm, cst, wp, img, st));
     GMA_CUDA(mk.mark("resp_q"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KG, gamma_layout(dm), st, 0));
     GMA_CUDA(mk.mark("resp_k"));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KG, gamma_layout(dm), st, 1));
-    if (imgp) {
+    if (wp.pruned) {
         GMA_CUDA(mk.mark("resp_dense"));
         GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, gamma_layout(dm), st));
     }
@@ -890,13 +906,12 @@ extern "C" gma_status gma_backward(const gma_shape *shape, int causal, gma_param
     float *gq = at<float>(ws, wp.gq), *gk = at<float>(ws, wp.gk);
     float *partial = at<float>(ws, wp.partial), *total = at<float>(ws, wp.total);
     const PrunedImages img = images(ws, wp);
-    const PrunedImages *imgp = wp.pruned ? &img : nullptr;
+    const PrunedImages *imgp = routing_images(wp, img);
     // the forward's responsibilities (fp32) and memory
-    if (wp.pruned) GMA_CUDA(launch_prep_all(dm, params, prm, cst, img, st));
-    else GMA_CUDA(launch_prep(dm, params, prm, cst, st));
+    GMA_CUDA(prep_routing(dm, params, prm, cst, wp, img, st));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, qx, gq, dm.KP, GL_F32, st, 0));
     GMA_CUDA(launch_resp(dm, prm, cst, imgp, kx, gk, dm.KP, GL_F32, st, 1));
-    if (imgp) GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, GL_F32, st));
+    if (wp.pruned) GMA_CUDA(launch_resp_dense(dm, qx, gq, dm, kx, gk, img, GL_F32, st));
     GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
     GMA_CUDA(launch_scan(dm, partial, nullptr, causal ? nullptr : total, causal != 0, st));
     // query side, key / value side, then the routings and the parameters

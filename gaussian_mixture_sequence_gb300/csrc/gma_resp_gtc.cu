@@ -1,0 +1,502 @@
+// Responsibilities (S1) on the tensor cores for 17 <= K <= 64 components and
+// d_route = 64: every log-joint of every row, for any inputs.
+//
+// The posterior of the GMA explainer ("핵심 메커니즘": gamma_ik = p(z = k | x_i)
+// under the diagonal GMM) is a softmax over the log-joints
+//   l_ik = c_k - 1/2 sum_d ((x_id - mu_kd) / sigma_kd)^2
+//        = c'_k + sum_d ( -1/2 a_kd x_id^2 + a_kd mu_kd x_id ),   a = 1/sigma^2,
+// one product of [x^2 | x] (128 rows x 128) with W^T (128 x KN components) per
+// tile of 128 rows, KN = K rounded up to 32 or 64 (the components past K have
+// W = 0 and c' = -1e30, so their posterior is 0).  As in the dense pass of the
+// K = 128 routing, each fp32 operand is held as three bf16 planes (v = v0 + v1
+// + v2 up to 2^-24 |v|) and the six plane products whose orders add up to at
+// most two are accumulated in fp32, smallest first: every log-joint carries the
+// rounding of an fp32 evaluation of the expanded form, a few fp32 units of
+//   S_i = 1/2 A sum_d x_id^2 + M sum_d |x_id|   (A = max a, M = max |a mu| over the head).
+// A row whose S_i exceeds kQSMax (|x| large against the components, where the
+// expansion cancels) has its log-joints evaluated exactly instead, in the
+// direct form, by the four threads that own the row.  With bf16 routing rows
+// the values are one plane and their squares two, and the products of the zero
+// planes are skipped.
+//
+// One CTA of 16 warps per tile of 128 rows: the head's planes of W (3 x KN x 256
+// B) and constants are bulk-copied while the routing tile arrives by TMA; warp w
+// owns TMEM lanes 32 (w % 4) .. + 31 (rows) and quarter q = w / 4: operand
+// positions 32 q .. 32 q + 31 (the squares, then the values, of features 16 q ..
+// 16 q + 15) and components KN q / 4 .. of the result; one thread issues the
+// products; the warps take the softmax from the accumulator and assemble the
+// output tile, which leaves by TMA stores.  (A persistent form that pipelined
+// several tiles per CTA gave wrong products for every tile after a CTA's first;
+// the one-tile form is the one kept.)
+#include "gma_internal.cuh"
+#include "gma_tc.cuh"
+
+#include <float.h>
+
+namespace gma {
+namespace {
+
+using namespace tc;
+
+constexpr int kQD = 64, kQDP = kQD / 2;   // d_route, feature pairs
+constexpr int kQRows = 128;
+constexpr int kQThreads = 512;
+constexpr float kQSMax = 4096.f;
+constexpr float kQLog2e = 1.4426950408889634f;
+constexpr float kQOff = -1.0e30f;         // c' of the components past K
+
+// Operand position of feature f's square (its value sits 16 positions later):
+// quarter q of the operand holds the squares of features 16 q .. 16 q + 15, then
+// their values.
+__host__ __device__ constexpr int gtc_pos(int f) { return 32 * (f >> 4) + (f & 15); }
+
+// Per-head image: the three bf16 planes of W ([KN][128], 128-byte-swizzled
+// K-major), then c'[KN], then A and M.
+template <int KN>
+struct GtcImg {
+    static constexpr uint32_t W = 3u * KN * 256u;
+    static constexpr uint32_t C = KN * 4u + 16u;
+    static constexpr uint32_t pitch = (W + C + 255u) & ~255u;
+};
+
+size_t gtc_pitch(int KN) { return KN <= 32 ? GtcImg<32>::pitch : GtcImg<64>::pitch; }
+
+// v = p0 + p1 + p2 + r with p0, p1, p2 bf16 and |r| <= 2^-24 |v|.
+__device__ __forceinline__ void split3(float v, unsigned short (&p)[3])
+{
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        p[j] = __bfloat16_as_ushort(b);
+        v -= __bfloat162float(b);
+    }
+}
+
+// Grid H, KN * 4 threads: component k = tid / 4 takes feature pairs 8 (tid % 4) .. + 7
+// from the packed parameters {s, s', -mu s, -mu' s'} and c_k that k_prep wrote.
+template <int KN>
+__global__ void __launch_bounds__(KN * 4)
+    k_prep_gtc(int K, const float4 *__restrict__ prm, const float *__restrict__ cst, unsigned char *__restrict__ img)
+{
+    __shared__ float red[2][KN * 4 / 32];
+    const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = tid >> 2, part = tid & 3;
+    unsigned char *im = img + (long long)h * GtcImg<KN>::pitch;
+    float amu2 = 0.f, amax = 0.f, mmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int dp = 8 * part + j, f = 2 * dp;
+        const float4 p = k < K ? prm[((long long)h * K + k) * kQDP + dp] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float wa0 = -0.5f * p.x * p.x, wa1 = -0.5f * p.y * p.y, wb0 = -p.x * p.z, wb1 = -p.y * p.w;
+        amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
+        amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
+        mmax = fmaxf(mmax, fmaxf(fabsf(wb0), fabsf(wb1)));
+        unsigned short a0[3], a1[3], b0[3], b1[3];
+        split3(wa0, a0);
+        split3(wa1, a1);
+        split3(wb0, b0);
+        split3(wb1, b1);
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+            unsigned char *w = im + pl * (KN * 256);
+            *reinterpret_cast<uint32_t *>(w + sw128_offset(k, gtc_pos(f), KN, 2)) = (uint32_t)a0[pl] | ((uint32_t)a1[pl] << 16);
+            *reinterpret_cast<uint32_t *>(w + sw128_offset(k, gtc_pos(f) + 16, KN, 2)) =
+                (uint32_t)b0[pl] | ((uint32_t)b1[pl] << 16);
+        }
+    }
+    for (int o = 1; o < 4; o <<= 1) {   // the component's four threads
+        amu2 += __shfl_xor_sync(0xffffffffu, amu2, o);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    }
+    float *c = reinterpret_cast<float *>(im + GtcImg<KN>::W);
+    if (part == 0) c[k] = k < K ? cst[(long long)h * K + k] - 0.5f * amu2 : kQOff;
+    // head-wide maxima of a and |a mu|
+    for (int o = 4; o < 32; o <<= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    }
+    if (lane == 0) {
+        red[0][warp] = amax;
+        red[1][warp] = mmax;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float a = 0.f, m = 0.f;
+        for (int w = 0; w < KN * 4 / 32; ++w) {
+            a = fmaxf(a, red[0][w]);
+            m = fmaxf(m, red[1][w]);
+        }
+        c[KN] = a;
+        c[KN + 1] = m;
+        c[KN + 2] = 0.f;
+        c[KN + 3] = 0.f;
+    }
+}
+
+// 2^t by the SFU's base-2 exponential (relative error about 2^-22; 0 for t below -126).
+__device__ __forceinline__ float ex2_sfu(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+// The three bf16 planes of a pair of values, packed two per word (the first value in the
+// low half): each plane the round-to-nearest of what the previous ones leave.
+__device__ __forceinline__ void split3_pair(float2 v, uint32_t &p0, uint32_t &p1, uint32_t &p2)
+{
+    const float2 m1 = make_float2(-1.f, -1.f);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+    p0 = *reinterpret_cast<const uint32_t *>(&b);
+    v = __ffma2_rn(make_float2(__uint_as_float(p0 << 16), __uint_as_float(p0 & 0xffff0000u)), m1, v);
+    b = __floats2bfloat162_rn(v.x, v.y);
+    p1 = *reinterpret_cast<const uint32_t *>(&b);
+    v = __ffma2_rn(make_float2(__uint_as_float(p1 << 16), __uint_as_float(p1 & 0xffff0000u)), m1, v);
+    b = __floats2bfloat162_rn(v.x, v.y);
+    p2 = *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// The exact log-joints l_k = c_k - 1/2 sum_d ((x_d - mu_kd) / sigma_kd)^2 of components
+// k0 .. k0 + n - 1 (those past K get kQOff) for routing row x (global memory), from the
+// packed parameters {s, s', -mu s, -mu' s'} of head h: the path of rows too large for the
+// expanded form, kept out of line.
+__device__ __noinline__ void exact_row(const void *x, bool x_bf16, const float4 *__restrict__ prm,
+                                       const float *__restrict__ cst, int h, int K, int k0, int n, float *l)
+{
+    float2 xr[kQDP];
+    if (x_bf16) {
+        const uint32_t *xw = static_cast<const uint32_t *>(x);
+#pragma unroll
+        for (int dp = 0; dp < kQDP; ++dp)
+            xr[dp] = make_float2(__uint_as_float(xw[dp] << 16), __uint_as_float(xw[dp] & 0xffff0000u));
+    } else {
+        const float2 *x2 = static_cast<const float2 *>(x);
+#pragma unroll
+        for (int dp = 0; dp < kQDP; ++dp) xr[dp] = x2[dp];
+    }
+    for (int j = 0; j < n; ++j) {
+        const int k = k0 + j;
+        float v = kQOff;
+        if (k < K) {
+            const float4 *pk = prm + ((long long)h * K + k) * kQDP;
+            float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int dp = 0; dp < kQDP; ++dp) {
+                const float4 p = pk[dp];
+                const float2 y = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
+                a2 = __ffma2_rn(y, y, a2);
+            }
+            v = fmaf(-0.5f, a2.x + a2.y, cst[(long long)h * K + k]);
+        }
+        l[j] = v;
+    }
+}
+
+template <int KN>
+struct GtcSmem {
+    static constexpr uint32_t W = GtcImg<KN>::W;        // three planes of W
+    static constexpr uint32_t WA = (W + 1023u) & ~1023u;
+    static constexpr uint32_t X = kQRows * kQD * 4;     // routing tile (fp32 worst case)
+    static constexpr uint32_t O = kQRows * 128 * 4;     // output tile (fp32 worst case, 128 columns)
+    static constexpr uint32_t C = GtcImg<KN>::C;        // c', A, M
+    static constexpr uint32_t EX = 4 * kQRows * 8;      // per quarter and row: (max, sum)
+    static constexpr uint32_t SS = 4 * kQRows * 8;      // per quarter and row: (sum x^2, sum |x|)
+    static constexpr size_t bytes = 1024 + (size_t)WA + X + O + C + EX + SS + 64;
+};
+static_assert(GtcSmem<64>::bytes <= 232448, "small-K tensor-core routing: shared memory above the per-block limit");
+
+// One CTA per tile of 128 rows (blockIdx.x = slice * tiles per slice + tile).
+template <int KN>
+__global__ void __launch_bounds__(kQThreads, 1)
+    k_resp_gtc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
+               const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, bool x_bf16,
+               const void *__restrict__ xg, const unsigned char *__restrict__ img, const float4 *__restrict__ prm,
+               const float *__restrict__ cst, int layout, int ow, unsigned int *timeout)
+{
+    constexpr int QC = KN / 4;   // components of a row per thread
+    using SM = GtcSmem<KN>;
+    extern __shared__ unsigned char sm_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, cq = warp >> 2;
+    const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
+    const int bh = blockIdx.x / tps, t = blockIdx.x % tps, h = bh % H;
+    const int row = t * kQRows + i;
+
+    unsigned char *w_s = sm;
+    unsigned char *xb = w_s + SM::WA;
+    unsigned char *ob = xb + SM::X;
+    float *c_s = reinterpret_cast<float *>(ob + SM::O);                  // [KN + 4]
+    float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);             // [4][128]
+    float2 *ss_s = ex_s + 4 * kQRows;                                    // [4][128]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 4 * kQRows);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2);
+    const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
+    const int ge = g_f32 ? 4 : 2;
+    constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's tile follows the hi plane's
+    constexpr uint32_t D_COL = 192;             // the accumulator; operand planes at 64 j
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tslot), 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
+        mbar_init_fence();
+        const unsigned char *src = img + (long long)h * GtcImg<KN>::pitch;
+        mbar_expect_tx(BAR_I, SM::W + SM::C);
+        bulk_g2s(smem_addr(w_s), src, SM::W, BAR_I);
+        bulk_g2s(smem_addr(c_s), src + SM::W, SM::C, BAR_I);
+        mbar_expect_tx(BAR_X, kQRows * kQD * (x_bf16 ? 2 : 4));
+        tma_load_3d(smem_addr(xb), &xmap, 0, t * kQRows, bh, BAR_X);
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kQRows * 128), &xmap, 32, t * kQRows, bh, BAR_X);
+    }
+    // the output tile starts as zeros: the columns past the components stay so
+    for (int o = tid; o < (int)(SM::O / 16); o += kQThreads) reinterpret_cast<uint4 *>(ob)[o] = make_uint4(0u, 0u, 0u, 0u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;
+    bool ok = mbar_wait(BAR_X, 0u);
+
+    // features 16 cq .. + 15 of row i: squares and values into the three planes, and the
+    // row's sums for S_i
+    {
+        float2 xv[8];
+        if (x_bf16) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kQRows, 2));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    xv[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kQRows, 4));
+                xv[2 * g] = make_float2(u.x, u.y);
+                xv[2 * g + 1] = make_float2(u.z, u.w);
+            }
+        }
+        uint32_t pw[3][16];
+        float2 s2 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float2 q = __fmul2_rn(xv[c], xv[c]);
+            s2 = __fadd2_rn(s2, q);
+            s1 = __fadd2_rn(s1, make_float2(fabsf(xv[c].x), fabsf(xv[c].y)));
+            split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
+            split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
+        }
+#pragma unroll
+        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
+        ss_s[cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
+        tmem_wait_st();
+    }
+    ok = mbar_wait(BAR_I, 0u) && ok;   // the planes of W and the constants
+    fence_before_sync();
+    ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM
+    fence_after_sync();
+    // one thread: the products, smallest first; with bf16 rows the values' lower planes and
+    // the squares' third plane are zero
+    bool issued = false;   // (thread 0)
+    if (tid == 0 && ok) {
+        issued = true;
+        const uint32_t id = idesc(128, KN, kFmtBF16);
+        bool first = true;
+#pragma unroll
+        for (int q = 0; q < 6; ++q) {
+            const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                // A plane
+            const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);    // W plane
+            if (x_bf16 && pa == 2) continue;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                if (x_bf16 && pa == 1 && (kk & 1)) continue;   // odd K steps: the values
+                const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+                const uint32_t boff = pb * (uint32_t)(KN * 256) + (kb >> 7) * (KN * 128) + (kb & 127);
+                mma_ts(0u, tbase + D_COL, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
+                       first ? 0u : 1u);
+                first = false;
+            }
+        }
+        mma_commit(BAR_M);
+    }
+    if (ok) ok = mbar_wait(BAR_M, 0u);
+    fence_after_sync();
+    float2 acc[QC / 2];
+    {
+        uint32_t r[QC];
+        if constexpr (QC == 16) {
+            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq), reinterpret_cast<uint32_t(&)[16]>(r));
+        } else {
+            uint32_t r16[16];   // columns QC cq .. + 7 of a 16-wide read (the other half belongs to
+                                // the neighbouring quarter)
+            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 16 * (cq >> 1)), r16);
+#pragma unroll
+            for (int j = 0; j < QC; ++j) r[j] = r16[8 * (cq & 1) + j];
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
+    }
+    // log-joints (rows beyond the magnitude limit exactly), then the softmax over the four
+    // quarters of the row
+    const float2 am = make_float2(c_s[KN], c_s[KN + 1]);
+    const float2 *sp = ss_s + i;
+    const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
+    const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
+    const float *cb = c_s + QC * cq;   // c'_k of this thread's components
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
+    if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
+        float lex[QC];
+        const long long xo = ((long long)bh * N + row) * kQD;
+        exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
+                         : (const void *)(static_cast<const float *>(xg) + xo),
+                  x_bf16, prm, cst, h, K, QC * cq, QC, lex);
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
+    }
+    float mq = -FLT_MAX;
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
+    const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
+    float2 sq2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) {
+        const float2 tt = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
+        acc[p] = make_float2(ex2_sfu(tt.x), ex2_sfu(tt.y));
+        sq2 = __fadd2_rn(sq2, acc[p]);
+    }
+    ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
+    __syncthreads();
+    float2 e4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
+    const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+    float tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
+    const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
+    const float2 sc2 = make_float2(sc, sc);
+    if (g_f32) {
+#pragma unroll
+        for (int g = 0; g < QC / 4; ++g) {
+            const float2 a = __fmul2_rn(acc[2 * g], sc2), b = __fmul2_rn(acc[2 * g + 1], sc2);
+            *reinterpret_cast<float4 *>(ob + sw128_offset(i, QC * cq + 4 * g, kQRows, 4)) = make_float4(a.x, a.y, b.x, b.y);
+        }
+    } else {
+        const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+        for (int g = 0; g < QC / 8; ++g) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 v = __fmul2_rn(acc[4 * g + u], sc2);
+                __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)),
+                                            m1, v);
+                b = __floats2bfloat162_rn(r.x, r.y);
+                lw[u] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            const uint32_t off = sw128_offset(i, QC * cq + 8 * g, kQRows, 2);
+            *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+    }
+    fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
+    fence_before_sync();
+    ok = __syncthreads_and(ok) != 0;
+    if (tid == 0) {
+        if (ok) {
+            const int boxes = (ow * ge + 127) / 128;
+            for (int a = 0; a < boxes; ++a) {
+                tma_store_3d(&gmap, a * (128 / ge), t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
+                if (g_split)
+                    tma_store_3d(&gmap_lo, a * (128 / ge), t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
+            }
+            bulk_commit();
+        } else {
+            // after a failed wait the products or a copy may still be in flight: let them end
+            // (bounded; a wait on a phase that has completed returns at once)
+            mbar_wait(BAR_I, 0u);
+            mbar_wait(BAR_X, 0u);
+            if (issued) mbar_wait(BAR_M, 0u);
+            report_timeout(timeout);
+        }
+        bulk_wait_all();
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+int gtc_width(int K) { return K <= 32 ? 32 : 64; }
+
+} // namespace
+
+bool resp_gtc_applies(const Dims &dm) { return dm.D == kQD && dm.K >= 17 && dm.K <= 64; }
+
+size_t gtc_image_bytes(const Dims &dm) { return resp_gtc_applies(dm) ? dm.H * gtc_pitch(gtc_width(dm.K)) : 0; }
+
+cudaError_t launch_prep_gtc(const Dims &dm, const float4 *prm, const float *cst, unsigned char *img, cudaStream_t st)
+{
+    if (!resp_gtc_applies(dm)) return cudaErrorInvalidValue;
+    if (gtc_width(dm.K) == 32)
+        k_prep_gtc<32><<<dm.H, 32 * 4, 0, st>>>(dm.K, prm, cst, img);
+    else
+        k_prep_gtc<64><<<dm.H, 64 * 4, 0, st>>>(dm.K, prm, cst, img);
+    return cudaGetLastError();
+}
+
+bool resp_gtc_output_ok(int ldg, int layout)
+{
+    // rows of the output start on 16-byte boundaries (a TMA store's strides)
+    return ldg <= 128 && (layout == GL_F32 ? ldg % 4 == 0 : ldg % 8 == 0);
+}
+
+template <int KN>
+cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst, const void *x,
+                       void *gamma, int ldg, int layout, cudaStream_t st)
+{
+    constexpr size_t smem = GtcSmem<KN>::bytes;
+    static std::atomic<unsigned long long> smem_set{0};
+    const cudaError_t attr = allow_smem(k_resp_gtc<KN>, smem, smem_set);
+    if (attr != cudaSuccess) return attr;
+    const int tps = (dm.N + kQRows - 1) / kQRows;
+    const long long items = dm.BH() * tps;
+    if (items == 0) return cudaSuccess;
+    CUtensorMap xmap, gmap, gmap_lo;
+    const bool g16 = layout != GL_F32;
+    const long long plane = dm.BH() * dm.N * (long long)ldg;   // elements per plane (split)
+    if (!make_tma_3d(&xmap, x, dm.x_bf16, kQD, dm.N, dm.BH(), kQRows) ||
+        !make_tma_3d(&gmap, gamma, g16, ldg, dm.N, dm.BH(), kQRows))
+        return cudaErrorInvalidValue;
+    if (layout == GL_SPLIT) {
+        if (!make_tma_3d(&gmap_lo, static_cast<__nv_bfloat16 *>(gamma) + plane, true, ldg, dm.N, dm.BH(), kQRows))
+            return cudaErrorInvalidValue;
+    } else {
+        gmap_lo = gmap;
+    }
+    unsigned int *flag = timeout_flag_dev();
+    if (!flag) return cudaErrorMemoryAllocation;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    k_resp_gtc<KN><<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x,
+                                                             img, prm, cst, layout, ldg, flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_resp_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst,
+                            const void *x, void *gamma, int ldg, int layout, cudaStream_t st)
+{
+    if (!resp_gtc_applies(dm) || !resp_gtc_output_ok(ldg, layout)) return cudaErrorInvalidValue;
+    return gtc_width(dm.K) == 32 ? launch_gtc<32>(dm, img, prm, cst, x, gamma, ldg, layout, st)
+                                 : launch_gtc<64>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+}
+
+} // namespace gma

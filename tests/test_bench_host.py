@@ -195,3 +195,20 @@ def test_clock_summary():
 def test_tokens_per_step():
     assert bench.tokens_per_step(W["causal_16k_peaked"]) == 2 * 16384
     assert bench.tokens_per_step(W["decode_b256"]) == 256
+
+
+def test_small_k_routing_roofline():
+    """For 17 <= K <= 64 with d = 64 both routings are tensor work (the six bf16 passes of
+    a product 32 or 64 components wide) and carry no FP32 work in the whole-step roofline."""
+    pk = dict(bench.FALLBACK)
+    wl = W["causal_8k_K32"]
+    ht = wl.B * wl.H * wl.N
+    f, pipe, _ = bench.stage_work("resp_q", wl)
+    assert pipe == "tensor_bf16" and f == 6 * 4 * 32 * 64 * ht
+    assert bench.stage_work("resp_q", W["causal_8k_K64"])[0] == 6 * 4 * 64 * 64 * ht
+    r = bench.roofline_of("resp_q", wl, 100e-6, pk)
+    assert r["bound"] in ("tensor", "hbm")
+    t, parts = bench.path_roofline_s(wl, pk)
+    assert parts["alu_s"] == 0.0
+    # K = 256 keeps the CUDA-core routing
+    assert bench.stage_work("resp_q", W["causal_8k_K256"])[1] == "alu"

@@ -42,6 +42,13 @@ def _report(name, err, tol):
     (W["tiny"].with_(mode="bidir", B=8, H=25, N=200, d=64, dv=64, K=128), None),
     (W["causal_8k_K512"], 2),
     (W["causal_64k_bf16"], 2),
+    # the tensor-core routing for 17 <= K <= 64 (d = 64): padded widths, bf16 rows; K = 33 keeps
+    # the CUDA-core kernel (fp32 rows of 33 are not 16-byte multiples)
+    (W["tiny"].with_(K=40, d=64, N=1000, B=2, H=3), None),
+    (W["tiny"].with_(K=64, d=64, N=777, H=2, x_dtype="bf16"), None),
+    (W["tiny"].with_(K=20, d=64, N=300, H=2), None),
+    (W["tiny"].with_(K=33, d=64, N=300, H=2), None),
+    (W["causal_8k_K32"], 2),
 ])
 def test_responsibilities(wl, sample):
     c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
@@ -81,17 +88,19 @@ def test_responsibilities_adversarial_rows():
     assert np.abs(out.sum(-1) - 1).max() < 1e-5
 
 
-@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
-def test_responsibilities_dense_tiles_across_scales(x_dtype):
-    """Tiles of N(0, s^2) rows, one scale per tile of 128 rows, from s = 0.3 to s = 6: the
-    wide tiles keep many components and go to the dense passes, the tensor-core one below
-    its magnitude limit (s up to about 2) and the exact one above it; a last tile mixes
-    N(0, 1) rows with one row of s = 6.  Each tile's posteriors must match the oracle's."""
+@pytest.mark.parametrize("K,x_dtype", [(128, "f32"), (128, "bf16"), (64, "f32"), (40, "bf16"), (32, "f32")])
+def test_responsibilities_dense_tiles_across_scales(K, x_dtype):
+    """Tiles of N(0, s^2) rows, one scale per tile of 128 rows, from s = 0.3 to s = 6.  At
+    K = 128 the wide tiles keep many components and go to the dense passes, the tensor-core
+    one below its magnitude limit (s up to about 2) and the exact one above it; at
+    K <= 64 every tile takes the tensor-core routing and the rows above the limit its exact
+    path.  A last tile mixes N(0, 1) rows with one row of s = 6.  Each tile's posteriors
+    must match the oracle's."""
     import oracle
     from gaussian_mixture_sequence_gb300 import gma
     from gpu_cases import shape_of
     scales = [0.3, 0.7, 1.0, 1.4, 1.8, 2.2, 3.0, 6.0]
-    wl = W["causal_4k"].with_(B=1, H=2, N=128 * (len(scales) + 1) - 37, x_dtype=x_dtype)
+    wl = W["causal_4k"].with_(B=1, H=2, N=128 * (len(scales) + 1) - 37, K=K, x_dtype=x_dtype)
     mu, vr, lp = workloads.params(wl)
     rng = np.random.default_rng(11)
     x = np.concatenate([s * rng.standard_normal((wl.H, 128, 64)) for s in scales] +
@@ -108,7 +117,7 @@ def test_responsibilities_dense_tiles_across_scales(x_dtype):
     out = g.reshape(wl.H, wl.N, wl.K).cpu().numpy()
     for j in range(len(scales) + 1):
         rows = slice(128 * j, min(wl.N, 128 * (j + 1)))
-        _report(f"gamma tile {j} (scale {scales[j] if j < len(scales) else 'mixed'}) {x_dtype}",
+        _report(f"gamma tile {j} (scale {scales[j] if j < len(scales) else 'mixed'}) K={K} {x_dtype}",
                 normwise(out[:, rows], ref[:, rows]), TOL["f32"])
     assert np.abs(out.sum(-1) - 1).max() < 1e-5
 
@@ -177,6 +186,9 @@ CAUSAL = [
     (W["tiny"].with_(B=1, H=2, N=700, d=32, dv=128, K=256, gemm_dtype="bf16", v_dtype="bf16"), None, 0),
     (W["tiny"].with_(B=4, H=16, N=1100, d=64, dv=64, K=512), None, 0),
     (W["tiny"].with_(B=1, H=2, N=600, d=64, dv=64, K=200), None, 0),
+    # the tensor-core routing for 17 <= K <= 64 with padded widths, fp32 and bf16 rows
+    (W["tiny"].with_(B=2, H=3, N=1000, d=64, dv=64, K=20), None, 0),
+    (W["tiny"].with_(B=1, H=2, N=700, d=64, dv=64, K=48, x_dtype="bf16"), None, 0),
 ]
 
 
