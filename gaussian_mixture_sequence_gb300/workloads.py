@@ -10,9 +10,10 @@ regenerated on its own (the oracle checks sampled slices of the large
 workloads) and the values do not depend on the machine or on numpy's thread
 count.  Per-head GMM parameters use ``SeedSequence([seed, tensor_code, h])``.
 
-Value distributions follow the workload descriptions of the GMA explainer
-("Gaussian Mixture Attention: Linear-Time Sequence Mixing via Probabilistic
-Latent Routing", section "핵심 메커니즘" / "변형 및 학습"):
+Value distributions are those of the benchmark and test workloads defined
+below (the pages fix the model -- the diagonal GMM of the GMA explainer's
+"핵심 메커니즘", with softplus variances and softmax mixture weights -- but
+print no input distributions):
 
 * mu_k ~ N(0, 1); raw variance r ~ N(0, 0.5^2) (0.5 read as a standard
   deviation); mixture logits l ~ N(0, 1).
