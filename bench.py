@@ -123,10 +123,10 @@ def stage_work(stage, wl):
     if stage in ("resp_q", "resp_k"):
         # K = 128, d = 64: the bound GEMM [x^2 | x] W has the same 4*K*d flop per row and runs on the
         # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work.
-        # 17 <= K <= 64, d = 64: every log-joint on the tensor pipe, the dense pass's bf16 passes of a
-        # product K_N wide (K rounded up to 32 or 64)
+        # 17 <= K <= 256 otherwise, d = 64: every log-joint on the tensor pipe, the dense pass's bf16
+        # passes of a product K_N wide (K rounded up to 32, 64, 128 or 256)
         if tc_routing(wl):
-            kn = 32 if K <= 32 else 64
+            kn = tc_width(K)
             return dense_passes(wl) * 4.0 * kn * d * ht, "tensor_bf16", (d * xb + K * gb) * ht
         pipe = "tensor_bf16" if bounded_routing(wl) else "alu"
         return 4.0 * K * d * ht, pipe, (d * xb + K * gb) * ht
@@ -254,9 +254,14 @@ def bounded_routing(wl):
 
 
 def tc_routing(wl):
-    """The library's tensor-core routing for 17 <= K <= 64 applies (d = 64; the rows of the
-    workspace layout are 128 wide on the chunked tensor-core path, K wide otherwise)."""
-    return wl.d == 64 and 17 <= wl.K <= 64
+    """The library's tensor-core routing for 17 <= K <= 256 applies (d = 64; K = 128 has the
+    bounded routing instead)."""
+    return wl.d == 64 and 17 <= wl.K <= 256 and not bounded_routing(wl)
+
+
+def tc_width(K):
+    """Components of the tensor-core routing's product: K rounded up to 32, 64, 128 or 256."""
+    return next(w for w in (32, 64, 128, 256) if K <= w)
 
 
 def pipe_peak(pipe, wl, pk):

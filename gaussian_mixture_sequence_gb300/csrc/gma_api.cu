@@ -18,7 +18,7 @@ struct WsPlan {
            cimg = 0, pimg2 = 0, dctl = 0, dlist = 0, dlist2 = 0, bytes = 0;
     long long dcap = 0;   // dense-list entries per head
     bool pruned = false;  // the bounded routing (K = 128, d = 64)
-    bool gtc = false;     // the tensor-core routing for 17 <= K <= 64, d = 64
+    bool gtc = false;     // the tensor-core routing for 17 <= K <= 256 (not 128), d = 64
 };
 
 bool valid_width(int w) { return w == 16 || w == 32 || w == 64 || w == 128; }

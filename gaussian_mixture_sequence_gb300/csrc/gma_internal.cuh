@@ -168,12 +168,13 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
 cudaError_t launch_resp_dense(const Dims &d0, const void *x0, void *g0, const Dims &d1, const void *x1, void *g1,
                               const PrunedImages &img, int layout, cudaStream_t st);
 
-// Responsibilities on the tensor cores for 17 <= K <= 64 and d_route = 64 (gma_resp_gtc.cu):
-// per-head images (the three bf16 planes of the log-joint matrix, c', the head's maxima)
-// built from k_prep's parameters into PrunedImages::w3, then every tile of a routing.
+// Responsibilities on the tensor cores for 17 <= K <= 256 (K = 128 excepted: the bounded
+// routing above takes it) and d_route = 64 (gma_resp_gtc.cu): per-head images (the three
+// bf16 planes of the log-joint matrix, c', the head's maxima) built from k_prep's
+// parameters into PrunedImages::w3, then every tile of a routing.
 bool resp_gtc_applies(const Dims &dm);
 size_t gtc_image_bytes(const Dims &dm);   // workspace for the images (0 where it does not apply)
-bool resp_gtc_output_ok(int ldg, int layout);
+bool resp_gtc_output_ok(const Dims &dm, int ldg, int layout);
 cudaError_t launch_prep_gtc(const Dims &dm, const float4 *prm, const float *cst, unsigned char *img, cudaStream_t st);
 cudaError_t launch_resp_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst,
                             const void *x, void *gamma, int ldg, int layout, cudaStream_t st);

@@ -357,7 +357,7 @@ cudaError_t launch_resp(const Dims &dm, const float4 *prm, const float *cst, con
                         const void *x, void *gamma, int ldg, int layout, cudaStream_t st, int src)
 {
     if (img && resp_pruned_applies(dm)) return launch_resp_pruned(dm, *img, x, gamma, ldg, layout, st, src);
-    if (img && img->w3 && resp_gtc_applies(dm) && resp_gtc_output_ok(ldg, layout))
+    if (img && img->w3 && resp_gtc_applies(dm) && resp_gtc_output_ok(dm, ldg, layout))
         return launch_resp_gtc(dm, img->w3, prm, cst, x, gamma, ldg, layout, st);
     switch (dm.D) {
     case 16: return launch_resp_d<16>(dm, prm, cst, x, gamma, ldg, layout, st);

@@ -1,13 +1,14 @@
-// Responsibilities (S1) on the tensor cores for 17 <= K <= 64 components and
-// d_route = 64: every log-joint of every row, for any inputs.
+// Responsibilities (S1) on the tensor cores for 17 <= K <= 256 components (K = 128
+// has the bounded routing of its own) and d_route = 64: every log-joint of every row,
+// for any inputs.
 //
 // The posterior of the GMA explainer ("핵심 메커니즘": gamma_ik = p(z = k | x_i)
 // under the diagonal GMM) is a softmax over the log-joints
 //   l_ik = c_k - 1/2 sum_d ((x_id - mu_kd) / sigma_kd)^2
 //        = c'_k + sum_d ( -1/2 a_kd x_id^2 + a_kd mu_kd x_id ),   a = 1/sigma^2,
 // one product of [x^2 | x] (128 rows x 128) with W^T (128 x KN components) per
-// tile of 128 rows, KN = K rounded up to 32 or 64 (the components past K have
-// W = 0 and c' = -1e30, so their posterior is 0).  As in the dense pass of the
+// tile of 128 rows, KN = K rounded up to 32, 64, 128 or 256 (the components past K
+// have W = 0 and c' = -1e30, so their posterior is 0).  As in the dense pass of the
 // K = 128 routing, each fp32 operand is held as three bf16 planes (v = v0 + v1
 // + v2 up to 2^-24 |v|) and the six plane products whose orders add up to at
 // most two are accumulated in fp32, smallest first: every log-joint carries the
@@ -20,14 +21,14 @@
 // planes are skipped.
 //
 // One CTA of 16 warps per tile of 128 rows: the head's planes of W (3 x KN x 256
-// B) and constants are bulk-copied while the routing tile arrives by TMA; warp w
-// owns TMEM lanes 32 (w % 4) .. + 31 (rows) and quarter q = w / 4: operand
-// positions 32 q .. 32 q + 31 (the squares, then the values, of features 16 q ..
-// 16 q + 15) and components KN q / 4 .. of the result; one thread issues the
-// products; the warps take the softmax from the accumulator and assemble the
-// output tile, which leaves by TMA stores.  (A persistent form that pipelined
-// several tiles per CTA gave wrong products for every tile after a CTA's first;
-// the one-tile form is the one kept.)
+// B, in chunks of 64 components past KN = 64) and constants are bulk-copied while
+// the routing tile arrives by TMA; warp w owns TMEM lanes 32 (w % 4) .. + 31 (rows)
+// and quarter q = w / 4: operand positions 32 q .. 32 q + 31 (the squares, then the
+// values, of features 16 q .. 16 q + 15) and components KN q / 4 .. of the result;
+// one thread issues the products; the warps take the softmax from the accumulator
+// and assemble the output tile, which leaves by TMA stores.  (A persistent form that
+// pipelined several tiles per CTA gave wrong products for every tile after a CTA's
+// first; the one-tile form is the one kept.)
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -50,16 +51,25 @@ constexpr float kQOff = -1.0e30f;         // c' of the components past K
 // their values.
 __host__ __device__ constexpr int gtc_pos(int f) { return 32 * (f >> 4) + (f & 15); }
 
-// Per-head image: the three bf16 planes of W ([KN][128], 128-byte-swizzled
-// K-major), then c'[KN], then A and M.
+// Per-head image: the three bf16 planes of W, each [KN][128] 128-byte-swizzled K-major
+// (one bulk copy brings a plane), then c'[KN], then A and M.
 template <int KN>
 struct GtcImg {
     static constexpr uint32_t W = 3u * KN * 256u;
     static constexpr uint32_t C = KN * 4u + 16u;
     static constexpr uint32_t pitch = (W + C + 255u) & ~255u;
+    // byte offset of operand position `pos` of component k in plane pl
+    __host__ __device__ __forceinline__ static uint32_t off(int k, int pos, int pl)
+    {
+        return (uint32_t)pl * (KN * 256u) + sw128_offset(k, pos, KN, 2);
+    }
 };
 
-size_t gtc_pitch(int KN) { return KN <= 32 ? GtcImg<32>::pitch : GtcImg<64>::pitch; }
+size_t gtc_pitch(int KN)
+{
+    return KN <= 32 ? GtcImg<32>::pitch
+                    : (KN <= 64 ? GtcImg<64>::pitch : (KN <= 128 ? GtcImg<128>::pitch : GtcImg<256>::pitch));
+}
 
 // v = p0 + p1 + p2 + r with p0, p1, p2 bf16 and |r| <= 2^-24 |v|.
 __device__ __forceinline__ void split3(float v, unsigned short (&p)[3])
@@ -98,9 +108,9 @@ __global__ void __launch_bounds__(KN * 4)
         split3(wb1, b1);
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl) {
-            unsigned char *w = im + pl * (KN * 256);
-            *reinterpret_cast<uint32_t *>(w + sw128_offset(k, gtc_pos(f), KN, 2)) = (uint32_t)a0[pl] | ((uint32_t)a1[pl] << 16);
-            *reinterpret_cast<uint32_t *>(w + sw128_offset(k, gtc_pos(f) + 16, KN, 2)) =
+            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(k, gtc_pos(f), pl)) =
+                (uint32_t)a0[pl] | ((uint32_t)a1[pl] << 16);
+            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(k, gtc_pos(f) + 16, pl)) =
                 (uint32_t)b0[pl] | ((uint32_t)b1[pl] << 16);
         }
     }
@@ -429,44 +439,353 @@ __global__ void __launch_bounds__(kQThreads, 1)
             if (issued) mbar_wait(BAR_M, 0u);
             report_timeout(timeout);
         }
-        bulk_wait_all();
+        bulk_wait_read();   // the output tile has left shared memory
     }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
-int gtc_width(int K) { return K <= 32 ? 32 : 64; }
+// ---- KN = 128 or 256 (65 <= K <= 256, d = 64): one product per plane pair, N = KN ----
+//
+// One CTA per tile of 128 rows.  The accumulator holds all KN log-joints of a row (TMEM
+// columns 256 ..; the operand planes at 0 .. 191).  The three planes of W do not fit
+// in shared memory beside the output tile, so they pass through two buffers, P and Q,
+// and the products are taken in the order the planes arrive: plane 1 into P and plane 2
+// into Q, then (1,1), (0,2), (0,1); once (0,2) is done Q takes plane 0, then (2,0), (1,0),
+// (0,0).  The terms before the last are at most 2^-8 of the log-joint, so the order keeps
+// the rounding of one fp32 evaluation.  The routing tile shares the output tile's
+// space (it is consumed before the first product).  Each thread then owns KN / 4
+// components of its row; the posteriors leave in halves of 128 components.
+template <int KN>
+struct GtcWSmem {
+    static constexpr uint32_t WB = KN * 256;             // one plane of W
+    static constexpr uint32_t O = kQRows * 128 * 4;      // half of the output tile (fp32 worst case),
+                                                         // first the routing tile
+    static constexpr uint32_t C = GtcImg<KN>::C;         // c', A, M
+    static constexpr uint32_t EX = 4 * kQRows * 8;       // per quarter and row: (max, sum)
+    static constexpr uint32_t SS = 4 * kQRows * 8;       // per quarter and row: (sum x^2, sum |x|)
+    static constexpr size_t bytes = 1024 + 2 * (size_t)WB + O + C + EX + SS + 64;
+};
+static_assert(GtcWSmem<256>::bytes <= 232448, "wide tensor-core routing: shared memory above the per-block limit");
+static_assert(kQRows * kQD * 4 <= GtcWSmem<256>::O, "the routing tile fits in the output tile's space");
+
+template <int KN>
+__global__ void __launch_bounds__(kQThreads, 1)
+    k_resp_gtc_wide(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
+                    const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, bool x_bf16,
+                    const void *__restrict__ xg, const unsigned char *__restrict__ img, const float4 *__restrict__ prm,
+                    const float *__restrict__ cst, int layout, int ow, unsigned int *timeout)
+{
+    constexpr int QC = KN / 4;
+    constexpr int HALVES = KN / 128, QPH = 4 / HALVES;   // output halves; quarters of a row per half
+    using SM = GtcWSmem<KN>;
+    using IM = GtcImg<KN>;
+    extern __shared__ unsigned char sm_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, cq = warp >> 2;
+    const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
+    const int bh = blockIdx.x / tps, t = blockIdx.x % tps, h = bh % H;
+    const int row = t * kQRows + i;
+    const unsigned char *src = img + (long long)h * IM::pitch;
+
+    unsigned char *wp = sm;              // buffer P: plane 1
+    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2, then plane 0
+    unsigned char *ob = wq + SM::WB;
+    unsigned char *xb = ob;
+    float *c_s = reinterpret_cast<float *>(ob + SM::O);       // [KN + 4]
+    float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);  // [4][128]
+    float2 *ss_s = ex_s + 4 * kQRows;                         // [4][128]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 4 * kQRows);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
+    // P landed, Q landed (twice), constants landed, routing tile landed, (0,2) done, all done
+    const uint32_t BAR_P = smem_addr(bar), BAR_Q = smem_addr(bar + 1), BAR_C = smem_addr(bar + 2);
+    const uint32_t BAR_X = smem_addr(bar + 3), BAR_Q2 = smem_addr(bar + 4), BAR_D = smem_addr(bar + 5);
+    const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
+    const int ge = g_f32 ? 4 : 2;
+    constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's half tile follows the hi plane's
+    constexpr uint32_t D_COL = 256;
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tslot), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 6; ++b) mbar_init(smem_addr(bar + b), 1);
+        mbar_init_fence();
+        mbar_expect_tx(BAR_X, kQRows * kQD * (x_bf16 ? 2 : 4));
+        tma_load_3d(smem_addr(xb), &xmap, 0, t * kQRows, bh, BAR_X);
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kQRows * 128), &xmap, 32, t * kQRows, bh, BAR_X);
+        mbar_expect_tx(BAR_C, SM::C);
+        bulk_g2s(smem_addr(c_s), src + IM::W, SM::C, BAR_C);
+        mbar_expect_tx(BAR_P, SM::WB);
+        bulk_g2s(smem_addr(wp), src + IM::off(0, 0, 1), SM::WB, BAR_P);
+        mbar_expect_tx(BAR_Q, SM::WB);
+        bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_Q);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tbase = *tslot;
+    bool ok = mbar_wait(BAR_X, 0u);
+    {   // features 16 cq .. + 15 of row i: squares and values into the three planes, and the
+        // row's sums for S_i
+        float2 xv[8];
+        if (x_bf16) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kQRows, 2));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    xv[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kQRows, 4));
+                xv[2 * g] = make_float2(u.x, u.y);
+                xv[2 * g + 1] = make_float2(u.z, u.w);
+            }
+        }
+        uint32_t pw[3][16];
+        float2 s2 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float2 q = __fmul2_rn(xv[c], xv[c]);
+            s2 = __fadd2_rn(s2, q);
+            s1 = __fadd2_rn(s1, make_float2(fabsf(xv[c].x), fabsf(xv[c].y)));
+            split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
+            split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
+        }
+#pragma unroll
+        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
+        ss_s[cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
+        tmem_wait_st();
+    }
+    ok = mbar_wait(BAR_C, 0u) && ok;
+    fence_before_sync();
+    ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, the routing tile is consumed
+    fence_after_sync();
+
+    // one thread: the six products in the order the planes of W arrive
+    int stage = 0;   // (thread 0) 1: products issued; 2: plane 0 requested
+    if (tid == 0 && ok) {
+        const uint32_t id = idesc(128, KN, kFmtBF16);
+        bool first = true;
+        // the K steps of a product: the values' (odd) steps first, then the squares' (even)
+        // ones.  Issued in ascending order, the odd steps of (1,0) were measured to take W
+        // from the step before them; in this order every product matched the fp64 terms.
+        auto prods = [&](uint32_t pa, const unsigned char *w) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int kk = s < 4 ? 2 * s + 1 : 2 * (s - 4);
+                if (x_bf16 && pa == 1 && (kk & 1)) continue;   // bf16 rows: the values' plane 1 is zero
+                const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+                const uint32_t boff = (kb >> 7) * (KN * 128) + (kb & 127);
+                mma_ts(0u, tbase + D_COL, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w + boff)), id,
+                       first ? 0u : 1u);
+                first = false;
+            }
+        };
+        ok = mbar_wait(BAR_P, 0u);
+        if (ok) {
+            stage = 1;
+            prods(1, wp);                          // (1,1)
+            ok = mbar_wait(BAR_Q, 0u);
+        }
+        if (ok) {
+            prods(0, wq);                          // (0,2)
+            mma_commit(BAR_Q2);
+            prods(0, wp);                          // (0,1)
+            ok = mbar_wait(BAR_Q2, 0u);
+        }
+        if (ok) {   // Q is free: plane 0
+            fence_proxy_async();
+            mbar_expect_tx(BAR_Q, SM::WB);
+            bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 0), SM::WB, BAR_Q);
+            stage = 2;
+            ok = mbar_wait(BAR_Q, 1u);
+        }
+        if (ok) {
+            if (!x_bf16) prods(2, wq);             // (2,0); zero for bf16 rows
+            prods(1, wq);                          // (1,0)
+            prods(0, wq);                          // (0,0)
+        }
+        if (stage >= 1) mma_commit(BAR_D);         // also after a failed wait: the products issued
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (ok) ok = mbar_wait(BAR_D, 0u);
+    fence_after_sync();
+    float2 acc[QC / 2];
+#pragma unroll
+    for (int b = 0; b < QC / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq + 16 * b), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int p = 0; p < 8; ++p) acc[8 * b + p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
+    }
+    // log-joints (rows beyond the magnitude limit exactly), then the softmax over the four
+    // quarters of the row
+    const float2 am = make_float2(c_s[KN], c_s[KN + 1]);
+    const float2 *sp = ss_s + i;
+    const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
+    const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
+    const float *cb = c_s + QC * cq;
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
+    if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
+        float lex[QC];
+        const long long xo = ((long long)bh * N + row) * kQD;
+        exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
+                         : (const void *)(static_cast<const float *>(xg) + xo),
+                  x_bf16, prm, cst, h, K, QC * cq, QC, lex);
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
+    }
+    float mq = -FLT_MAX;
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
+    const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
+    float2 sq2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < QC / 2; ++p) {
+        const float2 tt = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
+        acc[p] = make_float2(ex2_sfu(tt.x), ex2_sfu(tt.y));
+        sq2 = __fadd2_rn(sq2, acc[p]);
+    }
+    ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
+    ok = __syncthreads_and(ok) != 0;
+    {
+        float2 e4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
+        const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+        float tot = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
+        const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
+        const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = __fmul2_rn(acc[p], sc2);
+    }
+    // the posteriors in halves of 128 components: quarters QPH hf .. QPH hf + QPH - 1 write
+    // half hf
+#pragma unroll 1
+    for (int hf = 0; hf < HALVES; ++hf) {
+        if (hf > 0 && tid == 0) bulk_wait_read();   // the previous half has left shared memory
+        __syncthreads();
+        if (cq / QPH == hf) {
+            const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
+            if (g_f32) {
+#pragma unroll
+                for (int g = 0; g < QC / 4; ++g)
+                    *reinterpret_cast<float4 *>(ob + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
+                        make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
+            } else {
+                const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+                for (int g = 0; g < QC / 8; ++g) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 v = acc[4 * g + u];
+                        __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                        hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                        const float2 r = __ffma2_rn(
+                            make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
+                        b = __floats2bfloat162_rn(r.x, r.y);
+                        lw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                    const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
+                    *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            fence_proxy_async();   // the half tile, written by threads, is read by the TMA store
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            const int per = 128 / ge;   // columns of one 128-byte box
+            for (int a = 0; a < 128 / per; ++a) {
+                const int x0 = 128 * hf + a * per;
+                if (x0 >= ow) break;
+                tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
+                if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
+            }
+            bulk_commit();
+        }
+    }
+    if (tid == 0) {
+        if (!ok) {
+            // after a failed wait a copy or products may still be in flight: let them end
+            // (bounded; a wait on a phase that has completed returns at once)
+            mbar_wait(BAR_C, 0u);
+            mbar_wait(BAR_X, 0u);
+            mbar_wait(BAR_P, 0u);
+            mbar_wait(BAR_Q, 0u);
+            if (stage >= 2) mbar_wait(BAR_Q, 1u);
+            if (stage >= 1) mbar_wait(BAR_D, 0u);
+            report_timeout(timeout);
+        }
+        bulk_wait_read();   // the output tile has left shared memory
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+int gtc_width(int K) { return K <= 32 ? 32 : (K <= 64 ? 64 : (K <= 128 ? 128 : 256)); }
 
 } // namespace
 
-bool resp_gtc_applies(const Dims &dm) { return dm.D == kQD && dm.K >= 17 && dm.K <= 64; }
+bool resp_gtc_applies(const Dims &dm)
+{
+    return dm.D == kQD && dm.K >= 17 && dm.K <= 256 && !resp_pruned_applies(dm);
+}
 
 size_t gtc_image_bytes(const Dims &dm) { return resp_gtc_applies(dm) ? dm.H * gtc_pitch(gtc_width(dm.K)) : 0; }
 
 cudaError_t launch_prep_gtc(const Dims &dm, const float4 *prm, const float *cst, unsigned char *img, cudaStream_t st)
 {
     if (!resp_gtc_applies(dm)) return cudaErrorInvalidValue;
-    if (gtc_width(dm.K) == 32)
-        k_prep_gtc<32><<<dm.H, 32 * 4, 0, st>>>(dm.K, prm, cst, img);
-    else
-        k_prep_gtc<64><<<dm.H, 64 * 4, 0, st>>>(dm.K, prm, cst, img);
+    switch (gtc_width(dm.K)) {
+    case 32: k_prep_gtc<32><<<dm.H, 32 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 64: k_prep_gtc<64><<<dm.H, 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 128: k_prep_gtc<128><<<dm.H, 128 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    default: k_prep_gtc<256><<<dm.H, 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    }
     return cudaGetLastError();
 }
 
-bool resp_gtc_output_ok(int ldg, int layout)
+bool resp_gtc_output_ok(const Dims &dm, int ldg, int layout)
 {
-    // rows of the output start on 16-byte boundaries (a TMA store's strides)
-    return ldg <= 128 && (layout == GL_F32 ? ldg % 4 == 0 : ldg % 8 == 0);
+    // rows of the output start on 16-byte boundaries (a TMA store's strides); the output
+    // tile covers 128 columns, or KN for the wide form
+    const int KN = gtc_width(dm.K);
+    return ldg <= (KN < 128 ? 128 : KN) && (layout == GL_F32 ? ldg % 4 == 0 : ldg % 8 == 0);
 }
 
 template <int KN>
 cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst, const void *x,
                        void *gamma, int ldg, int layout, cudaStream_t st)
 {
-    constexpr size_t smem = GtcSmem<KN>::bytes;
+    constexpr bool wide = KN > 64;
+    size_t smem;
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, int, int, int, int, bool, const void *, const unsigned char *,
+                 const float4 *, const float *, int, int, unsigned int *);
+    if constexpr (wide) {
+        smem = GtcWSmem<KN>::bytes;
+        kern = k_resp_gtc_wide<KN>;
+    } else {
+        smem = GtcSmem<KN>::bytes;
+        kern = k_resp_gtc<KN>;
+    }
     static std::atomic<unsigned long long> smem_set{0};
-    const cudaError_t attr = allow_smem(k_resp_gtc<KN>, smem, smem_set);
+    const cudaError_t attr = allow_smem(kern, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     const int tps = (dm.N + kQRows - 1) / kQRows;
     const long long items = dm.BH() * tps;
@@ -486,17 +805,21 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    k_resp_gtc<KN><<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x,
-                                                             img, prm, cst, layout, ldg, flag);
+    kern<<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img, prm,
+                                                   cst, layout, ldg, flag);
     return cudaGetLastError();
 }
 
 cudaError_t launch_resp_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst,
                             const void *x, void *gamma, int ldg, int layout, cudaStream_t st)
 {
-    if (!resp_gtc_applies(dm) || !resp_gtc_output_ok(ldg, layout)) return cudaErrorInvalidValue;
-    return gtc_width(dm.K) == 32 ? launch_gtc<32>(dm, img, prm, cst, x, gamma, ldg, layout, st)
-                                 : launch_gtc<64>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    if (!resp_gtc_applies(dm) || !resp_gtc_output_ok(dm, ldg, layout)) return cudaErrorInvalidValue;
+    switch (gtc_width(dm.K)) {
+    case 32: return launch_gtc<32>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    case 64: return launch_gtc<64>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    case 128: return launch_gtc<128>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    default: return launch_gtc<256>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    }
 }
 
 } // namespace gma

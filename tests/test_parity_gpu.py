@@ -49,6 +49,14 @@ def _report(name, err, tol):
     (W["tiny"].with_(K=20, d=64, N=300, H=2), None),
     (W["tiny"].with_(K=33, d=64, N=300, H=2), None),
     (W["causal_8k_K32"], 2),
+    # the wide form (65 <= K <= 256 but 128, d = 64): chunks of 64 components through two
+    # buffers (K = 256: a buffer refilled while the other is multiplied), output in halves
+    (W["tiny"].with_(K=256, d=64, N=1000, B=2, H=2), None),
+    (W["tiny"].with_(K=200, d=64, N=555, H=3, x_dtype="bf16"), None),
+    (W["tiny"].with_(K=129, d=64, N=300, H=2), None),
+    (W["tiny"].with_(K=100, d=64, N=777, H=2), None),
+    (W["tiny"].with_(K=72, d=64, N=300, H=2, x_dtype="bf16"), None),
+    (W["causal_8k_K256"], 2),
 ])
 def test_responsibilities(wl, sample):
     c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
@@ -88,12 +96,13 @@ def test_responsibilities_adversarial_rows():
     assert np.abs(out.sum(-1) - 1).max() < 1e-5
 
 
-@pytest.mark.parametrize("K,x_dtype", [(128, "f32"), (128, "bf16"), (64, "f32"), (40, "bf16"), (32, "f32")])
+@pytest.mark.parametrize("K,x_dtype", [(128, "f32"), (128, "bf16"), (64, "f32"), (40, "bf16"), (32, "f32"),
+                                     (256, "f32"), (96, "bf16")])
 def test_responsibilities_dense_tiles_across_scales(K, x_dtype):
     """Tiles of N(0, s^2) rows, one scale per tile of 128 rows, from s = 0.3 to s = 6.  At
     K = 128 the wide tiles keep many components and go to the dense passes, the tensor-core
-    one below its magnitude limit (s up to about 2) and the exact one above it; at
-    K <= 64 every tile takes the tensor-core routing and the rows above the limit its exact
+    one below its magnitude limit (s up to about 2) and the exact one above it; at the
+    other K every tile takes the tensor-core routing and the rows above the limit its exact
     path.  A last tile mixes N(0, 1) rows with one row of s = 6.  Each tile's posteriors
     must match the oracle's."""
     import oracle
@@ -178,7 +187,8 @@ CAUSAL = [
     (W["causal_8k_K256"], 2, 0),
     (W["causal_8k_K512"], 2, 0),
     # tensor-core path with component groups: K < 128 padded, K = 256 / 384, bf16 and split operands,
-    # ragged chunks, more chunks than SMs; K = 200 stays on CUDA cores
+    # ragged chunks, more chunks than SMs; K = 200 stays on CUDA cores (its routing, like that of
+    # K = 100 and 256 at d = 64, takes the wide tensor-core form)
     (W["tiny"].with_(B=2, H=2, N=1000, d=64, dv=64, K=100), None, 0),
     (W["tiny"].with_(B=2, H=2, N=700, d=32, dv=64, K=8), None, 0),
     (W["tiny"].with_(B=2, H=2, N=1000, d=64, dv=64, K=256), None, 0),
