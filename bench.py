@@ -123,8 +123,8 @@ def stage_work(stage, wl):
     if stage in ("resp_q", "resp_k"):
         # K = 128, d = 64: the bound GEMM [x^2 | x] W has the same 4*K*d flop per row and runs on the
         # tensor pipe (bf16); the exact evaluation of the kept components is data-dependent extra work.
-        # 17 <= K <= 256 otherwise, d = 64: every log-joint on the tensor pipe, the dense pass's bf16
-        # passes of a product K_N wide (K rounded up to 32, 64, 128 or 256)
+        # 17 <= K <= 512 otherwise, d = 64: every log-joint on the tensor pipe, the dense pass's bf16
+        # passes of a product K_N wide (K rounded up to 32, 64, 128, 256 or 512)
         if tc_routing(wl):
             kn = tc_width(K)
             return dense_passes(wl) * 4.0 * kn * d * ht, "tensor_bf16", (d * xb + K * gb) * ht
@@ -254,14 +254,15 @@ def bounded_routing(wl):
 
 
 def tc_routing(wl):
-    """The library's tensor-core routing for 17 <= K <= 256 applies (d = 64; K = 128 has the
+    """The library's tensor-core routing for 17 <= K <= 512 applies (d = 64; K = 128 has the
     bounded routing instead)."""
-    return wl.d == 64 and 17 <= wl.K <= 256 and not bounded_routing(wl)
+    return wl.d == 64 and 17 <= wl.K <= 512 and not bounded_routing(wl)
 
 
 def tc_width(K):
-    """Components of the tensor-core routing's product: K rounded up to 32, 64, 128 or 256."""
-    return next(w for w in (32, 64, 128, 256) if K <= w)
+    """Components of the tensor-core routing's product: K rounded up to 32, 64, 128, 256 or
+    512 (two CTAs of 256)."""
+    return next(w for w in (32, 64, 128, 256, 512) if K <= w)
 
 
 def pipe_peak(pipe, wl, pk):

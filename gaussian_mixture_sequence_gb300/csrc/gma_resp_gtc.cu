@@ -67,8 +67,10 @@ struct GtcImg {
 
 size_t gtc_pitch(int KN)
 {
-    return KN <= 32 ? GtcImg<32>::pitch
-                    : (KN <= 64 ? GtcImg<64>::pitch : (KN <= 128 ? GtcImg<128>::pitch : GtcImg<256>::pitch));
+    return KN <= 32    ? GtcImg<32>::pitch
+           : KN <= 64  ? GtcImg<64>::pitch
+           : KN <= 128 ? GtcImg<128>::pitch
+                       : (size_t)(KN / 256) * GtcImg<256>::pitch;   // 512: two images of 256
 }
 
 // v = p0 + p1 + p2 + r with p0, p1, p2 bf16 and |r| <= 2^-24 |v|.
@@ -82,16 +84,17 @@ __device__ __forceinline__ void split3(float v, unsigned short (&p)[3])
     }
 }
 
-// Grid H, KN * 4 threads: component k = tid / 4 takes feature pairs 8 (tid % 4) .. + 7
-// from the packed parameters {s, s', -mu s, -mu' s'} and c_k that k_prep wrote.
+// Grid (H, halves), KN * 4 threads: component k = KN y + tid / 4 takes feature pairs
+// 8 (tid % 4) .. + 7 from the packed parameters {s, s', -mu s, -mu' s'} and c_k that k_prep
+// wrote, into image y of head h (past 256 components a head has two images of 256).
 template <int KN>
 __global__ void __launch_bounds__(KN * 4)
     k_prep_gtc(int K, const float4 *__restrict__ prm, const float *__restrict__ cst, unsigned char *__restrict__ img)
 {
     __shared__ float red[2][KN * 4 / 32];
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int k = tid >> 2, part = tid & 3;
-    unsigned char *im = img + (long long)h * GtcImg<KN>::pitch;
+    const int kl = tid >> 2, k = KN * blockIdx.y + kl, part = tid & 3;
+    unsigned char *im = img + ((long long)h * gridDim.y + blockIdx.y) * GtcImg<KN>::pitch;
     float amu2 = 0.f, amax = 0.f, mmax = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -108,9 +111,9 @@ __global__ void __launch_bounds__(KN * 4)
         split3(wb1, b1);
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl) {
-            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(k, gtc_pos(f), pl)) =
+            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(kl, gtc_pos(f), pl)) =
                 (uint32_t)a0[pl] | ((uint32_t)a1[pl] << 16);
-            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(k, gtc_pos(f) + 16, pl)) =
+            *reinterpret_cast<uint32_t *>(im + GtcImg<KN>::off(kl, gtc_pos(f) + 16, pl)) =
                 (uint32_t)b0[pl] | ((uint32_t)b1[pl] << 16);
         }
     }
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(KN * 4)
         mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     }
     float *c = reinterpret_cast<float *>(im + GtcImg<KN>::W);
-    if (part == 0) c[k] = k < K ? cst[(long long)h * K + k] - 0.5f * amu2 : kQOff;
+    if (part == 0) c[kl] = k < K ? cst[(long long)h * K + k] - 0.5f * amu2 : kQOff;
     // head-wide maxima of a and |a mu|
     for (int o = 4; o < 32; o <<= 1) {
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -447,8 +450,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // ---- KN = 128 or 256 (65 <= K <= 256, d = 64): one product per plane pair, N = KN ----
+// ---- and K up to 512 as a cluster of two CTAs per tile, 256 components each          ----
 //
-// One CTA per tile of 128 rows.  The accumulator holds all KN log-joints of a row (TMEM
+// One CTA (NH = 1) or a cluster of two (NH = 2, CTA r taking components 256 r ..) per
+// tile of 128 rows.  The accumulator holds all KN log-joints of a row (TMEM
 // columns 256 ..; the operand planes at 0 .. 191).  The three planes of W do not fit
 // in shared memory beside the output tile, so they pass through two buffers, P and Q,
 // and the products are taken in the order the planes arrive: plane 1 into P and plane 2
@@ -456,7 +461,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // (0,0).  The terms before the last are at most 2^-8 of the log-joint, so the order keeps
 // the rounding of one fp32 evaluation.  The routing tile shares the output tile's
 // space (it is consumed before the first product).  Each thread then owns KN / 4
-// components of its row; the posteriors leave in halves of 128 components.
+// components of its row; with two CTAs each row's maximum and sum pass to the other CTA
+// through distributed shared memory; the posteriors leave in halves of 128 components.
 template <int KN>
 struct GtcWSmem {
     static constexpr uint32_t WB = KN * 256;             // one plane of W
@@ -465,12 +471,34 @@ struct GtcWSmem {
     static constexpr uint32_t C = GtcImg<KN>::C;         // c', A, M
     static constexpr uint32_t EX = 4 * kQRows * 8;       // per quarter and row: (max, sum)
     static constexpr uint32_t SS = 4 * kQRows * 8;       // per quarter and row: (sum x^2, sum |x|)
-    static constexpr size_t bytes = 1024 + 2 * (size_t)WB + O + C + EX + SS + 64;
+    static constexpr uint32_t XS = kQRows * 8;           // per row: the CTA's (max, sum), read by the other
+    static constexpr size_t bytes = 1024 + 2 * (size_t)WB + O + C + EX + SS + XS + 64;
 };
 static_assert(GtcWSmem<256>::bytes <= 232448, "wide tensor-core routing: shared memory above the per-block limit");
 static_assert(kQRows * kQD * 4 <= GtcWSmem<256>::O, "the routing tile fits in the output tile's space");
 
-template <int KN>
+// All threads of both CTAs of the cluster (release / acquire of shared memory).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// A float2 of the shared memory of CTA `rank` of the cluster, at this CTA's address p.
+__device__ __forceinline__ float2 ld_cluster_f2(const void *p, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(p)), "r"(rank));
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra) : "memory");
+    return v;
+}
+
+template <int KN, int NH>
 __global__ void __launch_bounds__(kQThreads, 1)
     k_resp_gtc_wide(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
                     const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, bool x_bf16,
@@ -486,9 +514,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, cq = warp >> 2;
     const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
-    const int bh = blockIdx.x / tps, t = blockIdx.x % tps, h = bh % H;
+    const int item = blockIdx.x / NH;
+    const uint32_t rank = NH == 1 ? 0u : cluster_rank();
+    const int bh = item / tps, t = item % tps, h = bh % H;
     const int row = t * kQRows + i;
-    const unsigned char *src = img + (long long)h * IM::pitch;
+    const int kbase = KN * (int)rank;   // this CTA's first component
+    const unsigned char *src = img + ((long long)h * NH + rank) * IM::pitch;
 
     unsigned char *wp = sm;              // buffer P: plane 1
     unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2, then plane 0
@@ -497,7 +528,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     float *c_s = reinterpret_cast<float *>(ob + SM::O);       // [KN + 4]
     float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);  // [4][128]
     float2 *ss_s = ex_s + 4 * kQRows;                         // [4][128]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 4 * kQRows);
+    float2 *xs_s = ss_s + 4 * kQRows;                         // [128]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(xs_s + kQRows);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
     // P landed, Q landed (twice), constants landed, routing tile landed, (0,2) done, all done
     const uint32_t BAR_P = smem_addr(bar), BAR_Q = smem_addr(bar + 1), BAR_C = smem_addr(bar + 2);
@@ -641,7 +673,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const long long xo = ((long long)bh * N + row) * kQD;
         exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
                          : (const void *)(static_cast<const float *>(xg) + xo),
-                  x_bf16, prm, cst, h, K, QC * cq, QC, lex);
+                  x_bf16, prm, cst, h, K, kbase + QC * cq, QC, lex);
 #pragma unroll
         for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
     }
@@ -662,10 +694,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
         float2 e4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
-        const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+        float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
         float tot = 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
+        if constexpr (NH == 2) {   // the row's maximum and sum over the other CTA's components too
+            if (cq == 0) xs_s[i] = make_float2(mrow, tot);
+            cluster_sync();
+            const float2 pe = ld_cluster_f2(xs_s + i, rank ^ 1u);
+            const float m2 = fmaxf(mrow, pe.x);
+            tot = tot * ex2_sfu((mrow - m2) * kQLog2e) + pe.y * ex2_sfu((pe.x - m2) * kQLog2e);
+            mrow = m2;
+        }
         const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
         const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
@@ -711,7 +751,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (tid == 0 && ok) {
             const int per = 128 / ge;   // columns of one 128-byte box
             for (int a = 0; a < 128 / per; ++a) {
-                const int x0 = 128 * hf + a * per;
+                const int x0 = kbase + 128 * hf + a * per;
                 if (x0 >= ow) break;
                 tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
                 if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
@@ -735,16 +775,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     fence_before_sync();
     __syncthreads();
+    if constexpr (NH == 2) cluster_sync();   // the other CTA has read this one's (max, sum)
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-int gtc_width(int K) { return K <= 32 ? 32 : (K <= 64 ? 64 : (K <= 128 ? 128 : 256)); }
+int gtc_width(int K) { return K <= 32 ? 32 : (K <= 64 ? 64 : (K <= 128 ? 128 : (K <= 256 ? 256 : 512))); }
 
 } // namespace
 
 bool resp_gtc_applies(const Dims &dm)
 {
-    return dm.D == kQD && dm.K >= 17 && dm.K <= 256 && !resp_pruned_applies(dm);
+    return dm.D == kQD && dm.K >= 17 && dm.K <= 512 && !resp_pruned_applies(dm);
 }
 
 size_t gtc_image_bytes(const Dims &dm) { return resp_gtc_applies(dm) ? dm.H * gtc_pitch(gtc_width(dm.K)) : 0; }
@@ -756,7 +797,8 @@ cudaError_t launch_prep_gtc(const Dims &dm, const float4 *prm, const float *cst,
     case 32: k_prep_gtc<32><<<dm.H, 32 * 4, 0, st>>>(dm.K, prm, cst, img); break;
     case 64: k_prep_gtc<64><<<dm.H, 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
     case 128: k_prep_gtc<128><<<dm.H, 128 * 4, 0, st>>>(dm.K, prm, cst, img); break;
-    default: k_prep_gtc<256><<<dm.H, 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 256: k_prep_gtc<256><<<dm.H, 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    default: k_prep_gtc<256><<<dim3(dm.H, 2), 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
     }
     return cudaGetLastError();
 }
@@ -774,12 +816,14 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
                        void *gamma, int ldg, int layout, cudaStream_t st)
 {
     constexpr bool wide = KN > 64;
+    constexpr int NH = KN > 256 ? 2 : 1;   // CTAs per tile
     size_t smem;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, int, int, int, int, bool, const void *, const unsigned char *,
                  const float4 *, const float *, int, int, unsigned int *);
     if constexpr (wide) {
-        smem = GtcWSmem<KN>::bytes;
-        kern = k_resp_gtc_wide<KN>;
+        constexpr int KC = KN / NH;   // components of one CTA
+        smem = GtcWSmem<KC>::bytes;
+        kern = k_resp_gtc_wide<KC, NH>;
     } else {
         smem = GtcSmem<KN>::bytes;
         kern = k_resp_gtc<KN>;
@@ -804,10 +848,27 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
     }
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kern<<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img, prm,
-                                                   cst, layout, ldg, flag);
-    return cudaGetLastError();
+    if (items * NH > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if constexpr (NH == 1) {
+        kern<<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img,
+                                                       prm, cst, layout, ldg, flag);
+        return cudaGetLastError();
+    } else {   // the two CTAs of a tile as one cluster
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(items * NH));
+        cfg.blockDim = dim3(kQThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = NH;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img, prm, cst,
+                                  layout, ldg, flag);
+    }
 }
 
 cudaError_t launch_resp_gtc(const Dims &dm, const unsigned char *img, const float4 *prm, const float *cst,
@@ -818,7 +879,8 @@ cudaError_t launch_resp_gtc(const Dims &dm, const unsigned char *img, const floa
     case 32: return launch_gtc<32>(dm, img, prm, cst, x, gamma, ldg, layout, st);
     case 64: return launch_gtc<64>(dm, img, prm, cst, x, gamma, ldg, layout, st);
     case 128: return launch_gtc<128>(dm, img, prm, cst, x, gamma, ldg, layout, st);
-    default: return launch_gtc<256>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    case 256: return launch_gtc<256>(dm, img, prm, cst, x, gamma, ldg, layout, st);
+    default: return launch_gtc<512>(dm, img, prm, cst, x, gamma, ldg, layout, st);
     }
 }
 

@@ -94,9 +94,9 @@ def test_bounded_routing_roofline():
     dense = bench.roofline_of("resp_q", W["causal_4k"], 300e-6, pk, kept=64.0)
     assert dense["bound"] == "alu"
     assert dense["algorithmic_flop"] == 4 * 64 * 64.0 * 4 * 8 * 4096
-    # the generic kernel (here K = 512) is charged the dense routing on the FP32 pipe
-    g = bench.roofline_of("resp_q", W["causal_8k_K512"], 1300e-6, pk)
-    assert g["bound"] == "alu" and g["algorithmic_flop"] == 4 * 512 * 64 * 4 * 8 * 8192
+    # the generic kernel (here d = 128) is charged the dense routing on the FP32 pipe
+    g = bench.roofline_of("resp_q", W["causal_8k_K512"].with_(d=128), 2600e-6, pk)
+    assert g["bound"] == "alu" and g["algorithmic_flop"] == 4 * 512 * 128 * 4 * 8 * 8192
 
 
 def test_dense_pass_roofline():
@@ -198,9 +198,9 @@ def test_tokens_per_step():
 
 
 def test_small_k_routing_roofline():
-    """For 17 <= K <= 256 but 128 with d = 64 both routings are tensor work (the six bf16
-    passes of a product 32, 64, 128 or 256 components wide) and carry no FP32 work in the
-    whole-step roofline."""
+    """For 17 <= K <= 512 but 128 with d = 64 both routings are tensor work (the six bf16
+    passes of a product 32, 64, 128, 256 or 512 components wide) and carry no FP32 work in
+    the whole-step roofline."""
     pk = dict(bench.FALLBACK)
     wl = W["causal_8k_K32"]
     ht = wl.B * wl.H * wl.N
@@ -215,7 +215,8 @@ def test_small_k_routing_roofline():
     assert pipe == "tensor_bf16" and f == 6 * 4 * 256 * 64 * ht
     assert bench.stage_work("resp_q", W["causal_8k_K256"].with_(K=100))[0] == 6 * 4 * 128 * 64 * ht
     assert bench.stage_work("resp_q", W["causal_8k_K256"].with_(x_dtype="bf16"))[0] == 4 * 4 * 256 * 64 * ht
-    # K = 128 has the bounded routing; K = 512 and d = 128 keep the CUDA-core routing
+    assert bench.stage_work("resp_q", W["causal_8k_K512"])[0] == 6 * 4 * 512 * 64 * ht
+    # K = 128 has the bounded routing; K above 512 and d = 128 keep the CUDA-core routing
     assert not bench.tc_routing(W["causal_4k"])
-    assert bench.stage_work("resp_q", W["causal_8k_K512"])[1] == "alu"
+    assert bench.stage_work("resp_q", W["causal_8k_K512"].with_(K=520))[1] == "alu"
     assert bench.stage_work("resp_q", W["causal_8k_K256"].with_(d=128))[1] == "alu"

@@ -57,6 +57,11 @@ def _report(name, err, tol):
     (W["tiny"].with_(K=100, d=64, N=777, H=2), None),
     (W["tiny"].with_(K=72, d=64, N=300, H=2, x_dtype="bf16"), None),
     (W["causal_8k_K256"], 2),
+    # 256 < K <= 512 (d = 64): two CTAs per tile as a cluster, the softmax's row maxima and
+    # sums exchanged between them
+    (W["tiny"].with_(K=512, d=64, N=1000, B=2, H=2), None),
+    (W["tiny"].with_(K=384, d=64, N=555, H=3, x_dtype="bf16"), None),
+    (W["tiny"].with_(K=300, d=64, N=300, H=2), None),
 ])
 def test_responsibilities(wl, sample):
     c = Case(wl, None if sample is None else workloads.sample_slices(wl, sample))
@@ -97,7 +102,7 @@ def test_responsibilities_adversarial_rows():
 
 
 @pytest.mark.parametrize("K,x_dtype", [(128, "f32"), (128, "bf16"), (64, "f32"), (40, "bf16"), (32, "f32"),
-                                     (256, "f32"), (96, "bf16")])
+                                     (256, "f32"), (96, "bf16"), (512, "f32")])
 def test_responsibilities_dense_tiles_across_scales(K, x_dtype):
     """Tiles of N(0, s^2) rows, one scale per tile of 128 rows, from s = 0.3 to s = 6.  At
     K = 128 the wide tiles keep many components and go to the dense passes, the tensor-core
