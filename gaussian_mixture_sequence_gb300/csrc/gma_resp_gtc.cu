@@ -1,4 +1,4 @@
-// Responsibilities (S1) on the tensor cores for 17 <= K <= 256 components (K = 128
+// Responsibilities (S1) on the tensor cores for 17 <= K <= 512 components (K = 128
 // has the bounded routing of its own) and d_route = 64: every log-joint of every row,
 // for any inputs.
 //
@@ -7,7 +7,7 @@
 //   l_ik = c_k - 1/2 sum_d ((x_id - mu_kd) / sigma_kd)^2
 //        = c'_k + sum_d ( -1/2 a_kd x_id^2 + a_kd mu_kd x_id ),   a = 1/sigma^2,
 // one product of [x^2 | x] (128 rows x 128) with W^T (128 x KN components) per
-// tile of 128 rows, KN = K rounded up to 32, 64, 128 or 256 (the components past K
+// tile of 128 rows, KN = K rounded up to 32, 64, 128, 256 or 512 (the components past K
 // have W = 0 and c' = -1e30, so their posterior is 0).  As in the dense pass of the
 // K = 128 routing, each fp32 operand is held as three bf16 planes (v = v0 + v1
 // + v2 up to 2^-24 |v|) and the six plane products whose orders add up to at
@@ -20,15 +20,22 @@
 // the values are one plane and their squares two, and the products of the zero
 // planes are skipped.
 //
-// One CTA of 16 warps per tile of 128 rows: the head's planes of W (3 x KN x 256
-// B, in chunks of 64 components past KN = 64) and constants are bulk-copied while
-// the routing tile arrives by TMA; warp w owns TMEM lanes 32 (w % 4) .. + 31 (rows)
-// and quarter q = w / 4: operand positions 32 q .. 32 q + 31 (the squares, then the
-// values, of features 16 q .. 16 q + 15) and components KN q / 4 .. of the result;
-// one thread issues the products; the warps take the softmax from the accumulator
-// and assemble the output tile, which leaves by TMA stores.  (A persistent form that
-// pipelined several tiles per CTA gave wrong products for every tile after a CTA's
-// first; the one-tile form is the one kept.)
+// K <= 64: one persistent CTA of 16 warps per SM over a contiguous range of the
+// (slice, tile) items of one routing; the head's planes of W (3 x KN x 256 B) are
+// bulk-copied when the head changes.  Warp w owns TMEM lanes 32 (w % 4) .. + 31
+// (rows) and quarter q = w / 4: operand positions 32 q .. 32 q + 31 (the squares,
+// then the values, of features 16 q .. 16 q + 15) and components KN q / 4 .. of
+// the result.  The operand planes are double-buffered in TMEM and the accumulator
+// is read out before the next products are issued, so the products of item n + 1
+// run while the warps take the softmax of item n and split the routing tile of
+// item n + 2; the output tiles are double-buffered too, so a tile's TMA store
+// drains while the next one is written.  Past 64 components one CTA (or a cluster
+// of two) takes one tile (k_resp_gtc_wide below).
+//
+// Within each product the K steps of the values (odd) are issued before those of
+// the squares (even): in ascending order some odd steps were measured to take W
+// from the step before them (the products of the first tile of a CTA were exact,
+// later ones not), and in this order every product matches its fp64 terms.
 #include "gma_internal.cuh"
 #include "gma_tc.cuh"
 
@@ -211,72 +218,76 @@ struct GtcSmem {
     static constexpr uint32_t W = GtcImg<KN>::W;        // three planes of W
     static constexpr uint32_t WA = (W + 1023u) & ~1023u;
     static constexpr uint32_t X = kQRows * kQD * 4;     // routing tile (fp32 worst case)
-    static constexpr uint32_t O = kQRows * 128 * 4;     // output tile (fp32 worst case, 128 columns)
-    static constexpr uint32_t C = GtcImg<KN>::C;        // c', A, M
+    static constexpr uint32_t O = kQRows * 128 * 4;     // one output tile (fp32 worst case, 128 columns)
+    static constexpr uint32_t C = 2 * GtcImg<KN>::C;    // c', A, M of two heads
     static constexpr uint32_t EX = 4 * kQRows * 8;      // per quarter and row: (max, sum)
-    static constexpr uint32_t SS = 4 * kQRows * 8;      // per quarter and row: (sum x^2, sum |x|)
-    static constexpr size_t bytes = 1024 + (size_t)WA + X + O + C + EX + SS + 64;
+    static constexpr uint32_t SS = 2 * 4 * kQRows * 8;  // per item of two, quarter, row: (sum x^2, sum |x|)
+    static constexpr size_t bytes = 1024 + (size_t)WA + X + 2 * (size_t)O + C + EX + SS + 64;
 };
 static_assert(GtcSmem<64>::bytes <= 232448, "small-K tensor-core routing: shared memory above the per-block limit");
 
-// One CTA per tile of 128 rows (blockIdx.x = slice * tiles per slice + tile).
 template <int KN>
 __global__ void __launch_bounds__(kQThreads, 1)
     k_resp_gtc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
-               const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, bool x_bf16,
-               const void *__restrict__ xg, const unsigned char *__restrict__ img, const float4 *__restrict__ prm,
-               const float *__restrict__ cst, int layout, int ow, unsigned int *timeout)
+               const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, long long items,
+               bool x_bf16, const void *__restrict__ xg, const unsigned char *__restrict__ img,
+               const float4 *__restrict__ prm, const float *__restrict__ cst, int layout, int ow,
+               unsigned int *timeout)
 {
     constexpr int QC = KN / 4;   // components of a row per thread
     using SM = GtcSmem<KN>;
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ float2 am_s[2];   // A, M of the heads in the two constants' buffers
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, cq = warp >> 2;
     const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
-    const int bh = blockIdx.x / tps, t = blockIdx.x % tps, h = bh % H;
-    const int row = t * kQRows + i;
+
+    const long long per = (items + gridDim.x - 1) / gridDim.x;
+    const long long it0 = min(items, (long long)blockIdx.x * per), it1 = min(items, it0 + per);
+    if (it0 >= it1) return;
+    const int cnt = (int)(it1 - it0);
 
     unsigned char *w_s = sm;
     unsigned char *xb = w_s + SM::WA;
-    unsigned char *ob = xb + SM::X;
-    float *c_s = reinterpret_cast<float *>(ob + SM::O);                  // [KN + 4]
-    float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);             // [4][128]
-    float2 *ss_s = ex_s + 4 * kQRows;                                    // [4][128]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 4 * kQRows);
+    unsigned char *ob = xb + SM::X;   // two output tiles
+    float *c_s = reinterpret_cast<float *>(ob + 2 * SM::O);   // [2][KN + 4]
+    float2 *ex_s = reinterpret_cast<float2 *>(c_s + 2 * (KN + 4));
+    float2 *ss_s = ex_s + 4 * kQRows;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ss_s + 2 * 4 * kQRows);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
     const uint32_t BAR_I = smem_addr(bar), BAR_X = smem_addr(bar + 1), BAR_M = smem_addr(bar + 2);
+    const uint32_t xbytes = kQRows * kQD * (x_bf16 ? 2 : 4);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's tile follows the hi plane's
-    constexpr uint32_t D_COL = 192;             // the accumulator; operand planes at 64 j
-
-    if (warp == 0) {
-        tmem_alloc(smem_addr(tslot), 256);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
-        mbar_init_fence();
-        const unsigned char *src = img + (long long)h * GtcImg<KN>::pitch;
-        mbar_expect_tx(BAR_I, SM::W + SM::C);
-        bulk_g2s(smem_addr(w_s), src, SM::W, BAR_I);
-        bulk_g2s(smem_addr(c_s), src + SM::W, SM::C, BAR_I);
-        mbar_expect_tx(BAR_X, kQRows * kQD * (x_bf16 ? 2 : 4));
-        tma_load_3d(smem_addr(xb), &xmap, 0, t * kQRows, bh, BAR_X);
-        if (!x_bf16) tma_load_3d(smem_addr(xb + kQRows * 128), &xmap, 32, t * kQRows, bh, BAR_X);
-    }
-    // the output tile starts as zeros: the columns past the components stay so
-    for (int o = tid; o < (int)(SM::O / 16); o += kQThreads) reinterpret_cast<uint4 *>(ob)[o] = make_uint4(0u, 0u, 0u, 0u);
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tbase = *tslot;
-    bool ok = mbar_wait(BAR_X, 0u);
-
-    // features 16 cq .. + 15 of row i: squares and values into the three planes, and the
-    // row's sums for S_i
-    {
+    constexpr uint32_t D_COL = 384;             // the accumulator; operand planes at 192 b + 64 j
+    uint32_t tbase = 0;
+    auto slice_of = [&](int n) { return (int)((it0 + n) / tps); };
+    auto tile_of = [&](int n) { return (int)((it0 + n) % tps); };
+    auto load_x = [&](int n) {   // one thread
+        mbar_expect_tx(BAR_X, xbytes);
+        tma_load_3d(smem_addr(xb), &xmap, 0, tile_of(n) * kQRows, slice_of(n), BAR_X);
+        if (!x_bf16) tma_load_3d(smem_addr(xb + kQRows * 128), &xmap, 32, tile_of(n) * kQRows, slice_of(n), BAR_X);
+    };
+    int nimg = 0;
+    // the planes of W and the constants of `head` into buffer `buf` (every thread; no
+    // products may be running)
+    auto load_head = [&](int head, int buf) {
+        if (tid == 0) {
+            fence_proxy_async();   // earlier thread reads of the constants' buffer come first
+            mbar_expect_tx(BAR_I, SM::W + GtcImg<KN>::C);
+            const unsigned char *src = img + (long long)head * GtcImg<KN>::pitch;
+            bulk_g2s(smem_addr(w_s), src, SM::W, BAR_I);
+            bulk_g2s(smem_addr(c_s + buf * (KN + 4)), src + SM::W, GtcImg<KN>::C, BAR_I);
+        }
+        const bool got = mbar_wait(BAR_I, (uint32_t)(nimg & 1));
+        ++nimg;
+        if (tid == 0) am_s[buf] = make_float2(c_s[buf * (KN + 4) + KN], c_s[buf * (KN + 4) + KN + 1]);
+        return got;
+    };
+    // item n's landed routing tile into operand buffer n % 2, and its rows' sums for S_i
+    auto convert = [&](int n) {
         float2 xv[8];
         if (x_bf16) {
 #pragma unroll
@@ -305,21 +316,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
             split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
             split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
         }
+        const uint32_t acol = 192u * (uint32_t)(n & 1) + 16u * (uint32_t)cq;
 #pragma unroll
-        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
-        ss_s[cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
+        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, acol + 64 * j), pw[j]);
+        ss_s[(n & 1) * 4 * kQRows + cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
         tmem_wait_st();
-    }
-    ok = mbar_wait(BAR_I, 0u) && ok;   // the planes of W and the constants
-    fence_before_sync();
-    ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM
-    fence_after_sync();
-    // one thread: the products, smallest first; with bf16 rows the values' lower planes and
-    // the squares' third plane are zero
-    bool issued = false;   // (thread 0)
-    if (tid == 0 && ok) {
-        issued = true;
-        const uint32_t id = idesc(128, KN, kFmtBF16);
+    };
+    // one thread: item n's products (operand buffer n % 2) into the accumulator, smallest
+    // first, each with its values' (odd) K steps before its squares' (even) ones; with bf16
+    // rows the values' lower planes and the squares' third plane are zero
+    const uint32_t id = idesc(128, KN, kFmtBF16);
+    auto issue = [&](int n) {
+        const uint32_t ab = 192u * (uint32_t)(n & 1);
         bool first = true;
 #pragma unroll
         for (int q = 0; q < 6; ++q) {
@@ -327,126 +335,236 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);    // W plane
             if (x_bf16 && pa == 2) continue;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int s8 = 0; s8 < 8; ++s8) {
+                const int kk = s8 < 4 ? 2 * s8 + 1 : 2 * (s8 - 4);
                 if (x_bf16 && pa == 1 && (kk & 1)) continue;   // odd K steps: the values
                 const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
                 const uint32_t boff = pb * (uint32_t)(KN * 256) + (kb >> 7) * (KN * 128) + (kb & 127);
-                mma_ts(0u, tbase + D_COL, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
+                mma_ts(0u, tbase + D_COL, tbase + ab + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
                        first ? 0u : 1u);
                 first = false;
             }
         }
         mma_commit(BAR_M);
+    };
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tslot), 512);
+        tmem_relinquish();
     }
-    if (ok) ok = mbar_wait(BAR_M, 0u);
-    fence_after_sync();
-    float2 acc[QC / 2];
-    {
-        uint32_t r[QC];
-        if constexpr (QC == 16) {
-            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq), reinterpret_cast<uint32_t(&)[16]>(r));
-        } else {
-            uint32_t r16[16];   // columns QC cq .. + 7 of a 16-wide read (the other half belongs to
-                                // the neighbouring quarter)
-            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 16 * (cq >> 1)), r16);
-#pragma unroll
-            for (int j = 0; j < QC; ++j) r[j] = r16[8 * (cq & 1) + j];
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
-    }
-    // log-joints (rows beyond the magnitude limit exactly), then the softmax over the four
-    // quarters of the row
-    const float2 am = make_float2(c_s[KN], c_s[KN + 1]);
-    const float2 *sp = ss_s + i;
-    const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
-    const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
-    const float *cb = c_s + QC * cq;   // c'_k of this thread's components
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
-    if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
-        float lex[QC];
-        const long long xo = ((long long)bh * N + row) * kQD;
-        exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
-                         : (const void *)(static_cast<const float *>(xg) + xo),
-                  x_bf16, prm, cst, h, K, QC * cq, QC, lex);
-#pragma unroll
-        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
-    }
-    float mq = -FLT_MAX;
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
-    const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
-    float2 sq2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) {
-        const float2 tt = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
-        acc[p] = make_float2(ex2_sfu(tt.x), ex2_sfu(tt.y));
-        sq2 = __fadd2_rn(sq2, acc[p]);
-    }
-    ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
-    __syncthreads();
-    float2 e4[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
-    const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
-    float tot = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
-    const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
-    const float2 sc2 = make_float2(sc, sc);
-    if (g_f32) {
-#pragma unroll
-        for (int g = 0; g < QC / 4; ++g) {
-            const float2 a = __fmul2_rn(acc[2 * g], sc2), b = __fmul2_rn(acc[2 * g + 1], sc2);
-            *reinterpret_cast<float4 *>(ob + sw128_offset(i, QC * cq + 4 * g, kQRows, 4)) = make_float4(a.x, a.y, b.x, b.y);
-        }
-    } else {
-        const float2 m1 = make_float2(-1.f, -1.f);
-#pragma unroll
-        for (int g = 0; g < QC / 8; ++g) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 v = __fmul2_rn(acc[4 * g + u], sc2);
-                __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-                hw[u] = *reinterpret_cast<const uint32_t *>(&b);
-                const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)),
-                                            m1, v);
-                b = __floats2bfloat162_rn(r.x, r.y);
-                lw[u] = *reinterpret_cast<const uint32_t *>(&b);
-            }
-            const uint32_t off = sw128_offset(i, QC * cq + 8 * g, kQRows, 2);
-            *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-    }
-    fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
-    fence_before_sync();
-    ok = __syncthreads_and(ok) != 0;
     if (tid == 0) {
-        if (ok) {
-            const int boxes = (ow * ge + 127) / 128;
-            for (int a = 0; a < boxes; ++a) {
-                tma_store_3d(&gmap, a * (128 / ge), t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
-                if (g_split)
-                    tma_store_3d(&gmap_lo, a * (128 / ge), t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
-            }
-            bulk_commit();
-        } else {
-            // after a failed wait the products or a copy may still be in flight: let them end
-            // (bounded; a wait on a phase that has completed returns at once)
-            mbar_wait(BAR_I, 0u);
-            mbar_wait(BAR_X, 0u);
-            if (issued) mbar_wait(BAR_M, 0u);
-            report_timeout(timeout);
-        }
-        bulk_wait_read();   // the output tile has left shared memory
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
+        mbar_init_fence();
+        load_x(0);
     }
+    // both output tiles start as zeros: the columns past the components stay so
+    for (int o = tid; o < (int)(2 * SM::O / 16); o += kQThreads)
+        reinterpret_cast<uint4 *>(ob)[o] = make_uint4(0u, 0u, 0u, 0u);
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    fence_after_sync();
+    tbase = *tslot;
+    int head = slice_of(0) % H;
+    bool ok = load_head(head, 0);
+    int hp = 0;                        // constants' buffer of item n's head
+    uint32_t x_par = 0;                // tid 0: phase of the last routing tile fetched,
+    int m_issued = -1;                 // and the last item whose products were issued
+    ok = mbar_wait(BAR_X, 0u) && ok;
+    convert(0);
+    fence_before_sync();
+    ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, am_s is written
+    fence_after_sync();
+    if (tid == 0 && ok) {
+        issue(0);
+        m_issued = 0;
+        if (cnt > 1) {
+            load_x(1);
+            x_par = 1u;
+        }
+    }
+
+    float2 acc[QC / 2];                // the accumulator row of the previous item
+    int hpprev = hp;
+    // softmax of item m from acc into output tile m % 2 (rows beyond the magnitude limit
+    // evaluated exactly first)
+    auto softmax = [&](int m, int hpx) {
+        const int bh = slice_of(m), row = tile_of(m) * kQRows + i;
+        const float2 *sp = ss_s + (m & 1) * 4 * kQRows + i;
+        const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
+        const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
+        const float2 am = am_s[hpx];
+        const float *cb = c_s + hpx * (KN + 4) + QC * cq;   // c'_k of this thread's components
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
+        if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
+            // the direct form ((x - mu) / sigma)^2 of this thread's components, from global memory
+            const int h = bh % H;
+            float2 xr[kQDP];
+            if (x_bf16) {
+                const uint32_t *xw = reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(xg) +
+                                                                        ((long long)bh * N + row) * kQD);
+#pragma unroll
+                for (int dp = 0; dp < kQDP; ++dp)
+                    xr[dp] = make_float2(__uint_as_float(xw[dp] << 16), __uint_as_float(xw[dp] & 0xffff0000u));
+            } else {
+                const float2 *x2 = reinterpret_cast<const float2 *>(static_cast<const float *>(xg) +
+                                                                    ((long long)bh * N + row) * kQD);
+#pragma unroll
+                for (int dp = 0; dp < kQDP; ++dp) xr[dp] = x2[dp];
+            }
+#pragma unroll 1
+            for (int j = 0; j < QC; ++j) {
+                const int k = QC * cq + j;
+                float l = kQOff;
+                if (k < K) {
+                    const float4 *pk = prm + ((long long)h * K + k) * kQDP;
+                    float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+                    for (int dp = 0; dp < kQDP; ++dp) {
+                        const float4 p = pk[dp];
+                        const float2 y = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
+                        a2 = __ffma2_rn(y, y, a2);
+                    }
+                    l = fmaf(-0.5f, a2.x + a2.y, cst[(long long)h * K + k]);
+                }
+                if (j & 1) acc[j >> 1].y = l;
+                else acc[j >> 1].x = l;
+            }
+        }
+        float mq = -FLT_MAX;
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
+        const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
+        float2 sq2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) {
+            const float2 t = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
+            acc[p] = make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
+            sq2 = __fadd2_rn(sq2, acc[p]);
+        }
+        ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // the output tile of item m - 2 has left shared memory
+        __syncthreads();
+        float2 e4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
+        const float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+        float tot = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
+        const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
+        const float2 sc2 = make_float2(sc, sc);
+        unsigned char *o = ob + (m & 1) * SM::O;
+        if (g_f32) {
+#pragma unroll
+            for (int g = 0; g < QC / 4; ++g) {
+                const float2 a = __fmul2_rn(acc[2 * g], sc2), b = __fmul2_rn(acc[2 * g + 1], sc2);
+                *reinterpret_cast<float4 *>(o + sw128_offset(i, QC * cq + 4 * g, kQRows, 4)) =
+                    make_float4(a.x, a.y, b.x, b.y);
+            }
+        } else {
+            const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+            for (int g = 0; g < QC / 8; ++g) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 v = __fmul2_rn(acc[4 * g + u], sc2);
+                    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                    hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                    const float2 r = __ffma2_rn(
+                        make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
+                    b = __floats2bfloat162_rn(r.x, r.y);
+                    lw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+                const uint32_t off = sw128_offset(i, QC * cq + 8 * g, kQRows, 2);
+                *reinterpret_cast<uint4 *>(o + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if (g_split) *reinterpret_cast<uint4 *>(o + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+        fence_proxy_async();   // the output tile, written by threads, is read by the TMA store
+    };
+    // one thread, after a CTA barrier that follows the softmax of item m: its output tile out
+    auto finish = [&](int m) {
+        const unsigned char *o = ob + (m & 1) * SM::O;
+        const int bh = slice_of(m), t = tile_of(m);
+        const int boxes = (ow * ge + 127) / 128;
+        for (int a = 0; a < boxes; ++a) {
+            tma_store_3d(&gmap, a * (128 / ge), t * kQRows, bh, smem_addr(o + a * (kQRows * 128)));
+            if (g_split) tma_store_3d(&gmap_lo, a * (128 / ge), t * kQRows, bh, smem_addr(o + LO + a * (kQRows * 128)));
+        }
+        bulk_commit();
+    };
+
+    for (int n = 0; n < cnt && ok; ++n) {
+        // item n's products are running; acc holds item n - 1's accumulator row
+        if (n >= 1) softmax(n - 1, hpprev);
+        if (n + 1 < cnt) {   // item n + 1's routing tile into the other operand buffer
+            ok = mbar_wait(BAR_X, (uint32_t)((n + 1) & 1)) && ok;
+            convert(n + 1);
+        }
+        // item n's accumulator row into registers (free for item n + 1's products after the
+        // barrier below)
+        ok = mbar_wait(BAR_M, (uint32_t)(n & 1)) && ok;
+        fence_after_sync();
+        {
+            uint32_t r[QC];
+            if constexpr (QC == 16) {
+                tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq), reinterpret_cast<uint32_t(&)[16]>(r));
+            } else {
+                uint32_t r16[16];   // columns QC cq .. + 7 of a 16-wide read (the rest belongs to
+                                    // the next quarter and is not used)
+                tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 16 * (cq >> 1)), r16);
+#pragma unroll
+                for (int j = 0; j < QC; ++j) r[j] = r16[8 * (cq & 1) + j];
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
+        }
+        const int hpn = hp;
+        if (n + 1 < cnt && slice_of(n + 1) % H != head) {   // item n + 1 is of another head
+            head = slice_of(n + 1) % H;
+            hp ^= 1;   // the constants of item n's head stay for its softmax
+            ok = load_head(head, hp) && ok;
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(ok) != 0;   // operand planes written, accumulator read, softmax done
+        fence_after_sync();
+        if (tid == 0 && ok) {
+            // the routing tile was only read by threads (no proxy fence); its next contents
+            // and the previous item's output leave first, then the products start
+            if (n + 2 < cnt) {
+                load_x(n + 2);
+                x_par = (uint32_t)((n + 2) & 1);
+            }
+            if (n >= 1) finish(n - 1);
+            if (n + 1 < cnt) {
+                issue(n + 1);
+                m_issued = n + 1;
+            }
+        }
+        hpprev = hpn;
+    }
+    if (ok) {   // the last item's softmax and output
+        softmax(cnt - 1, hpprev);
+        ok = __syncthreads_and(ok) != 0;
+        if (tid == 0 && ok) finish(cnt - 1);
+    }
+    // after a failed wait a routing tile or products may still be in flight: let them finish
+    // (bounded) before TMEM and shared memory are released (a wait on a phase that has
+    // completed returns at once)
+    bool ok_end = ok;
+    if (tid == 0) {
+        if (!ok) {
+            ok_end = mbar_wait(BAR_X, x_par) && ok_end;
+            if (m_issued >= 0) ok_end = mbar_wait(BAR_M, (uint32_t)(m_issued & 1)) && ok_end;
+        }
+        bulk_wait_all();
+    }
+    fence_before_sync();
+    if (__syncthreads_and(ok_end) == 0 && tid == 0) report_timeout(timeout);
+    if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 // ---- KN = 128 or 256 (65 <= K <= 256, d = 64): one product per plane pair, N = KN ----
@@ -462,7 +580,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // the rounding of one fp32 evaluation.  The routing tile shares the output tile's
 // space (it is consumed before the first product).  Each thread then owns KN / 4
 // components of its row; with two CTAs each row's maximum and sum pass to the other CTA
-// through distributed shared memory; the posteriors leave in halves of 128 components.
+// through distributed shared memory; the posteriors leave in halves of 128 components,
+// the second staged in buffer P.
 template <int KN>
 struct GtcWSmem {
     static constexpr uint32_t WB = KN * 256;             // one plane of W
@@ -509,6 +628,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     constexpr int HALVES = KN / 128, QPH = 4 / HALVES;   // output halves; quarters of a row per half
     using SM = GtcWSmem<KN>;
     using IM = GtcImg<KN>;
+    static_assert(HALVES == 1 || SM::WB >= SM::O, "buffer P holds the second half of the output tile");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -711,53 +831,54 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int p = 0; p < QC / 2; ++p) acc[p] = __fmul2_rn(acc[p], sc2);
     }
-    // the posteriors in halves of 128 components: quarters QPH hf .. QPH hf + QPH - 1 write
-    // half hf
-#pragma unroll 1
-    for (int hf = 0; hf < HALVES; ++hf) {
-        if (hf > 0 && tid == 0) bulk_wait_read();   // the previous half has left shared memory
-        __syncthreads();
-        if (cq / QPH == hf) {
-            const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
-            if (g_f32) {
+    // the posteriors in halves of 128 components, quarters QPH hf .. QPH hf + QPH - 1 writing
+    // half hf: the first into the output tile, the second into buffer P, free once every
+    // product is done (ok is the same in every thread here)
+    {
+        const int hf = cq / QPH;
+        unsigned char *hb = (hf == 0 || !ok) ? ob : wp;
+        const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
+        if (g_f32) {
 #pragma unroll
-                for (int g = 0; g < QC / 4; ++g)
-                    *reinterpret_cast<float4 *>(ob + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
-                        make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
-            } else {
-                const float2 m1 = make_float2(-1.f, -1.f);
+            for (int g = 0; g < QC / 4; ++g)
+                *reinterpret_cast<float4 *>(hb + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
+                    make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
+        } else {
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
-                for (int g = 0; g < QC / 8; ++g) {
-                    uint32_t hw[4], lw[4];
+            for (int g = 0; g < QC / 8; ++g) {
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 v = acc[4 * g + u];
-                        __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-                        hw[u] = *reinterpret_cast<const uint32_t *>(&b);
-                        const float2 r = __ffma2_rn(
-                            make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
-                        b = __floats2bfloat162_rn(r.x, r.y);
-                        lw[u] = *reinterpret_cast<const uint32_t *>(&b);
-                    }
-                    const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
-                    *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                for (int u = 0; u < 4; ++u) {
+                    const float2 v = acc[4 * g + u];
+                    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                    hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                    const float2 r = __ffma2_rn(
+                        make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
+                    b = __floats2bfloat162_rn(r.x, r.y);
+                    lw[u] = *reinterpret_cast<const uint32_t *>(&b);
                 }
+                const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
+                *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if (g_split) *reinterpret_cast<uint4 *>(hb + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            fence_proxy_async();   // the half tile, written by threads, is read by the TMA store
         }
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0 && ok) {
-            const int per = 128 / ge;   // columns of one 128-byte box
+        fence_proxy_async();   // the half tiles, written by threads, are read by the TMA stores
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        const int per = 128 / ge;   // columns of one 128-byte box
+        for (int hf = 0; hf < HALVES; ++hf) {
+            const unsigned char *hb = hf == 0 ? ob : wp;
             for (int a = 0; a < 128 / per; ++a) {
                 const int x0 = kbase + 128 * hf + a * per;
                 if (x0 >= ow) break;
-                tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
-                if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
+                tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(hb + a * (kQRows * 128)));
+                if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(hb + LO + a * (kQRows * 128)));
             }
-            bulk_commit();
         }
+        bulk_commit();
     }
     if (tid == 0) {
         if (!ok) {
@@ -816,20 +937,15 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
                        void *gamma, int ldg, int layout, cudaStream_t st)
 {
     constexpr bool wide = KN > 64;
-    constexpr int NH = KN > 256 ? 2 : 1;   // CTAs per tile
-    size_t smem;
-    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, int, int, int, int, bool, const void *, const unsigned char *,
-                 const float4 *, const float *, int, int, unsigned int *);
-    if constexpr (wide) {
-        constexpr int KC = KN / NH;   // components of one CTA
-        smem = GtcWSmem<KC>::bytes;
-        kern = k_resp_gtc_wide<KC, NH>;
-    } else {
-        smem = GtcSmem<KN>::bytes;
-        kern = k_resp_gtc<KN>;
-    }
+    constexpr int NH = KN > 256 ? 2 : 1;   // CTAs per tile of the wide form
+    constexpr int KC = wide ? KN / NH : 64;
+    const size_t smem = wide ? GtcWSmem<KC>::bytes : GtcSmem<(wide ? 64 : KN)>::bytes;
     static std::atomic<unsigned long long> smem_set{0};
-    const cudaError_t attr = allow_smem(kern, smem, smem_set);
+    cudaError_t attr;
+    if constexpr (wide)
+        attr = allow_smem(k_resp_gtc_wide<KC, NH>, smem, smem_set);
+    else
+        attr = allow_smem(k_resp_gtc<KN>, smem, smem_set);
     if (attr != cudaSuccess) return attr;
     const int tps = (dm.N + kQRows - 1) / kQRows;
     const long long items = dm.BH() * tps;
@@ -849,9 +965,14 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     if (items * NH > 0x7fffffffLL) return cudaErrorInvalidValue;
-    if constexpr (NH == 1) {
-        kern<<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img,
-                                                       prm, cst, layout, ldg, flag);
+    if constexpr (!wide) {   // persistent: one CTA per SM over a contiguous range of the tiles
+        const int grid = (int)(items < sm_count() ? items : sm_count());
+        k_resp_gtc<KN><<<grid, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, items, dm.x_bf16, x,
+                                                      img, prm, cst, layout, ldg, flag);
+        return cudaGetLastError();
+    } else if constexpr (NH == 1) {
+        k_resp_gtc_wide<KC, 1><<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps,
+                                                                          dm.x_bf16, x, img, prm, cst, layout, ldg, flag);
         return cudaGetLastError();
     } else {   // the two CTAs of a tile as one cluster
         cudaLaunchConfig_t cfg = {};
@@ -866,8 +987,8 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16, x, img, prm, cst,
-                                  layout, ldg, flag);
+        return cudaLaunchKernelEx(&cfg, k_resp_gtc_wide<KC, NH>, xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16,
+                                  x, img, prm, cst, layout, ldg, flag);
     }
 }
 
