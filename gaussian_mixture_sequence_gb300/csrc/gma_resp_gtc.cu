@@ -91,26 +91,28 @@ __device__ __forceinline__ void split3(float v, unsigned short (&p)[3])
     }
 }
 
-// Grid (H, halves), KN * 4 threads: component k = KN y + tid / 4 takes feature pairs
-// 8 (tid % 4) .. + 7 from the packed parameters {s, s', -mu s, -mu' s'} and c_k that k_prep
-// wrote, into image y of head h (past 256 components a head has two images of 256).
+// Grid (H, images, KN / KB), KB * 4 threads (KB = min(KN, 64) components per block):
+// component k = KN y + KB z + tid / 4 takes feature pairs 8 (tid % 4) .. + 7 from the packed
+// parameters {s, s', -mu s, -mu' s'} and c_k that k_prep wrote, into image y of head h
+// (past 256 components a head has two images of 256).  Every block of an image also
+// takes the image's maxima A, M over all its components and writes them (the same
+// values from each block).
 template <int KN>
-__global__ void __launch_bounds__(KN * 4)
+__global__ void __launch_bounds__((KN < 64 ? KN : 64) * 4)
     k_prep_gtc(int K, const float4 *__restrict__ prm, const float *__restrict__ cst, unsigned char *__restrict__ img)
 {
-    __shared__ float red[2][KN * 4 / 32];
+    constexpr int KB = KN < 64 ? KN : 64, NT = KB * 4;
+    __shared__ float red[2][NT / 32];
     const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int kl = tid >> 2, k = KN * blockIdx.y + kl, part = tid & 3;
+    const int kl = KB * blockIdx.z + (tid >> 2), k = KN * blockIdx.y + kl, part = tid & 3;
     unsigned char *im = img + ((long long)h * gridDim.y + blockIdx.y) * GtcImg<KN>::pitch;
-    float amu2 = 0.f, amax = 0.f, mmax = 0.f;
+    float amu2 = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int dp = 8 * part + j, f = 2 * dp;
         const float4 p = k < K ? prm[((long long)h * K + k) * kQDP + dp] : make_float4(0.f, 0.f, 0.f, 0.f);
         const float wa0 = -0.5f * p.x * p.x, wa1 = -0.5f * p.y * p.y, wb0 = -p.x * p.z, wb1 = -p.y * p.w;
         amu2 = fmaf(p.z, p.z, fmaf(p.w, p.w, amu2));
-        amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
-        mmax = fmaxf(mmax, fmaxf(fabsf(wb0), fabsf(wb1)));
         unsigned short a0[3], a1[3], b0[3], b1[3];
         split3(wa0, a0);
         split3(wa1, a1);
@@ -124,15 +126,18 @@ __global__ void __launch_bounds__(KN * 4)
                 (uint32_t)b0[pl] | ((uint32_t)b1[pl] << 16);
         }
     }
-    for (int o = 1; o < 4; o <<= 1) {   // the component's four threads
-        amu2 += __shfl_xor_sync(0xffffffffu, amu2, o);
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
-    }
+    for (int o = 1; o < 4; o <<= 1) amu2 += __shfl_xor_sync(0xffffffffu, amu2, o);   // the component's four threads
     float *c = reinterpret_cast<float *>(im + GtcImg<KN>::W);
     if (part == 0) c[kl] = k < K ? cst[(long long)h * K + k] - 0.5f * amu2 : kQOff;
-    // head-wide maxima of a and |a mu|
-    for (int o = 4; o < 32; o <<= 1) {
+    // the image's maxima of a and |a mu| over all its components
+    float amax = 0.f, mmax = 0.f;
+    const int k0 = KN * blockIdx.y, kend = min(K, k0 + KN);
+    for (int e = tid; e < (kend - k0) * kQDP; e += NT) {
+        const float4 p = prm[((long long)h * K + k0) * kQDP + e];
+        amax = fmaxf(amax, fmaxf(p.x * p.x, p.y * p.y));
+        mmax = fmaxf(mmax, fmaxf(fabsf(p.x * p.z), fabsf(p.y * p.w)));
+    }
+    for (int o = 1; o < 32; o <<= 1) {
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     }
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(KN * 4)
     __syncthreads();
     if (tid == 0) {
         float a = 0.f, m = 0.f;
-        for (int w = 0; w < KN * 4 / 32; ++w) {
+        for (int w = 0; w < NT / 32; ++w) {
             a = fmaxf(a, red[0][w]);
             m = fmaxf(m, red[1][w]);
         }
@@ -152,6 +157,15 @@ __global__ void __launch_bounds__(KN * 4)
         c[KN + 2] = 0.f;
         c[KN + 3] = 0.f;
     }
+}
+
+// TMEM -> registers: 32 lanes x 32 bit, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 
 // 2^t by the SFU's base-2 exponential (relative error about 2^-22; 0 for t below -126).
@@ -367,8 +381,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     int head = slice_of(0) % H;
     bool ok = load_head(head, 0);
     int hp = 0;                        // constants' buffer of item n's head
-    uint32_t x_par = 0;                // tid 0: phase of the last routing tile fetched,
-    int m_issued = -1;                 // and the last item whose products were issued
+    uint32_t x_par = 0;                // tid 32: phase of the last routing tile fetched
+    int m_issued = -1;                 // tid 0: the last item whose products were issued
     ok = mbar_wait(BAR_X, 0u) && ok;
     convert(0);
     fence_before_sync();
@@ -377,10 +391,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (tid == 0 && ok) {
         issue(0);
         m_issued = 0;
-        if (cnt > 1) {
-            load_x(1);
-            x_par = 1u;
-        }
+    }
+    if (tid == 32 && ok && cnt > 1) {   // thread 32 moves the routing and output tiles from here on
+        load_x(1);
+        x_par = 1u;
     }
 
     float2 acc[QC / 2];                // the accumulator row of the previous item
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 if (k < K) {
                     const float4 *pk = prm + ((long long)h * K + k) * kQDP;
                     float2 a2 = make_float2(0.f, 0.f);
-#pragma unroll 8
+#pragma unroll
                     for (int dp = 0; dp < kQDP; ++dp) {
                         const float4 p = pk[dp];
                         const float2 y = __ffma2_rn(xr[dp], make_float2(p.x, p.y), make_float2(p.z, p.w));
@@ -443,7 +457,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             sq2 = __fadd2_rn(sq2, acc[p]);
         }
         ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // the output tile of item m - 2 has left shared memory
+        if (tid == 32)   // (the thread that stores the output tiles) item m - 2's has left shared memory
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncthreads();
         float2 e4[4];
 #pragma unroll
@@ -507,17 +522,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // barrier below)
         ok = mbar_wait(BAR_M, (uint32_t)(n & 1)) && ok;
         fence_after_sync();
-        {
+        {   // this thread's QC columns of the accumulator
             uint32_t r[QC];
-            if constexpr (QC == 16) {
+            if constexpr (QC == 16)
                 tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq), reinterpret_cast<uint32_t(&)[16]>(r));
-            } else {
-                uint32_t r16[16];   // columns QC cq .. + 7 of a 16-wide read (the rest belongs to
-                                    // the next quarter and is not used)
-                tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + 16 * (cq >> 1)), r16);
-#pragma unroll
-                for (int j = 0; j < QC; ++j) r[j] = r16[8 * (cq & 1) + j];
-            }
+            else
+                tmem_ld8(tmem_at(tbase, 32 * qd, D_COL + QC * cq), reinterpret_cast<uint32_t(&)[8]>(r));
             tmem_wait_ld();
 #pragma unroll
             for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
@@ -531,35 +541,33 @@ __global__ void __launch_bounds__(kQThreads, 1)
         fence_before_sync();
         ok = __syncthreads_and(ok) != 0;   // operand planes written, accumulator read, softmax done
         fence_after_sync();
-        if (tid == 0 && ok) {
-            // the routing tile was only read by threads (no proxy fence); its next contents
-            // and the previous item's output leave first, then the products start
+        if (tid == 0 && ok && n + 1 < cnt) {   // item n + 1's products
+            issue(n + 1);
+            m_issued = n + 1;
+        }
+        if (tid == 32 && ok) {
+            // the routing tile was only read by threads (no proxy fence): item n + 2's comes in,
+            // and item n - 1's output leaves
             if (n + 2 < cnt) {
                 load_x(n + 2);
                 x_par = (uint32_t)((n + 2) & 1);
             }
             if (n >= 1) finish(n - 1);
-            if (n + 1 < cnt) {
-                issue(n + 1);
-                m_issued = n + 1;
-            }
         }
         hpprev = hpn;
     }
     if (ok) {   // the last item's softmax and output
         softmax(cnt - 1, hpprev);
         ok = __syncthreads_and(ok) != 0;
-        if (tid == 0 && ok) finish(cnt - 1);
+        if (tid == 32 && ok) finish(cnt - 1);
     }
     // after a failed wait a routing tile or products may still be in flight: let them finish
     // (bounded) before TMEM and shared memory are released (a wait on a phase that has
     // completed returns at once)
     bool ok_end = ok;
-    if (tid == 0) {
-        if (!ok) {
-            ok_end = mbar_wait(BAR_X, x_par) && ok_end;
-            if (m_issued >= 0) ok_end = mbar_wait(BAR_M, (uint32_t)(m_issued & 1)) && ok_end;
-        }
+    if (tid == 0 && !ok && m_issued >= 0) ok_end = mbar_wait(BAR_M, (uint32_t)(m_issued & 1)) && ok_end;
+    if (tid == 32) {
+        if (!ok) ok_end = mbar_wait(BAR_X, x_par) && ok_end;
         bulk_wait_all();
     }
     fence_before_sync();
@@ -915,11 +923,11 @@ cudaError_t launch_prep_gtc(const Dims &dm, const float4 *prm, const float *cst,
 {
     if (!resp_gtc_applies(dm)) return cudaErrorInvalidValue;
     switch (gtc_width(dm.K)) {
-    case 32: k_prep_gtc<32><<<dm.H, 32 * 4, 0, st>>>(dm.K, prm, cst, img); break;
-    case 64: k_prep_gtc<64><<<dm.H, 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
-    case 128: k_prep_gtc<128><<<dm.H, 128 * 4, 0, st>>>(dm.K, prm, cst, img); break;
-    case 256: k_prep_gtc<256><<<dm.H, 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
-    default: k_prep_gtc<256><<<dim3(dm.H, 2), 256 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 32: k_prep_gtc<32><<<dim3(dm.H, 1, 1), 32 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 64: k_prep_gtc<64><<<dim3(dm.H, 1, 1), 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 128: k_prep_gtc<128><<<dim3(dm.H, 1, 2), 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    case 256: k_prep_gtc<256><<<dim3(dm.H, 1, 4), 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;
+    default: k_prep_gtc<256><<<dim3(dm.H, 2, 4), 64 * 4, 0, st>>>(dm.K, prm, cst, img); break;   // two images
     }
     return cudaGetLastError();
 }
