@@ -159,6 +159,32 @@ __global__ void __launch_bounds__((KN < 64 ? KN : 64) * 4)
     }
 }
 
+// One thread: the six plane products of a tile into the accumulator at d_tmem, smallest
+// first, A's planes at a_tmem + 64 j and W's planes (K_N x 256 B each, 128-byte-swizzled
+// K-major) described from bdesc; within each product the values' (odd) K steps before the
+// squares' (even) ones (in ascending order some odd steps were measured to take W from the
+// step before them).  XB16: bf16 rows, whose values' lower planes and squares' third plane
+// are zero.  Every address and flag is fixed at compile time but for the three bases.
+template <bool XB16, int KN>
+__device__ __forceinline__ void issue_products(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t id)
+{
+#pragma unroll
+    for (int q = 0; q < 6; ++q) {
+        const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                // A plane
+        const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);    // W plane
+        if (XB16 && pa == 2) continue;
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+            const int kk = s8 < 4 ? 2 * s8 + 1 : 2 * (s8 - 4);
+            if (XB16 && pa == 1 && (kk & 1)) continue;
+            const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+            const uint32_t boff = pb * (uint32_t)(KN * 256) + (kb >> 7) * (KN * 128) + (kb & 127);
+            const bool first = XB16 ? (q == 1 && s8 == 4) : (q == 0 && s8 == 0);
+            mma_ts(0u, d_tmem, a_tmem + 64u * pa + 8u * kk, bdesc + (boff >> 4), id, first ? 0u : 1u);
+        }
+    }
+}
+
 // TMEM -> registers: 32 lanes x 32 bit, 8 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
 {
@@ -336,29 +362,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
         ss_s[(n & 1) * 4 * kQRows + cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
         tmem_wait_st();
     };
-    // one thread: item n's products (operand buffer n % 2) into the accumulator, smallest
-    // first, each with its values' (odd) K steps before its squares' (even) ones; with bf16
-    // rows the values' lower planes and the squares' third plane are zero
+    // one thread: item n's products (operand buffer n % 2) into the accumulator
     const uint32_t id = idesc(128, KN, kFmtBF16);
+    const uint64_t wdesc = sdesc_sw128(smem_addr(w_s));
     auto issue = [&](int n) {
-        const uint32_t ab = 192u * (uint32_t)(n & 1);
-        bool first = true;
-#pragma unroll
-        for (int q = 0; q < 6; ++q) {
-            const uint32_t pa = q == 0 ? 2u : (q < 3 ? 1u : 0u);                // A plane
-            const uint32_t pb = (q == 1 || q == 4) ? 1u : (q == 3 ? 2u : 0u);    // W plane
-            if (x_bf16 && pa == 2) continue;
-#pragma unroll
-            for (int s8 = 0; s8 < 8; ++s8) {
-                const int kk = s8 < 4 ? 2 * s8 + 1 : 2 * (s8 - 4);
-                if (x_bf16 && pa == 1 && (kk & 1)) continue;   // odd K steps: the values
-                const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
-                const uint32_t boff = pb * (uint32_t)(KN * 256) + (kb >> 7) * (KN * 128) + (kb & 127);
-                mma_ts(0u, tbase + D_COL, tbase + ab + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w_s + boff)), id,
-                       first ? 0u : 1u);
-                first = false;
-            }
-        }
+        const uint32_t ab = tbase + 192u * (uint32_t)(n & 1);
+        if (x_bf16)
+            issue_products<true, KN>(tbase + D_COL, ab, wdesc, id);
+        else
+            issue_products<false, KN>(tbase + D_COL, ab, wdesc, id);
         mma_commit(BAR_M);
     };
 
