@@ -445,8 +445,8 @@ def traffic_record(stage, wl):
 def source_hash(stage, wl):
     d = os.path.join(ROOT, "gaussian_mixture_sequence_gb300", "csrc")
     src = KERNEL_SOURCE.get(stage)
-    if src is None:  # routing: the pruned kernel where it applies, else the generic one
-        src = "gma_resp_tc.cu" if bounded_routing(wl) else "gma_resp.cu"
+    if src is None:  # routing: the pruned kernel, the tensor-core kernels, else the generic one
+        src = "gma_resp_tc.cu" if bounded_routing(wl) else ("gma_resp_gtc.cu" if tc_routing(wl) else "gma_resp.cu")
     if stage in ("state_scan", "state_reduce") and eff_chunk(wl) == 128:   # the tensor-core path's scan
         src = "gma_causal_tc.cu"
     m = hashlib.sha256()
