@@ -592,21 +592,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
 //
 // One CTA (NH = 1) or a cluster of two (NH = 2, CTA r taking components 256 r ..) per
 // tile of 128 rows.  The accumulator holds all KN log-joints of a row (TMEM
-// columns 256 ..; the operand planes at 0 .. 191).  The three planes of W do not fit
-// in shared memory beside the output tile, so they pass through two buffers, P and Q,
-// and the products are taken in the order the planes arrive: plane 1 into P and plane 2
-// into Q, then (1,1), (0,2), (0,1); once (0,2) is done Q takes plane 0, then (2,0), (1,0),
-// (0,0).  The terms before the last are at most 2^-8 of the log-joint, so the order keeps
-// the rounding of one fp32 evaluation.  The routing tile shares the output tile's
-// space (it is consumed before the first product).  Each thread then owns KN / 4
+// columns 256 ..; the operand planes at 0 .. 191).  Plane 1 of W goes to buffer P,
+// plane 2 to buffer Q and the routing tile to the output tile's space; once the routing
+// tile is split into TMEM, plane 0 takes its place.  The products are taken in the order
+// the planes arrive: (1,1), (0,2), (0,1), then (2,0), (1,0), (0,0); the terms before the
+// last are at most 2^-8 of the log-joint, so the order keeps the rounding of one fp32
+// evaluation.  Each thread then owns KN / 4
 // components of its row; with two CTAs each row's maximum and sum pass to the other CTA
 // through distributed shared memory; the posteriors leave in halves of 128 components,
 // the second staged in buffer P.
 template <int KN>
 struct GtcWSmem {
     static constexpr uint32_t WB = KN * 256;             // one plane of W
-    static constexpr uint32_t O = kQRows * 128 * 4;      // half of the output tile (fp32 worst case),
-                                                         // first the routing tile
+    static constexpr uint32_t O = kQRows * 128 * 4;      // the routing tile, then plane 0, then half of
+                                                         // the output tile (fp32 worst case)
     static constexpr uint32_t C = GtcImg<KN>::C;         // c', A, M
     static constexpr uint32_t EX = 4 * kQRows * 8;       // per quarter and row: (max, sum)
     static constexpr uint32_t SS = 4 * kQRows * 8;       // per quarter and row: (sum x^2, sum |x|)
@@ -649,6 +648,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     using SM = GtcWSmem<KN>;
     using IM = GtcImg<KN>;
     static_assert(HALVES == 1 || SM::WB >= SM::O, "buffer P holds the second half of the output tile");
+    static_assert(SM::O >= SM::WB, "plane 0 fits in the output tile's space");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -661,9 +661,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int kbase = KN * (int)rank;   // this CTA's first component
     const unsigned char *src = img + ((long long)h * NH + rank) * IM::pitch;
 
-    unsigned char *wp = sm;              // buffer P: plane 1
-    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2, then plane 0
-    unsigned char *ob = wq + SM::WB;
+    unsigned char *wp = sm;              // buffer P: plane 1, then the second output half
+    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2
+    unsigned char *ob = wq + SM::WB;     // the routing tile, then plane 0, then the first output half
     unsigned char *xb = ob;
     float *c_s = reinterpret_cast<float *>(ob + SM::O);       // [KN + 4]
     float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);  // [4][128]
@@ -671,9 +671,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     float2 *xs_s = ss_s + 4 * kQRows;                         // [128]
     uint64_t *bar = reinterpret_cast<uint64_t *>(xs_s + kQRows);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
-    // P landed, Q landed (twice), constants landed, routing tile landed, (0,2) done, all done
+    // planes 1, 2 landed, constants landed, routing tile landed, plane 0 landed, products done
     const uint32_t BAR_P = smem_addr(bar), BAR_Q = smem_addr(bar + 1), BAR_C = smem_addr(bar + 2);
-    const uint32_t BAR_X = smem_addr(bar + 3), BAR_Q2 = smem_addr(bar + 4), BAR_D = smem_addr(bar + 5);
+    const uint32_t BAR_X = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4), BAR_D = smem_addr(bar + 5);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's half tile follows the hi plane's
@@ -741,9 +741,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
     ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, the routing tile is consumed
     fence_after_sync();
 
-    // one thread: the six products in the order the planes of W arrive
-    int stage = 0;   // (thread 0) 1: products issued; 2: plane 0 requested
+    // one thread: plane 0 into the routing tile's space (every thread has read the tile),
+    // then the six products in the order the planes of W arrive
+    int stage = 0;   // (thread 0) 1: plane 0 requested; 2: products issued
     if (tid == 0 && ok) {
+        fence_proxy_async();
+        mbar_expect_tx(BAR_O, SM::WB);
+        bulk_g2s(smem_addr(ob), src + IM::off(0, 0, 0), SM::WB, BAR_O);
+        stage = 1;
         const uint32_t id = idesc(128, KN, kFmtBF16);
         bool first = true;
         // the K steps of a product: the values' (odd) steps first, then the squares' (even)
@@ -763,29 +768,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
         };
         ok = mbar_wait(BAR_P, 0u);
         if (ok) {
-            stage = 1;
+            stage = 2;
             prods(1, wp);                          // (1,1)
             ok = mbar_wait(BAR_Q, 0u);
         }
         if (ok) {
             prods(0, wq);                          // (0,2)
-            mma_commit(BAR_Q2);
             prods(0, wp);                          // (0,1)
-            ok = mbar_wait(BAR_Q2, 0u);
-        }
-        if (ok) {   // Q is free: plane 0
-            fence_proxy_async();
-            mbar_expect_tx(BAR_Q, SM::WB);
-            bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 0), SM::WB, BAR_Q);
-            stage = 2;
-            ok = mbar_wait(BAR_Q, 1u);
+            ok = mbar_wait(BAR_O, 0u);
         }
         if (ok) {
-            if (!x_bf16) prods(2, wq);             // (2,0); zero for bf16 rows
-            prods(1, wq);                          // (1,0)
-            prods(0, wq);                          // (0,0)
+            if (!x_bf16) prods(2, ob);             // (2,0); zero for bf16 rows
+            prods(1, ob);                          // (1,0)
+            prods(0, ob);                          // (0,0)
         }
-        if (stage >= 1) mma_commit(BAR_D);         // also after a failed wait: the products issued
+        if (stage >= 2) mma_commit(BAR_D);         // also after a failed wait: the products issued
     }
     ok = __syncthreads_and(ok) != 0;
     if (ok) ok = mbar_wait(BAR_D, 0u);
@@ -908,8 +905,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             mbar_wait(BAR_X, 0u);
             mbar_wait(BAR_P, 0u);
             mbar_wait(BAR_Q, 0u);
-            if (stage >= 2) mbar_wait(BAR_Q, 1u);
-            if (stage >= 1) mbar_wait(BAR_D, 0u);
+            if (stage >= 1) mbar_wait(BAR_O, 0u);
+            if (stage >= 2) mbar_wait(BAR_D, 0u);
             report_timeout(timeout);
         }
         bulk_wait_read();   // the output tile has left shared memory
