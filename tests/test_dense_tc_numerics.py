@@ -1,4 +1,5 @@
-"""The arithmetic of the dense tensor-core routing pass (K = 128, d = 64), emulated on the CPU.
+"""The arithmetic of the tensor-core routings (d = 64), emulated on the CPU: the dense pass
+of K = 128 and the full routing of the other K up to 512.
 
 For the tiles the bounded routing leaves to the dense pass, every log-joint is
 evaluated in the expanded form
@@ -6,7 +7,10 @@ evaluated in the expanded form
 with both operands held as three bf16 planes (v = v0 + v1 + v2, each plane the
 round-to-nearest of what the previous ones leave) and the six plane products
 A2 W0, A1 W1, A1 W0, A0 W2, A0 W1, A0 W0 accumulated in fp32 in that order, one
-16-wide K step at a time (the tensor core's accumulation).  A tile whose rows
+16-wide K step at a time (the tensor core's accumulation), each product's values'
+(odd) K steps before its squares' (even) ones as the kernels issue them; the
+routing of 65 <= K <= 512 takes the products in the order its planes of W arrive,
+A1 W1, A0 W2, A0 W1, A2 W0, A1 W0, A0 W0.  A tile whose rows
 include one with S = A/2 sum x^2 + M sum |x| above 4096 (A = max a, M = max |a mu|
 over the head) is evaluated exactly instead.  This checks that on the rows the
 pass keeps the posteriors match the oracle's far inside the 1e-4 tolerance and
@@ -23,6 +27,8 @@ from gaussian_mixture_sequence_gb300 import workloads
 
 S_MAX = 4096.0
 ALL_PASSES = [(2, 0), (1, 1), (1, 0), (0, 2), (0, 1), (0, 0)]
+WIDE_PASSES = [(1, 1), (0, 2), (0, 1), (2, 0), (1, 0), (0, 0)]   # 65 <= K <= 512
+KERNEL_KSTEPS = [1, 3, 5, 7, 0, 2, 4, 6]                          # the values' steps first
 
 
 def _bf(a):
@@ -38,13 +44,13 @@ def _planes(v, n=3):
     return out
 
 
-def _head(seed=0):
-    wl = workloads.WORKLOADS["tiny"].with_(B=1, H=1, N=1024, d=64, dv=64, K=128)
+def _head(seed=0, K=128):
+    wl = workloads.WORKLOADS["tiny"].with_(B=1, H=1, N=1024, d=64, dv=64, K=K)
     mu, vr, lp = (p[0] for p in workloads.params(wl, seed=wl.seed + seed))
     return wl, mu, vr, lp
 
 
-def _emulate(mu, var_raw, logit_pi, x, passes=ALL_PASSES, nplanes=3):
+def _emulate(mu, var_raw, logit_pi, x, passes=ALL_PASSES, nplanes=3, ksteps=KERNEL_KSTEPS):
     """(estimated log-joints [n, K] as the pass forms them, S [n]) for one head."""
     v32 = np.logaddexp(np.float32(0), var_raw.astype(np.float32)).astype(np.float32)
     s = (1.0 / np.sqrt(v32)).astype(np.float32)
@@ -60,12 +66,21 @@ def _emulate(mu, var_raw, logit_pi, x, passes=ALL_PASSES, nplanes=3):
     for i, j in passes:
         if i >= nplanes or j >= nplanes:
             continue
-        for k0 in range(0, a.shape[1], 16):   # one MMA K step: exact products, one fp32 rounding
-            step = ap[i][:, k0:k0 + 16].astype(np.float64) @ wp[j][:, k0:k0 + 16].T.astype(np.float64)
+        for kk in ksteps:   # one MMA K step of 16 operand positions: exact products, one fp32 rounding
+            cols = _kstep_columns(kk)
+            step = ap[i][:, cols].astype(np.float64) @ wp[j][:, cols].T.astype(np.float64)
             acc = (acc + step).astype(np.float32)
     est = (acc + cp[None]).astype(np.float32)
     big_s = 0.5 * (s * s).max() * (x * x).sum(1) + np.abs(s * ms).max() * np.abs(x).sum(1)
     return est, big_s
+
+
+def _kstep_columns(kk):
+    """The 16 columns of [x^2 | x] in operand positions 16 kk .. 16 kk + 15: quarter q of
+    the operand holds the squares of features 16 q .. 16 q + 15 (even steps), then their
+    values (odd steps)."""
+    q, val = kk // 2, kk % 2
+    return np.arange(16 * q, 16 * q + 16) + (64 if val else 0)
 
 
 def _exact_logits(mu, var_raw, logit_pi, x):
@@ -94,8 +109,8 @@ def _softmax(l):
     return e / e.sum(1, keepdims=True)
 
 
-def _rows(case, n=512, seed=2):
-    wl, mu, vr, lp = _head()
+def _rows(case, n=512, seed=2, K=128):
+    wl, mu, vr, lp = _head(K=K)
     rng = np.random.default_rng(seed)
     if case == "peaked":
         x = workloads.full_inputs(wl.with_(dist="peaked"))[0][0, 0][:n]
@@ -153,3 +168,31 @@ def test_fewer_planes_or_products_do_not_suffice(passes, nplanes):
     est, _ = _emulate(mu, vr, lp, x, passes=passes, nplanes=nplanes)
     ref = oracle.responsibilities(mu[None], vr[None], lp[None], x[None])[0]
     assert np.abs(_softmax(est.astype(np.float64)) - ref).max() > 1e-5
+
+
+@pytest.mark.parametrize("K,passes", [(32, ALL_PASSES), (64, ALL_PASSES), (100, WIDE_PASSES),
+                                      (256, WIDE_PASSES), (512, WIDE_PASSES)])
+@pytest.mark.parametrize("case", ["normal", "wide 2.0"])
+def test_tensor_core_routing_orders_match_the_oracle(K, passes, case):
+    """The full tensor-core routing of K != 128 (every component of every row, in the
+    product order of its kernel) matches the oracle on the rows it keeps, as closely as
+    an fp32 evaluation of the direct form."""
+    mu, vr, lp, x = _rows(case, n=256, K=K)
+    est, big_s = _emulate(mu, vr, lp, x, passes=passes)
+    keep = big_s <= S_MAX
+    assert keep.any()
+    ref = oracle.responsibilities(mu[None], vr[None], lp[None], x[None])[0]
+    err = np.abs(_softmax(est.astype(np.float64)) - ref)[keep].max()
+    direct = np.abs(_softmax(_direct_fp32(mu, vr, lp, x).astype(np.float64)) - ref)[keep].max()
+    assert err <= 2e-5, err
+    assert err <= max(2 * direct, 1e-6), (err, direct)
+
+
+def test_kstep_order_changes_only_the_rounding():
+    """The odd-steps-first order of the kernels and the plain ascending order give
+    log-joints within a few fp32 units of S of each other."""
+    mu, vr, lp, x = _rows("normal")
+    a, big_s = _emulate(mu, vr, lp, x)
+    b, _ = _emulate(mu, vr, lp, x, ksteps=list(range(8)))
+    assert np.all(np.abs(a - b).max(1) <= big_s * 2.0 ** -20)
+    assert np.abs(a - b).max() > 0   # the orders do round differently
