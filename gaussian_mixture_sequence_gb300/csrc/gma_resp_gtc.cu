@@ -588,32 +588,33 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // ---- KN = 128 or 256 (65 <= K <= 256, d = 64): one product per plane pair, N = KN ----
-// ---- and K up to 512 as a cluster of two CTAs per tile, 256 components each          ----
+// ---- and K up to 512 as clusters of two CTAs, 256 components each                   ----
 //
-// One CTA (NH = 1) or a cluster of two (NH = 2, CTA r taking components 256 r ..) per
-// tile of 128 rows.  The accumulator holds all KN log-joints of a row (TMEM
-// columns 256 ..; the operand planes at 0 .. 191).  Plane 1 of W goes to buffer P,
-// plane 2 to buffer Q and the routing tile to the output tile's space; once the routing
-// tile is split into TMEM, plane 0 takes its place.  The products are taken in the order
-// the planes arrive: (1,1), (0,2), (0,1), then (2,0), (1,0), (0,0); the terms before the
-// last are at most 2^-8 of the log-joint, so the order keeps the rounding of one fp32
-// evaluation.  Each thread then owns KN / 4
-// components of its row; with two CTAs each row's maximum and sum pass to the other CTA
-// through distributed shared memory; the posteriors leave in halves of 128 components,
-// the second staged in buffer P.
+// Persistent: one CTA (NH = 1), or a cluster of two (NH = 2, CTA r taking components
+// 256 r ..), per SM pair, over a contiguous range of the (slice, tile) items.  The
+// accumulator holds all KN log-joints of a row (TMEM columns 256 ..; the operand planes at
+// 0 .. 191, the next tile's rows at 192 .. 255).  Planes 1 and 2 of the head's W stay in
+// buffers P and Q for all its tiles;
+// plane 0 comes into the output tile's space O for each tile, once the previous tile's
+// output has left it.  The products run in the order the planes are at hand: (1,1),
+// (0,2), (0,1), then (2,0), (1,0), (0,0); the terms before the last are at most 2^-8 of
+// the log-joint, so the order keeps the rounding of one fp32 evaluation.  The routing
+// rows go from global memory to registers, the next tile's while the products run, and
+// wait in TMEM until that tile starts.  Each thread owns KN / 4 components of its row; with two CTAs each row's maximum
+// and sum pass to the other CTA through distributed shared memory; the posteriors leave
+// through O in halves of 128 components.
 template <int KN>
 struct GtcWSmem {
     static constexpr uint32_t WB = KN * 256;             // one plane of W
-    static constexpr uint32_t O = kQRows * 128 * 4;      // the routing tile, then plane 0, then half of
-                                                         // the output tile (fp32 worst case)
+    static constexpr uint32_t O = kQRows * 128 * 4;      // plane 0, then half of the output tile (fp32
+                                                         // worst case)
     static constexpr uint32_t C = GtcImg<KN>::C;         // c', A, M
     static constexpr uint32_t EX = 4 * kQRows * 8;       // per quarter and row: (max, sum)
     static constexpr uint32_t SS = 4 * kQRows * 8;       // per quarter and row: (sum x^2, sum |x|)
-    static constexpr uint32_t XS = kQRows * 8;           // per row: the CTA's (max, sum), read by the other
+    static constexpr uint32_t XS = 2 * kQRows * 8;       // per tile parity and row: the CTA's (max, sum)
     static constexpr size_t bytes = 1024 + 2 * (size_t)WB + O + C + EX + SS + XS + 64;
 };
 static_assert(GtcWSmem<256>::bytes <= 232448, "wide tensor-core routing: shared memory above the per-block limit");
-static_assert(kQRows * kQD * 4 <= GtcWSmem<256>::O, "the routing tile fits in the output tile's space");
 
 // All threads of both CTAs of the cluster (release / acquire of shared memory).
 __device__ __forceinline__ void cluster_sync()
@@ -638,282 +639,326 @@ __device__ __forceinline__ float2 ld_cluster_f2(const void *p, uint32_t rank)
 
 template <int KN, int NH>
 __global__ void __launch_bounds__(kQThreads, 1)
-    k_resp_gtc_wide(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap gmap,
-                    const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int K, int tps, bool x_bf16,
-                    const void *__restrict__ xg, const unsigned char *__restrict__ img, const float4 *__restrict__ prm,
+    k_resp_gtc_wide(const __grid_constant__ CUtensorMap gmap, const __grid_constant__ CUtensorMap gmap_lo, int N,
+                    int H, int K, int tps, long long items, bool x_bf16, const void *__restrict__ xg,
+                    const unsigned char *__restrict__ img, const float4 *__restrict__ prm,
                     const float *__restrict__ cst, int layout, int ow, unsigned int *timeout)
 {
     constexpr int QC = KN / 4;
     constexpr int HALVES = KN / 128, QPH = 4 / HALVES;   // output halves; quarters of a row per half
     using SM = GtcWSmem<KN>;
     using IM = GtcImg<KN>;
-    static_assert(HALVES == 1 || SM::WB >= SM::O, "buffer P holds the second half of the output tile");
     static_assert(SM::O >= SM::WB, "plane 0 fits in the output tile's space");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, cq = warp >> 2;
     const int i = 32 * qd + lane;   // row of the tile (TMEM lane)
-    const int item = blockIdx.x / NH;
     const uint32_t rank = NH == 1 ? 0u : cluster_rank();
-    const int bh = item / tps, t = item % tps, h = bh % H;
-    const int row = t * kQRows + i;
     const int kbase = KN * (int)rank;   // this CTA's first component
-    const unsigned char *src = img + ((long long)h * NH + rank) * IM::pitch;
 
-    unsigned char *wp = sm;              // buffer P: plane 1, then the second output half
-    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2
-    unsigned char *ob = wq + SM::WB;     // the routing tile, then plane 0, then the first output half
-    unsigned char *xb = ob;
+    // the CTA (pair) takes a contiguous range of the (slice, tile) items
+    const long long groups = gridDim.x / NH, grp = blockIdx.x / NH;
+    const long long per = (items + groups - 1) / groups;
+    const long long it0 = min(items, grp * per), it1 = min(items, it0 + per);
+    if (it0 >= it1) return;   // (both CTAs of a pair alike)
+    const int cnt = (int)(it1 - it0);
+
+    unsigned char *wp = sm;              // buffer P: plane 1 of the head
+    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2 of the head
+    unsigned char *ob = wq + SM::WB;     // plane 0 while the products run, then the output tile
     float *c_s = reinterpret_cast<float *>(ob + SM::O);       // [KN + 4]
     float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);  // [4][128]
     float2 *ss_s = ex_s + 4 * kQRows;                         // [4][128]
-    float2 *xs_s = ss_s + 4 * kQRows;                         // [128]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(xs_s + kQRows);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 6);
-    // planes 1, 2 landed, constants landed, routing tile landed, plane 0 landed, products done
-    const uint32_t BAR_P = smem_addr(bar), BAR_Q = smem_addr(bar + 1), BAR_C = smem_addr(bar + 2);
-    const uint32_t BAR_X = smem_addr(bar + 3), BAR_O = smem_addr(bar + 4), BAR_D = smem_addr(bar + 5);
+    float2 *xs_s = ss_s + 4 * kQRows;                         // [2][128], by tile parity
+    uint64_t *bar = reinterpret_cast<uint64_t *>(xs_s + 2 * kQRows);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    // the head's planes 1, 2 and constants landed; plane 0 landed; products done
+    const uint32_t BAR_W = smem_addr(bar), BAR_O = smem_addr(bar + 1), BAR_D = smem_addr(bar + 2);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's half tile follows the hi plane's
-    constexpr uint32_t D_COL = 256;
+    constexpr uint32_t D_COL = 256, X_COL = 192;   // the accumulator; the next tile's rows (fp32)
 
     if (warp == 0) {
         tmem_alloc(smem_addr(tslot), 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
-        mbar_expect_tx(BAR_X, kQRows * kQD * (x_bf16 ? 2 : 4));
-        tma_load_3d(smem_addr(xb), &xmap, 0, t * kQRows, bh, BAR_X);
-        if (!x_bf16) tma_load_3d(smem_addr(xb + kQRows * 128), &xmap, 32, t * kQRows, bh, BAR_X);
-        mbar_expect_tx(BAR_C, SM::C);
-        bulk_g2s(smem_addr(c_s), src + IM::W, SM::C, BAR_C);
-        mbar_expect_tx(BAR_P, SM::WB);
-        bulk_g2s(smem_addr(wp), src + IM::off(0, 0, 1), SM::WB, BAR_P);
-        mbar_expect_tx(BAR_Q, SM::WB);
-        bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_Q);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = *tslot;
-    bool ok = mbar_wait(BAR_X, 0u);
-    {   // features 16 cq .. + 15 of row i: squares and values into the three planes, and the
-        // row's sums for S_i
-        float2 xv[8];
+
+    // features 16 cq .. + 15 of row i of an item, straight from global memory (zeros past N)
+    auto load_rows = [&](long long it, float2 (&xv)[8]) {
+        const long long bh = it / tps;
+        const int row = (int)(it % tps) * kQRows + i;
+        if (row >= N) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) xv[c] = make_float2(0.f, 0.f);
+            return;
+        }
+        const long long e = (bh * N + row) * kQD + 16 * cq;
         if (x_bf16) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(xg) + e);
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(xb + sw128_offset(i, 16 * cq + 8 * g, kQRows, 2));
+                const uint4 u = __ldg(p + g);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    xv[4 * g + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+                for (int q = 0; q < 4; ++q)
+                    xv[4 * g + q] = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
             }
         } else {
+            const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(xg) + e);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const float4 u = *reinterpret_cast<const float4 *>(xb + sw128_offset(i, 16 * cq + 4 * g, kQRows, 4));
+                const float4 u = __ldg(p + g);
                 xv[2 * g] = make_float2(u.x, u.y);
                 xv[2 * g + 1] = make_float2(u.z, u.w);
             }
         }
-        uint32_t pw[3][16];
-        float2 s2 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+    };
+    // one thread: the products of pa with the plane of W at w, the values' (odd) K steps first
+    // (issued in ascending order, some odd steps were measured to take W from the step before
+    // them); `first` clears the accumulator
+    const uint32_t id = idesc(128, KN, kFmtBF16);
+    bool first = true;
+    auto prods = [&](uint32_t pa, const unsigned char *w) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float2 q = __fmul2_rn(xv[c], xv[c]);
-            s2 = __fadd2_rn(s2, q);
-            s1 = __fadd2_rn(s1, make_float2(fabsf(xv[c].x), fabsf(xv[c].y)));
-            split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
-            split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
+        for (int s = 0; s < 8; ++s) {
+            const int kk = s < 4 ? 2 * s + 1 : 2 * (s - 4);
+            if (x_bf16 && pa == 1 && (kk & 1)) continue;   // bf16 rows: the values' plane 1 is zero
+            const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
+            const uint32_t boff = (kb >> 7) * (KN * 128) + (kb & 127);
+            mma_ts(0u, tbase + D_COL, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w + boff)), id,
+                   first ? 0u : 1u);
+            first = false;
         }
-#pragma unroll
-        for (int j = 0; j < 3; ++j) tmem_st16(tmem_at(tbase, 32 * qd, 64 * j + 16 * cq), pw[j]);
-        ss_s[cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
-        tmem_wait_st();
-    }
-    ok = mbar_wait(BAR_C, 0u) && ok;
-    fence_before_sync();
-    ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, the routing tile is consumed
-    fence_after_sync();
+    };
 
-    // one thread: plane 0 into the routing tile's space (every thread has read the tile),
-    // then the six products in the order the planes of W arrive
-    int stage = 0;   // (thread 0) 1: plane 0 requested; 2: products issued
-    if (tid == 0 && ok) {
-        fence_proxy_async();
-        mbar_expect_tx(BAR_O, SM::WB);
-        bulk_g2s(smem_addr(ob), src + IM::off(0, 0, 0), SM::WB, BAR_O);
-        stage = 1;
-        const uint32_t id = idesc(128, KN, kFmtBF16);
-        bool first = true;
-        // the K steps of a product: the values' (odd) steps first, then the squares' (even)
-        // ones.  Issued in ascending order, the odd steps of (1,0) were measured to take W
-        // from the step before them; in this order every product matched the fp64 terms.
-        auto prods = [&](uint32_t pa, const unsigned char *w) {
+    float2 xv[8];
+    load_rows(it0, xv);
+    int head = -1;
+    uint32_t nw = 0;                       // head loads so far
+    const unsigned char *src = img;        // the head's image
+    bool ok = true;
+    // (thread 0) copies or products whose wait has not completed, and their phases
+    bool w_pend = false, o_pend = false, d_pend = false;
+    uint32_t w_par = 0, o_par = 0, d_par = 0;
+    for (int j = 0; j < cnt; ++j) {
+        const long long it = it0 + j;
+        const int bh = (int)(it / tps), t = (int)(it % tps), h = bh % H;
+        const int row = t * kQRows + i;
+        if (j > 0) {   // this tile's rows, parked in TMEM while the previous tile's products ran
+            uint32_t w[16];
+            tmem_ld16(tmem_at(tbase, 32 * qd, X_COL + 16 * cq), w);
+            tmem_wait_ld();
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int kk = s < 4 ? 2 * s + 1 : 2 * (s - 4);
-                if (x_bf16 && pa == 1 && (kk & 1)) continue;   // bf16 rows: the values' plane 1 is zero
-                const uint32_t kb = kk * 32;   // byte offset of the K step in a row of W
-                const uint32_t boff = (kb >> 7) * (KN * 128) + (kb & 127);
-                mma_ts(0u, tbase + D_COL, tbase + 64u * pa + 8u * kk, sdesc_sw128(smem_addr(w + boff)), id,
-                       first ? 0u : 1u);
-                first = false;
-            }
-        };
-        ok = mbar_wait(BAR_P, 0u);
-        if (ok) {
-            stage = 2;
-            prods(1, wp);                          // (1,1)
-            ok = mbar_wait(BAR_Q, 0u);
+            for (int c = 0; c < 8; ++c) xv[c] = make_float2(__uint_as_float(w[2 * c]), __uint_as_float(w[2 * c + 1]));
         }
-        if (ok) {
+        if (h != head) {   // the previous tile's products and softmax are done (the barriers below)
+            head = h;
+            src = img + ((long long)h * NH + rank) * IM::pitch;
+            if (tid == 0 && ok) {
+                fence_proxy_async();
+                mbar_expect_tx(BAR_W, 2 * SM::WB + SM::C);
+                bulk_g2s(smem_addr(wp), src + IM::off(0, 0, 1), SM::WB, BAR_W);
+                bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_W);
+                bulk_g2s(smem_addr(c_s), src + IM::W, SM::C, BAR_W);
+                w_pend = true;
+                w_par = nw & 1;
+            }
+            if (ok) ok = mbar_wait(BAR_W, nw & 1);
+            if (tid == 0 && ok) w_pend = false;
+            ++nw;
+        }
+        {   // the rows' squares and values into the three planes of A, and their sums for S_i
+            uint32_t pw[3][16];
+            float2 s2 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float2 q = __fmul2_rn(xv[c], xv[c]);
+                s2 = __fadd2_rn(s2, q);
+                s1 = __fadd2_rn(s1, make_float2(fabsf(xv[c].x), fabsf(xv[c].y)));
+                split3_pair(q, pw[0][c], pw[1][c], pw[2][c]);
+                split3_pair(xv[c], pw[0][8 + c], pw[1][8 + c], pw[2][8 + c]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 3; ++jj) tmem_st16(tmem_at(tbase, 32 * qd, 64 * jj + 16 * cq), pw[jj]);
+            ss_s[cq * kQRows + i] = make_float2(s2.x + s2.y, s1.x + s1.y);
+            tmem_wait_st();
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, the accumulator was read
+        fence_after_sync();
+        if (tid == 0 && ok) {   // the products: planes 1 and 2 are resident, plane 0 comes into O
+            first = true;
+            d_pend = true;
+            d_par = j & 1;
+            prods(1, wp);                          // (1,1)
             prods(0, wq);                          // (0,2)
             prods(0, wp);                          // (0,1)
-            ok = mbar_wait(BAR_O, 0u);
-        }
-        if (ok) {
-            if (!x_bf16) prods(2, ob);             // (2,0); zero for bf16 rows
-            prods(1, ob);                          // (1,0)
-            prods(0, ob);                          // (0,0)
-        }
-        if (stage >= 2) mma_commit(BAR_D);         // also after a failed wait: the products issued
-    }
-    ok = __syncthreads_and(ok) != 0;
-    if (ok) ok = mbar_wait(BAR_D, 0u);
-    fence_after_sync();
-    float2 acc[QC / 2];
-#pragma unroll
-    for (int b = 0; b < QC / 16; ++b) {
-        uint32_t r[16];
-        tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq + 16 * b), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int p = 0; p < 8; ++p) acc[8 * b + p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
-    }
-    // log-joints (rows beyond the magnitude limit exactly), then the softmax over the four
-    // quarters of the row
-    const float2 am = make_float2(c_s[KN], c_s[KN + 1]);
-    const float2 *sp = ss_s + i;
-    const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
-    const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
-    const float *cb = c_s + QC * cq;
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
-    if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
-        float lex[QC];
-        const long long xo = ((long long)bh * N + row) * kQD;
-        exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
-                         : (const void *)(static_cast<const float *>(xg) + xo),
-                  x_bf16, prm, cst, h, K, kbase + QC * cq, QC, lex);
-#pragma unroll
-        for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
-    }
-    float mq = -FLT_MAX;
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
-    const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
-    float2 sq2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int p = 0; p < QC / 2; ++p) {
-        const float2 tt = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
-        acc[p] = make_float2(ex2_sfu(tt.x), ex2_sfu(tt.y));
-        sq2 = __fadd2_rn(sq2, acc[p]);
-    }
-    ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
-    ok = __syncthreads_and(ok) != 0;
-    {
-        float2 e4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
-        float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
-        float tot = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
-        if constexpr (NH == 2) {   // the row's maximum and sum over the other CTA's components too
-            if (cq == 0) xs_s[i] = make_float2(mrow, tot);
-            cluster_sync();
-            const float2 pe = ld_cluster_f2(xs_s + i, rank ^ 1u);
-            const float m2 = fmaxf(mrow, pe.x);
-            tot = tot * ex2_sfu((mrow - m2) * kQLog2e) + pe.y * ex2_sfu((pe.x - m2) * kQLog2e);
-            mrow = m2;
-        }
-        const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
-        const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-        for (int p = 0; p < QC / 2; ++p) acc[p] = __fmul2_rn(acc[p], sc2);
-    }
-    // the posteriors in halves of 128 components, quarters QPH hf .. QPH hf + QPH - 1 writing
-    // half hf: the first into the output tile, the second into buffer P, free once every
-    // product is done (ok is the same in every thread here)
-    {
-        const int hf = cq / QPH;
-        unsigned char *hb = (hf == 0 || !ok) ? ob : wp;
-        const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
-        if (g_f32) {
-#pragma unroll
-            for (int g = 0; g < QC / 4; ++g)
-                *reinterpret_cast<float4 *>(hb + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
-                    make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
-        } else {
-            const float2 m1 = make_float2(-1.f, -1.f);
-#pragma unroll
-            for (int g = 0; g < QC / 8; ++g) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 v = acc[4 * g + u];
-                    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-                    hw[u] = *reinterpret_cast<const uint32_t *>(&b);
-                    const float2 r = __ffma2_rn(
-                        make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
-                    b = __floats2bfloat162_rn(r.x, r.y);
-                    lw[u] = *reinterpret_cast<const uint32_t *>(&b);
-                }
-                const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
-                *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                if (g_split) *reinterpret_cast<uint4 *>(hb + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            bulk_wait_read();                      // the previous output tile has left O
+            mbar_expect_tx(BAR_O, SM::WB);
+            bulk_g2s(smem_addr(ob), src + IM::off(0, 0, 0), SM::WB, BAR_O);
+            o_par = j & 1;
+            if (mbar_wait(BAR_O, o_par)) {
+                if (!x_bf16) prods(2, ob);         // (2,0); zero for bf16 rows
+                prods(1, ob);                      // (1,0)
+                prods(0, ob);                      // (0,0)
+            } else {
+                o_pend = true;
+                ok = false;
             }
+            mma_commit(BAR_D);                     // also after a failed wait: the products issued
         }
-        fence_proxy_async();   // the half tiles, written by threads, are read by the TMA stores
-    }
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0 && ok) {
-        const int per = 128 / ge;   // columns of one 128-byte box
+        if (j + 1 < cnt) {   // the next tile's rows, read while the products run, parked in TMEM
+            float2 xn[8];
+            load_rows(it + 1, xn);
+            uint32_t w[16];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                w[2 * c] = __float_as_uint(xn[c].x);
+                w[2 * c + 1] = __float_as_uint(xn[c].y);
+            }
+            tmem_st16(tmem_at(tbase, 32 * qd, X_COL + 16 * cq), w);
+            tmem_wait_st();
+        }
+        if (ok) ok = mbar_wait(BAR_D, (uint32_t)(j & 1));
+        if (tid == 0 && ok) d_pend = false;
+        fence_after_sync();
+        float2 acc[QC / 2];
+#pragma unroll
+        for (int b = 0; b < QC / 16; ++b) {
+            uint32_t r[16];
+            tmem_ld16(tmem_at(tbase, 32 * qd, D_COL + QC * cq + 16 * b), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+                acc[8 * b + p] = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
+        }
+        // log-joints (rows beyond the magnitude limit exactly), then the softmax over the four
+        // quarters of the row (and the other CTA's components)
+        const float2 am = make_float2(c_s[KN], c_s[KN + 1]);
+        const float2 *sp = ss_s + i;
+        const float sx2 = (sp[0].x + sp[kQRows].x) + (sp[2 * kQRows].x + sp[3 * kQRows].x);
+        const float sx1 = (sp[0].y + sp[kQRows].y) + (sp[2 * kQRows].y + sp[3 * kQRows].y);
+        const float *cb = c_s + QC * cq;
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) acc[p] = __fadd2_rn(acc[p], make_float2(cb[2 * p], cb[2 * p + 1]));
+        if (fmaf(0.5f * am.x, sx2, am.y * sx1) > kQSMax && row < N) {
+            float lex[QC];
+            const long long xo = ((long long)bh * N + row) * kQD;
+            exact_row(x_bf16 ? (const void *)(static_cast<const uint16_t *>(xg) + xo)
+                             : (const void *)(static_cast<const float *>(xg) + xo),
+                      x_bf16, prm, cst, h, K, kbase + QC * cq, QC, lex);
+#pragma unroll
+            for (int p = 0; p < QC / 2; ++p) acc[p] = make_float2(lex[2 * p], lex[2 * p + 1]);
+        }
+        float mq = -FLT_MAX;
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) mq = fmaxf(mq, fmaxf(acc[p].x, acc[p].y));
+        const float2 mneg = make_float2(-mq, -mq), l2e = make_float2(kQLog2e, kQLog2e);
+        float2 sq2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < QC / 2; ++p) {
+            const float2 tt = __fmul2_rn(__fadd2_rn(acc[p], mneg), l2e);
+            acc[p] = make_float2(ex2_sfu(tt.x), ex2_sfu(tt.y));
+            sq2 = __fadd2_rn(sq2, acc[p]);
+        }
+        ex_s[cq * kQRows + i] = make_float2(mq, sq2.x + sq2.y);
+        ok = __syncthreads_and(ok) != 0;
+        {
+            float2 e4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e4[q] = ex_s[q * kQRows + i];
+            float mrow = fmaxf(fmaxf(e4[0].x, e4[1].x), fmaxf(e4[2].x, e4[3].x));
+            float tot = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tot = fmaf(e4[q].y, ex2_sfu((e4[q].x - mrow) * kQLog2e), tot);
+            if constexpr (NH == 2) {   // the row's maximum and sum over the other CTA's components too
+                float2 *xs = xs_s + (j & 1) * kQRows;   // by tile parity: the other CTA reads it before
+                if (cq == 0) xs[i] = make_float2(mrow, tot);   // this CTA writes the slot again
+                cluster_sync();
+                const float2 pe = ld_cluster_f2(xs + i, rank ^ 1u);
+                const float m2 = fmaxf(mrow, pe.x);
+                tot = tot * ex2_sfu((mrow - m2) * kQLog2e) + pe.y * ex2_sfu((pe.x - m2) * kQLog2e);
+                mrow = m2;
+            }
+            const float sc = ex2_sfu((mq - mrow) * kQLog2e) / tot;
+            const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+            for (int p = 0; p < QC / 2; ++p) acc[p] = __fmul2_rn(acc[p], sc2);
+        }
+        // the posteriors in halves of 128 components through O (free: the products are done):
+        // quarters QPH hf .. QPH hf + QPH - 1 write half hf once the previous half has left O
+#pragma unroll 1
         for (int hf = 0; hf < HALVES; ++hf) {
-            const unsigned char *hb = hf == 0 ? ob : wp;
-            for (int a = 0; a < 128 / per; ++a) {
-                const int x0 = kbase + 128 * hf + a * per;
-                if (x0 >= ow) break;
-                tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(hb + a * (kQRows * 128)));
-                if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(hb + LO + a * (kQRows * 128)));
+            if (hf > 0) {
+                if (tid == 0) bulk_wait_read();
+                __syncthreads();
+            }
+            if (cq / QPH == hf && ok) {
+                const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
+                if (g_f32) {
+#pragma unroll
+                    for (int g = 0; g < QC / 4; ++g)
+                        *reinterpret_cast<float4 *>(ob + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
+                            make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
+                } else {
+                    const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+                    for (int g = 0; g < QC / 8; ++g) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 v = acc[4 * g + u];
+                            __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                            hw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                            const float2 r = __ffma2_rn(
+                                make_float2(__uint_as_float(hw[u] << 16), __uint_as_float(hw[u] & 0xffff0000u)), m1, v);
+                            b = __floats2bfloat162_rn(r.x, r.y);
+                            lw[u] = *reinterpret_cast<const uint32_t *>(&b);
+                        }
+                        const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
+                        *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+                fence_proxy_async();   // the half tile, written by threads, is read by the TMA store
+            }
+            fence_before_sync();
+            __syncthreads();
+            if (tid == 0 && ok) {
+                const int pb = 128 / ge;   // columns of one 128-byte box
+                for (int a = 0; a < 128 / pb; ++a) {
+                    const int x0 = kbase + 128 * hf + a * pb;
+                    if (x0 >= ow) break;
+                    tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
+                    if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
+                }
+                bulk_commit();
             }
         }
-        bulk_commit();
     }
     if (tid == 0) {
         if (!ok) {
-            // after a failed wait a copy or products may still be in flight: let them end
-            // (bounded; a wait on a phase that has completed returns at once)
-            mbar_wait(BAR_C, 0u);
-            mbar_wait(BAR_X, 0u);
-            mbar_wait(BAR_P, 0u);
-            mbar_wait(BAR_Q, 0u);
-            if (stage >= 1) mbar_wait(BAR_O, 0u);
-            if (stage >= 2) mbar_wait(BAR_D, 0u);
+            // after a failed wait a copy or products may still be in flight: let them end (bounded)
+            if (w_pend) mbar_wait(BAR_W, w_par);
+            if (o_pend) mbar_wait(BAR_O, o_par);
+            if (d_pend) mbar_wait(BAR_D, d_par);
             report_timeout(timeout);
         }
         bulk_wait_read();   // the output tile has left shared memory
     }
     fence_before_sync();
     __syncthreads();
-    if constexpr (NH == 2) cluster_sync();   // the other CTA has read this one's (max, sum)
+    if constexpr (NH == 2) cluster_sync();   // the other CTA has read this one's last (max, sum)
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -987,13 +1032,15 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
         k_resp_gtc<KN><<<grid, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, items, dm.x_bf16, x,
                                                       img, prm, cst, layout, ldg, flag);
         return cudaGetLastError();
-    } else if constexpr (NH == 1) {
-        k_resp_gtc_wide<KC, 1><<<(unsigned)items, kQThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps,
-                                                                          dm.x_bf16, x, img, prm, cst, layout, ldg, flag);
+    } else if constexpr (NH == 1) {   // persistent too
+        const int grid = (int)(items < sm_count() ? items : sm_count());
+        k_resp_gtc_wide<KC, 1><<<grid, kQThreads, smem, st>>>(gmap, gmap_lo, dm.N, dm.H, dm.K, tps, items, dm.x_bf16,
+                                                               x, img, prm, cst, layout, ldg, flag);
         return cudaGetLastError();
-    } else {   // the two CTAs of a tile as one cluster
+    } else {   // clusters of two CTAs, each pair over a range of the tiles
+        const long long pairs = items < sm_count() / 2 ? items : sm_count() / 2;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(items * NH));
+        cfg.gridDim = dim3((unsigned)(pairs * NH));
         cfg.blockDim = dim3(kQThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
@@ -1004,8 +1051,8 @@ cudaError_t launch_gtc(const Dims &dm, const unsigned char *img, const float4 *p
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_resp_gtc_wide<KC, NH>, xmap, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, dm.x_bf16,
-                                  x, img, prm, cst, layout, ldg, flag);
+        return cudaLaunchKernelEx(&cfg, k_resp_gtc_wide<KC, NH>, gmap, gmap_lo, dm.N, dm.H, dm.K, tps, items,
+                                  dm.x_bf16, x, img, prm, cst, layout, ldg, flag);
     }
 }
 
