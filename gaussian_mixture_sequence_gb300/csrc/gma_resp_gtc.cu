@@ -29,8 +29,9 @@
 // is read out before the next products are issued, so the products of item n + 1
 // run while the warps take the softmax of item n and split the routing tile of
 // item n + 2; the output tiles are double-buffered too, so a tile's TMA store
-// drains while the next one is written.  Past 64 components one CTA (or a cluster
-// of two) takes one tile (k_resp_gtc_wide below).
+// drains while the next one is written.  Past 64 components the accumulator and a
+// single operand buffer fill TMEM (k_resp_gtc_wide below, persistent too; past 256
+// components a cluster of two CTAs per tile).
 //
 // Within each product the K steps of the values (odd) are issued before those of
 // the squares (even): in ascending order some odd steps were measured to take W
