@@ -14,6 +14,7 @@ using namespace gma;
 namespace {
 
 struct WsPlan {
+    size_t zq = 0;        // the routing of Q's zero-lo-plane flags (bounded routing, split layout)
     size_t prm = 0, cst = 0, gq = 0, gk = 0, partial = 0, total = 0, mem = 0, wimg = 0, wimg3 = 0, pimg = 0,
            cimg = 0, pimg2 = 0, dctl = 0, dlist = 0, dlist2 = 0, bytes = 0;
     long long dcap = 0;   // dense-list entries per head
@@ -83,11 +84,13 @@ gma_status make_dims_raw(const gma_shape *s, Dims *dm)
     return GMA_OK;
 }
 
-// The bounded routing's per-head images and its two tile lists (dcap entries per head each).
+// The bounded routing's per-head images and its two tile lists (dcap entries per head each), and
+// (zq_words > 0) the routing of Q's flags of tiles whose lo plane it leaves unwritten.
 template <class Take>
-void plan_pruned(WsPlan &p, int H, long long dcap, Take &&take)
+void plan_pruned(WsPlan &p, int H, long long dcap, Take &&take, long long zq_words = 0)
 {
     p.pruned = true;
+    if (zq_words > 0) p.zq = take((size_t)zq_words * 4);
     p.wimg = take((size_t)H * kPrunedWBytes);
     p.wimg3 = take((size_t)H * kPrunedW3Bytes);
     p.pimg = take((size_t)H * kPrunedPBytes);
@@ -98,6 +101,8 @@ void plan_pruned(WsPlan &p, int H, long long dcap, Take &&take)
     p.dlist = take((size_t)H * dcap * 8);
     p.dlist2 = take((size_t)H * dcap * 8);
 }
+
+int gamma_layout(const Dims &dm);
 
 WsPlan plan(const Dims &dm, gma_op op)
 {
@@ -110,8 +115,10 @@ WsPlan plan(const Dims &dm, gma_op op)
     };
     p.prm = take((size_t)dm.H * dm.K * (dm.D / 2) * 16);
     p.cst = take((size_t)dm.H * dm.K * 4);
-    if (op != GMA_OP_DECODE && resp_pruned_applies(dm))
-        plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take);   // both routings of a head
+    if (op != GMA_OP_DECODE && resp_pruned_applies(dm))   // both routings of a head; the flags where
+        plan_pruned(p, dm.H, 2 * routing_tiles(dm.B, dm.N), take,   // the chunk kernels read split planes
+                    (op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL) && gamma_layout(dm) == GL_SPLIT
+                        ? dm.BH() * ((dm.N + 127) / 128) : 0);
     if (op != GMA_OP_DECODE && resp_gtc_applies(dm)) {
         p.gtc = true;
         p.wimg3 = take(gtc_image_bytes(dm));
@@ -258,7 +265,8 @@ PrunedImages images(void *ws, const WsPlan &wp)
 {
     return PrunedImages{at<unsigned char>(ws, wp.wimg), at<unsigned char>(ws, wp.wimg3), at<float4>(ws, wp.pimg),
                         at<float>(ws, wp.cimg), at<float4>(ws, wp.pimg2), at<unsigned int>(ws, wp.dctl),
-                        at<int2>(ws, wp.dlist), at<int2>(ws, wp.dlist2), wp.dcap};
+                        at<int2>(ws, wp.dlist), at<int2>(ws, wp.dlist2), wp.dcap,
+                        wp.zq ? at<unsigned int>(ws, wp.zq) : nullptr};
 }
 
 // The routing images a call passes to launch_resp (null for the generic CUDA-core routing).
@@ -437,7 +445,7 @@ gma_status run_bidir(const gma_shape *shape, gma_params params, const void *qx, 
         unsigned char *tot = at<unsigned char>(ws, wp.total);
         GMA_CUDA(launch_scan_split(dm, partial, nullptr, nullptr, tot, nullptr, st));
         GMA_CUDA(mk.mark("bidir_read_tc"));
-        GMA_CUDA(launch_chunk_out_tc(dm, false, gq, gk, v, tot, out, st));
+        GMA_CUDA(launch_chunk_out_tc(dm, false, gq, gk, v, tot, out, st, img.zq));
     } else {
         GMA_CUDA(mk.mark("block_state"));
         GMA_CUDA(launch_block_state(dm, gk, v, partial, st));
@@ -462,7 +470,9 @@ WsPlan plan_cross(const Dims &dq, const Dims &dk)
     };
     p.prm = take((size_t)dq.H * dq.K * (dq.D / 2) * 16);
     p.cst = take((size_t)dq.H * dq.K * 4);
-    if (resp_pruned_applies(dq)) plan_pruned(p, dq.H, routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N), take);
+    if (resp_pruned_applies(dq))
+        plan_pruned(p, dq.H, routing_tiles(dq.B, dq.N) + routing_tiles(dk.B, dk.N), take,
+                    gamma_layout(dq) == GL_SPLIT ? dq.BH() * ((dq.N + 127) / 128) : 0);
     if (resp_gtc_applies(dq)) {
         p.gtc = true;
         p.wimg3 = take(gtc_image_bytes(dq));
@@ -526,7 +536,8 @@ gma_status run_cross(const gma_shape *shape, int n_kv, gma_params params, const 
         }
     }
     if (tc)
-        GMA_CUDA(launch_chunk_out_tc(dq, false, gq, gq, nullptr, reinterpret_cast<unsigned char *>(total), out, st));
+        GMA_CUDA(launch_chunk_out_tc(dq, false, gq, gq, nullptr, reinterpret_cast<unsigned char *>(total), out, st,
+                                     img.zq));
     else
         GMA_CUDA(launch_chunk_out(dq, false, gq, gq, nullptr, total, out, st));
     return GMA_OK;
@@ -611,7 +622,7 @@ gma_status run_causal(const gma_shape *shape, gma_params params, const void *qx,
         unsigned char *mem = at<unsigned char>(ws, wp.mem);
         GMA_CUDA(launch_scan_split(dm, partial, state_in, mem, nullptr, state_out, st));
         GMA_CUDA(mk.mark("chunk_out_tc"));
-        GMA_CUDA(launch_chunk_out_tc(dm, true, gq, gk, v, mem, out, st));
+        GMA_CUDA(launch_chunk_out_tc(dm, true, gq, gk, v, mem, out, st, img.zq));
     } else {
         GMA_CUDA(mk.mark("block_state"));
         GMA_CUDA(launch_block_state(dm, gk, v, partial, st));

@@ -471,7 +471,8 @@ struct OutMaps {
 template <bool SPLIT, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(kOutThreads, 1)
     k_chunk_out_tc(const __grid_constant__ OutMaps maps, int N, int nblk, long long items, int KH, float eps,
-                   const void *__restrict__ v, bool v_bf16, float *__restrict__ out, unsigned int *timeout)
+                   const void *__restrict__ v, bool v_bf16, float *__restrict__ out, unsigned int *timeout,
+                   const unsigned int *__restrict__ zq)
 {
     using Sm = OutSmem<SPLIT, DV>;
     constexpr int NP = Sm::NP;
@@ -511,15 +512,19 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 
     // block of the carried memory read by item it
     auto mem_block = [&](long long it) -> long long { return CAUSAL ? it : it / nblk; };
-    // one thread: component group g (components 128 g .. + 127) of item it
+    // one thread: component group g (components 128 g .. + 127) of item it.  Returns whether the
+    // lo plane of Gamma_Q is zero on this chunk (the routing of Q recorded it and did not write
+    // it): then it is not loaded, and the product it takes is not issued (it would add zeros)
     auto load_gamma = [&](long long it, int g) {
         const int row0 = (int)((it / nblk) * N + (it % nblk) * kC), x0 = kK * g;
-        mbar_expect_tx(BAR_G, (uint32_t)((CAUSAL ? 2 : 1) * NP * kC * kRowB));
+        const bool zl = SPLIT && zq != nullptr && zq[it] != 0u;   // (items are (slice, chunk), chunk = tile)
+        mbar_expect_tx(BAR_G, (uint32_t)(((CAUSAL ? 2 : 1) * NP - (zl ? 1 : 0)) * kC * kRowB));
         for (int pl = 0; pl < NP; ++pl)
             for (int a = 0; a < 2; ++a) {
                 if (CAUSAL) tma_load_2d(smem_addr((pl ? tb1 : tb0) + a * AS), &maps.gk[pl], x0 + a * 64, row0, BAR_G);
-                tma_load_2d(smem_addr((pl ? ta1 : ta0) + a * kAtom), &maps.gq[pl], x0 + a * 64, row0, BAR_G);
+                if (!(pl && zl)) tma_load_2d(smem_addr((pl ? ta1 : ta0) + a * kAtom), &maps.gq[pl], x0 + a * 64, row0, BAR_G);
             }
+        return zl;
     };
     auto load_memory = [&](long long it, int g) {
         const int srow = (int)(mem_block(it) * SROWS), x0 = kK * g;
@@ -539,11 +544,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // loads in flight that the loop has not waited for (thread 0's record)
     bool pend_g = false, pend_s = false;
     uint32_t ph_g = 0, ph_s = 0;
+    bool zq_l = false;   // (thread 0) the last loaded group's Gamma_Q lo plane is zero
     if (tid == 0) {
         for (int b = 0; b < 6; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
         if (it0 < it1) {
-            load_gamma(it0, 0);
+            zq_l = load_gamma(it0, 0);
             load_memory(it0, 0);
             pend_g = pend_s = true;
         }
@@ -614,7 +620,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 mma_pass_ss(tbase + d0, ta0, kAtom, tb0 + b0, nb, AS, gr > 0);
                 if constexpr (SPLIT) {
                     mma_pass_ss(tbase + d0, ta0, kAtom, tb1 + b0, nb, AS, true);
-                    mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
+                    if (!zq_l) mma_pass_ss(tbase + d0, ta1, kAtom, tb0 + b0, nb, AS, true);
                 }
                 if constexpr (!ZF)   // Gq [Z_hi | Z_lo] on its own
                     mma_pass_ss(tbase + D_Z, ta0, kAtom, bz, 16, Sm::ZATOM, gr > 0);
@@ -638,7 +644,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 // group's (or the next item's first group's) tiles and memory may land in them
                 const long long in = gr + 1 < KH ? it : it + 1;
                 const int gn = gr + 1 < KH ? gr + 1 : 0;
-                load_gamma(in, gn);
+                zq_l = load_gamma(in, gn);
                 load_memory(in, gn);
                 pend_g = pend_s = true;
                 ph_g = ph_s = pu ^ 1u;
@@ -839,7 +845,7 @@ cudaError_t state_tc(const Dims &dm, const void *gk, const void *v, float *parti
 
 template <bool SPLIT, int DV, bool CAUSAL>
 cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v, const unsigned char *mem,
-                   float *out, cudaStream_t st)
+                   float *out, cudaStream_t st, const unsigned int *zq)
 {
     constexpr size_t smem = OutSmem<SPLIT, DV>::bytes;
     static std::atomic<unsigned long long> smem_set{0};
@@ -869,7 +875,7 @@ cudaError_t out_tc(const Dims &dm, const void *gq, const void *gk, const void *v
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     k_chunk_out_tc<SPLIT, DV, CAUSAL><<<grid, kOutThreads, smem, st>>>(
-        maps, dm.N, dm.nblk(), items, KH, dm.eps, v, dm.v_bf16, out, flag);
+        maps, dm.N, dm.nblk(), items, KH, dm.eps, v, dm.v_bf16, out, flag, KH == 1 ? zq : nullptr);
     return cudaGetLastError();
 }
 
@@ -895,18 +901,18 @@ cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float 
 }
 
 cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
-                                const unsigned char *mem, float *out, cudaStream_t st)
+                                const unsigned char *mem, float *out, cudaStream_t st, const unsigned int *zq)
 {
     if (dm.g_bf16) {
         if (dm.DV == 64)
-            return causal ? out_tc<false, 64, true>(dm, gq, gk, v, mem, out, st)
-                          : out_tc<false, 64, false>(dm, gq, gk, v, mem, out, st);
+            return causal ? out_tc<false, 64, true>(dm, gq, gk, v, mem, out, st, zq)
+                          : out_tc<false, 64, false>(dm, gq, gk, v, mem, out, st, zq);
         if (dm.DV == 128)
-            return causal ? out_tc<false, 128, true>(dm, gq, gk, v, mem, out, st)
-                          : out_tc<false, 128, false>(dm, gq, gk, v, mem, out, st);
+            return causal ? out_tc<false, 128, true>(dm, gq, gk, v, mem, out, st, zq)
+                          : out_tc<false, 128, false>(dm, gq, gk, v, mem, out, st, zq);
     } else if (dm.DV == 64) {
-        return causal ? out_tc<true, 64, true>(dm, gq, gk, v, mem, out, st)
-                      : out_tc<true, 64, false>(dm, gq, gk, v, mem, out, st);
+        return causal ? out_tc<true, 64, true>(dm, gq, gk, v, mem, out, st, zq)
+                      : out_tc<true, 64, false>(dm, gq, gk, v, mem, out, st, zq);
     }
     return cudaErrorInvalidValue;
 }

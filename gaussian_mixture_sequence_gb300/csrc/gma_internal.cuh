@@ -146,6 +146,9 @@ struct PrunedImages {
     int2 *list;         // [H][cap]: (slice | source tag << 30, tile) of the tiles the routing left
     int2 *list2;        // [H][cap]: the same for the tiles the tensor-core pass leaves
     long long cap;      // list entries per head (the tiles of both routings of a head)
+    unsigned int *zq;   // [BH][tiles] or null: 1 where the routing of Q (split layout) left the lo
+                        // plane of a tile of 128 rows unwritten because every row kept its argmax
+                        // alone (posterior 1: the plane is zero), else 0
 };
 constexpr size_t kPrunedWBytes = 32768, kPrunedW3Bytes = 3 * kPrunedWBytes, kPrunedPBytes = 128 * 33 * 16,
                  kPrunedCBytes = 4 * 128 * 4, kPrunedP2Bytes = 128 * 32 * 16;
@@ -195,8 +198,10 @@ inline long long tc_mem_words(const Dims &dm) { return (long long)(dm.DV + 1) * 
 cudaError_t launch_chunk_state_tc(const Dims &dm, const void *gk, const void *v, float *partial, cudaStream_t st);
 cudaError_t launch_scan_split(const Dims &dm, const float *partial, const float *state_in, unsigned char *mem,
                               unsigned char *total, float *state_out, cudaStream_t st);
+// zq: the routing of Q's zero-lo-plane flags per (slice, chunk) (PrunedImages::zq), or null.
 cudaError_t launch_chunk_out_tc(const Dims &dm, bool causal, const void *gq, const void *gk, const void *v,
-                                const unsigned char *mem, float *out, cudaStream_t st);
+                                const unsigned char *mem, float *out, cudaStream_t st,
+                                const unsigned int *zq = nullptr);
 // Responsibility diagnostics (gma_stats.cu): blocks of rows per slice of the partial
 // pass, and the two launches (partial sums per block, then per head in fixed order).
 int usage_blocks(const Dims &dm);

@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                   const __grid_constant__ CUtensorMap gmap_lo, int N, int H, int BH, bool x_bf16,
                   const unsigned char *__restrict__ wimg, const float4 *__restrict__ pimg,
                   const float *__restrict__ cimg, int layout, int pstride, unsigned int *timeout,
-                  int2 *__restrict__ dlist, unsigned int *__restrict__ dctl, long long dcap, int src)
+                  int2 *__restrict__ dlist, unsigned int *__restrict__ dctl, long long dcap, int src,
+                  unsigned int *__restrict__ zq)
 {
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -291,6 +292,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kPRows * kPK * 2;   // split: the lo plane's tile follows the hi plane's
+    // the routing of Q in the split layout records the tiles whose lo plane it leaves unwritten
+    const bool zflag = g_split && zq != nullptr && src == 0;
 
     // one thread: TMA of slot it's rows, counted on the barrier of the group that takes it
     // (group 0 takes a run's first slot in the range, then the groups alternate)
@@ -502,6 +505,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // time would be bound by shared-memory reads
             if (group_popc(grp, __popc(xm0) + __popc(xm1) >= kDenseKept) >= kDenseRows) {
                 if (gt == 0) dlist[(long long)head * dcap + atomicAdd(dctl + head, 1u)] = make_int2(bh | (src << 30), t);
+                if (gt == 0 && zflag) zq[(long long)bh * tps + t] = 0u;   // the dense pass writes both planes
                 continue;   // no exact pass and no output tile here
             }
             // per 32-component word: the union of the warp's kept sets, whether its lanes walk
@@ -519,7 +523,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (!lanes[wd]) wpre[wd] = __ldg(ph + lane + (64 * hf + 32 * wd + __ffs(uni[wd]) - 1) * kPStride);
                 }
             }
-            if (group_or(grp, (xm0 | xm1) != 0u)) {
+            // a tile whose rows all keep their argmax alone has a zero lo plane (posteriors 0 and 1)
+            const bool any_exact = group_or(grp, (xm0 | xm1) != 0u);
+            const bool zlo = zflag && !any_exact;
+            if (any_exact) {
                 // exact log-joint of a component for this lane's row (parameters from global
                 // memory, L2-resident)
                 auto exact = [&](int k) {
@@ -638,10 +645,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (gt == 0) {
                 for (int a = 0; a < kPK * ge / 128; ++a) {
                     tma_store_3d(&gmap, a * (128 / ge), t * kPRows, bh, smem_addr(ob + a * (kPRows * 128)));
-                    if (g_split)
+                    if (g_split && !zlo)
                         tma_store_3d(&gmap_lo, a * (128 / ge), t * kPRows, bh, smem_addr(ob + LO + a * (kPRows * 128)));
                 }
                 bulk_commit();
+                if (zflag) zq[(long long)bh * tps + t] = zlo ? 1u : 0u;
             }
         }
         s0 = next_filled(s1);
@@ -1341,7 +1349,7 @@ cudaError_t launch_resp_pruned(const Dims &dm, const PrunedImages &img, const vo
     unsigned int *flag = timeout_flag_dev();
     if (!flag) return cudaErrorMemoryAllocation;
     k_resp_pruned<<<grid, kPThreads, smem, st>>>(xmap, gmap, gmap_lo, dm.N, dm.H, nsl, dm.x_bf16, img.w, img.p,
-                                                 img.c, layout, pstride, flag, img.list, img.ctl, img.cap, src);
+                                                 img.c, layout, pstride, flag, img.list, img.ctl, img.cap, src, img.zq);
     return cudaGetLastError();
 }
 
