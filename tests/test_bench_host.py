@@ -129,12 +129,17 @@ def test_decode_bytes_per_launch():
 
 def test_measured_traffic_matches_algorithmic_bytes():
     """The committed ncu counters of the chunk-output kernel (the headline's dominant
-    kernel) are within 5 % of its algorithmic bytes: no tile is read twice."""
+    kernel) stay within its kernel-byte model (no tile is read twice) and above the model
+    less the lo plane of Gamma_Q (256 B per head-token), which the kernel skips on
+    the chunks whose rows all keep their argmax alone (most of the headline's)."""
     wl = W["causal_16k_peaked"]
     t = bench.traffic_record("chunk_out_tc", wl)
     if t is None:
         pytest.skip("profiles/dram_traffic.txt holds no counters for the current chunk-output source")
-    assert t == pytest.approx(bench.stage_work("chunk_out_tc", wl)[2], rel=0.05)
+    model = bench.stage_work("chunk_out_tc", wl)[2]
+    lo_q = wl.K * 2 * wl.B * wl.H * wl.N            # Gamma_Q's lo plane (bf16)
+    # (ncu does not count dirty lines left in L2 at the end of a launch: 2 % below is allowed)
+    assert 0.98 * (model - lo_q) <= t <= 1.05 * model, (t, model)
     assert bench.traffic_record("decode", wl) is None                           # no counters recorded
 
 

@@ -289,6 +289,34 @@ def test_repeatable_bitwise():
     assert torch.equal(x, y)
 
 
+def test_unwritten_lo_planes_are_never_read():
+    """On peaked inputs the routing of Q leaves the lo plane of a tile unwritten when every row
+    keeps its argmax alone (the plane is zero) and the chunk output skips it.  A workspace that
+    an N(0, 1) call filled with non-zero lo planes must give, on the peaked call after it,
+    bitwise the output of a fresh workspace filled with NaN bytes, and match the oracle."""
+    from gaussian_mixture_sequence_gb300 import gma
+    from gpu_cases import shape_of
+    wl_p = W["causal_16k_peaked"].with_(B=1, H=2, N=2048 + 77)
+    wl_n = wl_p.with_(dist="normal")
+    cp, cn = Case(wl_p), Case(wl_n)
+    dev = "cuda:0"
+    for mode, op, fn in (("causal", gma.OP_CAUSAL, gma.gma_forward_causal),
+                         ("bidir", gma.OP_BIDIR, gma.gma_forward_bidir)):
+        size = gma.gma_workspace_size(shape_of(wl_p), op)
+        ws = torch.empty(size, dtype=torch.uint8, device=dev)
+        out_n = torch.empty(wl_p.B, wl_p.H, wl_p.N, wl_p.dv, device=dev)
+        fn(shape_of(wl_n), *cn.prm, *cn.dev["seq"], out_n, ws=ws)   # non-zero lo planes everywhere
+        out_a = torch.empty_like(out_n)
+        fn(shape_of(wl_p), *cp.prm, *cp.dev["seq"], out_a, ws=ws)
+        fresh = torch.full((size,), 0xFF, dtype=torch.uint8, device=dev)   # NaN in every plane
+        out_b = torch.empty_like(out_n)
+        fn(shape_of(wl_p), *cp.prm, *cp.dev["seq"], out_b, ws=fresh)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b), mode
+        ref = cp.ref_causal() if mode == "causal" else cp.ref_bidir()
+        _report(f"{mode} after a reused workspace", normwise(cp.pick(out_a), ref), TOL["f32"])
+
+
 # ------------------------------------------------------------ S5 --------------
 
 def _decode_run(c, prefill_state):
