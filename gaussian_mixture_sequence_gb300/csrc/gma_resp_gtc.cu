@@ -594,16 +594,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // Persistent: one CTA (NH = 1), or a cluster of two (NH = 2, CTA r taking components
 // 256 r ..), per SM pair, over a contiguous range of the (slice, tile) items.  The
 // accumulator holds all KN log-joints of a row (TMEM columns 256 ..; the operand planes at
-// 0 .. 191, the next tile's rows at 192 .. 255).  Planes 1 and 2 of the head's W stay in
-// buffers P and Q for all its tiles;
-// plane 0 comes into the output tile's space O for each tile, once the previous tile's
-// output has left it.  The products run in the order the planes are at hand: (1,1),
-// (0,2), (0,1), then (2,0), (1,0), (0,0); the terms before the last are at most 2^-8 of
-// the log-joint, so the order keeps the rounding of one fp32 evaluation.  The routing
-// rows go from global memory to registers, the next tile's while the products run, and
-// wait in TMEM until that tile starts.  Each thread owns KN / 4 components of its row; with two CTAs each row's maximum
-// and sum pass to the other CTA through distributed shared memory; the posteriors leave
-// through O in halves of 128 components.
+// 0 .. 191, the next tile's rows at 192 .. 255).  Plane 1 of the head's W stays in buffer
+// P for all its tiles; for each tile plane 0 comes into O and plane 2 into Q (with one
+// output half, Q keeps plane 2 for the head) as soon as the previous tile's output halves
+// have left them.  The products run in the order the planes are at hand: (1,1), (0,1),
+// then (2,0), (1,0), then (0,2) and last (0,0); every term before the last is at most
+// 2^-8 of the log-joint, so the order keeps the rounding of one fp32 evaluation.  The routing rows go
+// from global memory to registers, the next tile's while the products run, and wait in
+// TMEM until that tile starts.  Each thread owns KN / 4 components of its row; with two
+// CTAs each row's maximum and sum pass to the other CTA through distributed shared memory;
+// the posteriors leave in halves of 128 components, the first from O, the second from Q,
+// stored by thread 32 while thread 0 issues the next tile's products.
 template <int KN>
 struct GtcWSmem {
     static constexpr uint32_t WB = KN * 256;             // one plane of W
@@ -647,9 +648,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
 {
     constexpr int QC = KN / 4;
     constexpr int HALVES = KN / 128, QPH = 4 / HALVES;   // output halves; quarters of a row per half
+    constexpr bool QOUT = HALVES == 2;                   // the second half leaves through buffer Q
     using SM = GtcWSmem<KN>;
     using IM = GtcImg<KN>;
     static_assert(SM::O >= SM::WB, "plane 0 fits in the output tile's space");
+    static_assert(!QOUT || SM::WB >= SM::O, "buffer Q holds the second half of the output tile");
     extern __shared__ unsigned char sm_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -666,16 +669,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int cnt = (int)(it1 - it0);
 
     unsigned char *wp = sm;              // buffer P: plane 1 of the head
-    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2 of the head
-    unsigned char *ob = wq + SM::WB;     // plane 0 while the products run, then the output tile
+    unsigned char *wq = sm + SM::WB;     // buffer Q: plane 2 while the products run, then (two
+                                         // halves) the second output half
+    unsigned char *ob = wq + SM::WB;     // plane 0 while the products run, then the (first) output half
     float *c_s = reinterpret_cast<float *>(ob + SM::O);       // [KN + 4]
     float2 *ex_s = reinterpret_cast<float2 *>(c_s + KN + 4);  // [4][128]
     float2 *ss_s = ex_s + 4 * kQRows;                         // [4][128]
     float2 *xs_s = ss_s + 4 * kQRows;                         // [2][128], by tile parity
     uint64_t *bar = reinterpret_cast<uint64_t *>(xs_s + 2 * kQRows);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
-    // the head's planes 1, 2 and constants landed; plane 0 landed; products done
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    // the head's plane 1 (and plane 2 with one output half) and constants landed; the tile's
+    // plane 0 landed; its plane 2 landed (two halves); products done
     const uint32_t BAR_W = smem_addr(bar), BAR_O = smem_addr(bar + 1), BAR_D = smem_addr(bar + 2);
+    const uint32_t BAR_Q = smem_addr(bar + 3);
     const bool g_f32 = layout == GL_F32, g_split = layout == GL_SPLIT;
     const int ge = g_f32 ? 4 : 2;
     constexpr uint32_t LO = kQRows * 128 * 2;   // split: the lo plane's half tile follows the hi plane's
@@ -686,7 +692,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(smem_addr(bar + b), 1);
+        for (int b = 0; b < 4; ++b) mbar_init(smem_addr(bar + b), 1);
         mbar_init_fence();
     }
     fence_before_sync();
@@ -748,9 +754,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
     uint32_t nw = 0;                       // head loads so far
     const unsigned char *src = img;        // the head's image
     bool ok = true;
-    // (thread 0) copies or products whose wait has not completed, and their phases
-    bool w_pend = false, o_pend = false, d_pend = false;
-    uint32_t w_par = 0, o_par = 0, d_par = 0;
+    // (thread 0) copies or products whose wait has not completed, and their phases; (thread 32,
+    // which moves the output tiles and the per-tile planes) whether and with which phase it
+    // last requested plane 0 and plane 2
+    bool w_pend = false, d_pend = false;
+    uint32_t w_par = 0, d_par = 0;
+    bool o_req = false, q_req = false;
+    uint32_t o_rpar = 0, q_rpar = 0;
     for (int j = 0; j < cnt; ++j) {
         const long long it = it0 + j;
         const int bh = (int)(it / tps), t = (int)(it % tps), h = bh % H;
@@ -767,9 +777,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
             src = img + ((long long)h * NH + rank) * IM::pitch;
             if (tid == 0 && ok) {
                 fence_proxy_async();
-                mbar_expect_tx(BAR_W, 2 * SM::WB + SM::C);
+                mbar_expect_tx(BAR_W, (QOUT ? 1 : 2) * SM::WB + SM::C);
                 bulk_g2s(smem_addr(wp), src + IM::off(0, 0, 1), SM::WB, BAR_W);
-                bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_W);
+                if (!QOUT) bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_W);
                 bulk_g2s(smem_addr(c_s), src + IM::W, SM::C, BAR_W);
                 w_pend = true;
                 w_par = nw & 1;
@@ -777,6 +787,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
             if (ok) ok = mbar_wait(BAR_W, nw & 1);
             if (tid == 0 && ok) w_pend = false;
             ++nw;
+        }
+        if (tid == 32 && ok) {   // the previous tile's output halves have left O (and Q): the
+                                 // tile's plane 0 (and plane 2) come in
+            if constexpr (QOUT)
+                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // the first half's group
+            else
+                bulk_wait_read();
+            mbar_expect_tx(BAR_O, SM::WB);
+            bulk_g2s(smem_addr(ob), src + IM::off(0, 0, 0), SM::WB, BAR_O);
+            o_req = true;
+            o_rpar = j & 1;
+            if constexpr (QOUT) {
+                bulk_wait_read();
+                mbar_expect_tx(BAR_Q, SM::WB);
+                bulk_g2s(smem_addr(wq), src + IM::off(0, 0, 2), SM::WB, BAR_Q);
+                q_req = true;
+                q_rpar = j & 1;
+            }
         }
         {   // the rows' squares and values into the three planes of A, and their sums for S_i
             uint32_t pw[3][16];
@@ -797,23 +825,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
         fence_before_sync();
         ok = __syncthreads_and(ok) != 0;   // the planes are in TMEM, the accumulator was read
         fence_after_sync();
-        if (tid == 0 && ok) {   // the products: planes 1 and 2 are resident, plane 0 comes into O
+        if (tid == 0 && ok) {   // the products in the order the planes are at hand: plane 1 is
+                                // resident, plane 0 lands in O, plane 2 in Q (or is resident)
             first = true;
             d_pend = true;
             d_par = j & 1;
             prods(1, wp);                          // (1,1)
-            prods(0, wq);                          // (0,2)
             prods(0, wp);                          // (0,1)
-            bulk_wait_read();                      // the previous output tile has left O
-            mbar_expect_tx(BAR_O, SM::WB);
-            bulk_g2s(smem_addr(ob), src + IM::off(0, 0, 0), SM::WB, BAR_O);
-            o_par = j & 1;
-            if (mbar_wait(BAR_O, o_par)) {
+            if (mbar_wait(BAR_O, (uint32_t)(j & 1))) {
                 if (!x_bf16) prods(2, ob);         // (2,0); zero for bf16 rows
                 prods(1, ob);                      // (1,0)
-                prods(0, ob);                      // (0,0)
+                if (!QOUT || mbar_wait(BAR_Q, (uint32_t)(j & 1))) {
+                    prods(0, wq);                  // (0,2)
+                    prods(0, ob);                  // (0,0), the largest last
+                } else {
+                    ok = false;
+                }
             } else {
-                o_pend = true;
                 ok = false;
             }
             mma_commit(BAR_D);                     // also after a failed wait: the products issued
@@ -896,20 +924,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
             for (int p = 0; p < QC / 2; ++p) acc[p] = __fmul2_rn(acc[p], sc2);
         }
-        // the posteriors in halves of 128 components through O (free: the products are done):
-        // quarters QPH hf .. QPH hf + QPH - 1 write half hf once the previous half has left O
-#pragma unroll 1
-        for (int hf = 0; hf < HALVES; ++hf) {
-            if (hf > 0) {
-                if (tid == 0) bulk_wait_read();
-                __syncthreads();
-            }
-            if (cq / QPH == hf && ok) {
+        // the posteriors in halves of 128 components, quarters QPH hf .. QPH hf + QPH - 1 writing
+        // half hf: the first into O, the second into Q (both free: the products are done); thread
+        // 32 stores them as two groups, which drain while the next tile is split and multiplied
+        {
+            const int hf = cq / QPH;
+            unsigned char *hb = hf == 0 ? ob : wq;
+            if (ok) {
                 const int c0 = QC * (cq % QPH);   // this thread's columns in the half tile
                 if (g_f32) {
 #pragma unroll
                     for (int g = 0; g < QC / 4; ++g)
-                        *reinterpret_cast<float4 *>(ob + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
+                        *reinterpret_cast<float4 *>(hb + sw128_offset(i, c0 + 4 * g, kQRows, 4)) =
                             make_float4(acc[2 * g].x, acc[2 * g].y, acc[2 * g + 1].x, acc[2 * g + 1].y);
                 } else {
                     const float2 m1 = make_float2(-1.f, -1.f);
@@ -927,35 +953,42 @@ __global__ void __launch_bounds__(kQThreads, 1)
                             lw[u] = *reinterpret_cast<const uint32_t *>(&b);
                         }
                         const uint32_t off = sw128_offset(i, c0 + 8 * g, kQRows, 2);
-                        *reinterpret_cast<uint4 *>(ob + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        if (g_split) *reinterpret_cast<uint4 *>(ob + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        *reinterpret_cast<uint4 *>(hb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        if (g_split) *reinterpret_cast<uint4 *>(hb + LO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
                 fence_proxy_async();   // the half tile, written by threads, is read by the TMA store
             }
-            fence_before_sync();
-            __syncthreads();
-            if (tid == 0 && ok) {
-                const int pb = 128 / ge;   // columns of one 128-byte box
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 32 && ok) {
+            const int pb = 128 / ge;   // columns of one 128-byte box
+            for (int hf = 0; hf < HALVES; ++hf) {
+                const unsigned char *hb = hf == 0 ? ob : wq;
                 for (int a = 0; a < 128 / pb; ++a) {
                     const int x0 = kbase + 128 * hf + a * pb;
                     if (x0 >= ow) break;
-                    tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(ob + a * (kQRows * 128)));
-                    if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(ob + LO + a * (kQRows * 128)));
+                    tma_store_3d(&gmap, x0, t * kQRows, bh, smem_addr(hb + a * (kQRows * 128)));
+                    if (g_split) tma_store_3d(&gmap_lo, x0, t * kQRows, bh, smem_addr(hb + LO + a * (kQRows * 128)));
                 }
-                bulk_commit();
+                bulk_commit();   // one group per half
             }
         }
     }
-    if (tid == 0) {
+    if (tid == 0 && !ok) {
+        // after a failed wait a copy or products may still be in flight: let them end (bounded;
+        // a wait on a phase that has completed returns at once)
+        if (w_pend) mbar_wait(BAR_W, w_par);
+        if (d_pend) mbar_wait(BAR_D, d_par);
+        report_timeout(timeout);
+    }
+    if (tid == 32) {
         if (!ok) {
-            // after a failed wait a copy or products may still be in flight: let them end (bounded)
-            if (w_pend) mbar_wait(BAR_W, w_par);
-            if (o_pend) mbar_wait(BAR_O, o_par);
-            if (d_pend) mbar_wait(BAR_D, d_par);
-            report_timeout(timeout);
+            if (o_req) mbar_wait(BAR_O, o_rpar);
+            if (q_req) mbar_wait(BAR_Q, q_rpar);
         }
-        bulk_wait_read();   // the output tile has left shared memory
+        bulk_wait_read();   // the output tiles have left shared memory
     }
     fence_before_sync();
     __syncthreads();

@@ -9,8 +9,8 @@ round-to-nearest of what the previous ones leave) and the six plane products
 A2 W0, A1 W1, A1 W0, A0 W2, A0 W1, A0 W0 accumulated in fp32 in that order, one
 16-wide K step at a time (the tensor core's accumulation), each product's values'
 (odd) K steps before its squares' (even) ones as the kernels issue them; the
-routing of 65 <= K <= 512 takes the products in the order its planes of W arrive,
-A1 W1, A0 W2, A0 W1, A2 W0, A1 W0, A0 W0.  A tile whose rows
+routing of 65 <= K <= 512 takes the products in the order its planes of W are at
+hand, A1 W1, A0 W1, A2 W0, A1 W0, A0 W2, and A0 W0 last.  A tile whose rows
 include one with S = A/2 sum x^2 + M sum |x| above 4096 (A = max a, M = max |a mu|
 over the head) is evaluated exactly instead.  This checks that on the rows the
 pass keeps the posteriors match the oracle's far inside the 1e-4 tolerance and
@@ -27,7 +27,7 @@ from gaussian_mixture_sequence_gb300 import workloads
 
 S_MAX = 4096.0
 ALL_PASSES = [(2, 0), (1, 1), (1, 0), (0, 2), (0, 1), (0, 0)]
-WIDE_PASSES = [(1, 1), (0, 2), (0, 1), (2, 0), (1, 0), (0, 0)]   # 65 <= K <= 512
+WIDE_PASSES = [(1, 1), (0, 1), (2, 0), (1, 0), (0, 2), (0, 0)]   # 65 <= K <= 512
 KERNEL_KSTEPS = [1, 3, 5, 7, 0, 2, 4, 6]                          # the values' steps first
 
 
